@@ -1,0 +1,214 @@
+"""CPU oracle for q4mv / rmsq / swq / gsum -- TEST INFRASTRUCTURE ONLY.
+
+This package is the plain, slow definition the CUDA library is checked
+against.  Only the test suite, ``__graft_entry__.smoke()`` and the CPU-baseline
+leg of ``bench.py`` may import it; the library never does, and the two share
+no code.  The arithmetic lives in ``oracle.c`` (one IEEE binary32 operation per
+C operation, built without contraction); this module only marshals numpy
+arrays into it and composes the calls into a decode token.
+
+Sources are the three Bend pull-request pages on the 4-bit product:
+#1435 "Array.q4mv on Metal: one kernel thread per row ...", #1437
+"Array.q4go/Array.q4wait queue Metal Q4 products ...", and #1440 "Metal:
+queued rmsq, swq, gdn and atq kernels and a 4-row q4mv ...".
+
+parity unpinned: ``hash32`` against the pages' printed hash (their generator
+and hash function are not published).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+CFLAGS = ["-O2", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared", "-std=c11"]
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into liboracle.so with gcc (no contraction, no fast math)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.run(["gcc", *CFLAGS, "-o", tmp, _SRC, "-lm"], check=True)
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            f32p = ctypes.POINTER(ctypes.c_float)
+            u32p = ctypes.POINTER(ctypes.c_uint32)
+            f64p = ctypes.POINTER(ctypes.c_double)
+            i64 = ctypes.c_int64
+            lib.or_tree.argtypes = [f32p, i64]
+            lib.or_tree.restype = ctypes.c_float
+            lib.or_gsum.argtypes = [f32p, f32p, i64]
+            lib.or_q4mv.argtypes = [u32p, f32p, f32p, f32p, f32p, f32p, i64, i64, i64, i64]
+            lib.or_q4mv_absmag.argtypes = [u32p, f32p, f32p, f32p, f32p, f64p, i64, i64, i64, i64]
+            lib.or_rmsq.argtypes = [f32p, f32p, ctypes.c_float, f32p, f32p, i64]
+            lib.or_exp.argtypes = [ctypes.c_float]
+            lib.or_exp.restype = ctypes.c_float
+            lib.or_exp_array.argtypes = [f32p, f32p, i64]
+            lib.or_swq.argtypes = [f32p, f32p, f32p, i64]
+            lib.or_fnv1a.argtypes = [ctypes.c_char_p, i64]
+            lib.or_fnv1a.restype = ctypes.c_uint32
+            lib.or_hash32.argtypes = [f32p, i64]
+            lib.or_hash32.restype = ctypes.c_uint32
+            _lib = lib
+    return _lib
+
+
+def _f32(a):
+    a = np.ascontiguousarray(a, dtype=np.float32)
+    return a, a.ctypes.data_as(ctypes.POINTER(ctypes.c_float))
+
+
+def _u32(a):
+    a = np.ascontiguousarray(a, dtype=np.uint32)
+    return a, a.ctypes.data_as(ctypes.POINTER(ctypes.c_uint32))
+
+
+def _check_q4(w, scale, bias, x, xsum, rows, cols, row0, n):
+    if cols <= 0 or cols % 64:
+        raise ValueError("cols must be a positive multiple of 64")
+    if row0 < 0 or n < 0 or row0 + n > rows:
+        raise ValueError("row range out of bounds")
+    G, W = cols // 64, cols // 8
+    if w.size != rows * W or scale.size != rows * G or bias.size != rows * G:
+        raise ValueError("weight arrays do not match rows x cols")
+    if x.size != cols or xsum.size != G:
+        raise ValueError("x / xsum do not match cols")
+
+
+def tree(v) -> np.float32:
+    """TREE(v): balanced pairwise sum in index order, odd element carried."""
+    v, pv = _f32(v)
+    return np.float32(_load().or_tree(pv, v.size))
+
+
+def gsum(v) -> np.ndarray:
+    """s[g] = TREE(v[64g:64g+64])."""
+    v, pv = _f32(v)
+    if v.size % 64:
+        raise ValueError("length must be a multiple of 64")
+    s = np.empty(v.size // 64, np.float32)
+    _load().or_gsum(pv, _f32(s)[1], v.size)
+    return s
+
+
+def q4mv(w, scale, bias, x, xsum, cols, row0=0, n=None) -> np.ndarray:
+    """y[i] = row row0+i of the affine 4-bit product (tree order)."""
+    w, pw = _u32(w)
+    scale, ps = _f32(scale)
+    bias, pb = _f32(bias)
+    x, px = _f32(x)
+    xsum, pxs = _f32(xsum)
+    rows = w.size // (cols // 8)
+    n = rows - row0 if n is None else n
+    _check_q4(w, scale, bias, x, xsum, rows, cols, row0, n)
+    y = np.empty(n, np.float32)
+    _load().or_q4mv(pw, ps, pb, px, pxs, _f32(y)[1], rows, cols, row0, n)
+    return y
+
+
+def q4mv_absmag(w, scale, bias, x, xsum, cols, row0=0, n=None) -> np.ndarray:
+    """A_r = sum_g |scale*d| + |bias*xsum| in double (scales the fast-mode bound)."""
+    w, pw = _u32(w)
+    scale, ps = _f32(scale)
+    bias, pb = _f32(bias)
+    x, px = _f32(x)
+    xsum, pxs = _f32(xsum)
+    rows = w.size // (cols // 8)
+    n = rows - row0 if n is None else n
+    _check_q4(w, scale, bias, x, xsum, rows, cols, row0, n)
+    a = np.empty(n, np.float64)
+    _load().or_q4mv_absmag(pw, ps, pb, px, pxs, a.ctypes.data_as(ctypes.POINTER(ctypes.c_double)),
+                           rows, cols, row0, n)
+    return a
+
+
+def rmsq(x, wt, eps=1e-6):
+    """(xn, xsum): RMS norm with weights, plus the group sums of xn."""
+    x, px = _f32(x)
+    wt, pwt = _f32(wt)
+    if x.size % 64 or x.size == 0 or wt.size != x.size:
+        raise ValueError("n must be a positive multiple of 64 and match the weights")
+    xn = np.empty(x.size, np.float32)
+    xs = np.empty(x.size // 64, np.float32)
+    _load().or_rmsq(px, pwt, ctypes.c_float(np.float32(eps)), _f32(xn)[1], _f32(xs)[1], x.size)
+    return xn, xs
+
+
+def exp(v) -> np.ndarray:
+    """The specified binary32 exponential, elementwise."""
+    v, pv = _f32(v)
+    out = np.empty(v.shape, np.float32)
+    _load().or_exp_array(pv, _f32(out)[1], v.size)
+    return out
+
+
+def swq(a):
+    """(o, osum): o = silu(gate) * up for a = [gate | up], plus group sums."""
+    a, pa = _f32(a)
+    if a.size % 128 or a.size == 0:
+        raise ValueError("a must hold 2n values with n a positive multiple of 64")
+    n = a.size // 2
+    o = np.empty(n, np.float32)
+    os_ = np.empty(n // 64, np.float32)
+    _load().or_swq(pa, _f32(o)[1], _f32(os_)[1], n)
+    return o, os_
+
+
+def fnv1a(data: bytes) -> int:
+    """32-bit FNV-1a over a byte string."""
+    return int(_load().or_fnv1a(data, len(data)))
+
+
+def hash32(y) -> int:
+    """32-bit FNV-1a over y's little-endian binary32 bytes in index order."""
+    y, py = _f32(y)
+    return int(_load().or_hash32(py, y.size))
+
+
+def decode_token(model, hidden, eps=1e-6, keep=False):
+    """One synthetic decode token: the composition of the calls above.
+
+    ``model`` is a ``synth.DecodeModel``.  Per layer:
+    rmsq -> q, k, v products -> group sums of q -> o product (reads q) ->
+    rmsq -> gate, up products -> swq -> down product; then a final rmsq and
+    the output head.  Returns the head's output (and the per-layer values if
+    ``keep``).
+    """
+    h = np.asarray(hidden, np.float32)
+    trace = []
+    for L in model.layers:
+        xn, xs = rmsq(h, L.rms1, eps)
+        q = q4mv(*L.q.arrays(), xn, xs, L.q.cols)
+        k = q4mv(*L.k.arrays(), xn, xs, L.k.cols)
+        v = q4mv(*L.v.arrays(), xn, xs, L.v.cols)
+        qs = gsum(q)
+        o = q4mv(*L.o.arrays(), q, qs, L.o.cols)
+        xn2, xs2 = rmsq(o, L.rms2, eps)
+        gate = q4mv(*L.gate.arrays(), xn2, xs2, L.gate.cols)
+        up = q4mv(*L.up.arrays(), xn2, xs2, L.up.cols)
+        s, ss = swq(np.concatenate([gate, up]))
+        h = q4mv(*L.down.arrays(), s, ss, L.down.cols)
+        if keep:
+            trace.append(dict(xn=xn, xs=xs, q=q, k=k, v=v, qs=qs, o=o, xn2=xn2, xs2=xs2,
+                              gate=gate, up=up, s=s, ss=ss, h=h))
+    xf, xfs = rmsq(h, model.rms_final, eps)
+    logits = q4mv(*model.head.arrays(), xf, xfs, model.head.cols)
+    if keep:
+        return logits, trace, (xf, xfs)
+    return logits

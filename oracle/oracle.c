@@ -1,0 +1,296 @@
+/*
+ * Plain CPU oracle for the affine 4-bit group-quantized matrix-vector product
+ * (q4mv) and its two activation producers (rmsq, swq), plus the group sum
+ * (gsum) and the output hash used by the measurements.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the slow, obviously correct
+ * definition that the CUDA library is checked against.  Only the test suite,
+ * the smoke check and the benchmark's CPU-baseline leg may load it.  It shares
+ * no source, header, table or helper with the CUDA library.
+ *
+ * Build: gcc -O2 -ffp-contract=off -fno-fast-math -fPIC -shared.  Every float
+ * operation below is one IEEE binary32 operation rounded to nearest even; with
+ * contraction off no multiply is fused into an add, so each line is exactly
+ * the rounded operation it names.  (C's FLT_EVAL_METHOD is 0 on both x86-64
+ * and aarch64, so float expressions are evaluated in float.)
+ *
+ * Sources (Bend pull requests by the same author, all closed unmerged):
+ *   [q4mv-metal]  "Array.q4mv on Metal: one kernel thread per row for products
+ *                 of 4M weights or more, bit-identical" (bendlang/bend #1435)
+ *   [q4go]        "Array.q4go/Array.q4wait queue Metal Q4 products in one
+ *                 command buffer and wait once on a flag" (#1437)
+ *   [fused-token] "Metal: queued rmsq, swq, gdn and atq kernels and a 4-row
+ *                 q4mv, so a decode token is one command buffer with one wait"
+ *                 (#1440)
+ * The pages state the product (MLX-style 4-bit affine weights, groups of 64
+ * columns, a per-group activation sum for the bias term) and that the sum runs
+ * in a fixed tree order, but not the tree itself; the readings taken where the
+ * pages are silent are named at each function.
+ *
+ * parity unpinned: or_hash32 against the pages' printed hash (their input
+ * generator and hash function are not given).  Every other function is pinned
+ * by the CPU tests.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ------------------------------------------------------------------------ */
+/* TREE: the fixed summation order.                                          */
+/* [fused-token] Change, the bend_q4mv bullet, and the #1436 title it cites:  */
+/* sums run in a fixed tree order.  Reading: a balanced pairwise tree in      */
+/* index order.  At each level elements (2i, 2i+1) are added; an odd last    */
+/* element is carried to the next level unchanged (not added to a zero).      */
+/* For a power-of-two count this is recursive halving.                        */
+/* ------------------------------------------------------------------------ */
+float or_tree(const float *v, int64_t m)
+{
+    if (m <= 0) return -0.0f; /* never used by the method; -0 is the additive identity */
+    float local[128];
+    float *buf = m <= 128 ? local : (float *)malloc((size_t)m * sizeof(float));
+    memcpy(buf, v, (size_t)m * sizeof(float));
+    const int64_t m0 = m;
+    while (m > 1) {
+        const int64_t half = m / 2;
+        for (int64_t i = 0; i < half; ++i)
+            buf[i] = buf[2 * i] + buf[2 * i + 1];
+        if (m & 1) buf[half] = buf[m - 1];
+        m = half + (m & 1);
+    }
+    const float s = buf[0];
+    if (m0 > 128) free(buf);
+    return s;
+}
+
+/* ------------------------------------------------------------------------ */
+/* gsum: s[g] = TREE(v[64g .. 64g+63]).                                       */
+/* [fused-token] Change, Array.rmsq bullet: producers emit the 64-value      */
+/* group sums that Array.q4mv reads.                                          */
+/* ------------------------------------------------------------------------ */
+void or_gsum(const float *v, float *s, int64_t n)
+{
+    for (int64_t g = 0; g < n / 64; ++g)
+        s[g] = or_tree(v + 64 * g, 64);
+}
+
+/* ------------------------------------------------------------------------ */
+/* q4mv.  Weight format ([fused-token] Why; [q4go] Verification, whole       */
+/* model): MLX-style 4-bit affine weights w = scale*q + bias in groups of 64 */
+/* columns.  Packing: 8 nibbles per u32, column 8k+j is nibble j of word k,  */
+/* low nibble first; scale and bias are f32 [rows][cols/64].                 */
+/*                                                                          */
+/* For each row r and group g:                                              */
+/*   p_j = (float)q[r][64g+j] * x[64g+j]          (one rounding each)        */
+/*   d   = TREE(p_0 .. p_63)                                                 */
+/*   t_g = scale[r][g]*d + bias[r][g]*xsum[g]     (two products, one add)    */
+/* and y = TREE(t_0 .. t_{G-1}).  This is the dequantize-then-dot product     */
+/* with the bias folded into the activation's group sum:                     */
+/*   sum_j (s*q_j + b)*x_j = s*sum_j q_j*x_j + b*sum_j x_j.                  */
+/* Row range ([q4go] Change, Array.q4go(w, x, y, r, n, cols, rows)): rows    */
+/* row0 .. row0+n-1 of a rows x cols matrix; y[i] receives row row0+i.       */
+/* ------------------------------------------------------------------------ */
+void or_q4mv(const uint32_t *w, const float *scale, const float *bias,
+             const float *x, const float *xsum, float *y,
+             int64_t rows, int64_t cols, int64_t row0, int64_t n)
+{
+    (void)rows;
+    const int64_t W = cols / 8, G = cols / 64;
+    float *t = (float *)malloc((size_t)(G > 0 ? G : 1) * sizeof(float));
+    float p[64];
+    for (int64_t i = 0; i < n; ++i) {
+        const int64_t r = row0 + i;
+        for (int64_t g = 0; g < G; ++g) {
+            for (int j = 0; j < 64; ++j) {
+                const int64_t c = 64 * g + j;
+                const uint32_t word = w[r * W + c / 8];
+                const uint32_t q = (word >> (4 * (c % 8))) & 0xFu;
+                p[j] = (float)q * x[c];
+            }
+            const float d = or_tree(p, 64);
+            const float sd = scale[r * G + g] * d;
+            const float bx = bias[r * G + g] * xsum[g];
+            t[g] = sd + bx;
+        }
+        y[i] = or_tree(t, G);
+    }
+    free(t);
+}
+
+/* Magnitude of the terms of each output, in double: A_r = sum_g |scale*d| +
+ * |bias*xsum| with d = sum_j q*x in double.  Used only to scale the error
+ * allowed to the reordered (fast) mode, whose per-output error is bounded by
+ * a multiple of this sum, not of |y| (the bias term cancels most of y). */
+void or_q4mv_absmag(const uint32_t *w, const float *scale, const float *bias,
+                    const float *x, const float *xsum, double *a,
+                    int64_t rows, int64_t cols, int64_t row0, int64_t n)
+{
+    (void)rows;
+    const int64_t W = cols / 8, G = cols / 64;
+    for (int64_t i = 0; i < n; ++i) {
+        const int64_t r = row0 + i;
+        double acc = 0.0;
+        for (int64_t g = 0; g < G; ++g) {
+            double d = 0.0;
+            for (int j = 0; j < 64; ++j) {
+                const int64_t c = 64 * g + j;
+                const uint32_t q = (w[r * W + c / 8] >> (4 * (c % 8))) & 0xFu;
+                d += (double)q * (double)x[c];
+            }
+            acc += fabs((double)scale[r * G + g] * d) + fabs((double)bias[r * G + g] * (double)xsum[g]);
+        }
+        a[i] = acc;
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* rmsq: RMS norm with f32 weights plus the group sums of its output.        */
+/* [fused-token] Change, Array.rmsq bullet.  Readings: weights multiply the  */
+/* normalised value directly (not 1+w); the sum of squares uses the same     */
+/* two-level tree as every other sum (per 64-group, then across groups).     */
+/*   ss   = TREE_g( TREE_j( x_i*x_i ) )                                      */
+/*   mean = ss / n;  r = 1 / sqrt(mean + eps)                                */
+/*   xn_i = (x_i * r) * wt_i;  xsum[g] = TREE(xn in group g)                  */
+/* n must be a multiple of 64.                                               */
+/* ------------------------------------------------------------------------ */
+void or_rmsq(const float *x, const float *wt, float eps, float *xn, float *xsum, int64_t n)
+{
+    const int64_t G = n / 64;
+    float *gs = (float *)malloc((size_t)(G > 0 ? G : 1) * sizeof(float));
+    float sq[64];
+    for (int64_t g = 0; g < G; ++g) {
+        for (int j = 0; j < 64; ++j) {
+            const float v = x[64 * g + j];
+            sq[j] = v * v;
+        }
+        gs[g] = or_tree(sq, 64);
+    }
+    const float ss = or_tree(gs, G);
+    const float mean = ss / (float)n;
+    const float r = 1.0f / sqrtf(mean + eps);
+    for (int64_t i = 0; i < n; ++i) {
+        const float xr = x[i] * r;
+        xn[i] = xr * wt[i];
+    }
+    or_gsum(xn, xsum, n);
+    free(gs);
+}
+
+/* ------------------------------------------------------------------------ */
+/* EXP: an exponential both sides compute from this written definition, so  */
+/* that the SwiGLU product can be bit-exact ([fused-token] Change, last      */
+/* paragraph: a vendor exp moves the last bits).  Cody-Waite reduction with  */
+/* a two-part ln 2, degree-7 Taylor polynomial in Horner form, exact scaling */
+/* by 2^k.  Constants (IEEE binary32 bit patterns):                          */
+/*   L2E   = RN(log2 e)                         0x3FB8AA3B                   */
+/*   LN2HI = RN(ln 2) with its low 12 mantissa bits cleared  0x3F317000      */
+/*           (so k*LN2HI is exact for |k| < 2^12)                            */
+/*   LN2LO = RN(ln 2 - LN2HI)                   0x3805FDF4                   */
+/*   C_i   = RN(1/i!), i = 0..7                                              */
+/* Steps: NaN -> NaN; v > 89 -> +inf; v < -104 -> +0; otherwise              */
+/*   k  = round-half-even(v*L2E)                                             */
+/*   rr = (v + (-k)*LN2HI) + (-k)*LN2LO                                      */
+/*   p  = C_0 + rr*(C_1 + rr*(... + rr*C_7))   (Horner, mul then add)         */
+/*   result = p*2^k, applied as one multiply for -126 <= k <= 127, as        */
+/*   (p*2^(k+126))*2^-126 for k < -126 (first product exact) and as          */
+/*   (p*2^127)*2^(k-127) for k > 127, so the result is rounded once.         */
+/* ------------------------------------------------------------------------ */
+static float f32_from_bits(uint32_t b)
+{
+    float f;
+    memcpy(&f, &b, sizeof f);
+    return f;
+}
+
+static float pow2i(int e) /* 2^e for -126 <= e <= 127 */
+{
+    return f32_from_bits((uint32_t)(e + 127) << 23);
+}
+
+float or_exp(float v)
+{
+    if (v != v) return v;
+    if (v > 89.0f) return INFINITY;
+    if (v < -104.0f) return 0.0f;
+    const float L2E = f32_from_bits(0x3FB8AA3Bu);
+    const float LN2HI = f32_from_bits(0x3F317000u);
+    const float LN2LO = f32_from_bits(0x3805FDF4u);
+    const float C[8] = {
+        f32_from_bits(0x3F800000u), f32_from_bits(0x3F800000u), f32_from_bits(0x3F000000u),
+        f32_from_bits(0x3E2AAAABu), f32_from_bits(0x3D2AAAABu), f32_from_bits(0x3C088889u),
+        f32_from_bits(0x3AB60B61u), f32_from_bits(0x39500D01u),
+    };
+    const float kf = rintf(v * L2E); /* default rounding mode: nearest even */
+    const int k = (int)kf;
+    const float nk = -kf;
+    const float a = nk * LN2HI;
+    const float b = nk * LN2LO;
+    const float rr = (v + a) + b;
+    float p = C[7];
+    for (int i = 6; i >= 0; --i) {
+        const float pr = p * rr;
+        p = pr + C[i];
+    }
+    if (k > 127) {
+        const float t = p * pow2i(127);
+        return t * pow2i(k - 127);
+    }
+    if (k < -126) {
+        const float t = p * pow2i(k + 126);
+        return t * pow2i(-126);
+    }
+    return p * pow2i(k);
+}
+
+void or_exp_array(const float *v, float *out, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = or_exp(v[i]);
+}
+
+/* ------------------------------------------------------------------------ */
+/* swq: SwiGLU of a = [gate (n) | up (n)] plus the group sums of its output. */
+/* [fused-token] Change, Array.swq(a, o, n) bullet: o[i] is silu(a[i]) times */
+/* a[n+i], rounded (to binary32: every step here is an RN binary32 op).      */
+/* Reading: silu(g) = g / (1 + EXP(-g)).  n must be a multiple of 64.        */
+/* ------------------------------------------------------------------------ */
+void or_swq(const float *a, float *o, float *osum, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i) {
+        const float g = a[i];
+        const float e = or_exp(-g);
+        const float den = 1.0f + e;
+        const float silu = g / den;
+        o[i] = silu * a[n + i];
+    }
+    or_gsum(o, osum, n);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Hash of an output vector's bits ([q4mv-metal] Verification: the scratch   */
+/* program prints a hash of y's bits).  The pages do not name the function;  */
+/* reading: 32-bit FNV-1a over the little-endian bytes of y in index order.  */
+/* ------------------------------------------------------------------------ */
+uint32_t or_fnv1a(const uint8_t *bytes, int64_t nbytes)
+{
+    uint32_t h = 2166136261u;
+    for (int64_t i = 0; i < nbytes; ++i) {
+        h ^= bytes[i];
+        h *= 16777619u;
+    }
+    return h;
+}
+
+uint32_t or_hash32(const float *y, int64_t n)
+{
+    /* byte order fixed explicitly, so the hash does not depend on the host */
+    uint32_t h = 2166136261u;
+    for (int64_t i = 0; i < n; ++i) {
+        uint32_t b;
+        memcpy(&b, &y[i], sizeof b);
+        for (int s = 0; s < 32; s += 8) {
+            h ^= (b >> s) & 0xFFu;
+            h *= 16777619u;
+        }
+    }
+    return h;
+}
