@@ -1,0 +1,248 @@
+"""Python binding of libabg.so: the GB300 affine 4-bit group-quantized
+matrix-vector product (q4mv), its activation producers (rmsq, swq, gsum) and
+the decode-token stage graph.
+
+This module only marshals arguments: tensors become device pointers, the
+current torch stream becomes a cudaStream_t, and status codes become
+exceptions.  Every step of the computation runs in the library's CUDA kernels;
+there is no CPU path.  PyTorch supplies device memory and streams.
+
+The C declarations, with the meaning, layout, ownership and error behaviour
+of every argument, are in include/abg.h.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+__all__ = [
+    "TREE", "FAST", "AbgError", "library", "q4mv", "gsum", "rmsq", "swq", "StageGraph", "Node",
+    "device_status", "set_q4mv_tuning", "MAX_COLS",
+]
+
+TREE, FAST = 0, 1
+MAX_COLS = 16384
+NODE_Q4MV, NODE_RMSQ, NODE_SWQ, NODE_GSUM = 0, 1, 2, 3
+PRO_NONE, PRO_GSUM, PRO_RMSQ, PRO_SWQ = 0, 1, 2, 3
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "libabg.so")
+_lock = threading.Lock()
+_lib = None
+
+_STATUS = {0: "ok", 1: "invalid argument", 2: "misaligned pointer", 3: "bad shape", 4: "output overlaps an input",
+           5: "CUDA error", 6: "device wait timed out"}
+
+
+class AbgError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        msg = f"{what}: {_STATUS.get(status, 'unknown status')} ({status})"
+        if status == 5 and _lib is not None:
+            msg += ": " + _lib.abg_last_cuda_error().decode()
+        super().__init__(msg)
+
+
+class _Node(ctypes.Structure):
+    """Mirror of struct abg_node in include/abg.h."""
+    _fields_ = [
+        ("kind", ctypes.c_int32), ("stage", ctypes.c_int32),
+        ("w", ctypes.c_void_p), ("scale", ctypes.c_void_p), ("bias", ctypes.c_void_p),
+        ("rows", ctypes.c_int64), ("cols", ctypes.c_int64), ("row0", ctypes.c_int64), ("n", ctypes.c_int64),
+        ("y", ctypes.c_void_p),
+        ("prologue", ctypes.c_int32), ("eps", ctypes.c_float),
+        ("x", ctypes.c_void_p), ("xsum", ctypes.c_void_p), ("wt", ctypes.c_void_p),
+        ("out", ctypes.c_void_p), ("out_sum", ctypes.c_void_p),
+        ("len", ctypes.c_int64),
+    ]
+
+
+def library(build_if_missing: bool = True) -> ctypes.CDLL:
+    """Loads libabg.so (building it with nvcc first if it is missing or stale)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if build_if_missing:
+                from . import _build
+                if _build.stale():
+                    _build.build()
+            if not os.path.exists(_LIB_PATH):
+                raise RuntimeError(f"the CUDA library {_LIB_PATH} is not built")
+            lib = ctypes.CDLL(_LIB_PATH)
+            P, I64, I = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+            lib.abg_q4mv.argtypes = [P, P, P, P, P, P, I64, I64, I64, I64, I, I, P]
+            lib.abg_gsum.argtypes = [P, P, I64, I, P]
+            lib.abg_rmsq.argtypes = [P, P, ctypes.c_float, P, P, I64, I, P]
+            lib.abg_swq.argtypes = [P, P, P, I64, I, P]
+            lib.abg_stage_graph_create.argtypes = [ctypes.POINTER(_Node), I64, I, I, ctypes.POINTER(P)]
+            lib.abg_stage_graph_launch.argtypes = [P, P]
+            lib.abg_stage_graph_launches.argtypes = [P, ctypes.POINTER(I64)]
+            lib.abg_stage_graph_destroy.argtypes = [P]
+            lib.abg_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32), I]
+            lib.abg_set_q4mv_tuning.argtypes = [I, I, I]
+            lib.abg_status_str.argtypes = [I]
+            lib.abg_status_str.restype = ctypes.c_char_p
+            lib.abg_last_cuda_error.argtypes = []
+            lib.abg_last_cuda_error.restype = ctypes.c_char_p
+            for f in ("abg_q4mv", "abg_gsum", "abg_rmsq", "abg_swq", "abg_stage_graph_create",
+                      "abg_stage_graph_launch", "abg_stage_graph_launches", "abg_stage_graph_destroy",
+                      "abg_device_status", "abg_set_q4mv_tuning"):
+                getattr(lib, f).restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def _check(status: int, what: str):
+    if status != 0:
+        raise AbgError(status, what)
+
+
+def _ptr(t, dtype=None, numel=None, name="tensor"):
+    """Device pointer of a CUDA tensor (or an int address, passed through)."""
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype and not (dtype == "word" and t.element_size() == 4 and
+                                                         not t.is_floating_point()):
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if numel is not None and t.numel() < numel:
+        raise ValueError(f"{name} holds {t.numel()} elements, needs {numel}")
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _dtypes():
+    import torch
+    return torch.int32, torch.float32
+
+
+def q4mv(w, scale, bias, x, xsum, y, cols: int, row0: int = 0, n: int | None = None, mode: int = TREE,
+         rows_per_warp: int = 0, stream=None):
+    """y[i] = row row0+i of the packed (rows x cols) matrix times x (see abg_q4mv)."""
+    _, f32 = _dtypes()
+    rows = w.shape[0] if w.dim() == 2 else w.numel() // (cols // 8)
+    n = rows - row0 if n is None else n
+    G, W = cols // 64, cols // 8
+    st = library().abg_q4mv(
+        _ptr(w, "word", rows * W, "w"), _ptr(scale, f32, rows * G, "scale"), _ptr(bias, f32, rows * G, "bias"),
+        _ptr(x, f32, cols, "x"), _ptr(xsum, f32, G, "xsum"), _ptr(y, f32, n, "y"),
+        rows, cols, row0, n, mode, rows_per_warp, _stream(stream))
+    _check(st, "abg_q4mv")
+    return y
+
+
+def gsum(v, s, mode: int = TREE, stream=None):
+    """s[g] = tree sum of v[64g:64g+64]."""
+    _, f32 = _dtypes()
+    n = v.numel()
+    _check(library().abg_gsum(_ptr(v, f32, n, "v"), _ptr(s, f32, n // 64, "s"), n, mode, _stream(stream)), "abg_gsum")
+    return s
+
+
+def rmsq(x, wt, xn, xsum, eps: float = 1e-6, mode: int = TREE, stream=None):
+    """RMS norm with weights into xn, and the group sums of xn into xsum."""
+    _, f32 = _dtypes()
+    n = x.numel()
+    st = library().abg_rmsq(_ptr(x, f32, n, "x"), _ptr(wt, f32, n, "wt"), ctypes.c_float(eps), _ptr(xn, f32, n, "xn"),
+                            _ptr(xsum, f32, n // 64, "xsum"), n, mode, _stream(stream))
+    _check(st, "abg_rmsq")
+    return xn, xsum
+
+
+def swq(a, o, osum, mode: int = TREE, stream=None):
+    """o = silu(a[:n]) * a[n:], and the group sums of o into osum."""
+    _, f32 = _dtypes()
+    n = a.numel() // 2
+    st = library().abg_swq(_ptr(a, f32, 2 * n, "a"), _ptr(o, f32, n, "o"), _ptr(osum, f32, n // 64, "osum"), n, mode,
+                           _stream(stream))
+    _check(st, "abg_swq")
+    return o, osum
+
+
+class Node:
+    """Builders for the stage-graph node kinds (fields as in struct abg_node)."""
+
+    @staticmethod
+    def q4mv(stage, w, scale, bias, y, cols, x, xsum=None, prologue=PRO_NONE, wt=None, eps=1e-6, row0=0, n=None):
+        rows = w.shape[0] if w.dim() == 2 else w.numel() // (cols // 8)
+        n = rows - row0 if n is None else n
+        nd = _Node(kind=NODE_Q4MV, stage=stage, w=_ptr(w, name="w"), scale=_ptr(scale, name="scale"),
+                   bias=_ptr(bias, name="bias"), rows=rows, cols=cols, row0=row0, n=n, y=_ptr(y, name="y"),
+                   prologue=prologue, eps=eps, x=_ptr(x, name="x"), xsum=_ptr(xsum, name="xsum"),
+                   wt=_ptr(wt, name="wt"))
+        return nd
+
+    @staticmethod
+    def rmsq(stage, x, wt, out, out_sum, eps=1e-6):
+        return _Node(kind=NODE_RMSQ, stage=stage, x=_ptr(x, name="x"), wt=_ptr(wt, name="wt"), out=_ptr(out, name="out"),
+                     out_sum=_ptr(out_sum, name="out_sum"), eps=eps, len=x.numel())
+
+    @staticmethod
+    def swq(stage, a, out, out_sum):
+        return _Node(kind=NODE_SWQ, stage=stage, x=_ptr(a, name="a"), out=_ptr(out, name="out"),
+                     out_sum=_ptr(out_sum, name="out_sum"), len=a.numel() // 2)
+
+    @staticmethod
+    def gsum(stage, v, out_sum):
+        return _Node(kind=NODE_GSUM, stage=stage, x=_ptr(v, name="v"), out_sum=_ptr(out_sum, name="out_sum"),
+                     len=v.numel())
+
+
+class StageGraph:
+    """A decode token's stages recorded into one CUDA graph (abg_stage_graph_*).
+
+    ``keep`` holds references to the tensors the nodes point at, so they stay
+    allocated as long as the graph (the lifetime rule of abg.h).
+    """
+
+    def __init__(self, nodes, mode: int = TREE, rows_per_warp: int = 0, keep=()):
+        arr = (_Node * len(nodes))(*nodes)
+        h = ctypes.c_void_p()
+        _check(library().abg_stage_graph_create(arr, len(nodes), mode, rows_per_warp, ctypes.byref(h)),
+               "abg_stage_graph_create")
+        self._h = h
+        self._keep = list(keep)
+        n = ctypes.c_int64()
+        _check(library().abg_stage_graph_launches(self._h, ctypes.byref(n)), "abg_stage_graph_launches")
+        self.launches = n.value
+
+    def launch(self, stream=None):
+        _check(library().abg_stage_graph_launch(self._h, _stream(stream)), "abg_stage_graph_launch")
+
+    def close(self):
+        if getattr(self, "_h", None) is not None and self._h.value:
+            _check(library().abg_stage_graph_destroy(self._h), "abg_stage_graph_destroy")
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def device_status(clear: bool = True) -> int:
+    """The device status word's bits (bit 0: a bounded device wait timed out)."""
+    bits = ctypes.c_uint32()
+    st = library().abg_device_status(ctypes.byref(bits), 1 if clear else 0)
+    if st not in (0, 6):
+        _check(st, "abg_device_status")
+    return bits.value
+
+
+def set_q4mv_tuning(smem_kb: int = 0, consumer_warps: int = 0, blocks_per_sm: int = 0):
+    _check(library().abg_set_q4mv_tuning(smem_kb, consumer_warps, blocks_per_sm), "abg_set_q4mv_tuning")

@@ -1,0 +1,82 @@
+// Launch descriptors and host-side launchers of the library's kernels.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace abg {
+
+constexpr int kMaxProbs = 4;  // products that share one activation in a grouped launch
+
+enum Prologue { kProNone = 0, kProGsum = 1, kProRmsq = 2, kProSwq = 3 };
+
+// One matrix of a (grouped) product launch.  Pointers already point at row row0.
+struct Q4Prob {
+    const uint32_t *w;
+    const float *scale;
+    const float *bias;
+    float *y;
+    int64_t n;      // rows to compute
+    int64_t tiles;  // ceil(n / tile_rows)
+};
+
+// Everything the product kernel needs, passed by value (__grid_constant__).
+struct Q4Args {
+    Q4Prob prob[kMaxProbs];
+    int nprob;
+    int64_t total_tiles;
+    // activation: x/xsum for kProNone; producer inputs otherwise (see abg.h)
+    const float *x;
+    const float *xsum;
+    const float *wt;
+    float eps;
+    int prologue;
+    // shape
+    int cols, W, G, nch;
+    // tiling
+    int tile_rows, stages, nw;
+    // shared-memory layout (byte offsets)
+    uint32_t off_xs, off_red, off_stage, stage_w_bytes, stage_sb_bytes, stage_bytes, off_part, off_bar;
+    uint32_t smem_bytes;
+};
+
+struct Q4Tuning {
+    int smem_kb = 0;
+    int consumer_warps = 0;
+    int blocks_per_sm = 0;
+};
+
+struct Q4Plan {
+    Q4Args args;
+    dim3 grid, block;
+    int rows_per_warp;
+    bool tree;
+    bool sb_smem;
+};
+
+// Fills plan->args layout, grid and block for products sharing one activation.
+// Returns false if the shape cannot be planned (cols too large for shared memory).
+bool plan_q4mv(Q4Plan *plan, const Q4Prob *probs, int nprob, int cols, int prologue, const float *x,
+               const float *xsum, const float *wt, float eps, bool tree, int rows_per_warp, bool sb_smem,
+               const Q4Tuning &tune);
+
+// Sets the kernel's shared-memory limit for a plan (not a stream operation;
+// call it before stream capture).
+cudaError_t prepare_q4mv(const Q4Plan &plan);
+
+// Launches a planned product on `stream`; `pdl` marks it as a programmatic
+// dependent of the previous launch on the stream.
+cudaError_t launch_q4mv(const Q4Plan &plan, cudaStream_t stream, bool pdl);
+
+cudaError_t launch_gsum(const float *v, float *s, int64_t n, bool tree, cudaStream_t stream, bool pdl);
+cudaError_t launch_rmsq(const float *x, const float *wt, float eps, float *xn, float *xsum, int64_t n, bool tree,
+                        cudaStream_t stream, bool pdl);
+cudaError_t launch_swq(const float *a, float *o, float *osum, int64_t n, bool tree, cudaStream_t stream, bool pdl);
+
+int sm_count();
+
+// Each translation unit's device status word (OR-ed into *bits).
+cudaError_t q4mv_status(unsigned *bits, bool clear);
+cudaError_t vec_status(unsigned *bits, bool clear);
+
+}  // namespace abg

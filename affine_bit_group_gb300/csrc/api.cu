@@ -1,0 +1,459 @@
+// The library's C ABI (include/abg.h): argument validation, the single calls,
+// and the stage graph that records a decode token's dependent stages into one
+// CUDA graph.
+//
+// Stage semantics follow "Array.q4go/Array.q4wait queue Metal Q4 products in
+// one command buffer and wait once on a flag" (bendlang/bend #1437, Change:
+// queued products run concurrently, none may read another's y, dependent
+// stages need a wait) and "Metal: queued rmsq, swq, gdn and atq kernels ..."
+// (#1440, Why: a decode token as one command buffer with one wait).  Here a
+// token is one graph launch; the caller's single stream synchronization is
+// the one wait.
+#include "../../include/abg.h"
+#include "abg_kernels.cuh"
+
+#include <chrono>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <map>
+#include <string>
+#include <vector>
+
+using namespace abg;
+
+namespace {
+
+thread_local std::string g_cuda_error;
+Q4Tuning g_tuning;
+
+abg_status cuda_fail(cudaError_t e) {
+    if (e == cudaSuccess) return ABG_OK;
+    g_cuda_error = cudaGetErrorString(e);
+    return ABG_ECUDA;
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+struct Range {
+    uintptr_t lo = 0, hi = 0;  // [lo, hi) in bytes; empty when lo == hi
+};
+Range rng(const void *p, int64_t count, size_t elem) {
+    Range r;
+    r.lo = reinterpret_cast<uintptr_t>(p);
+    r.hi = r.lo + static_cast<uintptr_t>(count) * elem;
+    return r;
+}
+bool overlap(Range a, Range b) { return a.lo < a.hi && b.lo < b.hi && a.lo < b.hi && b.lo < a.hi; }
+
+bool valid_len(int64_t n) { return n > 0 && n % 64 == 0; }
+
+// ------------------------------------------------------------ products ----
+struct Q4Call {
+    const uint32_t *w;
+    const float *scale, *bias;
+    int64_t rows, cols, row0, n;
+    float *y;
+    int prologue;
+    const float *x, *xsum, *wt;
+    float eps;
+};
+
+int64_t act_len(const Q4Call &c) { return c.prologue == kProSwq ? 2 * c.cols : c.cols; }
+
+std::vector<Range> q4_inputs(const Q4Call &c) {
+    const int64_t W = c.cols / 8, G = c.cols / 64;
+    std::vector<Range> in = {rng(c.w, c.rows * W, 4), rng(c.scale, c.rows * G, 4), rng(c.bias, c.rows * G, 4),
+                             rng(c.x, act_len(c), 4)};
+    if (c.prologue == kProNone) in.push_back(rng(c.xsum, G, 4));
+    if (c.prologue == kProRmsq) in.push_back(rng(c.wt, c.cols, 4));
+    return in;
+}
+
+abg_status check_q4(const Q4Call &c, int mode, int rpw) {
+    if (mode != ABG_TREE && mode != ABG_FAST) return ABG_EINVAL;
+    if (rpw != 0 && rpw != 1 && rpw != 2 && rpw != 4 && rpw != 8) return ABG_EINVAL;
+    if (c.prologue < kProNone || c.prologue > kProSwq) return ABG_EINVAL;
+    if (c.cols <= 0 || c.cols % 64 != 0 || c.cols > ABG_MAX_COLS) return ABG_ESHAPE;
+    if (c.rows < 0 || c.row0 < 0 || c.n < 0 || c.row0 > c.rows || c.n > c.rows - c.row0) return ABG_ESHAPE;
+    if (c.n == 0) return ABG_OK;
+    if (!c.w || !c.scale || !c.bias || !c.x || !c.y) return ABG_EINVAL;
+    if (c.prologue == kProNone && !c.xsum) return ABG_EINVAL;
+    if (c.prologue == kProRmsq && !c.wt) return ABG_EINVAL;
+    if (!aligned(c.w, 16) || !aligned(c.x, 16) || !aligned(c.scale, 4) || !aligned(c.bias, 4) || !aligned(c.y, 4))
+        return ABG_EALIGN;
+    if (c.prologue == kProNone && !aligned(c.xsum, 4)) return ABG_EALIGN;
+    if (c.prologue == kProRmsq && !aligned(c.wt, 16)) return ABG_EALIGN;
+    const Range out = rng(c.y, c.n, 4);
+    for (const Range &r : q4_inputs(c))
+        if (overlap(out, r)) return ABG_EALIAS;
+    return ABG_OK;
+}
+
+// Scale and bias rows are bulk-copied when every row starts on 16 bytes.
+bool sb_bulk(const Q4Call &c) {
+    return (c.cols / 64) % 4 == 0 && aligned(c.scale, 16) && aligned(c.bias, 16);
+}
+
+Q4Prob make_prob(const Q4Call &c) {
+    Q4Prob p = {};
+    p.w = c.w + c.row0 * (c.cols / 8);
+    p.scale = c.scale + c.row0 * (c.cols / 64);
+    p.bias = c.bias + c.row0 * (c.cols / 64);
+    p.y = c.y;
+    p.n = c.n;
+    return p;
+}
+
+abg_status plan_calls(Q4Plan *plan, const std::vector<Q4Call> &calls, int mode, int rpw) {
+    Q4Prob probs[kMaxProbs];
+    for (size_t i = 0; i < calls.size(); ++i) probs[i] = make_prob(calls[i]);
+    const Q4Call &c0 = calls[0];
+    if (!plan_q4mv(plan, probs, static_cast<int>(calls.size()), static_cast<int>(c0.cols), c0.prologue, c0.x,
+                   c0.xsum, c0.wt, c0.eps, mode == ABG_TREE, rpw == 0 ? 4 : rpw, sb_bulk(c0), g_tuning))
+        return ABG_ESHAPE;
+    return ABG_OK;
+}
+
+// -------------------------------------------------------------- vectors ----
+abg_status check_gsum(const float *v, const float *s, int64_t n, int mode) {
+    if (mode != ABG_TREE && mode != ABG_FAST) return ABG_EINVAL;
+    if (!v || !s) return ABG_EINVAL;
+    if (!valid_len(n)) return ABG_ESHAPE;
+    if (!aligned(v, 16) || !aligned(s, 4)) return ABG_EALIGN;
+    if (overlap(rng(s, n / 64, 4), rng(v, n, 4))) return ABG_EALIAS;
+    return ABG_OK;
+}
+
+abg_status check_rmsq(const float *x, const float *wt, const float *xn, const float *xsum, int64_t n, int mode) {
+    if (mode != ABG_TREE && mode != ABG_FAST) return ABG_EINVAL;
+    if (!x || !wt || !xn || !xsum) return ABG_EINVAL;
+    if (!valid_len(n) || n > (int64_t(1) << 20)) return ABG_ESHAPE;
+    if (!aligned(x, 16) || !aligned(wt, 16) || !aligned(xn, 16) || !aligned(xsum, 4)) return ABG_EALIGN;
+    const Range rx = rng(x, n, 4), rw = rng(wt, n, 4), rn = rng(xn, n, 4), rs = rng(xsum, n / 64, 4);
+    if (overlap(rn, rx) || overlap(rn, rw) || overlap(rs, rx) || overlap(rs, rw) || overlap(rs, rn)) return ABG_EALIAS;
+    return ABG_OK;
+}
+
+abg_status check_swq(const float *a, const float *o, const float *osum, int64_t n, int mode) {
+    if (mode != ABG_TREE && mode != ABG_FAST) return ABG_EINVAL;
+    if (!a || !o || !osum) return ABG_EINVAL;
+    if (!valid_len(n)) return ABG_ESHAPE;
+    if (!aligned(a, 16) || !aligned(o, 16) || !aligned(osum, 4)) return ABG_EALIGN;
+    const Range ra = rng(a, 2 * n, 4), ro = rng(o, n, 4), rs = rng(osum, n / 64, 4);
+    if (overlap(ro, ra) || overlap(rs, ra) || overlap(rs, ro)) return ABG_EALIAS;
+    return ABG_OK;
+}
+
+// --------------------------------------------------------------- graphs ----
+struct Launch {
+    int kind;  // abg_node_kind
+    Q4Plan plan;
+    const float *a = nullptr, *b = nullptr;
+    float *o = nullptr, *os = nullptr;
+    float eps = 0.f;
+    int64_t len = 0;
+};
+
+struct StageGraph {
+    cudaGraph_t graph = nullptr;
+    cudaGraphExec_t exec = nullptr;
+    int64_t launches = 0;
+};
+
+cudaError_t prepare(const Launch &L) {
+    if (L.kind != ABG_NODE_Q4MV) return cudaSuccess;
+    return prepare_q4mv(L.plan);
+}
+
+cudaError_t run(const Launch &L, cudaStream_t s, bool pdl, bool tree) {
+    switch (L.kind) {
+    case ABG_NODE_Q4MV: return launch_q4mv(L.plan, s, pdl);
+    case ABG_NODE_RMSQ: return launch_rmsq(L.a, L.b, L.eps, L.o, L.os, L.len, tree, s, pdl);
+    case ABG_NODE_SWQ: return launch_swq(L.a, L.o, L.os, L.len, tree, s, pdl);
+    default: return launch_gsum(L.a, L.os, L.len, tree, s, pdl);
+    }
+}
+
+Q4Call call_of(const abg_node &nd) {
+    Q4Call c;
+    c.w = nd.w;
+    c.scale = nd.scale;
+    c.bias = nd.bias;
+    c.rows = nd.rows;
+    c.cols = nd.cols;
+    c.row0 = nd.row0;
+    c.n = nd.n;
+    c.y = nd.y;
+    c.prologue = nd.prologue;
+    c.x = nd.x;
+    c.xsum = nd.xsum;
+    c.wt = nd.wt;
+    c.eps = nd.eps;
+    return c;
+}
+
+void node_io(const abg_node &nd, std::vector<Range> &in, std::vector<Range> &out) {
+    switch (nd.kind) {
+    case ABG_NODE_Q4MV: {
+        const Q4Call c = call_of(nd);
+        in = q4_inputs(c);
+        out = {rng(c.y, c.n, 4)};
+        break;
+    }
+    case ABG_NODE_RMSQ:
+        in = {rng(nd.x, nd.len, 4), rng(nd.wt, nd.len, 4)};
+        out = {rng(nd.out, nd.len, 4), rng(nd.out_sum, nd.len / 64, 4)};
+        break;
+    case ABG_NODE_SWQ:
+        in = {rng(nd.x, 2 * nd.len, 4)};
+        out = {rng(nd.out, nd.len, 4), rng(nd.out_sum, nd.len / 64, 4)};
+        break;
+    default:
+        in = {rng(nd.x, nd.len, 4)};
+        out = {rng(nd.out_sum, nd.len / 64, 4)};
+        break;
+    }
+}
+
+bool same_activation(const Q4Call &a, const Q4Call &b) {
+    return a.prologue == b.prologue && a.cols == b.cols && a.x == b.x &&
+           (a.prologue != kProNone || a.xsum == b.xsum) && (a.prologue != kProRmsq || (a.wt == b.wt && a.eps == b.eps)) &&
+           sb_bulk(a) == sb_bulk(b);
+}
+
+}  // namespace
+
+extern "C" {
+
+abg_status abg_q4mv(const uint32_t *w, const float *scale, const float *bias, const float *x, const float *xsum,
+                    float *y, int64_t rows, int64_t cols, int64_t row0, int64_t n, int mode, int rows_per_warp,
+                    void *stream) {
+    Q4Call c{w, scale, bias, rows, cols, row0, n, y, kProNone, x, xsum, nullptr, 0.f};
+    abg_status st = check_q4(c, mode, rows_per_warp);
+    if (st != ABG_OK || n == 0) return st;
+    Q4Plan plan;
+    st = plan_calls(&plan, {c}, mode, rows_per_warp);
+    if (st != ABG_OK) return st;
+    cudaError_t e = prepare_q4mv(plan);
+    if (e == cudaSuccess) e = launch_q4mv(plan, static_cast<cudaStream_t>(stream), false);
+    return cuda_fail(e);
+}
+
+abg_status abg_gsum(const float *v, float *s, int64_t n, int mode, void *stream) {
+    abg_status st = check_gsum(v, s, n, mode);
+    if (st != ABG_OK) return st;
+    return cuda_fail(launch_gsum(v, s, n, mode == ABG_TREE, static_cast<cudaStream_t>(stream), false));
+}
+
+abg_status abg_rmsq(const float *x, const float *wt, float eps, float *xn, float *xsum, int64_t n, int mode,
+                    void *stream) {
+    abg_status st = check_rmsq(x, wt, xn, xsum, n, mode);
+    if (st != ABG_OK) return st;
+    return cuda_fail(launch_rmsq(x, wt, eps, xn, xsum, n, mode == ABG_TREE, static_cast<cudaStream_t>(stream), false));
+}
+
+abg_status abg_swq(const float *a, float *o, float *osum, int64_t n, int mode, void *stream) {
+    abg_status st = check_swq(a, o, osum, n, mode);
+    if (st != ABG_OK) return st;
+    return cuda_fail(launch_swq(a, o, osum, n, mode == ABG_TREE, static_cast<cudaStream_t>(stream), false));
+}
+
+abg_status abg_stage_graph_create(const abg_node *nodes, int64_t count, int mode, int rows_per_warp,
+                                  void **graph_out) {
+    if (!graph_out) return ABG_EINVAL;
+    *graph_out = nullptr;
+    if (!nodes || count <= 0) return ABG_EINVAL;
+    if (mode != ABG_TREE && mode != ABG_FAST) return ABG_EINVAL;
+    if (rows_per_warp != 0 && rows_per_warp != 1 && rows_per_warp != 2 && rows_per_warp != 4 && rows_per_warp != 8)
+        return ABG_EINVAL;
+    // 1. every node on its own
+    for (int64_t i = 0; i < count; ++i) {
+        const abg_node &nd = nodes[i];
+        abg_status st;
+        switch (nd.kind) {
+        case ABG_NODE_Q4MV: st = check_q4(call_of(nd), mode, rows_per_warp); break;
+        case ABG_NODE_RMSQ: st = check_rmsq(nd.x, nd.wt, nd.out, nd.out_sum, nd.len, mode); break;
+        case ABG_NODE_SWQ: st = check_swq(nd.x, nd.out, nd.out_sum, nd.len, mode); break;
+        case ABG_NODE_GSUM: st = check_gsum(nd.x, nd.out_sum, nd.len, mode); break;
+        default: st = ABG_EINVAL;
+        }
+        if (st != ABG_OK) return st;
+    }
+    // 2. stages: no node reads or writes what another node of its stage writes,
+    //    and no node writes any product's weights (they are fetched early)
+    std::map<int, std::vector<int64_t>> stages;
+    for (int64_t i = 0; i < count; ++i) stages[nodes[i].stage].push_back(i);
+    std::vector<std::vector<Range>> ins(count), outs(count);
+    for (int64_t i = 0; i < count; ++i) node_io(nodes[i], ins[i], outs[i]);
+    for (auto &kv : stages) {
+        const auto &idx = kv.second;
+        for (int64_t i : idx)
+            for (int64_t j : idx) {
+                if (i == j) continue;
+                for (const Range &o : outs[i]) {
+                    for (const Range &r : ins[j])
+                        if (overlap(o, r)) return ABG_EALIAS;
+                    for (const Range &r : outs[j])
+                        if (overlap(o, r)) return ABG_EALIAS;
+                }
+            }
+    }
+    for (int64_t i = 0; i < count; ++i) {
+        if (nodes[i].kind != ABG_NODE_Q4MV || nodes[i].n == 0) continue;
+        const Q4Call c = call_of(nodes[i]);
+        const Range wr[3] = {rng(c.w, c.rows * (c.cols / 8), 4), rng(c.scale, c.rows * (c.cols / 64), 4),
+                             rng(c.bias, c.rows * (c.cols / 64), 4)};
+        for (int64_t j = 0; j < count; ++j)
+            for (const Range &o : outs[j])
+                for (const Range &r : wr)
+                    if (overlap(o, r)) return ABG_EALIAS;
+    }
+    // 3. launches: stage by stage; products of a stage that share their
+    //    activation become one grouped launch
+    std::vector<Launch> launches;
+    for (auto &kv : stages) {
+        std::vector<bool> used(kv.second.size(), false);
+        for (size_t a = 0; a < kv.second.size(); ++a) {
+            if (used[a]) continue;
+            const abg_node &nd = nodes[kv.second[a]];
+            used[a] = true;
+            Launch L;
+            L.kind = nd.kind;
+            if (nd.kind == ABG_NODE_Q4MV) {
+                if (nd.n == 0) continue;
+                std::vector<Q4Call> group = {call_of(nd)};
+                for (size_t b = a + 1; b < kv.second.size() && group.size() < static_cast<size_t>(kMaxProbs); ++b) {
+                    const abg_node &nb = nodes[kv.second[b]];
+                    if (used[b] || nb.kind != ABG_NODE_Q4MV || nb.n == 0) continue;
+                    const Q4Call cb = call_of(nb);
+                    if (!same_activation(group[0], cb)) continue;
+                    group.push_back(cb);
+                    used[b] = true;
+                }
+                abg_status st = plan_calls(&L.plan, group, mode, rows_per_warp);
+                if (st != ABG_OK) return st;
+            } else {
+                L.a = nd.x;
+                L.b = nd.wt;
+                L.o = nd.out;
+                L.os = nd.out_sum;
+                L.eps = nd.eps;
+                L.len = nd.len;
+            }
+            launches.push_back(L);
+        }
+    }
+    auto *g = new StageGraph();
+    g->launches = static_cast<int64_t>(launches.size());
+    cudaError_t e = cudaSuccess;
+    for (const Launch &L : launches)
+        if (e == cudaSuccess) e = prepare(L);
+    cudaStream_t cs = nullptr;
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal);
+    if (e == cudaSuccess) {
+        for (size_t i = 0; i < launches.size() && e == cudaSuccess; ++i) e = run(launches[i], cs, i > 0, mode == ABG_TREE);
+        cudaGraph_t graph = nullptr;
+        const cudaError_t e2 = cudaStreamEndCapture(cs, &graph);
+        if (e == cudaSuccess) e = e2;
+        g->graph = graph;
+    }
+    if (e == cudaSuccess) e = cudaGraphInstantiate(&g->exec, g->graph, 0);
+    if (cs) cudaStreamDestroy(cs);
+    if (e != cudaSuccess) {
+        if (g->exec) cudaGraphExecDestroy(g->exec);
+        if (g->graph) cudaGraphDestroy(g->graph);
+        delete g;
+        return cuda_fail(e);
+    }
+    *graph_out = g;
+    return ABG_OK;
+}
+
+abg_status abg_stage_graph_launch(void *graph, void *stream) {
+    if (!graph) return ABG_EINVAL;
+    auto *g = static_cast<StageGraph *>(graph);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    static const bool trace = [] {
+        const char *v = std::getenv("ABG_TRACE");
+        return v && std::strcmp(v, "1") == 0;
+    }();
+    if (!trace) return cuda_fail(cudaGraphLaunch(g->exec, s));
+    cudaEvent_t e0 = nullptr, e1 = nullptr;
+    cudaError_t e = cudaEventCreate(&e0);
+    if (e == cudaSuccess) e = cudaEventCreate(&e1);
+    const auto t0 = std::chrono::steady_clock::now();
+    if (e == cudaSuccess) e = cudaEventRecord(e0, s);
+    if (e == cudaSuccess) e = cudaGraphLaunch(g->exec, s);
+    if (e == cudaSuccess) e = cudaEventRecord(e1, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    const auto t1 = std::chrono::steady_clock::now();
+    float ms = 0.f;
+    if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, e0, e1);
+    if (e == cudaSuccess)
+        std::fprintf(stderr, "abg: stage graph %lld launches, GPU %.3f ms, wall %.3f ms\n",
+                     static_cast<long long>(g->launches), ms,
+                     std::chrono::duration<double, std::milli>(t1 - t0).count());
+    if (e0) cudaEventDestroy(e0);
+    if (e1) cudaEventDestroy(e1);
+    return cuda_fail(e);
+}
+
+abg_status abg_stage_graph_launches(void *graph, int64_t *launches) {
+    if (!graph || !launches) return ABG_EINVAL;
+    *launches = static_cast<StageGraph *>(graph)->launches;
+    return ABG_OK;
+}
+
+abg_status abg_stage_graph_destroy(void *graph) {
+    if (!graph) return ABG_EINVAL;
+    auto *g = static_cast<StageGraph *>(graph);
+    cudaError_t e = cudaSuccess;
+    if (g->exec) e = cudaGraphExecDestroy(g->exec);
+    if (g->graph) {
+        const cudaError_t e2 = cudaGraphDestroy(g->graph);
+        if (e == cudaSuccess) e = e2;
+    }
+    delete g;
+    return cuda_fail(e);
+}
+
+abg_status abg_device_status(uint32_t *bits, int clear) {
+    if (!bits) return ABG_EINVAL;
+    *bits = 0;
+    cudaError_t e = cudaDeviceSynchronize();
+    unsigned v = 0;
+    if (e == cudaSuccess) e = q4mv_status(&v, clear != 0);
+    if (e == cudaSuccess) e = vec_status(&v, clear != 0);
+    if (e != cudaSuccess) return cuda_fail(e);
+    *bits = v;
+    return (v & 1u) ? ABG_ETIMEOUT : ABG_OK;  // bit 0: a bounded wait timed out
+}
+
+abg_status abg_set_q4mv_tuning(int smem_kb, int consumer_warps, int blocks_per_sm) {
+    if (smem_kb < 0 || smem_kb > 227 || consumer_warps < 0 || consumer_warps > 12 || blocks_per_sm < 0 ||
+        blocks_per_sm > 4)
+        return ABG_EINVAL;
+    g_tuning.smem_kb = smem_kb;
+    g_tuning.consumer_warps = consumer_warps;
+    g_tuning.blocks_per_sm = blocks_per_sm;
+    return ABG_OK;
+}
+
+const char *abg_status_str(int status) {
+    switch (status) {
+    case ABG_OK: return "ok";
+    case ABG_EINVAL: return "invalid argument";
+    case ABG_EALIGN: return "misaligned pointer";
+    case ABG_ESHAPE: return "bad shape";
+    case ABG_EALIAS: return "output overlaps an input";
+    case ABG_ECUDA: return "CUDA error";
+    case ABG_ETIMEOUT: return "device wait timed out";
+    default: return "unknown status";
+    }
+}
+
+const char *abg_last_cuda_error(void) { return g_cuda_error.c_str(); }
+
+}  // extern "C"

@@ -1,0 +1,395 @@
+"""Benchmark of the affine 4-bit group-quantized product on one GB300 per rank.
+
+Headline workload: the 4096x2048 product called 400 times back to back (the
+pages' per-call measurement, "Array.q4mv on Metal ..." bendlang/bend #1435,
+Verification: a 4096x2048 product run 400 times, printing a hash of y).  One
+step = the activation's group sums, then 400 dependent products, recorded as
+one stage graph and launched once.  Each product reads its own copy of the
+weights from a ring whose total size is several times the L2 cache, so every
+call streams its weights from HBM.
+
+Also measured in the same run (as "extra"): the 248320x2048 output head and
+one synthetic 24-layer decode token (fused and unfused stage graphs).
+
+Output: one JSON line on rank 0.  --impl reference times the CPU oracle (the
+plain C definition the library is tested against) on the same workload.
+Multi-GPU runs are independent replicas (the product has no exchange step).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from affine_bit_group_gb300 import synth  # noqa: E402
+
+CALLS = 400
+MID_ROWS, MID_COLS = 4096, 2048
+PEAK_FALLBACK_GBS = 6800.0
+
+
+def product_bytes(rows: int, cols: int) -> int:
+    """Algorithmic bytes of one product: nibbles, scale and bias, x, xsum and y."""
+    return rows * cols // 2 + 8 * rows * (cols // 64) + 4 * cols + 4 * (cols // 64) + 4 * rows
+
+
+def measured_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    return PEAK_FALLBACK_GBS, "fallback"
+
+
+def profile_traffic(kernel_src: str, profile: str):
+    """DRAM bytes per launch from a committed ncu summary, or None once the kernel changed."""
+    path = os.path.join(ROOT, "profiles", profile)
+    if not os.path.exists(path):
+        return None
+    vals = {}
+    with open(path) as f:
+        for line in f:
+            if ":" in line and line.strip().startswith(("dram_bytes_per_launch", "kernel_source_sha256")):
+                k, v = line.split(":", 1)
+                vals[k.strip()] = v.strip().strip("`")
+    with open(kernel_src, "rb") as f:
+        sha = hashlib.sha256(f.read()).hexdigest()
+    if vals.get("kernel_source_sha256") != sha or "dram_bytes_per_launch" not in vals:
+        return None
+    return float(vals["dram_bytes_per_launch"])
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_uuid: str | None):
+        self.rows = []
+        self.proc = None
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200"]
+        if device_uuid:
+            cmd += ["-i", device_uuid]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) == 8:
+                self.rows.append(parts)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        if not self.rows:
+            return None
+        sm = [float(r[0]) for r in self.rows if r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
+        reasons = set()
+        for r in self.rows:
+            for name, v in zip(("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"), r[4:]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(self.rows)}
+
+
+def device_uuid():
+    import torch
+    try:
+        u = torch.cuda.get_device_properties(0).uuid
+        s = str(u)
+        return s if s.startswith("GPU-") else "GPU-" + s
+    except Exception:
+        return None
+
+
+def rotating_copies(m, copies: int):
+    """`copies` device copies of one matrix (same bits; separate memory)."""
+    import torch
+    w = torch.from_numpy(m.w.view(np.int32)).cuda()
+    s = torch.from_numpy(m.scale).cuda()
+    b = torch.from_numpy(m.bias).cuda()
+    return [(w.clone(), s.clone(), b.clone()) for _ in range(copies)]
+
+
+def build_mid_graph(abg, mats, x, xsum, ys, calls, mode=0):
+    nodes = [abg.Node.gsum(0, x, xsum)]
+    for i in range(calls):
+        w, s, b = mats[i % len(mats)]
+        nodes.append(abg.Node.q4mv(1 + i, w, s, b, ys[i % 2], MID_COLS, x=x, xsum=xsum))
+    keep = [x, xsum] + ys + [t for m in mats for t in m]
+    return abg.StageGraph(nodes, mode=mode, keep=keep)
+
+
+def time_graph(graph, stream, steps, warmup, sampler_uuid=None):
+    """(ms per replay, clocks) with CUDA events on `stream`, synchronize on both sides."""
+    import torch
+    for _ in range(warmup):
+        graph.launch(stream)
+    torch.cuda.synchronize()
+    sampler = ClockSampler(sampler_uuid) if sampler_uuid is not False else None
+    time.sleep(0.3 if sampler else 0)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(steps):
+        graph.launch(stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop() if sampler else None
+    return e0.elapsed_time(e1) / steps, clocks
+
+
+def run_ours(args, rank, world):
+    import torch
+
+    import affine_bit_group_gb300 as abg
+    import oracle
+    from affine_bit_group_gb300 import decode
+
+    torch.cuda.set_device(0 if world == 1 else int(os.environ.get("LOCAL_RANK", rank)))
+    stream = torch.cuda.Stream()
+    props = torch.cuda.get_device_properties(torch.cuda.current_device())
+    l2 = getattr(props, "L2_cache_size", 126 * 2 ** 20)
+    peak, peak_kind = measured_peak()
+
+    # ---------------------------------------------------------------- mid ---
+    m, x_np = synth.mid()
+    pbytes = product_bytes(MID_ROWS, MID_COLS)
+    copies = max(2, math.ceil(3 * l2 / (m.nbytes)))
+    mats = rotating_copies(m, copies)
+    x = torch.from_numpy(x_np).cuda()
+    xsum = torch.empty(MID_COLS // 64, dtype=torch.float32, device="cuda")
+    ys = [torch.empty(MID_ROWS, dtype=torch.float32, device="cuda") for _ in range(2)]
+    with torch.cuda.stream(stream):
+        g = build_mid_graph(abg, mats, x, xsum, ys, CALLS)
+    uuid = device_uuid()
+    ms_step, clocks = time_graph(g, stream, args.steps, args.warmup, uuid if rank == 0 else False)
+    y_hash = oracle.hash32(ys[(CALLS - 1) % 2].cpu().numpy())
+    exp_hash = oracle.hash32(oracle.q4mv(*m.arrays(), x_np, oracle.gsum(x_np), MID_COLS))
+    if y_hash != exp_hash:
+        raise SystemExit(f"mid product hash {y_hash} differs from the oracle's {exp_hash}")
+    step_bytes = CALLS * pbytes
+    value = step_bytes / (ms_step * 1e-3) / 1e9
+    us_per_product = ms_step * 1e3 / CALLS
+    launches_per_step = g.launches
+
+    # per-launch duration of the product kernel inside the timed graph: the
+    # step is 1 group-sum launch (about 2 us) + 400 chained products
+    achieved = pbytes / (us_per_product * 1e-6) / 1e9
+
+    # ---------------------------------------------------------------- e2e ---
+    x_host = torch.from_numpy(x_np).pin_memory()
+    y_host = torch.empty(MID_ROWS, dtype=torch.float32).pin_memory()
+    for _ in range(args.warmup):
+        with torch.cuda.stream(stream):
+            x.copy_(x_host, non_blocking=True)
+        g.launch(stream)
+        with torch.cuda.stream(stream):
+            y_host.copy_(ys[(CALLS - 1) % 2], non_blocking=True)
+        stream.synchronize()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        with torch.cuda.stream(stream):
+            x.copy_(x_host, non_blocking=True)
+        g.launch(stream)
+        with torch.cuda.stream(stream):
+            y_host.copy_(ys[(CALLS - 1) % 2], non_blocking=True)
+        stream.synchronize()
+    e2e_s = (time.perf_counter() - t0) / args.steps
+    e2e = {"value": step_bytes / e2e_s / 1e9, "unit": "GB/s", "h2d_bytes_per_step": 4 * MID_COLS,
+           "d2h_bytes_per_step": 4 * MID_ROWS, "ms_per_step": e2e_s * 1e3}
+    g.close()
+    del mats, g
+    torch.cuda.empty_cache()
+
+    extra = {}
+    if not args.no_extra:
+        extra["head"] = bench_head(abg, stream, args, peak)
+        extra["decode_token"] = bench_decode(abg, decode, stream, args)
+
+    res = dict(value=value, ms_step=ms_step, us_per_product=us_per_product, achieved=achieved, clocks=clocks,
+               e2e=e2e, extra=extra, launches=launches_per_step * args.steps, peak=peak, peak_kind=peak_kind,
+               hash=y_hash, copies=copies)
+    return res
+
+
+def bench_head(abg, stream, args, peak):
+    import torch
+    m, hidden, wt = synth.head()
+    rows, cols = m.rows, m.cols
+    w = torch.from_numpy(m.w.view(np.int32)).cuda()
+    s = torch.from_numpy(m.scale).cuda()
+    b = torch.from_numpy(m.bias).cuda()
+    h = torch.from_numpy(hidden).cuda()
+    wtd = torch.from_numpy(wt).cuda()
+    xn = torch.empty(cols, dtype=torch.float32, device="cuda")
+    xs = torch.empty(cols // 64, dtype=torch.float32, device="cuda")
+    y = torch.empty(rows, dtype=torch.float32, device="cuda")
+    n = 20
+    nodes = [abg.Node.rmsq(0, h, wtd, xn, xs)] + [abg.Node.q4mv(1 + i, w, s, b, y, cols, x=xn, xsum=xs)
+                                                  for i in range(n)]
+    with torch.cuda.stream(stream):
+        g = abg.StageGraph(nodes, keep=[w, s, b, h, wtd, xn, xs, y])
+    ms, _ = time_graph(g, stream, max(1, args.steps // 2), args.warmup, False)
+    g.close()
+    us = ms * 1e3 / n
+    gbs = product_bytes(rows, cols) / (us * 1e-6) / 1e9
+    return {"workload": "q4mv 248320x2048 output head, x = rmsq(hidden), 20 products per replay",
+            "us_per_product": us, "gbs": gbs, "frac_of_measured_peak": gbs / peak}
+
+
+def bench_decode(abg, decode, stream, args):
+    import torch
+    model, h = synth.decode_model()
+    dm = decode.DeviceModel.upload(model)
+    del model
+    h0 = torch.from_numpy(h).cuda()
+    out = {"workload": "24 layers, hidden 2048, MLP 6144, 248320-row head; 169 products",
+           "product_bytes": dm.product_bytes}
+    for fused in (True, False):
+        with torch.cuda.stream(stream):
+            g, _ = decode.decode_token_graph(dm, h0, fused=fused)
+        ms, _ = time_graph(g, stream, max(3, args.steps), args.warmup, False)
+        # wall time of launch + one sync, per token
+        walls = []
+        for _ in range(max(3, args.steps)):
+            t0 = time.perf_counter()
+            g.launch(stream)
+            stream.synchronize()
+            walls.append((time.perf_counter() - t0) * 1e3)
+        key = "fused" if fused else "unfused"
+        out[key] = {"gpu_ms_per_token": ms, "wall_ms_per_token": statistics.median(walls), "launches": g.launches,
+                    "gbs": dm.product_bytes / (ms * 1e-3) / 1e9}
+        g.close()
+    return out
+
+
+def cpu_baseline(seconds: float = 10.0):
+    """The oracle (plain C, one thread) on the 4096x2048 product, repeated for about `seconds`."""
+    import oracle
+    m, x = synth.mid()
+    xs = oracle.gsum(x)
+    oracle.q4mv(*m.arrays(), x, xs, MID_COLS)
+    n, t0 = 0, time.perf_counter()
+    while time.perf_counter() - t0 < seconds:
+        oracle.q4mv(*m.arrays(), x, xs, MID_COLS)
+        n += 1
+    dt = time.perf_counter() - t0
+    return {"value": n * product_bytes(MID_ROWS, MID_COLS) / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{n} calls of the 4096x2048 product (single-threaded C oracle, {dt:.1f} s)"}
+
+
+def run_reference(args):
+    """The oracle as the reference arm: each step is a bounded sample of the workload on the host."""
+    import oracle
+    m, x = synth.mid()
+    xs = oracle.gsum(x)
+    per_step = 20
+    for _ in range(args.warmup):
+        oracle.q4mv(*m.arrays(), x, xs, MID_COLS)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        xs = oracle.gsum(x)
+        for _ in range(per_step):
+            oracle.q4mv(*m.arrays(), x, xs, MID_COLS)
+    dt = (time.perf_counter() - t0) / args.steps
+    value = per_step * product_bytes(MID_ROWS, MID_COLS) / dt / 1e9
+    sample = f"{per_step} of the step's {CALLS} products per step (single-threaded C oracle)"
+    return {"metric": "q4mv achieved HBM GB/s", "value": value, "unit": "GB/s", "impl": "reference", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": config_dict(),
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def config_dict(copies=None):
+    return {"workload": "q4mv mid: 4096x2048, 400 dependent calls per step (+ group sums of x), seed 1",
+            "rows": MID_ROWS, "cols": MID_COLS, "calls_per_step": CALLS, "mode": "tree",
+            "l2": f"inputs larger than L2: weights rotate over {copies} device copies" if copies else None,
+            "parallelism": "replicas"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-extra", action="store_true", help="skip the head and decode-token measurements")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
+    args = ap.parse_args()
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if os.environ.get("ABG_BENCH_BACKEND") != "gloo" else "gloo")
+    res = run_ours(args, rank, world)
+    ms_step = res["ms_step"]
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        t = torch.tensor([ms_step], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_step = float(t.item())
+        dist.barrier()
+    if rank != 0:
+        return
+    step_bytes = CALLS * product_bytes(MID_ROWS, MID_COLS)
+    value = world * step_bytes / (ms_step * 1e-3) / 1e9
+    kernel_src = os.path.join(ROOT, "affine_bit_group_gb300", "csrc", "q4mv.cu")
+    traffic = profile_traffic(kernel_src, "q4mv_mid_4096x2048.md")
+    line = {
+        "metric": "q4mv achieved HBM GB/s", "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": config_dict(res["copies"]),
+        "us_per_product": res["us_per_product"],
+        "frac_of_peak": {"measured": res["value"] / res["peak"], "nominal_8tbs": res["value"] / 8000.0},
+        "hash32": res["hash"],
+        "roofline": {"bound": "hbm", "achieved": res["achieved"], "peak": res["peak"], "unit": "GB/s",
+                     "frac": res["achieved"] / res["peak"], "traffic": traffic, "peak_kind": res["peak_kind"],
+                     "kernel": "q4mv_kernel<4,tree,bulk scale/bias>"},
+        "clocks": res["clocks"], "e2e": res["e2e"], "gpu_launches": res["launches"], "extra": res["extra"],
+    }
+    if not args.no_cpu:
+        line["cpu_baseline"] = cpu_baseline()
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

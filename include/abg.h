@@ -1,0 +1,223 @@
+/*
+ * abg.h -- C ABI of the GB300 (sm_103a) affine 4-bit group-quantized
+ * matrix-vector product and its two activation producers.
+ *
+ * The operation comes from three Bend pull-request pages by one author:
+ *   [q4mv-metal]  "Array.q4mv on Metal: one kernel thread per row for products
+ *                 of 4M weights or more, bit-identical" (bendlang/bend #1435)
+ *   [q4go]        "Array.q4go/Array.q4wait queue Metal Q4 products in one
+ *                 command buffer and wait once on a flag" (#1437)
+ *   [fused-token] "Metal: queued rmsq, swq, gdn and atq kernels and a 4-row
+ *                 q4mv, so a decode token is one command buffer with one wait"
+ *                 (#1440)
+ *
+ * Weight format ([fused-token] Why and Change; [q4go] Verification): MLX-style
+ * 4-bit affine weights, w = scale*q + bias with q in 0..15, in groups of 64
+ * columns.  q is packed 8 nibbles per u32: column 8k+j of a row is bits
+ * 4j..4j+3 of word k (low nibble first).  scale and bias are f32, one per row
+ * and 64-column group.  The product reads the activation x together with its
+ * 64-value group sums xsum, so that
+ *
+ *     y[r] = sum_g ( scale[r][g] * sum_j q[r][64g+j] * x[64g+j]
+ *                    + bias[r][g] * xsum[g] ).
+ *
+ * Modes.  ABG_TREE reproduces a fixed summation order bit for bit ([fused-token]
+ * Change, bend_q4mv bullet: "sums in a fixed tree order").  Every sum is a
+ * balanced pairwise tree in index order: at each level elements (2i, 2i+1)
+ * are added and an odd last element is carried up unchanged.  Products are
+ * rounded once (RN binary32), the affine term is RN(RN(scale*d) + RN(bias*xsum))
+ * without fused multiply-add, and each row's group terms are summed by the
+ * same tree.  ABG_FAST may reorder and contract; its outputs stay within
+ * 1e-5 * max(|y|, sum_g |scale*d| + |bias*xsum|) of the tree result.
+ *
+ * Conventions shared by every call:
+ *   - Pointers are DEVICE pointers owned by the caller (the library allocates
+ *     nothing per call).  Packed weights and every vector read in pairs
+ *     (x, wt, a, and the xn / o outputs) must be 16-byte aligned; group sums,
+ *     scale, bias and y 4-byte aligned (else ABG_EALIGN).  scale and bias
+ *     rows are streamed with bulk copies when both are 16-byte aligned and
+ *     cols is a multiple of 256, and read with ordinary loads otherwise.
+ *   - Calls are asynchronous: they enqueue on `stream` (a cudaStream_t, NULL =
+ *     the legacy default stream) and return.  The caller synchronizes.
+ *   - Lifetime ([q4go] Change, last paragraph; Limits): every buffer a call
+ *     reads or writes must stay allocated and unmodified by others until the
+ *     stream work has completed.  Freeing w early was seen to corrupt row 0.
+ *   - An output may not overlap any input of the same call (else ABG_EALIAS):
+ *     concurrent products must not read one another's y ([q4go] Change).
+ *   - Lengths that are not whole 64-value groups are rejected (ABG_ESHAPE).
+ *     The pages' GPU kernels silently left such outputs untouched
+ *     ([fused-token] reviewer reply); here it is an error.
+ *   - A device-side wait that exceeds its time limit (about 2 s) stops the
+ *     kernel and sets a bit in the library's device status word; read it with
+ *     abg_device_status().  No call hangs the GPU.
+ */
+#ifndef ABG_H
+#define ABG_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    ABG_OK = 0,
+    ABG_EINVAL = 1,   /* null pointer, bad mode, bad enum, bad count */
+    ABG_EALIGN = 2,   /* a pointer is not aligned as the call requires */
+    ABG_ESHAPE = 3,   /* size not a positive multiple of 64, row range out of bounds, cols too large */
+    ABG_EALIAS = 4,   /* an output overlaps an input (or, in a graph, a same-stage read) */
+    ABG_ECUDA = 5,    /* a CUDA runtime call failed; see abg_last_cuda_error() */
+    ABG_ETIMEOUT = 6  /* a device-side wait ran out of time (reported by abg_device_status) */
+} abg_status;
+
+typedef enum { ABG_TREE = 0, ABG_FAST = 1 } abg_mode;
+
+/* Largest `cols` a product accepts: the activation row is staged once per
+ * thread block in shared memory. */
+#define ABG_MAX_COLS 16384
+
+/*
+ * q4mv: rows row0 .. row0+n-1 of the packed rows x cols matrix times x.
+ * ([q4go] Change: Array.q4go(w, x, y, r, n, cols, rows) -- reading: r is the
+ *  first row, n the number of rows computed, rows the matrix height that
+ *  locates each row's words, scale and bias.)
+ *
+ *   w      u32 [rows][cols/8]   packed nibbles (see the header comment)
+ *   scale  f32 [rows][cols/64]
+ *   bias   f32 [rows][cols/64]
+ *   x      f32 [cols]
+ *   xsum   f32 [cols/64]        xsum[g] = tree sum of x[64g .. 64g+63]
+ *   y      f32 [n]              y[i] = row row0+i
+ *   cols   positive multiple of 64, at most ABG_MAX_COLS
+ *   0 <= row0, 0 <= n, row0 + n <= rows.  n == 0 enqueues nothing.
+ *   mode   ABG_TREE or ABG_FAST
+ *   rows_per_warp  1, 2, 4 or 8 rows share one staging of each 1024-column
+ *          slice of x in a warp's registers ([fused-token] Change: a SIMD
+ *          group does 4 rows and reads each group's activations once); 0 picks
+ *          the default (4).  It never changes the result.
+ */
+abg_status abg_q4mv(const uint32_t *w, const float *scale, const float *bias,
+                    const float *x, const float *xsum, float *y,
+                    int64_t rows, int64_t cols, int64_t row0, int64_t n,
+                    int mode, int rows_per_warp, void *stream);
+
+/*
+ * gsum: s[g] = tree sum of v[64g .. 64g+63], g < n/64.  The group sums a
+ * product reads for its bias term ([fused-token] Change, Array.rmsq bullet:
+ * "the 64-value group sums that Array.q4mv reads").  n a positive multiple of 64.
+ */
+abg_status abg_gsum(const float *v, float *s, int64_t n, int mode, void *stream);
+
+/*
+ * rmsq: RMS norm with weights plus the group sums of its output
+ * ([fused-token] Change, Array.rmsq bullet).
+ *   ss      = tree over groups of (tree over the group of x[i]*x[i])
+ *   r       = 1 / sqrt(ss / n + eps)
+ *   xn[i]   = (x[i] * r) * wt[i]
+ *   xsum[g] = tree sum of xn over group g
+ * x, wt, xn f32 [n]; xsum f32 [n/64]; n a positive multiple of 64, at most
+ * 2^20.  Runs in one thread block.
+ */
+abg_status abg_rmsq(const float *x, const float *wt, float eps, float *xn, float *xsum,
+                    int64_t n, int mode, void *stream);
+
+/*
+ * swq: SwiGLU plus the group sums of its output ([fused-token] Change,
+ * Array.swq(a, o, n) bullet).  a = [gate (n) | up (n)].
+ *   o[i]    = silu(a[i]) * a[n+i],  silu(g) = g / (1 + EXP(-g))
+ *   osum[g] = tree sum of o over group g
+ * In ABG_TREE mode EXP is the library's own binary32 exponential (Cody-Waite
+ * reduction with a two-part ln 2, degree-7 Taylor polynomial with RN(1/i!)
+ * coefficients, exact scaling by 2^k), so the result is bit-exact across
+ * devices; a vendor exp moves the last bits ([fused-token] Change, last
+ * paragraph).  a f32 [2n]; o f32 [n]; osum f32 [n/64]; n a positive multiple
+ * of 64.
+ */
+abg_status abg_swq(const float *a, float *o, float *osum, int64_t n, int mode, void *stream);
+
+/* ---------------------------------------------------------------------------
+ * Stage graph: one decode token's dependent stages recorded into one CUDA
+ * graph, replayed with one launch and synchronized once by the caller
+ * ([fused-token] Why and Verification: one command buffer, one wait per
+ * token; [q4go] Change: products queued together run concurrently, and a
+ * dependent stage needs the previous one finished).
+ *
+ * Nodes carry a stage index.  Nodes with the same index form one stage and
+ * may run concurrently; every node of stage s+1 runs after every node of
+ * stage s has finished.  Products of one stage that read the same x (for
+ * example q/k/v, or gate/up) are run as one grouped launch.  Consecutive
+ * launches overlap through programmatic dependent launch: a product fetches
+ * its weights before the previous stage has finished and waits only before
+ * it reads its activation.  Weights must therefore not be written by any node
+ * of the graph (checked: ABG_EALIAS).
+ *
+ * Node kinds and the fields each reads (unused fields are ignored):
+ *   ABG_NODE_Q4MV  w, scale, bias, rows, cols, row0, n, y, prologue, and
+ *                  prologue ABG_PRO_NONE: x [cols], xsum [cols/64]
+ *                  prologue ABG_PRO_GSUM: x [cols]; xsum computed in-kernel
+ *                  prologue ABG_PRO_RMSQ: x [cols] (un-normalized), wt [cols],
+ *                                         eps; the product reads rmsq(x, wt)
+ *                  prologue ABG_PRO_SWQ:  x [2*cols] = [gate | up]; the
+ *                                         product reads swq(x)
+ *                  A prologue recomputes the producer inside each thread
+ *                  block with the same trees, so the product's result is
+ *                  bit-identical to running the producer node first.
+ *   ABG_NODE_RMSQ  x, wt, eps, len -> out (xn), out_sum (xsum)
+ *   ABG_NODE_SWQ   x (2*len), len -> out (o), out_sum (osum)
+ *   ABG_NODE_GSUM  x, len -> out_sum
+ * ------------------------------------------------------------------------- */
+typedef enum { ABG_NODE_Q4MV = 0, ABG_NODE_RMSQ = 1, ABG_NODE_SWQ = 2, ABG_NODE_GSUM = 3 } abg_node_kind;
+typedef enum { ABG_PRO_NONE = 0, ABG_PRO_GSUM = 1, ABG_PRO_RMSQ = 2, ABG_PRO_SWQ = 3 } abg_prologue;
+
+typedef struct abg_node {
+    int32_t kind;      /* abg_node_kind */
+    int32_t stage;     /* stage index; any order, grouped by value */
+    const uint32_t *w; /* Q4MV */
+    const float *scale;
+    const float *bias;
+    int64_t rows, cols, row0, n;
+    float *y;
+    int32_t prologue;  /* abg_prologue, Q4MV only */
+    float eps;         /* RMSQ node and ABG_PRO_RMSQ */
+    const float *x;    /* activation / producer input (see above) */
+    const float *xsum; /* Q4MV with ABG_PRO_NONE */
+    const float *wt;   /* RMSQ node and ABG_PRO_RMSQ */
+    float *out;        /* RMSQ, SWQ */
+    float *out_sum;    /* RMSQ, SWQ, GSUM */
+    int64_t len;       /* RMSQ, SWQ, GSUM vector length n */
+} abg_node;
+
+/* Validates every node (same rules as the single calls), checks that no node
+ * reads an output of its own stage, records the launches on a private stream
+ * and instantiates the graph.  *graph_out receives an opaque handle. */
+abg_status abg_stage_graph_create(const abg_node *nodes, int64_t count, int mode, int rows_per_warp,
+                                  void **graph_out);
+/* Enqueues one replay of the whole graph on `stream`; the caller syncs once.
+ * With the environment variable ABG_TRACE=1 each launch also synchronizes and
+ * prints the launch count, GPU milliseconds and wall milliseconds to stderr. */
+abg_status abg_stage_graph_launch(void *graph, void *stream);
+/* Number of kernel launches one replay performs (after sibling grouping). */
+abg_status abg_stage_graph_launches(void *graph, int64_t *launches);
+abg_status abg_stage_graph_destroy(void *graph);
+
+/* Reads (and, if clear != 0, resets) the device status word on the current
+ * device: bit 0 = a device-side wait timed out.  Synchronizes the device.
+ * Returns ABG_ETIMEOUT when bit 0 was set, else ABG_OK. */
+abg_status abg_device_status(uint32_t *bits, int clear);
+
+/* Tuning of the product kernel, process-wide; 0 keeps the default.
+ *   smem_kb          shared-memory budget per thread block (default 100, so
+ *                    two blocks fit on an SM and consecutive launches overlap)
+ *   consumer_warps   warps that compute (default: chosen from cols)
+ *   blocks_per_sm    thread blocks per SM in the grid (default: 1)
+ * It never changes results. */
+abg_status abg_set_q4mv_tuning(int smem_kb, int consumer_warps, int blocks_per_sm);
+
+const char *abg_status_str(int status);
+/* Text of the last CUDA error seen by any call on this thread ("" if none). */
+const char *abg_last_cuda_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* ABG_H */

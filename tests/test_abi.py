@@ -1,0 +1,149 @@
+"""The C ABI without a GPU: the library loads, exports every declared entry
+point, mirrors struct abg_node exactly, and rejects bad arguments with the
+documented status before touching the device."""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "abg.h")
+
+import affine_bit_group_gb300 as abg  # noqa: E402
+
+OK, EINVAL, EALIGN, ESHAPE, EALIAS = 0, 1, 2, 3, 4
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return abg.library()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(abg_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_every_declared_function_is_exported(lib):
+    names = declared_functions()
+    assert len(names) >= 12
+    for n in names:
+        assert hasattr(lib, n), n
+    nm = subprocess.run(["nm", "-D", "--defined-only", os.path.join(ROOT, "affine_bit_group_gb300", "libabg.so")],
+                        capture_output=True, text=True, check=True).stdout
+    exported = set(re.findall(r"\bT (abg_\w+)", nm))
+    assert set(names) <= exported
+
+
+def test_node_struct_layout_matches_c(tmp_path):
+    """sizeof and field offsets of struct abg_node as gcc sees the header."""
+    fields = [f for f, _ in abg._Node._fields_]
+    prog = tmp_path / "layout.c"
+    lines = ["#include <stdio.h>", "#include <stddef.h>", '#include "abg.h"', "int main(void){",
+             'printf("%zu\\n", sizeof(abg_node));']
+    lines += [f'printf("%zu\\n", offsetof(abg_node, {f}));' for f in fields]
+    lines += ["return 0;}"]
+    prog.write_text("\n".join(lines))
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), str(prog), "-o", str(exe)], check=True)
+    out = [int(v) for v in subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()]
+    assert out[0] == ctypes.sizeof(abg._Node)
+    for f, off in zip(fields, out[1:]):
+        assert getattr(abg._Node, f).offset == off, f
+
+
+def test_status_strings(lib):
+    assert lib.abg_status_str(0) == b"ok"
+    assert lib.abg_status_str(4) == b"output overlaps an input"
+    assert lib.abg_status_str(99) == b"unknown status"
+
+
+A = 0x7F0000000000  # fake, 256-byte aligned device addresses: only validation runs
+
+
+def q4(lib, w=A, s=A + 0x100000, b=A + 0x200000, x=A + 0x300000, xs=A + 0x310000, y=A + 0x400000, rows=8, cols=128,
+       row0=0, n=8, mode=0, rpw=0):
+    return lib.abg_q4mv(w, s, b, x, xs, y, rows, cols, row0, n, mode, rpw, None)
+
+
+def test_q4mv_validation(lib):
+    assert q4(lib, w=0) == EINVAL
+    assert q4(lib, mode=2) == EINVAL
+    assert q4(lib, rpw=3) == EINVAL
+    assert q4(lib, cols=100) == ESHAPE
+    assert q4(lib, cols=0) == ESHAPE
+    assert q4(lib, cols=16384 + 64) == ESHAPE
+    assert q4(lib, row0=4, n=5) == ESHAPE
+    assert q4(lib, n=-1) == ESHAPE
+    assert q4(lib, w=A + 4) == EALIGN
+    assert q4(lib, x=A + 0x300008) == EALIGN
+    assert q4(lib, y=A + 0x400002) == EALIGN
+    assert q4(lib, y=A + 0x300010) == EALIAS          # y overlaps x
+    assert q4(lib, y=A + 8) == EALIAS                 # y overlaps the packed weights
+    assert q4(lib, n=0, row0=8) == OK                 # empty: nothing enqueued, no device use
+
+
+def test_vector_validation(lib):
+    assert lib.abg_gsum(A, A + 0x1000, 100, 0, None) == ESHAPE
+    assert lib.abg_gsum(A + 4, A + 0x1000, 128, 0, None) == EALIGN
+    assert lib.abg_gsum(A, A + 4, 128, 0, None) == EALIAS
+    assert lib.abg_rmsq(A, A + 0x1000, ctypes.c_float(1e-6), A + 0x2000, A + 0x3000, (1 << 20) + 64, 0, None) == ESHAPE
+    assert lib.abg_rmsq(A, A + 0x1000, ctypes.c_float(1e-6), A, A + 0x3000, 128, 0, None) == EALIAS
+    assert lib.abg_rmsq(A, A + 0x1000, ctypes.c_float(1e-6), A + 0x2000, A + 0x2000, 128, 0, None) == EALIAS
+    assert lib.abg_swq(A, A + 0x100, A + 0x3000, 128, 0, None) == EALIAS   # o inside a = [gate | up]
+    assert lib.abg_swq(A, A + 0x2000, A + 0x3000, 96, 0, None) == ESHAPE
+    assert lib.abg_swq(None, A + 0x2000, A + 0x3000, 128, 0, None) == EINVAL
+    assert lib.abg_swq(A, A + 0x2000, A + 0x3000, 128, 7, None) == EINVAL
+
+
+def node(**kw):
+    return abg._Node(**kw)
+
+
+def create(lib, nodes, mode=0, rpw=0):
+    arr = (abg._Node * len(nodes))(*nodes)
+    h = ctypes.c_void_p()
+    st = lib.abg_stage_graph_create(arr, len(nodes), mode, rpw, ctypes.byref(h))
+    assert not h.value
+    return st
+
+
+def test_stage_graph_validation(lib):
+    h = ctypes.c_void_p()
+    assert lib.abg_stage_graph_create(None, 0, 0, 0, ctypes.byref(h)) == EINVAL
+    assert lib.abg_stage_graph_create(None, 1, 0, 0, None) == EINVAL
+    prod = dict(kind=0, stage=1, w=A, scale=A + 0x100000, bias=A + 0x200000, rows=8, cols=128, row0=0, n=8,
+                y=A + 0x400000, x=A + 0x300000, xsum=A + 0x310000)
+    assert create(lib, [node(**{**prod, "kind": 9})]) == EINVAL
+    assert create(lib, [node(**{**prod, "cols": 96})]) == ESHAPE
+    assert create(lib, [node(**{**prod, "prologue": 7})]) == EINVAL
+    # the producer of x in the same stage as the product reading it
+    rms = dict(kind=1, stage=1, x=A + 0x500000, wt=A + 0x510000, out=A + 0x300000, out_sum=A + 0x310000, len=128)
+    assert create(lib, [node(**rms), node(**prod)]) == EALIAS
+    # a node that writes a product's scale
+    gs = dict(kind=3, stage=0, x=A + 0x500000, out_sum=A + 0x100000, len=128)
+    assert create(lib, [node(**gs), node(**prod)]) == EALIAS
+    # two products of one stage writing the same y
+    assert create(lib, [node(**prod), node(**{**prod, "w": A + 0x600000})]) == EALIAS
+    assert lib.abg_stage_graph_launch(None, None) == EINVAL
+    assert lib.abg_stage_graph_destroy(None) == EINVAL
+
+
+def test_tuning_validation(lib):
+    assert lib.abg_set_q4mv_tuning(300, 0, 0) == EINVAL
+    assert lib.abg_set_q4mv_tuning(0, 13, 0) == EINVAL
+    assert lib.abg_set_q4mv_tuning(0, 0, 0) == OK
+
+
+def test_product_path_has_no_cpu_fallback():
+    """The package never imports the oracle: its modules name no oracle import."""
+    pkg = os.path.join(ROOT, "affine_bit_group_gb300")
+    for f in os.listdir(pkg):
+        if f.endswith(".py"):
+            src = open(os.path.join(pkg, f)).read()
+            assert "import oracle" not in src and "from oracle" not in src, f

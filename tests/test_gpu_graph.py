@@ -1,0 +1,133 @@
+"""The decode-token stage graph on the GPU against the oracle's decode token.
+
+Tree mode: the head's output (and every intermediate) is bit-for-bit the
+oracle's, for the unfused graph (one launch per step) and the fused one
+(producers recomputed inside the products).  Replays are deterministic and
+two graphs replayed in turn match their solo runs.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+
+import oracle
+from affine_bit_group_gb300 import synth
+from helpers import assert_bits_equal, dev, empty, host
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+abg = pytest.importorskip("affine_bit_group_gb300")
+from affine_bit_group_gb300 import decode  # noqa: E402
+
+SMALL = dict(seed=7, n_layers=3, hidden=1024, mlp=3072, head_rows=5000, q_rows=2048, kv_rows=256)
+
+
+@pytest.fixture(scope="module")
+def small():
+    model, h = synth.decode_model(**SMALL)
+    logits, trace, (xf, xfs) = oracle.decode_token(model, h, keep=True)
+    return model, h, logits, trace, decode.DeviceModel.upload(model)
+
+
+@pytest.mark.parametrize("fused", [False, True])
+def test_small_decode_token_bit_exact(small, fused):
+    model, h, logits, trace, dm = small
+    h0 = dev(h)
+    g, out = decode.decode_token_graph(dm, h0, fused=fused)
+    g.launch()
+    torch.cuda.synchronize()
+    for i, (o, t) in enumerate(zip(out["layers"], trace)):
+        for key in ("q", "k", "v", "o", "h"):
+            assert_bits_equal(host(o[key]), t[key], f"layer {i} {key}")
+        assert_bits_equal(host(o["gu"]), np.concatenate([t["gate"], t["up"]]), f"layer {i} gate|up")
+        if not fused:
+            assert_bits_equal(host(o["xn"]), t["xn"], f"layer {i} xn")
+            assert_bits_equal(host(o["qs"]), t["qs"], f"layer {i} qs")
+            assert_bits_equal(host(o["s"]), t["s"], f"layer {i} s")
+    assert_bits_equal(host(out["logits"]), logits, "logits")
+    expected_launches = (4 if fused else 8) * SMALL["n_layers"] + (1 if fused else 2)
+    assert g.launches == expected_launches
+    g.close()
+
+
+def test_replay_and_interleaving(small):
+    model, h, logits, trace, dm = small
+    h0 = dev(h)
+    g1, out1 = decode.decode_token_graph(dm, h0, fused=True)
+    h2 = synth.activations(np.random.default_rng(99), SMALL["hidden"])
+    h0b = dev(h2)
+    g2, out2 = decode.decode_token_graph(dm, h0b, fused=False)
+    exp2 = oracle.decode_token(model, h2)
+    for _ in range(3):
+        g1.launch()
+        g2.launch()
+    torch.cuda.synchronize()
+    assert_bits_equal(host(out1["logits"]), logits, "graph 1 after interleaving")
+    assert_bits_equal(host(out2["logits"]), exp2, "graph 2 after interleaving")
+    # replacing the input between replays changes only what it should
+    h0.copy_(h0b)
+    g1.launch()
+    torch.cuda.synchronize()
+    assert_bits_equal(host(out1["logits"]), exp2, "graph 1 with the second input")
+    g1.close()
+    g2.close()
+
+
+def test_fast_graph_equals_fast_calls(small):
+    """Fast mode is deterministic: the graph gives the same bits as the same kernels called one by one."""
+    model, h, logits, trace, dm = small
+    h0 = dev(h)
+    g, out = decode.decode_token_graph(dm, h0, fused=False, mode=abg.FAST)
+    g.launch()
+    torch.cuda.synchronize()
+    L = dm.layers[0]
+    xn, xs = empty(dm.hidden), empty(dm.hidden // 64)
+    abg.rmsq(h0, L["rms1"], xn, xs, mode=abg.FAST)
+    q = empty(L["q"].rows)
+    abg.q4mv(L["q"].w, L["q"].scale, L["q"].bias, xn, xs, q, cols=L["q"].cols, mode=abg.FAST)
+    torch.cuda.synchronize()
+    assert_bits_equal(host(q), host(out["layers"][0]["q"]), "fast q")
+    # and stays close to the tree result: errors of 1e-6 relative per step, renormalized every layer
+    rel = np.max(np.abs(host(out["logits"]) - logits)) / np.max(np.abs(logits))
+    assert rel < 1e-3, rel
+    g.close()
+
+
+def test_graph_rejects_same_stage_hazards(small):
+    model, h, logits, trace, dm = small
+    L = dm.layers[0]
+    x, xs = empty(dm.hidden), empty(dm.hidden // 64)
+    y = empty(L["q"].rows)
+    q = L["q"]
+    # a product and the producer of its input in the same stage
+    nodes = [abg.Node.rmsq(0, dev(h), L["rms1"], x, xs), abg.Node.q4mv(0, q.w, q.scale, q.bias, y, q.cols, x=x, xsum=xs)]
+    with pytest.raises(abg.AbgError) as e:
+        abg.StageGraph(nodes)
+    assert e.value.status == 4
+    # a node that writes a product's weights
+    wview = q.scale.view(-1)[: dm.hidden // 64]
+    nodes = [abg.Node.gsum(0, x, wview), abg.Node.q4mv(1, q.w, q.scale, q.bias, y, q.cols, x=x, xsum=xs)]
+    with pytest.raises(abg.AbgError) as e:
+        abg.StageGraph(nodes)
+    assert e.value.status == 4
+
+
+@pytest.mark.slow
+def test_full_decode_token_bit_exact():
+    """24 layers, hidden 2048, MLP 6144, the 248320-row head: fused graph == oracle, bit for bit."""
+    model, h = synth.decode_model()
+    exp = oracle.decode_token(model, h)
+    dm = decode.DeviceModel.upload(model)
+    h0 = dev(h)
+    g, out = decode.decode_token_graph(dm, h0, fused=True)
+    g.launch()
+    torch.cuda.synchronize()
+    assert_bits_equal(host(out["logits"]), exp, "full decode logits")
+    g2, out2 = decode.decode_token_graph(dm, h0, fused=False)
+    g2.launch()
+    torch.cuda.synchronize()
+    assert_bits_equal(host(out2["logits"]), exp, "full decode logits, unfused")
+    assert abg.device_status(clear=True) == 0
+    g.close()
+    g2.close()
