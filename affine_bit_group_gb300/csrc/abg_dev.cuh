@@ -104,6 +104,9 @@ __device__ __forceinline__ void named_bar(unsigned id, unsigned threads) {
 // ------------------------------------------------------- packed f32x2 ------
 // Two independent binary32 operations, each rounded to nearest even (no
 // flush to zero); element-wise identical to the scalar __f*_rn intrinsics.
+// Unlike the scalar intrinsics, a packed multiply followed by a packed add
+// may be fused into one packed FMA by the compiler, so exact code never
+// feeds mul2's result into add2.
 __device__ __forceinline__ float2 add2(float2 a, float2 b) {
     unsigned long long d;
     asm("add.rn.f32x2 %0, %1, %2;"

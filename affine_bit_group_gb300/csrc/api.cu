@@ -27,9 +27,9 @@ namespace {
 thread_local std::string g_cuda_error;
 Q4Tuning g_tuning;
 
-abg_status cuda_fail(cudaError_t e) {
+abg_status cuda_fail(cudaError_t e, const char *where = nullptr) {
     if (e == cudaSuccess) return ABG_OK;
-    g_cuda_error = cudaGetErrorString(e);
+    g_cuda_error = where ? std::string(where) + ": " + cudaGetErrorString(e) : std::string(cudaGetErrorString(e));
     return ABG_ECUDA;
 }
 
@@ -236,8 +236,8 @@ abg_status abg_q4mv(const uint32_t *w, const float *scale, const float *bias, co
     st = plan_calls(&plan, {c}, mode, rows_per_warp);
     if (st != ABG_OK) return st;
     cudaError_t e = prepare_q4mv(plan);
-    if (e == cudaSuccess) e = launch_q4mv(plan, static_cast<cudaStream_t>(stream), false);
-    return cuda_fail(e);
+    if (e != cudaSuccess) return cuda_fail(e, "kernel attributes");
+    return cuda_fail(launch_q4mv(plan, static_cast<cudaStream_t>(stream), false), "q4mv launch");
 }
 
 abg_status abg_gsum(const float *v, float *s, int64_t n, int mode, void *stream) {
@@ -347,25 +347,32 @@ abg_status abg_stage_graph_create(const abg_node *nodes, int64_t count, int mode
     auto *g = new StageGraph();
     g->launches = static_cast<int64_t>(launches.size());
     cudaError_t e = cudaSuccess;
+    std::string where;
     for (const Launch &L : launches)
-        if (e == cudaSuccess) e = prepare(L);
+        if (e == cudaSuccess && (e = prepare(L)) != cudaSuccess) where = "kernel attributes";
     cudaStream_t cs = nullptr;
-    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking);
-    if (e == cudaSuccess) e = cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal);
+    if (e == cudaSuccess && (e = cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking)) != cudaSuccess)
+        where = "cudaStreamCreateWithFlags";
+    if (e == cudaSuccess && (e = cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal)) != cudaSuccess)
+        where = "cudaStreamBeginCapture";
     if (e == cudaSuccess) {
-        for (size_t i = 0; i < launches.size() && e == cudaSuccess; ++i) e = run(launches[i], cs, i > 0, mode == ABG_TREE);
+        for (size_t i = 0; i < launches.size() && e == cudaSuccess; ++i)
+            if ((e = run(launches[i], cs, i > 0, mode == ABG_TREE)) != cudaSuccess)
+                where = "launch " + std::to_string(i) + " (kind " + std::to_string(launches[i].kind) + ")";
         cudaGraph_t graph = nullptr;
         const cudaError_t e2 = cudaStreamEndCapture(cs, &graph);
-        if (e == cudaSuccess) e = e2;
+        if (e == cudaSuccess && (e = e2) != cudaSuccess) where = "cudaStreamEndCapture";
         g->graph = graph;
     }
-    if (e == cudaSuccess) e = cudaGraphInstantiate(&g->exec, g->graph, 0);
+    if (e == cudaSuccess && (e = cudaGraphInstantiate(&g->exec, g->graph, 0)) != cudaSuccess)
+        where = "cudaGraphInstantiate";
     if (cs) cudaStreamDestroy(cs);
     if (e != cudaSuccess) {
         if (g->exec) cudaGraphExecDestroy(g->exec);
         if (g->graph) cudaGraphDestroy(g->graph);
         delete g;
-        return cuda_fail(e);
+        cudaGetLastError();
+        return cuda_fail(e, where.c_str());
     }
     *graph_out = g;
     return ABG_OK;

@@ -43,6 +43,8 @@
 #include "abg_kernels.cuh"
 
 #include <algorithm>
+#include <mutex>
+#include <set>
 
 namespace abg {
 
@@ -79,8 +81,11 @@ __device__ __forceinline__ float lane_sum32(uint4 wq, const float2 (&X)[16], con
             if (kExact) {
                 P[m] = fma2(v, X[m], Cc[m]);
             } else {
+                // q*x rounded once.  Written as fma(q, x, -0) (exact: adding -0
+                // changes nothing, not even a zero's sign) because the compiler
+                // fuses a packed multiply with the packed add that follows it.
                 const float e = -__uint_as_float(magic_bits(m & 3));
-                P[m] = mul2(add2(v, f2(e, e)), X[m]);
+                P[m] = fma2(add2(v, f2(e, e)), X[m], f2(kNegZero, kNegZero));
             }
         }
         // P[m] = {p_m, p_(m+16)}: adding P[2i] and P[2i+1] pairs leaves (2i, 2i+1)
@@ -336,7 +341,7 @@ __global__ void __launch_bounds__(416, 1) q4mv_kernel(const __grid_constant__ Q4
 #pragma unroll
                 for (int m = 0; m < 16; ++m) {
                     const float e = -__uint_as_float(magic_bits(m & 3));
-                    Cc[m] = mul2(X[m], f2(e, e));
+                    Cc[m] = f2(__fmul_rn(X[m].x, e), __fmul_rn(X[m].y, e));
                 }
                 xsg = active ? xs[g] : 0.f;
             }
@@ -424,6 +429,8 @@ void *select_kernel(int R, bool tree, bool sb) {
 
 inline uint32_t align_up(uint32_t v, uint32_t a) { return (v + a - 1) / a * a; }
 
+cudaError_t raise_smem_limit(void *fn);
+
 }  // namespace
 
 cudaError_t q4mv_status(unsigned *bits, bool clear) {
@@ -448,7 +455,8 @@ int sm_count() {
     return n;
 }
 
-bool plan_q4mv(Q4Plan *plan, const Q4Prob *probs, int nprob, int cols, int prologue, const float *x,
+namespace {
+bool plan_once(Q4Plan *plan, const Q4Prob *probs, int nprob, int cols, int prologue, const float *x,
                const float *xsum, const float *wt, float eps, bool tree, int rows_per_warp, bool sb_smem,
                const Q4Tuning &tune) {
     Q4Args &a = plan->args;
@@ -526,8 +534,7 @@ bool plan_q4mv(Q4Plan *plan, const Q4Prob *probs, int nprob, int cols, int prolo
     // blocks per SM: what fits (registers and shared memory), at most 2 unless tuned
     int fit = 1;
     void *fn = select_kernel(R, tree, sb_smem);
-    if (fn && cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   static_cast<int>(a.smem_bytes)) == cudaSuccess) {
+    if (fn && raise_smem_limit(fn) == cudaSuccess) {
         int nb = 0;
         if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, fn, static_cast<int>(32 * (1 + nw)), a.smem_bytes) ==
                 cudaSuccess &&
@@ -546,11 +553,42 @@ bool plan_q4mv(Q4Plan *plan, const Q4Prob *probs, int nprob, int cols, int prolo
     return true;
 }
 
+// Every instantiation gets the device's largest dynamic shared-memory limit
+// once, so launches with different plans (different sizes) of one kernel can
+// share it (a per-plan limit would be overwritten by the last plan prepared).
+cudaError_t raise_smem_limit(void *fn) {
+    static std::mutex mu;
+    static std::set<void *> done;
+    std::lock_guard<std::mutex> lock(mu);
+    if (done.count(fn)) return cudaSuccess;
+    int dev = 0, optin = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    cudaFuncAttributes fa;
+    if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, fn);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 optin - static_cast<int>(fa.sharedSizeBytes));
+    if (e == cudaSuccess) done.insert(fn);
+    return e;
+}
+
+}  // namespace
+
+// Plans with the requested rows per item; if the stages do not fit in shared
+// memory (very wide rows), retries with fewer rows per item (same results).
+bool plan_q4mv(Q4Plan *plan, const Q4Prob *probs, int nprob, int cols, int prologue, const float *x,
+               const float *xsum, const float *wt, float eps, bool tree, int rows_per_warp, bool sb_smem,
+               const Q4Tuning &tune) {
+    for (int R = rows_per_warp; R >= 1; R /= 2)
+        if (plan_once(plan, probs, nprob, cols, prologue, x, xsum, wt, eps, tree, R, sb_smem, tune)) return true;
+    return false;
+}
+
 cudaError_t prepare_q4mv(const Q4Plan &plan) {
     void *fn = select_kernel(plan.rows_per_warp, plan.tree, plan.sb_smem);
     if (!fn) return cudaErrorInvalidValue;
-    return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                static_cast<int>(plan.args.smem_bytes));
+    return raise_smem_limit(fn);
 }
 
 cudaError_t launch_q4mv(const Q4Plan &plan, cudaStream_t stream, bool pdl) {

@@ -347,7 +347,19 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-extra", action="store_true", help="skip the head and decode-token measurements")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
+    ap.add_argument("--only", choices=["head", "decode"], default=None,
+                    help="run one secondary workload alone and print its numbers (for profiling)")
     args = ap.parse_args()
+    if args.only:
+        import torch
+
+        import affine_bit_group_gb300 as abg
+        from affine_bit_group_gb300 import decode
+        stream = torch.cuda.Stream()
+        peak, _ = measured_peak()
+        out = bench_head(abg, stream, args, peak) if args.only == "head" else bench_decode(abg, decode, stream, args)
+        print(json.dumps(out), flush=True)
+        return
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))
 
