@@ -75,23 +75,33 @@ __device__ __forceinline__ float lane_sum32(uint4 wq, const float2 (&X)[16], con
     const uint32_t h0 = w0 >> 16, h1 = w1 >> 16, h2 = w2 >> 16, h3 = w3 >> 16;
     if (kTree) {
         float2 P[16];
+        if (kExact) {
 #pragma unroll
-        for (int m = 0; m < 16; ++m) {
-            const float2 v = (m < 8) ? nib2(w0, h0, w2, h2, m & 7) : nib2(w1, h1, w3, h3, m & 7);
-            if (kExact) {
+            for (int m = 0; m < 16; ++m) {
+                const float2 v = (m < 8) ? nib2(w0, h0, w2, h2, m & 7) : nib2(w1, h1, w3, h3, m & 7);
                 P[m] = fma2(v, X[m], Cc[m]);
-            } else {
-                // q*x rounded once.  Written as fma(q, x, -0) (exact: adding -0
-                // changes nothing, not even a zero's sign) because the compiler
-                // fuses a packed multiply with the packed add that follows it.
-                const float e = -__uint_as_float(magic_bits(m & 3));
-                P[m] = fma2(add2(v, f2(e, e)), X[m], f2(kNegZero, kNegZero));
             }
-        }
-        // P[m] = {p_m, p_(m+16)}: adding P[2i] and P[2i+1] pairs leaves (2i, 2i+1)
-        // in both halves; the halves stay aligned level after level.
+            // P[m] = {p_m, p_(m+16)}: adding P[2i] and P[2i+1] pairs leaves (2i, 2i+1)
+            // in both halves; the halves stay aligned level after level.
 #pragma unroll
-        for (int i = 0; i < 8; ++i) P[i] = add2(P[2 * i], P[2 * i + 1]);
+            for (int i = 0; i < 8; ++i) P[i] = add2(P[2 * i], P[2 * i + 1]);
+        } else {
+            // Plain path: q converted exactly, products and the first tree level
+            // as scalar RN operations.  (The compiler may fuse a packed multiply
+            // or a packed fma with a -0 addend into the packed add after it; the
+            // scalar __fmul_rn / __fadd_rn intrinsics are never contracted.)
+            float p[32];
+#pragma unroll
+            for (int m = 0; m < 16; ++m) {
+                const float2 v = (m < 8) ? nib2(w0, h0, w2, h2, m & 7) : nib2(w1, h1, w3, h3, m & 7);
+                const float e = -__uint_as_float(magic_bits(m & 3));
+                p[m] = __fmul_rn(__fadd_rn(v.x, e), X[m].x);
+                p[m + 16] = __fmul_rn(__fadd_rn(v.y, e), X[m].y);
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                P[i] = f2(__fadd_rn(p[2 * i], p[2 * i + 1]), __fadd_rn(p[16 + 2 * i], p[17 + 2 * i]));
+        }
 #pragma unroll
         for (int i = 0; i < 4; ++i) P[i] = add2(P[2 * i], P[2 * i + 1]);
 #pragma unroll
