@@ -80,7 +80,7 @@ def library(build_if_missing: bool = True) -> ctypes.CDLL:
             lib.abg_stage_graph_launches.argtypes = [P, ctypes.POINTER(I64)]
             lib.abg_stage_graph_destroy.argtypes = [P]
             lib.abg_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32), I]
-            lib.abg_set_q4mv_tuning.argtypes = [I, I, I]
+            lib.abg_set_q4mv_tuning.argtypes = [I, I, I, I]
             lib.abg_status_str.argtypes = [I]
             lib.abg_status_str.restype = ctypes.c_char_p
             lib.abg_last_cuda_error.argtypes = []
@@ -244,5 +244,5 @@ def device_status(clear: bool = True) -> int:
     return bits.value
 
 
-def set_q4mv_tuning(smem_kb: int = 0, consumer_warps: int = 0, blocks_per_sm: int = 0):
-    _check(library().abg_set_q4mv_tuning(smem_kb, consumer_warps, blocks_per_sm), "abg_set_q4mv_tuning")
+def set_q4mv_tuning(smem_kb: int = 0, consumer_warps: int = 0, blocks_per_sm: int = 0, stage_kb: int = 0):
+    _check(library().abg_set_q4mv_tuning(smem_kb, consumer_warps, blocks_per_sm, stage_kb), "abg_set_q4mv_tuning")

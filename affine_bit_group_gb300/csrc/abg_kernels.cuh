@@ -36,7 +36,7 @@ struct Q4Args {
     // tiling
     int tile_rows, stages, nw;
     // shared-memory layout (byte offsets)
-    uint32_t off_xs, off_red, off_stage, stage_w_bytes, stage_sb_bytes, stage_bytes, off_part, off_bar;
+    uint32_t off_stage, stage_w_bytes, stage_sb_bytes, stage_bytes, off_part, off_bar;
     uint32_t smem_bytes;
 };
 
@@ -44,6 +44,7 @@ struct Q4Tuning {
     int smem_kb = 0;
     int consumer_warps = 0;
     int blocks_per_sm = 0;
+    int stage_kb = 0;
 };
 
 struct Q4Plan {

@@ -438,13 +438,14 @@ abg_status abg_device_status(uint32_t *bits, int clear) {
     return (v & 1u) ? ABG_ETIMEOUT : ABG_OK;  // bit 0: a bounded wait timed out
 }
 
-abg_status abg_set_q4mv_tuning(int smem_kb, int consumer_warps, int blocks_per_sm) {
-    if (smem_kb < 0 || smem_kb > 227 || consumer_warps < 0 || consumer_warps > 12 || blocks_per_sm < 0 ||
-        blocks_per_sm > 4)
+abg_status abg_set_q4mv_tuning(int smem_kb, int consumer_warps, int blocks_per_sm, int stage_kb) {
+    if (smem_kb < 0 || smem_kb > 227 || consumer_warps < 0 || consumer_warps > 8 || blocks_per_sm < 0 ||
+        blocks_per_sm > 4 || stage_kb < 0 || stage_kb > 200)
         return ABG_EINVAL;
     g_tuning.smem_kb = smem_kb;
     g_tuning.consumer_warps = consumer_warps;
     g_tuning.blocks_per_sm = blocks_per_sm;
+    g_tuning.stage_kb = stage_kb;
     return ABG_OK;
 }
 

@@ -52,174 +52,232 @@ namespace {
 
 __device__ __forceinline__ float2 f2(float a, float b) { return make_float2(a, b); }
 
-// Exponent bits of 2^(23-4k), k = 0..3: the float 2^(23-4k) + q sits in the
-// low 23 bits when q occupies bits 4k..4k+3.
-__device__ __forceinline__ uint32_t magic_bits(int k) { return static_cast<uint32_t>(150 - 4 * k) << 23; }
+// Nibble j (0..7) of a word is read at bit position 4k of the word itself
+// (j <= 4, k = j) or of the word shifted right by 12 (j >= 5, k = j - 3), so
+// it always sits inside the 23 significand bits.
+__host__ __device__ constexpr int nib_k(int j) { return j <= 4 ? j : j - 3; }
 
-// The pair of magic floats for nibble j (0..7) of words a and b.
-__device__ __forceinline__ float2 nib2(uint32_t a_lo, uint32_t a_hi, uint32_t b_lo, uint32_t b_hi, int j) {
-    const int k = j & 3;
-    const uint32_t mask = 0xFu << (4 * k);
-    const uint32_t a = (j < 4) ? a_lo : a_hi;
-    const uint32_t b = (j < 4) ? b_lo : b_hi;
-    return f2(__uint_as_float((a & mask) | magic_bits(k)), __uint_as_float((b & mask) | magic_bits(k)));
+// The pair of floats -(1 + q * 2^(4k-23)) for nibble j of words a and b
+// (sign and exponent of -1.0 OR-ed onto the masked nibble).
+__device__ __forceinline__ float2 neg_u2(uint32_t a, uint32_t ah, uint32_t b, uint32_t bh, int j) {
+    const uint32_t mask = 0xFu << (4 * nib_k(j));
+    const uint32_t sa = (j <= 4) ? a : ah, sb = (j <= 4) ? b : bh;
+    return f2(__uint_as_float((sa & mask) | 0xBF800000u), __uint_as_float((sb & mask) | 0xBF800000u));
 }
 
-// Sum over the lane's 32 columns of one row chunk.
-//   X[m] = {x(m), x(m+16)}, Cc[m] = {c(m), c(m+16)} for lane-local columns m.
-//   kExact: the fused-multiply-add identity (x is ordinary); else convert and multiply.
-//   kTree: pairwise tree in column order; else FMA accumulation (fast mode).
-template <bool kTree, bool kExact>
-__device__ __forceinline__ float lane_sum32(uint4 wq, const float2 (&X)[16], const float2 (&Cc)[16]) {
+// q of nibble j as a float, exactly: (2^(23-4k) + q) - 2^(23-4k).
+__device__ __forceinline__ float q_exact(uint32_t w, uint32_t wh, int j) {
+    const int k = nib_k(j);
+    const uint32_t src = (j <= 4) ? w : wh;
+    const float v = __uint_as_float((src & (0xFu << (4 * k))) | (static_cast<uint32_t>(150 - 4 * k) << 23));
+    return __fadd_rn(v, -__uint_as_float(static_cast<uint32_t>(150 - 4 * k) << 23));
+}
+
+// 2^(23-4k) for nibble j: the factor that turns q * 2^(4k-23) back into q.
+__device__ __forceinline__ float nib_scale(int j) {
+    return __uint_as_float(static_cast<uint32_t>(150 - 4 * nib_k(j)) << 23);
+}
+
+// Pairwise tree over the lane's 32 products, given as P[m] = {p_m, p_(m+16)}:
+// adding P[2i] and P[2i+1] pairs leaves (2i, 2i+1) in both halves, and the
+// halves stay aligned level after level.
+__device__ __forceinline__ float tree32_pairs(float2 (&P)[16]) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) P[i] = add2(P[2 * i], P[2 * i + 1]);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) P[i] = add2(P[2 * i], P[2 * i + 1]);
+#pragma unroll
+    for (int i = 0; i < 2; ++i) P[i] = add2(P[2 * i], P[2 * i + 1]);
+    P[0] = add2(P[0], P[1]);
+    return __fadd_rn(P[0].x, P[0].y);
+}
+
+// Tree sum of q*x over the lane's 32 columns of one row chunk (words wq).
+//   exact path: X[m] = {-x(m) S_m, -x(m+16) S_m} with S_m = 2^(23-4k); the
+//     product fma(-(1 + q 2^(4k-23)), -x S, -x S) = q x exactly before its one
+//     rounding, so it is RN(q*x), at one logic op and half a packed FMA per
+//     weight.
+//   plain path (activations with zeros of either sign, infinities, NaN, huge
+//     values, or a group of all-negative values): X[m] = {x(m), x(m+16)}; q is
+//     converted exactly and multiplied with scalar RN ops.  (The compiler may
+//     fuse a packed multiply into the packed add after it; the scalar
+//     __fmul_rn / __fadd_rn intrinsics are never contracted.)
+template <bool kExact>
+__device__ __forceinline__ float lane_sum32(uint4 wq, const float2 (&X)[16]) {
     const uint32_t w0 = wq.x, w1 = wq.y, w2 = wq.z, w3 = wq.w;
-    const uint32_t h0 = w0 >> 16, h1 = w1 >> 16, h2 = w2 >> 16, h3 = w3 >> 16;
-    if (kTree) {
-        float2 P[16];
-        if (kExact) {
-#pragma unroll
-            for (int m = 0; m < 16; ++m) {
-                const float2 v = (m < 8) ? nib2(w0, h0, w2, h2, m & 7) : nib2(w1, h1, w3, h3, m & 7);
-                P[m] = fma2(v, X[m], Cc[m]);
-            }
-            // P[m] = {p_m, p_(m+16)}: adding P[2i] and P[2i+1] pairs leaves (2i, 2i+1)
-            // in both halves; the halves stay aligned level after level.
-#pragma unroll
-            for (int i = 0; i < 8; ++i) P[i] = add2(P[2 * i], P[2 * i + 1]);
-        } else {
-            // Plain path: q converted exactly, products and the first tree level
-            // as scalar RN operations.  (The compiler may fuse a packed multiply
-            // or a packed fma with a -0 addend into the packed add after it; the
-            // scalar __fmul_rn / __fadd_rn intrinsics are never contracted.)
-            float p[32];
-#pragma unroll
-            for (int m = 0; m < 16; ++m) {
-                const float2 v = (m < 8) ? nib2(w0, h0, w2, h2, m & 7) : nib2(w1, h1, w3, h3, m & 7);
-                const float e = -__uint_as_float(magic_bits(m & 3));
-                p[m] = __fmul_rn(__fadd_rn(v.x, e), X[m].x);
-                p[m + 16] = __fmul_rn(__fadd_rn(v.y, e), X[m].y);
-            }
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-                P[i] = f2(__fadd_rn(p[2 * i], p[2 * i + 1]), __fadd_rn(p[16 + 2 * i], p[17 + 2 * i]));
-        }
-#pragma unroll
-        for (int i = 0; i < 4; ++i) P[i] = add2(P[2 * i], P[2 * i + 1]);
-#pragma unroll
-        for (int i = 0; i < 2; ++i) P[i] = add2(P[2 * i], P[2 * i + 1]);
-        P[0] = add2(P[0], P[1]);
-        return __fadd_rn(P[0].x, P[0].y);
-    } else {
-        float2 acc[4] = {f2(0.f, 0.f), f2(0.f, 0.f), f2(0.f, 0.f), f2(0.f, 0.f)};
+    const uint32_t h0 = w0 >> 12, h1 = w1 >> 12, h2 = w2 >> 12, h3 = w3 >> 12;
+    float2 P[16];
+    if constexpr (kExact) {
 #pragma unroll
         for (int m = 0; m < 16; ++m) {
-            const float2 v = (m < 8) ? nib2(w0, h0, w2, h2, m & 7) : nib2(w1, h1, w3, h3, m & 7);
-            const float e = -__uint_as_float(magic_bits(m & 3));
-            acc[m & 3] = fma2(add2(v, f2(e, e)), X[m], acc[m & 3]);
+            const float2 u = (m < 8) ? neg_u2(w0, h0, w2, h2, m & 7) : neg_u2(w1, h1, w3, h3, m & 7);
+            P[m] = fma2(u, X[m], X[m]);
         }
-        const float2 s = add2(add2(acc[0], acc[1]), add2(acc[2], acc[3]));
-        return s.x + s.y;
+        return tree32_pairs(P);
+    } else {
+    float p[32];
+#pragma unroll
+    for (int m = 0; m < 16; ++m) {
+        const int j = m & 7;
+        const float qa = (m < 8) ? q_exact(w0, h0, j) : q_exact(w1, h1, j);
+        const float qb = (m < 8) ? q_exact(w2, h2, j) : q_exact(w3, h3, j);
+        p[m] = __fmul_rn(qa, X[m].x);
+        p[m + 16] = __fmul_rn(qb, X[m].y);
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        P[i] = f2(__fadd_rn(p[2 * i], p[2 * i + 1]), __fadd_rn(p[16 + 2 * i], p[17 + 2 * i]));
+#pragma unroll
+    for (int i = 0; i < 4; ++i) P[i] = add2(P[2 * i], P[2 * i + 1]);
+#pragma unroll
+    for (int i = 0; i < 2; ++i) P[i] = add2(P[2 * i], P[2 * i + 1]);
+    P[0] = add2(P[0], P[1]);
+    return __fadd_rn(P[0].x, P[0].y);
     }
 }
 
-// Location of column `col` in the staged activation: chunk ch = col/1024, lane
-// L = (col/32)%32, lane-local m = col%32.  Quad i (0..7) of (ch, L) holds
-// {x(2i), x(2i+16), x(2i+1), x(2i+17)} so one 16-byte load gives X[2i], X[2i+1]
-// and consecutive lanes read consecutive 16-byte words.
-__device__ __forceinline__ int xc_index(int col) {
-    const int ch = col >> 10, L = (col >> 5) & 31, m = col & 31;
-    const int half = m >> 4, mm = m & 15;
-    const int quad = ((ch * 8 + (mm >> 1)) * 32 + L);
-    return quad * 4 + (((mm & 1) << 1) | half);
+// True when the exact path gives RN(q*x) for this activation value (finite,
+// not a zero of either sign... +0 is fine for the identity but a zero is
+// cheap to route to the plain path, and |x| < 2^100 so x * 2^23 cannot overflow).
+__device__ __forceinline__ bool x_ordinary(float v) { return fabsf(v) < 1.2676506e30f && v != 0.0f; }
+
+// Pairwise tree over 32 values in index order (scalar RN adds).
+__device__ __forceinline__ float tree32(const float (&v)[32]) {
+    float t[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) t[i] = __fadd_rn(v[2 * i], v[2 * i + 1]);
+#pragma unroll
+    for (int h = 8; h >= 1; h >>= 1)
+#pragma unroll
+        for (int i = 0; i < h; ++i) t[i] = __fadd_rn(t[2 * i], t[2 * i + 1]);
+    return t[0];
 }
 
-// True when the fused-multiply-add identity gives RN(q*x) for this x.
-__device__ __forceinline__ bool x_ordinary(float v) {
-    const uint32_t b = __float_as_uint(v);
-    return fabsf(v) < 1.2676506e30f /* 2^100 */ && b != 0x80000000u;
+// 1/sqrt(ss/n + eps) for the RMS norm: ss = tree over groups of the tree over
+// the group of x*x.  Computed by one warp on its own (every warp of the block
+// gets the same bits).  Lane l sums the squares of groups l, l+32, ...; a
+// butterfly sums each block of 32 groups; the blocks' sums (at most 8, padded
+// with -0) meet in a fixed pairwise tree.
+template <bool kTree>
+__device__ float warp_rms_factor(const float *__restrict__ x, int C, float eps, int lane) {
+    const int G = C / 64, nblk = (G + 31) / 32;
+    float blk[8];
+#pragma unroll
+    for (int b = 0; b < 8; ++b) {
+        blk[b] = kNegZero;
+        if (b < nblk) {
+            const int g = 32 * b + lane;
+            float s = kNegZero;
+            if (g < G) {
+                float v[32], t[32];
+                const float4 *p4 = reinterpret_cast<const float4 *>(x + 64 * g);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const float4 q = p4[8 * h + i];
+                        v[4 * i] = __fmul_rn(q.x, q.x);
+                        v[4 * i + 1] = __fmul_rn(q.y, q.y);
+                        v[4 * i + 2] = __fmul_rn(q.z, q.z);
+                        v[4 * i + 3] = __fmul_rn(q.w, q.w);
+                    }
+                    t[h] = tree32(v);
+                }
+                s = __fadd_rn(t[0], t[1]);
+            }
+            blk[b] = warp_tree<32>(s);
+        }
+    }
+#pragma unroll
+    for (int h = 4; h >= 1; h >>= 1)
+#pragma unroll
+        for (int i = 0; i < h; ++i) blk[i] = __fadd_rn(blk[2 * i], blk[2 * i + 1]);
+    const float ss = blk[0];
+    if (kTree) {
+        const float mean = __fdiv_rn(ss, static_cast<float>(C));
+        return __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(mean, eps)));
+    }
+    return rsqrtf(ss / static_cast<float>(C) + eps);
 }
 
-struct Staging {
-    float *xc;   // activation quads
-    float *xs;   // group sums [G]
-    float *red;  // reduction scratch [next_pow2(G)]
-    int *flags;  // [0] = some x is not ordinary, [1] = rms factor bits
+// One warp's slice of the activation: columns ch*1024 + lane*32 + (0..31).
+struct Slice {
+    float2 X[16];  // see lane_sum32
+    float xs;      // group sum of the lane's 64-column group
+    bool exact;    // warp-uniform: the exact path applies to the whole slice
 };
 
-// Emits the activation pair (v0, v1) at columns (col, col+1) and returns its
-// contribution to the special-value flag.
-__device__ __forceinline__ int emit_x(const Staging &st, int col, float v0, float v1) {
-    st.xc[xc_index(col)] = v0;
-    st.xc[xc_index(col + 1)] = v1;
-    return (x_ordinary(v0) && x_ordinary(v1)) ? 0 : 1;
-}
-
-// Stages (or computes) the activation for a product block.  Runs on the
-// consumer threads only (ct = consumer thread index, nct threads, ncw warps);
-// ends with those threads synchronized on named barrier 1.
 template <bool kTree>
-__device__ void stage_activation(const Q4Args &a, const Staging &st, int ct, int nct) {
-    const int cw = ct >> 5, lane = ct & 31, ncw = nct >> 5;
-    const int C = a.cols, G = a.G;
-    int special = 0;
-    if (ct == 0) st.flags[0] = 0;
-    named_bar(1, nct);
-    if (a.prologue == kProNone) {
-        for (int p = ct; p < C / 2; p += nct) {
-            const float2 v = reinterpret_cast<const float2 *>(a.x)[p];
-            special |= emit_x(st, 2 * p, v.x, v.y);
-        }
-        for (int g = ct; g < G; g += nct) st.xs[g] = a.xsum[g];
-    } else if (a.prologue == kProGsum || a.prologue == kProSwq) {
-        for (int g = cw; g < G; g += ncw) {
-            const int col = 64 * g + 2 * lane;
-            float v0, v1;
-            if (a.prologue == kProGsum) {
-                const float2 v = reinterpret_cast<const float2 *>(a.x)[col / 2];
-                v0 = v.x, v1 = v.y;
-            } else {
-                const float2 gg = reinterpret_cast<const float2 *>(a.x)[col / 2];
-                const float2 uu = reinterpret_cast<const float2 *>(a.x + C)[col / 2];
-                v0 = swiglu<kTree>(gg.x, uu.x);
-                v1 = swiglu<kTree>(gg.y, uu.y);
+__device__ __forceinline__ void load_slice(const Q4Args &a, int ch, int lane, float rms_r, Slice &sl) {
+    const int C = a.cols, base = ch * 1024 + lane * 32;
+    const bool active = base < C;
+    float v[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = 0.f;
+    if (active) {
+        const float4 *x4 = reinterpret_cast<const float4 *>(a.x + base);
+        if (a.prologue == kProNone || a.prologue == kProGsum) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float4 q = x4[i];
+                v[4 * i] = q.x, v[4 * i + 1] = q.y, v[4 * i + 2] = q.z, v[4 * i + 3] = q.w;
             }
-            special |= emit_x(st, col, v0, v1);
-            const float s = warp_tree<32>(kTree ? __fadd_rn(v0, v1) : v0 + v1);
-            if (lane == 0) st.xs[g] = s;
-        }
-    } else {  // kProRmsq
-        for (int g = cw; g < G; g += ncw) {
-            const float2 v = reinterpret_cast<const float2 *>(a.x)[32 * g + lane];
-            const float s = warp_tree<32>(__fadd_rn(__fmul_rn(v.x, v.x), __fmul_rn(v.y, v.y)));
-            if (lane == 0) st.red[g] = s;
-        }
-        named_bar(1, nct);
-        if (cw == 0) {
-            const float ss = warp_tree_smem(st.red, G);
-            if (lane == 0) {
-                float r;
-                if (kTree) {
-                    const float mean = __fdiv_rn(ss, static_cast<float>(C));
-                    r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(mean, a.eps)));
-                } else {
-                    r = rsqrtf(ss / static_cast<float>(C) + a.eps);
-                }
-                st.flags[1] = __float_as_int(r);
+        } else if (a.prologue == kProRmsq) {
+            const float4 *w4 = reinterpret_cast<const float4 *>(a.wt + base);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float4 q = x4[i], w = w4[i];
+                v[4 * i] = __fmul_rn(__fmul_rn(q.x, rms_r), w.x);
+                v[4 * i + 1] = __fmul_rn(__fmul_rn(q.y, rms_r), w.y);
+                v[4 * i + 2] = __fmul_rn(__fmul_rn(q.z, rms_r), w.z);
+                v[4 * i + 3] = __fmul_rn(__fmul_rn(q.w, rms_r), w.w);
             }
-        }
-        named_bar(1, nct);
-        const float r = __int_as_float(st.flags[1]);
-        for (int g = cw; g < G; g += ncw) {
-            const float2 v = reinterpret_cast<const float2 *>(a.x)[32 * g + lane];
-            const float2 wt = reinterpret_cast<const float2 *>(a.wt)[32 * g + lane];
-            const float v0 = __fmul_rn(__fmul_rn(v.x, r), wt.x);
-            const float v1 = __fmul_rn(__fmul_rn(v.y, r), wt.y);
-            special |= emit_x(st, 64 * g + 2 * lane, v0, v1);
-            const float s = warp_tree<32>(kTree ? __fadd_rn(v0, v1) : v0 + v1);
-            if (lane == 0) st.xs[g] = s;
+        } else {  // kProSwq: x = [gate | up]
+            const float4 *u4 = reinterpret_cast<const float4 *>(a.x + C + base);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float4 g = x4[i], u = u4[i];
+                v[4 * i] = swiglu<kTree>(g.x, u.x);
+                v[4 * i + 1] = swiglu<kTree>(g.y, u.y);
+                v[4 * i + 2] = swiglu<kTree>(g.z, u.z);
+                v[4 * i + 3] = swiglu<kTree>(g.w, u.w);
+            }
         }
     }
-    if (special) atomicOr(st.flags, 1);
-    named_bar(1, nct);
+    // special values, and groups whose 64 values are all negative (there the
+    // exact path's q = 0 products would be +0 where RN(0 * x) is -0, and a
+    // whole group of them could leave -0 in the sum)
+    bool sp = false, allneg = true;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        sp |= !x_ordinary(v[i]);
+        allneg &= v[i] < 0.f;
+    }
+    if (!active) sp = false, allneg = false;
+    const bool grpneg = allneg && __shfl_xor_sync(0xffffffffu, allneg, 1);
+    sl.exact = !__any_sync(0xffffffffu, sp || grpneg);
+    // group sum of the lane's group: given, or the tree over the slice's values
+    if (a.prologue == kProNone) {
+        sl.xs = active ? a.xsum[ch * 16 + (lane >> 1)] : 0.f;
+    } else {
+        const float t = kTree ? tree32(v) : [&] {
+            float s = 0.f;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) s += v[i];
+            return s;
+        }();
+        const float o = __shfl_xor_sync(0xffffffffu, t, 1);
+        sl.xs = kTree ? __fadd_rn(t, o) : t + o;
+    }
+#pragma unroll
+    for (int m = 0; m < 16; ++m) {
+        if (sl.exact) {
+            const float s = -nib_scale(m & 7);
+            sl.X[m] = f2(__fmul_rn(v[m], s), __fmul_rn(v[m + 16], s));
+        } else {
+            sl.X[m] = f2(v[m], v[m + 16]);
+        }
+    }
 }
 
 // Locates tile t of a grouped launch.
@@ -250,24 +308,65 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, vo
     }
 }
 
+// One step of a transposed butterfly over N values (N -> N/2): lanes whose
+// `d` bit is clear keep the first half and send the second, their partners
+// the other way round, so each lane adds N/2 pairs with N/2 shuffles.  The
+// sums pair the same two leaves as a plain butterfly step.
+template <int N, bool kTree>
+__device__ __forceinline__ void tstep(float (&v)[N], int d, bool hi) {
+#pragma unroll
+    for (int i = 0; i < N / 2; ++i) {
+        const float send = hi ? v[i] : v[N / 2 + i];
+        const float keep = hi ? v[N / 2 + i] : v[i];
+        const float recv = __shfl_xor_sync(0xffffffffu, send, d);
+        v[i] = kTree ? __fadd_rn(keep, recv) : keep + recv;
+    }
+}
+
+// Butterfly levels from distance `dist` up to 16 over N held values: while
+// N > 1 each level is a transposed step (the lane keeps the half selected by
+// its `dist` bit, recorded in rowsel); then plain butterfly steps.
+template <int N, bool kTree>
+__device__ __forceinline__ float group_levels(float (&v)[N], int lane, int dist, int &rowsel) {
+    if constexpr (N == 1) {
+        float val = v[0];
+        for (int dd = dist; dd < 32; dd <<= 1) {
+            const float o = __shfl_xor_sync(0xffffffffu, val, dd);
+            val = kTree ? __fadd_rn(val, o) : val + o;
+        }
+        return val;
+    } else {
+        const bool hi = (lane & dist) != 0;
+        tstep<N, kTree>(v, dist, hi);
+        rowsel += hi ? N / 2 : 0;
+        float w[N / 2];
+#pragma unroll
+        for (int i = 0; i < N / 2; ++i) w[i] = v[i];
+        return group_levels<N / 2, kTree>(w, lane, dist * 2, rowsel);
+    }
+}
+
+// Partial-sum buffers (and their barriers) rotate over 4 tiles: a warp writes
+// a tile's buffer only after every warp has finished the final sums of the
+// tile four back.
+constexpr int kParts = 4;
+
 template <int R, bool kTree, bool kSbSmem>
-__global__ void __launch_bounds__(416, 1) q4mv_kernel(const __grid_constant__ Q4Args a) {
+__global__ void __launch_bounds__(288, 2) q4mv_kernel(const __grid_constant__ Q4Args a) {
     extern __shared__ __align__(128) unsigned char smem[];
-    __shared__ int s_flags[2];
     __shared__ volatile int s_abort;
-    float4 *xc4 = reinterpret_cast<float4 *>(smem);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + a.off_bar);
     uint64_t *empty = full + a.stages;
     uint64_t *done = empty + a.stages;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int S = a.stages, TR = a.tile_rows, W = a.W, G = a.G, nch = a.nch;
+    const int S = a.stages, TR = a.tile_rows, W = a.W, G = a.G, nch = a.nch, nw = a.nw;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], a.nw);
-            mbar_init(&done[s], a.nw);
+            mbar_init(&empty[s], nw);
         }
+        for (int i = 0; i < kParts; ++i) mbar_init(&done[i], nw);
         s_abort = 0;
         fence_mbar_init();
     }
@@ -297,113 +396,39 @@ __global__ void __launch_bounds__(416, 1) q4mv_kernel(const __grid_constant__ Q4
                 bulk_g2s(st + a.stage_w_bytes + a.stage_sb_bytes, P.bias + r0 * G, sbb, &full[s], policy);
             }
         }
-        // Drain: the CTA may not exit while a copy into its shared memory is in
-        // flight.  Waiting on a phase that already completed returns at once.
+        // Drain: the block may not exit while a copy into its shared memory is
+        // in flight.  Waiting on a phase that already completed returns at once.
         for (int64_t j = max(static_cast<int64_t>(0), k - S); j < k; ++j)
             mbar_wait(&full[j % S], static_cast<uint32_t>((j / S) & 1));
         return;
     }
 
     // ---------------------------------------------------- consumer warps ----
-    const int ct = threadIdx.x - 32, nct = a.nw * 32, cw = warp - 1;
-    grid_dep_wait();
-    Staging st;
-    st.xc = reinterpret_cast<float *>(smem);
-    st.xs = reinterpret_cast<float *>(smem + a.off_xs);
-    st.red = reinterpret_cast<float *>(smem + a.off_red);
-    st.flags = s_flags;
-    stage_activation<kTree>(a, st, ct, nct);
-    const bool exact = (s_flags[0] == 0);
-    const float *xs = st.xs;
+    const int ct = threadIdx.x - 32, cw = warp - 1;
     float *part = reinterpret_cast<float *>(smem + a.off_part);
+    // chunk positions and row blocks of this warp
+    const bool fixed_ch = nch <= nw;
+    const int kk = fixed_ch ? nw / nch : 1;
+    const bool idle = fixed_ch && cw >= nch * kk;
+    const int ch0 = fixed_ch ? cw % nch : cw;
+    const int rb0 = fixed_ch ? cw / nch : 0;
+    const int chstep = fixed_ch ? nch : nw;
 
-    float2 X[16], Cc[16];
-    float xsg = 0.f;
+    grid_dep_wait();
+    float rms_r = 0.f;
+    if (a.prologue == kProRmsq) rms_r = warp_rms_factor<kTree>(a.x, a.cols, a.eps, lane);
+    Slice sl;
     int cur_ch = -1;
-    int64_t k = 0;
-    for (int64_t t = blockIdx.x; t < a.total_tiles; t += gridDim.x, ++k) {
-        const int s = static_cast<int>(k % S);
-        const uint32_t ph = static_cast<uint32_t>((k / S) & 1);
-        if (!wait_or_abort(&full[s], ph, &s_abort)) return;
+    // Final sums of tile j: thread ct adds row ct's chunk partials by the tree.
+    auto finish = [&](int64_t j, int64_t tj) -> bool {
+        const int pi = static_cast<int>(j % kParts);
+        if (!wait_or_abort(&done[pi], static_cast<uint32_t>((j / kParts) & 1), &s_abort)) return false;
         int64_t tile;
-        const Q4Prob &P = a.prob[find_prob(a, t, tile)];
+        const Q4Prob &P = a.prob[find_prob(a, tj, tile)];
         const int64_t r0 = tile * TR;
         const int rows = static_cast<int>(min(static_cast<int64_t>(TR), P.n - r0));
-        const unsigned char *stg = smem + a.off_stage + static_cast<size_t>(s) * a.stage_bytes;
-        const uint4 *sw = reinterpret_cast<const uint4 *>(stg);
-        const float *ssc = reinterpret_cast<const float *>(stg + a.stage_w_bytes);
-        const float *sbi = reinterpret_cast<const float *>(stg + a.stage_w_bytes + a.stage_sb_bytes);
-        float *prt = part + static_cast<size_t>(s) * TR * nch;
-        const int nrb = (rows + R - 1) / R;
-        const int items = nrb * nch;
-        for (int item = cw; item < items; item += a.nw) {
-            const int ch = item % nch, rb = item / nch;
-            const bool active = (ch * 1024 + lane * 32) < a.cols;
-            const int g = ch * 16 + (lane >> 1);
-            if (ch != cur_ch) {
-                cur_ch = ch;
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const float4 q = xc4[(ch * 8 + i) * 32 + lane];
-                    X[2 * i] = f2(q.x, q.y);
-                    X[2 * i + 1] = f2(q.z, q.w);
-                }
-#pragma unroll
-                for (int m = 0; m < 16; ++m) {
-                    const float e = -__uint_as_float(magic_bits(m & 3));
-                    Cc[m] = f2(__fmul_rn(X[m].x, e), __fmul_rn(X[m].y, e));
-                }
-                xsg = active ? xs[g] : 0.f;
-            }
-            // Lanes past the end of the row (last chunk only) come in whole
-            // groups (lane pairs); they contribute -0 to the group butterfly.
-            float tv[R];
-#pragma unroll
-            for (int r = 0; r < R; ++r) {
-                const int row = rb * R + r;  // uniform across the warp
-                tv[r] = kNegZero;
-                if (row < rows) {
-                    float part32 = 0.f, sc = 0.f, bi = 0.f;
-                    if (active) {
-                        const uint4 wq = sw[static_cast<size_t>(row) * (W / 4) + ch * 32 + lane];
-                        part32 = exact ? lane_sum32<kTree, true>(wq, X, Cc) : lane_sum32<kTree, false>(wq, X, Cc);
-                        if (kSbSmem) {
-                            sc = ssc[row * G + g];
-                            bi = sbi[row * G + g];
-                        } else {
-                            sc = __ldg(P.scale + (r0 + row) * G + g);
-                            bi = __ldg(P.bias + (r0 + row) * G + g);
-                        }
-                    }
-                    const float o = __shfl_xor_sync(0xffffffffu, part32, 1);
-                    if (active) {
-                        if (kTree) {
-                            const float d = __fadd_rn(part32, o);
-                            tv[r] = __fadd_rn(__fmul_rn(sc, d), __fmul_rn(bi, xsg));
-                        } else {
-                            tv[r] = fmaf(sc, part32 + o, bi * xsg);
-                        }
-                    }
-                }
-            }
-#pragma unroll
-            for (int r = 0; r < R; ++r) {
-                float v = tv[r];
-#pragma unroll
-                for (int d = 2; d < 32; d <<= 1) {
-                    const float o = __shfl_xor_sync(0xffffffffu, v, d);
-                    v = kTree ? __fadd_rn(v, o) : v + o;
-                }
-                const int row = rb * R + r;
-                if (lane == 0 && row < rows) prt[row * nch + ch] = v;
-            }
-        }
-        // all chunk partials of the tile are in shared memory
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&done[s]);
-        if (!wait_or_abort(&done[s], ph, &s_abort)) return;
         if (ct < rows) {
-            float *pr = prt + ct * nch;
+            float *pr = part + (static_cast<size_t>(pi) * TR + ct) * nch;
             int m = nch;
             while (m > 1) {
                 const int h = m >> 1;
@@ -413,9 +438,96 @@ __global__ void __launch_bounds__(416, 1) q4mv_kernel(const __grid_constant__ Q4
             }
             P.y[r0 + ct] = pr[0];
         }
+        return true;
+    };
+
+    int64_t k = 0, tprev = -1;
+    for (int64_t t = blockIdx.x; t < a.total_tiles; t += gridDim.x, ++k) {
+        const int s = static_cast<int>(k % S);
+        if (!wait_or_abort(&full[s], static_cast<uint32_t>((k / S) & 1), &s_abort)) return;
+        int64_t tile;
+        const Q4Prob &P = a.prob[find_prob(a, t, tile)];
+        const int64_t r0 = tile * TR;
+        const int rows = static_cast<int>(min(static_cast<int64_t>(TR), P.n - r0));
+        const unsigned char *stg = smem + a.off_stage + static_cast<size_t>(s) * a.stage_bytes;
+        const uint4 *sw = reinterpret_cast<const uint4 *>(stg);
+        const float *ssc = reinterpret_cast<const float *>(stg + a.stage_w_bytes);
+        const float *sbi = reinterpret_cast<const float *>(stg + a.stage_w_bytes + a.stage_sb_bytes);
+        float *prt = part + static_cast<size_t>(k % kParts) * TR * nch;
+        const int nrb = (rows + R - 1) / R;
+        if (!idle) {
+            for (int ch = ch0; ch < nch; ch += chstep) {
+                if (ch != cur_ch) {
+                    load_slice<kTree>(a, ch, lane, rms_r, sl);
+                    cur_ch = ch;
+                }
+                const bool active = (ch * 1024 + lane * 32) < a.cols;
+                const int g = ch * 16 + (lane >> 1);
+                for (int rb = rb0; rb < nrb; rb += kk) {
+                    // lane sums of R rows
+                    float v[R];
+#pragma unroll
+                    for (int r = 0; r < R; ++r) {
+                        const int row = rb * R + r;  // uniform across the warp
+                        v[r] = 0.f;
+                        if (row < rows && active) {
+                            const uint4 wq = sw[static_cast<size_t>(row) * (W / 4) + ch * 32 + lane];
+                            v[r] = sl.exact ? lane_sum32<true>(wq, sl.X) : lane_sum32<false>(wq, sl.X);
+                        }
+                    }
+                    // group completion (lane pair), transposed when R > 1: this
+                    // lane keeps rows [ofs, ofs + R/2)
+                    constexpr int H = (R > 1) ? R / 2 : 1;
+                    int ofs = 0;
+                    float d[H];
+                    if constexpr (R > 1) {
+                        const bool hi = lane & 1;
+                        tstep<R, kTree>(v, 1, hi);
+                        ofs = hi ? R / 2 : 0;
+#pragma unroll
+                        for (int i = 0; i < H; ++i) d[i] = v[i];
+                    } else {
+                        const float o = __shfl_xor_sync(0xffffffffu, v[0], 1);
+                        d[0] = kTree ? __fadd_rn(v[0], o) : v[0] + o;
+                    }
+                    // affine term per (row, group); groups past the row end add -0
+                    float tv[H];
+#pragma unroll
+                    for (int i = 0; i < H; ++i) {
+                        const int row = rb * R + ofs + i;
+                        tv[i] = kNegZero;
+                        if (active && row < rows) {
+                            float sc, bi;
+                            if (kSbSmem) {
+                                sc = ssc[row * G + g];
+                                bi = sbi[row * G + g];
+                            } else {
+                                sc = __ldg(P.scale + (r0 + row) * G + g);
+                                bi = __ldg(P.bias + (r0 + row) * G + g);
+                            }
+                            tv[i] = kTree ? __fadd_rn(__fmul_rn(sc, d[i]), __fmul_rn(bi, sl.xs))
+                                          : fmaf(sc, d[i], bi * sl.xs);
+                        }
+                    }
+                    // the chunk's 16 groups: butterfly over lane pairs (distances
+                    // 2..16), transposed while more than one row is held
+                    int rowsel = ofs;
+                    const float val = group_levels<H, kTree>(tv, lane, 2, rowsel);
+                    // lanes 0..R-1 hold the R rows (row rb*R + rowsel)
+                    const int row = rb * R + rowsel;
+                    if (lane < R && row < rows) prt[row * nch + ch] = val;
+                }
+            }
+        }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[s]);
+        if (lane == 0) {
+            mbar_arrive(&empty[s]);       // weights of this stage no longer needed
+            mbar_arrive(&done[k % kParts]);  // this warp's partials are written
+        }
+        if (tprev >= 0 && !finish(k - 1, tprev)) return;
+        tprev = t;
     }
+    if (tprev >= 0) finish(k - 1, tprev);
 }
 
 template <int R, bool kTree, bool kSb>
@@ -473,23 +585,20 @@ bool plan_once(Q4Plan *plan, const Q4Prob *probs, int nprob, int cols, int prolo
     a = Q4Args{};
     const int R = rows_per_warp;
     const int C = cols, W = C / 8, G = C / 64, nch = (C + 1023) / 1024;
+    // consumer warps: a multiple of the chunk count (each warp keeps one
+    // 1024-column slice of x), at most 8 (the kernel's launch bound)
     int nw = tune.consumer_warps;
-    if (nw <= 0) nw = nch <= 8 ? std::min(12, nch * ((8 + nch - 1) / nch)) : 8;
-    nw = std::min(std::max(nw, 1), 12);
-    const int kk = (nw % nch == 0) ? nw / nch : 1;  // warps per chunk position
+    if (nw <= 0) nw = nch <= 8 ? nch * (8 / nch) : 8;
+    nw = std::min(std::max(nw, 1), 8);
+    const int kk = (nch <= nw) ? nw / nch : 1;  // warps per chunk position
     const uint32_t row_bytes = static_cast<uint32_t>(C / 2 + (sb_smem ? 8 * G : 0));
-    int gp = 1;
-    while (gp < G) gp <<= 1;
-    const uint32_t xc_bytes = static_cast<uint32_t>(nch) * 8u * 32u * 16u;
-    const uint32_t xs_bytes = align_up(static_cast<uint32_t>(G) * 4u, 16);
-    const uint32_t red_bytes = align_up(static_cast<uint32_t>(std::max(gp, 32)) * 4u, 16);
-    const uint32_t fixed = xc_bytes + xs_bytes + red_bytes + 1024;  // + barriers and slack
+    const uint32_t fixed = 1024;  // barriers and alignment slack
     uint32_t budget = static_cast<uint32_t>(tune.smem_kb > 0 ? tune.smem_kb : 110) * 1024u;
-    const uint32_t hard_max = 227u * 1024u;
-    // tile rows: a multiple of R*kk so items spread evenly over the warps
+    const uint32_t hard_max = 227u * 1024u - 64u;
+    // tile rows: a multiple of R*kk so row blocks spread evenly over the warps
     const int unit = R * kk;
     int TR = unit;
-    const uint32_t stage_target = 48u * 1024u;
+    const uint32_t stage_target = static_cast<uint32_t>(tune.stage_kb > 0 ? tune.stage_kb : 40) * 1024u;
     while (TR * 2 <= nw * 32 && (TR * 2) * row_bytes <= stage_target) TR *= 2;
     TR = std::min(TR, nw * 32);
     if (TR < R) return false;
@@ -497,13 +606,13 @@ bool plan_once(Q4Plan *plan, const Q4Prob *probs, int nprob, int cols, int prolo
         return align_up(static_cast<uint32_t>(tr) * (C / 2), 16) +
                2u * align_up(sb_smem ? static_cast<uint32_t>(tr) * G * 4u : 0u, 16);
     };
-    auto part_bytes = [&](int tr, int s) { return align_up(static_cast<uint32_t>(s * tr * nch) * 4u, 16); };
+    auto part_bytes = [&](int tr) { return align_up(static_cast<uint32_t>(kParts * tr * nch) * 4u, 16); };
     int S = 0;
     for (int attempt = 0; attempt < 2; ++attempt) {
         for (;;) {
             const uint32_t sb = stage_bytes(TR);
             S = 0;
-            while (S < 8 && fixed + (S + 1) * sb + part_bytes(TR, S + 1) + 24u * (S + 1) <= budget) ++S;
+            while (S < 8 && fixed + (S + 1) * sb + part_bytes(TR) + 16u * (S + 1) + 8u * kParts <= budget) ++S;
             if (S >= 2 || TR <= unit) break;
             TR = std::max(unit, TR / 2);
         }
@@ -531,15 +640,13 @@ bool plan_once(Q4Plan *plan, const Q4Prob *probs, int nprob, int cols, int prolo
     a.tile_rows = TR;
     a.stages = S;
     a.nw = nw;
-    a.off_xs = xc_bytes;
-    a.off_red = a.off_xs + xs_bytes;
-    a.off_stage = align_up(a.off_red + red_bytes, 128);
+    a.off_stage = 0;
     a.stage_w_bytes = align_up(static_cast<uint32_t>(TR) * (C / 2), 16);
     a.stage_sb_bytes = align_up(sb_smem ? static_cast<uint32_t>(TR) * G * 4u : 0u, 16);
     a.stage_bytes = a.stage_w_bytes + 2 * a.stage_sb_bytes;
     a.off_part = a.off_stage + S * a.stage_bytes;
-    a.off_bar = align_up(a.off_part + part_bytes(TR, S), 16);
-    a.smem_bytes = a.off_bar + 24u * S;
+    a.off_bar = align_up(a.off_part + part_bytes(TR), 16);
+    a.smem_bytes = a.off_bar + 16u * S + 8u * kParts;
 
     // blocks per SM: what fits (registers and shared memory), at most 2 unless tuned
     int fit = 1;

@@ -205,13 +205,18 @@ abg_status abg_stage_graph_destroy(void *graph);
  * Returns ABG_ETIMEOUT when bit 0 was set, else ABG_OK. */
 abg_status abg_device_status(uint32_t *bits, int clear);
 
-/* Tuning of the product kernel, process-wide; 0 keeps the default.
- *   smem_kb          shared-memory budget per thread block (default 100, so
- *                    two blocks fit on an SM and consecutive launches overlap)
- *   consumer_warps   warps that compute (default: chosen from cols)
- *   blocks_per_sm    thread blocks per SM in the grid (default: 1)
+/* Tuning of the product kernel, process-wide; 0 keeps the default.  Applies
+ * to calls and graphs created afterwards.
+ *   smem_kb          shared-memory budget per thread block (default 110, so
+ *                    two blocks fit on an SM and a dependent launch can start
+ *                    while its predecessor still runs)
+ *   consumer_warps   warps that compute, 1..8 (default: chosen from cols)
+ *   blocks_per_sm    thread blocks per SM in the grid, at most what fits
+ *                    (default: 2)
+ *   stage_kb         target size of one pipeline stage of streamed rows
+ *                    (default 40)
  * It never changes results. */
-abg_status abg_set_q4mv_tuning(int smem_kb, int consumer_warps, int blocks_per_sm);
+abg_status abg_set_q4mv_tuning(int smem_kb, int consumer_warps, int blocks_per_sm, int stage_kb);
 
 const char *abg_status_str(int status);
 /* Text of the last CUDA error seen by any call on this thread ("" if none). */
