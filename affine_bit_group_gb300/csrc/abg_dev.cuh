@@ -32,7 +32,12 @@ __device__ __forceinline__ unsigned long long globaltimer() {
 // Programmatic dependent launch: a kernel launched with programmatic stream
 // serialization may start before its predecessor finishes; grid_dep_wait()
 // blocks until the predecessor grid has completed and its writes are
-// visible.  Both are no-ops for a kernel launched without the attribute.
+// visible; grid_dep_launch() lets the next launch start.  Every kernel here
+// calls grid_dep_launch() only after its own grid_dep_wait() has returned, so
+// a chain of launches never has more than two grids resident and waiting
+// (signalling at kernel start let a long chain fill the GPU with grids all
+// waiting on their predecessors, which hung).  Both are no-ops for a kernel
+// launched without the attribute.
 __device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
@@ -72,7 +77,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
     for (unsigned spin = 1;; ++spin) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((spin & 255u) == 0 && globaltimer() - t0 > kWaitLimitNs) {
-            atomicOr(&g_status, kStatusTimeout);
+            atomicOr(&g_status, kStatusTimeout | (1u << 7));
             return false;
         }
     }

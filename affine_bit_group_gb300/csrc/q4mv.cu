@@ -292,7 +292,9 @@ __device__ __forceinline__ int find_prob(const Q4Args &a, int64_t t, int64_t &ti
 }
 
 // Bounded mbarrier wait that also gives up when another warp has aborted.
-__device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, volatile int *abort_flag) {
+// On a timeout it sets the timeout bit plus `site` (which wait gave up).
+__device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                              unsigned site) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = globaltimer();
     for (unsigned spin = 1;; ++spin) {
@@ -300,13 +302,15 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, vo
         if ((spin & 255u) == 0) {
             if (*abort_flag) return false;
             if (globaltimer() - t0 > kWaitLimitNs) {
-                atomicOr(&g_status, kStatusTimeout);
+                atomicOr(&g_status, kStatusTimeout | site);
                 *abort_flag = 1;
                 return false;
             }
         }
     }
 }
+// wait sites recorded in the status word
+constexpr unsigned kSiteEmpty = 1u << 4, kSiteFull = 1u << 5, kSiteDone = 1u << 6;
 
 // One step of a transposed butterfly over N values (N -> N/2): lanes whose
 // `d` bit is clear keep the first half and send the second, their partners
@@ -371,16 +375,26 @@ __global__ void __launch_bounds__(288, 2) q4mv_kernel(const __grid_constant__ Q4
         fence_mbar_init();
     }
     __syncthreads();
-    grid_dep_launch();
 
+    // Programmatic dependent launch: the first S tiles of weights are fetched
+    // before waiting for the preceding launch (weights never depend on it);
+    // every thread signals its dependents only after that wait has returned,
+    // so at most this launch and the next one are ever waiting or running.
     if (warp == 0) {
         // ------------------------------------------------ producer warp ----
         if (lane != 0) return;
         const uint64_t policy = l2_evict_first();
+        bool released = false;
         int64_t k = 0;
         for (int64_t t = blockIdx.x; t < a.total_tiles; t += gridDim.x, ++k) {
             const int s = static_cast<int>(k % S);
-            if (k >= S && !wait_or_abort(&empty[s], static_cast<uint32_t>(((k / S) & 1) ^ 1), &s_abort)) break;
+            if (k == S) {
+                grid_dep_wait();
+                grid_dep_launch();
+                released = true;
+            }
+            if (k >= S && !wait_or_abort(&empty[s], static_cast<uint32_t>(((k / S) & 1) ^ 1), &s_abort, kSiteEmpty))
+                break;
             if (s_abort) break;
             int64_t tile;
             const Q4Prob &P = a.prob[find_prob(a, t, tile)];
@@ -395,6 +409,10 @@ __global__ void __launch_bounds__(288, 2) q4mv_kernel(const __grid_constant__ Q4
                 bulk_g2s(st + a.stage_w_bytes, P.scale + r0 * G, sbb, &full[s], policy);
                 bulk_g2s(st + a.stage_w_bytes + a.stage_sb_bytes, P.bias + r0 * G, sbb, &full[s], policy);
             }
+        }
+        if (!released) {
+            grid_dep_wait();
+            grid_dep_launch();
         }
         // Drain: the block may not exit while a copy into its shared memory is
         // in flight.  Waiting on a phase that already completed returns at once.
@@ -415,6 +433,7 @@ __global__ void __launch_bounds__(288, 2) q4mv_kernel(const __grid_constant__ Q4
     const int chstep = fixed_ch ? nch : nw;
 
     grid_dep_wait();
+    grid_dep_launch();
     float rms_r = 0.f;
     if (a.prologue == kProRmsq) rms_r = warp_rms_factor<kTree>(a.x, a.cols, a.eps, lane);
     Slice sl;
@@ -422,7 +441,7 @@ __global__ void __launch_bounds__(288, 2) q4mv_kernel(const __grid_constant__ Q4
     // Final sums of tile j: thread ct adds row ct's chunk partials by the tree.
     auto finish = [&](int64_t j, int64_t tj) -> bool {
         const int pi = static_cast<int>(j % kParts);
-        if (!wait_or_abort(&done[pi], static_cast<uint32_t>((j / kParts) & 1), &s_abort)) return false;
+        if (!wait_or_abort(&done[pi], static_cast<uint32_t>((j / kParts) & 1), &s_abort, kSiteDone)) return false;
         int64_t tile;
         const Q4Prob &P = a.prob[find_prob(a, tj, tile)];
         const int64_t r0 = tile * TR;
@@ -444,7 +463,7 @@ __global__ void __launch_bounds__(288, 2) q4mv_kernel(const __grid_constant__ Q4
     int64_t k = 0, tprev = -1;
     for (int64_t t = blockIdx.x; t < a.total_tiles; t += gridDim.x, ++k) {
         const int s = static_cast<int>(k % S);
-        if (!wait_or_abort(&full[s], static_cast<uint32_t>((k / S) & 1), &s_abort)) return;
+        if (!wait_or_abort(&full[s], static_cast<uint32_t>((k / S) & 1), &s_abort, kSiteFull)) return;
         int64_t tile;
         const Q4Prob &P = a.prob[find_prob(a, t, tile)];
         const int64_t r0 = tile * TR;

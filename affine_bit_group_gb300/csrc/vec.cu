@@ -27,8 +27,8 @@ __device__ __forceinline__ float add_(float a, float b) {
 
 template <bool kTree>
 __global__ void __launch_bounds__(256) gsum_kernel(const float *__restrict__ v, float *__restrict__ s, int64_t G) {
-    grid_dep_launch();
     grid_dep_wait();
+    grid_dep_launch();
     const int lane = threadIdx.x & 31;
     const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
     for (int64_t g = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); g < G; g += nwarps) {
@@ -43,8 +43,8 @@ __global__ void __launch_bounds__(256) gsum_kernel(const float *__restrict__ v, 
 template <bool kTree>
 __global__ void __launch_bounds__(256) swq_kernel(const float *__restrict__ a, float *__restrict__ o,
                                                   float *__restrict__ osum, int64_t n) {
-    grid_dep_launch();
     grid_dep_wait();
+    grid_dep_launch();
     const int lane = threadIdx.x & 31;
     const int64_t G = n / 64;
     const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
@@ -69,8 +69,8 @@ __global__ void __launch_bounds__(1024) rmsq_kernel(const float *__restrict__ x,
                                                     int64_t n) {
     extern __shared__ float red[];
     __shared__ float s_r;
-    grid_dep_launch();
     grid_dep_wait();
+    grid_dep_launch();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
     const int G = static_cast<int>(n / 64);
     for (int g = warp; g < G; g += nwarps) {
