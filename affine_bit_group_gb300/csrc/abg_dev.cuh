@@ -19,8 +19,9 @@ namespace abg {
 // abg_device_status() combines them.
 static __device__ unsigned int g_status;
 constexpr unsigned kStatusTimeout = 1u;
-// A bounded wait gives up after this many nanoseconds of %globaltimer.
-constexpr unsigned long long kWaitLimitNs = 2000000000ull;
+// A bounded wait gives up after this many nanoseconds of %globaltimer (no
+// legitimate wait here lasts more than microseconds).
+constexpr unsigned long long kWaitLimitNs = 500000000ull;
 
 __device__ __forceinline__ unsigned long long globaltimer() {
     unsigned long long t;

@@ -355,9 +355,15 @@ abg_status abg_stage_graph_create(const abg_node *nodes, int64_t count, int mode
         where = "cudaStreamCreateWithFlags";
     if (e == cudaSuccess && (e = cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal)) != cudaSuccess)
         where = "cudaStreamBeginCapture";
+    // ABG_PDL=0 records plain stream-ordered launches (no early start of a
+    // dependent launch); results are the same.
+    static const bool pdl_on = [] {
+        const char *v = std::getenv("ABG_PDL");
+        return !(v && std::strcmp(v, "0") == 0);
+    }();
     if (e == cudaSuccess) {
         for (size_t i = 0; i < launches.size() && e == cudaSuccess; ++i)
-            if ((e = run(launches[i], cs, i > 0, mode == ABG_TREE)) != cudaSuccess)
+            if ((e = run(launches[i], cs, pdl_on && i > 0, mode == ABG_TREE)) != cudaSuccess)
                 where = "launch " + std::to_string(i) + " (kind " + std::to_string(launches[i].kind) + ")";
         cudaGraph_t graph = nullptr;
         const cudaError_t e2 = cudaStreamEndCapture(cs, &graph);

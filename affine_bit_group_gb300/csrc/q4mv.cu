@@ -254,7 +254,10 @@ __device__ __forceinline__ void load_slice(const Q4Args &a, int ch, int lane, fl
         allneg &= v[i] < 0.f;
     }
     if (!active) sp = false, allneg = false;
-    const bool grpneg = allneg && __shfl_xor_sync(0xffffffffu, allneg, 1);
+    // every lane takes part in the shuffle (a full-mask shuffle that only some
+    // lanes reach, e.g. behind a short-circuit &&, stalls the warp for good)
+    const bool partner_neg = __shfl_xor_sync(0xffffffffu, allneg ? 1 : 0, 1) != 0;
+    const bool grpneg = allneg && partner_neg;
     sl.exact = !__any_sync(0xffffffffu, sp || grpneg);
     // group sum of the lane's group: given, or the tree over the slice's values
     if (a.prologue == kProNone) {

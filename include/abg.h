@@ -47,7 +47,7 @@
  *   - Lengths that are not whole 64-value groups are rejected (ABG_ESHAPE).
  *     The pages' GPU kernels silently left such outputs untouched
  *     ([fused-token] reviewer reply); here it is an error.
- *   - A device-side wait that exceeds its time limit (about 2 s) stops the
+ *   - A device-side wait that exceeds its time limit (0.5 s) stops the
  *     kernel and sets a bit in the library's device status word; read it with
  *     abg_device_status().  No call hangs the GPU.
  */
@@ -192,6 +192,9 @@ typedef struct abg_node {
  * and instantiates the graph.  *graph_out receives an opaque handle. */
 abg_status abg_stage_graph_create(const abg_node *nodes, int64_t count, int mode, int rows_per_warp,
                                   void **graph_out);
+/* With the environment variable ABG_PDL=0 at creation, launches are recorded
+ * without programmatic dependent launch (each waits for the previous one to
+ * finish before starting); results are identical. */
 /* Enqueues one replay of the whole graph on `stream`; the caller syncs once.
  * With the environment variable ABG_TRACE=1 each launch also synchronizes and
  * prints the launch count, GPU milliseconds and wall milliseconds to stderr. */

@@ -183,5 +183,37 @@ def test_grouped_launch_matches_single_calls():
     g.close()
 
 
+def test_grouped_launch_plain_path():
+    """A grouped launch whose activation takes the plain product path (groups of all-negative values)."""
+    mats = [synth.random_case(80 + i, r, 1024)[0] for i, r in enumerate([2048, 256, 256])]
+    x = -np.abs(synth.activations(np.random.default_rng(10), 1024))
+    xs = oracle.gsum(x)
+    xd, xsd = dev(x), dev(xs)
+    ys = [empty(m.rows) for m in mats]
+    dms = [(dev_words(m.w), dev(m.scale), dev(m.bias)) for m in mats]
+    nodes = [abg.Node.q4mv(0, w, s, b, y, 1024, x=xd, xsum=xsd) for (w, s, b), y in zip(dms, ys)]
+    g = abg.StageGraph(nodes, keep=[xd, xsd] + ys + [t for d in dms for t in d])
+    g.launch()
+    torch.cuda.synchronize()
+    for m, y in zip(mats, ys):
+        assert_bits_equal(host(y), oracle.q4mv(*m.arrays(), x, xs, 1024), "grouped plain path")
+    g.close()
+    assert abg.device_status(clear=True) == 0
+
+
+@pytest.mark.parametrize("cols", [1024, 2048, 6144])
+def test_mixed_negative_groups(cols):
+    """Some 64-value groups all negative, others not: lanes of one warp disagree about
+    their own group, the warp must still agree on its path (and not stall)."""
+    m, x = synth.random_case(90, 300, cols)
+    x = np.abs(x)
+    for g in range(0, cols // 64, 3):
+        x[64 * g:64 * g + 64] *= -1
+    x[64:128] *= -1  # a lone positive-negative mix
+    xs = oracle.gsum(x)
+    assert_bits_equal(run(m, x, xs=xs), oracle.q4mv(*m.arrays(), x, xs, cols), f"mixed {cols}")
+    assert abg.device_status(clear=True) == 0
+
+
 def test_no_device_timeouts():
     assert abg.device_status(clear=True) == 0
