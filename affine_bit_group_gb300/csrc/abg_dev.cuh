@@ -70,14 +70,29 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
+// try_wait that may suspend the thread until the phase completes or
+// `hint_ns` nanoseconds pass, so a waiting warp does not spin on issue slots.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+constexpr uint32_t kSleepHintNs = 100000;
+
 // Waits for the phase with the given parity to complete.  Returns false (and
 // sets the timeout bit) if it has not completed within kWaitLimitNs.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = globaltimer();
-    for (unsigned spin = 1;; ++spin) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((spin & 255u) == 0 && globaltimer() - t0 > kWaitLimitNs) {
+    for (;;) {
+        if (mbar_try_wait_sleep(bar, parity, kSleepHintNs)) return true;
+        if (globaltimer() - t0 > kWaitLimitNs) {
             atomicOr(&g_status, kStatusTimeout | (1u << 7));
             return false;
         }

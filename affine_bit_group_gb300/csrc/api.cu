@@ -106,11 +106,12 @@ Q4Prob make_prob(const Q4Call &c) {
 }
 
 abg_status plan_calls(Q4Plan *plan, const std::vector<Q4Call> &calls, int mode, int rpw) {
+    // rows per item: 8 unless asked otherwise (it never changes results)
     Q4Prob probs[kMaxProbs];
     for (size_t i = 0; i < calls.size(); ++i) probs[i] = make_prob(calls[i]);
     const Q4Call &c0 = calls[0];
     if (!plan_q4mv(plan, probs, static_cast<int>(calls.size()), static_cast<int>(c0.cols), c0.prologue, c0.x,
-                   c0.xsum, c0.wt, c0.eps, mode == ABG_TREE, rpw == 0 ? 4 : rpw, sb_bulk(c0), g_tuning))
+                   c0.xsum, c0.wt, c0.eps, mode == ABG_TREE, rpw == 0 ? 8 : rpw, sb_bulk(c0), g_tuning))
         return ABG_ESHAPE;
     return ABG_OK;
 }

@@ -57,12 +57,21 @@ __device__ __forceinline__ float2 f2(float a, float b) { return make_float2(a, b
 // it always sits inside the 23 significand bits.
 __host__ __device__ constexpr int nib_k(int j) { return j <= 4 ? j : j - 3; }
 
-// The pair of floats -(1 + q * 2^(4k-23)) for nibble j of words a and b
-// (sign and exponent of -1.0 OR-ed onto the masked nibble).
-__device__ __forceinline__ float2 neg_u2(uint32_t a, uint32_t ah, uint32_t b, uint32_t bh, int j) {
-    const uint32_t mask = 0xFu << (4 * nib_k(j));
-    const uint32_t sa = (j <= 4) ? a : ah, sb = (j <= 4) ? b : bh;
-    return f2(__uint_as_float((sa & mask) | 0xBF800000u), __uint_as_float((sb & mask) | 0xBF800000u));
+// (w & mask) | c as one three-input logic op (mask an immediate).
+template <uint32_t kMask>
+__device__ __forceinline__ uint32_t and_or(uint32_t w, uint32_t c) {
+    uint32_t d;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(w), "n"(kMask), "r"(c));
+    return d;
+}
+
+// The pair of floats -(1 + q * 2^(4k-23)) for nibble J of words a and b
+// (sign and exponent of -1.0, held in `neg_one`, OR-ed onto the masked nibble).
+template <int J>
+__device__ __forceinline__ float2 neg_u2(uint32_t a, uint32_t ah, uint32_t b, uint32_t bh, uint32_t neg_one) {
+    constexpr uint32_t kMask = 0xFu << (4 * nib_k(J));
+    const uint32_t sa = (J <= 4) ? a : ah, sb = (J <= 4) ? b : bh;
+    return f2(__uint_as_float(and_or<kMask>(sa, neg_one)), __uint_as_float(and_or<kMask>(sb, neg_one)));
 }
 
 // q of nibble j as a float, exactly: (2^(23-4k) + q) - 2^(23-4k).
@@ -83,13 +92,24 @@ __device__ __forceinline__ float nib_scale(int j) {
 // halves stay aligned level after level.
 __device__ __forceinline__ float tree32_pairs(float2 (&P)[16]) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) P[i] = add2(P[2 * i], P[2 * i + 1]);
+    for (int i = 0; i < 8; ++i) P[i] = __fadd2_rn(P[2 * i], P[2 * i + 1]);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) P[i] = add2(P[2 * i], P[2 * i + 1]);
+    for (int i = 0; i < 4; ++i) P[i] = __fadd2_rn(P[2 * i], P[2 * i + 1]);
 #pragma unroll
-    for (int i = 0; i < 2; ++i) P[i] = add2(P[2 * i], P[2 * i + 1]);
-    P[0] = add2(P[0], P[1]);
+    for (int i = 0; i < 2; ++i) P[i] = __fadd2_rn(P[2 * i], P[2 * i + 1]);
+    P[0] = __fadd2_rn(P[0], P[1]);
     return __fadd_rn(P[0].x, P[0].y);
+}
+
+template <int M>
+__device__ __forceinline__ void exact_products(float2 (&P)[16], uint32_t w0, uint32_t h0, uint32_t w1, uint32_t h1,
+                                               uint32_t w2, uint32_t h2, uint32_t w3, uint32_t h3,
+                                               const float2 (&X)[16], uint32_t neg_one) {
+    if constexpr (M < 16) {
+        const float2 u = (M < 8) ? neg_u2<M & 7>(w0, h0, w2, h2, neg_one) : neg_u2<M & 7>(w1, h1, w3, h3, neg_one);
+        P[M] = __ffma2_rn(u, X[M], X[M]);
+        exact_products<M + 1>(P, w0, h0, w1, h1, w2, h2, w3, h3, X, neg_one);
+    }
 }
 
 // Tree sum of q*x over the lane's 32 columns of one row chunk (words wq).
@@ -108,11 +128,7 @@ __device__ __forceinline__ float lane_sum32(uint4 wq, const float2 (&X)[16]) {
     const uint32_t h0 = w0 >> 12, h1 = w1 >> 12, h2 = w2 >> 12, h3 = w3 >> 12;
     float2 P[16];
     if constexpr (kExact) {
-#pragma unroll
-        for (int m = 0; m < 16; ++m) {
-            const float2 u = (m < 8) ? neg_u2(w0, h0, w2, h2, m & 7) : neg_u2(w1, h1, w3, h3, m & 7);
-            P[m] = fma2(u, X[m], X[m]);
-        }
+        exact_products<0>(P, w0, h0, w1, h1, w2, h2, w3, h3, X, 0xBF800000u);
         return tree32_pairs(P);
     } else {
     float p[32];
@@ -300,15 +316,13 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, vo
                                               unsigned site) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = globaltimer();
-    for (unsigned spin = 1;; ++spin) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((spin & 255u) == 0) {
-            if (*abort_flag) return false;
-            if (globaltimer() - t0 > kWaitLimitNs) {
-                atomicOr(&g_status, kStatusTimeout | site);
-                *abort_flag = 1;
-                return false;
-            }
+    for (;;) {
+        if (mbar_try_wait_sleep(bar, parity, kSleepHintNs)) return true;
+        if (*abort_flag) return false;
+        if (globaltimer() - t0 > kWaitLimitNs) {
+            atomicOr(&g_status, kStatusTimeout | site);
+            *abort_flag = 1;
+            return false;
         }
     }
 }
@@ -485,17 +499,24 @@ __global__ void __launch_bounds__(288, 2) q4mv_kernel(const __grid_constant__ Q4
                 }
                 const bool active = (ch * 1024 + lane * 32) < a.cols;
                 const int g = ch * 16 + (lane >> 1);
+                // this lane's 16-byte column quad in row 0 of the stage; lanes
+                // past the row end (last chunk only) read row 0's first quad
+                // instead and their sums are discarded
+                const uint4 *wl = sw + (active ? ch * 32 + lane : 0);
+                const int wq_stride = W / 4;
                 for (int rb = rb0; rb < nrb; rb += kk) {
-                    // lane sums of R rows
+                    // lane sums of R rows: all loads first, then the arithmetic
                     float v[R];
+                    uint4 wq[R];
+                    const int nr = min(R, rows - rb * R);  // uniform; R except in the last block
 #pragma unroll
-                    for (int r = 0; r < R; ++r) {
-                        const int row = rb * R + r;  // uniform across the warp
-                        v[r] = 0.f;
-                        if (row < rows && active) {
-                            const uint4 wq = sw[static_cast<size_t>(row) * (W / 4) + ch * 32 + lane];
-                            v[r] = sl.exact ? lane_sum32<true>(wq, sl.X) : lane_sum32<false>(wq, sl.X);
-                        }
+                    for (int r = 0; r < R; ++r) wq[r] = wl[(r < nr ? rb * R + r : 0) * wq_stride];
+                    if (sl.exact) {
+#pragma unroll
+                        for (int r = 0; r < R; ++r) v[r] = lane_sum32<true>(wq[r], sl.X);
+                    } else {
+#pragma unroll
+                        for (int r = 0; r < R; ++r) v[r] = lane_sum32<false>(wq[r], sl.X);
                     }
                     // group completion (lane pair), transposed when R > 1: this
                     // lane keeps rows [ofs, ofs + R/2)

@@ -94,7 +94,7 @@ typedef enum { ABG_TREE = 0, ABG_FAST = 1 } abg_mode;
  *   rows_per_warp  1, 2, 4 or 8 rows share one staging of each 1024-column
  *          slice of x in a warp's registers ([fused-token] Change: a SIMD
  *          group does 4 rows and reads each group's activations once); 0 picks
- *          the default (4).  It never changes the result.
+ *          the default (8).  It never changes the result.
  */
 abg_status abg_q4mv(const uint32_t *w, const float *scale, const float *bias,
                     const float *x, const float *xsum, float *y,
