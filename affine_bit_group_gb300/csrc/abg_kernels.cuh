@@ -31,6 +31,11 @@ struct Q4Args {
     const float *wt;
     float eps;
     int prologue;
+    // 1: read the activation only after the preceding launch has finished
+    // (it produced it).  0: the preceding launch is a sibling of the same
+    // stage, the activation is ready at start; wait for that launch only
+    // before exiting, so finishing still implies every earlier launch finished.
+    int wait_first;
     // shape
     int cols, W, G, nch;
     // tiling
@@ -66,7 +71,8 @@ bool plan_q4mv(Q4Plan *plan, const Q4Prob *probs, int nprob, int cols, int prolo
 cudaError_t prepare_q4mv(const Q4Plan &plan);
 
 // Launches a planned product on `stream`; `pdl` marks it as a programmatic
-// dependent of the previous launch on the stream.
+// dependent of the previous launch on the stream (plan.args.wait_first says
+// whether it also depends on that launch's results).
 cudaError_t launch_q4mv(const Q4Plan &plan, cudaStream_t stream, bool pdl);
 
 cudaError_t launch_gsum(const float *v, float *s, int64_t n, bool tree, cudaStream_t stream, bool pdl);

@@ -149,6 +149,7 @@ abg_status check_swq(const float *a, const float *o, const float *osum, int64_t 
 // --------------------------------------------------------------- graphs ----
 struct Launch {
     int kind;  // abg_node_kind
+    int stage = 0;
     Q4Plan plan;
     const float *a = nullptr, *b = nullptr;
     float *o = nullptr, *os = nullptr;
@@ -321,6 +322,7 @@ abg_status abg_stage_graph_create(const abg_node *nodes, int64_t count, int mode
             used[a] = true;
             Launch L;
             L.kind = nd.kind;
+            L.stage = kv.first;
             if (nd.kind == ABG_NODE_Q4MV) {
                 if (nd.n == 0) continue;
                 std::vector<Q4Call> group = {call_of(nd)};
@@ -362,6 +364,11 @@ abg_status abg_stage_graph_create(const abg_node *nodes, int64_t count, int mode
         const char *v = std::getenv("ABG_PDL");
         return !(v && std::strcmp(v, "0") == 0);
     }();
+    // a product launch that follows a launch of its own stage does not depend
+    // on it (siblings of one stage share their inputs)
+    for (size_t i = 1; i < launches.size(); ++i)
+        if (launches[i].kind == ABG_NODE_Q4MV && launches[i].stage == launches[i - 1].stage)
+            launches[i].plan.args.wait_first = 0;
     if (e == cudaSuccess) {
         for (size_t i = 0; i < launches.size() && e == cudaSuccess; ++i)
             if ((e = run(launches[i], cs, pdl_on && i > 0, mode == ABG_TREE)) != cudaSuccess)

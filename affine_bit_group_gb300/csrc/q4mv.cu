@@ -393,15 +393,19 @@ __global__ void __launch_bounds__(288, 2) q4mv_kernel(const __grid_constant__ Q4
     }
     __syncthreads();
 
-    // Programmatic dependent launch: the first S tiles of weights are fetched
-    // before waiting for the preceding launch (weights never depend on it);
-    // every thread signals its dependents only after that wait has returned,
-    // so at most this launch and the next one are ever waiting or running.
+    // Programmatic dependent launch.  When the activation comes from the
+    // preceding launch (wait_first), the first S tiles of weights are fetched
+    // before waiting for it (weights never depend on it) and every thread
+    // signals its dependents only after that wait has returned.  A sibling
+    // launch of the same stage signals at once, computes, and waits for its
+    // predecessor only before exiting.
+    const bool wait_first = a.wait_first != 0;
+    if (!wait_first) grid_dep_launch();
     if (warp == 0) {
         // ------------------------------------------------ producer warp ----
         if (lane != 0) return;
         const uint64_t policy = l2_evict_first();
-        bool released = false;
+        bool released = !wait_first;
         int64_t k = 0;
         for (int64_t t = blockIdx.x; t < a.total_tiles; t += gridDim.x, ++k) {
             const int s = static_cast<int>(k % S);
@@ -449,8 +453,10 @@ __global__ void __launch_bounds__(288, 2) q4mv_kernel(const __grid_constant__ Q4
     const int rb0 = fixed_ch ? cw / nch : 0;
     const int chstep = fixed_ch ? nch : nw;
 
-    grid_dep_wait();
-    grid_dep_launch();
+    if (wait_first) {
+        grid_dep_wait();
+        grid_dep_launch();
+    }
     float rms_r = 0.f;
     if (a.prologue == kProRmsq) rms_r = warp_rms_factor<kTree>(a.x, a.cols, a.eps, lane);
     Slice sl;
@@ -480,7 +486,7 @@ __global__ void __launch_bounds__(288, 2) q4mv_kernel(const __grid_constant__ Q4
     int64_t k = 0, tprev = -1;
     for (int64_t t = blockIdx.x; t < a.total_tiles; t += gridDim.x, ++k) {
         const int s = static_cast<int>(k % S);
-        if (!wait_or_abort(&full[s], static_cast<uint32_t>((k / S) & 1), &s_abort, kSiteFull)) return;
+        if (!wait_or_abort(&full[s], static_cast<uint32_t>((k / S) & 1), &s_abort, kSiteFull)) break;
         int64_t tile;
         const Q4Prob &P = a.prob[find_prob(a, t, tile)];
         const int64_t r0 = tile * TR;
@@ -567,10 +573,11 @@ __global__ void __launch_bounds__(288, 2) q4mv_kernel(const __grid_constant__ Q4
             mbar_arrive(&empty[s]);       // weights of this stage no longer needed
             mbar_arrive(&done[k % kParts]);  // this warp's partials are written
         }
-        if (tprev >= 0 && !finish(k - 1, tprev)) return;
+        if (tprev >= 0 && !finish(k - 1, tprev)) break;
         tprev = t;
     }
     if (tprev >= 0) finish(k - 1, tprev);
+    if (!wait_first) grid_dep_wait();
 }
 
 template <int R, bool kTree, bool kSb>
@@ -676,6 +683,7 @@ bool plan_once(Q4Plan *plan, const Q4Prob *probs, int nprob, int cols, int prolo
     a.wt = wt;
     a.eps = eps;
     a.prologue = prologue;
+    a.wait_first = 1;
     a.cols = C;
     a.W = W;
     a.G = G;
