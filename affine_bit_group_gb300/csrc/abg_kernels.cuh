@@ -6,7 +6,7 @@
 
 namespace abg {
 
-constexpr int kMaxProbs = 16;  // products that share one activation in a grouped launch
+constexpr int kMaxProbs = 64;  // products that share one activation in a grouped launch
 
 enum Prologue { kProNone = 0, kProGsum = 1, kProRmsq = 2, kProSwq = 3 };
 

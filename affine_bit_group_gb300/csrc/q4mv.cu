@@ -299,16 +299,20 @@ __device__ __forceinline__ void load_slice(const Q4Args &a, int ch, int lane, fl
     }
 }
 
-// Locates tile t of a grouped launch.
-__device__ __forceinline__ int find_prob(const Q4Args &a, int64_t t, int64_t &tile) {
+// Locates tiles of a grouped launch.  A block visits its tiles in increasing
+// order, so the problem index only moves forward.
+struct ProbCursor {
     int p = 0;
-    while (p + 1 < a.nprob && t >= a.prob[p].tiles) {
-        t -= a.prob[p].tiles;
-        ++p;
+    int64_t base = 0;  // first tile of problem p
+    __device__ __forceinline__ int find(const Q4Args &a, int64_t t, int64_t &tile) {
+        while (p + 1 < a.nprob && t >= base + a.prob[p].tiles) {
+            base += a.prob[p].tiles;
+            ++p;
+        }
+        tile = t - base;
+        return p;
     }
-    tile = t;
-    return p;
-}
+};
 
 // Bounded mbarrier wait that also gives up when another warp has aborted.
 // On a timeout it sets the timeout bit plus `site` (which wait gave up).
@@ -406,6 +410,7 @@ __global__ void __launch_bounds__(288, 2) q4mv_kernel(const __grid_constant__ Q4
         if (lane != 0) return;
         const uint64_t policy = l2_evict_first();
         bool released = !wait_first;
+        ProbCursor cur;
         int64_t k = 0;
         for (int64_t t = blockIdx.x; t < a.total_tiles; t += gridDim.x, ++k) {
             const int s = static_cast<int>(k % S);
@@ -418,7 +423,7 @@ __global__ void __launch_bounds__(288, 2) q4mv_kernel(const __grid_constant__ Q4
                 break;
             if (s_abort) break;
             int64_t tile;
-            const Q4Prob &P = a.prob[find_prob(a, t, tile)];
+            const Q4Prob &P = a.prob[cur.find(a, t, tile)];
             const int64_t r0 = tile * TR;
             const int rows = static_cast<int>(min(static_cast<int64_t>(TR), P.n - r0));
             unsigned char *st = smem + a.off_stage + static_cast<size_t>(s) * a.stage_bytes;
@@ -462,11 +467,12 @@ __global__ void __launch_bounds__(288, 2) q4mv_kernel(const __grid_constant__ Q4
     Slice sl;
     int cur_ch = -1;
     // Final sums of tile j: thread ct adds row ct's chunk partials by the tree.
+    ProbCursor cur, fcur;
     auto finish = [&](int64_t j, int64_t tj) -> bool {
         const int pi = static_cast<int>(j % kParts);
         if (!wait_or_abort(&done[pi], static_cast<uint32_t>((j / kParts) & 1), &s_abort, kSiteDone)) return false;
         int64_t tile;
-        const Q4Prob &P = a.prob[find_prob(a, tj, tile)];
+        const Q4Prob &P = a.prob[fcur.find(a, tj, tile)];
         const int64_t r0 = tile * TR;
         const int rows = static_cast<int>(min(static_cast<int64_t>(TR), P.n - r0));
         if (ct < rows) {
@@ -488,7 +494,7 @@ __global__ void __launch_bounds__(288, 2) q4mv_kernel(const __grid_constant__ Q4
         const int s = static_cast<int>(k % S);
         if (!wait_or_abort(&full[s], static_cast<uint32_t>((k / S) & 1), &s_abort, kSiteFull)) break;
         int64_t tile;
-        const Q4Prob &P = a.prob[find_prob(a, t, tile)];
+        const Q4Prob &P = a.prob[cur.find(a, t, tile)];
         const int64_t r0 = tile * TR;
         const int rows = static_cast<int>(min(static_cast<int64_t>(TR), P.n - r0));
         const unsigned char *stg = smem + a.off_stage + static_cast<size_t>(s) * a.stage_bytes;
@@ -511,18 +517,24 @@ __global__ void __launch_bounds__(288, 2) q4mv_kernel(const __grid_constant__ Q4
                 const uint4 *wl = sw + (active ? ch * 32 + lane : 0);
                 const int wq_stride = W / 4;
                 for (int rb = rb0; rb < nrb; rb += kk) {
-                    // lane sums of R rows: all loads first, then the arithmetic
+                    // lane sums of R rows, four rows at a time: their loads
+                    // first, then the arithmetic
                     float v[R];
-                    uint4 wq[R];
                     const int nr = min(R, rows - rb * R);  // uniform; R except in the last block
+                    constexpr int B = (R < 4) ? R : 4;
 #pragma unroll
-                    for (int r = 0; r < R; ++r) wq[r] = wl[(r < nr ? rb * R + r : 0) * wq_stride];
-                    if (sl.exact) {
+                    for (int r0 = 0; r0 < R; r0 += B) {
+                        uint4 wq[B];
 #pragma unroll
-                        for (int r = 0; r < R; ++r) v[r] = lane_sum32<true>(wq[r], sl.X);
-                    } else {
+                        for (int r = 0; r < B; ++r)
+                            wq[r] = wl[(r0 + r < nr ? rb * R + r0 + r : 0) * wq_stride];
+                        if (sl.exact) {
 #pragma unroll
-                        for (int r = 0; r < R; ++r) v[r] = lane_sum32<false>(wq[r], sl.X);
+                            for (int r = 0; r < B; ++r) v[r0 + r] = lane_sum32<true>(wq[r], sl.X);
+                        } else {
+#pragma unroll
+                            for (int r = 0; r < B; ++r) v[r0 + r] = lane_sum32<false>(wq[r], sl.X);
+                        }
                     }
                     // group completion (lane pair), transposed when R > 1: this
                     // lane keeps rows [ofs, ofs + R/2)
