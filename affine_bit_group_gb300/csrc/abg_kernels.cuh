@@ -58,6 +58,7 @@ struct Q4Plan {
     int rows_per_warp;
     bool tree;
     bool sb_smem;
+    bool wide;
 };
 
 // Fills plan->args layout, grid and block for products sharing one activation.

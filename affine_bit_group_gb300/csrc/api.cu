@@ -453,7 +453,7 @@ abg_status abg_device_status(uint32_t *bits, int clear) {
 }
 
 abg_status abg_set_q4mv_tuning(int smem_kb, int consumer_warps, int blocks_per_sm, int stage_kb) {
-    if (smem_kb < 0 || smem_kb > 227 || consumer_warps < 0 || consumer_warps > 8 || blocks_per_sm < 0 ||
+    if (smem_kb < 0 || smem_kb > 227 || consumer_warps < 0 || consumer_warps > 16 || blocks_per_sm < 0 ||
         blocks_per_sm > 4 || stage_kb < 0 || stage_kb > 200)
         return ABG_EINVAL;
     g_tuning.smem_kb = smem_kb;

@@ -376,8 +376,11 @@ __device__ __forceinline__ float group_levels(float (&v)[N], int lane, int dist,
 // tile four back.
 constexpr int kParts = 4;
 
-template <int R, bool kTree, bool kSbSmem>
-__global__ void __launch_bounds__(288, 2) q4mv_kernel(const __grid_constant__ Q4Args a) {
+// kWide: one block per SM with up to 16 computing warps (large products);
+// otherwise up to 8 computing warps and two blocks per SM, so that the next
+// launch of a chain can start beside this one.
+template <int R, bool kTree, bool kSbSmem, bool kWide>
+__global__ void __launch_bounds__(kWide ? 544 : 288, kWide ? 1 : 2) q4mv_kernel(const __grid_constant__ Q4Args a) {
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ volatile int s_abort;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + a.off_bar);
@@ -592,16 +595,21 @@ __global__ void __launch_bounds__(288, 2) q4mv_kernel(const __grid_constant__ Q4
     if (!wait_first) grid_dep_wait();
 }
 
-template <int R, bool kTree, bool kSb>
+template <int R, bool kTree, bool kSb, bool kWide>
 void *kernel_ptr() {
-    return reinterpret_cast<void *>(&q4mv_kernel<R, kTree, kSb>);
+    return reinterpret_cast<void *>(&q4mv_kernel<R, kTree, kSb, kWide>);
 }
 
-void *select_kernel(int R, bool tree, bool sb) {
-#define ABG_SEL(RR)                                                                            \
-    if (R == RR) {                                                                             \
-        if (tree) return sb ? kernel_ptr<RR, true, true>() : kernel_ptr<RR, true, false>();    \
-        return sb ? kernel_ptr<RR, false, true>() : kernel_ptr<RR, false, false>();            \
+void *select_kernel(int R, bool tree, bool sb, bool wide) {
+    if (wide) {  // built for 8 rows per item only
+        if (R != 8) return nullptr;
+        if (tree) return sb ? kernel_ptr<8, true, true, true>() : kernel_ptr<8, true, false, true>();
+        return sb ? kernel_ptr<8, false, true, true>() : kernel_ptr<8, false, false, true>();
+    }
+#define ABG_SEL(RR)                                                                                          \
+    if (R == RR) {                                                                                           \
+        if (tree) return sb ? kernel_ptr<RR, true, true, false>() : kernel_ptr<RR, true, false, false>();    \
+        return sb ? kernel_ptr<RR, false, true, false>() : kernel_ptr<RR, false, false, false>();            \
     }
     ABG_SEL(1)
     ABG_SEL(2)
@@ -649,13 +657,17 @@ bool plan_once(Q4Plan *plan, const Q4Prob *probs, int nprob, int cols, int prolo
     const int C = cols, W = C / 8, G = C / 64, nch = (C + 1023) / 1024;
     // consumer warps: a multiple of the chunk count (each warp keeps one
     // 1024-column slice of x), at most 8 (the kernel's launch bound)
-    int nw = tune.consumer_warps;
+    // tuned consumer_warps > 8 selects the one-block-per-SM layout (8 rows per item)
+    const bool wide = tune.consumer_warps > 8 && R == 8;
+    const int nw_max = wide ? 16 : 8;
+    int nw = wide ? tune.consumer_warps : tune.consumer_warps;
     if (nw <= 0) nw = nch <= 8 ? nch * (8 / nch) : 8;
-    nw = std::min(std::max(nw, 1), 8);
+    if (wide && nch <= 16) nw = nch * (std::min(nw, 16) / nch);
+    nw = std::min(std::max(nw, 1), nw_max);
     const int kk = (nch <= nw) ? nw / nch : 1;  // warps per chunk position
     const uint32_t row_bytes = static_cast<uint32_t>(C / 2 + (sb_smem ? 8 * G : 0));
     const uint32_t fixed = 1024;  // barriers and alignment slack
-    uint32_t budget = static_cast<uint32_t>(tune.smem_kb > 0 ? tune.smem_kb : 110) * 1024u;
+    uint32_t budget = static_cast<uint32_t>(tune.smem_kb > 0 ? tune.smem_kb : (wide ? 220 : 110)) * 1024u;
     const uint32_t hard_max = 227u * 1024u - 64u;
     // tile rows: a multiple of R*kk so row blocks spread evenly over the warps
     const int unit = R * kk;
@@ -713,7 +725,7 @@ bool plan_once(Q4Plan *plan, const Q4Prob *probs, int nprob, int cols, int prolo
 
     // blocks per SM: what fits (registers and shared memory), at most 2 unless tuned
     int fit = 1;
-    void *fn = select_kernel(R, tree, sb_smem);
+    void *fn = select_kernel(R, tree, sb_smem, wide);
     if (fn && raise_smem_limit(fn) == cudaSuccess) {
         int nb = 0;
         if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, fn, static_cast<int>(32 * (1 + nw)), a.smem_bytes) ==
@@ -722,7 +734,7 @@ bool plan_once(Q4Plan *plan, const Q4Prob *probs, int nprob, int cols, int prolo
             fit = nb;
     }
     cudaGetLastError();
-    int bps = std::min(fit, tune.blocks_per_sm > 0 ? tune.blocks_per_sm : 2);
+    int bps = std::min(fit, wide ? 1 : (tune.blocks_per_sm > 0 ? tune.blocks_per_sm : 2));
     bps = std::max(bps, 1);
     const int64_t cap = static_cast<int64_t>(sm_count()) * bps;
     plan->grid = dim3(static_cast<unsigned>(std::max<int64_t>(1, std::min(a.total_tiles, cap))));
@@ -730,6 +742,7 @@ bool plan_once(Q4Plan *plan, const Q4Prob *probs, int nprob, int cols, int prolo
     plan->rows_per_warp = R;
     plan->tree = tree;
     plan->sb_smem = sb_smem;
+    plan->wide = wide;
     return true;
 }
 
@@ -766,14 +779,14 @@ bool plan_q4mv(Q4Plan *plan, const Q4Prob *probs, int nprob, int cols, int prolo
 }
 
 cudaError_t prepare_q4mv(const Q4Plan &plan) {
-    void *fn = select_kernel(plan.rows_per_warp, plan.tree, plan.sb_smem);
+    void *fn = select_kernel(plan.rows_per_warp, plan.tree, plan.sb_smem, plan.wide);
     if (!fn) return cudaErrorInvalidValue;
     return raise_smem_limit(fn);
 }
 
 cudaError_t launch_q4mv(const Q4Plan &plan, cudaStream_t stream, bool pdl) {
     if (plan.args.total_tiles == 0) return cudaSuccess;
-    void *fn = select_kernel(plan.rows_per_warp, plan.tree, plan.sb_smem);
+    void *fn = select_kernel(plan.rows_per_warp, plan.tree, plan.sb_smem, plan.wide);
     if (!fn) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = plan.grid;

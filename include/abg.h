@@ -213,7 +213,9 @@ abg_status abg_device_status(uint32_t *bits, int clear);
  *   smem_kb          shared-memory budget per thread block (default 110, so
  *                    two blocks fit on an SM and a dependent launch can start
  *                    while its predecessor still runs)
- *   consumer_warps   warps that compute, 1..8 (default: chosen from cols)
+ *   consumer_warps   warps that compute, 1..16 (default: chosen from cols, at
+ *                    most 8); above 8 selects one block per SM (with 8 rows
+ *                    per warp item)
  *   blocks_per_sm    thread blocks per SM in the grid, at most what fits
  *                    (default: 2)
  *   stage_kb         target size of one pipeline stage of streamed rows

@@ -136,7 +136,7 @@ def test_stage_graph_validation(lib):
 
 def test_tuning_validation(lib):
     assert lib.abg_set_q4mv_tuning(300, 0, 0, 0) == EINVAL
-    assert lib.abg_set_q4mv_tuning(0, 9, 0, 0) == EINVAL
+    assert lib.abg_set_q4mv_tuning(0, 17, 0, 0) == EINVAL
     assert lib.abg_set_q4mv_tuning(0, 0, 0, 300) == EINVAL
     assert lib.abg_set_q4mv_tuning(0, 0, 0, 0) == OK
 
