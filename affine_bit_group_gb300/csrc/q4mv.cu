@@ -39,6 +39,7 @@
 // in shared memory, where one thread per row sums them with the same tree
 // (odd element carried).  Groups past the end of the row contribute -0, which
 // leaves every tree sum unchanged.
+#include "../../include/abg.h"
 #include "abg_dev.cuh"
 #include "abg_kernels.cuh"
 
@@ -169,51 +170,47 @@ __device__ __forceinline__ float tree32(const float (&v)[32]) {
     return t[0];
 }
 
-// 1/sqrt(ss/n + eps) for the RMS norm: ss = tree over groups of the tree over
-// the group of x*x.  Computed by one warp on its own (every warp of the block
-// gets the same bits).  Lane l sums the squares of groups l, l+32, ...; a
-// butterfly sums each block of 32 groups; the blocks' sums (at most 8, padded
-// with -0) meet in a fixed pairwise tree.
+// The same factor computed by all computing warps of a block together: each
+// 64-value group is summed by 8 lanes (8 consecutive squares each, then a
+// 3-step butterfly: the pairwise tree over 8 blocks of 8), group sums meet in
+// shared memory, one warp takes the tree over groups (padded with -0).  Uses
+// named barrier 1 over the nct computing threads (all of them call this).
 template <bool kTree>
-__device__ float warp_rms_factor(const float *__restrict__ x, int C, float eps, int lane) {
-    const int G = C / 64, nblk = (G + 31) / 32;
-    float blk[8];
+__device__ float block_rms_factor(const float *__restrict__ x, int C, float eps, int cw, int nw, int lane,
+                                  float *red, float *rbox) {
+    const int G = C / 64, nct = nw * 32;
+    for (int g0 = 4 * cw; g0 < G; g0 += 4 * nw) {
+        const int g = g0 + (lane >> 3);
+        float s = kNegZero;
+        if (g < G) {
+            const float4 *p4 = reinterpret_cast<const float4 *>(x + 64 * g + 8 * (lane & 7));
+            const float4 a = p4[0], b = p4[1];
+            const float t0 = __fadd_rn(__fmul_rn(a.x, a.x), __fmul_rn(a.y, a.y));
+            const float t1 = __fadd_rn(__fmul_rn(a.z, a.z), __fmul_rn(a.w, a.w));
+            const float t2 = __fadd_rn(__fmul_rn(b.x, b.x), __fmul_rn(b.y, b.y));
+            const float t3 = __fadd_rn(__fmul_rn(b.z, b.z), __fmul_rn(b.w, b.w));
+            s = __fadd_rn(__fadd_rn(t0, t1), __fadd_rn(t2, t3));
+        }
 #pragma unroll
-    for (int b = 0; b < 8; ++b) {
-        blk[b] = kNegZero;
-        if (b < nblk) {
-            const int g = 32 * b + lane;
-            float s = kNegZero;
-            if (g < G) {
-                float v[32], t[32];
-                const float4 *p4 = reinterpret_cast<const float4 *>(x + 64 * g);
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const float4 q = p4[8 * h + i];
-                        v[4 * i] = __fmul_rn(q.x, q.x);
-                        v[4 * i + 1] = __fmul_rn(q.y, q.y);
-                        v[4 * i + 2] = __fmul_rn(q.z, q.z);
-                        v[4 * i + 3] = __fmul_rn(q.w, q.w);
-                    }
-                    t[h] = tree32(v);
-                }
-                s = __fadd_rn(t[0], t[1]);
+        for (int d = 1; d < 8; d <<= 1) s = __fadd_rn(s, __shfl_xor_sync(0xffffffffu, s, d));
+        if (g < G && (lane & 7) == 0) red[g] = s;
+    }
+    named_bar(1, nct);
+    if (cw == 0) {
+        const float ss = warp_tree_smem(red, G);
+        if (lane == 0) {
+            float r;
+            if (kTree) {
+                const float mean = __fdiv_rn(ss, static_cast<float>(C));
+                r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(mean, eps)));
+            } else {
+                r = rsqrtf(ss / static_cast<float>(C) + eps);
             }
-            blk[b] = warp_tree<32>(s);
+            *rbox = r;
         }
     }
-#pragma unroll
-    for (int h = 4; h >= 1; h >>= 1)
-#pragma unroll
-        for (int i = 0; i < h; ++i) blk[i] = __fadd_rn(blk[2 * i], blk[2 * i + 1]);
-    const float ss = blk[0];
-    if (kTree) {
-        const float mean = __fdiv_rn(ss, static_cast<float>(C));
-        return __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(mean, eps)));
-    }
-    return rsqrtf(ss / static_cast<float>(C) + eps);
+    named_bar(1, nct);
+    return *rbox;
 }
 
 // One warp's slice of the activation: columns ch*1024 + lane*32 + (0..31).
@@ -383,6 +380,8 @@ template <int R, bool kTree, bool kSbSmem, bool kWide>
 __global__ void __launch_bounds__(kWide ? 544 : 288, kWide ? 1 : 2) q4mv_kernel(const __grid_constant__ Q4Args a) {
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ volatile int s_abort;
+    __shared__ float s_red[ABG_MAX_COLS / 64];  // group sums of squares (RMS-norm prologue)
+    __shared__ float s_rbox;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + a.off_bar);
     uint64_t *empty = full + a.stages;
     uint64_t *done = empty + a.stages;
@@ -466,7 +465,7 @@ __global__ void __launch_bounds__(kWide ? 544 : 288, kWide ? 1 : 2) q4mv_kernel(
         grid_dep_launch();
     }
     float rms_r = 0.f;
-    if (a.prologue == kProRmsq) rms_r = warp_rms_factor<kTree>(a.x, a.cols, a.eps, lane);
+    if (a.prologue == kProRmsq) rms_r = block_rms_factor<kTree>(a.x, a.cols, a.eps, cw, nw, lane, s_red, &s_rbox);
     Slice sl;
     int cur_ch = -1;
     // Final sums of tile j: thread ct adds row ct's chunk partials by the tree.
@@ -526,17 +525,17 @@ __global__ void __launch_bounds__(kWide ? 544 : 288, kWide ? 1 : 2) q4mv_kernel(
                     const int nr = min(R, rows - rb * R);  // uniform; R except in the last block
                     constexpr int B = (R < 4) ? R : 4;
 #pragma unroll
-                    for (int r0 = 0; r0 < R; r0 += B) {
+                    for (int bq = 0; bq < R; bq += B) {
                         uint4 wq[B];
 #pragma unroll
                         for (int r = 0; r < B; ++r)
-                            wq[r] = wl[(r0 + r < nr ? rb * R + r0 + r : 0) * wq_stride];
+                            wq[r] = wl[(bq + r < nr ? rb * R + bq + r : 0) * wq_stride];
                         if (sl.exact) {
 #pragma unroll
-                            for (int r = 0; r < B; ++r) v[r0 + r] = lane_sum32<true>(wq[r], sl.X);
+                            for (int r = 0; r < B; ++r) v[bq + r] = lane_sum32<true>(wq[r], sl.X);
                         } else {
 #pragma unroll
-                            for (int r = 0; r < B; ++r) v[r0 + r] = lane_sum32<false>(wq[r], sl.X);
+                            for (int r = 0; r < B; ++r) v[bq + r] = lane_sum32<false>(wq[r], sl.X);
                         }
                     }
                     // group completion (lane pair), transposed when R > 1: this
@@ -668,7 +667,7 @@ bool plan_once(Q4Plan *plan, const Q4Prob *probs, int nprob, int cols, int prolo
     const uint32_t row_bytes = static_cast<uint32_t>(C / 2 + (sb_smem ? 8 * G : 0));
     const uint32_t fixed = 1024;  // barriers and alignment slack
     uint32_t budget = static_cast<uint32_t>(tune.smem_kb > 0 ? tune.smem_kb : (wide ? 220 : 110)) * 1024u;
-    const uint32_t hard_max = 227u * 1024u - 64u;
+    const uint32_t hard_max = 225u * 1024u;  // leaves room for the static shared memory
     // tile rows: a multiple of R*kk so row blocks spread evenly over the warps
     const int unit = R * kk;
     int TR = unit;

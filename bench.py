@@ -40,6 +40,7 @@ sys.path.insert(0, ROOT)
 from affine_bit_group_gb300 import synth  # noqa: E402
 
 CALLS = 400
+GROUP = 64  # products per grouped launch (the library's limit)
 MID_ROWS, MID_COLS = 4096, 2048
 PEAK_FALLBACK_GBS = 6800.0
 
@@ -210,9 +211,14 @@ def run_ours(args, rank, world):
     us_per_product = ms_step * 1e3 / CALLS
     launches_per_step = g.launches
 
-    # the product kernel's share of the step: all launches but the group sums
-    # (a few microseconds) are product launches of 16 products each
-    achieved = value
+    # the dominant kernel alone: one grouped launch of 64 products (the
+    # step's product launches are of this kind), timed with CUDA events on
+    # the stream it runs on
+    g1 = abg.StageGraph([abg.Node.q4mv(0, *mats[i % len(mats)], ys[i], MID_COLS, x=x, xsum=xsum)
+                         for i in range(GROUP)], keep=[x, xsum] + ys)
+    ms_launch, _ = time_graph(g1, stream, max(args.steps, 10), args.warmup, False)
+    g1.close()
+    achieved = GROUP * pbytes / (ms_launch * 1e-3) / 1e9
 
     # the same 400 products as 400 dependent stages (decode-like latency)
     gc = build_mid_graph(abg, mats, x, xsum, ys[:2], CALLS, chained=True)
@@ -252,7 +258,8 @@ def run_ours(args, rank, world):
         extra["head"] = bench_head(abg, stream, args, peak)
         extra["decode_token"] = bench_decode(abg, decode, stream, args)
 
-    res = dict(value=value, ms_step=ms_step, us_per_product=us_per_product, achieved=achieved, clocks=clocks,
+    res = dict(value=value, ms_step=ms_step, us_per_product=us_per_product, achieved=achieved,
+               launch_us=ms_launch * 1e3, clocks=clocks,
                e2e=e2e, extra=extra, launches=launches_per_step * args.steps, peak=peak, peak_kind=peak_kind,
                hash=y_hash, copies=copies)
     return res
@@ -353,6 +360,24 @@ def config_dict(copies=None):
             "parallelism": "replicas"}
 
 
+def max_over_ranks(ms: float, world: int, device: str) -> float:
+    """The slowest rank's step time (replicas run the same work; the job is as
+    fast as its slowest replica).  Ends with a barrier."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.barrier()
+    return float(t.item())
+
+
+def job_value(ms_step: float, world: int) -> float:
+    """Whole-job GB/s: every replica streams one step's products per step."""
+    return world * CALLS * product_bytes(MID_ROWS, MID_COLS) / (ms_step * 1e-3) / 1e9
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -386,18 +411,10 @@ def main():
         import torch.distributed as dist
         dist.init_process_group("nccl" if os.environ.get("ABG_BENCH_BACKEND") != "gloo" else "gloo")
     res = run_ours(args, rank, world)
-    ms_step = res["ms_step"]
-    if world > 1:
-        import torch
-        import torch.distributed as dist
-        t = torch.tensor([ms_step], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_step = float(t.item())
-        dist.barrier()
+    ms_step = max_over_ranks(res["ms_step"], world, "cuda")
     if rank != 0:
         return
-    step_bytes = CALLS * product_bytes(MID_ROWS, MID_COLS)
-    value = world * step_bytes / (ms_step * 1e-3) / 1e9
+    value = job_value(ms_step, world)
     kernel_src = os.path.join(ROOT, "affine_bit_group_gb300", "csrc", "q4mv.cu")
     traffic = profile_traffic(kernel_src, "q4mv_mid_4096x2048.md")
     line = {
@@ -409,7 +426,9 @@ def main():
         "hash32": res["hash"],
         "roofline": {"bound": "hbm", "achieved": res["achieved"], "peak": res["peak"], "unit": "GB/s",
                      "frac": res["achieved"] / res["peak"], "traffic": traffic, "peak_kind": res["peak_kind"],
-                     "kernel": "q4mv_kernel<8,tree,bulk scale/bias>"},
+                     "kernel": "q4mv_kernel<8,tree,bulk scale/bias>: one launch of 64 products of 4096x2048",
+                     "bytes_per_launch": GROUP * product_bytes(MID_ROWS, MID_COLS),
+                     "launch_us": res["launch_us"]},
         "clocks": res["clocks"], "e2e": res["e2e"], "gpu_launches": res["launches"], "extra": res["extra"],
     }
     if not args.no_cpu:
