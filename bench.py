@@ -68,7 +68,7 @@ def profile_traffic(kernel_src: str, profile: str):
         for line in f:
             if ":" in line and line.strip().startswith(("dram_bytes_per_launch", "kernel_source_sha256")):
                 k, v = line.split(":", 1)
-                vals[k.strip()] = v.strip().strip("`")
+                vals[k.strip()] = v.split()[0].strip("`")
     with open(kernel_src, "rb") as f:
         sha = hashlib.sha256(f.read()).hexdigest()
     if vals.get("kernel_source_sha256") != sha or "dram_bytes_per_launch" not in vals:
