@@ -58,7 +58,7 @@ struct Q4Plan {
     int rows_per_warp;
     bool tree;
     bool sb_smem;
-    bool wide;
+    int layout;  // block layout (see the kernel)
 };
 
 // Fills plan->args layout, grid and block for products sharing one activation.

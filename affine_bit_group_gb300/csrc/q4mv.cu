@@ -373,11 +373,18 @@ __device__ __forceinline__ float group_levels(float (&v)[N], int lane, int dist,
 // tile four back.
 constexpr int kParts = 4;
 
-// kWide: one block per SM with up to 16 computing warps (large products);
-// otherwise up to 8 computing warps and two blocks per SM, so that the next
-// launch of a chain can start beside this one.
-template <int R, bool kTree, bool kSbSmem, bool kWide>
-__global__ void __launch_bounds__(kWide ? 544 : 288, kWide ? 1 : 2) q4mv_kernel(const __grid_constant__ Q4Args a) {
+// Block layouts (the register file is split over the SM's four schedulers,
+// so the warps per SM set the registers per thread):
+//   kLayout 0: up to 8 computing warps, two blocks per SM (96 registers);
+//   kLayout 1: up to 16 computing warps, one block per SM;
+//   kLayout 2: up to 6 computing warps, two blocks per SM (128 registers).
+// With two blocks per SM the next launch of a chain can start beside this one.
+constexpr int layout_threads(int l) { return l == 1 ? 544 : (l == 2 ? 224 : 288); }
+constexpr int layout_blocks(int l) { return l == 1 ? 1 : 2; }
+
+template <int R, bool kTree, bool kSbSmem, int kLayout>
+__global__ void __launch_bounds__(layout_threads(kLayout), layout_blocks(kLayout))
+    q4mv_kernel(const __grid_constant__ Q4Args a) {
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ volatile int s_abort;
     __shared__ float s_red[ABG_MAX_COLS / 64];  // group sums of squares (RMS-norm prologue)
@@ -594,21 +601,25 @@ __global__ void __launch_bounds__(kWide ? 544 : 288, kWide ? 1 : 2) q4mv_kernel(
     if (!wait_first) grid_dep_wait();
 }
 
-template <int R, bool kTree, bool kSb, bool kWide>
+template <int R, bool kTree, bool kSb, int kLayout>
 void *kernel_ptr() {
-    return reinterpret_cast<void *>(&q4mv_kernel<R, kTree, kSb, kWide>);
+    return reinterpret_cast<void *>(&q4mv_kernel<R, kTree, kSb, kLayout>);
 }
 
-void *select_kernel(int R, bool tree, bool sb, bool wide) {
-    if (wide) {  // built for 8 rows per item only
+void *select_kernel(int R, bool tree, bool sb, int layout) {
+    if (layout != 0) {  // built for 8 rows per item only
         if (R != 8) return nullptr;
-        if (tree) return sb ? kernel_ptr<8, true, true, true>() : kernel_ptr<8, true, false, true>();
-        return sb ? kernel_ptr<8, false, true, true>() : kernel_ptr<8, false, false, true>();
+        if (layout == 1) {
+            if (tree) return sb ? kernel_ptr<8, true, true, 1>() : kernel_ptr<8, true, false, 1>();
+            return sb ? kernel_ptr<8, false, true, 1>() : kernel_ptr<8, false, false, 1>();
+        }
+        if (tree) return sb ? kernel_ptr<8, true, true, 2>() : kernel_ptr<8, true, false, 2>();
+        return sb ? kernel_ptr<8, false, true, 2>() : kernel_ptr<8, false, false, 2>();
     }
-#define ABG_SEL(RR)                                                                                          \
-    if (R == RR) {                                                                                           \
-        if (tree) return sb ? kernel_ptr<RR, true, true, false>() : kernel_ptr<RR, true, false, false>();    \
-        return sb ? kernel_ptr<RR, false, true, false>() : kernel_ptr<RR, false, false, false>();            \
+#define ABG_SEL(RR)                                                                                  \
+    if (R == RR) {                                                                                   \
+        if (tree) return sb ? kernel_ptr<RR, true, true, 0>() : kernel_ptr<RR, true, false, 0>();    \
+        return sb ? kernel_ptr<RR, false, true, 0>() : kernel_ptr<RR, false, false, 0>();            \
     }
     ABG_SEL(1)
     ABG_SEL(2)
@@ -656,12 +667,14 @@ bool plan_once(Q4Plan *plan, const Q4Prob *probs, int nprob, int cols, int prolo
     const int C = cols, W = C / 8, G = C / 64, nch = (C + 1023) / 1024;
     // consumer warps: a multiple of the chunk count (each warp keeps one
     // 1024-column slice of x), at most 8 (the kernel's launch bound)
-    // tuned consumer_warps > 8 selects the one-block-per-SM layout (8 rows per item)
-    const bool wide = tune.consumer_warps > 8 && R == 8;
-    const int nw_max = wide ? 16 : 8;
-    int nw = wide ? tune.consumer_warps : tune.consumer_warps;
+    // layout: tuned consumer_warps > 8 selects one block per SM; 1..6 with 8
+    // rows per item selects the 128-register two-block layout
+    const int layout = (R != 8 || tune.consumer_warps == 0) ? 0 : (tune.consumer_warps > 8 ? 1 : (tune.consumer_warps <= 6 ? 2 : 0));
+    const bool wide = layout == 1;
+    const int nw_max = wide ? 16 : (layout == 2 ? 6 : 8);
+    int nw = tune.consumer_warps;
     if (nw <= 0) nw = nch <= 8 ? nch * (8 / nch) : 8;
-    if (wide && nch <= 16) nw = nch * (std::min(nw, 16) / nch);
+    if (nch <= nw_max) nw = nch * (std::min(nw, nw_max) / nch);
     nw = std::min(std::max(nw, 1), nw_max);
     const int kk = (nch <= nw) ? nw / nch : 1;  // warps per chunk position
     const uint32_t row_bytes = static_cast<uint32_t>(C / 2 + (sb_smem ? 8 * G : 0));
@@ -724,7 +737,7 @@ bool plan_once(Q4Plan *plan, const Q4Prob *probs, int nprob, int cols, int prolo
 
     // blocks per SM: what fits (registers and shared memory), at most 2 unless tuned
     int fit = 1;
-    void *fn = select_kernel(R, tree, sb_smem, wide);
+    void *fn = select_kernel(R, tree, sb_smem, layout);
     if (fn && raise_smem_limit(fn) == cudaSuccess) {
         int nb = 0;
         if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, fn, static_cast<int>(32 * (1 + nw)), a.smem_bytes) ==
@@ -741,7 +754,7 @@ bool plan_once(Q4Plan *plan, const Q4Prob *probs, int nprob, int cols, int prolo
     plan->rows_per_warp = R;
     plan->tree = tree;
     plan->sb_smem = sb_smem;
-    plan->wide = wide;
+    plan->layout = layout;
     return true;
 }
 
@@ -778,14 +791,14 @@ bool plan_q4mv(Q4Plan *plan, const Q4Prob *probs, int nprob, int cols, int prolo
 }
 
 cudaError_t prepare_q4mv(const Q4Plan &plan) {
-    void *fn = select_kernel(plan.rows_per_warp, plan.tree, plan.sb_smem, plan.wide);
+    void *fn = select_kernel(plan.rows_per_warp, plan.tree, plan.sb_smem, plan.layout);
     if (!fn) return cudaErrorInvalidValue;
     return raise_smem_limit(fn);
 }
 
 cudaError_t launch_q4mv(const Q4Plan &plan, cudaStream_t stream, bool pdl) {
     if (plan.args.total_tiles == 0) return cudaSuccess;
-    void *fn = select_kernel(plan.rows_per_warp, plan.tree, plan.sb_smem, plan.wide);
+    void *fn = select_kernel(plan.rows_per_warp, plan.tree, plan.sb_smem, plan.layout);
     if (!fn) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = plan.grid;
