@@ -28,6 +28,13 @@ head of a 2B-class model, and one decode token's products):
   down 2048x6144], then the final RMS-norm weights, the 248320x2048 head and
   the N(0,1) hidden vector.
 * ``sweep`` point (rows, cols): ``default_rng([4, rows, cols])``, matrix then x.
+
+Other formats (group size 32, 64 or 128 columns; scale and bias stored as f32,
+bf16 or f16): the same draws with cols/group groups, then the f32 scale and
+bias are stored in the 16-bit type -- bf16 as the upper half of the f32 bits
+(truncation), f16 by numpy's ``astype(float16)`` -- and passed as uint16 bit
+patterns.  ``fmt_case(group, sb, rows, cols)`` uses ``default_rng([5, group,
+code(sb), rows, cols])``, matrix then x.
 """
 from __future__ import annotations
 
@@ -42,15 +49,22 @@ N_LAYERS = 24
 EPS = 1e-6
 
 
+GROUPS = (32, 64, 128)
+SB_TYPES = ("f32", "bf16", "f16")
+
+
 @dataclass
 class Q4Matrix:
-    """A packed 4-bit affine matrix: words u32[rows, cols/8], scale/bias f32[rows, cols/64]."""
+    """A packed 4-bit affine matrix: words u32[rows, cols/8], scale/bias [rows, cols/group]
+    (f32 values, or uint16 bit patterns of bf16 / f16 values)."""
 
     w: np.ndarray
     scale: np.ndarray
     bias: np.ndarray
     rows: int
     cols: int
+    group: int = 64
+    sb: str = "f32"
 
     def arrays(self):
         return self.w, self.scale, self.bias
@@ -60,15 +74,32 @@ class Q4Matrix:
         return self.w.nbytes + self.scale.nbytes + self.bias.nbytes
 
 
-def q4_matrix(rng: np.random.Generator, rows: int, cols: int) -> Q4Matrix:
-    if cols % 64:
-        raise ValueError("cols must be a multiple of 64")
-    G, W = cols // 64, cols // 8
+def q4_matrix(rng: np.random.Generator, rows: int, cols: int, group: int = 64, sb: str = "f32") -> Q4Matrix:
+    if cols % 64 or group not in GROUPS or cols % group or sb not in SB_TYPES:
+        raise ValueError("cols a multiple of 64 and of group; group 32, 64 or 128; sb f32, bf16 or f16")
+    G, W = cols // group, cols // 8
     w = rng.integers(0, 2**32, size=(rows, W), dtype=np.uint32)
     scale = rng.uniform(0.002, 0.02, size=(rows, G)).astype(np.float32)
     noise = rng.normal(0.0, 0.001, size=(rows, G))
     bias = (-8.0 * scale.astype(np.float64) + noise).astype(np.float32)
-    return Q4Matrix(w, scale, bias, rows, cols)
+    if sb != "f32":
+        scale, bias = store16(scale, sb), store16(bias, sb)
+    return Q4Matrix(w, scale, bias, rows, cols, group, sb)
+
+
+def store16(v: np.ndarray, sb: str) -> np.ndarray:
+    """f32 values as bf16 (upper half of the bits) or f16 (numpy rounding) bit patterns."""
+    v = np.ascontiguousarray(v, np.float32)
+    if sb == "bf16":
+        return (v.view(np.uint32) >> np.uint32(16)).astype(np.uint16)
+    return v.astype(np.float16).view(np.uint16)
+
+
+def fmt_case(group: int, sb: str, rows: int, cols: int):
+    """(matrix, x) in the given format; see the module docstring."""
+    rng = np.random.default_rng([5, group, SB_TYPES.index(sb), rows, cols])
+    m = q4_matrix(rng, rows, cols, group, sb)
+    return m, activations(rng, cols)
 
 
 def activations(rng: np.random.Generator, n: int) -> np.ndarray:

@@ -65,6 +65,13 @@ def _load():
             lib.or_fnv1a.restype = ctypes.c_uint32
             lib.or_hash32.argtypes = [f32p, i64]
             lib.or_hash32.restype = ctypes.c_uint32
+            vp = ctypes.c_void_p
+            lib.or_bf16_to_f32.argtypes = [ctypes.c_uint16]
+            lib.or_bf16_to_f32.restype = ctypes.c_float
+            lib.or_f16_to_f32.argtypes = [ctypes.c_uint16]
+            lib.or_f16_to_f32.restype = ctypes.c_float
+            lib.or_gsum_ex.argtypes = [f32p, f32p, i64, ctypes.c_int]
+            lib.or_q4mv_ex.argtypes = [u32p, vp, vp, ctypes.c_int, ctypes.c_int, f32p, f32p, f32p, i64, i64, i64, i64]
             _lib = lib
     return _lib
 
@@ -212,3 +219,50 @@ def decode_token(model, hidden, eps=1e-6, keep=False):
     if keep:
         return logits, trace, (xf, xfs)
     return logits
+
+
+SB_DTYPES = {"f32": 0, "bf16": 1, "f16": 2}
+
+
+def half_to_f32(bits, dtype: str) -> np.ndarray:
+    """Stored bf16 or f16 bit patterns (uint16) widened to f32, elementwise (exact)."""
+    bits = np.ascontiguousarray(bits, dtype=np.uint16).ravel()
+    f = _load().or_bf16_to_f32 if dtype == "bf16" else _load().or_f16_to_f32
+    return np.array([f(int(b)) for b in bits], np.float32)
+
+
+def gsum_ex(v, gs: int) -> np.ndarray:
+    """s[g] = TREE(v[gs*g : gs*g + gs])."""
+    v, pv = _f32(v)
+    if gs not in (32, 64, 128) or v.size % gs:
+        raise ValueError("group size 32, 64 or 128 dividing the length")
+    s = np.empty(v.size // gs, np.float32)
+    _load().or_gsum_ex(pv, _f32(s)[1], v.size, gs)
+    return s
+
+
+def q4mv_ex(w, scale, bias, sb_dtype: str, gs: int, x, xsum, cols, row0=0, n=None) -> np.ndarray:
+    """The product for group size gs and scale/bias stored as f32, bf16 or f16
+    (scale and bias given as float32 arrays, or as uint16 bit patterns)."""
+    if gs not in (32, 64, 128) or cols % gs or cols % 64:
+        raise ValueError("group size 32, 64 or 128; cols a multiple of 64 and of gs")
+    w, pw = _u32(w)
+    dt = SB_DTYPES[sb_dtype]
+    if dt == 0:
+        scale = np.ascontiguousarray(scale, np.float32)
+        bias = np.ascontiguousarray(bias, np.float32)
+    else:
+        scale = np.ascontiguousarray(scale, np.uint16)
+        bias = np.ascontiguousarray(bias, np.uint16)
+    x, px = _f32(x)
+    xsum, pxs = _f32(xsum)
+    rows = w.size // (cols // 8)
+    n = rows - row0 if n is None else n
+    G = cols // gs
+    if scale.size != rows * G or bias.size != rows * G or x.size != cols or xsum.size != G:
+        raise ValueError("array sizes do not match rows, cols and gs")
+    if row0 < 0 or n < 0 or row0 + n > rows:
+        raise ValueError("row range out of bounds")
+    y = np.empty(n, np.float32)
+    _load().or_q4mv_ex(pw, scale.ctypes.data, bias.ctypes.data, dt, gs, px, pxs, _f32(y)[1], rows, cols, row0, n)
+    return y

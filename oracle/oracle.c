@@ -294,3 +294,78 @@ uint32_t or_hash32(const float *y, int64_t n)
     }
     return h;
 }
+
+/* ------------------------------------------------------------------------ */
+/* Other formats of the same product (the MLX 4-bit family the pages name:  */
+/* [fused-token] Why, "MLX 4-bit"): group size gs in {32, 64, 128} columns   */
+/* and scale/bias stored as f32, bf16 or f16.  Every stored scale and bias   */
+/* is widened to f32 exactly, then the product is the one above with gs in   */
+/* place of 64:                                                              */
+/*   d = TREE_gs(RN(q*x)),  t = RN(RN(s*d) + RN(b*xsum[g])),  y = TREE_G(t)  */
+/* with G = cols/gs and xsum[g] = TREE(x over group g).                      */
+/* ------------------------------------------------------------------------ */
+enum { OR_F32 = 0, OR_BF16 = 1, OR_F16 = 2 };
+
+/* bf16 is the upper half of an f32 */
+float or_bf16_to_f32(uint16_t h)
+{
+    return f32_from_bits((uint32_t)h << 16);
+}
+
+/* f16 (1 sign, 5 exponent, 10 significand bits, bias 15) to f32, exactly */
+float or_f16_to_f32(uint16_t h)
+{
+    const uint32_t sign = (uint32_t)(h >> 15) << 31;
+    const uint32_t e = (h >> 10) & 0x1Fu;
+    uint32_t m = h & 0x3FFu;
+    if (e == 0x1Fu) return f32_from_bits(sign | 0x7F800000u | (m << 13)); /* inf, NaN */
+    if (e != 0) return f32_from_bits(sign | ((e - 15u + 127u) << 23) | (m << 13));
+    if (m == 0) return f32_from_bits(sign); /* signed zero */
+    /* subnormal: m * 2^-24, normalised */
+    int ex = -14;
+    while (!(m & 0x400u)) {
+        m <<= 1;
+        --ex;
+    }
+    m &= 0x3FFu;
+    return f32_from_bits(sign | ((uint32_t)(ex + 127) << 23) | (m << 13));
+}
+
+static float or_load_sb(const void *p, int dtype, int64_t i)
+{
+    if (dtype == OR_BF16) return or_bf16_to_f32(((const uint16_t *)p)[i]);
+    if (dtype == OR_F16) return or_f16_to_f32(((const uint16_t *)p)[i]);
+    return ((const float *)p)[i];
+}
+
+void or_gsum_ex(const float *v, float *s, int64_t n, int gs)
+{
+    for (int64_t g = 0; g < n / gs; ++g)
+        s[g] = or_tree(v + gs * g, gs);
+}
+
+void or_q4mv_ex(const uint32_t *w, const void *scale, const void *bias, int sb_dtype, int gs,
+                const float *x, const float *xsum, float *y,
+                int64_t rows, int64_t cols, int64_t row0, int64_t n)
+{
+    (void)rows;
+    const int64_t W = cols / 8, G = cols / gs;
+    float *t = (float *)malloc((size_t)(G > 0 ? G : 1) * sizeof(float));
+    float p[128];
+    for (int64_t i = 0; i < n; ++i) {
+        const int64_t r = row0 + i;
+        for (int64_t g = 0; g < G; ++g) {
+            for (int j = 0; j < gs; ++j) {
+                const int64_t c = gs * g + j;
+                const uint32_t q = (w[r * W + c / 8] >> (4 * (c % 8))) & 0xFu;
+                p[j] = (float)q * x[c];
+            }
+            const float d = or_tree(p, gs);
+            const float sd = or_load_sb(scale, sb_dtype, r * G + g) * d;
+            const float bx = or_load_sb(bias, sb_dtype, r * G + g) * xsum[g];
+            t[g] = sd + bx;
+        }
+        y[i] = or_tree(t, G);
+    }
+    free(t);
+}
