@@ -17,14 +17,16 @@ import os
 import threading
 
 __all__ = [
-    "TREE", "FAST", "AbgError", "library", "q4mv", "gsum", "rmsq", "swq", "StageGraph", "Node",
-    "device_status", "set_q4mv_tuning", "MAX_COLS",
+    "TREE", "FAST", "AbgError", "library", "q4mv", "q4mv_ex", "gsum", "rmsq", "swq", "StageGraph", "Node",
+    "device_status", "set_q4mv_tuning", "MAX_COLS", "SB_F32", "SB_BF16", "SB_F16", "SB_TYPES",
 ]
 
 TREE, FAST = 0, 1
 MAX_COLS = 16384
 NODE_Q4MV, NODE_RMSQ, NODE_SWQ, NODE_GSUM = 0, 1, 2, 3
 PRO_NONE, PRO_GSUM, PRO_RMSQ, PRO_SWQ = 0, 1, 2, 3
+SB_F32, SB_BF16, SB_F16 = 0, 1, 2
+SB_TYPES = {"f32": SB_F32, "bf16": SB_BF16, "f16": SB_F16}
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "libabg.so")
@@ -55,6 +57,7 @@ class _Node(ctypes.Structure):
         ("x", ctypes.c_void_p), ("xsum", ctypes.c_void_p), ("wt", ctypes.c_void_p),
         ("out", ctypes.c_void_p), ("out_sum", ctypes.c_void_p),
         ("len", ctypes.c_int64),
+        ("group", ctypes.c_int32), ("sb_type", ctypes.c_int32),
     ]
 
 
@@ -75,6 +78,10 @@ def library(build_if_missing: bool = True) -> ctypes.CDLL:
             lib.abg_gsum.argtypes = [P, P, I64, I, P]
             lib.abg_rmsq.argtypes = [P, P, ctypes.c_float, P, P, I64, I, P]
             lib.abg_swq.argtypes = [P, P, P, I64, I, P]
+            lib.abg_q4mv_ex.argtypes = [P, P, P, I, I, P, P, P, I64, I64, I64, I64, I, I, P]
+            lib.abg_gsum_ex.argtypes = [P, P, I64, I, I, P]
+            lib.abg_rmsq_ex.argtypes = [P, P, ctypes.c_float, P, P, I64, I, I, P]
+            lib.abg_swq_ex.argtypes = [P, P, P, I64, I, I, P]
             lib.abg_stage_graph_create.argtypes = [ctypes.POINTER(_Node), I64, I, I, ctypes.POINTER(P)]
             lib.abg_stage_graph_launch.argtypes = [P, P]
             lib.abg_stage_graph_launches.argtypes = [P, ctypes.POINTER(I64)]
@@ -85,7 +92,8 @@ def library(build_if_missing: bool = True) -> ctypes.CDLL:
             lib.abg_status_str.restype = ctypes.c_char_p
             lib.abg_last_cuda_error.argtypes = []
             lib.abg_last_cuda_error.restype = ctypes.c_char_p
-            for f in ("abg_q4mv", "abg_gsum", "abg_rmsq", "abg_swq", "abg_stage_graph_create",
+            for f in ("abg_q4mv", "abg_gsum", "abg_rmsq", "abg_swq", "abg_q4mv_ex", "abg_gsum_ex", "abg_rmsq_ex",
+                      "abg_swq_ex", "abg_stage_graph_create",
                       "abg_stage_graph_launch", "abg_stage_graph_launches", "abg_stage_graph_destroy",
                       "abg_device_status", "abg_set_q4mv_tuning"):
                 getattr(lib, f).restype = ctypes.c_int
@@ -109,7 +117,8 @@ def _ptr(t, dtype=None, numel=None, name="tensor"):
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
     if dtype is not None and t.dtype != dtype and not (dtype == "word" and t.element_size() == 4 and
-                                                         not t.is_floating_point()):
+                                                         not t.is_floating_point()) \
+            and not (dtype == "half" and t.element_size() == 2):
         raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
     if numel is not None and t.numel() < numel:
         raise ValueError(f"{name} holds {t.numel()} elements, needs {numel}")
@@ -145,31 +154,52 @@ def q4mv(w, scale, bias, x, xsum, y, cols: int, row0: int = 0, n: int | None = N
     return y
 
 
-def gsum(v, s, mode: int = TREE, stream=None):
-    """s[g] = tree sum of v[64g:64g+64]."""
+def q4mv_ex(w, scale, bias, sb_type, group: int, x, xsum, y, cols: int, row0: int = 0, n: int | None = None,
+            mode: int = TREE, rows_per_warp: int = 0, stream=None):
+    """The product for groups of `group` columns with scale/bias stored as sb_type
+    ("f32", "bf16", "f16" or an SB_* code); 16-bit scale and bias may be any
+    2-byte tensor holding the bit patterns (see abg_q4mv_ex)."""
+    _, f32 = _dtypes()
+    sb = SB_TYPES[sb_type] if isinstance(sb_type, str) else sb_type
+    rows = w.shape[0] if w.dim() == 2 else w.numel() // (cols // 8)
+    n = rows - row0 if n is None else n
+    G, W = cols // group, cols // 8
+    sdt = f32 if sb == SB_F32 else "half"
+    st = library().abg_q4mv_ex(
+        _ptr(w, "word", rows * W, "w"), _ptr(scale, sdt, rows * G, "scale"), _ptr(bias, sdt, rows * G, "bias"),
+        sb, group, _ptr(x, f32, cols, "x"), _ptr(xsum, f32, G, "xsum"), _ptr(y, f32, n, "y"),
+        rows, cols, row0, n, mode, rows_per_warp, _stream(stream))
+    _check(st, "abg_q4mv_ex")
+    return y
+
+
+def gsum(v, s, mode: int = TREE, stream=None, group: int = 64):
+    """s[g] = tree sum of v[group*g : group*g+group]."""
     _, f32 = _dtypes()
     n = v.numel()
-    _check(library().abg_gsum(_ptr(v, f32, n, "v"), _ptr(s, f32, n // 64, "s"), n, mode, _stream(stream)), "abg_gsum")
+    st = library().abg_gsum_ex(_ptr(v, f32, n, "v"), _ptr(s, f32, n // group, "s"), n, group, mode, _stream(stream))
+    _check(st, "abg_gsum_ex")
     return s
 
 
-def rmsq(x, wt, xn, xsum, eps: float = 1e-6, mode: int = TREE, stream=None):
+def rmsq(x, wt, xn, xsum, eps: float = 1e-6, mode: int = TREE, stream=None, group: int = 64):
     """RMS norm with weights into xn, and the group sums of xn into xsum."""
     _, f32 = _dtypes()
     n = x.numel()
-    st = library().abg_rmsq(_ptr(x, f32, n, "x"), _ptr(wt, f32, n, "wt"), ctypes.c_float(eps), _ptr(xn, f32, n, "xn"),
-                            _ptr(xsum, f32, n // 64, "xsum"), n, mode, _stream(stream))
-    _check(st, "abg_rmsq")
+    st = library().abg_rmsq_ex(_ptr(x, f32, n, "x"), _ptr(wt, f32, n, "wt"), ctypes.c_float(eps),
+                               _ptr(xn, f32, n, "xn"), _ptr(xsum, f32, n // group, "xsum"), n, group, mode,
+                               _stream(stream))
+    _check(st, "abg_rmsq_ex")
     return xn, xsum
 
 
-def swq(a, o, osum, mode: int = TREE, stream=None):
+def swq(a, o, osum, mode: int = TREE, stream=None, group: int = 64):
     """o = silu(a[:n]) * a[n:], and the group sums of o into osum."""
     _, f32 = _dtypes()
     n = a.numel() // 2
-    st = library().abg_swq(_ptr(a, f32, 2 * n, "a"), _ptr(o, f32, n, "o"), _ptr(osum, f32, n // 64, "osum"), n, mode,
-                           _stream(stream))
-    _check(st, "abg_swq")
+    st = library().abg_swq_ex(_ptr(a, f32, 2 * n, "a"), _ptr(o, f32, n, "o"), _ptr(osum, f32, n // group, "osum"), n,
+                              group, mode, _stream(stream))
+    _check(st, "abg_swq_ex")
     return o, osum
 
 
@@ -177,29 +207,31 @@ class Node:
     """Builders for the stage-graph node kinds (fields as in struct abg_node)."""
 
     @staticmethod
-    def q4mv(stage, w, scale, bias, y, cols, x, xsum=None, prologue=PRO_NONE, wt=None, eps=1e-6, row0=0, n=None):
+    def q4mv(stage, w, scale, bias, y, cols, x, xsum=None, prologue=PRO_NONE, wt=None, eps=1e-6, row0=0, n=None,
+             group=64, sb_type=SB_F32):
         rows = w.shape[0] if w.dim() == 2 else w.numel() // (cols // 8)
         n = rows - row0 if n is None else n
+        sb = SB_TYPES[sb_type] if isinstance(sb_type, str) else sb_type
         nd = _Node(kind=NODE_Q4MV, stage=stage, w=_ptr(w, name="w"), scale=_ptr(scale, name="scale"),
                    bias=_ptr(bias, name="bias"), rows=rows, cols=cols, row0=row0, n=n, y=_ptr(y, name="y"),
                    prologue=prologue, eps=eps, x=_ptr(x, name="x"), xsum=_ptr(xsum, name="xsum"),
-                   wt=_ptr(wt, name="wt"))
+                   wt=_ptr(wt, name="wt"), group=group, sb_type=sb)
         return nd
 
     @staticmethod
-    def rmsq(stage, x, wt, out, out_sum, eps=1e-6):
+    def rmsq(stage, x, wt, out, out_sum, eps=1e-6, group=64):
         return _Node(kind=NODE_RMSQ, stage=stage, x=_ptr(x, name="x"), wt=_ptr(wt, name="wt"), out=_ptr(out, name="out"),
-                     out_sum=_ptr(out_sum, name="out_sum"), eps=eps, len=x.numel())
+                     out_sum=_ptr(out_sum, name="out_sum"), eps=eps, len=x.numel(), group=group)
 
     @staticmethod
-    def swq(stage, a, out, out_sum):
+    def swq(stage, a, out, out_sum, group=64):
         return _Node(kind=NODE_SWQ, stage=stage, x=_ptr(a, name="a"), out=_ptr(out, name="out"),
-                     out_sum=_ptr(out_sum, name="out_sum"), len=a.numel() // 2)
+                     out_sum=_ptr(out_sum, name="out_sum"), len=a.numel() // 2, group=group)
 
     @staticmethod
-    def gsum(stage, v, out_sum):
+    def gsum(stage, v, out_sum, group=64):
         return _Node(kind=NODE_GSUM, stage=stage, x=_ptr(v, name="v"), out_sum=_ptr(out_sum, name="out_sum"),
-                     len=v.numel())
+                     len=v.numel(), group=group)
 
 
 class StageGraph:

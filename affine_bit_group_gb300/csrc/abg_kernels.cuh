@@ -13,8 +13,8 @@ enum Prologue { kProNone = 0, kProGsum = 1, kProRmsq = 2, kProSwq = 3 };
 // One matrix of a (grouped) product launch.  Pointers already point at row row0.
 struct Q4Prob {
     const uint32_t *w;
-    const float *scale;
-    const float *bias;
+    const void *scale;  // f32, or bf16 / f16 bit patterns
+    const void *bias;
     float *y;
     int64_t n;      // rows to compute
     int64_t tiles;  // ceil(n / tile_rows)
@@ -36,8 +36,9 @@ struct Q4Args {
     // stage, the activation is ready at start; wait for that launch only
     // before exiting, so finishing still implies every earlier launch finished.
     int wait_first;
-    // shape
+    // shape (G = cols / group size)
     int cols, W, G, nch;
+    int sb_f16;  // 16-bit scale and bias: 1 = f16, 0 = bf16
     // tiling
     int tile_rows, stages, nw;
     // shared-memory layout (byte offsets)
@@ -59,13 +60,16 @@ struct Q4Plan {
     bool tree;
     bool sb_smem;
     int layout;  // block layout (see the kernel)
+    int lg;      // group size 32 << lg
+    bool half;   // 16-bit scale and bias
 };
 
-// Fills plan->args layout, grid and block for products sharing one activation.
+// Fills plan->args layout, grid and block for products sharing one activation
+// and one weight format (group 32, 64 or 128; sb_type an abg_sb_type).
 // Returns false if the shape cannot be planned (cols too large for shared memory).
-bool plan_q4mv(Q4Plan *plan, const Q4Prob *probs, int nprob, int cols, int prologue, const float *x,
-               const float *xsum, const float *wt, float eps, bool tree, int rows_per_warp, bool sb_smem,
-               const Q4Tuning &tune);
+bool plan_q4mv(Q4Plan *plan, const Q4Prob *probs, int nprob, int cols, int group, int sb_type, int prologue,
+               const float *x, const float *xsum, const float *wt, float eps, bool tree, int rows_per_warp,
+               bool sb_smem, const Q4Tuning &tune);
 
 // Sets the kernel's shared-memory limit for a plan (not a stream operation;
 // call it before stream capture).
@@ -76,10 +80,12 @@ cudaError_t prepare_q4mv(const Q4Plan &plan);
 // whether it also depends on that launch's results).
 cudaError_t launch_q4mv(const Q4Plan &plan, cudaStream_t stream, bool pdl);
 
-cudaError_t launch_gsum(const float *v, float *s, int64_t n, bool tree, cudaStream_t stream, bool pdl);
-cudaError_t launch_rmsq(const float *x, const float *wt, float eps, float *xn, float *xsum, int64_t n, bool tree,
-                        cudaStream_t stream, bool pdl);
-cudaError_t launch_swq(const float *a, float *o, float *osum, int64_t n, bool tree, cudaStream_t stream, bool pdl);
+// Producers; their group sums cover `group` (32, 64 or 128) values each.
+cudaError_t launch_gsum(const float *v, float *s, int64_t n, int group, bool tree, cudaStream_t stream, bool pdl);
+cudaError_t launch_rmsq(const float *x, const float *wt, float eps, float *xn, float *xsum, int64_t n, int group,
+                        bool tree, cudaStream_t stream, bool pdl);
+cudaError_t launch_swq(const float *a, float *o, float *osum, int64_t n, int group, bool tree, cudaStream_t stream,
+                       bool pdl);
 
 int sm_count();
 

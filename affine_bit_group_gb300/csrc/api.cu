@@ -46,26 +46,39 @@ Range rng(const void *p, int64_t count, size_t elem) {
 }
 bool overlap(Range a, Range b) { return a.lo < a.hi && b.lo < b.hi && a.lo < b.hi && b.lo < a.hi; }
 
-bool valid_len(int64_t n) { return n > 0 && n % 64 == 0; }
+bool valid_group(int group) { return group == 32 || group == 64 || group == 128; }
+// a vector length: whole 64-value groups and whole groups of `group`
+bool valid_len(int64_t n, int group = 64) { return n > 0 && n % 64 == 0 && n % group == 0; }
+// node field: 0 means 64
+int node_group(int32_t g) { return g == 0 ? 64 : g; }
 
 // ------------------------------------------------------------ products ----
 struct Q4Call {
     const uint32_t *w;
-    const float *scale, *bias;
+    const void *scale, *bias;
     int64_t rows, cols, row0, n;
     float *y;
     int prologue;
     const float *x, *xsum, *wt;
     float eps;
+    int group = 64;
+    int sb_type = ABG_SB_F32;
 };
 
 int64_t act_len(const Q4Call &c) { return c.prologue == kProSwq ? 2 * c.cols : c.cols; }
+size_t sb_elem(const Q4Call &c) { return c.sb_type == ABG_SB_F32 ? 4 : 2; }
+int64_t groups(const Q4Call &c) { return c.cols / c.group; }
+
+// the weight arrays of a product (packed words, scale, bias)
+std::vector<Range> q4_weights(const Q4Call &c) {
+    const int64_t W = c.cols / 8, G = groups(c);
+    return {rng(c.w, c.rows * W, 4), rng(c.scale, c.rows * G, sb_elem(c)), rng(c.bias, c.rows * G, sb_elem(c))};
+}
 
 std::vector<Range> q4_inputs(const Q4Call &c) {
-    const int64_t W = c.cols / 8, G = c.cols / 64;
-    std::vector<Range> in = {rng(c.w, c.rows * W, 4), rng(c.scale, c.rows * G, 4), rng(c.bias, c.rows * G, 4),
-                             rng(c.x, act_len(c), 4)};
-    if (c.prologue == kProNone) in.push_back(rng(c.xsum, G, 4));
+    std::vector<Range> in = q4_weights(c);
+    in.push_back(rng(c.x, act_len(c), 4));
+    if (c.prologue == kProNone) in.push_back(rng(c.xsum, groups(c), 4));
     if (c.prologue == kProRmsq) in.push_back(rng(c.wt, c.cols, 4));
     return in;
 }
@@ -74,13 +87,15 @@ abg_status check_q4(const Q4Call &c, int mode, int rpw) {
     if (mode != ABG_TREE && mode != ABG_FAST) return ABG_EINVAL;
     if (rpw != 0 && rpw != 1 && rpw != 2 && rpw != 4 && rpw != 8) return ABG_EINVAL;
     if (c.prologue < kProNone || c.prologue > kProSwq) return ABG_EINVAL;
-    if (c.cols <= 0 || c.cols % 64 != 0 || c.cols > ABG_MAX_COLS) return ABG_ESHAPE;
+    if (!valid_group(c.group) || c.sb_type < ABG_SB_F32 || c.sb_type > ABG_SB_F16) return ABG_EINVAL;
+    if (c.cols <= 0 || c.cols % 64 != 0 || c.cols % c.group != 0 || c.cols > ABG_MAX_COLS) return ABG_ESHAPE;
     if (c.rows < 0 || c.row0 < 0 || c.n < 0 || c.row0 > c.rows || c.n > c.rows - c.row0) return ABG_ESHAPE;
     if (c.n == 0) return ABG_OK;
     if (!c.w || !c.scale || !c.bias || !c.x || !c.y) return ABG_EINVAL;
     if (c.prologue == kProNone && !c.xsum) return ABG_EINVAL;
     if (c.prologue == kProRmsq && !c.wt) return ABG_EINVAL;
-    if (!aligned(c.w, 16) || !aligned(c.x, 16) || !aligned(c.scale, 4) || !aligned(c.bias, 4) || !aligned(c.y, 4))
+    if (!aligned(c.w, 16) || !aligned(c.x, 16) || !aligned(c.scale, sb_elem(c)) || !aligned(c.bias, sb_elem(c)) ||
+        !aligned(c.y, 4))
         return ABG_EALIGN;
     if (c.prologue == kProNone && !aligned(c.xsum, 4)) return ABG_EALIGN;
     if (c.prologue == kProRmsq && !aligned(c.wt, 16)) return ABG_EALIGN;
@@ -92,14 +107,15 @@ abg_status check_q4(const Q4Call &c, int mode, int rpw) {
 
 // Scale and bias rows are bulk-copied when every row starts on 16 bytes.
 bool sb_bulk(const Q4Call &c) {
-    return (c.cols / 64) % 4 == 0 && aligned(c.scale, 16) && aligned(c.bias, 16);
+    return (groups(c) * static_cast<int64_t>(sb_elem(c))) % 16 == 0 && aligned(c.scale, 16) && aligned(c.bias, 16);
 }
 
 Q4Prob make_prob(const Q4Call &c) {
     Q4Prob p = {};
+    const size_t sbo = static_cast<size_t>(c.row0 * groups(c)) * sb_elem(c);
     p.w = c.w + c.row0 * (c.cols / 8);
-    p.scale = c.scale + c.row0 * (c.cols / 64);
-    p.bias = c.bias + c.row0 * (c.cols / 64);
+    p.scale = static_cast<const unsigned char *>(c.scale) + sbo;
+    p.bias = static_cast<const unsigned char *>(c.bias) + sbo;
     p.y = c.y;
     p.n = c.n;
     return p;
@@ -110,38 +126,40 @@ abg_status plan_calls(Q4Plan *plan, const std::vector<Q4Call> &calls, int mode, 
     Q4Prob probs[kMaxProbs];
     for (size_t i = 0; i < calls.size(); ++i) probs[i] = make_prob(calls[i]);
     const Q4Call &c0 = calls[0];
-    if (!plan_q4mv(plan, probs, static_cast<int>(calls.size()), static_cast<int>(c0.cols), c0.prologue, c0.x,
-                   c0.xsum, c0.wt, c0.eps, mode == ABG_TREE, rpw == 0 ? 8 : rpw, sb_bulk(c0), g_tuning))
+    if (!plan_q4mv(plan, probs, static_cast<int>(calls.size()), static_cast<int>(c0.cols), c0.group, c0.sb_type,
+                   c0.prologue, c0.x, c0.xsum, c0.wt, c0.eps, mode == ABG_TREE, rpw == 0 ? 8 : rpw, sb_bulk(c0),
+                   g_tuning))
         return ABG_ESHAPE;
     return ABG_OK;
 }
 
 // -------------------------------------------------------------- vectors ----
-abg_status check_gsum(const float *v, const float *s, int64_t n, int mode) {
+abg_status check_gsum(const float *v, const float *s, int64_t n, int group, int mode) {
     if (mode != ABG_TREE && mode != ABG_FAST) return ABG_EINVAL;
-    if (!v || !s) return ABG_EINVAL;
-    if (!valid_len(n)) return ABG_ESHAPE;
+    if (!v || !s || !valid_group(group)) return ABG_EINVAL;
+    if (!valid_len(n, group)) return ABG_ESHAPE;
     if (!aligned(v, 16) || !aligned(s, 4)) return ABG_EALIGN;
-    if (overlap(rng(s, n / 64, 4), rng(v, n, 4))) return ABG_EALIAS;
+    if (overlap(rng(s, n / group, 4), rng(v, n, 4))) return ABG_EALIAS;
     return ABG_OK;
 }
 
-abg_status check_rmsq(const float *x, const float *wt, const float *xn, const float *xsum, int64_t n, int mode) {
+abg_status check_rmsq(const float *x, const float *wt, const float *xn, const float *xsum, int64_t n, int group,
+                      int mode) {
     if (mode != ABG_TREE && mode != ABG_FAST) return ABG_EINVAL;
-    if (!x || !wt || !xn || !xsum) return ABG_EINVAL;
-    if (!valid_len(n) || n > (int64_t(1) << 20)) return ABG_ESHAPE;
+    if (!x || !wt || !xn || !xsum || !valid_group(group)) return ABG_EINVAL;
+    if (!valid_len(n, group) || n > (int64_t(1) << 20)) return ABG_ESHAPE;
     if (!aligned(x, 16) || !aligned(wt, 16) || !aligned(xn, 16) || !aligned(xsum, 4)) return ABG_EALIGN;
-    const Range rx = rng(x, n, 4), rw = rng(wt, n, 4), rn = rng(xn, n, 4), rs = rng(xsum, n / 64, 4);
+    const Range rx = rng(x, n, 4), rw = rng(wt, n, 4), rn = rng(xn, n, 4), rs = rng(xsum, n / group, 4);
     if (overlap(rn, rx) || overlap(rn, rw) || overlap(rs, rx) || overlap(rs, rw) || overlap(rs, rn)) return ABG_EALIAS;
     return ABG_OK;
 }
 
-abg_status check_swq(const float *a, const float *o, const float *osum, int64_t n, int mode) {
+abg_status check_swq(const float *a, const float *o, const float *osum, int64_t n, int group, int mode) {
     if (mode != ABG_TREE && mode != ABG_FAST) return ABG_EINVAL;
-    if (!a || !o || !osum) return ABG_EINVAL;
-    if (!valid_len(n)) return ABG_ESHAPE;
+    if (!a || !o || !osum || !valid_group(group)) return ABG_EINVAL;
+    if (!valid_len(n, group)) return ABG_ESHAPE;
     if (!aligned(a, 16) || !aligned(o, 16) || !aligned(osum, 4)) return ABG_EALIGN;
-    const Range ra = rng(a, 2 * n, 4), ro = rng(o, n, 4), rs = rng(osum, n / 64, 4);
+    const Range ra = rng(a, 2 * n, 4), ro = rng(o, n, 4), rs = rng(osum, n / group, 4);
     if (overlap(ro, ra) || overlap(rs, ra) || overlap(rs, ro)) return ABG_EALIAS;
     return ABG_OK;
 }
@@ -155,6 +173,7 @@ struct Launch {
     float *o = nullptr, *os = nullptr;
     float eps = 0.f;
     int64_t len = 0;
+    int group = 64;
 };
 
 struct StageGraph {
@@ -171,9 +190,9 @@ cudaError_t prepare(const Launch &L) {
 cudaError_t run(const Launch &L, cudaStream_t s, bool pdl, bool tree) {
     switch (L.kind) {
     case ABG_NODE_Q4MV: return launch_q4mv(L.plan, s, pdl);
-    case ABG_NODE_RMSQ: return launch_rmsq(L.a, L.b, L.eps, L.o, L.os, L.len, tree, s, pdl);
-    case ABG_NODE_SWQ: return launch_swq(L.a, L.o, L.os, L.len, tree, s, pdl);
-    default: return launch_gsum(L.a, L.os, L.len, tree, s, pdl);
+    case ABG_NODE_RMSQ: return launch_rmsq(L.a, L.b, L.eps, L.o, L.os, L.len, L.group, tree, s, pdl);
+    case ABG_NODE_SWQ: return launch_swq(L.a, L.o, L.os, L.len, L.group, tree, s, pdl);
+    default: return launch_gsum(L.a, L.os, L.len, L.group, tree, s, pdl);
     }
 }
 
@@ -192,6 +211,8 @@ Q4Call call_of(const abg_node &nd) {
     c.xsum = nd.xsum;
     c.wt = nd.wt;
     c.eps = nd.eps;
+    c.group = node_group(nd.group);
+    c.sb_type = nd.sb_type;
     return c;
 }
 
@@ -205,21 +226,23 @@ void node_io(const abg_node &nd, std::vector<Range> &in, std::vector<Range> &out
     }
     case ABG_NODE_RMSQ:
         in = {rng(nd.x, nd.len, 4), rng(nd.wt, nd.len, 4)};
-        out = {rng(nd.out, nd.len, 4), rng(nd.out_sum, nd.len / 64, 4)};
+        out = {rng(nd.out, nd.len, 4), rng(nd.out_sum, nd.len / node_group(nd.group), 4)};
         break;
     case ABG_NODE_SWQ:
         in = {rng(nd.x, 2 * nd.len, 4)};
-        out = {rng(nd.out, nd.len, 4), rng(nd.out_sum, nd.len / 64, 4)};
+        out = {rng(nd.out, nd.len, 4), rng(nd.out_sum, nd.len / node_group(nd.group), 4)};
         break;
     default:
         in = {rng(nd.x, nd.len, 4)};
-        out = {rng(nd.out_sum, nd.len / 64, 4)};
+        out = {rng(nd.out_sum, nd.len / node_group(nd.group), 4)};
         break;
     }
 }
 
+// one grouped launch: same activation, same format, same scale/bias staging
 bool same_activation(const Q4Call &a, const Q4Call &b) {
-    return a.prologue == b.prologue && a.cols == b.cols && a.x == b.x &&
+    return a.prologue == b.prologue && a.cols == b.cols && a.x == b.x && a.group == b.group &&
+           a.sb_type == b.sb_type &&
            (a.prologue != kProNone || a.xsum == b.xsum) && (a.prologue != kProRmsq || (a.wt == b.wt && a.eps == b.eps)) &&
            sb_bulk(a) == sb_bulk(b);
 }
@@ -231,7 +254,13 @@ extern "C" {
 abg_status abg_q4mv(const uint32_t *w, const float *scale, const float *bias, const float *x, const float *xsum,
                     float *y, int64_t rows, int64_t cols, int64_t row0, int64_t n, int mode, int rows_per_warp,
                     void *stream) {
-    Q4Call c{w, scale, bias, rows, cols, row0, n, y, kProNone, x, xsum, nullptr, 0.f};
+    return abg_q4mv_ex(w, scale, bias, ABG_SB_F32, 64, x, xsum, y, rows, cols, row0, n, mode, rows_per_warp, stream);
+}
+
+abg_status abg_q4mv_ex(const uint32_t *w, const void *scale, const void *bias, int sb_type, int group, const float *x,
+                       const float *xsum, float *y, int64_t rows, int64_t cols, int64_t row0, int64_t n, int mode,
+                       int rows_per_warp, void *stream) {
+    Q4Call c{w, scale, bias, rows, cols, row0, n, y, kProNone, x, xsum, nullptr, 0.f, group, sb_type};
     abg_status st = check_q4(c, mode, rows_per_warp);
     if (st != ABG_OK || n == 0) return st;
     Q4Plan plan;
@@ -243,22 +272,36 @@ abg_status abg_q4mv(const uint32_t *w, const float *scale, const float *bias, co
 }
 
 abg_status abg_gsum(const float *v, float *s, int64_t n, int mode, void *stream) {
-    abg_status st = check_gsum(v, s, n, mode);
+    return abg_gsum_ex(v, s, n, 64, mode, stream);
+}
+
+abg_status abg_gsum_ex(const float *v, float *s, int64_t n, int group, int mode, void *stream) {
+    abg_status st = check_gsum(v, s, n, group, mode);
     if (st != ABG_OK) return st;
-    return cuda_fail(launch_gsum(v, s, n, mode == ABG_TREE, static_cast<cudaStream_t>(stream), false));
+    return cuda_fail(launch_gsum(v, s, n, group, mode == ABG_TREE, static_cast<cudaStream_t>(stream), false));
 }
 
 abg_status abg_rmsq(const float *x, const float *wt, float eps, float *xn, float *xsum, int64_t n, int mode,
                     void *stream) {
-    abg_status st = check_rmsq(x, wt, xn, xsum, n, mode);
+    return abg_rmsq_ex(x, wt, eps, xn, xsum, n, 64, mode, stream);
+}
+
+abg_status abg_rmsq_ex(const float *x, const float *wt, float eps, float *xn, float *xsum, int64_t n, int group,
+                       int mode, void *stream) {
+    abg_status st = check_rmsq(x, wt, xn, xsum, n, group, mode);
     if (st != ABG_OK) return st;
-    return cuda_fail(launch_rmsq(x, wt, eps, xn, xsum, n, mode == ABG_TREE, static_cast<cudaStream_t>(stream), false));
+    return cuda_fail(
+        launch_rmsq(x, wt, eps, xn, xsum, n, group, mode == ABG_TREE, static_cast<cudaStream_t>(stream), false));
 }
 
 abg_status abg_swq(const float *a, float *o, float *osum, int64_t n, int mode, void *stream) {
-    abg_status st = check_swq(a, o, osum, n, mode);
+    return abg_swq_ex(a, o, osum, n, 64, mode, stream);
+}
+
+abg_status abg_swq_ex(const float *a, float *o, float *osum, int64_t n, int group, int mode, void *stream) {
+    abg_status st = check_swq(a, o, osum, n, group, mode);
     if (st != ABG_OK) return st;
-    return cuda_fail(launch_swq(a, o, osum, n, mode == ABG_TREE, static_cast<cudaStream_t>(stream), false));
+    return cuda_fail(launch_swq(a, o, osum, n, group, mode == ABG_TREE, static_cast<cudaStream_t>(stream), false));
 }
 
 abg_status abg_stage_graph_create(const abg_node *nodes, int64_t count, int mode, int rows_per_warp,
@@ -275,9 +318,9 @@ abg_status abg_stage_graph_create(const abg_node *nodes, int64_t count, int mode
         abg_status st;
         switch (nd.kind) {
         case ABG_NODE_Q4MV: st = check_q4(call_of(nd), mode, rows_per_warp); break;
-        case ABG_NODE_RMSQ: st = check_rmsq(nd.x, nd.wt, nd.out, nd.out_sum, nd.len, mode); break;
-        case ABG_NODE_SWQ: st = check_swq(nd.x, nd.out, nd.out_sum, nd.len, mode); break;
-        case ABG_NODE_GSUM: st = check_gsum(nd.x, nd.out_sum, nd.len, mode); break;
+        case ABG_NODE_RMSQ: st = check_rmsq(nd.x, nd.wt, nd.out, nd.out_sum, nd.len, node_group(nd.group), mode); break;
+        case ABG_NODE_SWQ: st = check_swq(nd.x, nd.out, nd.out_sum, nd.len, node_group(nd.group), mode); break;
+        case ABG_NODE_GSUM: st = check_gsum(nd.x, nd.out_sum, nd.len, node_group(nd.group), mode); break;
         default: st = ABG_EINVAL;
         }
         if (st != ABG_OK) return st;
@@ -303,9 +346,7 @@ abg_status abg_stage_graph_create(const abg_node *nodes, int64_t count, int mode
     }
     for (int64_t i = 0; i < count; ++i) {
         if (nodes[i].kind != ABG_NODE_Q4MV || nodes[i].n == 0) continue;
-        const Q4Call c = call_of(nodes[i]);
-        const Range wr[3] = {rng(c.w, c.rows * (c.cols / 8), 4), rng(c.scale, c.rows * (c.cols / 64), 4),
-                             rng(c.bias, c.rows * (c.cols / 64), 4)};
+        const std::vector<Range> wr = q4_weights(call_of(nodes[i]));
         for (int64_t j = 0; j < count; ++j)
             for (const Range &o : outs[j])
                 for (const Range &r : wr)
@@ -343,6 +384,7 @@ abg_status abg_stage_graph_create(const abg_node *nodes, int64_t count, int mode
                 L.os = nd.out_sum;
                 L.eps = nd.eps;
                 L.len = nd.len;
+                L.group = node_group(nd.group);
             }
             launches.push_back(L);
         }

@@ -1,0 +1,6 @@
+// q4mv instantiations for one weight format: groups of 32 columns, f32 scale and bias.
+#include "q4mv_kernel.cuh"
+
+namespace abg {
+ABG_Q4MV_FORMAT_UNIT(g32, 0, false)
+}  // namespace abg

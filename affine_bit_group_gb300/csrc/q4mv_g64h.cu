@@ -1,0 +1,6 @@
+// q4mv instantiations for one weight format: groups of 64 columns, bf16 or f16 scale and bias.
+#include "q4mv_kernel.cuh"
+
+namespace abg {
+ABG_Q4MV_FORMAT_UNIT(g64h, 1, true)
+}  // namespace abg

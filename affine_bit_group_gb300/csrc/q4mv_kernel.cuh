@@ -1,0 +1,697 @@
+// q4mv kernel: affine 4-bit group-quantized matrix-vector product for sm_103a.
+// Included by each translation unit that instantiates it for a weight format.
+//
+// Source: "Array.q4mv on Metal: one kernel thread per row ..." (bendlang/bend
+// #1435, Change and Limits), "Metal: queued rmsq, swq, gdn and atq kernels and
+// a 4-row q4mv ..." (#1440, Change: bend_q4mv bullet; Why: the MLX 4-bit
+// formats) and the product, for groups of gs columns,
+//     y[r] = sum_g ( scale[r][g] * sum_j q[r][gs*g+j] * x[gs*g+j] + bias[r][g] * xsum[g] ).
+// Formats (template parameters): gs = 32 << kLg (32, 64 or 128 columns) and
+// scale/bias stored as f32 or, with kHalf, as 16-bit bf16 or f16 (chosen at
+// run time), widened to f32 exactly before use.
+//
+// Data flow (one thread block per SM slot, persistent over row tiles):
+//   warp 0 (producer)  streams tiles of whole rows -- packed words, and scale
+//                      and bias where their rows are 16-byte aligned -- from
+//                      HBM into a ring of shared-memory stages with 1-D bulk
+//                      copies (cp.async.bulk) completing on mbarriers.  The
+//                      weights are read once, so the copies carry an
+//                      evict-first L2 policy.  They start before the kernel
+//                      waits on its predecessor (programmatic dependent
+//                      launch): weights never depend on an earlier stage.
+//   warps 1..nw        wait for the predecessor, stage the activation row x
+//                      (or compute it: group sums, RMS norm or SwiGLU) in
+//                      shared memory, then work on (row block, 1024-column
+//                      chunk) items.  A warp keeps its chunk of x in registers
+//                      across items, so the activation is read from shared
+//                      memory once per kernel, not once per row.
+//
+// Per lane and row a chunk is one 16-byte word quad (32 columns).  Nibble j of
+// a word is turned into the float 2^(23-4(j%4)) + q by OR-ing an exponent into
+// the masked word (the high half-word is shifted down first), and one fused
+// multiply-add with c = -2^(23-4(j%4)) * x gives RN(q * x) exactly: the exact
+// value (2^E + q)x - 2^E x = qx is rounded once.  So the product is the
+// correctly rounded q*x that the tree order calls for, at one logic op and one
+// FMA per weight (packed two at a time with the f32x2 ops).  The identity
+// needs x finite, not -0 and |x| < 2^100; a block whose x has any other value
+// takes the plain path (convert, then multiply), which is bit-identical.
+//
+// Reduction, tree order: the lane's 32 products are summed by the pairwise
+// tree (16 packed adds carry two columns 16 apart, so every level pairs the
+// right leaves); a group of gs columns spans gs/32 lanes, and as many
+// butterfly steps (0, 1 or 2) complete its sum d; the affine term is
+// RN(RN(scale*d) + RN(bias*xsum)), and the remaining butterfly steps sum the
+// chunk's 1024/gs groups.  Chunk partials meet in shared memory, where one
+// thread per row sums them with the same tree (odd element carried).  Groups
+// past the end of the row contribute -0, which leaves every tree sum
+// unchanged.  Since every group and chunk is a power-of-two block of the
+// row, these steps are exactly the pairwise tree over the groups.
+#pragma once
+
+#include "../../include/abg.h"
+#include "abg_dev.cuh"
+#include "abg_kernels.cuh"
+
+#include <cuda_fp16.h>
+
+namespace abg {
+
+namespace {
+
+__device__ __forceinline__ float2 f2(float a, float b) { return make_float2(a, b); }
+
+// Nibble j (0..7) of a word is read at bit position 4k of the word itself
+// (j <= 4, k = j) or of the word shifted right by 12 (j >= 5, k = j - 3), so
+// it always sits inside the 23 significand bits.
+__host__ __device__ constexpr int nib_k(int j) { return j <= 4 ? j : j - 3; }
+
+// (w & mask) | c as one three-input logic op (mask an immediate).
+template <uint32_t kMask>
+__device__ __forceinline__ uint32_t and_or(uint32_t w, uint32_t c) {
+    uint32_t d;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(w), "n"(kMask), "r"(c));
+    return d;
+}
+
+// The pair of floats -(1 + q * 2^(4k-23)) for nibble J of words a and b
+// (sign and exponent of -1.0, held in `neg_one`, OR-ed onto the masked nibble).
+template <int J>
+__device__ __forceinline__ float2 neg_u2(uint32_t a, uint32_t ah, uint32_t b, uint32_t bh, uint32_t neg_one) {
+    constexpr uint32_t kMask = 0xFu << (4 * nib_k(J));
+    const uint32_t sa = (J <= 4) ? a : ah, sb = (J <= 4) ? b : bh;
+    return f2(__uint_as_float(and_or<kMask>(sa, neg_one)), __uint_as_float(and_or<kMask>(sb, neg_one)));
+}
+
+// q of nibble j as a float, exactly: (2^(23-4k) + q) - 2^(23-4k).
+__device__ __forceinline__ float q_exact(uint32_t w, uint32_t wh, int j) {
+    const int k = nib_k(j);
+    const uint32_t src = (j <= 4) ? w : wh;
+    const float v = __uint_as_float((src & (0xFu << (4 * k))) | (static_cast<uint32_t>(150 - 4 * k) << 23));
+    return __fadd_rn(v, -__uint_as_float(static_cast<uint32_t>(150 - 4 * k) << 23));
+}
+
+// 2^(23-4k) for nibble j: the factor that turns q * 2^(4k-23) back into q.
+__device__ __forceinline__ float nib_scale(int j) {
+    return __uint_as_float(static_cast<uint32_t>(150 - 4 * nib_k(j)) << 23);
+}
+
+// A stored 16-bit scale or bias widened to f32 (exact for both types).
+__device__ __forceinline__ float widen16(unsigned short h, bool f16) {
+    return f16 ? __half2float(__ushort_as_half(h)) : __uint_as_float(static_cast<uint32_t>(h) << 16);
+}
+
+// Pairwise tree over the lane's 32 products, given as P[m] = {p_m, p_(m+16)}:
+// adding P[2i] and P[2i+1] pairs leaves (2i, 2i+1) in both halves, and the
+// halves stay aligned level after level.
+__device__ __forceinline__ float tree32_pairs(float2 (&P)[16]) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) P[i] = __fadd2_rn(P[2 * i], P[2 * i + 1]);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) P[i] = __fadd2_rn(P[2 * i], P[2 * i + 1]);
+#pragma unroll
+    for (int i = 0; i < 2; ++i) P[i] = __fadd2_rn(P[2 * i], P[2 * i + 1]);
+    P[0] = __fadd2_rn(P[0], P[1]);
+    return __fadd_rn(P[0].x, P[0].y);
+}
+
+template <int M>
+__device__ __forceinline__ void exact_products(float2 (&P)[16], uint32_t w0, uint32_t h0, uint32_t w1, uint32_t h1,
+                                               uint32_t w2, uint32_t h2, uint32_t w3, uint32_t h3,
+                                               const float2 (&X)[16], uint32_t neg_one) {
+    if constexpr (M < 16) {
+        const float2 u = (M < 8) ? neg_u2<M & 7>(w0, h0, w2, h2, neg_one) : neg_u2<M & 7>(w1, h1, w3, h3, neg_one);
+        P[M] = __ffma2_rn(u, X[M], X[M]);
+        exact_products<M + 1>(P, w0, h0, w1, h1, w2, h2, w3, h3, X, neg_one);
+    }
+}
+
+// Tree sum of q*x over the lane's 32 columns of one row chunk (words wq).
+//   exact path: X[m] = {-x(m) S_m, -x(m+16) S_m} with S_m = 2^(23-4k); the
+//     product fma(-(1 + q 2^(4k-23)), -x S, -x S) = q x exactly before its one
+//     rounding, so it is RN(q*x), at one logic op and half a packed FMA per
+//     weight.
+//   plain path (activations with zeros of either sign, infinities, NaN, huge
+//     values, or a group of all-negative values): X[m] = {x(m), x(m+16)}; q is
+//     converted exactly and multiplied with scalar RN ops.  (The compiler may
+//     fuse a packed multiply into the packed add after it; the scalar
+//     __fmul_rn / __fadd_rn intrinsics are never contracted.)
+template <bool kExact>
+__device__ __forceinline__ float lane_sum32(uint4 wq, const float2 (&X)[16]) {
+    const uint32_t w0 = wq.x, w1 = wq.y, w2 = wq.z, w3 = wq.w;
+    const uint32_t h0 = w0 >> 12, h1 = w1 >> 12, h2 = w2 >> 12, h3 = w3 >> 12;
+    float2 P[16];
+    if constexpr (kExact) {
+        exact_products<0>(P, w0, h0, w1, h1, w2, h2, w3, h3, X, 0xBF800000u);
+        return tree32_pairs(P);
+    } else {
+    float p[32];
+#pragma unroll
+    for (int m = 0; m < 16; ++m) {
+        const int j = m & 7;
+        const float qa = (m < 8) ? q_exact(w0, h0, j) : q_exact(w1, h1, j);
+        const float qb = (m < 8) ? q_exact(w2, h2, j) : q_exact(w3, h3, j);
+        p[m] = __fmul_rn(qa, X[m].x);
+        p[m + 16] = __fmul_rn(qb, X[m].y);
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        P[i] = f2(__fadd_rn(p[2 * i], p[2 * i + 1]), __fadd_rn(p[16 + 2 * i], p[17 + 2 * i]));
+#pragma unroll
+    for (int i = 0; i < 4; ++i) P[i] = add2(P[2 * i], P[2 * i + 1]);
+#pragma unroll
+    for (int i = 0; i < 2; ++i) P[i] = add2(P[2 * i], P[2 * i + 1]);
+    P[0] = add2(P[0], P[1]);
+    return __fadd_rn(P[0].x, P[0].y);
+    }
+}
+
+// True when the exact path gives RN(q*x) for this activation value (finite,
+// not a zero of either sign... +0 is fine for the identity but a zero is
+// cheap to route to the plain path, and |x| < 2^100 so x * 2^23 cannot overflow).
+__device__ __forceinline__ bool x_ordinary(float v) { return fabsf(v) < 1.2676506e30f && v != 0.0f; }
+
+// Pairwise tree over 32 values in index order (scalar RN adds).
+__device__ __forceinline__ float tree32(const float (&v)[32]) {
+    float t[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) t[i] = __fadd_rn(v[2 * i], v[2 * i + 1]);
+#pragma unroll
+    for (int h = 8; h >= 1; h >>= 1)
+#pragma unroll
+        for (int i = 0; i < h; ++i) t[i] = __fadd_rn(t[2 * i], t[2 * i + 1]);
+    return t[0];
+}
+
+// The same factor computed by all computing warps of a block together: each
+// 64-value group is summed by 8 lanes (8 consecutive squares each, then a
+// 3-step butterfly: the pairwise tree over 8 blocks of 8), group sums meet in
+// shared memory, one warp takes the tree over groups (padded with -0).  Uses
+// named barrier 1 over the nct computing threads (all of them call this).
+template <bool kTree>
+__device__ float block_rms_factor(const float *__restrict__ x, int C, float eps, int cw, int nw, int lane,
+                                  float *red, float *rbox) {
+    const int G = C / 64, nct = nw * 32;
+    for (int g0 = 4 * cw; g0 < G; g0 += 4 * nw) {
+        const int g = g0 + (lane >> 3);
+        float s = kNegZero;
+        if (g < G) {
+            const float4 *p4 = reinterpret_cast<const float4 *>(x + 64 * g + 8 * (lane & 7));
+            const float4 a = p4[0], b = p4[1];
+            const float t0 = __fadd_rn(__fmul_rn(a.x, a.x), __fmul_rn(a.y, a.y));
+            const float t1 = __fadd_rn(__fmul_rn(a.z, a.z), __fmul_rn(a.w, a.w));
+            const float t2 = __fadd_rn(__fmul_rn(b.x, b.x), __fmul_rn(b.y, b.y));
+            const float t3 = __fadd_rn(__fmul_rn(b.z, b.z), __fmul_rn(b.w, b.w));
+            s = __fadd_rn(__fadd_rn(t0, t1), __fadd_rn(t2, t3));
+        }
+#pragma unroll
+        for (int d = 1; d < 8; d <<= 1) s = __fadd_rn(s, __shfl_xor_sync(0xffffffffu, s, d));
+        if (g < G && (lane & 7) == 0) red[g] = s;
+    }
+    named_bar(1, nct);
+    if (cw == 0) {
+        const float ss = warp_tree_smem(red, G);
+        if (lane == 0) {
+            float r;
+            if (kTree) {
+                const float mean = __fdiv_rn(ss, static_cast<float>(C));
+                r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(mean, eps)));
+            } else {
+                r = rsqrtf(ss / static_cast<float>(C) + eps);
+            }
+            *rbox = r;
+        }
+    }
+    named_bar(1, nct);
+    return *rbox;
+}
+
+// One warp's slice of the activation: columns ch*1024 + lane*32 + (0..31).
+struct Slice {
+    float2 X[16];  // see lane_sum32
+    float xs;      // group sum of the group the lane's columns belong to
+    bool exact;    // warp-uniform: the exact path applies to the whole slice
+};
+
+template <bool kTree, int kLg>
+__device__ __forceinline__ void load_slice(const Q4Args &a, int ch, int lane, float rms_r, Slice &sl) {
+    const int C = a.cols, base = ch * 1024 + lane * 32;
+    const bool active = base < C;
+    float v[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = 0.f;
+    if (active) {
+        const float4 *x4 = reinterpret_cast<const float4 *>(a.x + base);
+        if (a.prologue == kProNone || a.prologue == kProGsum) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float4 q = x4[i];
+                v[4 * i] = q.x, v[4 * i + 1] = q.y, v[4 * i + 2] = q.z, v[4 * i + 3] = q.w;
+            }
+        } else if (a.prologue == kProRmsq) {
+            const float4 *w4 = reinterpret_cast<const float4 *>(a.wt + base);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float4 q = x4[i], w = w4[i];
+                v[4 * i] = __fmul_rn(__fmul_rn(q.x, rms_r), w.x);
+                v[4 * i + 1] = __fmul_rn(__fmul_rn(q.y, rms_r), w.y);
+                v[4 * i + 2] = __fmul_rn(__fmul_rn(q.z, rms_r), w.z);
+                v[4 * i + 3] = __fmul_rn(__fmul_rn(q.w, rms_r), w.w);
+            }
+        } else {  // kProSwq: x = [gate | up]
+            const float4 *u4 = reinterpret_cast<const float4 *>(a.x + C + base);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float4 g = x4[i], u = u4[i];
+                v[4 * i] = swiglu<kTree>(g.x, u.x);
+                v[4 * i + 1] = swiglu<kTree>(g.y, u.y);
+                v[4 * i + 2] = swiglu<kTree>(g.z, u.z);
+                v[4 * i + 3] = swiglu<kTree>(g.w, u.w);
+            }
+        }
+    }
+    // special values, and groups whose values are all negative (there the
+    // exact path's q = 0 products would be +0 where RN(0 * x) is -0, and a
+    // whole group of them could leave -0 in the sum)
+    bool sp = false, allneg = true;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        sp |= !x_ordinary(v[i]);
+        allneg &= v[i] < 0.f;
+    }
+    if (!active) sp = false, allneg = false;
+    // a group spans 1 << kLg lanes; every lane takes part in the shuffles (a
+    // full-mask shuffle that only some lanes reach, e.g. behind a
+    // short-circuit &&, stalls the warp for good)
+    int grpneg = allneg ? 1 : 0;
+#pragma unroll
+    for (int d = 1; d < (1 << kLg); d <<= 1) grpneg &= __shfl_xor_sync(0xffffffffu, grpneg, d);
+    sl.exact = !__any_sync(0xffffffffu, sp || grpneg != 0);
+    // group sum of the lane's group: given, or the tree over the slice's values
+    // completed across the group's lanes
+    if (a.prologue == kProNone) {
+        sl.xs = active ? a.xsum[ch * (32 >> kLg) + (lane >> kLg)] : 0.f;
+    } else {
+        float t = kTree ? tree32(v) : [&] {
+            float s = 0.f;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) s += v[i];
+            return s;
+        }();
+#pragma unroll
+        for (int d = 1; d < (1 << kLg); d <<= 1) {
+            const float o = __shfl_xor_sync(0xffffffffu, t, d);
+            t = kTree ? __fadd_rn(t, o) : t + o;
+        }
+        sl.xs = t;
+    }
+#pragma unroll
+    for (int m = 0; m < 16; ++m) {
+        if (sl.exact) {
+            const float s = -nib_scale(m & 7);
+            sl.X[m] = f2(__fmul_rn(v[m], s), __fmul_rn(v[m + 16], s));
+        } else {
+            sl.X[m] = f2(v[m], v[m + 16]);
+        }
+    }
+}
+
+// Locates tiles of a grouped launch.  A block visits its tiles in increasing
+// order, so the problem index only moves forward.
+// Tile counts fit in 32 bits (the planner checks the launch's total).
+struct ProbCursor {
+    int p = 0;
+    int base = 0;  // first tile of problem p
+    __device__ __forceinline__ int find(const Q4Args &a, int t, int &tile) {
+        while (p + 1 < a.nprob && t >= base + static_cast<int>(a.prob[p].tiles)) {
+            base += static_cast<int>(a.prob[p].tiles);
+            ++p;
+        }
+        tile = t - base;
+        return p;
+    }
+};
+
+// Bounded mbarrier wait that also gives up when another warp has aborted.
+// On a timeout it sets the timeout bit plus `site` (which wait gave up).  The
+// abort flag and the clock are looked at every 16th poll (a poll suspends the
+// warp for at most the sleep hint), which keeps short waits cheap.
+__device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                              unsigned site) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = globaltimer();
+    for (unsigned i = 1;; ++i) {
+        if (mbar_try_wait_sleep(bar, parity, kSleepHintNs)) return true;
+        if ((i & 15u) == 0) {
+            if (*abort_flag) return false;
+            if (globaltimer() - t0 > kWaitLimitNs) {
+                atomicOr(&g_status, kStatusTimeout | site);
+                *abort_flag = 1;
+                return false;
+            }
+        }
+    }
+}
+// wait sites recorded in the status word
+constexpr unsigned kSiteEmpty = 1u << 4, kSiteFull = 1u << 5, kSiteDone = 1u << 6;
+
+// One step of a transposed butterfly over N values (N -> N/2): lanes whose
+// `d` bit is clear keep the first half and send the second, their partners
+// the other way round, so each lane adds N/2 pairs with N/2 shuffles.  The
+// sums pair the same two leaves as a plain butterfly step.
+template <int N, bool kTree>
+__device__ __forceinline__ void tstep(float (&v)[N], int d, bool hi) {
+#pragma unroll
+    for (int i = 0; i < N / 2; ++i) {
+        const float send = hi ? v[i] : v[N / 2 + i];
+        const float keep = hi ? v[N / 2 + i] : v[i];
+        const float recv = __shfl_xor_sync(0xffffffffu, send, d);
+        v[i] = kTree ? __fadd_rn(keep, recv) : keep + recv;
+    }
+}
+
+// Values a lane still holds after the butterfly levels at distances D, 2D,
+// ... below E, starting from N (each transposed step halves them).
+template <int N, int D, int E>
+__host__ __device__ constexpr int lv_count() {
+    if constexpr (D >= E || N == 1) {
+        return N;
+    } else {
+        return lv_count<N / 2, 2 * D, E>();
+    }
+}
+
+// Butterfly levels at distances D, 2D, ... below E over N held values: while
+// N > 1 each level is a transposed step (the lane keeps the half selected by
+// its distance bit, and rowsel records the offset of the rows it keeps);
+// then plain butterfly steps.
+template <int N, int D, int E, bool kTree>
+__device__ __forceinline__ void levels(float (&v)[N], float (&out)[lv_count<N, D, E>()], int lane, int &rowsel) {
+    if constexpr (D >= E) {
+#pragma unroll
+        for (int i = 0; i < N; ++i) out[i] = v[i];
+    } else if constexpr (N == 1) {
+        float val = v[0];
+#pragma unroll
+        for (int dd = D; dd < E; dd <<= 1) {
+            const float o = __shfl_xor_sync(0xffffffffu, val, dd);
+            val = kTree ? __fadd_rn(val, o) : val + o;
+        }
+        out[0] = val;
+    } else {
+        const bool hi = (lane & D) != 0;
+        tstep<N, kTree>(v, D, hi);
+        rowsel += hi ? N / 2 : 0;
+        float w[N / 2];
+#pragma unroll
+        for (int i = 0; i < N / 2; ++i) w[i] = v[i];
+        levels<N / 2, 2 * D, E, kTree>(w, out, lane, rowsel);
+    }
+}
+
+// Partial-sum buffers (and their barriers) rotate over 4 tiles: a warp writes
+// a tile's buffer only after every warp has finished the final sums of the
+// tile four back.
+constexpr int kParts = 4;
+
+// Block layouts (the register file is split over the SM's four schedulers,
+// so the warps per SM set the registers per thread):
+//   kLayout 0: up to 8 computing warps, two blocks per SM (96 registers);
+//   kLayout 1: up to 16 computing warps, one block per SM;
+//   kLayout 2: up to 6 computing warps, two blocks per SM (128 registers).
+// With two blocks per SM the next launch of a chain can start beside this one.
+constexpr int layout_threads(int l) { return l == 1 ? 544 : (l == 2 ? 224 : 288); }
+constexpr int layout_blocks(int l) { return l == 1 ? 1 : 2; }
+
+template <int R, bool kTree, bool kSbSmem, int kLayout, int kLg, bool kHalf>
+__global__ void __launch_bounds__(layout_threads(kLayout), layout_blocks(kLayout))
+    q4mv_kernel(const __grid_constant__ Q4Args a) {
+    constexpr int kL = 1 << kLg;                  // lanes per group
+    constexpr uint32_t kElem = kHalf ? 2u : 4u;   // bytes per stored scale or bias
+    extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ volatile int s_abort;
+    __shared__ float s_red[ABG_MAX_COLS / 64];  // group sums of squares (RMS-norm prologue)
+    __shared__ float s_rbox;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + a.off_bar);
+    uint64_t *empty = full + a.stages;
+    uint64_t *done = empty + a.stages;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int S = a.stages, TR = a.tile_rows, W = a.W, G = a.G, nch = a.nch, nw = a.nw;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], nw);
+        }
+        for (int i = 0; i < kParts; ++i) mbar_init(&done[i], nw);
+        s_abort = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    // Programmatic dependent launch.  When the activation comes from the
+    // preceding launch (wait_first), the first S tiles of weights are fetched
+    // before waiting for it (weights never depend on it) and every thread
+    // signals its dependents only after that wait has returned.  A sibling
+    // launch of the same stage signals at once, computes, and waits for its
+    // predecessor only before exiting.
+    const bool wait_first = a.wait_first != 0;
+    if (!wait_first) grid_dep_launch();
+    if (warp == 0) {
+        // ------------------------------------------------ producer warp ----
+        if (lane != 0) return;
+        const uint64_t policy = l2_evict_first();
+        bool released = !wait_first;
+        ProbCursor cur;
+        const int total = static_cast<int>(a.total_tiles);
+        int k = 0;
+        for (int t = blockIdx.x; t < total; t += gridDim.x, ++k) {
+            const int s = k % S;
+            if (k == S) {
+                grid_dep_wait();
+                grid_dep_launch();
+                released = true;
+            }
+            if (k >= S && !wait_or_abort(&empty[s], static_cast<uint32_t>(((k / S) & 1) ^ 1), &s_abort, kSiteEmpty))
+                break;
+            if (s_abort) break;
+            int tile;
+            const Q4Prob &P = a.prob[cur.find(a, t, tile)];
+            const int64_t r0 = static_cast<int64_t>(tile) * TR;
+            const int rows = static_cast<int>(min(static_cast<int64_t>(TR), P.n - r0));
+            unsigned char *st = smem + a.off_stage + static_cast<size_t>(s) * a.stage_bytes;
+            const uint32_t wb = static_cast<uint32_t>(rows) * W * 4u;
+            const uint32_t sbb = kSbSmem ? static_cast<uint32_t>(rows) * G * kElem : 0u;
+            mbar_arrive_expect_tx(&full[s], wb + 2 * sbb);
+            bulk_g2s(st, P.w + r0 * W, wb, &full[s], policy);
+            if (kSbSmem) {
+                const size_t sbo = static_cast<size_t>(r0) * G * kElem;
+                bulk_g2s(st + a.stage_w_bytes, static_cast<const unsigned char *>(P.scale) + sbo, sbb, &full[s],
+                         policy);
+                bulk_g2s(st + a.stage_w_bytes + a.stage_sb_bytes, static_cast<const unsigned char *>(P.bias) + sbo,
+                         sbb, &full[s], policy);
+            }
+        }
+        if (!released) {
+            grid_dep_wait();
+            grid_dep_launch();
+        }
+        // Drain: the block may not exit while a copy into its shared memory is
+        // in flight.  Waiting on a phase that already completed returns at once.
+        for (int j = max(0, k - S); j < k; ++j) mbar_wait(&full[j % S], static_cast<uint32_t>((j / S) & 1));
+        return;
+    }
+
+    // ---------------------------------------------------- consumer warps ----
+    const int ct = threadIdx.x - 32, cw = warp - 1;
+    float *part = reinterpret_cast<float *>(smem + a.off_part);
+    // chunk positions and row blocks of this warp
+    const bool fixed_ch = nch <= nw;
+    const int kk = fixed_ch ? nw / nch : 1;
+    const bool idle = fixed_ch && cw >= nch * kk;
+    const int ch0 = fixed_ch ? cw % nch : cw;
+    const int rb0 = fixed_ch ? cw / nch : 0;
+    const int chstep = fixed_ch ? nch : nw;
+
+    if (wait_first) {
+        grid_dep_wait();
+        grid_dep_launch();
+    }
+    float rms_r = 0.f;
+    if (a.prologue == kProRmsq) rms_r = block_rms_factor<kTree>(a.x, a.cols, a.eps, cw, nw, lane, s_red, &s_rbox);
+    const bool f16 = a.sb_f16 != 0;
+    // stored scale or bias i of a row block, from the stage or from global memory
+    auto sb_at = [&](const void *base, int64_t i) -> float {
+        if constexpr (kHalf) {
+            const unsigned short h = kSbSmem ? static_cast<const unsigned short *>(base)[i]
+                                             : __ldg(static_cast<const unsigned short *>(base) + i);
+            return widen16(h, f16);
+        } else {
+            return kSbSmem ? static_cast<const float *>(base)[i] : __ldg(static_cast<const float *>(base) + i);
+        }
+    };
+    Slice sl;
+    int cur_ch = -1;
+    // Final sums of tile j: thread ct adds row ct's chunk partials by the tree.
+    ProbCursor cur, fcur;
+    auto finish = [&](int j, int tj) -> bool {
+        const int pi = j % kParts;
+        if (!wait_or_abort(&done[pi], static_cast<uint32_t>((j / kParts) & 1), &s_abort, kSiteDone)) return false;
+        int tile;
+        const Q4Prob &P = a.prob[fcur.find(a, tj, tile)];
+        const int64_t r0 = static_cast<int64_t>(tile) * TR;
+        const int rows = static_cast<int>(min(static_cast<int64_t>(TR), P.n - r0));
+        if (ct < rows) {
+            float *pr = part + (static_cast<size_t>(pi) * TR + ct) * nch;
+            int m = nch;
+            while (m > 1) {
+                const int h = m >> 1;
+                for (int i = 0; i < h; ++i) pr[i] = kTree ? __fadd_rn(pr[2 * i], pr[2 * i + 1]) : pr[2 * i] + pr[2 * i + 1];
+                if (m & 1) pr[h] = pr[m - 1];
+                m = h + (m & 1);
+            }
+            P.y[r0 + ct] = pr[0];
+        }
+        return true;
+    };
+
+    const int total = static_cast<int>(a.total_tiles);
+    int k = 0, tprev = -1;
+    for (int t = blockIdx.x; t < total; t += gridDim.x, ++k) {
+        const int s = k % S;
+        if (!wait_or_abort(&full[s], static_cast<uint32_t>((k / S) & 1), &s_abort, kSiteFull)) break;
+        int tile;
+        const Q4Prob &P = a.prob[cur.find(a, t, tile)];
+        const int64_t r0 = static_cast<int64_t>(tile) * TR;
+        const int rows = static_cast<int>(min(static_cast<int64_t>(TR), P.n - r0));
+        const unsigned char *stg = smem + a.off_stage + static_cast<size_t>(s) * a.stage_bytes;
+        const uint4 *sw = reinterpret_cast<const uint4 *>(stg);
+        const void *ssc = stg + a.stage_w_bytes;
+        const void *sbi = stg + a.stage_w_bytes + a.stage_sb_bytes;
+        float *prt = part + static_cast<size_t>(k % kParts) * TR * nch;
+        const int nrb = (rows + R - 1) / R;
+        if (!idle) {
+            for (int ch = ch0; ch < nch; ch += chstep) {
+                if (ch != cur_ch) {
+                    load_slice<kTree, kLg>(a, ch, lane, rms_r, sl);
+                    cur_ch = ch;
+                }
+                const bool active = (ch * 1024 + lane * 32) < a.cols;
+                // this lane's group, and its 16-byte column quad in row 0 of
+                // the stage; lanes past the row end (last chunk only) read
+                // group 0 and row 0's first quad instead, and add -0
+                const int g = active ? ch * (32 >> kLg) + (lane >> kLg) : 0;
+                const uint4 *wl = sw + (active ? ch * 32 + lane : 0);
+                const int wq_stride = W / 4;
+                for (int rb = rb0; rb < nrb; rb += kk) {
+                    // lane sums of R rows, four rows at a time: their loads
+                    // first, then the arithmetic.  Rows past the end of a
+                    // ragged last tile are still inside the stage (a tile has
+                    // a multiple of R rows of room): they are summed from
+                    // stale words and discarded.
+                    float v[R];
+                    constexpr int B = (R < 4) ? R : 4;
+                    const uint4 *wr = wl + rb * R * wq_stride;
+#pragma unroll
+                    for (int bq = 0; bq < R; bq += B) {
+                        uint4 wq[B];
+#pragma unroll
+                        for (int r = 0; r < B; ++r) wq[r] = wr[(bq + r) * wq_stride];
+                        if (sl.exact) {
+#pragma unroll
+                            for (int r = 0; r < B; ++r) v[bq + r] = lane_sum32<true>(wq[r], sl.X);
+                        } else {
+#pragma unroll
+                            for (int r = 0; r < B; ++r) v[bq + r] = lane_sum32<false>(wq[r], sl.X);
+                        }
+                    }
+                    // group completion over the group's kL lanes, transposed
+                    // while more than one row is held: this lane keeps the
+                    // group sums d of rows [ofs, ofs + H)
+                    constexpr int H = lv_count<R, 1, kL>();
+                    int rowsel = 0;
+                    float d[H];
+                    levels<R, 1, kL, kTree>(v, d, lane, rowsel);
+                    const int ofs = rowsel;
+                    // affine term per (row, group); groups past the row end add
+                    // -0.  Branch-free: rows past a ragged tile's end read the
+                    // stage's stale scale and bias (or, from global memory,
+                    // the tile's last row) and are discarded.
+                    float tv[H];
+#pragma unroll
+                    for (int i = 0; i < H; ++i) {
+                        const int row = rb * R + ofs + i;
+                        const int64_t idx = kSbSmem ? static_cast<int64_t>(row * G + g)
+                                                    : (r0 + min(row, rows - 1)) * G + g;
+                        const float sc = sb_at(kSbSmem ? ssc : P.scale, idx);
+                        const float bi = sb_at(kSbSmem ? sbi : P.bias, idx);
+                        const float t = kTree ? __fadd_rn(__fmul_rn(sc, d[i]), __fmul_rn(bi, sl.xs))
+                                              : fmaf(sc, d[i], bi * sl.xs);
+                        tv[i] = active ? t : kNegZero;
+                    }
+                    // the chunk's groups: butterfly over distances kL..16,
+                    // transposed while more than one row is held
+                    float fin[1];
+                    levels<H, kL, 32, kTree>(tv, fin, lane, rowsel);
+                    const float val = fin[0];
+                    // lanes 0..R-1 hold the R rows (row rb*R + rowsel)
+                    const int row = rb * R + rowsel;
+                    if (lane < R && row < rows) prt[row * nch + ch] = val;
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0) {
+            mbar_arrive(&empty[s]);       // weights of this stage no longer needed
+            mbar_arrive(&done[k % kParts]);  // this warp's partials are written
+        }
+        if (tprev >= 0 && !finish(k - 1, tprev)) break;
+        tprev = t;
+    }
+    if (tprev >= 0) finish(k - 1, tprev);
+    if (!wait_first) grid_dep_wait();
+}
+
+// Kernel entry for one instantiation, as an untyped pointer.
+template <int R, bool kTree, bool kSb, int kLayout, int kLg, bool kHalf>
+void *kernel_ptr() {
+    return reinterpret_cast<void *>(&q4mv_kernel<R, kTree, kSb, kLayout, kLg, kHalf>);
+}
+
+// Layout-0 instantiations of one format for rows per item 1, 2, 4 or 8.
+template <int kLg, bool kHalf>
+void *select_layout0(int R, bool tree, bool sb) {
+#define ABG_SEL(RR)                                                                                              \
+    if (R == RR) {                                                                                               \
+        if (tree) return sb ? kernel_ptr<RR, true, true, 0, kLg, kHalf>() : kernel_ptr<RR, true, false, 0, kLg, kHalf>(); \
+        return sb ? kernel_ptr<RR, false, true, 0, kLg, kHalf>() : kernel_ptr<RR, false, false, 0, kLg, kHalf>();        \
+    }
+    ABG_SEL(1)
+    ABG_SEL(2)
+    ABG_SEL(4)
+    ABG_SEL(8)
+#undef ABG_SEL
+    return nullptr;
+}
+
+// This translation unit's device status word (OR-ed into *bits).  Internal
+// linkage: every unit that includes this header has its own word.
+cudaError_t read_status_word(unsigned *bits, bool clear) {
+    unsigned v = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&v, g_status, sizeof v);
+    if (e == cudaSuccess && clear && v) {
+        const unsigned z = 0;
+        e = cudaMemcpyToSymbol(g_status, &z, sizeof z);
+    }
+    *bits |= v;
+    return e;
+}
+
+}  // namespace
+
+// Defines the kernel selector and status reader of a unit that instantiates
+// one format (block layout 0).
+#define ABG_Q4MV_FORMAT_UNIT(tag, lg, half)                                                        \
+    void *q4mv_select_##tag(int R, bool tree, bool sb) { return select_layout0<lg, half>(R, tree, sb); } \
+    cudaError_t q4mv_status_##tag(unsigned *bits, bool clear) { return read_status_word(bits, clear); }
+
+}  // namespace abg

@@ -12,8 +12,10 @@ weights from HBM.
 
 Also measured in the same run (as "extra"): the same 400 products as 400
 dependent stages (each waits for the previous one: decode-like latency), the
-248320x2048 output head, and one synthetic 24-layer decode token (fused and
-unfused stage graphs).
+248320x2048 output head, one synthetic 24-layer decode token (fused and
+unfused stage graphs), and the 4096x2048 product in every weight format
+(groups of 32, 64 or 128 columns; f32, bf16 or f16 scale and bias), each as a
+grouped launch of 64 products streaming from HBM.
 
 Output: one JSON line on rank 0.  --impl reference times the CPU oracle (the
 plain C definition the library is tested against) on the same workload.
@@ -45,9 +47,10 @@ MID_ROWS, MID_COLS = 4096, 2048
 PEAK_FALLBACK_GBS = 6800.0
 
 
-def product_bytes(rows: int, cols: int) -> int:
+def product_bytes(rows: int, cols: int, group: int = 64, sb_bytes: int = 4) -> int:
     """Algorithmic bytes of one product: nibbles, scale and bias, x, xsum and y."""
-    return rows * cols // 2 + 8 * rows * (cols // 64) + 4 * cols + 4 * (cols // 64) + 4 * rows
+    G = cols // group
+    return rows * cols // 2 + 2 * sb_bytes * rows * G + 4 * cols + 4 * G + 4 * rows
 
 
 def measured_peak():
@@ -257,6 +260,7 @@ def run_ours(args, rank, world):
     if not args.no_extra:
         extra["head"] = bench_head(abg, stream, args, peak)
         extra["decode_token"] = bench_decode(abg, decode, stream, args)
+        extra["formats"] = bench_formats(abg, stream, args, peak, l2)
 
     res = dict(value=value, ms_step=ms_step, us_per_product=us_per_product, achieved=achieved,
                launch_us=ms_launch * 1e3, clocks=clocks,
@@ -287,6 +291,44 @@ def bench_head(abg, stream, args, peak):
     gbs = product_bytes(rows, cols) / (us * 1e-6) / 1e9
     return {"workload": "q4mv 248320x2048 output head, x = rmsq(hidden), 20 products per replay",
             "us_per_product": us, "gbs": gbs, "frac_of_measured_peak": gbs / peak}
+
+
+def bench_formats(abg, stream, args, peak, l2):
+    """The 4096x2048 product in each format: one grouped launch of 64 products,
+    each on its own copy of the weights (the copies total several times L2)."""
+    import torch
+
+    import oracle
+    out = {"workload": "q4mv 4096x2048, one grouped launch of 64 products per replay, weights from HBM"}
+    for group in synth.GROUPS:
+        for sb in synth.SB_TYPES:
+            m, x_np = synth.fmt_case(group, sb, MID_ROWS, MID_COLS)
+            sbb = 4 if sb == "f32" else 2
+            pb = product_bytes(MID_ROWS, MID_COLS, group, sbb)
+            copies = max(2, math.ceil(3 * l2 / m.nbytes))
+            w = torch.from_numpy(m.w.view(np.int32)).cuda()
+            sc = torch.from_numpy(m.scale.view(np.int16) if sbb == 2 else m.scale).cuda()
+            bi = torch.from_numpy(m.bias.view(np.int16) if sbb == 2 else m.bias).cuda()
+            mats = [(w.clone(), sc.clone(), bi.clone()) for _ in range(copies)]
+            x = torch.from_numpy(x_np).cuda()
+            xs = torch.empty(MID_COLS // group, dtype=torch.float32, device="cuda")
+            ys = [torch.empty(MID_ROWS, dtype=torch.float32, device="cuda") for _ in range(GROUP)]
+            abg.gsum(x, xs, group=group)
+            g = abg.StageGraph([abg.Node.q4mv(0, *mats[i % copies], ys[i], MID_COLS, x=x, xsum=xs, group=group,
+                                              sb_type=sb) for i in range(GROUP)], keep=[x, xs] + ys)
+            ms, _ = time_graph(g, stream, max(args.steps, 10), args.warmup, False)
+            g.close()
+            got = oracle.hash32(ys[GROUP - 1].cpu().numpy())
+            exp = oracle.hash32(oracle.q4mv_ex(*m.arrays(), sb, group, x_np, oracle.gsum_ex(x_np, group), MID_COLS))
+            if got != exp:
+                raise SystemExit(f"format g{group} {sb}: hash {got} differs from the oracle's {exp}")
+            us = ms * 1e3 / GROUP
+            gbs = GROUP * pb / (ms * 1e-3) / 1e9
+            out[f"g{group}_{sb}"] = {"us_per_product": round(us, 3), "gbs": round(gbs, 1),
+                                     "frac_of_measured_peak": round(gbs / peak, 3), "bytes_per_product": pb}
+            del mats, g, w, sc, bi
+            torch.cuda.empty_cache()
+    return out
 
 
 def bench_decode(abg, decode, stream, args):
@@ -386,7 +428,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-extra", action="store_true", help="skip the head and decode-token measurements")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
-    ap.add_argument("--only", choices=["head", "decode"], default=None,
+    ap.add_argument("--only", choices=["head", "decode", "formats"], default=None,
                     help="run one secondary workload alone and print its numbers (for profiling)")
     args = ap.parse_args()
     if args.only:
@@ -396,7 +438,13 @@ def main():
         from affine_bit_group_gb300 import decode
         stream = torch.cuda.Stream()
         peak, _ = measured_peak()
-        out = bench_head(abg, stream, args, peak) if args.only == "head" else bench_decode(abg, decode, stream, args)
+        if args.only == "head":
+            out = bench_head(abg, stream, args, peak)
+        elif args.only == "decode":
+            out = bench_decode(abg, decode, stream, args)
+        else:
+            l2 = getattr(torch.cuda.get_device_properties(0), "L2_cache_size", 126 * 2 ** 20)
+            out = bench_formats(abg, stream, args, peak, l2)
         print(json.dumps(out), flush=True)
         return
     rank = int(os.environ.get("RANK", 0))
@@ -415,7 +463,7 @@ def main():
     if rank != 0:
         return
     value = job_value(ms_step, world)
-    kernel_src = os.path.join(ROOT, "affine_bit_group_gb300", "csrc", "q4mv.cu")
+    kernel_src = os.path.join(ROOT, "affine_bit_group_gb300", "csrc", "q4mv_kernel.cuh")
     traffic = profile_traffic(kernel_src, "q4mv_mid_4096x2048.md")
     line = {
         "metric": "q4mv achieved HBM GB/s", "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,

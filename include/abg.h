@@ -72,6 +72,12 @@ typedef enum {
 
 typedef enum { ABG_TREE = 0, ABG_FAST = 1 } abg_mode;
 
+/* Storage type of scale and bias ([fused-token] Why: the MLX 4-bit formats).
+ * 16-bit values are widened to f32 exactly before use (bf16: the upper half
+ * of an f32; f16: IEEE binary16), so the arithmetic is the same as for f32
+ * storage of the widened values. */
+typedef enum { ABG_SB_F32 = 0, ABG_SB_BF16 = 1, ABG_SB_F16 = 2 } abg_sb_type;
+
 /* Largest `cols` a product accepts: the activation row is staged once per
  * thread block in shared memory. */
 #define ABG_MAX_COLS 16384
@@ -102,11 +108,37 @@ abg_status abg_q4mv(const uint32_t *w, const float *scale, const float *bias,
                     int mode, int rows_per_warp, void *stream);
 
 /*
+ * q4mv_ex: the same product for the other MLX 4-bit formats ([fused-token]
+ * Why): groups of `group` columns (32, 64 or 128) and scale/bias stored as
+ * `sb_type` (abg_sb_type).
+ *
+ *     y[r] = sum_g ( scale[r][g] * sum_j q[r][group*g+j] * x[group*g+j]
+ *                    + bias[r][g] * xsum[g] ),   g < cols/group,
+ *
+ * with the same tree order and rounding as abg_q4mv (which is this call with
+ * group 64 and ABG_SB_F32).
+ *   scale, bias  [rows][cols/group] of f32, or of 16-bit bf16 / f16 patterns;
+ *                aligned to their element size (4 or 2 bytes)
+ *   xsum   f32 [cols/group]   xsum[g] = tree sum of x[group*g .. group*g+group-1]
+ *   cols   a positive multiple of 64 and of group, at most ABG_MAX_COLS
+ * scale and bias rows are streamed with bulk copies when both pointers are
+ * 16-byte aligned and a row of them is a multiple of 16 bytes.  Other
+ * arguments and errors as abg_q4mv; a bad group or sb_type is ABG_EINVAL.
+ */
+abg_status abg_q4mv_ex(const uint32_t *w, const void *scale, const void *bias, int sb_type, int group,
+                       const float *x, const float *xsum, float *y,
+                       int64_t rows, int64_t cols, int64_t row0, int64_t n,
+                       int mode, int rows_per_warp, void *stream);
+
+/*
  * gsum: s[g] = tree sum of v[64g .. 64g+63], g < n/64.  The group sums a
  * product reads for its bias term ([fused-token] Change, Array.rmsq bullet:
  * "the 64-value group sums that Array.q4mv reads").  n a positive multiple of 64.
  */
 abg_status abg_gsum(const float *v, float *s, int64_t n, int mode, void *stream);
+/* gsum_ex: s[g] = tree sum of v[group*g .. group*g+group-1], group 32, 64 or
+ * 128; n a positive multiple of 64 and of group. */
+abg_status abg_gsum_ex(const float *v, float *s, int64_t n, int group, int mode, void *stream);
 
 /*
  * rmsq: RMS norm with weights plus the group sums of its output
@@ -120,6 +152,12 @@ abg_status abg_gsum(const float *v, float *s, int64_t n, int mode, void *stream)
  */
 abg_status abg_rmsq(const float *x, const float *wt, float eps, float *xn, float *xsum,
                     int64_t n, int mode, void *stream);
+/* rmsq_ex: the same with xsum over groups of `group` values (32, 64 or 128;
+ * xsum f32 [n/group]; n also a multiple of group).  The norm factor does not
+ * depend on the group size: the two-level tree of squares is the pairwise tree
+ * over all n values. */
+abg_status abg_rmsq_ex(const float *x, const float *wt, float eps, float *xn, float *xsum,
+                       int64_t n, int group, int mode, void *stream);
 
 /*
  * swq: SwiGLU plus the group sums of its output ([fused-token] Change,
@@ -134,6 +172,9 @@ abg_status abg_rmsq(const float *x, const float *wt, float eps, float *xn, float
  * of 64.
  */
 abg_status abg_swq(const float *a, float *o, float *osum, int64_t n, int mode, void *stream);
+/* swq_ex: the same with osum over groups of `group` values (32, 64 or 128;
+ * osum f32 [n/group]; n also a multiple of group). */
+abg_status abg_swq_ex(const float *a, float *o, float *osum, int64_t n, int group, int mode, void *stream);
 
 /* ---------------------------------------------------------------------------
  * Stage graph: one decode token's dependent stages recorded into one CUDA
@@ -165,6 +206,11 @@ abg_status abg_swq(const float *a, float *o, float *osum, int64_t n, int mode, v
  *   ABG_NODE_RMSQ  x, wt, eps, len -> out (xn), out_sum (xsum)
  *   ABG_NODE_SWQ   x (2*len), len -> out (o), out_sum (osum)
  *   ABG_NODE_GSUM  x, len -> out_sum
+ * Every kind also reads `group` (0 means 64): the group size of the product's
+ * scale, bias and xsum (Q4MV, including the group sums its prologue
+ * computes) or of out_sum (RMSQ, SWQ, GSUM); Q4MV reads `sb_type` (an
+ * abg_sb_type; scale and bias then point at that type).  Sizes given above
+ * as cols/64 or len/64 are cols/group and len/group.
  * ------------------------------------------------------------------------- */
 typedef enum { ABG_NODE_Q4MV = 0, ABG_NODE_RMSQ = 1, ABG_NODE_SWQ = 2, ABG_NODE_GSUM = 3 } abg_node_kind;
 typedef enum { ABG_PRO_NONE = 0, ABG_PRO_GSUM = 1, ABG_PRO_RMSQ = 2, ABG_PRO_SWQ = 3 } abg_prologue;
@@ -173,8 +219,8 @@ typedef struct abg_node {
     int32_t kind;      /* abg_node_kind */
     int32_t stage;     /* stage index; any order, grouped by value */
     const uint32_t *w; /* Q4MV */
-    const float *scale;
-    const float *bias;
+    const void *scale; /* f32, or 16-bit patterns (sb_type) */
+    const void *bias;
     int64_t rows, cols, row0, n;
     float *y;
     int32_t prologue;  /* abg_prologue, Q4MV only */
@@ -185,6 +231,8 @@ typedef struct abg_node {
     float *out;        /* RMSQ, SWQ */
     float *out_sum;    /* RMSQ, SWQ, GSUM */
     int64_t len;       /* RMSQ, SWQ, GSUM vector length n */
+    int32_t group;     /* group size 32, 64 or 128; 0 = 64 */
+    int32_t sb_type;   /* Q4MV: abg_sb_type of scale and bias */
 } abg_node;
 
 /* Validates every node (same rules as the single calls), checks that no node

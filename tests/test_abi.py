@@ -88,6 +88,38 @@ def test_q4mv_validation(lib):
     assert q4(lib, n=0, row0=8) == OK                 # empty: nothing enqueued, no device use
 
 
+def q4x(lib, sb=0, group=64, w=A, s=A + 0x100000, b=A + 0x200000, x=A + 0x300000, xs=A + 0x310000, y=A + 0x400000,
+        rows=8, cols=256, row0=0, n=8, mode=0, rpw=0):
+    return lib.abg_q4mv_ex(w, s, b, sb, group, x, xs, y, rows, cols, row0, n, mode, rpw, None)
+
+
+def test_q4mv_ex_validation(lib):
+    assert q4x(lib, group=16) == EINVAL
+    assert q4x(lib, group=0) == EINVAL
+    assert q4x(lib, sb=3) == EINVAL
+    assert q4x(lib, sb=-1) == EINVAL
+    assert q4x(lib, group=128, cols=192) == ESHAPE     # not whole 128-column groups
+    assert q4x(lib, group=32, cols=96) == ESHAPE       # whole groups but not a multiple of 64
+    assert q4x(lib, sb=1, s=A + 0x100001) == EALIGN    # 16-bit scale must be 2-byte aligned
+    assert q4x(lib, sb=0, s=A + 0x100002) == EALIGN    # f32 scale must be 4-byte aligned
+    assert q4x(lib, sb=1, s=A + 0x100002, y=0) == EINVAL  # 2-byte aligned 16-bit scale passes the alignment check
+    # y overlapping the bias: bias spans rows*cols/group elements of the stored type
+    assert q4x(lib, sb=0, group=32, y=A + 0x200000 + 4 * (8 * 8 - 1)) == EALIAS
+    assert q4x(lib, sb=2, group=32, y=A + 0x200000 + 2 * (8 * 8 - 2)) == EALIAS   # last 4 bytes of the bias
+    assert q4x(lib, n=0, row0=8, group=128, sb=1) == OK
+
+
+def test_vector_ex_validation(lib):
+    assert lib.abg_gsum_ex(A, A + 0x1000, 128, 16, 0, None) == EINVAL
+    assert lib.abg_gsum_ex(A, A + 0x1000, 192, 128, 0, None) == ESHAPE
+    assert lib.abg_gsum_ex(A, A + 4 * 127, 128, 32, 0, None) == EALIAS
+    assert lib.abg_rmsq_ex(A, A + 0x1000, ctypes.c_float(1e-6), A + 0x2000, A + 0x3000, 64, 128, 0, None) == ESHAPE
+    assert lib.abg_rmsq_ex(A, A + 0x1000, ctypes.c_float(1e-6), A + 0x2000, A + 0x2000 + 4 * 127, 128, 32, 0,
+                           None) == EALIAS
+    assert lib.abg_swq_ex(A, A + 0x2000, A + 0x3000, 128, 48, 0, None) == EINVAL
+    assert lib.abg_swq_ex(A, A + 0x2000, A + 0x3000, 320, 128, 0, None) == ESHAPE
+
+
 def test_vector_validation(lib):
     assert lib.abg_gsum(A, A + 0x1000, 100, 0, None) == ESHAPE
     assert lib.abg_gsum(A + 4, A + 0x1000, 128, 0, None) == EALIGN
