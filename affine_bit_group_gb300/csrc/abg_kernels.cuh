@@ -39,8 +39,8 @@ struct Q4Args {
     // shape (G = cols / group size)
     int cols, W, G, nch;
     int sb_f16;  // 16-bit scale and bias: 1 = f16, 0 = bf16
-    // tiling
-    int tile_rows, stages, nw;
+    // tiling (parts: partial-sum buffers, stages + 2)
+    int tile_rows, stages, nw, parts;
     // shared-memory layout (byte offsets)
     uint32_t off_stage, stage_w_bytes, stage_sb_bytes, stage_bytes, off_part, off_bar;
     uint32_t smem_bytes;

@@ -121,13 +121,15 @@ bool plan_once(Q4Plan *plan, const Q4Prob *probs, int nprob, int cols, int group
         return align_up(static_cast<uint32_t>(tr) * (C / 2), 16) +
                2u * align_up(sb_smem ? static_cast<uint32_t>(tr) * G * elem : 0u, 16);
     };
-    auto part_bytes = [&](int tr) { return align_up(static_cast<uint32_t>(kParts * tr * nch) * 4u, 16); };
+    auto part_bytes = [&](int tr, int stages) {
+        return align_up(static_cast<uint32_t>((stages + 2) * tr * nch) * 4u, 16);
+    };
     int S = 0;
     for (int attempt = 0; attempt < 2; ++attempt) {
         for (;;) {
             const uint32_t sb = stage_bytes(TR);
             S = 0;
-            while (S < 8 && fixed + (S + 1) * sb + part_bytes(TR) + 16u * (S + 1) + 8u * kParts <= budget) ++S;
+            while (S < 8 && fixed + (S + 1) * sb + part_bytes(TR, S + 1) + 8u * (3 * (S + 1) + 2) <= budget) ++S;
             if (S >= 2 || TR <= unit) break;
             TR = std::max(unit, TR / 2);
         }
@@ -163,8 +165,9 @@ bool plan_once(Q4Plan *plan, const Q4Prob *probs, int nprob, int cols, int group
     a.sb_f16 = sb_type == ABG_SB_F16 ? 1 : 0;
     a.stage_bytes = a.stage_w_bytes + 2 * a.stage_sb_bytes;
     a.off_part = a.off_stage + S * a.stage_bytes;
-    a.off_bar = align_up(a.off_part + part_bytes(TR), 16);
-    a.smem_bytes = a.off_bar + 16u * S + 8u * kParts;
+    a.off_bar = align_up(a.off_part + part_bytes(TR, S), 16);
+    a.parts = S + 2;
+    a.smem_bytes = a.off_bar + 8u * (2 * S + a.parts);
 
     // blocks per SM: what fits (registers and shared memory), at most 2 unless tuned
     int fit = 1;

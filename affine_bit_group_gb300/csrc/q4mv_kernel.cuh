@@ -138,7 +138,10 @@ __device__ __forceinline__ void exact_products(float2 (&P)[16], uint32_t w0, uin
 template <bool kExact>
 __device__ __forceinline__ float lane_sum32(uint4 wq, const float2 (&X)[16]) {
     const uint32_t w0 = wq.x, w1 = wq.y, w2 = wq.z, w3 = wq.w;
-    const uint32_t h0 = w0 >> 12, h1 = w1 >> 12, h2 = w2 >> 12, h3 = w3 >> 12;
+    // w >> 12 as the high word of w * 2^20: the multiplier pipe, not the
+    // logic pipe that the unpacking keeps busy
+    const uint32_t h0 = __umulhi(w0, 1u << 20), h1 = __umulhi(w1, 1u << 20), h2 = __umulhi(w2, 1u << 20),
+                   h3 = __umulhi(w3, 1u << 20);
     float2 P[16];
     if constexpr (kExact) {
         exact_products<0>(P, w0, h0, w1, h1, w2, h2, w3, h3, X, 0xBF800000u);
@@ -408,10 +411,13 @@ __device__ __forceinline__ void levels(float (&v)[N], float (&out)[lv_count<N, D
     }
 }
 
-// Partial-sum buffers (and their barriers) rotate over 4 tiles: a warp writes
-// a tile's buffer only after every warp has finished the final sums of the
-// tile four back.
-constexpr int kParts = 4;
+// Partial-sum buffers (and their `done` barriers) rotate over S + 2 tiles.
+// Only the warps that compute a tile's final sums (threads ct < tile rows)
+// wait for every warp's partials of that tile.  The others never wait on
+// `done`: a warp reaches tile k only after the producer refilled its stage,
+// i.e. after every warp released tile k - S, by which time the finishing
+// warps have completed the final sums of tile k - S - 2.  Tiles k - S - 1 .. k
+// hold S + 2 distinct buffers, so no buffer is rewritten while still read.
 
 // Block layouts (the register file is split over the SM's four schedulers,
 // so the warps per SM set the registers per thread):
@@ -442,7 +448,7 @@ __global__ void __launch_bounds__(layout_threads(kLayout), layout_blocks(kLayout
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], nw);
         }
-        for (int i = 0; i < kParts; ++i) mbar_init(&done[i], nw);
+        for (int i = 0; i < a.parts; ++i) mbar_init(&done[i], nw);
         s_abort = 0;
         fence_mbar_init();
     }
@@ -463,16 +469,17 @@ __global__ void __launch_bounds__(layout_threads(kLayout), layout_blocks(kLayout
         bool released = !wait_first;
         ProbCursor cur;
         const int total = static_cast<int>(a.total_tiles);
-        int k = 0;
+        // eph: parity of the empty phase that frees stage s for round k / S,
+        // i.e. ((k / S) & 1) ^ 1 (the consumers' release of the round before)
+        int k = 0, s = 0;
+        uint32_t eph = 1;
         for (int t = blockIdx.x; t < total; t += gridDim.x, ++k) {
-            const int s = k % S;
             if (k == S) {
                 grid_dep_wait();
                 grid_dep_launch();
                 released = true;
             }
-            if (k >= S && !wait_or_abort(&empty[s], static_cast<uint32_t>(((k / S) & 1) ^ 1), &s_abort, kSiteEmpty))
-                break;
+            if (k >= S && !wait_or_abort(&empty[s], eph, &s_abort, kSiteEmpty)) break;
             if (s_abort) break;
             int tile;
             const Q4Prob &P = a.prob[cur.find(a, t, tile)];
@@ -489,6 +496,10 @@ __global__ void __launch_bounds__(layout_threads(kLayout), layout_blocks(kLayout
                          policy);
                 bulk_g2s(st + a.stage_w_bytes + a.stage_sb_bytes, static_cast<const unsigned char *>(P.bias) + sbo,
                          sbb, &full[s], policy);
+            }
+            if (++s == S) {
+                s = 0;
+                eph ^= 1u;
             }
         }
         if (!released) {
@@ -533,9 +544,9 @@ __global__ void __launch_bounds__(layout_threads(kLayout), layout_blocks(kLayout
     int cur_ch = -1;
     // Final sums of tile j: thread ct adds row ct's chunk partials by the tree.
     ProbCursor cur, fcur;
-    auto finish = [&](int j, int tj) -> bool {
-        const int pi = j % kParts;
-        if (!wait_or_abort(&done[pi], static_cast<uint32_t>((j / kParts) & 1), &s_abort, kSiteDone)) return false;
+    // (pi, dph): tile j's partial buffer and the parity of its done phase
+    auto finish = [&](int tj, int pi, uint32_t dph) -> bool {
+        if (!wait_or_abort(&done[pi], dph, &s_abort, kSiteDone)) return false;
         int tile;
         const Q4Prob &P = a.prob[fcur.find(a, tj, tile)];
         const int64_t r0 = static_cast<int64_t>(tile) * TR;
@@ -554,11 +565,12 @@ __global__ void __launch_bounds__(layout_threads(kLayout), layout_blocks(kLayout
         return true;
     };
 
-    const int total = static_cast<int>(a.total_tiles);
-    int k = 0, tprev = -1;
+    const int total = static_cast<int>(a.total_tiles), NP = a.parts;
+    const bool finisher = cw * 32 < TR;  // holds final-sum threads (ct < rows)
+    int k = 0, tprev = -1, s = 0, pi = 0, ppi = 0;
+    uint32_t fph = 0, dph = 0, pdph = 0;  // full and done phase parities (current and previous tile)
     for (int t = blockIdx.x; t < total; t += gridDim.x, ++k) {
-        const int s = k % S;
-        if (!wait_or_abort(&full[s], static_cast<uint32_t>((k / S) & 1), &s_abort, kSiteFull)) break;
+        if (!wait_or_abort(&full[s], fph, &s_abort, kSiteFull)) break;
         int tile;
         const Q4Prob &P = a.prob[cur.find(a, t, tile)];
         const int64_t r0 = static_cast<int64_t>(tile) * TR;
@@ -567,7 +579,7 @@ __global__ void __launch_bounds__(layout_threads(kLayout), layout_blocks(kLayout
         const uint4 *sw = reinterpret_cast<const uint4 *>(stg);
         const void *ssc = stg + a.stage_w_bytes;
         const void *sbi = stg + a.stage_w_bytes + a.stage_sb_bytes;
-        float *prt = part + static_cast<size_t>(k % kParts) * TR * nch;
+        float *prt = part + static_cast<size_t>(pi) * TR * nch;
         const int nrb = (rows + R - 1) / R;
         if (!idle) {
             for (int ch = ch0; ch < nch; ch += chstep) {
@@ -641,13 +653,23 @@ __global__ void __launch_bounds__(layout_threads(kLayout), layout_blocks(kLayout
         }
         __syncwarp();
         if (lane == 0) {
-            mbar_arrive(&empty[s]);       // weights of this stage no longer needed
-            mbar_arrive(&done[k % kParts]);  // this warp's partials are written
+            mbar_arrive(&empty[s]);  // weights of this stage no longer needed
+            mbar_arrive(&done[pi]);  // this warp's partials are written
         }
-        if (tprev >= 0 && !finish(k - 1, tprev)) break;
+        if (finisher && tprev >= 0 && !finish(tprev, ppi, pdph)) break;
         tprev = t;
+        ppi = pi;
+        pdph = dph;
+        if (++s == S) {
+            s = 0;
+            fph ^= 1u;
+        }
+        if (++pi == NP) {
+            pi = 0;
+            dph ^= 1u;
+        }
     }
-    if (tprev >= 0) finish(k - 1, tprev);
+    if (finisher && tprev >= 0) finish(tprev, ppi, pdph);
     if (!wait_first) grid_dep_wait();
 }
 

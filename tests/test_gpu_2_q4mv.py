@@ -217,3 +217,18 @@ def test_mixed_negative_groups(cols):
 
 def test_no_device_timeouts():
     assert abg.device_status(clear=True) == 0
+
+
+@pytest.mark.parametrize("tuning", [(0, 0, 1, 1), (0, 4, 1, 2), (0, 0, 0, 0), (220, 16, 0, 64)])
+def test_many_tiles_per_block(tuning):
+    """Stage rings and partial buffers that wrap many times per block: small
+    stages (up to 8 of them), one block per SM, 500000 short rows; every
+    output bit-exact (a phase or buffer-rotation error shows up here)."""
+    m, x = synth.random_case(95, 500_000, 128)
+    abg.set_q4mv_tuning(*tuning)
+    try:
+        got = run(m, x)
+    finally:
+        abg.set_q4mv_tuning(0, 0, 0, 0)
+    assert_bits_equal(got, expect(m, x), f"tuning {tuning}")
+    assert abg.device_status(clear=True) == 0
