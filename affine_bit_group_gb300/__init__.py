@@ -17,7 +17,7 @@ import os
 import threading
 
 __all__ = [
-    "TREE", "FAST", "AbgError", "library", "q4mv", "q4mv_ex", "gsum", "rmsq", "swq", "StageGraph", "Node",
+    "TREE", "FAST", "AbgError", "library", "q4mv", "q4mv_ex", "q4mm", "gsum", "rmsq", "swq", "StageGraph", "Node",
     "device_status", "set_q4mv_tuning", "MAX_COLS", "SB_F32", "SB_BF16", "SB_F16", "SB_TYPES",
 ]
 
@@ -79,6 +79,7 @@ def library(build_if_missing: bool = True) -> ctypes.CDLL:
             lib.abg_rmsq.argtypes = [P, P, ctypes.c_float, P, P, I64, I, P]
             lib.abg_swq.argtypes = [P, P, P, I64, I, P]
             lib.abg_q4mv_ex.argtypes = [P, P, P, I, I, P, P, P, I64, I64, I64, I64, I, I, P]
+            lib.abg_q4mm.argtypes = [P, P, P, P, P, P, I64, I64, I64, I64, I64, I, I, P]
             lib.abg_gsum_ex.argtypes = [P, P, I64, I, I, P]
             lib.abg_rmsq_ex.argtypes = [P, P, ctypes.c_float, P, P, I64, I, I, P]
             lib.abg_swq_ex.argtypes = [P, P, P, I64, I, I, P]
@@ -92,7 +93,7 @@ def library(build_if_missing: bool = True) -> ctypes.CDLL:
             lib.abg_status_str.restype = ctypes.c_char_p
             lib.abg_last_cuda_error.argtypes = []
             lib.abg_last_cuda_error.restype = ctypes.c_char_p
-            for f in ("abg_q4mv", "abg_gsum", "abg_rmsq", "abg_swq", "abg_q4mv_ex", "abg_gsum_ex", "abg_rmsq_ex",
+            for f in ("abg_q4mv", "abg_q4mm", "abg_gsum", "abg_rmsq", "abg_swq", "abg_q4mv_ex", "abg_gsum_ex", "abg_rmsq_ex",
                       "abg_swq_ex", "abg_stage_graph_create",
                       "abg_stage_graph_launch", "abg_stage_graph_launches", "abg_stage_graph_destroy",
                       "abg_device_status", "abg_set_q4mv_tuning"):
@@ -171,6 +172,23 @@ def q4mv_ex(w, scale, bias, sb_type, group: int, x, xsum, y, cols: int, row0: in
         rows, cols, row0, n, mode, rows_per_warp, _stream(stream))
     _check(st, "abg_q4mv_ex")
     return y
+
+
+def q4mm(w, scale, bias, X, XS, Y, cols: int, row0: int = 0, n: int | None = None, mode: int = TREE,
+         rows_per_warp: int = 0, stream=None):
+    """Y[t] = the product for token t of X [T][cols] (group sums XS [T][cols/64]),
+    Y [T][n]; the weights are read once for the batch (see abg_q4mm)."""
+    _, f32 = _dtypes()
+    T = X.shape[0] if X.dim() == 2 else 1
+    rows = w.shape[0] if w.dim() == 2 else w.numel() // (cols // 8)
+    n = rows - row0 if n is None else n
+    G, W = cols // 64, cols // 8
+    st = library().abg_q4mm(
+        _ptr(w, "word", rows * W, "w"), _ptr(scale, f32, rows * G, "scale"), _ptr(bias, f32, rows * G, "bias"),
+        _ptr(X, f32, T * cols, "X"), _ptr(XS, f32, T * G, "XS"), _ptr(Y, f32, T * n, "Y"),
+        rows, cols, row0, n, T, mode, rows_per_warp, _stream(stream))
+    _check(st, "abg_q4mm")
+    return Y
 
 
 def gsum(v, s, mode: int = TREE, stream=None, group: int = 64):

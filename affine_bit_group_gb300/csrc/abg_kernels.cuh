@@ -44,6 +44,11 @@ struct Q4Args {
     // shared-memory layout (byte offsets)
     uint32_t off_stage, stage_w_bytes, stage_sb_bytes, stage_bytes, off_part, off_bar;
     uint32_t smem_bytes;
+    // batched product only: activation and group-sum rows of the T token
+    // slots, and how many of them are real tokens
+    const float *xt[4];
+    const float *xst[4];
+    int ntok;
 };
 
 struct Q4Tuning {
@@ -62,6 +67,7 @@ struct Q4Plan {
     int layout;  // block layout (see the kernel)
     int lg;      // group size 32 << lg
     bool half;   // 16-bit scale and bias
+    int mm = 0;  // batched product: kernel width in tokens (0: single token)
 };
 
 // Fills plan->args layout, grid and block for products sharing one activation
@@ -88,6 +94,17 @@ cudaError_t launch_swq(const float *a, float *o, float *osum, int64_t n, int gro
                        bool pdl);
 
 int sm_count();
+
+// Raises a kernel's dynamic shared-memory limit to the device maximum (once).
+cudaError_t raise_smem_limit(void *fn);
+
+// Batched product (q4mm.cu): plan and launch for kernel width T (2 or 4)
+// tokens, of which ntok are real (x and y rows of the others are never read
+// or written beyond the duplicated pointers the caller passes).
+bool plan_q4mm(Q4Plan *plan, const Q4Prob *probs, int nprob, int cols, int T, int ntok, const float *const *xt,
+               const float *const *xst, int prologue, bool tree, int rows_per_warp, bool sb_smem);
+cudaError_t launch_q4mm(const Q4Plan &plan, cudaStream_t stream, bool pdl);
+cudaError_t q4mm_status(unsigned *bits, bool clear);
 
 // Each translation unit's device status word (OR-ed into *bits).
 cudaError_t q4mv_status(unsigned *bits, bool clear);

@@ -12,6 +12,7 @@
 #include "../../include/abg.h"
 #include "abg_kernels.cuh"
 
+#include <algorithm>
 #include <chrono>
 #include <cstdio>
 #include <cstdlib>
@@ -271,6 +272,57 @@ abg_status abg_q4mv_ex(const uint32_t *w, const void *scale, const void *bias, i
     return cuda_fail(launch_q4mv(plan, static_cast<cudaStream_t>(stream), false), "q4mv launch");
 }
 
+abg_status abg_q4mm(const uint32_t *w, const float *scale, const float *bias, const float *x, const float *xsum,
+                    float *y, int64_t rows, int64_t cols, int64_t row0, int64_t n, int64_t T, int mode,
+                    int rows_per_warp, void *stream) {
+    if (T < 1 || T > 8) return ABG_EINVAL;
+    // token 0 validates the matrix, row range, pointers and alignment
+    Q4Call c{w, scale, bias, rows, cols, row0, n, y, kProNone, x, xsum, nullptr, 0.f};
+    abg_status st = check_q4(c, mode, rows_per_warp);
+    if (st != ABG_OK || n == 0) return st;
+    // y [T][n] overlaps no input, x [T][cols] or xsum [T][cols/64] included
+    const Range out = rng(y, T * n, 4);
+    Q4Call all = c;
+    const int64_t G = cols / 64;
+    std::vector<Range> in = q4_weights(all);
+    in.push_back(rng(x, T * cols, 4));
+    in.push_back(rng(xsum, T * G, 4));
+    for (const Range &r : in)
+        if (overlap(out, r)) return ABG_EALIAS;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    for (int64_t t0 = 0; t0 < T;) {
+        // token pairs share a launch; an odd last token runs alone
+        const int width = (T - t0 >= 2) ? 2 : 1;
+        const int ntok = width;
+        Q4Call ct = c;
+        ct.x = x + t0 * cols;
+        ct.xsum = xsum + t0 * G;
+        ct.y = y + t0 * n;
+        Q4Plan plan;
+        if (width == 1) {
+            st = plan_calls(&plan, {ct}, mode, rows_per_warp);
+            if (st != ABG_OK) return st;
+            cudaError_t e = prepare_q4mv(plan);
+            if (e == cudaSuccess) e = launch_q4mv(plan, s, false);
+            if (e != cudaSuccess) return cuda_fail(e, "q4mm launch");
+        } else {
+            const float *xt[4], *xst[4];
+            for (int i = 0; i < ntok; ++i) {
+                xt[i] = ct.x + i * cols;
+                xst[i] = ct.xsum + i * G;
+            }
+            Q4Prob p = make_prob(ct);
+            if (!plan_q4mm(&plan, &p, 1, static_cast<int>(cols), width, ntok, xt, xst, kProNone, mode == ABG_TREE,
+                           rows_per_warp == 0 ? 8 : rows_per_warp, sb_bulk(ct)))
+                return ABG_ESHAPE;
+            const cudaError_t e = launch_q4mm(plan, s, false);
+            if (e != cudaSuccess) return cuda_fail(e, "q4mm launch");
+        }
+        t0 += ntok;
+    }
+    return ABG_OK;
+}
+
 abg_status abg_gsum(const float *v, float *s, int64_t n, int mode, void *stream) {
     return abg_gsum_ex(v, s, n, 64, mode, stream);
 }
@@ -489,6 +541,7 @@ abg_status abg_device_status(uint32_t *bits, int clear) {
     unsigned v = 0;
     if (e == cudaSuccess) e = q4mv_status(&v, clear != 0);
     if (e == cudaSuccess) e = vec_status(&v, clear != 0);
+    if (e == cudaSuccess) e = q4mm_status(&v, clear != 0);
     if (e != cudaSuccess) return cuda_fail(e);
     *bits = v;
     return (v & 1u) ? ABG_ETIMEOUT : ABG_OK;  // bit 0: a bounded wait timed out

@@ -54,8 +54,6 @@ void *select_kernel(int lg, bool half, int R, bool tree, bool sb, int layout) {
 
 inline uint32_t align_up(uint32_t v, uint32_t a) { return (v + a - 1) / a * a; }
 
-cudaError_t raise_smem_limit(void *fn);
-
 }  // namespace
 
 cudaError_t q4mv_status(unsigned *bits, bool clear) {
@@ -192,8 +190,12 @@ bool plan_once(Q4Plan *plan, const Q4Prob *probs, int nprob, int cols, int group
     plan->layout = layout;
     plan->lg = lg;
     plan->half = half;
+    plan->mm = 0;
     return true;
 }
+
+
+}  // namespace
 
 // Every instantiation gets the device's largest dynamic shared-memory limit
 // once, so launches with different plans (different sizes) of one kernel can
@@ -214,8 +216,6 @@ cudaError_t raise_smem_limit(void *fn) {
     if (e == cudaSuccess) done.insert(fn);
     return e;
 }
-
-}  // namespace
 
 // Plans with the requested rows per item; if the stages do not fit in shared
 // memory (very wide rows), retries with fewer rows per item (same results).

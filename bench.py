@@ -13,9 +13,10 @@ weights from HBM.
 Also measured in the same run (as "extra"): the same 400 products as 400
 dependent stages (each waits for the previous one: decode-like latency), the
 248320x2048 output head, one synthetic 24-layer decode token (fused and
-unfused stage graphs), and the 4096x2048 product in every weight format
+unfused stage graphs), the 4096x2048 product in every weight format
 (groups of 32, 64 or 128 columns; f32, bf16 or f16 scale and bias), each as a
-grouped launch of 64 products streaming from HBM.
+grouped launch of 64 products streaming from HBM, and the batched product
+(1, 2, 4 and 8 tokens sharing the 248320x2048 head's weights).
 
 Output: one JSON line on rank 0.  --impl reference times the CPU oracle (the
 plain C definition the library is tested against) on the same workload.
@@ -261,6 +262,7 @@ def run_ours(args, rank, world):
         extra["head"] = bench_head(abg, stream, args, peak)
         extra["decode_token"] = bench_decode(abg, decode, stream, args)
         extra["formats"] = bench_formats(abg, stream, args, peak, l2)
+        extra["batched"] = bench_batched(abg, stream, args)
 
     res = dict(value=value, ms_step=ms_step, us_per_product=us_per_product, achieved=achieved,
                launch_us=ms_launch * 1e3, clocks=clocks,
@@ -328,6 +330,48 @@ def bench_formats(abg, stream, args, peak, l2):
                                      "frac_of_measured_peak": round(gbs / peak, 3), "bytes_per_product": pb}
             del mats, g, w, sc, bi
             torch.cuda.empty_cache()
+    return out
+
+
+def bench_batched(abg, stream, args):
+    """The 248320x2048 head for a batch of T tokens (abg_q4mm): us per call and per
+    token; every token's output hash checked against the oracle on a sample."""
+    import torch
+
+    import oracle
+    m, _, _ = synth.head()
+    w = torch.from_numpy(m.w.view(np.int32)).cuda()
+    s = torch.from_numpy(m.scale).cuda()
+    b = torch.from_numpy(m.bias).cuda()
+    pb = product_bytes(m.rows, m.cols)
+    out = {"workload": "q4mm 248320x2048 head, T tokens per call (pairs share a launch)"}
+    for T in (1, 2, 4, 8):
+        rng = np.random.default_rng([6, T])
+        X_np = np.stack([synth.activations(rng, m.cols) for _ in range(T)])
+        XS_np = np.stack([oracle.gsum(x) for x in X_np])
+        X = torch.from_numpy(X_np).cuda()
+        XS = torch.from_numpy(XS_np).cuda()
+        Y = torch.empty(T * m.rows, dtype=torch.float32, device="cuda")
+        with torch.cuda.stream(stream):
+            for _ in range(args.warmup):
+                abg.q4mm(w, s, b, X, XS, Y, cols=m.cols, stream=stream)
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            reps = max(3, args.steps // 2)
+            for _ in range(reps):
+                abg.q4mm(w, s, b, X, XS, Y, cols=m.cols, stream=stream)
+            e1.record(stream)
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) * 1e3 / reps
+        got = Y.view(T, m.rows)[:, :512].cpu().numpy()
+        exp = oracle.q4mm(*m.arrays(), X_np, XS_np, m.cols, n=512)
+        if not np.array_equal(got.view(np.uint32), exp.view(np.uint32)):
+            raise SystemExit(f"batched product T={T} differs from the oracle")
+        out[f"T{T}"] = {"us_per_call": round(us, 2), "us_per_token": round(us / T, 2),
+                        "token_gbs": round(T * pb / (us * 1e-6) / 1e9, 1)}
+    del w, s, b
+    torch.cuda.empty_cache()
     return out
 
 
@@ -428,7 +472,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-extra", action="store_true", help="skip the head and decode-token measurements")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
-    ap.add_argument("--only", choices=["head", "decode", "formats"], default=None,
+    ap.add_argument("--only", choices=["head", "decode", "formats", "batched"], default=None,
                     help="run one secondary workload alone and print its numbers (for profiling)")
     args = ap.parse_args()
     if args.only:
@@ -442,6 +486,8 @@ def main():
             out = bench_head(abg, stream, args, peak)
         elif args.only == "decode":
             out = bench_decode(abg, decode, stream, args)
+        elif args.only == "batched":
+            out = bench_batched(abg, stream, args)
         else:
             l2 = getattr(torch.cuda.get_device_properties(0), "L2_cache_size", 126 * 2 ** 20)
             out = bench_formats(abg, stream, args, peak, l2)

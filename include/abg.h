@@ -131,6 +131,27 @@ abg_status abg_q4mv_ex(const uint32_t *w, const void *scale, const void *bias, i
                        int mode, int rows_per_warp, void *stream);
 
 /*
+ * q4mm: the product for a batch of T decode tokens that share the weights
+ * (the 4-row q4mv of [fused-token] Change reads each activation group once for
+ * several rows; here each weight is read once for several tokens):
+ *
+ *     y[t*n + i] = q4mv row row0+i of x[t*cols .. t*cols+cols-1],  t < T,
+ *
+ * each token's result bit-identical to abg_q4mv on that token alone (ABG_TREE).
+ *   x     f32 [T][cols], 16-byte aligned (rows follow each other)
+ *   xsum  f32 [T][cols/64]   xsum[t][g] = tree sum of token t's group g
+ *   y     f32 [T][n]
+ *   T     1..8.  Each pair of tokens is one launch that reads the weights
+ *         once for both; an odd last token runs as a single-token product.
+ * Groups of 64 columns with f32 scale and bias; other arguments and errors as
+ * abg_q4mv.
+ */
+abg_status abg_q4mm(const uint32_t *w, const float *scale, const float *bias,
+                    const float *x, const float *xsum, float *y,
+                    int64_t rows, int64_t cols, int64_t row0, int64_t n, int64_t T,
+                    int mode, int rows_per_warp, void *stream);
+
+/*
  * gsum: s[g] = tree sum of v[64g .. 64g+63], g < n/64.  The group sums a
  * product reads for its bias term ([fused-token] Change, Array.rmsq bullet:
  * "the 64-value group sums that Array.q4mv reads").  n a positive multiple of 64.

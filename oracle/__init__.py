@@ -266,3 +266,16 @@ def q4mv_ex(w, scale, bias, sb_dtype: str, gs: int, x, xsum, cols, row0=0, n=Non
     y = np.empty(n, np.float32)
     _load().or_q4mv_ex(pw, scale.ctypes.data, bias.ctypes.data, dt, gs, px, pxs, _f32(y)[1], rows, cols, row0, n)
     return y
+
+
+def q4mm(w, scale, bias, X, XS, cols, row0=0, n=None) -> np.ndarray:
+    """Batched product: Y[t] = q4mv(w, scale, bias, X[t], XS[t]) for each of the T
+    activation rows of X [T][cols] (group sums XS [T][cols/64]).  A batch of
+    decode tokens reads the same weights once for all of them; each token's
+    result is by definition its own product, so this is that product applied
+    row by row of X (no reordering across tokens)."""
+    X = np.atleast_2d(np.asarray(X, np.float32))
+    XS = np.atleast_2d(np.asarray(XS, np.float32))
+    if X.shape[0] != XS.shape[0]:
+        raise ValueError("X and XS hold different token counts")
+    return np.stack([q4mv(w, scale, bias, X[t], XS[t], cols, row0=row0, n=n) for t in range(X.shape[0])])

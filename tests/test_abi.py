@@ -109,6 +109,18 @@ def test_q4mv_ex_validation(lib):
     assert q4x(lib, n=0, row0=8, group=128, sb=1) == OK
 
 
+def test_q4mm_validation(lib):
+    w, s, b, x, xs, y = A, A + 0x100000, A + 0x200000, A + 0x300000, A + 0x310000, A + 0x400000
+    assert lib.abg_q4mm(w, s, b, x, xs, y, 8, 128, 0, 8, 0, 0, 0, None) == EINVAL   # T = 0
+    assert lib.abg_q4mm(w, s, b, x, xs, y, 8, 128, 0, 8, 9, 0, 0, None) == EINVAL   # T > 8
+    assert lib.abg_q4mm(w, s, b, x, xs, y, 8, 100, 0, 8, 2, 0, 0, None) == ESHAPE
+    # y [T][n] reaching into token 3's activation row x[3]
+    assert lib.abg_q4mm(w, s, b, x, xs, x + 4 * 128 * 3 - 4 * 8, 8, 128, 0, 8, 4, 0, 0, None) == EALIAS
+    # y overlapping the last token's group sums
+    assert lib.abg_q4mm(w, s, b, x, xs, xs + 4 * 2 * 3, 8, 128, 0, 8, 4, 0, 0, None) == EALIAS
+    assert lib.abg_q4mm(w, s, b, x, xs, y, 8, 128, 8, 0, 4, 0, 0, None) == OK      # empty
+
+
 def test_vector_ex_validation(lib):
     assert lib.abg_gsum_ex(A, A + 0x1000, 128, 16, 0, None) == EINVAL
     assert lib.abg_gsum_ex(A, A + 0x1000, 192, 128, 0, None) == ESHAPE

@@ -458,3 +458,35 @@ def test_decode_token_wiring_small():
         hid = t["h"]
     assert close(xf, rms(hid, model.rms_final))
     assert close(logits, dq(model.head, xf))
+
+
+# ------------------------------------------------------------- batched ----
+
+def test_q4mm_is_the_product_per_token_exactly():
+    """Batched tokens: with small integers and power-of-two scales every row of Y is
+    the exact dequantize-then-dot value for its own token (tokens never mix)."""
+    rng = np.random.default_rng(77)
+    rows, cols, T = 5, 192, 3
+    G = cols // 64
+    q = rng.integers(0, 16, (rows, cols))
+    scale = (2.0 ** rng.integers(-3, 2, (rows, G))).astype(np.float32)
+    bias = (rng.integers(-16, 16, (rows, G)) * 0.25).astype(np.float32)
+    X = rng.integers(-4, 5, (T, cols)).astype(np.float32)
+    XS = np.stack([oracle.gsum(x) for x in X])
+    Y = oracle.q4mm(pack_nibbles(q), scale, bias, X, XS, cols)
+    assert Y.shape == (T, rows)
+    for t in range(T):
+        assert [Fraction(float(v)) for v in Y[t]] == exact_q4mv(q, scale, bias, X[t])
+
+
+def test_q4mm_token_order_and_single_token():
+    m, x = synth.random_case(78, 19, 256)
+    rng = np.random.default_rng(79)
+    X = np.stack([x, synth.activations(rng, 256), synth.activations(rng, 256)])
+    XS = np.stack([oracle.gsum(v) for v in X])
+    Y = oracle.q4mm(*m.arrays(), X, XS, 256)
+    assert np.array_equal(Y[0], oracle.q4mv(*m.arrays(), x, oracle.gsum(x), 256))
+    P = oracle.q4mm(*m.arrays(), X[::-1], XS[::-1], 256)
+    assert np.array_equal(P, Y[::-1])
+    with pytest.raises(ValueError):
+        oracle.q4mm(*m.arrays(), X, XS[:2], 256)
