@@ -15,8 +15,11 @@ dependent stages (each waits for the previous one: decode-like latency), the
 248320x2048 output head, one synthetic 24-layer decode token (fused and
 unfused stage graphs), the 4096x2048 product in every weight format
 (groups of 32, 64 or 128 columns; f32, bf16 or f16 scale and bias), each as a
-grouped launch of 64 products streaming from HBM, and the batched product
-(1, 2, 4 and 8 tokens sharing the 248320x2048 head's weights).
+grouped launch of 64 products streaming from HBM, the batched product
+(1, 2, 4 and 8 tokens sharing the 248320x2048 head's weights), and the pages'
+own timing of the 4096x2048 product ((400-call - 1-call)/400, median of 6).
+`--only sweep` runs the rows x cols x rows-per-item x mode sweep (GB/s and
+fraction of peak per point, and the fast-mode error on sampled rows).
 
 Output: one JSON line on rank 0.  --impl reference times the CPU oracle (the
 plain C definition the library is tested against) on the same workload.
@@ -263,6 +266,7 @@ def run_ours(args, rank, world):
         extra["decode_token"] = bench_decode(abg, decode, stream, args)
         extra["formats"] = bench_formats(abg, stream, args, peak, l2)
         extra["batched"] = bench_batched(abg, stream, args)
+        extra["pages_way"] = bench_pages_way(abg, stream, args)
 
     res = dict(value=value, ms_step=ms_step, us_per_product=us_per_product, achieved=achieved,
                launch_us=ms_launch * 1e3, clocks=clocks,
@@ -375,6 +379,98 @@ def bench_batched(abg, stream, args):
     return out
 
 
+SWEEP_ROWS = (512, 2048, 4096, 6144, 16384, 65536, 248320)
+SWEEP_COLS = (2048, 4096, 6144)
+
+
+def bench_sweep(abg, stream, args, peak, l2):
+    """Every (rows, cols) point of the sweep, each rows-per-item setting, tree and
+    fast mode: products queued as one stage over copies of the weights totalling
+    more than 3x L2.  Also the fast-mode error on a sample of rows: the largest
+    |y_fast - y_tree| / |y_tree| over rows with |y_tree| >= 1e-3 A_r."""
+    import torch
+
+    import oracle
+    out = {"workload": "sweep: seed [4, rows, cols]; products queued as one stage, weights > 3x L2", "points": []}
+    for cols in SWEEP_COLS:
+        for rows in SWEEP_ROWS:
+            m, x_np = synth.sweep_point(rows, cols)
+            pb = product_bytes(rows, cols)
+            copies = int(min(600, max(2, math.ceil(3 * l2 / m.nbytes))))
+            w = torch.from_numpy(m.w.view(np.int32)).cuda()
+            sc = torch.from_numpy(m.scale).cuda()
+            bi = torch.from_numpy(m.bias).cuda()
+            mats = [(w.clone(), sc.clone(), bi.clone()) for _ in range(copies)]
+            del w, sc, bi
+            x = torch.from_numpy(x_np).cuda()
+            xs = torch.empty(cols // 64, dtype=torch.float32, device="cuda")
+            abg.gsum(x, xs)
+            calls = max(copies, 8)
+            ys = [torch.empty(rows, dtype=torch.float32, device="cuda") for _ in range(calls)]
+            point = {"rows": rows, "cols": cols, "copies": copies}
+            y_tree = None
+            for mode, mname in ((abg.TREE, "tree"), (abg.FAST, "fast")):
+                for R in (1, 2, 4, 8):
+                    g = abg.StageGraph([abg.Node.q4mv(0, *mats[i % copies], ys[i % len(ys)], cols, x=x, xsum=xs)
+                                        for i in range(calls)], mode=mode, rows_per_warp=R, keep=[x, xs] + ys)
+                    ms, _ = time_graph(g, stream, 3, 1, False)
+                    g.close()
+                    gbs = calls * pb / (ms * 1e-3) / 1e9
+                    point[f"{mname}_R{R}_gbs"] = round(gbs, 1)
+                    point[f"{mname}_R{R}_frac"] = round(gbs / peak, 3)
+                    if mname == "tree" and R == 8:
+                        y_tree = ys[(calls - 1) % len(ys)].cpu().numpy().copy()
+                    if mname == "fast" and R == 8:
+                        y_fast = ys[(calls - 1) % len(ys)].cpu().numpy().copy()
+            n = min(rows, 256)
+            mag = oracle.q4mv_absmag(*m.arrays(), x_np, oracle.gsum(x_np), cols, n=n)
+            yt, yf = y_tree[:n].astype(np.float64), y_fast[:n].astype(np.float64)
+            keep = np.abs(yt) >= 1e-3 * mag
+            point["fast_max_rel_err"] = float(np.max(np.abs(yf - yt)[keep] / np.abs(yt)[keep])) if keep.any() else 0.0
+            point["fast_max_err_over_A"] = float(np.max(np.abs(yf - yt) / mag))
+            out["points"].append(point)
+            del mats, ys, x, xs
+            torch.cuda.empty_cache()
+    return out
+
+
+def bench_pages_way(abg, stream, args):
+    """The pages' timing of the 4096x2048 product: (400-call - 1-call) / 400, rounds
+    alternating, median of 6, calls back to back on one stream over rotating
+    weight copies (> 3x L2)."""
+    import torch
+    m, x_np = synth.mid()
+    l2 = getattr(torch.cuda.get_device_properties(0), "L2_cache_size", 126 * 2 ** 20)
+    copies = max(2, math.ceil(3 * l2 / m.nbytes))
+    mats = rotating_copies(m, copies)
+    x = torch.from_numpy(x_np).cuda()
+    xs = torch.empty(MID_COLS // 64, dtype=torch.float32, device="cuda")
+    abg.gsum(x, xs)
+    y = torch.empty(MID_ROWS, dtype=torch.float32, device="cuda")
+
+    def run(n):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for i in range(n):
+            abg.q4mv(*mats[i % copies], x, xs, y, cols=MID_COLS, stream=stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1)
+
+    run(20)
+    per = []
+    for _ in range(6):
+        t400 = run(CALLS)
+        t1 = run(1)
+        per.append((t400 - t1) / CALLS)
+    us = statistics.median(per) * 1e3
+    del mats
+    torch.cuda.empty_cache()
+    return {"workload": "4096x2048, 400 single-call launches back to back, (400-call - 1-call)/400, median of 6",
+            "us_per_call": round(us, 3), "gbs": round(product_bytes(MID_ROWS, MID_COLS) / (us * 1e-6) / 1e9, 1)}
+
+
 def bench_decode(abg, decode, stream, args):
     import torch
     model, h = synth.decode_model()
@@ -385,10 +481,10 @@ def bench_decode(abg, decode, stream, args):
            "product_bytes": dm.product_bytes}
     for fused in (True, False):
         g, _ = decode.decode_token_graph(dm, h0, fused=fused)
-        ms, _ = time_graph(g, stream, max(3, args.steps), args.warmup, False)
-        # wall time of launch + one sync, per token
+        ms, _ = time_graph(g, stream, 50, 5, False)
+        # wall time of launch + one sync, per token: median of 50 replays
         walls = []
-        for _ in range(max(3, args.steps)):
+        for _ in range(50):
             t0 = time.perf_counter()
             g.launch(stream)
             stream.synchronize()
@@ -472,7 +568,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-extra", action="store_true", help="skip the head and decode-token measurements")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
-    ap.add_argument("--only", choices=["head", "decode", "formats", "batched"], default=None,
+    ap.add_argument("--only", choices=["head", "decode", "formats", "batched", "sweep", "pages_way"], default=None,
                     help="run one secondary workload alone and print its numbers (for profiling)")
     args = ap.parse_args()
     if args.only:
@@ -488,6 +584,11 @@ def main():
             out = bench_decode(abg, decode, stream, args)
         elif args.only == "batched":
             out = bench_batched(abg, stream, args)
+        elif args.only == "pages_way":
+            out = bench_pages_way(abg, stream, args)
+        elif args.only == "sweep":
+            l2 = getattr(torch.cuda.get_device_properties(0), "L2_cache_size", 126 * 2 ** 20)
+            out = bench_sweep(abg, stream, args, peak, l2)
         else:
             l2 = getattr(torch.cuda.get_device_properties(0), "L2_cache_size", 126 * 2 ** 20)
             out = bench_formats(abg, stream, args, peak, l2)
