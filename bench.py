@@ -511,6 +511,35 @@ def cpu_baseline(seconds: float = 10.0):
             "sample": f"{n} calls of the 4096x2048 product (single-threaded C oracle, {dt:.1f} s)"}
 
 
+def _oracle_rows_worker(job):
+    """One host process of the all-cores baseline: rows [r0, r1) of the 4096x2048
+    product, repeated for `seconds`; returns (calls, rows per call)."""
+    r0, r1, seconds = job
+    import oracle
+    m, x = synth.mid()
+    xs = oracle.gsum(x)
+    oracle.q4mv(*m.arrays(), x, xs, MID_COLS, row0=r0, n=r1 - r0)
+    n, t0 = 0, time.perf_counter()
+    while time.perf_counter() - t0 < seconds:
+        oracle.q4mv(*m.arrays(), x, xs, MID_COLS, row0=r0, n=r1 - r0)
+        n += 1
+    return n, r1 - r0, time.perf_counter() - t0
+
+
+def cpu_all_cores(seconds: float = 10.0):
+    """The same oracle on every host core: one spawned process per core, each on its
+    own slice of the rows (the oracle itself is single-threaded C)."""
+    import multiprocessing as mp
+    cores = os.cpu_count() or 1
+    bounds = [(MID_ROWS * i // cores, MID_ROWS * (i + 1) // cores, seconds) for i in range(cores)]
+    with mp.get_context("spawn").Pool(cores) as pool:
+        res = pool.map(_oracle_rows_worker, bounds)
+    dt = max(r[2] for r in res)
+    total = sum(n * product_bytes(rows, MID_COLS) for n, rows, _ in res)
+    return {"value": total / dt / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"4096x2048 product, rows split over {cores} processes, {dt:.1f} s"}
+
+
 def run_reference(args):
     """The oracle as the reference arm: each step is a bounded sample of the workload on the host."""
     import oracle
@@ -628,6 +657,7 @@ def main():
     }
     if not args.no_cpu:
         line["cpu_baseline"] = cpu_baseline()
+        line["extra"]["cpu_all_cores"] = cpu_all_cores()
     print(json.dumps(line), flush=True)
 
 
