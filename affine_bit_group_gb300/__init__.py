@@ -88,6 +88,7 @@ def library(build_if_missing: bool = True) -> ctypes.CDLL:
             lib.abg_stage_graph_launches.argtypes = [P, ctypes.POINTER(I64)]
             lib.abg_stage_graph_destroy.argtypes = [P]
             lib.abg_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32), I]
+            lib.abg_selftest_wait_timeout.argtypes = [P]
             lib.abg_set_q4mv_tuning.argtypes = [I, I, I, I]
             lib.abg_status_str.argtypes = [I]
             lib.abg_status_str.restype = ctypes.c_char_p
@@ -96,7 +97,7 @@ def library(build_if_missing: bool = True) -> ctypes.CDLL:
             for f in ("abg_q4mv", "abg_q4mm", "abg_gsum", "abg_rmsq", "abg_swq", "abg_q4mv_ex", "abg_gsum_ex", "abg_rmsq_ex",
                       "abg_swq_ex", "abg_stage_graph_create",
                       "abg_stage_graph_launch", "abg_stage_graph_launches", "abg_stage_graph_destroy",
-                      "abg_device_status", "abg_set_q4mv_tuning"):
+                      "abg_device_status", "abg_set_q4mv_tuning", "abg_selftest_wait_timeout"):
                 getattr(lib, f).restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -292,6 +293,12 @@ def device_status(clear: bool = True) -> int:
     if st not in (0, 6):
         _check(st, "abg_device_status")
     return bits.value
+
+
+def selftest_wait_timeout(stream=None):
+    """Enqueues the failure-detection self-test (abg_selftest_wait_timeout): a product
+    whose bounded waits run out after about 0.5 s; read the result with device_status()."""
+    _check(library().abg_selftest_wait_timeout(_stream(stream)), "abg_selftest_wait_timeout")
 
 
 def set_q4mv_tuning(smem_kb: int = 0, consumer_warps: int = 0, blocks_per_sm: int = 0, stage_kb: int = 0):

@@ -44,6 +44,9 @@ struct Q4Args {
     // shared-memory layout (byte offsets)
     uint32_t off_stage, stage_w_bytes, stage_sb_bytes, stage_bytes, off_part, off_bar;
     uint32_t smem_bytes;
+    // failure-detection self-test only: the producer delivers no tile, so the
+    // computing warps' bounded waits run out (see abg_selftest_wait_timeout)
+    int withhold;
     // batched product only: activation and group-sum rows of the T token
     // slots, and how many of them are real tokens
     const float *xt[4];

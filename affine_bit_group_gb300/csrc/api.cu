@@ -18,6 +18,8 @@
 #include <cstdlib>
 #include <cstring>
 #include <map>
+#include <mutex>
+#include <set>
 #include <string>
 #include <vector>
 
@@ -26,6 +28,17 @@ using namespace abg;
 namespace {
 
 thread_local std::string g_cuda_error;
+
+// Live stage-graph handles: launching or destroying a handle that was never
+// created here, or was destroyed already, is refused with ABG_EINVAL instead
+// of touching freed memory.
+std::mutex g_graphs_mu;
+std::set<void *> g_graphs;
+
+bool graph_live(void *g) {
+    std::lock_guard<std::mutex> lock(g_graphs_mu);
+    return g && g_graphs.count(g) != 0;
+}
 Q4Tuning g_tuning;
 
 abg_status cuda_fail(cudaError_t e, const char *where = nullptr) {
@@ -482,12 +495,16 @@ abg_status abg_stage_graph_create(const abg_node *nodes, int64_t count, int mode
         cudaGetLastError();
         return cuda_fail(e, where.c_str());
     }
+    {
+        std::lock_guard<std::mutex> lock(g_graphs_mu);
+        g_graphs.insert(g);
+    }
     *graph_out = g;
     return ABG_OK;
 }
 
 abg_status abg_stage_graph_launch(void *graph, void *stream) {
-    if (!graph) return ABG_EINVAL;
+    if (!graph_live(graph)) return ABG_EINVAL;
     auto *g = static_cast<StageGraph *>(graph);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     static const bool trace = [] {
@@ -516,13 +533,16 @@ abg_status abg_stage_graph_launch(void *graph, void *stream) {
 }
 
 abg_status abg_stage_graph_launches(void *graph, int64_t *launches) {
-    if (!graph || !launches) return ABG_EINVAL;
+    if (!graph_live(graph) || !launches) return ABG_EINVAL;
     *launches = static_cast<StageGraph *>(graph)->launches;
     return ABG_OK;
 }
 
 abg_status abg_stage_graph_destroy(void *graph) {
-    if (!graph) return ABG_EINVAL;
+    {
+        std::lock_guard<std::mutex> lock(g_graphs_mu);
+        if (!graph || g_graphs.erase(graph) == 0) return ABG_EINVAL;
+    }
     auto *g = static_cast<StageGraph *>(graph);
     cudaError_t e = cudaSuccess;
     if (g->exec) e = cudaGraphExecDestroy(g->exec);
@@ -532,6 +552,22 @@ abg_status abg_stage_graph_destroy(void *graph) {
     }
     delete g;
     return cuda_fail(e);
+}
+
+abg_status abg_selftest_wait_timeout(void *stream) {
+    // one 64x1024 product whose producer withholds its only tile; the
+    // computing warps touch no memory before that wait, so no pointer is read
+    Q4Prob p = {};
+    p.n = 64;
+    Q4Plan plan;
+    Q4Tuning none;
+    if (!plan_q4mv(&plan, &p, 1, 1024, 64, ABG_SB_F32, kProNone, nullptr, nullptr, nullptr, 0.f, true, 8, false,
+                   none))
+        return ABG_ESHAPE;
+    plan.args.withhold = 1;
+    cudaError_t e = prepare_q4mv(plan);
+    if (e != cudaSuccess) return cuda_fail(e, "kernel attributes");
+    return cuda_fail(launch_q4mv(plan, static_cast<cudaStream_t>(stream), false), "self-test launch");
 }
 
 abg_status abg_device_status(uint32_t *bits, int clear) {

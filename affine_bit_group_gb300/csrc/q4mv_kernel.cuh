@@ -474,6 +474,7 @@ __global__ void __launch_bounds__(layout_threads(kLayout), layout_blocks(kLayout
         int k = 0, s = 0;
         uint32_t eph = 1;
         for (int t = blockIdx.x; t < total; t += gridDim.x, ++k) {
+            if (a.withhold) break;  // self-test: nothing is copied, nothing is in flight
             if (k == S) {
                 grid_dep_wait();
                 grid_dep_launch();

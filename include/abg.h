@@ -273,9 +273,20 @@ abg_status abg_stage_graph_launches(void *graph, int64_t *launches);
 abg_status abg_stage_graph_destroy(void *graph);
 
 /* Reads (and, if clear != 0, resets) the device status word on the current
- * device: bit 0 = a device-side wait timed out.  Synchronizes the device.
+ * device: bit 0 = a device-side wait timed out; bits 4.. name the wait that
+ * gave up (16: a stage's release, 32: a stage's arrival, 64: the partial sums
+ * of a tile, 128: a final drain of copies).  Synchronizes the device.
  * Returns ABG_ETIMEOUT when bit 0 was set, else ABG_OK. */
 abg_status abg_device_status(uint32_t *bits, int clear);
+
+/* Failure-detection self-test (no counterpart on the pages, whose queued
+ * kernels had no bounded waits): enqueues one small product whose producer
+ * warp withholds its only tile, so the computing warps' bounded waits run out
+ * after the 0.5 s limit.  The kernel then sets bits 0 and 32 of the device
+ * status word and exits with no copy in flight; the GPU context stays usable.
+ * Reads no caller memory.  Expect abg_device_status to return ABG_ETIMEOUT
+ * (and clear it there) after syncing the stream. */
+abg_status abg_selftest_wait_timeout(void *stream);
 
 /* Tuning of the product kernel, process-wide; 0 keeps the default.  Applies
  * to calls and graphs created afterwards.

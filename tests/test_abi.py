@@ -192,3 +192,11 @@ def test_product_path_has_no_cpu_fallback():
         if f.endswith(".py"):
             src = open(os.path.join(pkg, f)).read()
             assert "import oracle" not in src and "from oracle" not in src, f
+
+
+def test_unknown_graph_handles_are_refused(lib):
+    fake = 0x7F0000001000
+    assert lib.abg_stage_graph_launch(fake, None) == EINVAL
+    assert lib.abg_stage_graph_destroy(fake) == EINVAL
+    n = ctypes.c_int64()
+    assert lib.abg_stage_graph_launches(fake, ctypes.byref(n)) == EINVAL
