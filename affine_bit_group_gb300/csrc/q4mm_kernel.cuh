@@ -80,6 +80,8 @@ struct MSlice {
     float2 X[T][LC / 2];
     float xs[T];  // group sums of the lane's group, per token
     bool exact;
+    int negs;     // tree mode, bit t: every value of the lane's group of token t is negative
+    bool anyneg;  // warp-uniform: negs != 0 in some lane
 };
 
 // Activation slices for chunk ch: x of token t at a.xt[t]; group sums given
@@ -113,7 +115,9 @@ __device__ __forceinline__ void load_mslice(const Q4Args &a, int ch, int lane, M
     // takes part in the shuffles)
 #pragma unroll
     for (int d = 1; d < kL; d <<= 1) negs &= __shfl_xor_sync(0xffffffffu, negs, d);
-    sl.exact = !__any_sync(0xffffffffu, sp || negs != 0);
+    sl.exact = !__any_sync(0xffffffffu, sp);
+    sl.negs = kTree ? negs : 0;
+    sl.anyneg = __any_sync(0xffffffffu, sl.negs != 0);
     const int g = ch * GPC + lane / kL;
 #pragma unroll
     for (int t = 0; t < T; ++t) {
@@ -365,6 +369,13 @@ __global__ void __launch_bounds__(288, 2) q4mm_kernel(const __grid_constant__ Q4
                     float d[H];
                     levels<NV, 1, kL, kTree>(v, d, lane, sel);
                     const int ofs = sel;
+                    if (kTree && sl.exact && sl.anyneg) {
+                        // zero sums are +0 on the exact path; in an all-negative
+                        // group a zero sum means every q is 0, and RN's sum is -0
+#pragma unroll
+                        for (int i = 0; i < H; ++i)
+                            d[i] = (((sl.negs >> ((ofs + i) % T)) & 1) && d[i] == 0.f) ? kNegZero : d[i];
+                    }
                     float tv[H];
 #pragma unroll
                     for (int i = 0; i < H; ++i) {

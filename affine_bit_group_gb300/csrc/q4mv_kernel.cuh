@@ -130,8 +130,8 @@ __device__ __forceinline__ void exact_products(float2 (&P)[16], uint32_t w0, uin
 //     product fma(-(1 + q 2^(4k-23)), -x S, -x S) = q x exactly before its one
 //     rounding, so it is RN(q*x), at one logic op and half a packed FMA per
 //     weight.
-//   plain path (activations with zeros of either sign, infinities, NaN, huge
-//     values, or a group of all-negative values): X[m] = {x(m), x(m+16)}; q is
+//   plain path (activations with zeros of either sign, infinities, NaN or
+//     huge values): X[m] = {x(m), x(m+16)}; q is
 //     converted exactly and multiplied with scalar RN ops.  (The compiler may
 //     fuse a packed multiply into the packed add after it; the scalar
 //     __fmul_rn / __fadd_rn intrinsics are never contracted.)
@@ -233,6 +233,8 @@ struct Slice {
     float2 X[16];  // see lane_sum32
     float xs;      // group sum of the group the lane's columns belong to
     bool exact;    // warp-uniform: the exact path applies to the whole slice
+    bool neg;      // tree mode: every activation of this lane's group is negative
+    bool anyneg;   // tree mode, warp-uniform: some lane's group is all negative
 };
 
 template <bool kTree, int kLg>
@@ -272,9 +274,9 @@ __device__ __forceinline__ void load_slice(const Q4Args &a, int ch, int lane, fl
             }
         }
     }
-    // special values, and groups whose values are all negative (there the
-    // exact path's q = 0 products would be +0 where RN(0 * x) is -0, and a
-    // whole group of them could leave -0 in the sum)
+    // special values take the plain path; groups whose values are all
+    // negative are marked for the sign of a zero group sum (see the product
+    // loop)
     bool sp = false, allneg = true;
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
@@ -288,7 +290,9 @@ __device__ __forceinline__ void load_slice(const Q4Args &a, int ch, int lane, fl
     int grpneg = allneg ? 1 : 0;
 #pragma unroll
     for (int d = 1; d < (1 << kLg); d <<= 1) grpneg &= __shfl_xor_sync(0xffffffffu, grpneg, d);
-    sl.exact = !__any_sync(0xffffffffu, sp || grpneg != 0);
+    sl.exact = !__any_sync(0xffffffffu, sp);
+    sl.neg = kTree && grpneg != 0;
+    sl.anyneg = __any_sync(0xffffffffu, sl.neg);
     // group sum of the lane's group: given, or the tree over the slice's values
     // completed across the group's lanes
     if (a.prologue == kProNone) {
@@ -624,6 +628,16 @@ __global__ void __launch_bounds__(layout_threads(kLayout), layout_blocks(kLayout
                     int rowsel = 0;
                     float d[H];
                     levels<R, 1, kL, kTree>(v, d, lane, rowsel);
+                    if (kTree && sl.exact && sl.anyneg) {
+                        // The exact path's tree values equal RN's except that
+                        // a zero is always +0 (q = 0 products are x' - x').  In
+                        // an all-negative group every product is <= 0, so the
+                        // sum is zero only when every q is 0, and then RN's
+                        // products and sum are all -0.  Elsewhere a zero sum
+                        // holds a +0 product or a cancellation: +0 either way.
+#pragma unroll
+                        for (int i = 0; i < H; ++i) d[i] = (sl.neg && d[i] == 0.f) ? kNegZero : d[i];
+                    }
                     const int ofs = rowsel;
                     // affine term per (row, group); groups past the row end add
                     // -0.  Branch-free: rows past a ragged tile's end read the

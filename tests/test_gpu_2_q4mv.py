@@ -183,9 +183,12 @@ def test_grouped_launch_matches_single_calls():
     g.close()
 
 
-def test_grouped_launch_plain_path():
-    """A grouped launch whose activation takes the plain product path (groups of all-negative values)."""
+def test_grouped_launch_negative_activation():
+    """A grouped launch over all-negative activations: the exact path with the
+    sign fix for zero group sums, one product holding rows whose every term is zero."""
     mats = [synth.random_case(80 + i, r, 1024)[0] for i, r in enumerate([2048, 256, 256])]
+    mats[1].w[:3] = 0
+    mats[1].bias[:3] = 0.0
     x = -np.abs(synth.activations(np.random.default_rng(10), 1024))
     xs = oracle.gsum(x)
     xd, xsd = dev(x), dev(xs)
@@ -196,7 +199,7 @@ def test_grouped_launch_plain_path():
     g.launch()
     torch.cuda.synchronize()
     for m, y in zip(mats, ys):
-        assert_bits_equal(host(y), oracle.q4mv(*m.arrays(), x, xs, 1024), "grouped plain path")
+        assert_bits_equal(host(y), oracle.q4mv(*m.arrays(), x, xs, 1024), "grouped negative")
     g.close()
     assert abg.device_status(clear=True) == 0
 
@@ -213,6 +216,48 @@ def test_mixed_negative_groups(cols):
     xs = oracle.gsum(x)
     assert_bits_equal(run(m, x, xs=xs), oracle.q4mv(*m.arrays(), x, xs, cols), f"mixed {cols}")
     assert abg.device_status(clear=True) == 0
+
+
+def zero_group_case(seed, rows, cols, group=64):
+    """All-negative activations with zero groups planted in the weights: rows
+    0..9 all nibbles and bias zero (the oracle's y is -0), rows 40..79 one zero
+    group each, rows 100..109 one zero group whose bias is also zero."""
+    m, x = synth.random_case(seed, rows, cols)
+    x = -np.abs(x)
+    G, wpg = cols // group, group // 8
+    rng = np.random.default_rng(seed)
+    m.w[:10] = 0
+    m.bias[:10] = 0.0
+    for r in range(40, min(rows, 110)):
+        if 80 <= r < 100:
+            continue
+        g = int(rng.integers(G))
+        m.w[r, wpg * g:wpg * (g + 1)] = 0
+        if r >= 100:
+            m.bias[r, g] = 0.0
+    return m, x
+
+
+@pytest.mark.parametrize("rpw", [1, 2, 4, 8])
+@pytest.mark.parametrize("cols", [256, 1088, 2048, 6144])
+def test_zero_groups_of_negative_activations(rpw, cols):
+    """All-negative groups take the exact product path, whose zero sums are +0;
+    there a zero group sum means every q is 0, and RN's sum is -0 (RN(0*x) = -0),
+    so rows whose every term is zero come out -0 like the oracle's, and rows
+    with a single zero group match bit for bit."""
+    m, x = zero_group_case(400 + cols, 300, cols)
+    exp = expect(m, x)
+    assert (exp[:10] == 0).all() and np.signbit(exp[:10]).all()
+    assert_bits_equal(run(m, x, rpw=rpw), exp, f"zero groups {cols} R={rpw}")
+    assert abg.device_status(clear=True) == 0
+
+
+def test_zero_groups_fast_mode():
+    """Fast mode does not fix the sign of zero group sums; zeros of either sign are within the bound."""
+    m, x = zero_group_case(401, 300, 2048)
+    xs = oracle.gsum(x)
+    y = run(m, x, mode=abg.FAST)
+    assert_fast_close(y, oracle.q4mv(*m.arrays(), x, xs, 2048), oracle.q4mv_absmag(*m.arrays(), x, xs, 2048), what="zero groups fast")
 
 
 def test_no_device_timeouts():

@@ -124,8 +124,9 @@ def test_row_range_and_unaligned_scale_bias(group, sb):
 @pytest.mark.parametrize("group", synth.GROUPS)
 @pytest.mark.parametrize("case", ["neg_zero", "inf", "nan", "all_negative", "mixed_negative_groups"])
 def test_formats_special_activations(group, case):
-    """Values outside the fused-multiply-add identity take the plain path: a group
-    spans 1, 2 or 4 lanes, and its all-negative test must cover exactly those."""
+    """Values outside the fused-multiply-add identity take the plain path; groups
+    of all-negative values (spanning 1, 2 or 4 lanes) are marked for the sign
+    of a zero group sum, and the mark must cover exactly the group's lanes."""
     m, x = synth.fmt_case(group, "bf16", 70, 2048)
     x = x.copy()
     if case == "neg_zero":
@@ -155,6 +156,29 @@ def test_all_q_zero_with_negative_group_keeps_signed_zero():
         m.bias[:] = 0.0
         x = -np.abs(x)
         assert_bits_equal(run(m, x), expect(m, x), f"signed zero g{group}")
+
+
+@pytest.mark.parametrize("group", synth.GROUPS)
+@pytest.mark.parametrize("sb", synth.SB_TYPES)
+def test_formats_zero_groups_of_negative_activations(group, sb):
+    """All-negative activations with planted zero groups (whole rows with zero
+    bias, single groups, single groups with zero bias): the exact path with the
+    sign fix for zero group sums must give the oracle's bits, -0 results included."""
+    m, x = synth.fmt_case(group, sb, 150, 2048)
+    x = -np.abs(x)
+    G, wpg = 2048 // group, group // 8
+    rng = np.random.default_rng(group)
+    m.w[:6] = 0
+    m.bias[:6] = 0
+    for r in range(20, 60):
+        g = int(rng.integers(G))
+        m.w[r, wpg * g:wpg * (g + 1)] = 0
+        if r >= 40:
+            m.bias[r, g] = 0
+    exp = expect(m, x)
+    assert (exp[:6] == 0).all() and np.signbit(exp[:6]).all()
+    assert_bits_equal(run(m, x), exp, f"zero groups g{group} {sb}")
+    assert abg.device_status(clear=True) == 0
 
 
 @pytest.mark.parametrize("group", synth.GROUPS)

@@ -68,8 +68,8 @@ def test_batched_fast_within_bound(T):
 
 @pytest.mark.parametrize("T", [2, 3, 4])
 def test_batched_special_and_negative_tokens(T):
-    """One token with -0, inf and NaN, one with all-negative groups: the slices take
-    the plain path for the whole batch, every token still exact."""
+    """One token with -0, inf and NaN (the plain path for the whole batch), one
+    with all-negative groups: every token still exact."""
     m, _ = synth.random_case(3200, 200, 2048)
     X = tokens(3, T, 2048)
     X[0, ::7] = -0.0
@@ -79,6 +79,30 @@ def test_batched_special_and_negative_tokens(T):
     if T > 2:
         X[2, 64:128] = -np.abs(X[2, 64:128])
     assert_bits_equal(run(m, X), expect(m, X), f"special T={T}")
+    assert abg.device_status(clear=True) == 0
+
+
+@pytest.mark.parametrize("T", [1, 2, 3, 4])
+def test_batched_zero_groups_of_negative_tokens(T):
+    """Tokens of all-negative values (token 1 of a pair mixed) with planted zero
+    groups: whole rows with zero bias (-0 results for the negative tokens) and
+    single zero groups; the sign of each token's zero group sums as RN's."""
+    m, _ = synth.random_case(3250, 200, 2048)
+    X = -np.abs(tokens(6, T, 2048))
+    if T > 1:
+        X[1] = np.abs(X[1])
+        X[1, ::2] *= -1
+    rng = np.random.default_rng(T)
+    m.w[:5] = 0
+    m.bias[:5] = 0.0
+    for r in range(30, 70):
+        g = int(rng.integers(32))
+        m.w[r, 8 * g:8 * g + 8] = 0
+        if r >= 50:
+            m.bias[r, g] = 0.0
+    exp = expect(m, X)
+    assert (exp[0, :5] == 0).all() and np.signbit(exp[0, :5]).all()
+    assert_bits_equal(run(m, X), exp, f"zero groups T={T}")
     assert abg.device_status(clear=True) == 0
 
 
