@@ -78,6 +78,8 @@ int sm_count() {
 }
 
 namespace {
+constexpr int kFewTilesPerSm = 4;
+
 bool plan_once(Q4Plan *plan, const Q4Prob *probs, int nprob, int cols, int group, int sb_type, int prologue,
                const float *x, const float *xsum, const float *wt, float eps, bool tree, int rows_per_warp,
                bool sb_smem, const Q4Tuning &tune) {
@@ -106,8 +108,6 @@ bool plan_once(Q4Plan *plan, const Q4Prob *probs, int nprob, int cols, int group
     const int kk = (nch <= nw) ? nw / nch : 1;  // warps per chunk position
     const uint32_t row_bytes = static_cast<uint32_t>(C / 2) + (sb_smem ? 2u * G * elem : 0u);
     const uint32_t fixed = 1024;  // barriers and alignment slack
-    uint32_t budget = static_cast<uint32_t>(tune.smem_kb > 0 ? tune.smem_kb : (wide ? 220 : 110)) * 1024u;
-    const uint32_t hard_max = 225u * 1024u;  // leaves room for the static shared memory
     // tile rows: a multiple of R*kk so row blocks spread evenly over the warps
     const int unit = R * kk;
     int TR = unit;
@@ -115,6 +115,18 @@ bool plan_once(Q4Plan *plan, const Q4Prob *probs, int nprob, int cols, int group
     while (TR * 2 <= nw * 32 && (TR * 2) * row_bytes <= stage_target) TR *= 2;
     TR = std::min(TR, nw * 32);
     if (TR < R) return false;
+    // A launch of few tiles (at most kFewTilesPerSm per SM, e.g. a decode
+    // token's products) runs one block per SM with a larger stage ring: two
+    // blocks of a small launch would share some SMs and leave others idle,
+    // and those SMs finish last.  Large launches keep two blocks per SM,
+    // which hides each block's per-tile bubbles behind the other.
+    int64_t tiles_est = 0;
+    for (int i = 0; i < nprob; ++i) tiles_est += (probs[i].n + TR - 1) / TR;
+    const bool few = !wide && tune.smem_kb == 0 && tune.blocks_per_sm == 0 &&
+                     tiles_est <= static_cast<int64_t>(kFewTilesPerSm) * sm_count();
+    uint32_t budget =
+        static_cast<uint32_t>(tune.smem_kb > 0 ? tune.smem_kb : (wide ? 220 : (few ? 160 : 110))) * 1024u;
+    const uint32_t hard_max = 225u * 1024u;  // leaves room for the static shared memory
     auto stage_bytes = [&](int tr) {
         return align_up(static_cast<uint32_t>(tr) * (C / 2), 16) +
                2u * align_up(sb_smem ? static_cast<uint32_t>(tr) * G * elem : 0u, 16);
@@ -179,7 +191,7 @@ bool plan_once(Q4Plan *plan, const Q4Prob *probs, int nprob, int cols, int group
             fit = nb;
     }
     cudaGetLastError();
-    int bps = std::min(fit, wide ? 1 : (tune.blocks_per_sm > 0 ? tune.blocks_per_sm : 2));
+    int bps = std::min(fit, wide ? 1 : (tune.blocks_per_sm > 0 ? tune.blocks_per_sm : (few ? 1 : 2)));
     bps = std::max(bps, 1);
     const int64_t cap = static_cast<int64_t>(sm_count()) * bps;
     plan->grid = dim3(static_cast<unsigned>(std::max<int64_t>(1, std::min(a.total_tiles, cap))));
