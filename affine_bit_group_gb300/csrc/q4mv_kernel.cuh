@@ -185,6 +185,28 @@ __device__ __forceinline__ float tree32(const float (&v)[32]) {
     return t[0];
 }
 
+// The factor from the C/64 block sums of squares posted in red: one warp takes
+// the tree over them, every computing thread (nct, named barrier 1) reads it.
+template <bool kTree>
+__device__ __forceinline__ float rms_from_blocks(float *red, int C, float eps, int cw, int nct, float *rbox) {
+    named_bar(1, nct);
+    if (cw == 0) {
+        const float ss = warp_tree_smem(red, C / 64);
+        if ((threadIdx.x & 31) == 0) {
+            float r;
+            if (kTree) {
+                const float mean = __fdiv_rn(ss, static_cast<float>(C));
+                r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(mean, eps)));
+            } else {
+                r = rsqrtf(ss / static_cast<float>(C) + eps);
+            }
+            *rbox = r;
+        }
+    }
+    named_bar(1, nct);
+    return *rbox;
+}
+
 // The same factor computed by all computing warps of a block together: each
 // 64-value group is summed by 8 lanes (8 consecutive squares each, then a
 // 3-step butterfly: the pairwise tree over 8 blocks of 8), group sums meet in
@@ -210,22 +232,7 @@ __device__ float block_rms_factor(const float *__restrict__ x, int C, float eps,
         for (int d = 1; d < 8; d <<= 1) s = __fadd_rn(s, __shfl_xor_sync(0xffffffffu, s, d));
         if (g < G && (lane & 7) == 0) red[g] = s;
     }
-    named_bar(1, nct);
-    if (cw == 0) {
-        const float ss = warp_tree_smem(red, G);
-        if (lane == 0) {
-            float r;
-            if (kTree) {
-                const float mean = __fdiv_rn(ss, static_cast<float>(C));
-                r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(mean, eps)));
-            } else {
-                r = rsqrtf(ss / static_cast<float>(C) + eps);
-            }
-            *rbox = r;
-        }
-    }
-    named_bar(1, nct);
-    return *rbox;
+    return rms_from_blocks<kTree>(red, C, eps, cw, nct, rbox);
 }
 
 // One warp's slice of the activation: columns ch*1024 + lane*32 + (0..31).
@@ -237,43 +244,11 @@ struct Slice {
     bool anyneg;   // tree mode, warp-uniform: some lane's group is all negative
 };
 
+// The rest of a slice from its activation values v (zero where inactive):
+// the product path, the group sums, and the pairs X of lane_sum32.
 template <bool kTree, int kLg>
-__device__ __forceinline__ void load_slice(const Q4Args &a, int ch, int lane, float rms_r, Slice &sl) {
-    const int C = a.cols, base = ch * 1024 + lane * 32;
-    const bool active = base < C;
-    float v[32];
-#pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = 0.f;
-    if (active) {
-        const float4 *x4 = reinterpret_cast<const float4 *>(a.x + base);
-        if (a.prologue == kProNone || a.prologue == kProGsum) {
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const float4 q = x4[i];
-                v[4 * i] = q.x, v[4 * i + 1] = q.y, v[4 * i + 2] = q.z, v[4 * i + 3] = q.w;
-            }
-        } else if (a.prologue == kProRmsq) {
-            const float4 *w4 = reinterpret_cast<const float4 *>(a.wt + base);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const float4 q = x4[i], w = w4[i];
-                v[4 * i] = __fmul_rn(__fmul_rn(q.x, rms_r), w.x);
-                v[4 * i + 1] = __fmul_rn(__fmul_rn(q.y, rms_r), w.y);
-                v[4 * i + 2] = __fmul_rn(__fmul_rn(q.z, rms_r), w.z);
-                v[4 * i + 3] = __fmul_rn(__fmul_rn(q.w, rms_r), w.w);
-            }
-        } else {  // kProSwq: x = [gate | up]
-            const float4 *u4 = reinterpret_cast<const float4 *>(a.x + C + base);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const float4 g = x4[i], u = u4[i];
-                v[4 * i] = swiglu<kTree>(g.x, u.x);
-                v[4 * i + 1] = swiglu<kTree>(g.y, u.y);
-                v[4 * i + 2] = swiglu<kTree>(g.z, u.z);
-                v[4 * i + 3] = swiglu<kTree>(g.w, u.w);
-            }
-        }
-    }
+__device__ __forceinline__ void finish_slice(const Q4Args &a, int ch, int lane, bool active, float (&v)[32],
+                                             Slice &sl) {
     // special values take the plain path; groups whose values are all
     // negative are marked for the sign of a zero group sum (see the product
     // loop)
@@ -320,6 +295,85 @@ __device__ __forceinline__ void load_slice(const Q4Args &a, int ch, int lane, fl
             sl.X[m] = f2(v[m], v[m + 16]);
         }
     }
+}
+
+template <bool kTree, int kLg>
+__device__ __forceinline__ void load_slice(const Q4Args &a, int ch, int lane, float rms_r, Slice &sl) {
+    const int C = a.cols, base = ch * 1024 + lane * 32;
+    const bool active = base < C;
+    float v[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = 0.f;
+    if (active) {
+        const float4 *x4 = reinterpret_cast<const float4 *>(a.x + base);
+        if (a.prologue == kProNone || a.prologue == kProGsum) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float4 q = x4[i];
+                v[4 * i] = q.x, v[4 * i + 1] = q.y, v[4 * i + 2] = q.z, v[4 * i + 3] = q.w;
+            }
+        } else if (a.prologue == kProRmsq) {
+            const float4 *w4 = reinterpret_cast<const float4 *>(a.wt + base);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float4 q = x4[i], w = w4[i];
+                v[4 * i] = __fmul_rn(__fmul_rn(q.x, rms_r), w.x);
+                v[4 * i + 1] = __fmul_rn(__fmul_rn(q.y, rms_r), w.y);
+                v[4 * i + 2] = __fmul_rn(__fmul_rn(q.z, rms_r), w.z);
+                v[4 * i + 3] = __fmul_rn(__fmul_rn(q.w, rms_r), w.w);
+            }
+        } else {  // kProSwq: x = [gate | up]
+            const float4 *u4 = reinterpret_cast<const float4 *>(a.x + C + base);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float4 g = x4[i], u = u4[i];
+                v[4 * i] = swiglu<kTree>(g.x, u.x);
+                v[4 * i + 1] = swiglu<kTree>(g.y, u.y);
+                v[4 * i + 2] = swiglu<kTree>(g.z, u.z);
+                v[4 * i + 3] = swiglu<kTree>(g.w, u.w);
+            }
+        }
+    }
+    finish_slice<kTree, kLg>(a, ch, lane, active, v, sl);
+}
+
+// RMS-norm prologue in one pass over x, for warps that keep one chunk for the
+// whole launch: each lane loads its 32 values of x and of the weights once; the
+// 64-value block sums of squares come from those registers (the lane's 32
+// squares by the pairwise tree, then the partner lane's half: the same tree as
+// block_rms_factor's), one warp per chunk posts them (post), and the factor
+// scales the values in place.  Every computing warp calls this, idle ones with
+// has = false, since it holds the block barriers.
+template <bool kTree, int kLg>
+__device__ __forceinline__ void rms_slice(const Q4Args &a, int ch, bool has, bool post, int cw, int nw, int lane,
+                                          float *red, float *rbox, Slice &sl) {
+    const int C = a.cols, base = ch * 1024 + lane * 32;
+    const bool active = has && base < C;
+    float v[32], w[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = 0.f, w[i] = 0.f;
+    if (active) {
+        const float4 *x4 = reinterpret_cast<const float4 *>(a.x + base);
+        const float4 *w4 = reinterpret_cast<const float4 *>(a.wt + base);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float4 q = x4[i], u = w4[i];
+            v[4 * i] = q.x, v[4 * i + 1] = q.y, v[4 * i + 2] = q.z, v[4 * i + 3] = q.w;
+            w[4 * i] = u.x, w[4 * i + 1] = u.y, w[4 * i + 2] = u.z, w[4 * i + 3] = u.w;
+        }
+    }
+    float sq[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) sq[i] = __fmul_rn(v[i], v[i]);
+    float s2 = tree32(sq);
+    s2 = __fadd_rn(s2, __shfl_xor_sync(0xffffffffu, s2, 1));
+    if (post && active && (lane & 1) == 0) red[base >> 6] = s2;
+    const float r = rms_from_blocks<kTree>(red, C, a.eps, cw, nw * 32, rbox);
+    if (active) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = __fmul_rn(__fmul_rn(v[i], r), w[i]);
+    }
+    finish_slice<kTree, kLg>(a, ch, lane, active, v, sl);
 }
 
 // Locates tiles of a grouped launch.  A block visits its tiles in increasing
@@ -532,8 +586,22 @@ __global__ void __launch_bounds__(layout_threads(kLayout), layout_blocks(kLayout
         grid_dep_wait();
         grid_dep_launch();
     }
+    Slice sl;
+    int cur_ch = -1;
     float rms_r = 0.f;
-    if (a.prologue == kProRmsq) rms_r = block_rms_factor<kTree>(a.x, a.cols, a.eps, cw, nw, lane, s_red, &s_rbox);
+    if (a.prologue == kProRmsq) {
+        // one pass over x, after which the warp's slice is ready for every
+        // tile; only in the main instantiations (tree mode, 8 rows per item,
+        // two blocks per SM, staged scale/bias): in the others the product
+        // loop would lose registers to it, so they keep the two passes
+        constexpr bool kOnePass = kTree && R == 8 && kLayout == 0 && kSbSmem;
+        if (kOnePass && fixed_ch) {
+            rms_slice<kTree, kLg>(a, ch0, !idle, rb0 == 0, cw, nw, lane, s_red, &s_rbox, sl);
+            if (!idle) cur_ch = ch0;
+        } else {
+            rms_r = block_rms_factor<kTree>(a.x, a.cols, a.eps, cw, nw, lane, s_red, &s_rbox);
+        }
+    }
     const bool f16 = a.sb_f16 != 0;
     // stored scale or bias i of a row block, from the stage or from global memory
     auto sb_at = [&](const void *base, int64_t i) -> float {
@@ -545,8 +613,6 @@ __global__ void __launch_bounds__(layout_threads(kLayout), layout_blocks(kLayout
             return kSbSmem ? static_cast<const float *>(base)[i] : __ldg(static_cast<const float *>(base) + i);
         }
     };
-    Slice sl;
-    int cur_ch = -1;
     // Final sums of tile j: thread ct adds row ct's chunk partials by the tree.
     ProbCursor cur, fcur;
     // (pi, dph): tile j's partial buffer and the parity of its done phase
