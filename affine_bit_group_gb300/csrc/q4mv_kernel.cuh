@@ -27,14 +27,18 @@
 //                      memory once per kernel, not once per row.
 //
 // Per lane and row a chunk is one 16-byte word quad (32 columns).  Nibble j of
-// a word is turned into the float 2^(23-4(j%4)) + q by OR-ing an exponent into
-// the masked word (the high half-word is shifted down first), and one fused
-// multiply-add with c = -2^(23-4(j%4)) * x gives RN(q * x) exactly: the exact
-// value (2^E + q)x - 2^E x = qx is rounded once.  So the product is the
-// correctly rounded q*x that the tree order calls for, at one logic op and one
-// FMA per weight (packed two at a time with the f32x2 ops).  The identity
-// needs x finite, not -0 and |x| < 2^100; a block whose x has any other value
-// takes the plain path (convert, then multiply), which is bit-identical.
+// a word sits at bit 4k of the word (j <= 4, k = j) or of the word shifted
+// right by 12 (j >= 5, k = j - 3); masking it and OR-ing in the sign and
+// exponent of -1.0 gives u = -(1 + q 2^(4k-23)), and with the activation held
+// as x' = -x 2^(23-4k) one fused multiply-add u x' + x' is q x exactly before
+// its single rounding: RN(q * x), the product the tree order calls for, at one
+// logic op and half a packed FMA per weight.  The identity needs x finite,
+// nonzero and |x| < 2^100; a warp whose slice holds any other value takes the
+// plain path (convert, then multiply).  Its one difference from RN is the sign
+// of a zero (q = 0 gives +0 where RN(0 * x) is -0 for x < 0), which can reach
+// the output only through a zero group sum of an all-negative group; there the
+// sum is set to -0 (see the product loop).  Both paths are bit-identical to
+// the plain definition.
 //
 // Reduction, tree order: the lane's 32 products are summed by the pairwise
 // tree (16 packed adds carry two columns 16 apart, so every level pairs the

@@ -65,20 +65,38 @@ def measured_peak():
     return PEAK_FALLBACK_GBS, "fallback"
 
 
+def code_sha256(path: str) -> str:
+    """sha256 of a C/CUDA source's code: // comments, trailing blanks and empty
+    lines removed, so that an edit of comments alone keeps a profile valid."""
+    out = []
+    with open(path) as f:
+        for line in f:
+            quote = False
+            cut = len(line)
+            for i, c in enumerate(line):
+                if c == '"' and (i == 0 or line[i - 1] != "\\"):
+                    quote = not quote
+                elif not quote and line.startswith("//", i):
+                    cut = i
+                    break
+            code = line[:cut].rstrip()
+            if code:
+                out.append(code)
+    return hashlib.sha256("\n".join(out).encode()).hexdigest()
+
+
 def profile_traffic(kernel_src: str, profile: str):
-    """DRAM bytes per launch from a committed ncu summary, or None once the kernel changed."""
+    """DRAM bytes per launch from a committed ncu summary, or None once the kernel's code changed."""
     path = os.path.join(ROOT, "profiles", profile)
     if not os.path.exists(path):
         return None
     vals = {}
     with open(path) as f:
         for line in f:
-            if ":" in line and line.strip().startswith(("dram_bytes_per_launch", "kernel_source_sha256")):
+            if ":" in line and line.strip().startswith(("dram_bytes_per_launch", "kernel_code_sha256")):
                 k, v = line.split(":", 1)
                 vals[k.strip()] = v.split()[0].strip("`")
-    with open(kernel_src, "rb") as f:
-        sha = hashlib.sha256(f.read()).hexdigest()
-    if vals.get("kernel_source_sha256") != sha or "dram_bytes_per_launch" not in vals:
+    if vals.get("kernel_code_sha256") != code_sha256(kernel_src) or "dram_bytes_per_launch" not in vals:
         return None
     return float(vals["dram_bytes_per_launch"])
 
