@@ -12,7 +12,7 @@ import pytest
 
 import oracle
 from affine_bit_group_gb300 import synth
-from helpers import assert_bits_equal, dev, empty, host
+from helpers import assert_bits_equal, assert_fast_close, dev, dev_words, empty, host
 
 pytestmark = pytest.mark.gpu
 
@@ -111,6 +111,37 @@ def test_graph_rejects_same_stage_hazards(small):
     with pytest.raises(abg.AbgError) as e:
         abg.StageGraph(nodes)
     assert e.value.status == 4
+
+
+@pytest.mark.parametrize("cols", [128, 1088, 2048, 6144, 16384])
+@pytest.mark.parametrize("rows", [40, 700, 9000])
+def test_rmsq_prologue_shapes(rows, cols):
+    """The RMS-norm prologue inside a product, over column counts with a ragged
+    last chunk (1088), up to 8 chunks (one pass over x, warps keeping one chunk)
+    and 16 chunks (two passes, warps walking chunks), and launches of few and of
+    many tiles: bit-exact in tree mode (the norm's tree and rounding are the
+    oracle's), within the bound in fast mode."""
+    rng = np.random.default_rng([rows, cols])
+    m = synth.q4_matrix(rng, rows, cols)
+    h = synth.activations(rng, cols)
+    wt = synth.rms_weights(rng, cols)
+    hd, wtd = dev(h), dev(wt)
+    w, sc, bi = dev_words(m.w), dev(m.scale), dev(m.bias)
+    xn, xs = oracle.rmsq(h, wt, 1e-6)
+    tree = oracle.q4mv(*m.arrays(), xn, xs, cols)
+    for mode in (abg.TREE, abg.FAST):
+        y = empty(rows)
+        g = abg.StageGraph([abg.Node.q4mv(0, w, sc, bi, y, cols, x=hd, wt=wtd, eps=1e-6, prologue=abg.PRO_RMSQ)],
+                           keep=[hd, wtd, w, sc, bi, y], mode=mode)
+        g.launch()
+        torch.cuda.synchronize()
+        if mode == abg.TREE:
+            assert_bits_equal(host(y), tree, f"rmsq prologue {rows}x{cols}")
+        else:
+            assert_fast_close(host(y), tree, oracle.q4mv_absmag(*m.arrays(), xn, xs, cols),
+                              what=f"fast rmsq prologue {rows}x{cols}")
+        g.close()
+    assert abg.device_status(clear=True) == 0
 
 
 @pytest.mark.slow
