@@ -179,7 +179,8 @@ bool plan_once(Q4Plan *plan, const Q4Prob *probs, int nprob, int cols, int group
     a.parts = S + 2;
     a.smem_bytes = a.off_bar + 8u * (2 * S + a.parts);
 
-    // blocks per SM: what fits (registers and shared memory), at most 2 unless tuned
+    // blocks per SM: what fits (registers and shared memory), at most 2 (1 for a
+    // launch of few tiles) unless tuned
     int fit = 1;
     void *fn = select_kernel(lg, half, R, tree, sb_smem, layout);
     if (!fn) return false;

@@ -596,7 +596,7 @@ __global__ void __launch_bounds__(layout_threads(kLayout), layout_blocks(kLayout
     if (a.prologue == kProRmsq) {
         // one pass over x, after which the warp's slice is ready for every
         // tile; only in the main instantiations (tree mode, 8 rows per item,
-        // two blocks per SM, staged scale/bias): in the others the product
+        // block layout 0, staged scale/bias): in the others the product
         // loop would lose registers to it, so they keep the two passes
         constexpr bool kOnePass = kTree && R == 8 && kLayout == 0 && kSbSmem;
         if (kOnePass && fixed_ch) {
