@@ -245,6 +245,33 @@ def test_q4mv_zero_weights_reduce_to_bias_term():
     assert np.all(y == np.float32(expected))
 
 
+def test_zero_group_sum_of_negative_activations_is_minus_zero():
+    """The fact the GPU kernels' sign rule rests on, checked on the plain
+    definition: with every x of a 64-value group negative, products RN(q*x)
+    are all <= 0, so the group sum d is zero exactly when every q of the group
+    is 0, and then d = -0 (the sum of -0 products); otherwise d < 0.  With
+    scale 1 and bias 0 the output is d itself (RN(1*d) + RN(0*xsum) = d + -0),
+    so each row's y shows its group sum, sign of zero included."""
+    rng = np.random.default_rng(11)
+    rows, cols = 400, 64
+    x = -np.abs(synth.activations(rng, cols)).astype(np.float32)
+    x[:8] = -np.float32(1e-40)  # subnormal magnitudes: q*x still never rounds to zero
+    q = rng.integers(0, 16, size=(rows, cols))
+    q[::3] = 0                                      # whole groups of zeros
+    q[1::3] = np.maximum(q[1::3], 1)                # no zero ...
+    for r in range(1, rows, 3):
+        q[r, rng.integers(0, cols)] = 0             # ... but one
+    scale = np.ones((rows, 1), np.float32)
+    bias = np.zeros((rows, 1), np.float32)
+    xs = oracle.gsum(x)
+    y = oracle.q4mv(pack_nibbles(q), scale, bias, x, xs, cols)
+    allzero = (q == 0).all(axis=1)
+    assert allzero.sum() == len(range(0, rows, 3))
+    assert np.all((y == 0) == allzero)
+    assert np.all(np.signbit(y[allzero]))
+    assert np.all(y[~allzero] < 0)
+
+
 def test_q4mv_row_range():
     """Array.q4go(w, x, y, r, n, cols, rows): rows r..r+n-1 of the matrix land in y[0..n)."""
     m, x = synth.random_case(9, 37, 256)
