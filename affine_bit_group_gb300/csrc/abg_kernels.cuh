@@ -68,6 +68,7 @@ struct Q4Plan {
     bool tree;
     bool sb_smem;
     int layout;  // block layout (see the kernel)
+    int shape = 0;  // row length of a fixed-shape instantiation (0: sizes from the arguments)
     int lg;      // group size 32 << lg
     bool half;   // 16-bit scale and bias
     int mm = 0;  // batched product: kernel width in tokens (0: single token)

@@ -22,14 +22,18 @@ cudaError_t q4mv_status_g32h(unsigned *bits, bool clear);
 cudaError_t q4mv_status_g64h(unsigned *bits, bool clear);
 cudaError_t q4mv_status_g128(unsigned *bits, bool clear);
 cudaError_t q4mv_status_g128h(unsigned *bits, bool clear);
+void *q4mv_select_fixed(int cols, bool tree);
+cudaError_t q4mv_status_fixed(unsigned *bits, bool clear);
 
 namespace {
 
 // The instantiation for a format (group = 32 << lg columns; 16-bit scale and
 // bias when half), rows per item, mode, scale/bias staging and block layout;
 // nullptr if it is not built (layouts 1 and 2 exist for the default format
-// with 8 rows per item only).
-void *select_kernel(int lg, bool half, int R, bool tree, bool sb, int layout) {
+// with 8 rows per item only).  shape != 0 selects the fixed-shape
+// instantiation for that row length (q4mv_fixed.cu).
+void *select_kernel(int lg, bool half, int R, bool tree, bool sb, int layout, int shape = 0) {
+    if (shape != 0) return q4mv_select_fixed(shape, tree);
     if (lg == 1 && !half) {
         if (layout == 0) return select_layout0<1, false>(R, tree, sb);
         if (R != 8) return nullptr;
@@ -57,8 +61,9 @@ inline uint32_t align_up(uint32_t v, uint32_t a) { return (v + a - 1) / a * a; }
 }  // namespace
 
 cudaError_t q4mv_status(unsigned *bits, bool clear) {
-    cudaError_t (*const units[])(unsigned *, bool) = {read_status_word, q4mv_status_g32, q4mv_status_g32h,
-                                                      q4mv_status_g64h, q4mv_status_g128, q4mv_status_g128h};
+    cudaError_t (*const units[])(unsigned *, bool) = {read_status_word,   q4mv_status_g32,  q4mv_status_g32h,
+                                                      q4mv_status_g64h,   q4mv_status_g128, q4mv_status_g128h,
+                                                      q4mv_status_fixed};
     for (auto f : units) {
         const cudaError_t e = f(bits, clear);
         if (e != cudaSuccess) return e;
@@ -179,10 +184,18 @@ bool plan_once(Q4Plan *plan, const Q4Prob *probs, int nprob, int cols, int group
     a.parts = S + 2;
     a.smem_bytes = a.off_bar + 8u * (2 * S + a.parts);
 
+    // a plan with the compile-time shape of its row length runs the
+    // fixed-shape instantiation (same results, constant sizes)
+    int shape = 0;
+    if (fmt_default && sb_smem && layout == 0 && R == 8 && (C == 2048 || C == 4096 || C == 6144) &&
+        TR == fixed_tr(C, 8) && nw == fixed_nw(C) && nch == fixed_nch(C) &&
+        a.stage_w_bytes == static_cast<uint32_t>(TR * C / 2) && a.stage_sb_bytes == static_cast<uint32_t>(TR * G * 4))
+        shape = C;
+
     // blocks per SM: what fits (registers and shared memory), at most 2 (1 for a
     // launch of few tiles) unless tuned
     int fit = 1;
-    void *fn = select_kernel(lg, half, R, tree, sb_smem, layout);
+    void *fn = select_kernel(lg, half, R, tree, sb_smem, layout, shape);
     if (!fn) return false;
     if (raise_smem_limit(fn) == cudaSuccess) {
         int nb = 0;
@@ -201,6 +214,7 @@ bool plan_once(Q4Plan *plan, const Q4Prob *probs, int nprob, int cols, int group
     plan->tree = tree;
     plan->sb_smem = sb_smem;
     plan->layout = layout;
+    plan->shape = shape;
     plan->lg = lg;
     plan->half = half;
     plan->mm = 0;
@@ -242,14 +256,14 @@ bool plan_q4mv(Q4Plan *plan, const Q4Prob *probs, int nprob, int cols, int group
 }
 
 cudaError_t prepare_q4mv(const Q4Plan &plan) {
-    void *fn = select_kernel(plan.lg, plan.half, plan.rows_per_warp, plan.tree, plan.sb_smem, plan.layout);
+    void *fn = select_kernel(plan.lg, plan.half, plan.rows_per_warp, plan.tree, plan.sb_smem, plan.layout, plan.shape);
     if (!fn) return cudaErrorInvalidValue;
     return raise_smem_limit(fn);
 }
 
 cudaError_t launch_q4mv(const Q4Plan &plan, cudaStream_t stream, bool pdl) {
     if (plan.args.total_tiles == 0) return cudaSuccess;
-    void *fn = select_kernel(plan.lg, plan.half, plan.rows_per_warp, plan.tree, plan.sb_smem, plan.layout);
+    void *fn = select_kernel(plan.lg, plan.half, plan.rows_per_warp, plan.tree, plan.sb_smem, plan.layout, plan.shape);
     if (!fn) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = plan.grid;

@@ -58,6 +58,8 @@
 
 #include <cuda_fp16.h>
 
+#include <type_traits>
+
 namespace abg {
 
 namespace {
@@ -243,9 +245,13 @@ __device__ float block_rms_factor(const float *__restrict__ x, int C, float eps,
 struct Slice {
     float2 X[16];  // see lane_sum32
     float xs;      // group sum of the group the lane's columns belong to
+    float xsp;     // group sum of the partner group (the other group of its pair)
     bool exact;    // warp-uniform: the exact path applies to the whole slice
     bool neg;      // tree mode: every activation of this lane's group is negative
     bool anyneg;   // tree mode, warp-uniform: some lane's group is all negative
+    bool act;      // the lane's columns lie inside the row
+    bool actp;     // the partner group's columns lie inside the row
+    bool full;     // warp-uniform: every lane's columns lie inside the row
 };
 
 // The rest of a slice from its activation values v (zero where inactive):
@@ -290,6 +296,12 @@ __device__ __forceinline__ void finish_slice(const Q4Args &a, int ch, int lane, 
         }
         sl.xs = t;
     }
+    // the partner group g ^ 1 sits kL lanes away (groups are aligned pairs of
+    // 2 kL lanes); its sum and activity feed the paired affine term
+    sl.xsp = __shfl_xor_sync(0xffffffffu, sl.xs, 1 << kLg);
+    sl.act = active;
+    sl.actp = __shfl_xor_sync(0xffffffffu, active ? 1 : 0, 1 << kLg) != 0;
+    sl.full = __all_sync(0xffffffffu, active);
 #pragma unroll
     for (int m = 0; m < 16; ++m) {
         if (sl.exact) {
@@ -480,6 +492,7 @@ __device__ __forceinline__ void levels(float (&v)[N], float (&out)[lv_count<N, D
 // i.e. after every warp released tile k - S, by which time the finishing
 // warps have completed the final sums of tile k - S - 2.  Tiles k - S - 1 .. k
 // hold S + 2 distinct buffers, so no buffer is rewritten while still read.
+// A launch whose rows fit in one 1024-column chunk writes y directly.
 
 // Block layouts (the register file is split over the SM's four schedulers,
 // so the warps per SM set the registers per thread):
@@ -490,20 +503,135 @@ __device__ __forceinline__ void levels(float (&v)[N], float (&out)[lv_count<N, D
 constexpr int layout_threads(int l) { return l == 1 ? 544 : (l == 2 ? 224 : 288); }
 constexpr int layout_blocks(int l) { return l == 1 ? 1 : 2; }
 
-template <int R, bool kTree, bool kSbSmem, int kLayout, int kLg, bool kHalf>
+// Where a tile's results go.  The producer writes the header of a block's
+// k-th tile into slot k mod (S + 2) -- the slot of the tile's partial-sum
+// buffer -- before it arms the tile's `full` barrier (that arrival releases
+// the write; the computing warps' wait on the barrier acquires it).  The slot
+// is rewritten for tile k + S + 2 only after every warp has released tile
+// k + 2, and a warp reads it at tile k and, for the final sums, before it
+// starts tile k + 2.
+struct TileHdr {
+    float *y;        // output of the tile's first row
+    const void *sc;  // scale and bias of the tile's first row in global memory
+    const void *bi;  // (read there when they are not staged)
+    int rows;        // rows of the tile: tile_rows, fewer at a problem's end
+    int pad;
+};
+constexpr int kMaxStages = 8;
+constexpr int kMaxHdr = kMaxStages + 2;
+
+__host__ __device__ constexpr int log2_rows(int r) { return r >= 8 ? 3 : (r >= 4 ? 2 : (r >= 2 ? 1 : 0)); }
+
+// The lane's row permutation pi: the low log2(R) bits of the lane index,
+// reversed.  Item value v[i] holds row (i ^ pi) of its row block, so two lanes
+// kL apart (a butterfly level's partners) hold each row in registers whose
+// indices differ exactly in the bit that level splits.
+template <int kBits>
+__device__ __forceinline__ int rev_lane_bits(int lane) {
+    int r = 0;
+#pragma unroll
+    for (int b = 0; b < kBits; ++b) r |= ((lane >> b) & 1) << (kBits - 1 - b);
+    return r;
+}
+
+// Butterfly levels over lanes at distances D, 2D, ... below E, on N held
+// values with the row permutation above: while N > 1 every lane keeps v[i]
+// (i < N/2) plus its partner's v[N/2 + i], which is the same row (transposed
+// step, no lane-dependent selection); with one value left the remaining
+// levels are plain butterfly steps.  Each sum pairs the same two leaves as
+// the pairwise tree.
+template <int N, int D, int E, bool kTree>
+__device__ __forceinline__ void plevels(const float (&v)[N], float (&out)[lv_count<N, D, E>()]) {
+    if constexpr (D >= E) {
+#pragma unroll
+        for (int i = 0; i < N; ++i) out[i] = v[i];
+    } else if constexpr (N == 1) {
+        float val = v[0];
+#pragma unroll
+        for (int dd = D; dd < E; dd <<= 1) {
+            const float o = __shfl_xor_sync(0xffffffffu, val, dd);
+            val = kTree ? __fadd_rn(val, o) : val + o;
+        }
+        out[0] = val;
+    } else {
+        float w[N / 2];
+#pragma unroll
+        for (int i = 0; i < N / 2; ++i) {
+            const float o = __shfl_xor_sync(0xffffffffu, v[N / 2 + i], D);
+            w[i] = kTree ? __fadd_rn(v[i], o) : v[i] + o;
+        }
+        plevels<N / 2, 2 * D, E, kTree>(w, out);
+    }
+}
+
+// Tree sum of a row's m chunk partials p[0..m) (m <= 16): the pairwise tree,
+// odd element carried, as the tree over the partials padded with -0.
+template <bool kTree>
+__device__ __forceinline__ float tree_chunks(const float *p, int m) {
+    auto add = [](float x, float y) { return kTree ? __fadd_rn(x, y) : x + y; };
+    if (m == 2) return add(p[0], p[1]);
+    float v[16];
+    if (m <= 4) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) v[i] = i < m ? p[i] : kNegZero;
+        return add(add(v[0], v[1]), add(v[2], v[3]));
+    }
+    const int n = m <= 8 ? 8 : 16;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = i < m ? p[i] : kNegZero;
+    for (int h = n / 2; h >= 1; h >>= 1)
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            if (i < h) v[i] = add(v[2 * i], v[2 * i + 1]);
+    return v[0];
+}
+
+// Compile-time tile shape of a product of kC columns in groups of 64 with f32
+// scale and bias staged, block layout 0 and R rows per item, following the
+// planner's rule for the default tuning: computing warps a multiple of the
+// chunk count (at most 8), tile rows doubled from R times the warps per chunk
+// while a tile stays within one row per computing thread and a 40 KB stage.
+// A launch whose plan has exactly this shape may use the kC instantiation,
+// in which the shape's sizes and offsets are constants.
+__host__ __device__ constexpr int fixed_nch(int C) { return (C + 1023) / 1024; }
+__host__ __device__ constexpr int fixed_nw(int C) { return fixed_nch(C) <= 8 ? fixed_nch(C) * (8 / fixed_nch(C)) : 8; }
+__host__ __device__ constexpr int fixed_tr(int C, int R) {
+    const int nch = fixed_nch(C), nw = fixed_nw(C), kk = nch <= nw ? nw / nch : 1;
+    const int row_bytes = C / 2 + 2 * (C / 64) * 4;
+    int tr = R * kk;
+    while (tr * 2 <= nw * 32 && tr * 2 * row_bytes <= 40 * 1024) tr *= 2;
+    return tr < nw * 32 ? tr : nw * 32;
+}
+
+template <int R, bool kTree, bool kSbSmem, int kLayout, int kLg, bool kHalf, int kC = 0>
 __global__ void __launch_bounds__(layout_threads(kLayout), layout_blocks(kLayout))
     q4mv_kernel(const __grid_constant__ Q4Args a) {
+    static_assert(kC == 0 || (kLayout == 0 && kLg == 1 && !kHalf && kSbSmem), "fixed shapes: default format only");
+    constexpr bool kFix = kC != 0;
     constexpr int kL = 1 << kLg;                  // lanes per group
     constexpr uint32_t kElem = kHalf ? 2u : 4u;   // bytes per stored scale or bias
+    constexpr int kLogR = log2_rows(R);
+    // values a lane holds after the group completion (levels below kL) and
+    // after the exchange with the partner group (level kL), each then a pair
+    constexpr int NA = lv_count<R, 1, kL>();
+    constexpr bool kSplitB = NA > 1;
+    constexpr int NB = kSplitB ? NA / 2 : 1;
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ volatile int s_abort;
     __shared__ float s_red[ABG_MAX_COLS / 64];  // group sums of squares (RMS-norm prologue)
     __shared__ float s_rbox;
+    __shared__ TileHdr s_hdr[kMaxHdr];
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + a.off_bar);
     uint64_t *empty = full + a.stages;
     uint64_t *done = empty + a.stages;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int S = a.stages, TR = a.tile_rows, W = a.W, G = a.G, nch = a.nch, nw = a.nw;
+    // shape: constants in a fixed-shape instantiation, else from the plan
+    const int S = a.stages;
+    const int TR = kFix ? fixed_tr(kC, R) : a.tile_rows, W = kFix ? kC / 8 : a.W, G = kFix ? kC / 64 : a.G;
+    const int nch = kFix ? fixed_nch(kC) : a.nch, nw = kFix ? fixed_nw(kC) : a.nw;
+    const uint32_t stage_w_bytes = kFix ? static_cast<uint32_t>(fixed_tr(kC, R) * kC / 2) : a.stage_w_bytes;
+    const uint32_t stage_sb_bytes = kFix ? static_cast<uint32_t>(fixed_tr(kC, R) * (kC / 64) * 4) : a.stage_sb_bytes;
+    const uint32_t stage_bytes = kFix ? stage_w_bytes + 2 * stage_sb_bytes : a.stage_bytes;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -533,7 +661,8 @@ __global__ void __launch_bounds__(layout_threads(kLayout), layout_blocks(kLayout
         const int total = static_cast<int>(a.total_tiles);
         // eph: parity of the empty phase that frees stage s for round k / S,
         // i.e. ((k / S) & 1) ^ 1 (the consumers' release of the round before)
-        int k = 0, s = 0;
+        int k = 0, s = 0, hs = 0;
+        const int NP = a.parts;
         uint32_t eph = 1;
         for (int t = blockIdx.x; t < total; t += gridDim.x, ++k) {
             if (a.withhold) break;  // self-test: nothing is copied, nothing is in flight
@@ -548,16 +677,22 @@ __global__ void __launch_bounds__(layout_threads(kLayout), layout_blocks(kLayout
             const Q4Prob &P = a.prob[cur.find(a, t, tile)];
             const int64_t r0 = static_cast<int64_t>(tile) * TR;
             const int rows = static_cast<int>(min(static_cast<int64_t>(TR), P.n - r0));
-            unsigned char *st = smem + a.off_stage + static_cast<size_t>(s) * a.stage_bytes;
+            unsigned char *st = smem + a.off_stage + static_cast<size_t>(s) * stage_bytes;
             const uint32_t wb = static_cast<uint32_t>(rows) * W * 4u;
             const uint32_t sbb = kSbSmem ? static_cast<uint32_t>(rows) * G * kElem : 0u;
+            const size_t sbo = static_cast<size_t>(r0) * G * kElem;
+            TileHdr &h = s_hdr[hs];
+            if (++hs == NP) hs = 0;
+            h.y = P.y + r0;
+            h.sc = static_cast<const unsigned char *>(P.scale) + sbo;
+            h.bi = static_cast<const unsigned char *>(P.bias) + sbo;
+            h.rows = rows;
             mbar_arrive_expect_tx(&full[s], wb + 2 * sbb);
             bulk_g2s(st, P.w + r0 * W, wb, &full[s], policy);
             if (kSbSmem) {
-                const size_t sbo = static_cast<size_t>(r0) * G * kElem;
-                bulk_g2s(st + a.stage_w_bytes, static_cast<const unsigned char *>(P.scale) + sbo, sbb, &full[s],
+                bulk_g2s(st + stage_w_bytes, static_cast<const unsigned char *>(P.scale) + sbo, sbb, &full[s],
                          policy);
-                bulk_g2s(st + a.stage_w_bytes + a.stage_sb_bytes, static_cast<const unsigned char *>(P.bias) + sbo,
+                bulk_g2s(st + stage_w_bytes + stage_sb_bytes, static_cast<const unsigned char *>(P.bias) + sbo,
                          sbb, &full[s], policy);
             }
             if (++s == S) {
@@ -577,7 +712,8 @@ __global__ void __launch_bounds__(layout_threads(kLayout), layout_blocks(kLayout
 
     // ---------------------------------------------------- consumer warps ----
     const int ct = threadIdx.x - 32, cw = warp - 1;
-    float *part = reinterpret_cast<float *>(smem + a.off_part);
+    float *const part = reinterpret_cast<float *>(smem + a.off_part);
+    const unsigned char *const stage0 = smem + a.off_stage;
     // chunk positions and row blocks of this warp
     const bool fixed_ch = nch <= nw;
     const int kk = fixed_ch ? nw / nch : 1;
@@ -585,6 +721,7 @@ __global__ void __launch_bounds__(layout_threads(kLayout), layout_blocks(kLayout
     const int ch0 = fixed_ch ? cw % nch : cw;
     const int rb0 = fixed_ch ? cw / nch : 0;
     const int chstep = fixed_ch ? nch : nw;
+    const bool direct = nch == 1;  // one chunk per row: y is written by the item
 
     if (wait_first) {
         grid_dep_wait();
@@ -607,7 +744,7 @@ __global__ void __launch_bounds__(layout_threads(kLayout), layout_blocks(kLayout
         }
     }
     const bool f16 = a.sb_f16 != 0;
-    // stored scale or bias i of a row block, from the stage or from global memory
+    // stored scale or bias i (elements) from the stage or from global memory
     auto sb_at = [&](const void *base, int64_t i) -> float {
         if constexpr (kHalf) {
             const unsigned short h = kSbSmem ? static_cast<const unsigned short *>(base)[i]
@@ -617,151 +754,193 @@ __global__ void __launch_bounds__(layout_threads(kLayout), layout_blocks(kLayout
             return kSbSmem ? static_cast<const float *>(base)[i] : __ldg(static_cast<const float *>(base) + i);
         }
     };
-    // Final sums of tile j: thread ct adds row ct's chunk partials by the tree.
-    ProbCursor cur, fcur;
-    // (pi, dph): tile j's partial buffer and the parity of its done phase
-    auto finish = [&](int tj, int pi, uint32_t dph) -> bool {
-        if (!wait_or_abort(&done[pi], dph, &s_abort, kSiteDone)) return false;
-        int tile;
-        const Q4Prob &P = a.prob[fcur.find(a, tj, tile)];
-        const int64_t r0 = static_cast<int64_t>(tile) * TR;
-        const int rows = static_cast<int>(min(static_cast<int64_t>(TR), P.n - r0));
-        if (ct < rows) {
-            float *pr = part + (static_cast<size_t>(pi) * TR + ct) * nch;
-            int m = nch;
-            while (m > 1) {
-                const int h = m >> 1;
-                for (int i = 0; i < h; ++i) pr[i] = kTree ? __fadd_rn(pr[2 * i], pr[2 * i + 1]) : pr[2 * i] + pr[2 * i + 1];
-                if (m & 1) pr[h] = pr[m - 1];
-                m = h + (m & 1);
+
+    // Lane constants of the current chunk position (set with its slice):
+    // byte offsets in a row block of the item rows' 16-byte column quads,
+    // v[i] <- row (i ^ pi), and the lane's and its partner's group.
+    // Rows are loaded in batches of B = min(R, 4): batch b's row i is row
+    // (4b + i) ^ pi = (i ^ pi) + 4b or - 4b, so one set of B offsets and the
+    // batch step serve all batches.
+    constexpr int B = R < 4 ? R : 4;
+    const int pi = rev_lane_bits<kLogR>(lane);
+    const uint32_t rowW = static_cast<uint32_t>(W) * 4u;
+    const int bstep = (pi & 4) ? -4 * static_cast<int>(rowW) : 4 * static_cast<int>(rowW);
+    uint32_t roff[B];
+    int gown = 0, gpar = 0;
+    auto set_chunk = [&](int ch) {
+        const uint32_t quad = sl.act ? static_cast<uint32_t>(ch * 32 + lane) * 16u : 0u;
+#pragma unroll
+        for (int i = 0; i < B; ++i) roff[i] = static_cast<uint32_t>(i ^ pi) * rowW + quad;
+        // a lane past the row end keeps its group index only to name its
+        // partner; its own term is replaced by -0 and reads group 0
+        const int gv = ch * (32 >> kLg) + (lane >> kLg);
+        gown = sl.act ? gv : 0;
+        gpar = sl.actp ? (gv ^ 1) : gown;
+    };
+    if (cur_ch >= 0) set_chunk(cur_ch);  // slice computed by the prologue
+
+    // One item: rows rb*R .. rb*R + R-1 of the tile in the stage at stg, for
+    // the lane's 32 columns of chunk ch.  Rows past a ragged tile's end are
+    // computed from the stage's stale words and discarded.
+    auto item = [&](auto exact_c, auto partial_c, const unsigned char *stg, const TileHdr &h, float *prt, int ch,
+                    int rb) {
+        constexpr bool kExact = decltype(exact_c)::value;
+        constexpr bool kPartial = decltype(partial_c)::value;
+        const unsigned char *blk = stg + static_cast<uint32_t>(rb * R) * rowW;
+        float v[R];
+#pragma unroll
+        for (int b = 0; b < R / B; ++b) {
+            const unsigned char *bb = blk + b * bstep;
+            uint4 wq[B];
+#pragma unroll
+            for (int i = 0; i < B; ++i) wq[i] = *reinterpret_cast<const uint4 *>(bb + roff[i]);
+#pragma unroll
+            for (int i = 0; i < B; ++i) v[B * b + i] = lane_sum32<kExact>(wq[i], sl.X);
+        }
+        // group completion over the group's kL lanes
+        float d[NA];
+        plevels<R, 1, kL, kTree>(v, d);
+        if (kTree && kExact && sl.anyneg) {
+            // The exact path's tree values equal RN's except that a zero is
+            // always +0 (q = 0 products are x' - x').  In an all-negative
+            // group every product is <= 0, so the sum is zero only when
+            // every q is 0, and then RN's products and sum are all -0.
+            // Elsewhere a zero sum holds a +0 product or a cancellation: +0
+            // either way.
+#pragma unroll
+            for (int i = 0; i < NA; ++i) d[i] = (sl.neg && d[i] == 0.f) ? kNegZero : d[i];
+        }
+        // exchange with the partner group (kL lanes away): pairs {own, partner}
+        // for rows (i ^ pi), i < NB
+        float2 dp[NB];
+        if constexpr (kSplitB) {
+#pragma unroll
+            for (int i = 0; i < NB; ++i) dp[i] = f2(d[i], __shfl_xor_sync(0xffffffffu, d[NB + i], kL));
+        } else {
+            dp[0] = f2(d[0], __shfl_xor_sync(0xffffffffu, d[0], kL));
+        }
+        // affine terms of the group pair and their sum (the first level of the
+        // groups' tree: t(2j) + t(2j+1), in either order, is the same sum)
+        float tv[NB];
+        const int rows = h.rows;
+#pragma unroll
+        for (int i = 0; i < NB; ++i) {
+            const int row = rb * R + (i ^ pi);
+            float2 sc, bi;
+            if constexpr (kSbSmem) {
+                const unsigned char *ssc = stg + stage_w_bytes;
+                const unsigned char *sbi = ssc + stage_sb_bytes;
+                const int e = row * G;
+                sc = f2(sb_at(ssc, e + gown), sb_at(ssc, e + gpar));
+                bi = f2(sb_at(sbi, e + gown), sb_at(sbi, e + gpar));
+            } else {
+                const int64_t e = static_cast<int64_t>(min(row, rows - 1)) * G;
+                sc = f2(sb_at(h.sc, e + gown), sb_at(h.sc, e + gpar));
+                bi = f2(sb_at(h.bi, e + gown), sb_at(h.bi, e + gpar));
             }
-            P.y[r0 + ct] = pr[0];
+            float2 t2;
+            if constexpr (kTree) {
+                // scalar RN intrinsics: the compiler fuses a packed multiply
+                // into a following packed add, and these must round twice
+                t2 = f2(__fadd_rn(__fmul_rn(sc.x, dp[i].x), __fmul_rn(bi.x, sl.xs)),
+                        __fadd_rn(__fmul_rn(sc.y, dp[i].y), __fmul_rn(bi.y, sl.xsp)));
+            } else {
+                t2 = __ffma2_rn(sc, dp[i], __fmul2_rn(bi, f2(sl.xs, sl.xsp)));
+            }
+            if constexpr (kPartial) {
+                // groups past the row end contribute -0
+                if (!sl.act) t2.x = kNegZero;
+                if (!sl.actp) t2.y = kNegZero;
+            }
+            tv[i] = kTree ? __fadd_rn(t2.x, t2.y) : t2.x + t2.y;
+        }
+        // the rest of the chunk's group tree
+        float fin[1];
+        plevels<NB, 2 * kL, 32, kTree>(tv, fin);
+        // lane l < R holds row pi of the block
+        if (lane < R) {
+            const int row = rb * R + pi;
+            if (direct) {
+                if (row < rows) h.y[row] = fin[0];
+            } else {
+                prt[row * nch + ch] = fin[0];
+            }
+        }
+    };
+
+    // Final sums of a finished tile: thread ct adds row ct's chunk partials by
+    // the tree (q: the tile's slot, i.e. its partial buffer, header and done
+    // barrier; ph: the parity of that barrier's phase).
+    auto finish = [&](int q, uint32_t ph) -> bool {
+        if (!wait_or_abort(&done[q], ph, &s_abort, kSiteDone)) return false;
+        const TileHdr &fh = s_hdr[q];
+        if (ct < fh.rows) {
+            const float *pr = part + (q * TR + ct) * nch;
+            if (nch == 2) {
+                const float2 v2 = *reinterpret_cast<const float2 *>(pr);
+                fh.y[ct] = kTree ? __fadd_rn(v2.x, v2.y) : v2.x + v2.y;
+            } else {
+                fh.y[ct] = tree_chunks<kTree>(pr, nch);
+            }
         }
         return true;
     };
 
     const int total = static_cast<int>(a.total_tiles), NP = a.parts;
-    const bool finisher = cw * 32 < TR;  // holds final-sum threads (ct < rows)
-    int k = 0, tprev = -1, s = 0, pi = 0, ppi = 0;
+    const bool finisher = !direct && cw * 32 < TR;  // holds final-sum threads (ct < rows)
+    int s = 0, p = 0, pp = -1;
     uint32_t fph = 0, dph = 0, pdph = 0;  // full and done phase parities (current and previous tile)
-    for (int t = blockIdx.x; t < total; t += gridDim.x, ++k) {
+    for (int t = blockIdx.x; t < total; t += gridDim.x) {
         if (!wait_or_abort(&full[s], fph, &s_abort, kSiteFull)) break;
-        int tile;
-        const Q4Prob &P = a.prob[cur.find(a, t, tile)];
-        const int64_t r0 = static_cast<int64_t>(tile) * TR;
-        const int rows = static_cast<int>(min(static_cast<int64_t>(TR), P.n - r0));
-        const unsigned char *stg = smem + a.off_stage + static_cast<size_t>(s) * a.stage_bytes;
-        const uint4 *sw = reinterpret_cast<const uint4 *>(stg);
-        const void *ssc = stg + a.stage_w_bytes;
-        const void *sbi = stg + a.stage_w_bytes + a.stage_sb_bytes;
-        float *prt = part + static_cast<size_t>(pi) * TR * nch;
-        const int nrb = (rows + R - 1) / R;
+        const unsigned char *stg = stage0 + static_cast<uint32_t>(s) * stage_bytes;
+        const TileHdr &h = s_hdr[p];
+        const int nrb = (h.rows + R - 1) >> kLogR;
+        float *prt = part + p * TR * nch;
         if (!idle) {
             for (int ch = ch0; ch < nch; ch += chstep) {
                 if (ch != cur_ch) {
                     load_slice<kTree, kLg>(a, ch, lane, rms_r, sl);
                     cur_ch = ch;
+                    set_chunk(ch);
                 }
-                const bool active = (ch * 1024 + lane * 32) < a.cols;
-                // this lane's group, and its 16-byte column quad in row 0 of
-                // the stage; lanes past the row end (last chunk only) read
-                // group 0 and row 0's first quad instead, and add -0
-                const int g = active ? ch * (32 >> kLg) + (lane >> kLg) : 0;
-                const uint4 *wl = sw + (active ? ch * 32 + lane : 0);
-                const int wq_stride = W / 4;
                 for (int rb = rb0; rb < nrb; rb += kk) {
-                    // lane sums of R rows, four rows at a time: their loads
-                    // first, then the arithmetic.  Rows past the end of a
-                    // ragged last tile are still inside the stage (a tile has
-                    // a multiple of R rows of room): they are summed from
-                    // stale words and discarded.
-                    float v[R];
-                    constexpr int B = (R < 4) ? R : 4;
-                    const uint4 *wr = wl + rb * R * wq_stride;
-#pragma unroll
-                    for (int bq = 0; bq < R; bq += B) {
-                        uint4 wq[B];
-#pragma unroll
-                        for (int r = 0; r < B; ++r) wq[r] = wr[(bq + r) * wq_stride];
-                        if (sl.exact) {
-#pragma unroll
-                            for (int r = 0; r < B; ++r) v[bq + r] = lane_sum32<true>(wq[r], sl.X);
+                    if (sl.exact) {
+                        if (sl.full) {
+                            item(std::true_type{}, std::false_type{}, stg, h, prt, ch, rb);
                         } else {
-#pragma unroll
-                            for (int r = 0; r < B; ++r) v[bq + r] = lane_sum32<false>(wq[r], sl.X);
+                            item(std::true_type{}, std::true_type{}, stg, h, prt, ch, rb);
                         }
+                    } else {
+                        item(std::false_type{}, std::true_type{}, stg, h, prt, ch, rb);
                     }
-                    // group completion over the group's kL lanes, transposed
-                    // while more than one row is held: this lane keeps the
-                    // group sums d of rows [ofs, ofs + H)
-                    constexpr int H = lv_count<R, 1, kL>();
-                    int rowsel = 0;
-                    float d[H];
-                    levels<R, 1, kL, kTree>(v, d, lane, rowsel);
-                    if (kTree && sl.exact && sl.anyneg) {
-                        // The exact path's tree values equal RN's except that
-                        // a zero is always +0 (q = 0 products are x' - x').  In
-                        // an all-negative group every product is <= 0, so the
-                        // sum is zero only when every q is 0, and then RN's
-                        // products and sum are all -0.  Elsewhere a zero sum
-                        // holds a +0 product or a cancellation: +0 either way.
-#pragma unroll
-                        for (int i = 0; i < H; ++i) d[i] = (sl.neg && d[i] == 0.f) ? kNegZero : d[i];
-                    }
-                    const int ofs = rowsel;
-                    // affine term per (row, group); groups past the row end add
-                    // -0.  Branch-free: rows past a ragged tile's end read the
-                    // stage's stale scale and bias (or, from global memory,
-                    // the tile's last row) and are discarded.
-                    float tv[H];
-#pragma unroll
-                    for (int i = 0; i < H; ++i) {
-                        const int row = rb * R + ofs + i;
-                        const int64_t idx = kSbSmem ? static_cast<int64_t>(row * G + g)
-                                                    : (r0 + min(row, rows - 1)) * G + g;
-                        const float sc = sb_at(kSbSmem ? ssc : P.scale, idx);
-                        const float bi = sb_at(kSbSmem ? sbi : P.bias, idx);
-                        const float t = kTree ? __fadd_rn(__fmul_rn(sc, d[i]), __fmul_rn(bi, sl.xs))
-                                              : fmaf(sc, d[i], bi * sl.xs);
-                        tv[i] = active ? t : kNegZero;
-                    }
-                    // the chunk's groups: butterfly over distances kL..16,
-                    // transposed while more than one row is held
-                    float fin[1];
-                    levels<H, kL, 32, kTree>(tv, fin, lane, rowsel);
-                    const float val = fin[0];
-                    // lanes 0..R-1 hold the R rows (row rb*R + rowsel)
-                    const int row = rb * R + rowsel;
-                    if (lane < R && row < rows) prt[row * nch + ch] = val;
                 }
             }
         }
         __syncwarp();
         if (lane == 0) {
-            mbar_arrive(&empty[s]);  // weights of this stage no longer needed
-            mbar_arrive(&done[pi]);  // this warp's partials are written
+            mbar_arrive(&empty[s]);               // weights of this stage no longer needed
+            if (!direct) mbar_arrive(&done[p]);   // this warp's partials are written
         }
-        if (finisher && tprev >= 0 && !finish(tprev, ppi, pdph)) break;
-        tprev = t;
-        ppi = pi;
+        if (finisher && pp >= 0 && !finish(pp, pdph)) break;
+        pp = p;
         pdph = dph;
         if (++s == S) {
             s = 0;
             fph ^= 1u;
         }
-        if (++pi == NP) {
-            pi = 0;
+        if (++p == NP) {
+            p = 0;
             dph ^= 1u;
         }
     }
-    if (finisher && tprev >= 0) finish(tprev, ppi, pdph);
+    if (finisher && pp >= 0) finish(pp, pdph);
     if (!wait_first) grid_dep_wait();
 }
 
 // Kernel entry for one instantiation, as an untyped pointer.
-template <int R, bool kTree, bool kSb, int kLayout, int kLg, bool kHalf>
+template <int R, bool kTree, bool kSb, int kLayout, int kLg, bool kHalf, int kC = 0>
 void *kernel_ptr() {
-    return reinterpret_cast<void *>(&q4mv_kernel<R, kTree, kSb, kLayout, kLg, kHalf>);
+    return reinterpret_cast<void *>(&q4mv_kernel<R, kTree, kSb, kLayout, kLg, kHalf, kC>);
 }
 
 // Layout-0 instantiations of one format for rows per item 1, 2, 4 or 8.
