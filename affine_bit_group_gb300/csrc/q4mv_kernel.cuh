@@ -890,47 +890,86 @@ __global__ void __launch_bounds__(layout_threads(kLayout), layout_blocks(kLayout
     const bool finisher = !direct && cw * 32 < TR;  // holds final-sum threads (ct < rows)
     int s = 0, p = 0, pp = -1;
     uint32_t fph = 0, dph = 0, pdph = 0;  // full and done phase parities (current and previous tile)
-    for (int t = blockIdx.x; t < total; t += gridDim.x) {
-        if (!wait_or_abort(&full[s], fph, &s_abort, kSiteFull)) break;
-        const unsigned char *stg = stage0 + static_cast<uint32_t>(s) * stage_bytes;
-        const TileHdr &h = s_hdr[p];
-        const int nrb = (h.rows + R - 1) >> kLogR;
-        float *prt = part + p * TR * nch;
-        if (!idle) {
-            for (int ch = ch0; ch < nch; ch += chstep) {
-                if (ch != cur_ch) {
-                    load_slice<kTree, kLg>(a, ch, lane, rms_r, sl);
-                    cur_ch = ch;
-                    set_chunk(ch);
-                }
-                for (int rb = rb0; rb < nrb; rb += kk) {
-                    if (sl.exact) {
-                        if (sl.full) {
-                            item(std::true_type{}, std::false_type{}, stg, h, prt, ch, rb);
+    if constexpr (kFix) {
+        // One item per warp and tile: rows rb0*R .. rb0*R + R-1 of chunk ch0
+        // (the tile has R rows per warp of a chunk).  A ragged last tile's
+        // rows past its end are computed from stale words into partial slots
+        // that the final sums never read.
+        if (cur_ch != ch0) {
+            load_slice<kTree, kLg>(a, ch0, lane, rms_r, sl);
+            cur_ch = ch0;
+            set_chunk(ch0);
+        }
+        const bool exact = sl.exact;
+        for (int t = blockIdx.x; t < total; t += gridDim.x) {
+            if (!wait_or_abort(&full[s], fph, &s_abort, kSiteFull)) break;
+            const unsigned char *stg = stage0 + static_cast<uint32_t>(s) * stage_bytes;
+            float *prt = part + p * TR * nch;
+            if (exact) {
+                item(std::true_type{}, std::false_type{}, stg, s_hdr[p], prt, ch0, rb0);
+            } else {
+                item(std::false_type{}, std::true_type{}, stg, s_hdr[p], prt, ch0, rb0);
+            }
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&empty[s]);
+                mbar_arrive(&done[p]);
+            }
+            if (finisher && pp >= 0 && !finish(pp, pdph)) break;
+            pp = p;
+            pdph = dph;
+            if (++s == S) {
+                s = 0;
+                fph ^= 1u;
+            }
+            if (++p == NP) {
+                p = 0;
+                dph ^= 1u;
+            }
+        }
+    } else {
+        for (int t = blockIdx.x; t < total; t += gridDim.x) {
+            if (!wait_or_abort(&full[s], fph, &s_abort, kSiteFull)) break;
+            const unsigned char *stg = stage0 + static_cast<uint32_t>(s) * stage_bytes;
+            const TileHdr &h = s_hdr[p];
+            const int nrb = (h.rows + R - 1) >> kLogR;
+            float *prt = part + p * TR * nch;
+            if (!idle) {
+                for (int ch = ch0; ch < nch; ch += chstep) {
+                    if (ch != cur_ch) {
+                        load_slice<kTree, kLg>(a, ch, lane, rms_r, sl);
+                        cur_ch = ch;
+                        set_chunk(ch);
+                    }
+                    for (int rb = rb0; rb < nrb; rb += kk) {
+                        if (sl.exact) {
+                            if (sl.full) {
+                                item(std::true_type{}, std::false_type{}, stg, h, prt, ch, rb);
+                            } else {
+                                item(std::true_type{}, std::true_type{}, stg, h, prt, ch, rb);
+                            }
                         } else {
-                            item(std::true_type{}, std::true_type{}, stg, h, prt, ch, rb);
+                            item(std::false_type{}, std::true_type{}, stg, h, prt, ch, rb);
                         }
-                    } else {
-                        item(std::false_type{}, std::true_type{}, stg, h, prt, ch, rb);
                     }
                 }
             }
-        }
-        __syncwarp();
-        if (lane == 0) {
-            mbar_arrive(&empty[s]);               // weights of this stage no longer needed
-            if (!direct) mbar_arrive(&done[p]);   // this warp's partials are written
-        }
-        if (finisher && pp >= 0 && !finish(pp, pdph)) break;
-        pp = p;
-        pdph = dph;
-        if (++s == S) {
-            s = 0;
-            fph ^= 1u;
-        }
-        if (++p == NP) {
-            p = 0;
-            dph ^= 1u;
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&empty[s]);               // weights of this stage no longer needed
+                if (!direct) mbar_arrive(&done[p]);   // this warp's partials are written
+            }
+            if (finisher && pp >= 0 && !finish(pp, pdph)) break;
+            pp = p;
+            pdph = dph;
+            if (++s == S) {
+                s = 0;
+                fph ^= 1u;
+            }
+            if (++p == NP) {
+                p = 0;
+                dph ^= 1u;
+            }
         }
     }
     if (finisher && pp >= 0) finish(pp, pdph);
