@@ -603,6 +603,21 @@ __host__ __device__ constexpr int fixed_tr(int C, int R) {
     return tr < nw * 32 ? tr : nw * 32;
 }
 
+// Pairwise tree over N values (odd element carried), N a compile-time count.
+template <int N, bool kTree>
+__device__ __forceinline__ float tree_fixed(const float (&v)[N]) {
+    if constexpr (N == 1) {
+        return v[0];
+    } else {
+        constexpr int M = (N + 1) / 2;
+        float w[M];
+#pragma unroll
+        for (int i = 0; i < N / 2; ++i) w[i] = kTree ? __fadd_rn(v[2 * i], v[2 * i + 1]) : v[2 * i] + v[2 * i + 1];
+        if constexpr (N % 2 == 1) w[M - 1] = v[N - 1];
+        return tree_fixed<M, kTree>(w);
+    }
+}
+
 template <int R, bool kTree, bool kSbSmem, int kLayout, int kLg, bool kHalf, int kC = 0>
 __global__ void __launch_bounds__(layout_threads(kLayout), layout_blocks(kLayout))
     q4mv_kernel(const __grid_constant__ Q4Args a) {
@@ -766,6 +781,11 @@ __global__ void __launch_bounds__(layout_threads(kLayout), layout_blocks(kLayout
     const uint32_t rowW = static_cast<uint32_t>(W) * 4u;
     const int bstep = (pi & 4) ? -4 * static_cast<int>(rowW) : 4 * static_cast<int>(rowW);
     uint32_t roff[B];
+    // staged scale/bias of the item's affine rows (i ^ pi), i < NB: byte
+    // offsets of the lane's own group in a row block, and the step to the
+    // partner group
+    uint32_t sbo[NB];
+    int sbd = 0;
     int gown = 0, gpar = 0;
     auto set_chunk = [&](int ch) {
         const uint32_t quad = sl.act ? static_cast<uint32_t>(ch * 32 + lane) * 16u : 0u;
@@ -776,6 +796,9 @@ __global__ void __launch_bounds__(layout_threads(kLayout), layout_blocks(kLayout
         const int gv = ch * (32 >> kLg) + (lane >> kLg);
         gown = sl.act ? gv : 0;
         gpar = sl.actp ? (gv ^ 1) : gown;
+#pragma unroll
+        for (int i = 0; i < NB; ++i) sbo[i] = (static_cast<uint32_t>(i ^ pi) * G + gown) * kElem;
+        sbd = (gpar - gown) * static_cast<int>(kElem);
     };
     if (cur_ch >= 0) set_chunk(cur_ch);  // slice computed by the prologue
 
@@ -783,7 +806,7 @@ __global__ void __launch_bounds__(layout_threads(kLayout), layout_blocks(kLayout
     // the lane's 32 columns of chunk ch.  Rows past a ragged tile's end are
     // computed from the stage's stale words and discarded.
     auto item = [&](auto exact_c, auto partial_c, const unsigned char *stg, const TileHdr &h, float *prt, int ch,
-                    int rb) {
+                    int rb, bool keep) -> float {
         constexpr bool kExact = decltype(exact_c)::value;
         constexpr bool kPartial = decltype(partial_c)::value;
         const unsigned char *blk = stg + static_cast<uint32_t>(rb * R) * rowW;
@@ -828,11 +851,10 @@ __global__ void __launch_bounds__(layout_threads(kLayout), layout_blocks(kLayout
             const int row = rb * R + (i ^ pi);
             float2 sc, bi;
             if constexpr (kSbSmem) {
-                const unsigned char *ssc = stg + stage_w_bytes;
-                const unsigned char *sbi = ssc + stage_sb_bytes;
-                const int e = row * G;
-                sc = f2(sb_at(ssc, e + gown), sb_at(ssc, e + gpar));
-                bi = f2(sb_at(sbi, e + gown), sb_at(sbi, e + gpar));
+                const unsigned char *so = stg + stage_w_bytes + static_cast<uint32_t>(rb * R * G) * kElem + sbo[i];
+                const unsigned char *sp = so + sbd;
+                sc = f2(sb_at(so, 0), sb_at(sp, 0));
+                bi = f2(sb_at(so + stage_sb_bytes, 0), sb_at(sp + stage_sb_bytes, 0));
             } else {
                 const int64_t e = static_cast<int64_t>(min(row, rows - 1)) * G;
                 sc = f2(sb_at(h.sc, e + gown), sb_at(h.sc, e + gpar));
@@ -858,7 +880,7 @@ __global__ void __launch_bounds__(layout_threads(kLayout), layout_blocks(kLayout
         float fin[1];
         plevels<NB, 2 * kL, 32, kTree>(tv, fin);
         // lane l < R holds row pi of the block
-        if (lane < R) {
+        if (lane < R && !keep) {
             const int row = rb * R + pi;
             if (direct) {
                 if (row < rows) h.y[row] = fin[0];
@@ -866,6 +888,7 @@ __global__ void __launch_bounds__(layout_threads(kLayout), layout_blocks(kLayout
                 prt[row * nch + ch] = fin[0];
             }
         }
+        return fin[0];
     };
 
     // Final sums of a finished tile: thread ct adds row ct's chunk partials by
@@ -893,39 +916,65 @@ __global__ void __launch_bounds__(layout_threads(kLayout), layout_blocks(kLayout
     if constexpr (kFix) {
         // One item per warp and tile: rows rb0*R .. rb0*R + R-1 of chunk ch0
         // (the tile has R rows per warp of a chunk).  A ragged last tile's
-        // rows past its end are computed from stale words into partial slots
-        // that the final sums never read.
+        // rows past its end are computed from stale words into values that
+        // are never written to y.  Warps of chunk 0 keep their chunk totals
+        // in a register and, one tile later (once every warp's partials of
+        // that tile are in), add the other chunks' partials by the tree and
+        // write y for their own rows.  The path (exact or plain) is chosen
+        // once: each has its own copy of the loop.
         if (cur_ch != ch0) {
             load_slice<kTree, kLg>(a, ch0, lane, rms_r, sl);
             cur_ch = ch0;
             set_chunk(ch0);
         }
-        const bool exact = sl.exact;
-        for (int t = blockIdx.x; t < total; t += gridDim.x) {
-            if (!wait_or_abort(&full[s], fph, &s_abort, kSiteFull)) break;
-            const unsigned char *stg = stage0 + static_cast<uint32_t>(s) * stage_bytes;
-            float *prt = part + p * TR * nch;
-            if (exact) {
-                item(std::true_type{}, std::false_type{}, stg, s_hdr[p], prt, ch0, rb0);
-            } else {
-                item(std::false_type{}, std::true_type{}, stg, s_hdr[p], prt, ch0, rb0);
+        const bool lead = ch0 == 0;
+        const int frow = rb0 * R + pi;  // the row whose final sum this lane writes (lane < R)
+        auto final_rows = [&](int q, uint32_t ph, float own) -> bool {
+            if (!wait_or_abort(&done[q], ph, &s_abort, kSiteDone)) return false;
+            if (lane < R) {
+                const TileHdr &fh = s_hdr[q];
+                if (frow < fh.rows) {
+                    const float *pr = part + (q * TR + frow) * nch;
+                    float c[fixed_nch(kC)];
+                    c[0] = own;
+#pragma unroll
+                    for (int i = 1; i < fixed_nch(kC); ++i) c[i] = pr[i];
+                    fh.y[frow] = tree_fixed<fixed_nch(kC), kTree>(c);
+                }
             }
-            __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(&empty[s]);
-                mbar_arrive(&done[p]);
+            return true;
+        };
+        auto run = [&](auto exact_c) {
+            float own = 0.f;
+            for (int t = blockIdx.x; t < total; t += gridDim.x) {
+                if (!wait_or_abort(&full[s], fph, &s_abort, kSiteFull)) break;
+                const unsigned char *stg = stage0 + static_cast<uint32_t>(s) * stage_bytes;
+                float *prt = part + p * TR * nch;
+                const float v = item(exact_c, std::false_type{}, stg, s_hdr[p], prt, ch0, rb0, lead);
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&empty[s]);
+                    mbar_arrive(&done[p]);
+                }
+                if (lead && pp >= 0 && !final_rows(pp, pdph, own)) break;
+                own = v;
+                pp = p;
+                pdph = dph;
+                if (++s == S) {
+                    s = 0;
+                    fph ^= 1u;
+                }
+                if (++p == NP) {
+                    p = 0;
+                    dph ^= 1u;
+                }
             }
-            if (finisher && pp >= 0 && !finish(pp, pdph)) break;
-            pp = p;
-            pdph = dph;
-            if (++s == S) {
-                s = 0;
-                fph ^= 1u;
-            }
-            if (++p == NP) {
-                p = 0;
-                dph ^= 1u;
-            }
+            if (lead && pp >= 0) final_rows(pp, pdph, own);
+        };
+        if (sl.exact) {
+            run(std::true_type{});
+        } else {
+            run(std::false_type{});
         }
     } else {
         for (int t = blockIdx.x; t < total; t += gridDim.x) {
@@ -944,12 +993,12 @@ __global__ void __launch_bounds__(layout_threads(kLayout), layout_blocks(kLayout
                     for (int rb = rb0; rb < nrb; rb += kk) {
                         if (sl.exact) {
                             if (sl.full) {
-                                item(std::true_type{}, std::false_type{}, stg, h, prt, ch, rb);
+                                item(std::true_type{}, std::false_type{}, stg, h, prt, ch, rb, false);
                             } else {
-                                item(std::true_type{}, std::true_type{}, stg, h, prt, ch, rb);
+                                item(std::true_type{}, std::true_type{}, stg, h, prt, ch, rb, false);
                             }
                         } else {
-                            item(std::false_type{}, std::true_type{}, stg, h, prt, ch, rb);
+                            item(std::false_type{}, std::true_type{}, stg, h, prt, ch, rb, false);
                         }
                     }
                 }
@@ -971,8 +1020,8 @@ __global__ void __launch_bounds__(layout_threads(kLayout), layout_blocks(kLayout
                 dph ^= 1u;
             }
         }
+        if (finisher && pp >= 0) finish(pp, pdph);
     }
-    if (finisher && pp >= 0) finish(pp, pdph);
     if (!wait_first) grid_dep_wait();
 }
 
