@@ -43,6 +43,9 @@ struct Q4Args {
     int tile_rows, stages, nw, parts;
     // shared-memory layout (byte offsets)
     uint32_t off_stage, stage_w_bytes, stage_sb_bytes, stage_bytes, off_part, off_bar;
+    // the activation staged by the fixed-shape prologue (0 bytes when unused):
+    // cols floats in the per-lane layout, then group sums and group flags
+    uint32_t off_act, act_bytes;
     uint32_t smem_bytes;
     // failure-detection self-test only: the producer delivers no tile, so the
     // computing warps' bounded waits run out (see abg_selftest_wait_timeout)

@@ -136,12 +136,13 @@ Q4Prob make_prob(const Q4Call &c) {
 }
 
 abg_status plan_calls(Q4Plan *plan, const std::vector<Q4Call> &calls, int mode, int rpw) {
-    // rows per item: 8 unless asked otherwise (it never changes results)
+    // rows per item: chosen by the planner unless asked for (it never
+    // changes results)
     Q4Prob probs[kMaxProbs];
     for (size_t i = 0; i < calls.size(); ++i) probs[i] = make_prob(calls[i]);
     const Q4Call &c0 = calls[0];
     if (!plan_q4mv(plan, probs, static_cast<int>(calls.size()), static_cast<int>(c0.cols), c0.group, c0.sb_type,
-                   c0.prologue, c0.x, c0.xsum, c0.wt, c0.eps, mode == ABG_TREE, rpw == 0 ? 8 : rpw, sb_bulk(c0),
+                   c0.prologue, c0.x, c0.xsum, c0.wt, c0.eps, mode == ABG_TREE, rpw, sb_bulk(c0),
                    g_tuning))
         return ABG_ESHAPE;
     return ABG_OK;
@@ -391,7 +392,8 @@ abg_status abg_stage_graph_create(const abg_node *nodes, int64_t count, int mode
         if (st != ABG_OK) return st;
     }
     // 2. stages: no node reads or writes what another node of its stage writes,
-    //    and no node writes any product's weights (they are fetched early)
+    //    and no node writes any product's weights or RMS-norm prologue weights
+    //    (they are fetched before the wait for the previous stage)
     std::map<int, std::vector<int64_t>> stages;
     for (int64_t i = 0; i < count; ++i) stages[nodes[i].stage].push_back(i);
     std::vector<std::vector<Range>> ins(count), outs(count);
@@ -411,7 +413,9 @@ abg_status abg_stage_graph_create(const abg_node *nodes, int64_t count, int mode
     }
     for (int64_t i = 0; i < count; ++i) {
         if (nodes[i].kind != ABG_NODE_Q4MV || nodes[i].n == 0) continue;
-        const std::vector<Range> wr = q4_weights(call_of(nodes[i]));
+        std::vector<Range> wr = q4_weights(call_of(nodes[i]));
+        // an RMS-norm prologue's weights are read early too
+        if (nodes[i].prologue == ABG_PRO_RMSQ) wr.push_back(rng(nodes[i].wt, nodes[i].cols, 4));
         for (int64_t j = 0; j < count; ++j)
             for (const Range &o : outs[j])
                 for (const Range &r : wr)

@@ -22,7 +22,7 @@ cudaError_t q4mv_status_g32h(unsigned *bits, bool clear);
 cudaError_t q4mv_status_g64h(unsigned *bits, bool clear);
 cudaError_t q4mv_status_g128(unsigned *bits, bool clear);
 cudaError_t q4mv_status_g128h(unsigned *bits, bool clear);
-void *q4mv_select_fixed(int cols, bool tree);
+void *q4mv_select_fixed(int cols, bool tree, int R, int layout);
 cudaError_t q4mv_status_fixed(unsigned *bits, bool clear);
 
 namespace {
@@ -33,7 +33,7 @@ namespace {
 // with 8 rows per item only).  shape != 0 selects the fixed-shape
 // instantiation for that row length (q4mv_fixed.cu).
 void *select_kernel(int lg, bool half, int R, bool tree, bool sb, int layout, int shape = 0) {
-    if (shape != 0) return q4mv_select_fixed(shape, tree);
+    if (shape != 0) return q4mv_select_fixed(shape, tree, R, layout);
     if (lg == 1 && !half) {
         if (layout == 0) return select_layout0<1, false>(R, tree, sb);
         if (R != 8) return nullptr;
@@ -87,7 +87,7 @@ constexpr int kFewTilesPerSm = 4;
 
 bool plan_once(Q4Plan *plan, const Q4Prob *probs, int nprob, int cols, int group, int sb_type, int prologue,
                const float *x, const float *xsum, const float *wt, float eps, bool tree, int rows_per_warp,
-               bool sb_smem, const Q4Tuning &tune) {
+               bool sb_smem, const Q4Tuning &tune, bool allow_few, int force_layout = -1) {
     Q4Args &a = plan->args;
     a = Q4Args{};
     const int R = rows_per_warp;
@@ -101,18 +101,23 @@ bool plan_once(Q4Plan *plan, const Q4Prob *probs, int nprob, int cols, int group
     // block per SM; 1..6 with 8 rows per item selects the 128-register
     // two-block layout
     const bool fmt_default = lg == 1 && !half;
-    const int layout = (!fmt_default || R != 8 || tune.consumer_warps == 0)
+    const int layout = force_layout >= 0 ? force_layout
+                       : (!fmt_default || R != 8 || tune.consumer_warps == 0)
                            ? 0
                            : (tune.consumer_warps > 8 ? 1 : (tune.consumer_warps <= 6 ? 2 : 0));
     const bool wide = layout == 1;
     const int nw_max = wide ? 16 : (layout == 2 ? 6 : 8);
-    int nw = tune.consumer_warps;
-    if (nw <= 0) nw = nch <= 8 ? nch * (8 / nch) : 8;
+    int nw = force_layout >= 0 ? 0 : tune.consumer_warps;
+    if (nw <= 0) nw = nch <= nw_max ? nch * (nw_max / nch) : nw_max;
     if (nch <= nw_max) nw = nch * (std::min(nw, nw_max) / nch);
     nw = std::min(std::max(nw, 1), nw_max);
     const int kk = (nch <= nw) ? nw / nch : 1;  // warps per chunk position
     const uint32_t row_bytes = static_cast<uint32_t>(C / 2) + (sb_smem ? 2u * G * elem : 0u);
-    const uint32_t fixed = 1024;  // barriers and alignment slack
+    // the fixed-shape prologue stages the activation: cols floats, G group
+    // sums, G group flags and a flag per 128 columns
+    const bool act_stage = fmt_default && sb_smem && (C == 2048 || C == 4096 || C == 6144);
+    const uint32_t act_bytes = act_stage ? align_up(static_cast<uint32_t>(C * 4 + G * 8 + C / 32), 128) : 0u;
+    const uint32_t fixed = 1024 + act_bytes;  // barriers, alignment slack and the staged activation
     // tile rows: a multiple of R*kk so row blocks spread evenly over the warps
     const int unit = R * kk;
     int TR = unit;
@@ -127,7 +132,7 @@ bool plan_once(Q4Plan *plan, const Q4Prob *probs, int nprob, int cols, int group
     // which hides each block's per-tile bubbles behind the other.
     int64_t tiles_est = 0;
     for (int i = 0; i < nprob; ++i) tiles_est += (probs[i].n + TR - 1) / TR;
-    const bool few = !wide && tune.smem_kb == 0 && tune.blocks_per_sm == 0 &&
+    const bool few = allow_few && !wide && tune.smem_kb == 0 && tune.blocks_per_sm == 0 &&
                      tiles_est <= static_cast<int64_t>(kFewTilesPerSm) * sm_count();
     uint32_t budget =
         static_cast<uint32_t>(tune.smem_kb > 0 ? tune.smem_kb : (wide ? 220 : (few ? 160 : 110))) * 1024u;
@@ -161,6 +166,12 @@ bool plan_once(Q4Plan *plan, const Q4Prob *probs, int nprob, int cols, int group
         a.total_tiles += a.prob[i].tiles;
     }
     if (a.total_tiles > 0x7fffffff) return false;  // the kernel counts tiles in 32 bits
+    // the budget loop may have halved the tile rows after the few-tiles
+    // decision: a launch that has more tiles than that rule admits is planned
+    // again with two blocks per SM
+    if (few && a.total_tiles > static_cast<int64_t>(kFewTilesPerSm) * sm_count())
+        return plan_once(plan, probs, nprob, cols, group, sb_type, prologue, x, xsum, wt, eps, tree, rows_per_warp,
+                         sb_smem, tune, false, force_layout);
     a.x = x;
     a.xsum = xsum;
     a.wt = wt;
@@ -182,14 +193,17 @@ bool plan_once(Q4Plan *plan, const Q4Prob *probs, int nprob, int cols, int group
     a.off_part = a.off_stage + S * a.stage_bytes;
     a.off_bar = align_up(a.off_part + part_bytes(TR, S), 16);
     a.parts = S + 2;
-    a.smem_bytes = a.off_bar + 8u * (2 * S + a.parts);
+    a.off_act = align_up(a.off_bar + 8u * (2 * S + a.parts), 128);
+    a.act_bytes = act_bytes;
+    a.smem_bytes = a.off_act + act_bytes;
 
     // a plan with the compile-time shape of its row length runs the
     // fixed-shape instantiation (same results, constant sizes)
     int shape = 0;
-    if (fmt_default && sb_smem && layout == 0 && R == 8 && (C == 2048 || C == 4096 || C == 6144) &&
-        TR == fixed_tr(C, 8) && nw == fixed_nw(C) && nch == fixed_nch(C) &&
-        a.stage_w_bytes == static_cast<uint32_t>(TR * C / 2) && a.stage_sb_bytes == static_cast<uint32_t>(TR * G * 4))
+    if (fmt_default && sb_smem && ((layout == 0 && R == 8) || (layout == 1 && R == 4)) &&
+        (C == 2048 || C == 4096 || C == 6144) && TR == fixed_tr(C, R, layout) && nw == fixed_nw(C, layout) &&
+        nch == fixed_nch(C) && a.stage_w_bytes == static_cast<uint32_t>(TR * C / 2) &&
+        a.stage_sb_bytes == static_cast<uint32_t>(TR * G * 4))
         shape = C;
 
     // blocks per SM: what fits (registers and shared memory), at most 2 (1 for a
@@ -246,11 +260,32 @@ cudaError_t raise_smem_limit(void *fn) {
 
 // Plans with the requested rows per item; if the stages do not fit in shared
 // memory (very wide rows), retries with fewer rows per item (same results).
+// rows_per_warp 0 chooses: a launch of few tiles (a decode token's products)
+// of a row length with a fixed-shape instantiation runs 16 computing warps
+// with 4 rows per item in one block per SM, so each tile is split over twice
+// as many warps and finishes sooner; every other launch runs 8 rows per item.
 bool plan_q4mv(Q4Plan *plan, const Q4Prob *probs, int nprob, int cols, int group, int sb_type, int prologue,
                const float *x, const float *xsum, const float *wt, float eps, bool tree, int rows_per_warp,
                bool sb_smem, const Q4Tuning &tune) {
+    if (rows_per_warp == 0) {
+        const bool plain_tuning = tune.smem_kb == 0 && tune.consumer_warps == 0 && tune.blocks_per_sm == 0 &&
+                                  tune.stage_kb == 0;
+        if (plain_tuning && group == 64 && sb_type == ABG_SB_F32 && sb_smem &&
+            (cols == 2048 || cols == 4096 || cols == 6144)) {
+            const int tr = fixed_tr(cols, 4, 1);
+            int64_t tiles = 0;
+            for (int i = 0; i < nprob; ++i) tiles += (probs[i].n + tr - 1) / tr;
+            if (tiles <= static_cast<int64_t>(kFewTilesPerSm) * sm_count() &&
+                plan_once(plan, probs, nprob, cols, group, sb_type, prologue, x, xsum, wt, eps, tree, 4, sb_smem,
+                          tune, false, 1) &&
+                plan->shape == cols)
+                return true;
+        }
+        rows_per_warp = 8;
+    }
     for (int R = rows_per_warp; R >= 1; R /= 2)
-        if (plan_once(plan, probs, nprob, cols, group, sb_type, prologue, x, xsum, wt, eps, tree, R, sb_smem, tune))
+        if (plan_once(plan, probs, nprob, cols, group, sb_type, prologue, x, xsum, wt, eps, tree, R, sb_smem, tune,
+                      true))
             return true;
     return false;
 }

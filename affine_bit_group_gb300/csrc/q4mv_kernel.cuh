@@ -392,6 +392,130 @@ __device__ __forceinline__ void rms_slice(const Q4Args &a, int ch, bool has, boo
     finish_slice<kTree, kLg>(a, ch, lane, active, v, sl);
 }
 
+// The fixed-shape prologue.  The block's computing threads produce the
+// activation once, cooperatively, and stage it in shared memory for the
+// warps' slices:
+//   act  column c = 1024 ch + 32 l + 4 i + e at float index 4 (32 (8 ch + i)
+//        + l) + e: lane l of a warp with chunk ch reads its 32 columns with 8
+//        conflict-free 16-byte loads;
+//   gs   the group sums (computed by the prologue);
+//   gneg 1 where every value of the group is negative;
+//   spec 1 where a 128-column block holds a value outside the exact path's
+//        range (zero of either sign, infinite, NaN or |x| >= 2^100).
+// Thread t takes the 4-column units u = t, t + nct, ...; the 16 units of a
+// 64-column group are 16 consecutive threads of one half-warp, so a group's
+// sum is the thread's pairwise sum of its 4 values followed by butterfly
+// steps at distances 1, 2, 4 and 8: the pairwise tree over the 64 values.
+// The RMS-norm factor takes the tree over the group sums of squares in
+// shared memory between two barriers (rms_from_blocks).  All three sums are
+// the oracle's trees, so the staged values are the producers' bits.
+template <int kNU>
+struct CoopIn {
+    float4 w[kNU];  // RMS-norm weights of the thread's units, read before the dependency wait
+};
+
+template <bool kTree>
+__device__ __forceinline__ float sum4_group(float4 v) {
+    float s = kTree ? __fadd_rn(__fadd_rn(v.x, v.y), __fadd_rn(v.z, v.w)) : (v.x + v.y) + (v.z + v.w);
+#pragma unroll
+    for (int d = 1; d < 16; d <<= 1) {
+        const float o = __shfl_xor_sync(0xffffffffu, s, d);
+        s = kTree ? __fadd_rn(s, o) : s + o;
+    }
+    return s;
+}
+
+template <bool kTree, int kC, int kNct>
+__device__ __forceinline__ void coop_prologue(const Q4Args &a, const CoopIn<(kC / 4 + kNct - 1) / kNct> &in,
+                                              float *act, float *gs, unsigned *gneg, unsigned *spec, int cw,
+                                              float *red, float *rbox) {
+    constexpr int NU = (kC / 4 + kNct - 1) / kNct;
+    static_assert((kC / 4) % kNct == 0, "every thread has NU whole units");
+    const int t = threadIdx.x - 32, lane = threadIdx.x & 31;
+    const float4 *x4 = reinterpret_cast<const float4 *>(a.x);
+    float4 v[NU];
+    if (a.prologue == kProSwq) {
+        const float4 *u4 = reinterpret_cast<const float4 *>(a.x + kC);
+#pragma unroll
+        for (int k = 0; k < NU; ++k) {
+            const float4 g = x4[t + k * kNct], u = u4[t + k * kNct];
+            v[k] = make_float4(swiglu<kTree>(g.x, u.x), swiglu<kTree>(g.y, u.y), swiglu<kTree>(g.z, u.z),
+                               swiglu<kTree>(g.w, u.w));
+        }
+    } else {
+#pragma unroll
+        for (int k = 0; k < NU; ++k) v[k] = x4[t + k * kNct];
+    }
+    if (a.prologue == kProRmsq) {
+#pragma unroll
+        for (int k = 0; k < NU; ++k) {
+            const float4 q = v[k];
+            const float s = sum4_group<kTree>(make_float4(__fmul_rn(q.x, q.x), __fmul_rn(q.y, q.y),
+                                                          __fmul_rn(q.z, q.z), __fmul_rn(q.w, q.w)));
+            const int u = t + k * kNct;
+            if ((u & 15) == 0) red[u >> 4] = s;
+        }
+        const float r = rms_from_blocks<kTree>(red, kC, a.eps, cw, kNct, rbox);
+#pragma unroll
+        for (int k = 0; k < NU; ++k) {
+            const float4 q = v[k], w = in.w[k];
+            v[k] = make_float4(__fmul_rn(__fmul_rn(q.x, r), w.x), __fmul_rn(__fmul_rn(q.y, r), w.y),
+                               __fmul_rn(__fmul_rn(q.z, r), w.z), __fmul_rn(__fmul_rn(q.w, r), w.w));
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < NU; ++k) {
+        const int u = t + k * kNct, c = 4 * u;
+        const float4 q = v[k];
+        if (a.prologue != kProNone) {
+            const float s = sum4_group<kTree>(q);
+            if ((u & 15) == 0) gs[u >> 4] = s;
+        }
+        const bool sp = !x_ordinary(q.x) || !x_ordinary(q.y) || !x_ordinary(q.z) || !x_ordinary(q.w);
+        const bool neg = q.x < 0.f && q.y < 0.f && q.z < 0.f && q.w < 0.f;
+        const unsigned bsp = __ballot_sync(0xffffffffu, sp), bneg = __ballot_sync(0xffffffffu, neg);
+        if (lane == 0) spec[u >> 5] = bsp != 0u;
+        if ((u & 15) == 0) gneg[u >> 4] = ((bneg >> (lane & 16)) & 0xffffu) == 0xffffu;
+        const int ch = c >> 10, l = (c & 1023) >> 5, i = (c & 31) >> 2;
+        reinterpret_cast<float4 *>(act)[(ch * 8 + i) * 32 + l] = q;
+    }
+    named_bar(1, kNct);
+}
+
+// A warp's slice of the staged activation (chunk ch; fixed shapes: every
+// lane's columns lie inside the row).
+template <bool kTree, int kLg>
+__device__ __forceinline__ void slice_from_stage(const Q4Args &a, int ch, int lane, const float *act,
+                                                 const float *gs, const unsigned *gneg, const unsigned *spec,
+                                                 Slice &sl) {
+    float v[32];
+    const float4 *s4 = reinterpret_cast<const float4 *>(act);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const float4 q = s4[(ch * 8 + i) * 32 + lane];
+        v[4 * i] = q.x, v[4 * i + 1] = q.y, v[4 * i + 2] = q.z, v[4 * i + 3] = q.w;
+    }
+    bool sp = false;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) sp |= spec[ch * 8 + i] != 0u;
+    const int g = ch * (32 >> kLg) + (lane >> kLg);
+    sl.exact = !sp;
+    sl.xs = a.prologue == kProNone ? a.xsum[g] : gs[g];
+    sl.xsp = __shfl_xor_sync(0xffffffffu, sl.xs, 1 << kLg);
+    sl.neg = kTree && gneg[g] != 0u;
+    sl.anyneg = __any_sync(0xffffffffu, sl.neg);
+    sl.act = sl.actp = sl.full = true;
+#pragma unroll
+    for (int m = 0; m < 16; ++m) {
+        if (sl.exact) {
+            const float s = -nib_scale(m & 7);
+            sl.X[m] = f2(__fmul_rn(v[m], s), __fmul_rn(v[m + 16], s));
+        } else {
+            sl.X[m] = f2(v[m], v[m + 16]);
+        }
+    }
+}
+
 // Locates tiles of a grouped launch.  A block visits its tiles in increasing
 // order, so the problem index only moves forward.
 // Tile counts fit in 32 bits (the planner checks the launch's total).
@@ -587,16 +711,20 @@ __device__ __forceinline__ float tree_chunks(const float *p, int m) {
 }
 
 // Compile-time tile shape of a product of kC columns in groups of 64 with f32
-// scale and bias staged, block layout 0 and R rows per item, following the
-// planner's rule for the default tuning: computing warps a multiple of the
-// chunk count (at most 8), tile rows doubled from R times the warps per chunk
-// while a tile stays within one row per computing thread and a 40 KB stage.
-// A launch whose plan has exactly this shape may use the kC instantiation,
-// in which the shape's sizes and offsets are constants.
+// scale and bias staged, R rows per item and block layout 0 (at most 8
+// computing warps) or 1 (at most 16), following the planner's rule for the
+// default tuning: computing warps a multiple of the chunk count, tile rows
+// doubled from R times the warps per chunk while a tile stays within one row
+// per computing thread and a 40 KB stage.  A launch whose plan has exactly
+// this shape may use the kC instantiation, in which the shape's sizes and
+// offsets are constants.
 __host__ __device__ constexpr int fixed_nch(int C) { return (C + 1023) / 1024; }
-__host__ __device__ constexpr int fixed_nw(int C) { return fixed_nch(C) <= 8 ? fixed_nch(C) * (8 / fixed_nch(C)) : 8; }
-__host__ __device__ constexpr int fixed_tr(int C, int R) {
-    const int nch = fixed_nch(C), nw = fixed_nw(C), kk = nch <= nw ? nw / nch : 1;
+__host__ __device__ constexpr int fixed_nw(int C, int layout = 0) {
+    return fixed_nch(C) <= (layout == 1 ? 16 : 8) ? fixed_nch(C) * ((layout == 1 ? 16 : 8) / fixed_nch(C))
+                                                 : (layout == 1 ? 16 : 8);
+}
+__host__ __device__ constexpr int fixed_tr(int C, int R, int layout = 0) {
+    const int nch = fixed_nch(C), nw = fixed_nw(C, layout), kk = nch <= nw ? nw / nch : 1;
     const int row_bytes = C / 2 + 2 * (C / 64) * 4;
     int tr = R * kk;
     while (tr * 2 <= nw * 32 && tr * 2 * row_bytes <= 40 * 1024) tr *= 2;
@@ -621,7 +749,7 @@ __device__ __forceinline__ float tree_fixed(const float (&v)[N]) {
 template <int R, bool kTree, bool kSbSmem, int kLayout, int kLg, bool kHalf, int kC = 0>
 __global__ void __launch_bounds__(layout_threads(kLayout), layout_blocks(kLayout))
     q4mv_kernel(const __grid_constant__ Q4Args a) {
-    static_assert(kC == 0 || (kLayout == 0 && kLg == 1 && !kHalf && kSbSmem), "fixed shapes: default format only");
+    static_assert(kC == 0 || (kLayout <= 1 && kLg == 1 && !kHalf && kSbSmem), "fixed shapes: default format only");
     constexpr bool kFix = kC != 0;
     constexpr int kL = 1 << kLg;                  // lanes per group
     constexpr uint32_t kElem = kHalf ? 2u : 4u;   // bytes per stored scale or bias
@@ -642,10 +770,12 @@ __global__ void __launch_bounds__(layout_threads(kLayout), layout_blocks(kLayout
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // shape: constants in a fixed-shape instantiation, else from the plan
     const int S = a.stages;
-    const int TR = kFix ? fixed_tr(kC, R) : a.tile_rows, W = kFix ? kC / 8 : a.W, G = kFix ? kC / 64 : a.G;
-    const int nch = kFix ? fixed_nch(kC) : a.nch, nw = kFix ? fixed_nw(kC) : a.nw;
-    const uint32_t stage_w_bytes = kFix ? static_cast<uint32_t>(fixed_tr(kC, R) * kC / 2) : a.stage_w_bytes;
-    const uint32_t stage_sb_bytes = kFix ? static_cast<uint32_t>(fixed_tr(kC, R) * (kC / 64) * 4) : a.stage_sb_bytes;
+    constexpr int kTRf = kFix ? fixed_tr(kC, R, kLayout) : 0;
+    static_assert(!kFix || kTRf == R * (fixed_nw(kC, kLayout) / fixed_nch(kC)), "one item per warp and tile");
+    const int TR = kFix ? kTRf : a.tile_rows, W = kFix ? kC / 8 : a.W, G = kFix ? kC / 64 : a.G;
+    const int nch = kFix ? fixed_nch(kC) : a.nch, nw = kFix ? fixed_nw(kC, kLayout) : a.nw;
+    const uint32_t stage_w_bytes = kFix ? static_cast<uint32_t>(kTRf * kC / 2) : a.stage_w_bytes;
+    const uint32_t stage_sb_bytes = kFix ? static_cast<uint32_t>(kTRf * (kC / 64) * 4) : a.stage_sb_bytes;
     const uint32_t stage_bytes = kFix ? stage_w_bytes + 2 * stage_sb_bytes : a.stage_bytes;
 
     if (threadIdx.x == 0) {
@@ -738,6 +868,16 @@ __global__ void __launch_bounds__(layout_threads(kLayout), layout_blocks(kLayout
     const int chstep = fixed_ch ? nch : nw;
     const bool direct = nch == 1;  // one chunk per row: y is written by the item
 
+    // fixed shapes: the RMS-norm weights are read before the dependency wait
+    // (the preceding launch does not produce them)
+    constexpr int kNct = kFix ? 32 * fixed_nw(kC, kLayout) : 32;
+    constexpr int kNU = kFix ? (kC / 4 + kNct - 1) / kNct : 1;
+    CoopIn<kNU> cin;
+    if (kFix && a.prologue == kProRmsq) {
+        const float4 *w4 = reinterpret_cast<const float4 *>(a.wt);
+#pragma unroll
+        for (int k = 0; k < kNU; ++k) cin.w[k] = __ldg(w4 + ct + k * kNct);
+    }
     if (wait_first) {
         grid_dep_wait();
         grid_dep_launch();
@@ -745,7 +885,16 @@ __global__ void __launch_bounds__(layout_threads(kLayout), layout_blocks(kLayout
     Slice sl;
     int cur_ch = -1;
     float rms_r = 0.f;
-    if (a.prologue == kProRmsq) {
+    if constexpr (kFix) {
+        // the activation once per block, staged in shared memory
+        float *act = reinterpret_cast<float *>(smem + a.off_act);
+        float *gs = act + kC;
+        unsigned *gneg = reinterpret_cast<unsigned *>(gs + kC / 64);
+        unsigned *spec = gneg + kC / 64;
+        coop_prologue<kTree, kC, kNct>(a, cin, act, gs, gneg, spec, cw, s_red, &s_rbox);
+        slice_from_stage<kTree, kLg>(a, ch0, lane, act, gs, gneg, spec, sl);
+        cur_ch = ch0;
+    } else if (a.prologue == kProRmsq) {
         // one pass over x, after which the warp's slice is ready for every
         // tile; only in the main instantiations (tree mode, 8 rows per item,
         // block layout 0, staged scale/bias): in the others the product

@@ -18,8 +18,8 @@ unfused stage graphs), the 4096x2048 product in every weight format
 grouped launch of 64 products streaming from HBM, the batched product
 (1, 2, 4 and 8 tokens sharing the 248320x2048 head's weights), and the pages'
 own timing of the 4096x2048 product ((400-call - 1-call)/400, median of 6).
-`--only sweep` runs the rows x cols x rows-per-item x mode sweep (GB/s and
-fraction of peak per point, and the fast-mode error on sampled rows).
+and the rows x cols x rows-per-item x mode sweep (GB/s and fraction of peak
+per point, and the fast-mode error over every row of each point).
 
 Output: one JSON line on rank 0.  --impl reference times the CPU oracle (the
 plain C definition the library is tested against) on the same workload.
@@ -85,7 +85,21 @@ def code_sha256(path: str) -> str:
     return hashlib.sha256("\n".join(out).encode()).hexdigest()
 
 
-def profile_traffic(kernel_src: str, profile: str):
+# Every source the product kernel's code and launch plan depend on: a profile
+# recorded for one version of these stays valid only while none of them changes.
+KERNEL_SOURCES = tuple(os.path.join("affine_bit_group_gb300", "csrc", f) for f in
+                       ("q4mv_kernel.cuh", "abg_dev.cuh", "abg_kernels.cuh", "q4mv.cu", "q4mv_fixed.cu"))
+
+
+def kernel_code_sha256(paths=None) -> str:
+    """sha256 over the code (comments and blank lines removed) of the kernel's sources, in order."""
+    h = hashlib.sha256()
+    for rel in (paths or KERNEL_SOURCES):
+        h.update(rel.encode() + b"\0" + code_sha256(os.path.join(ROOT, rel)).encode() + b"\n")
+    return h.hexdigest()
+
+
+def profile_traffic(profile: str):
     """DRAM bytes per launch from a committed ncu summary, or None once the kernel's code changed."""
     path = os.path.join(ROOT, "profiles", profile)
     if not os.path.exists(path):
@@ -96,7 +110,7 @@ def profile_traffic(kernel_src: str, profile: str):
             if ":" in line and line.strip().startswith(("dram_bytes_per_launch", "kernel_code_sha256")):
                 k, v = line.split(":", 1)
                 vals[k.strip()] = v.split()[0].strip("`")
-    if vals.get("kernel_code_sha256") != code_sha256(kernel_src) or "dram_bytes_per_launch" not in vals:
+    if vals.get("kernel_code_sha256") != kernel_code_sha256() or "dram_bytes_per_launch" not in vals:
         return None
     return float(vals["dram_bytes_per_launch"])
 
@@ -285,6 +299,7 @@ def run_ours(args, rank, world):
         extra["formats"] = bench_formats(abg, stream, args, peak, l2)
         extra["batched"] = bench_batched(abg, stream, args)
         extra["pages_way"] = bench_pages_way(abg, stream, args)
+        extra["sweep"] = bench_sweep(abg, stream, args, peak, l2)
 
     res = dict(value=value, ms_step=ms_step, us_per_product=us_per_product, achieved=achieved,
                launch_us=ms_launch * 1e3, clocks=clocks,
@@ -357,7 +372,7 @@ def bench_formats(abg, stream, args, peak, l2):
 
 def bench_batched(abg, stream, args):
     """The 248320x2048 head for a batch of T tokens (abg_q4mm): us per call and per
-    token; every token's output hash checked against the oracle on a sample."""
+    token; every row of every token checked against the oracle."""
     import torch
 
     import oracle
@@ -386,8 +401,8 @@ def bench_batched(abg, stream, args):
             e1.record(stream)
         torch.cuda.synchronize()
         us = e0.elapsed_time(e1) * 1e3 / reps
-        got = Y.view(T, m.rows)[:, :512].cpu().numpy()
-        exp = oracle.q4mm(*m.arrays(), X_np, XS_np, m.cols, n=512)
+        got = Y.view(T, m.rows).cpu().numpy()
+        exp = oracle.q4mm(*m.arrays(), X_np, XS_np, m.cols)
         if not np.array_equal(got.view(np.uint32), exp.view(np.uint32)):
             raise SystemExit(f"batched product T={T} differs from the oracle")
         out[f"T{T}"] = {"us_per_call": round(us, 2), "us_per_token": round(us / T, 2),
@@ -404,8 +419,11 @@ SWEEP_COLS = (2048, 4096, 6144)
 def bench_sweep(abg, stream, args, peak, l2):
     """Every (rows, cols) point of the sweep, each rows-per-item setting, tree and
     fast mode: products queued as one stage over copies of the weights totalling
-    more than 3x L2.  Also the fast-mode error on a sample of rows: the largest
-    |y_fast - y_tree| / |y_tree| over rows with |y_tree| >= 1e-3 A_r."""
+    more than 3x L2.  Also the fast-mode error over every row of each point,
+    against the tree result: the largest |y_fast - y_tree| / A_r (A_r = sum over
+    groups of |scale*d| + |bias*xsum|, the stated bound's scale), the largest
+    |y_fast - y_tree| / |y_tree| over all rows, and the same over rows with
+    |y_tree| >= 1e-3 A_r."""
     import torch
 
     import oracle
@@ -426,7 +444,7 @@ def bench_sweep(abg, stream, args, peak, l2):
             calls = max(copies, 8)
             ys = [torch.empty(rows, dtype=torch.float32, device="cuda") for _ in range(calls)]
             point = {"rows": rows, "cols": cols, "copies": copies}
-            y_tree = None
+            y_tree = y_fast = None
             for mode, mname in ((abg.TREE, "tree"), (abg.FAST, "fast")):
                 for R in (1, 2, 4, 8):
                     g = abg.StageGraph([abg.Node.q4mv(0, *mats[i % copies], ys[i % len(ys)], cols, x=x, xsum=xs)
@@ -436,16 +454,24 @@ def bench_sweep(abg, stream, args, peak, l2):
                     gbs = calls * pb / (ms * 1e-3) / 1e9
                     point[f"{mname}_R{R}_gbs"] = round(gbs, 1)
                     point[f"{mname}_R{R}_frac"] = round(gbs / peak, 3)
-                    if mname == "tree" and R == 8:
-                        y_tree = ys[(calls - 1) % len(ys)].cpu().numpy().copy()
-                    if mname == "fast" and R == 8:
-                        y_fast = ys[(calls - 1) % len(ys)].cpu().numpy().copy()
-            n = min(rows, 256)
-            mag = oracle.q4mv_absmag(*m.arrays(), x_np, oracle.gsum(x_np), cols, n=n)
-            yt, yf = y_tree[:n].astype(np.float64), y_fast[:n].astype(np.float64)
+                    if R == 8:
+                        y8 = ys[(calls - 1) % len(ys)].cpu().numpy().copy()
+                        if mname == "tree":
+                            y_tree = y8
+                        else:
+                            y_fast = y8
+            xs_np = oracle.gsum(x_np)
+            if oracle.hash32(y_tree) != oracle.hash32(oracle.q4mv(*m.arrays(), x_np, xs_np, cols)):
+                raise SystemExit(f"sweep {rows}x{cols}: tree mode differs from the oracle")
+            mag = oracle.q4mv_absmag(*m.arrays(), x_np, xs_np, cols)
+            yt, yf = y_tree.astype(np.float64), y_fast.astype(np.float64)
+            d = np.abs(yf - yt)
+            nz = yt != 0
             keep = np.abs(yt) >= 1e-3 * mag
-            point["fast_max_rel_err"] = float(np.max(np.abs(yf - yt)[keep] / np.abs(yt)[keep])) if keep.any() else 0.0
-            point["fast_max_err_over_A"] = float(np.max(np.abs(yf - yt) / mag))
+            point["fast_max_err_over_A"] = float(np.max(d / mag))
+            point["fast_max_rel_err_all_rows"] = float(np.max(d[nz] / np.abs(yt[nz]))) if nz.any() else 0.0
+            point["fast_max_rel_err"] = float(np.max(d[keep] / np.abs(yt[keep]))) if keep.any() else 0.0
+            point["fast_rows_over_1e-5_rel"] = int(np.count_nonzero(d > 1e-5 * np.abs(yt)))
             out["points"].append(point)
             del mats, ys, x, xs
             torch.cuda.empty_cache()
@@ -657,8 +683,7 @@ def main():
     if rank != 0:
         return
     value = job_value(ms_step, world)
-    kernel_src = os.path.join(ROOT, "affine_bit_group_gb300", "csrc", "q4mv_kernel.cuh")
-    traffic = profile_traffic(kernel_src, "q4mv_mid_4096x2048.md")
+    traffic = profile_traffic("q4mv_mid_4096x2048.md")
     line = {
         "metric": "q4mv achieved HBM GB/s", "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",

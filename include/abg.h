@@ -210,8 +210,9 @@ abg_status abg_swq_ex(const float *a, float *o, float *osum, int64_t n, int grou
  * example q/k/v, or gate/up) are run as one grouped launch.  Consecutive
  * launches overlap through programmatic dependent launch: a product fetches
  * its weights before the previous stage has finished and waits only before
- * it reads its activation.  Weights must therefore not be written by any node
- * of the graph (checked: ABG_EALIAS).
+ * it reads its activation.  Weights, and the norm weights of an RMS-norm
+ * prologue, must therefore not be written by any node of the graph (checked:
+ * ABG_EALIAS).
  *
  * Node kinds and the fields each reads (unused fields are ignored):
  *   ABG_NODE_Q4MV  w, scale, bias, rows, cols, row0, n, y, prologue, and

@@ -135,8 +135,8 @@ def test_mid_400_calls_hash():
         assert oracle.hash32(host(y)) == oracle.hash32(exp)
 
 
-def test_head_sampled_rows():
-    """248320x2048 output head with x = rmsq(hidden): sampled rows equal the oracle's."""
+def test_head_all_rows():
+    """248320x2048 output head with x = rmsq(hidden): every row equals the oracle's."""
     m, hidden, wt = synth.head()
     xn_o, xs_o = oracle.rmsq(hidden, wt, 1e-6)
     xn, xsd = empty(2048), empty(32)
@@ -148,21 +148,15 @@ def test_head_sampled_rows():
     abg.q4mv(dev_words(m.w), dev(m.scale), dev(m.bias), xn, xsd, y, cols=m.cols)
     torch.cuda.synchronize()
     got = host(y)
-    rng = np.random.default_rng(0)
-    starts = sorted(set([0, m.rows - 97] + list(rng.integers(0, m.rows - 97, 30))))
-    for r0 in starts:
-        exp = oracle.q4mv(*m.arrays(), xn_o, xs_o, m.cols, row0=int(r0), n=97)
-        assert_bits_equal(got[r0:r0 + 97], exp, f"head rows {r0}+97")
+    assert_bits_equal(got, oracle.q4mv(*m.arrays(), xn_o, xs_o, m.cols), "head, all rows")
     assert np.all(np.isfinite(got))
 
 
 @pytest.mark.parametrize("rows,cols", [(16384, 6144), (65536, 2048), (6144, 4096)])
-def test_sweep_points_sampled(rows, cols):
+def test_sweep_points_whole_output(rows, cols):
     m, x = synth.sweep_point(rows, cols)
     xs = oracle.gsum(x)
-    got = run(m, x, xs=xs)
-    for r0 in (0, rows // 3, rows - 50):
-        assert_bits_equal(got[r0:r0 + 50], oracle.q4mv(*m.arrays(), x, xs, cols, row0=r0, n=50), f"{rows}x{cols}@{r0}")
+    assert_bits_equal(run(m, x, xs=xs), oracle.q4mv(*m.arrays(), x, xs, cols), f"{rows}x{cols}")
 
 
 def test_grouped_launch_matches_single_calls():

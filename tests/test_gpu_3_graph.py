@@ -111,6 +111,15 @@ def test_graph_rejects_same_stage_hazards(small):
     with pytest.raises(abg.AbgError) as e:
         abg.StageGraph(nodes)
     assert e.value.status == 4
+    # a node that writes the norm weights of a later product's RMS-norm prologue
+    # (they are read before the wait for the previous stage)
+    wt = empty(dm.hidden)
+    wt.copy_(L["rms1"])
+    nodes = [abg.Node.gsum(0, x, wt[: dm.hidden // 64]),
+             abg.Node.q4mv(1, q.w, q.scale, q.bias, y, q.cols, x=dev(h), prologue=abg.PRO_RMSQ, wt=wt)]
+    with pytest.raises(abg.AbgError) as e:
+        abg.StageGraph(nodes)
+    assert e.value.status == 4
 
 
 @pytest.mark.parametrize("cols", [128, 1088, 2048, 6144, 16384])

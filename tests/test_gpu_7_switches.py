@@ -1,0 +1,98 @@
+"""The stage graph's environment switches, each in a child process (both are
+read once per process, at the first graph creation or launch).
+
+ABG_TRACE=1: every graph launch synchronizes and prints one stderr line with
+the launch count, the GPU milliseconds and the wall milliseconds.
+ABG_PDL=0: launches are recorded without programmatic dependent launch; the
+results are the same bits as with it.
+"""
+from __future__ import annotations
+
+import os
+import re
+import subprocess
+import sys
+
+import numpy as np
+import pytest
+
+import oracle
+from affine_bit_group_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+abg = pytest.importorskip("affine_bit_group_gb300")
+from affine_bit_group_gb300 import decode  # noqa: E402
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SMALL = dict(seed=11, n_layers=2, hidden=1024, mlp=3072, head_rows=3000, q_rows=2048, kv_rows=256)
+
+CHILD = """
+import sys
+sys.path.insert(0, {root!r})
+import numpy as np, torch
+import affine_bit_group_gb300 as abg
+import oracle
+from affine_bit_group_gb300 import decode, synth
+model, h = synth.decode_model(**{small!r})
+dm = decode.DeviceModel.upload(model)
+g, out = decode.decode_token_graph(dm, torch.from_numpy(h).cuda(), fused={fused!r})
+for _ in range({reps}):
+    g.launch()
+torch.cuda.synchronize()
+got = out["logits"].cpu().numpy()
+exp = oracle.decode_token(model, h)
+print("LAUNCHES", g.launches)
+print("EQUAL", int(np.array_equal(got.view(np.uint32), exp.view(np.uint32))))
+print("HASH", oracle.hash32(got))
+"""
+
+
+def child(env_extra, fused, reps):
+    env = dict(os.environ)
+    env.update(env_extra)
+    code = CHILD.format(root=ROOT, small=SMALL, fused=fused, reps=reps)
+    r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    vals = dict(line.split(None, 1) for line in r.stdout.splitlines() if line and line.split()[0].isupper())
+    return vals, r.stderr
+
+
+def in_process_hash(fused):
+    model, h = synth.decode_model(**SMALL)
+    dm = decode.DeviceModel.upload(model)
+    g, out = decode.decode_token_graph(dm, torch.from_numpy(h).cuda(), fused=fused)
+    g.launch()
+    torch.cuda.synchronize()
+    got = out["logits"].cpu().numpy()
+    g.close()
+    return oracle.hash32(got)
+
+
+@pytest.mark.parametrize("fused", [False, True])
+def test_pdl_off_gives_the_same_bits(fused):
+    vals, _ = child({"ABG_PDL": "0"}, fused, reps=2)
+    assert vals["EQUAL"].strip() == "1"
+    assert int(vals["HASH"]) == in_process_hash(fused)
+
+
+def test_trace_prints_one_line_per_launch():
+    vals, err = child({"ABG_TRACE": "1"}, True, reps=3)
+    assert vals["EQUAL"].strip() == "1"
+    lines = [l for l in err.splitlines() if l.startswith("abg: stage graph")]
+    assert len(lines) == 3, err[-2000:]
+    n = int(vals["LAUNCHES"])
+    pat = re.compile(r"abg: stage graph (\d+) launches, GPU ([0-9.]+) ms, wall ([0-9.]+) ms")
+    for l in lines:
+        m = pat.fullmatch(l.strip())
+        assert m, l
+        assert int(m.group(1)) == n
+        gpu, wall = float(m.group(2)), float(m.group(3))
+        assert 0.0 < gpu and 0.0 < wall and gpu <= wall * 1.5 + 0.05
+
+
+def test_trace_off_prints_nothing():
+    vals, err = child({}, True, reps=1)
+    assert vals["EQUAL"].strip() == "1"
+    assert "abg: stage graph" not in err
