@@ -86,6 +86,7 @@ def library(build_if_missing: bool = True) -> ctypes.CDLL:
             lib.abg_stage_graph_create.argtypes = [ctypes.POINTER(_Node), I64, I, I, ctypes.POINTER(P)]
             lib.abg_stage_graph_launch.argtypes = [P, P]
             lib.abg_stage_graph_launches.argtypes = [P, ctypes.POINTER(I64)]
+            lib.abg_stage_graph_swiglu_pairs.argtypes = [P, ctypes.POINTER(I64)]
             lib.abg_stage_graph_destroy.argtypes = [P]
             lib.abg_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32), I]
             lib.abg_selftest_wait_timeout.argtypes = [P]
@@ -96,7 +97,8 @@ def library(build_if_missing: bool = True) -> ctypes.CDLL:
             lib.abg_last_cuda_error.restype = ctypes.c_char_p
             for f in ("abg_q4mv", "abg_q4mm", "abg_gsum", "abg_rmsq", "abg_swq", "abg_q4mv_ex", "abg_gsum_ex", "abg_rmsq_ex",
                       "abg_swq_ex", "abg_stage_graph_create",
-                      "abg_stage_graph_launch", "abg_stage_graph_launches", "abg_stage_graph_destroy",
+                      "abg_stage_graph_launch", "abg_stage_graph_launches", "abg_stage_graph_swiglu_pairs",
+                      "abg_stage_graph_destroy",
                       "abg_device_status", "abg_set_q4mv_tuning", "abg_selftest_wait_timeout"):
                 getattr(lib, f).restype = ctypes.c_int
             _lib = lib
@@ -270,6 +272,8 @@ class StageGraph:
         n = ctypes.c_int64()
         _check(library().abg_stage_graph_launches(self._h, ctypes.byref(n)), "abg_stage_graph_launches")
         self.launches = n.value
+        _check(library().abg_stage_graph_swiglu_pairs(self._h, ctypes.byref(n)), "abg_stage_graph_swiglu_pairs")
+        self.swiglu_pairs = n.value
 
     def launch(self, stream=None):
         _check(library().abg_stage_graph_launch(self._h, _stream(stream)), "abg_stage_graph_launch")

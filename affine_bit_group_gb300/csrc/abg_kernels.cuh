@@ -50,6 +50,13 @@ struct Q4Args {
     // failure-detection self-test only: the producer delivers no tile, so the
     // computing warps' bounded waits run out (see abg_selftest_wait_timeout)
     int withhold;
+    // SwiGLU pair (fixed shapes, 4 rows per item): problems 0 and 1 are the
+    // gate and up products of one activation, with equal shapes; a tile holds
+    // tile_rows/2 rows of each (the same row indices), every item 2 gate rows
+    // and the same 2 up rows, and the computing warps write
+    // epi[r] = silu(gate y[r]) * up y[r] besides both outputs
+    int paired;
+    float *epi;
     // batched product only: activation and group-sum rows of the T token
     // slots, and how many of them are real tokens
     const float *xt[4];

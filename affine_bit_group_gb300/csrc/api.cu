@@ -184,6 +184,7 @@ struct Launch {
     int kind;  // abg_node_kind
     int stage = 0;
     Q4Plan plan;
+    std::vector<Q4Call> calls;  // the products of a Q4MV launch
     const float *a = nullptr, *b = nullptr;
     float *o = nullptr, *os = nullptr;
     float eps = 0.f;
@@ -195,7 +196,72 @@ struct StageGraph {
     cudaGraph_t graph = nullptr;
     cudaGraphExec_t exec = nullptr;
     int64_t launches = 0;
+    int64_t swiglu_pairs = 0;
+    std::vector<void *> scratch;  // device buffers of fused SwiGLU vectors
 };
+
+void free_scratch(StageGraph *g) {
+    for (void *p : g->scratch) cudaFree(p);
+    g->scratch.clear();
+}
+
+// SwiGLU pairs.  A product launch D whose activation is the SwiGLU of a =
+// [gate | up] (the SwiGLU prologue), right after a launch GU of the previous
+// stage that holds exactly the two products writing a[0, n) (gate) and
+// a[n, 2n) (up), gets that vector from GU's epilogue: each of GU's tiles holds
+// the same rows of both products, and the warp that finishes a gate row and
+// its up row writes silu(gate) * up, once per element, into a buffer the graph
+// owns; D reads it with the group-sum prologue instead of recomputing the
+// SwiGLU in every thread block.  Both write the same outputs as before, bit
+// for bit (the same SwiGLU of the same values, the same group-sum tree).  Only
+// launches planned with a fixed shape and 4 rows per item are paired.
+abg_status fuse_swiglu_pairs(std::vector<Launch> &launches, StageGraph *g, int mode, int rpw) {
+    for (size_t d = 1; d < launches.size(); ++d) {
+        Launch &D = launches[d], &GU = launches[d - 1];
+        if (D.kind != ABG_NODE_Q4MV || D.calls.empty() || D.calls[0].prologue != kProSwq) continue;
+        if (GU.kind != ABG_NODE_Q4MV || GU.calls.size() != 2 || GU.stage + 1 != D.stage) continue;
+        const float *a = D.calls[0].x;
+        const int64_t n = D.calls[0].cols;
+        if (D.calls[0].group != 64) continue;
+        int gi = -1, ui = -1;
+        for (int i = 0; i < 2; ++i) {
+            const Q4Call &c = GU.calls[i];
+            if (c.n != n) continue;
+            if (c.y == a) gi = i;
+            if (c.y == a + n) ui = i;
+        }
+        if (gi < 0 || ui < 0 || gi == ui) continue;
+        Q4Plan pair_plan;
+        const std::vector<Q4Call> gu = {GU.calls[gi], GU.calls[ui]};
+        if (plan_calls(&pair_plan, gu, mode, rpw) != ABG_OK || pair_plan.shape == 0 || pair_plan.rows_per_warp != 4)
+            continue;
+        void *o = nullptr;
+        const cudaError_t e = cudaMalloc(&o, static_cast<size_t>(n) * sizeof(float));
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc (SwiGLU vector)");
+        g->scratch.push_back(o);
+        std::vector<Q4Call> dc = D.calls;
+        for (Q4Call &c : dc) {
+            c.prologue = kProGsum;
+            c.x = static_cast<const float *>(o);
+        }
+        Q4Plan d_plan;
+        const abg_status st = plan_calls(&d_plan, dc, mode, rpw);
+        if (st != ABG_OK) return st;
+        // a tile holds tile_rows/2 rows of each product
+        Q4Args &pa = pair_plan.args;
+        pa.paired = 1;
+        pa.epi = static_cast<float *>(o);
+        const int64_t half_rows = pa.tile_rows / 2;
+        pa.total_tiles = (n + half_rows - 1) / half_rows;
+        pair_plan.grid.x = static_cast<unsigned>(std::min<int64_t>(pair_plan.grid.x, pa.total_tiles));
+        GU.plan = pair_plan;
+        GU.calls = gu;
+        D.plan = d_plan;
+        D.calls = dc;
+        ++g->swiglu_pairs;
+    }
+    return ABG_OK;
+}
 
 cudaError_t prepare(const Launch &L) {
     if (L.kind != ABG_NODE_Q4MV) return cudaSuccess;
@@ -446,6 +512,7 @@ abg_status abg_stage_graph_create(const abg_node *nodes, int64_t count, int mode
                 }
                 abg_status st = plan_calls(&L.plan, group, mode, rows_per_warp);
                 if (st != ABG_OK) return st;
+                L.calls = group;
             } else {
                 L.a = nd.x;
                 L.b = nd.wt;
@@ -460,6 +527,14 @@ abg_status abg_stage_graph_create(const abg_node *nodes, int64_t count, int mode
     }
     auto *g = new StageGraph();
     g->launches = static_cast<int64_t>(launches.size());
+    {
+        const abg_status st = fuse_swiglu_pairs(launches, g, mode, rows_per_warp);
+        if (st != ABG_OK) {
+            free_scratch(g);
+            delete g;
+            return st;
+        }
+    }
     cudaError_t e = cudaSuccess;
     std::string where;
     for (const Launch &L : launches)
@@ -495,6 +570,7 @@ abg_status abg_stage_graph_create(const abg_node *nodes, int64_t count, int mode
     if (e != cudaSuccess) {
         if (g->exec) cudaGraphExecDestroy(g->exec);
         if (g->graph) cudaGraphDestroy(g->graph);
+        free_scratch(g);
         delete g;
         cudaGetLastError();
         return cuda_fail(e, where.c_str());
@@ -542,6 +618,12 @@ abg_status abg_stage_graph_launches(void *graph, int64_t *launches) {
     return ABG_OK;
 }
 
+abg_status abg_stage_graph_swiglu_pairs(void *graph, int64_t *pairs) {
+    if (!graph_live(graph) || !pairs) return ABG_EINVAL;
+    *pairs = static_cast<StageGraph *>(graph)->swiglu_pairs;
+    return ABG_OK;
+}
+
 abg_status abg_stage_graph_destroy(void *graph) {
     {
         std::lock_guard<std::mutex> lock(g_graphs_mu);
@@ -554,6 +636,7 @@ abg_status abg_stage_graph_destroy(void *graph) {
         const cudaError_t e2 = cudaGraphDestroy(g->graph);
         if (e == cudaSuccess) e = e2;
     }
+    free_scratch(g);
     delete g;
     return cuda_fail(e);
 }

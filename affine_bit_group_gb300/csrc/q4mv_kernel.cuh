@@ -635,12 +635,19 @@ constexpr int layout_blocks(int l) { return l == 1 ? 1 : 2; }
 // k + 2, and a warp reads it at tile k and, for the final sums, before it
 // starts tile k + 2.
 struct TileHdr {
-    float *y;        // output of the tile's first row
+    float *y;        // output of the tile's first row (a SwiGLU pair: of its gate rows)
+    float *y2;       // a SwiGLU pair: output of the tile's first up row
+    float *epi;      // a SwiGLU pair: SwiGLU output of the tile's first row
     const void *sc;  // scale and bias of the tile's first row in global memory
     const void *bi;  // (read there when they are not staged)
-    int rows;        // rows of the tile: tile_rows, fewer at a problem's end
+    int rows;        // rows of the tile (a SwiGLU pair: of each product); fewer at a problem's end
     int pad;
 };
+
+// The i-th tile of this block: tiles blockIdx.x, blockIdx.x + gridDim.x, ...
+__device__ __forceinline__ int tile_of(const Q4Args &, int i) {
+    return static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x);
+}
 constexpr int kMaxStages = 8;
 constexpr int kMaxHdr = kMaxStages + 2;
 
@@ -809,7 +816,7 @@ __global__ void __launch_bounds__(layout_threads(kLayout), layout_blocks(kLayout
         int k = 0, s = 0, hs = 0;
         const int NP = a.parts;
         uint32_t eph = 1;
-        for (int t = blockIdx.x; t < total; t += gridDim.x, ++k) {
+        for (int t = tile_of(a, 0); t < total; t = tile_of(a, ++k)) {
             if (a.withhold) break;  // self-test: nothing is copied, nothing is in flight
             if (k == S) {
                 grid_dep_wait();
@@ -818,10 +825,14 @@ __global__ void __launch_bounds__(layout_threads(kLayout), layout_blocks(kLayout
             }
             if (k >= S && !wait_or_abort(&empty[s], eph, &s_abort, kSiteEmpty)) break;
             if (s_abort) break;
-            int tile;
-            const Q4Prob &P = a.prob[cur.find(a, t, tile)];
-            const int64_t r0 = static_cast<int64_t>(tile) * TR;
-            const int rows = static_cast<int>(min(static_cast<int64_t>(TR), P.n - r0));
+            int tile = t;
+            const int pidx = a.paired ? 0 : cur.find(a, t, tile);
+            const Q4Prob &P = a.prob[pidx];
+            // a SwiGLU pair's tile: TR/2 rows of the gate product into the
+            // stage's first half, the same rows of the up product after them
+            const int trp = a.paired ? TR / 2 : TR;
+            const int64_t r0 = static_cast<int64_t>(tile) * trp;
+            const int rows = static_cast<int>(min(static_cast<int64_t>(trp), P.n - r0));
             unsigned char *st = smem + a.off_stage + static_cast<size_t>(s) * stage_bytes;
             const uint32_t wb = static_cast<uint32_t>(rows) * W * 4u;
             const uint32_t sbb = kSbSmem ? static_cast<uint32_t>(rows) * G * kElem : 0u;
@@ -829,16 +840,23 @@ __global__ void __launch_bounds__(layout_threads(kLayout), layout_blocks(kLayout
             TileHdr &h = s_hdr[hs];
             if (++hs == NP) hs = 0;
             h.y = P.y + r0;
+            h.y2 = a.paired ? a.prob[1].y + r0 : nullptr;
+            h.epi = a.paired ? a.epi + r0 : nullptr;
             h.sc = static_cast<const unsigned char *>(P.scale) + sbo;
             h.bi = static_cast<const unsigned char *>(P.bias) + sbo;
             h.rows = rows;
-            mbar_arrive_expect_tx(&full[s], wb + 2 * sbb);
-            bulk_g2s(st, P.w + r0 * W, wb, &full[s], policy);
-            if (kSbSmem) {
-                bulk_g2s(st + stage_w_bytes, static_cast<const unsigned char *>(P.scale) + sbo, sbb, &full[s],
-                         policy);
-                bulk_g2s(st + stage_w_bytes + stage_sb_bytes, static_cast<const unsigned char *>(P.bias) + sbo,
-                         sbb, &full[s], policy);
+            mbar_arrive_expect_tx(&full[s], (a.paired ? 2u : 1u) * (wb + 2 * sbb));
+            for (int q = 0; q < (a.paired ? 2 : 1); ++q) {
+                const Q4Prob &Q = a.prob[pidx + q];
+                const uint32_t hw = q ? static_cast<uint32_t>(trp) * W * 4u : 0u;
+                const uint32_t hsb = q ? static_cast<uint32_t>(trp) * G * kElem : 0u;
+                bulk_g2s(st + hw, Q.w + r0 * W, wb, &full[s], policy);
+                if (kSbSmem) {
+                    bulk_g2s(st + stage_w_bytes + hsb, static_cast<const unsigned char *>(Q.scale) + sbo, sbb,
+                             &full[s], policy);
+                    bulk_g2s(st + stage_w_bytes + stage_sb_bytes + hsb,
+                             static_cast<const unsigned char *>(Q.bias) + sbo, sbb, &full[s], policy);
+                }
             }
             if (++s == S) {
                 s = 0;
@@ -936,17 +954,25 @@ __global__ void __launch_bounds__(layout_threads(kLayout), layout_blocks(kLayout
     uint32_t sbo[NB];
     int sbd = 0;
     int gown = 0, gpar = 0;
+    // item row j -> stage row (relative to the item's first row): j, or in a
+    // SwiGLU pair (R = 4: gate rows 0..R/2-1, then the same up rows in the
+    // stage's second half) j < R/2 ? j : TR/2 + j - R/2
+    const bool paired = R == 4 && a.paired != 0;
+    const int rbm = paired ? R / 2 : R;  // stage rows per item block
+    auto srow = [&](int j) -> uint32_t {
+        return static_cast<uint32_t>(paired && j >= R / 2 ? TR / 2 + j - R / 2 : j);
+    };
     auto set_chunk = [&](int ch) {
         const uint32_t quad = sl.act ? static_cast<uint32_t>(ch * 32 + lane) * 16u : 0u;
 #pragma unroll
-        for (int i = 0; i < B; ++i) roff[i] = static_cast<uint32_t>(i ^ pi) * rowW + quad;
+        for (int i = 0; i < B; ++i) roff[i] = srow(i ^ pi) * rowW + quad;
         // a lane past the row end keeps its group index only to name its
         // partner; its own term is replaced by -0 and reads group 0
         const int gv = ch * (32 >> kLg) + (lane >> kLg);
         gown = sl.act ? gv : 0;
         gpar = sl.actp ? (gv ^ 1) : gown;
 #pragma unroll
-        for (int i = 0; i < NB; ++i) sbo[i] = (static_cast<uint32_t>(i ^ pi) * G + gown) * kElem;
+        for (int i = 0; i < NB; ++i) sbo[i] = (srow(i ^ pi) * G + gown) * kElem;
         sbd = (gpar - gown) * static_cast<int>(kElem);
     };
     if (cur_ch >= 0) set_chunk(cur_ch);  // slice computed by the prologue
@@ -958,7 +984,7 @@ __global__ void __launch_bounds__(layout_threads(kLayout), layout_blocks(kLayout
                     int rb, bool keep) -> float {
         constexpr bool kExact = decltype(exact_c)::value;
         constexpr bool kPartial = decltype(partial_c)::value;
-        const unsigned char *blk = stg + static_cast<uint32_t>(rb * R) * rowW;
+        const unsigned char *blk = stg + static_cast<uint32_t>(rb * rbm) * rowW;
         float v[R];
 #pragma unroll
         for (int b = 0; b < R / B; ++b) {
@@ -1000,7 +1026,7 @@ __global__ void __launch_bounds__(layout_threads(kLayout), layout_blocks(kLayout
             const int row = rb * R + (i ^ pi);
             float2 sc, bi;
             if constexpr (kSbSmem) {
-                const unsigned char *so = stg + stage_w_bytes + static_cast<uint32_t>(rb * R * G) * kElem + sbo[i];
+                const unsigned char *so = stg + stage_w_bytes + static_cast<uint32_t>(rb * rbm * G) * kElem + sbo[i];
                 const unsigned char *sp = so + sbd;
                 sc = f2(sb_at(so, 0), sb_at(sp, 0));
                 bi = f2(sb_at(so + stage_sb_bytes, 0), sb_at(sp + stage_sb_bytes, 0));
@@ -1080,22 +1106,39 @@ __global__ void __launch_bounds__(layout_threads(kLayout), layout_blocks(kLayout
         const int frow = rb0 * R + pi;  // the row whose final sum this lane writes (lane < R)
         auto final_rows = [&](int q, uint32_t ph, float own) -> bool {
             if (!wait_or_abort(&done[q], ph, &s_abort, kSiteDone)) return false;
+            const TileHdr &fh = s_hdr[q];
+            float yv = 0.f;
             if (lane < R) {
-                const TileHdr &fh = s_hdr[q];
-                if (frow < fh.rows) {
-                    const float *pr = part + (q * TR + frow) * nch;
-                    float c[fixed_nch(kC)];
-                    c[0] = own;
+                const float *pr = part + (q * TR + frow) * nch;
+                float c[fixed_nch(kC)];
+                c[0] = own;
 #pragma unroll
-                    for (int i = 1; i < fixed_nch(kC); ++i) c[i] = pr[i];
-                    fh.y[frow] = tree_fixed<fixed_nch(kC), kTree>(c);
+                for (int i = 1; i < fixed_nch(kC); ++i) c[i] = pr[i];
+                yv = tree_fixed<fixed_nch(kC), kTree>(c);
+            }
+            if (paired) {
+                // item row j = pi: gate row rb0*R/2 + j (j < R/2) or up row
+                // rb0*R/2 + j - R/2; the up value of a gate lane's row sits one
+                // lane away (pi reverses the lane bits)
+                const float up = __shfl_xor_sync(0xffffffffu, yv, 1);
+                const int j = pi, prow = rb0 * (R / 2) + (j & (R / 2 - 1));
+                if (lane < R && prow < fh.rows) {
+                    if (j < R / 2) {
+                        fh.y[prow] = yv;
+                        fh.epi[prow] = swiglu<kTree>(yv, up);
+                    } else {
+                        fh.y2[prow] = yv;
+                    }
                 }
+            } else if (lane < R && frow < fh.rows) {
+                fh.y[frow] = yv;
             }
             return true;
         };
         auto run = [&](auto exact_c) {
             float own = 0.f;
-            for (int t = blockIdx.x; t < total; t += gridDim.x) {
+            int i = 0;
+            for (int t = tile_of(a, 0); t < total; t = tile_of(a, ++i)) {
                 if (!wait_or_abort(&full[s], fph, &s_abort, kSiteFull)) break;
                 const unsigned char *stg = stage0 + static_cast<uint32_t>(s) * stage_bytes;
                 float *prt = part + p * TR * nch;
@@ -1126,7 +1169,8 @@ __global__ void __launch_bounds__(layout_threads(kLayout), layout_blocks(kLayout
             run(std::false_type{});
         }
     } else {
-        for (int t = blockIdx.x; t < total; t += gridDim.x) {
+        int ti = 0;
+        for (int t = tile_of(a, 0); t < total; t = tile_of(a, ++ti)) {
             if (!wait_or_abort(&full[s], fph, &s_abort, kSiteFull)) break;
             const unsigned char *stg = stage0 + static_cast<uint32_t>(s) * stage_bytes;
             const TileHdr &h = s_hdr[p];

@@ -259,7 +259,9 @@ typedef struct abg_node {
 
 /* Validates every node (same rules as the single calls), checks that no node
  * reads an output of its own stage, records the launches on a private stream
- * and instantiates the graph.  *graph_out receives an opaque handle. */
+ * and instantiates the graph.  *graph_out receives an opaque handle.  The
+ * graph owns its executable graph and, for SwiGLU pairs (see
+ * abg_stage_graph_swiglu_pairs), one device buffer of n floats per pair. */
 abg_status abg_stage_graph_create(const abg_node *nodes, int64_t count, int mode, int rows_per_warp,
                                   void **graph_out);
 /* With the environment variable ABG_PDL=0 at creation, launches are recorded
@@ -271,6 +273,16 @@ abg_status abg_stage_graph_create(const abg_node *nodes, int64_t count, int mode
 abg_status abg_stage_graph_launch(void *graph, void *stream);
 /* Number of kernel launches one replay performs (after sibling grouping). */
 abg_status abg_stage_graph_launches(void *graph, int64_t *launches);
+/* SwiGLU pairs: when a Q4MV node with the ABG_PRO_SWQ prologue reads a =
+ * [gate | up] (2n values) written by the only two products of the launch
+ * right before it (gate y = a[0, n), up y = a[n, 2n), one activation, n rows
+ * each, groups of 64 with f32 scale and bias, 2048, 4096 or 6144 columns), the
+ * gate/up launch also writes silu(gate) * up once per element into a device
+ * buffer of n floats that the graph allocates at creation and frees in
+ * abg_stage_graph_destroy, and the reading product takes its group sums from
+ * that buffer instead of recomputing the SwiGLU in every thread block.  Every
+ * node's outputs keep their bits.  *pairs receives how many were formed. */
+abg_status abg_stage_graph_swiglu_pairs(void *graph, int64_t *pairs);
 abg_status abg_stage_graph_destroy(void *graph);
 
 /* Reads (and, if clear != 0, resets) the device status word on the current

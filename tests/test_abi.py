@@ -200,3 +200,4 @@ def test_unknown_graph_handles_are_refused(lib):
     assert lib.abg_stage_graph_destroy(fake) == EINVAL
     n = ctypes.c_int64()
     assert lib.abg_stage_graph_launches(fake, ctypes.byref(n)) == EINVAL
+    assert lib.abg_stage_graph_swiglu_pairs(fake, ctypes.byref(n)) == EINVAL

@@ -161,6 +161,7 @@ def test_full_decode_token_bit_exact():
     dm = decode.DeviceModel.upload(model)
     h0 = dev(h)
     g, out = decode.decode_token_graph(dm, h0, fused=True)
+    assert g.swiglu_pairs == len(dm.layers)  # every layer's gate/up launch writes the SwiGLU vector
     g.launch()
     torch.cuda.synchronize()
     assert_bits_equal(host(out["logits"]), exp, "full decode logits")
@@ -171,3 +172,38 @@ def test_full_decode_token_bit_exact():
     assert abg.device_status(clear=True) == 0
     g.close()
     g2.close()
+
+
+@pytest.mark.parametrize("cols", [2048, 4096, 6144])
+@pytest.mark.parametrize("adjacent", [True, False])
+def test_swiglu_pair(cols, adjacent):
+    """gate/up products into a = [gate | up], then a product with the SwiGLU
+    prologue on a: with the reader in the next stage the gate/up launch writes
+    the SwiGLU vector (one pair formed), otherwise not; either way every output
+    equals the oracle's (gate, up, the SwiGLU of them, the product)."""
+    n = 1088  # rows of gate and up, the reader's columns (not a whole tile count)
+    mg, x = synth.random_case(8100 + cols, n, cols)
+    mu, _ = synth.random_case(8200 + cols, n, cols)
+    md, _ = synth.random_case(8300 + cols, 700, n)
+    xd, xsd = dev(x), dev(oracle.gsum(x))
+    a = empty(2 * n)
+    yd = empty(700)
+    G, U, D = [(dev_words(m.w), dev(m.scale), dev(m.bias)) for m in (mg, mu, md)]
+    nodes = [abg.Node.q4mv(0, *G, a[:n], cols, x=xd, xsum=xsd), abg.Node.q4mv(0, *U, a[n:], cols, x=xd, xsum=xsd)]
+    if not adjacent:
+        spare = empty(64)
+        nodes.append(abg.Node.gsum(1, xd[:64], spare[:1]))
+    nodes.append(abg.Node.q4mv(1 if adjacent else 2, *D, yd, n, x=a, prologue=abg.PRO_SWQ))
+    g = abg.StageGraph(nodes, keep=[xd, xsd, a, yd] + list(G) + list(U) + list(D))
+    assert g.swiglu_pairs == (1 if adjacent else 0)
+    g.launch()
+    torch.cuda.synchronize()
+    xs = oracle.gsum(x)
+    gy = oracle.q4mv(*mg.arrays(), x, xs, cols)
+    uy = oracle.q4mv(*mu.arrays(), x, xs, cols)
+    assert_bits_equal(host(a)[:n], gy, "gate")
+    assert_bits_equal(host(a)[n:], uy, "up")
+    o, osum = oracle.swq(np.concatenate([gy, uy]))
+    assert_bits_equal(host(yd), oracle.q4mv(*md.arrays(), o, osum, n), "reader of the SwiGLU")
+    assert abg.device_status(clear=True) == 0
+    g.close()
