@@ -18,7 +18,7 @@ import threading
 
 __all__ = [
     "TREE", "FAST", "AbgError", "library", "q4mv", "q4mv_ex", "q4mm", "gsum", "rmsq", "swq", "StageGraph", "Node",
-    "device_status", "set_q4mv_tuning", "MAX_COLS", "SB_F32", "SB_BF16", "SB_F16", "SB_TYPES",
+    "device_status", "set_q4mv_tuning", "MAX_COLS", "SB_F32", "SB_BF16", "SB_F16", "SB_TYPES", "swiglu_mlp_static",
 ]
 
 TREE, FAST = 0, 1
@@ -87,6 +87,7 @@ def library(build_if_missing: bool = True) -> ctypes.CDLL:
             lib.abg_stage_graph_launch.argtypes = [P, P]
             lib.abg_stage_graph_launches.argtypes = [P, ctypes.POINTER(I64)]
             lib.abg_stage_graph_swiglu_pairs.argtypes = [P, ctypes.POINTER(I64)]
+            lib.abg_swiglu_mlp_static.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P, I64, I64, I64, I, P]
             lib.abg_stage_graph_destroy.argtypes = [P]
             lib.abg_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32), I]
             lib.abg_selftest_wait_timeout.argtypes = [P]
@@ -98,7 +99,7 @@ def library(build_if_missing: bool = True) -> ctypes.CDLL:
             for f in ("abg_q4mv", "abg_q4mm", "abg_gsum", "abg_rmsq", "abg_swq", "abg_q4mv_ex", "abg_gsum_ex", "abg_rmsq_ex",
                       "abg_swq_ex", "abg_stage_graph_create",
                       "abg_stage_graph_launch", "abg_stage_graph_launches", "abg_stage_graph_swiglu_pairs",
-                      "abg_stage_graph_destroy",
+                      "abg_stage_graph_destroy", "abg_swiglu_mlp_static",
                       "abg_device_status", "abg_set_q4mv_tuning", "abg_selftest_wait_timeout"):
                 getattr(lib, f).restype = ctypes.c_int
             _lib = lib
@@ -192,6 +193,25 @@ def q4mm(w, scale, bias, X, XS, Y, cols: int, row0: int = 0, n: int | None = Non
         rows, cols, row0, n, T, mode, rows_per_warp, _stream(stream))
     _check(st, "abg_q4mm")
     return Y
+
+
+def swiglu_mlp_static(gate, up, down, x, xsum, y, cols: int, mode: int = TREE, stream=None):
+    """y = down(silu(gate x) * (up x)) with no device allocation (abg_swiglu_mlp_static).
+
+    gate, up, down are (w, scale, bias) triples of CUDA tensors: gate and up
+    n x cols, down rows x n, with n <= 16384.  The intermediate vectors live in
+    a static device array inside the library, shared by every call (see
+    include/abg.h for who needs this and the ordering rule).
+    """
+    (wg, sg, bg), (wu, su, bu), (wd, sd, bd) = gate, up, down
+    n = wg.numel() * 8 // cols
+    rows = y.numel()
+    _check(library().abg_swiglu_mlp_static(
+        _ptr(wg, name="gate w"), _ptr(sg, name="gate scale"), _ptr(bg, name="gate bias"),
+        _ptr(wu, name="up w"), _ptr(su, name="up scale"), _ptr(bu, name="up bias"),
+        _ptr(wd, name="down w"), _ptr(sd, name="down scale"), _ptr(bd, name="down bias"),
+        _ptr(x, name="x"), _ptr(xsum, name="xsum"), _ptr(y, name="y"), n, cols, rows, mode, _stream(stream)),
+        "abg_swiglu_mlp_static")
 
 
 def gsum(v, s, mode: int = TREE, stream=None, group: int = 64):

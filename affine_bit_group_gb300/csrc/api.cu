@@ -328,6 +328,38 @@ bool same_activation(const Q4Call &a, const Q4Call &b) {
            sb_bulk(a) == sb_bulk(b);
 }
 
+// ------------------------------------------------- allocation-free MLP ----
+// abg_swiglu_mlp_static keeps its intermediate vectors in this array instead
+// of memory it would have to allocate: the gate outputs, the up outputs and
+// their SwiGLU, kMlpMaxHidden floats each (192 KB).  Every device that loads
+// the library holds one copy until the process exits.  In host code the
+// name is only a stand-in for the device symbol: its device address comes
+// from cudaGetSymbolAddress, once per device (mlp_scratch below).
+constexpr int64_t kMlpMaxHidden = 16384;
+static __device__ __align__(256) float g_mlp_scratch[3 * kMlpMaxHidden];
+
+std::mutex g_mlp_mu;
+constexpr int kMlpMaxDevices = 64;
+float *g_mlp_ptr[kMlpMaxDevices] = {};
+
+// The device address of g_mlp_scratch on the current device (looked up on
+// the first call per device, with that device current).
+abg_status mlp_scratch(float **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMlpMaxDevices) return ABG_EINVAL;
+    std::lock_guard<std::mutex> lock(g_mlp_mu);
+    if (!g_mlp_ptr[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_mlp_scratch);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress (MLP scratch)");
+        g_mlp_ptr[dev] = static_cast<float *>(p);
+    }
+    *out = g_mlp_ptr[dev];
+    return ABG_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -695,5 +727,70 @@ const char *abg_status_str(int status) {
 }
 
 const char *abg_last_cuda_error(void) { return g_cuda_error.c_str(); }
+
+abg_status abg_swiglu_mlp_static(const uint32_t *wg, const float *sg, const float *bg, const uint32_t *wu,
+                                 const float *su, const float *bu, const uint32_t *wd, const float *sd,
+                                 const float *bd, const float *x, const float *xsum, float *y, int64_t n,
+                                 int64_t cols, int64_t rows, int mode, void *stream) {
+    // Checked before any device work (this call allocates no device memory
+    // and takes no buffer from the caller for its intermediate vectors).
+    if (mode != ABG_TREE && mode != ABG_FAST) return ABG_EINVAL;
+    if (n <= 0 || n % 64 != 0) return ABG_ESHAPE;
+    if (n > kMlpMaxHidden) return ABG_ESHAPE;  // larger than the static scratch
+    if (cols <= 0 || cols % 64 != 0 || cols > ABG_MAX_COLS || rows < 0) return ABG_ESHAPE;
+    if (rows == 0) return ABG_OK;
+    if (!wg || !sg || !bg || !wu || !su || !bu || !wd || !sd || !bd || !x || !xsum || !y) return ABG_EINVAL;
+    const void *a16[] = {wg, wu, wd, x};
+    for (const void *q : a16)
+        if (!aligned(q, 16)) return ABG_EALIGN;
+    const void *a4[] = {sg, bg, su, bu, sd, bd, xsum, y};
+    for (const void *q : a4)
+        if (!aligned(q, 4)) return ABG_EALIGN;
+    const int64_t G = cols / 64, Gd = n / 64;
+    const Range ins[] = {rng(wg, n * (cols / 8), 4), rng(sg, n * G, 4), rng(bg, n * G, 4),
+                         rng(wu, n * (cols / 8), 4), rng(su, n * G, 4), rng(bu, n * G, 4),
+                         rng(wd, rows * (n / 8), 4), rng(sd, rows * Gd, 4), rng(bd, rows * Gd, 4),
+                         rng(x, cols, 4),           rng(xsum, G, 4)};
+    const Range out = rng(y, rows, 4);
+    for (const Range &r : ins)
+        if (overlap(out, r)) return ABG_EALIAS;
+    float *sp = nullptr;
+    abg_status st = mlp_scratch(&sp);
+    if (st != ABG_OK) return st;
+    // scratch: gate outputs [0, n), up outputs [n, 2n), SwiGLU [2n, 3n);
+    // every element is written before it is read, so nothing is cleared
+    const Q4Call gc{wg, sg, bg, n, cols, 0, n, sp, kProNone, x, xsum, nullptr, 0.f};
+    const Q4Call uc{wu, su, bu, n, cols, 0, n, sp + n, kProNone, x, xsum, nullptr, 0.f};
+    const bool tree = mode == ABG_TREE;
+    Q4Prob probs[2] = {make_prob(gc), make_prob(uc)};
+    Q4Plan pu, pd;
+    if (!plan_q4mv(&pu, probs, 2, static_cast<int>(cols), 64, ABG_SB_F32, kProNone, x, xsum, nullptr, 0.f, tree, 0,
+                   sb_bulk(gc) && sb_bulk(uc), g_tuning))
+        return ABG_ESHAPE;
+    Q4Call dc{wd, sd, bd, rows, n, 0, rows, y, kProSwq, sp, nullptr, nullptr, 0.f};
+    if (pu.shape != 0 && pu.rows_per_warp == 4) {
+        // the gate/up launch writes the SwiGLU itself (a tile holds the same
+        // rows of both products) and the down product reads it with the
+        // group-sum prologue
+        Q4Args &pa = pu.args;
+        pa.paired = 1;
+        pa.epi = sp + 2 * n;
+        const int64_t half_rows = pa.tile_rows / 2;
+        pa.total_tiles = (n + half_rows - 1) / half_rows;
+        pu.grid.x = static_cast<unsigned>(std::min<int64_t>(pu.grid.x, pa.total_tiles));
+        dc.prologue = kProGsum;
+        dc.x = sp + 2 * n;
+    }  // else the down product computes the SwiGLU of [gate | up] in its prologue
+    Q4Prob pdown = make_prob(dc);
+    if (!plan_q4mv(&pd, &pdown, 1, static_cast<int>(n), 64, ABG_SB_F32, dc.prologue, dc.x, nullptr, nullptr, 0.f, tree,
+                   0, sb_bulk(dc), g_tuning))
+        return ABG_ESHAPE;
+    cudaError_t e = prepare_q4mv(pu);
+    if (e == cudaSuccess) e = prepare_q4mv(pd);
+    if (e != cudaSuccess) return cuda_fail(e, "kernel attributes");
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if ((e = launch_q4mv(pu, s, false)) != cudaSuccess) return cuda_fail(e, "gate/up launch");
+    return cuda_fail(launch_q4mv(pd, s, false), "down launch");
+}
 
 }  // extern "C"

@@ -316,6 +316,41 @@ abg_status abg_selftest_wait_timeout(void *stream);
  * It never changes results. */
 abg_status abg_set_q4mv_tuning(int smem_kb, int consumer_warps, int blocks_per_sm, int stage_kb);
 
+/*
+ * swiglu_mlp_static: the MLP block y = down( silu(gate x) * (up x) ) with
+ * no device allocation and no buffer from the caller for the intermediate
+ * vectors.  The pages have no counterpart of this call: it exists for callers
+ * that cannot allocate device memory themselves, such as code whose device
+ * memory all belongs to another allocator (a framework's caching allocator,
+ * or a server that reserves its memory up front), or code on a latency path
+ * where cudaMalloc/cudaFree would synchronize the device.
+ *   wg, sg, bg  gate product: u32 [n][cols/8], f32 [n][cols/64] x2
+ *   wu, su, bu  up product:   the same shapes
+ *   wd, sd, bd  down product: u32 [rows][n/8], f32 [rows][n/64] x2
+ *   x     f32 [cols], xsum f32 [cols/64] (x's group sums)
+ *   y     f32 [rows]  y[i] = row i of the down product of o[j] =
+ *                     silu(gate_y[j]) * up_y[j], silu(g) = g / (1 + EXP(-g))
+ *   n     rows of gate and up, columns of down: a positive multiple of 64, at
+ *         most 16384 (else ABG_ESHAPE)
+ * Groups of 64 columns with f32 scale and bias; every result, tree order and
+ * error rule as the separate calls (abg_q4mv twice, abg_swq, abg_q4mv), whose
+ * results it equals bit for bit in ABG_TREE mode.
+ * The intermediate vectors (gate_y, up_y and o, 3n floats) live in one
+ * static device array of 3 * 16384 floats inside the library, which every
+ * device that loads the library holds until the process exits.  The first
+ * call on a device looks up that array's device address (with the device
+ * current), so make the first call on each device before any stream capture
+ * begins.  Every call uses the same array: calls that can overlap on the GPU
+ * (on different streams, or different host threads) race on it and must be
+ * ordered by the caller.  Nothing in the array needs clearing: each call
+ * writes every element it reads.  Asynchronous like the other calls.
+ */
+abg_status abg_swiglu_mlp_static(const uint32_t *wg, const float *sg, const float *bg,
+                                 const uint32_t *wu, const float *su, const float *bu,
+                                 const uint32_t *wd, const float *sd, const float *bd,
+                                 const float *x, const float *xsum, float *y,
+                                 int64_t n, int64_t cols, int64_t rows, int mode, void *stream);
+
 const char *abg_status_str(int status);
 /* Text of the last CUDA error seen by any call on this thread ("" if none). */
 const char *abg_last_cuda_error(void);

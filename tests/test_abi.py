@@ -201,3 +201,21 @@ def test_unknown_graph_handles_are_refused(lib):
     n = ctypes.c_int64()
     assert lib.abg_stage_graph_launches(fake, ctypes.byref(n)) == EINVAL
     assert lib.abg_stage_graph_swiglu_pairs(fake, ctypes.byref(n)) == EINVAL
+
+
+def test_static_mlp_rejects_before_device_work(lib):
+    """abg_swiglu_mlp_static checks sizes against its static scratch (n <= 16384)
+    and its arguments before touching the device."""
+    f = lib.abg_swiglu_mlp_static
+    p = [0x7F0000100000 + 4096 * i for i in range(12)]
+    assert f(*p, 16384 + 64, 2048, 10, 0, None) == ESHAPE   # more than the static scratch holds
+    assert f(*p, 100, 2048, 10, 0, None) == ESHAPE          # n not a multiple of 64
+    assert f(*p, 1024, 2000, 10, 0, None) == ESHAPE         # cols not a multiple of 64
+    assert f(*p, 1024, 2048, 10, 7, None) == EINVAL         # bad mode
+    q = list(p)
+    q[11] = p[9]                                           # y == x
+    assert f(*q, 1024, 2048, 10, 0, None) == EALIAS
+    q = list(p)
+    q[0] += 4                                              # gate words not 16-byte aligned
+    assert f(*q, 1024, 2048, 10, 0, None) == EALIGN
+    assert f(*([None] + p[1:]), 1024, 2048, 10, 0, None) == EINVAL
