@@ -360,6 +360,17 @@ abg_status mlp_scratch(float **out) {
     return ABG_OK;
 }
 
+// ABG_PDL=0: plain stream-ordered launches (no early start of a dependent
+// launch) in stage graphs and between the launches of one batched call;
+// results are the same.
+bool pdl_enabled() {
+    static const bool on = [] {
+        const char *v = std::getenv("ABG_PDL");
+        return !(v && std::strcmp(v, "0") == 0);
+    }();
+    return on;
+}
+
 }  // namespace
 
 extern "C" {
@@ -402,9 +413,14 @@ abg_status abg_q4mm(const uint32_t *w, const float *scale, const float *bias, co
     for (const Range &r : in)
         if (overlap(out, r)) return ABG_EALIAS;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // The first launch waits for the work queued before the call; the later
+    // ones share its inputs and write other outputs, so they may start early
+    // (programmatic launch) without waiting for it.
+    const bool pdl = pdl_enabled();
     for (int64_t t0 = 0; t0 < T;) {
         // token pairs share a launch; an odd last token runs alone
         const int width = (T - t0 >= 2) ? 2 : 1;
+        const bool sibling = pdl && t0 > 0;
         const int ntok = width;
         Q4Call ct = c;
         ct.x = x + t0 * cols;
@@ -414,8 +430,9 @@ abg_status abg_q4mm(const uint32_t *w, const float *scale, const float *bias, co
         if (width == 1) {
             st = plan_calls(&plan, {ct}, mode, rows_per_warp);
             if (st != ABG_OK) return st;
+            if (sibling) plan.args.wait_first = 0;
             cudaError_t e = prepare_q4mv(plan);
-            if (e == cudaSuccess) e = launch_q4mv(plan, s, false);
+            if (e == cudaSuccess) e = launch_q4mv(plan, s, sibling);
             if (e != cudaSuccess) return cuda_fail(e, "q4mm launch");
         } else {
             const float *xt[4], *xst[4];
@@ -427,7 +444,8 @@ abg_status abg_q4mm(const uint32_t *w, const float *scale, const float *bias, co
             if (!plan_q4mm(&plan, &p, 1, static_cast<int>(cols), width, ntok, xt, xst, kProNone, mode == ABG_TREE,
                            rows_per_warp == 0 ? 8 : rows_per_warp, sb_bulk(ct)))
                 return ABG_ESHAPE;
-            const cudaError_t e = launch_q4mm(plan, s, false);
+            if (sibling) plan.args.wait_first = 0;
+            const cudaError_t e = launch_q4mm(plan, s, sibling);
             if (e != cudaSuccess) return cuda_fail(e, "q4mm launch");
         }
         t0 += ntok;
@@ -576,12 +594,7 @@ abg_status abg_stage_graph_create(const abg_node *nodes, int64_t count, int mode
         where = "cudaStreamCreateWithFlags";
     if (e == cudaSuccess && (e = cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal)) != cudaSuccess)
         where = "cudaStreamBeginCapture";
-    // ABG_PDL=0 records plain stream-ordered launches (no early start of a
-    // dependent launch); results are the same.
-    static const bool pdl_on = [] {
-        const char *v = std::getenv("ABG_PDL");
-        return !(v && std::strcmp(v, "0") == 0);
-    }();
+    const bool pdl_on = pdl_enabled();
     // a product launch that follows a launch of its own stage does not depend
     // on it (siblings of one stage share their inputs)
     for (size_t i = 1; i < launches.size(); ++i)

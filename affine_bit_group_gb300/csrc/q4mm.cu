@@ -4,7 +4,7 @@
 // several pair launches: a 4-token lane mapping (8 columns per lane) was
 // measured slower per token than pairs, its butterflies and register pressure
 // outweighing the shared unpacking.
-#include "q4mm_kernel.cuh"
+#include "q4mm_fixed.cuh"
 
 #include <algorithm>
 
@@ -17,8 +17,16 @@ void *mm_ptr() {
     return reinterpret_cast<void *>(&q4mm_kernel<T, R, kTree, kSb>);
 }
 
-// Rows per item: T * R = 8 values per lane.
-void *select_mm(int T, bool tree, bool sb) {
+template <bool kTree, int kC>
+void *mmf_ptr() {
+    return reinterpret_cast<void *>(&q4mm_fixed_kernel<kTree, kC>);
+}
+
+// Rows per item: T * R = 8 values per lane.  shape != 0: the fixed-shape pair
+// kernel for rows of `shape` columns.
+void *select_mm(int T, bool tree, bool sb, int shape = 0) {
+    if (T == 2 && sb && shape == 2048) return tree ? mmf_ptr<true, 2048>() : mmf_ptr<false, 2048>();
+    if (T == 2 && sb && shape == 4096) return tree ? mmf_ptr<true, 4096>() : mmf_ptr<false, 4096>();
     if (T == 2) {
         if (tree) return sb ? mm_ptr<2, 4, true, true>() : mm_ptr<2, 4, true, false>();
         return sb ? mm_ptr<2, 4, false, true>() : mm_ptr<2, 4, false, false>();
@@ -35,8 +43,7 @@ inline uint32_t align_up(uint32_t v, uint32_t a) { return (v + a - 1) / a * a; }
 bool plan_q4mm(Q4Plan *plan, const Q4Prob *probs, int nprob, int cols, int T, int ntok, const float *const *xt,
                const float *const *xst, int prologue, bool tree, int rows_per_warp, bool sb_smem) {
     (void)rows_per_warp;  // rows per item follow from T (T * R = 8 values per lane)
-    void *fn = select_mm(T, tree, sb_smem);
-    if (!fn || ntok < 1 || ntok > T) return false;
+    if (!select_mm(T, tree, sb_smem) || ntok < 1 || ntok > T) return false;
     Q4Args &a = plan->args;
     a = Q4Args{};
     const int R = mm_rows(T);
@@ -102,6 +109,12 @@ bool plan_q4mm(Q4Plan *plan, const Q4Prob *probs, int nprob, int cols, int T, in
     a.off_bar = align_up(a.off_part + part_bytes(TR, S), 16);
     a.parts = S + 2;
     a.smem_bytes = a.off_bar + 8u * (2 * S + a.parts);
+    // the fixed-shape kernel when the plan has its shape (its stage layout and
+    // tile rows are compile-time constants equal to these)
+    const bool fixed_shape = T == 2 && sb_smem && (C == 2048 || C == 4096) && nw == 8 && TR == mmf_tr(C) &&
+                             a.parts <= kMaxHdr;
+    plan->shape = fixed_shape ? C : 0;
+    void *fn = select_mm(T, tree, sb_smem, plan->shape);
     int fit = 1;
     if (raise_smem_limit(fn) == cudaSuccess) {
         int nb = 0;
@@ -125,7 +138,7 @@ bool plan_q4mm(Q4Plan *plan, const Q4Prob *probs, int nprob, int cols, int T, in
 
 cudaError_t launch_q4mm(const Q4Plan &plan, cudaStream_t stream, bool pdl) {
     if (plan.args.total_tiles == 0) return cudaSuccess;
-    void *fn = select_mm(plan.mm, plan.tree, plan.sb_smem);
+    void *fn = select_mm(plan.mm, plan.tree, plan.sb_smem, plan.shape);
     if (!fn) return cudaErrorInvalidValue;
     cudaError_t e = raise_smem_limit(fn);
     if (e != cudaSuccess) return e;

@@ -143,6 +143,10 @@ abg_status abg_q4mv_ex(const uint32_t *w, const void *scale, const void *bias, i
  *   y     f32 [T][n]
  *   T     1..8.  Each pair of tokens is one launch that reads the weights
  *         once for both; an odd last token runs as a single-token product.
+ *         The first launch waits for the stream's earlier work; the later
+ *         ones may start while it runs (programmatic dependent launch, off
+ *         with ABG_PDL=0), since they read the same inputs and write other
+ *         rows of y.
  * Groups of 64 columns with f32 scale and bias; other arguments and errors as
  * abg_q4mv.
  */

@@ -56,13 +56,14 @@ def test_batched_tree_bit_exact(T, rows, cols):
 
 
 @pytest.mark.parametrize("T", [2, 4])
-def test_batched_fast_within_bound(T):
-    m, _ = synth.random_case(3100, 300, 3072)
-    X = tokens(2, T, 3072)
+@pytest.mark.parametrize("cols", [2048, 3072, 4096])
+def test_batched_fast_within_bound(T, cols):
+    m, _ = synth.random_case(3100 + cols, 300, cols)
+    X = tokens(2, T, cols)
     tree = expect(m, X)
     got = run(m, X, mode=abg.FAST)
     for t in range(T):
-        mag = oracle.q4mv_absmag(*m.arrays(), X[t], oracle.gsum(X[t]), 3072)
+        mag = oracle.q4mv_absmag(*m.arrays(), X[t], oracle.gsum(X[t]), cols)
         assert_fast_close(got[t], tree[t], mag, what=f"fast T={T} token {t}")
 
 

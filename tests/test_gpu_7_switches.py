@@ -3,8 +3,9 @@ read once per process, at the first graph creation or launch).
 
 ABG_TRACE=1: every graph launch synchronizes and prints one stderr line with
 the launch count, the GPU milliseconds and the wall milliseconds.
-ABG_PDL=0: launches are recorded without programmatic dependent launch; the
-results are the same bits as with it.
+ABG_PDL=0: launches are recorded without programmatic dependent launch, and a
+batched call's launches after its first wait for the one before; the results
+are the same bits as with it.
 """
 from __future__ import annotations
 
@@ -96,3 +97,38 @@ def test_trace_off_prints_nothing():
     vals, err = child({}, True, reps=1)
     assert vals["EQUAL"].strip() == "1"
     assert "abg: stage graph" not in err
+
+
+CHILD_MM = """
+import sys
+sys.path.insert(0, {root!r})
+import numpy as np, torch
+import affine_bit_group_gb300 as abg
+import oracle
+from affine_bit_group_gb300 import synth
+m, _ = synth.mid()
+rng = np.random.default_rng(17)
+X = np.stack([synth.activations(rng, m.cols) for _ in range(5)])
+XS = np.stack([oracle.gsum(x) for x in X])
+w = torch.from_numpy(m.w.view(np.int32)).cuda()
+Y = torch.empty(5 * m.rows, device="cuda")
+for _ in range(2):
+    abg.q4mm(w, torch.from_numpy(m.scale).cuda(), torch.from_numpy(m.bias).cuda(), torch.from_numpy(X).cuda(),
+             torch.from_numpy(XS).cuda(), Y, cols=m.cols)
+torch.cuda.synchronize()
+got = Y.view(5, m.rows).cpu().numpy()
+exp = oracle.q4mm(*m.arrays(), X, XS, m.cols)
+print("EQUAL", int(np.array_equal(got.view(np.uint32), exp.view(np.uint32))))
+"""
+
+
+@pytest.mark.parametrize("pdl", ["0", "1"])
+def test_batched_pdl_switch_gives_the_same_bits(pdl):
+    """Five tokens (two pair launches and a single-token launch, the later ones
+    started early unless ABG_PDL=0): every token bit-exact either way."""
+    env = dict(os.environ)
+    env["ABG_PDL"] = pdl
+    r = subprocess.run([sys.executable, "-c", CHILD_MM.format(root=ROOT)], env=env, capture_output=True, text=True,
+                       timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    assert "EQUAL 1" in r.stdout
