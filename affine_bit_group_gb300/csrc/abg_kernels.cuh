@@ -17,7 +17,8 @@ struct Q4Prob {
     const void *bias;
     float *y;
     int64_t n;      // rows to compute
-    int64_t tiles;  // ceil(n / tile_rows)
+    int64_t tiles;  // ceil(n / tr)
+    int64_t tr;     // rows per tile of this problem: tile_rows, or a quarter of it (see plan_q4mv)
 };
 
 // Everything the product kernel needs, passed by value (__grid_constant__).

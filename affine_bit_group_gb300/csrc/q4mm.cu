@@ -83,6 +83,7 @@ bool plan_q4mm(Q4Plan *plan, const Q4Prob *probs, int nprob, int cols, int T, in
     a.total_tiles = 0;
     for (int i = 0; i < nprob; ++i) {
         a.prob[i] = probs[i];
+        a.prob[i].tr = TR;
         a.prob[i].tiles = (probs[i].n + TR - 1) / TR;
         a.total_tiles += a.prob[i].tiles;
     }

@@ -85,6 +85,31 @@ int sm_count() {
 namespace {
 constexpr int kFewTilesPerSm = 4;
 
+// A launch of one block per SM whose tiles exceed the SMs by a little (a
+// decode token's q/k/v products: 160 tiles on 152 SMs) would run a second
+// round of whole tiles on a few SMs.  Its last problems are cut into quarter
+// tiles instead (TR/4 rows, a whole number of items), as long as the whole
+// tiles left number at most the SMs and all tiles at most twice that: tile t
+// runs on block t mod SMs, so no block then takes more than one whole and one
+// quarter tile.  Results are unchanged (a tile's rows are summed as before).
+void quarter_tail(Q4Args &a, int TR, int R, int64_t sms) {
+    const int tq = TR / 4;
+    if (tq < R || tq % R != 0 || a.paired || a.total_tiles <= sms) return;
+    int64_t whole = a.total_tiles, quarter = 0;
+    int first = a.nprob;
+    while (first > 0 && whole > sms) {
+        --first;
+        whole -= a.prob[first].tiles;
+        quarter += (a.prob[first].n + tq - 1) / tq;
+    }
+    if (whole > sms || whole + quarter > 2 * sms) return;
+    for (int i = first; i < a.nprob; ++i) {
+        a.prob[i].tr = tq;
+        a.prob[i].tiles = (a.prob[i].n + tq - 1) / tq;
+    }
+    a.total_tiles = whole + quarter;
+}
+
 bool plan_once(Q4Plan *plan, const Q4Prob *probs, int nprob, int cols, int group, int sb_type, int prologue,
                const float *x, const float *xsum, const float *wt, float eps, bool tree, int rows_per_warp,
                bool sb_smem, const Q4Tuning &tune, bool allow_few, int force_layout = -1) {
@@ -162,6 +187,7 @@ bool plan_once(Q4Plan *plan, const Q4Prob *probs, int nprob, int cols, int group
     a.total_tiles = 0;
     for (int i = 0; i < nprob; ++i) {
         a.prob[i] = probs[i];
+        a.prob[i].tr = TR;
         a.prob[i].tiles = (probs[i].n + TR - 1) / TR;
         a.total_tiles += a.prob[i].tiles;
     }
@@ -221,6 +247,7 @@ bool plan_once(Q4Plan *plan, const Q4Prob *probs, int nprob, int cols, int group
     cudaGetLastError();
     int bps = std::min(fit, wide ? 1 : (tune.blocks_per_sm > 0 ? tune.blocks_per_sm : (few ? 1 : 2)));
     bps = std::max(bps, 1);
+    if (bps == 1) quarter_tail(a, TR, R, sm_count());
     const int64_t cap = static_cast<int64_t>(sm_count()) * bps;
     plan->grid = dim3(static_cast<unsigned>(std::max<int64_t>(1, std::min(a.total_tiles, cap))));
     plan->block = dim3(32u * (1 + nw));

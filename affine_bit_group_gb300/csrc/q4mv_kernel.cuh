@@ -101,6 +101,11 @@ __device__ __forceinline__ float nib_scale(int j) {
     return __uint_as_float(static_cast<uint32_t>(150 - 4 * nib_k(j)) << 23);
 }
 
+// 2^(4k-23) for nibble j, the inverse of nib_scale (exact).
+__device__ __forceinline__ float nib_unscale(int j) {
+    return __uint_as_float(static_cast<uint32_t>(104 + 4 * nib_k(j)) << 23);
+}
+
 // A stored 16-bit scale or bias widened to f32 (exact for both types).
 __device__ __forceinline__ float widen16(unsigned short h, bool f16) {
     return f16 ? __half2float(__ushort_as_half(h)) : __uint_as_float(static_cast<uint32_t>(h) << 16);
@@ -414,21 +419,66 @@ struct CoopIn {
     float4 w[kNU];  // RMS-norm weights of the thread's units, read before the dependency wait
 };
 
-template <bool kTree>
-__device__ __forceinline__ float sum4_group(float4 v) {
-    float s = kTree ? __fadd_rn(__fadd_rn(v.x, v.y), __fadd_rn(v.z, v.w)) : (v.x + v.y) + (v.z + v.w);
+// The RMS-norm factor of a fixed-shape prologue, computed by every warp from
+// the group sums of squares in red[0 .. kC/64) (one barrier; no broadcast):
+// each lane takes the pairwise tree over its V consecutive group sums (the
+// groups padded with -0 to 32 V), then a 5-step butterfly finishes the tree.
+// The mean divides by kC; for a power of two that is the exact product with
+// 1/kC, the same correctly rounded value.  The factor is the correctly
+// rounded reciprocal of the correctly rounded square root.
+template <bool kTree, int kC>
+__device__ __forceinline__ float rms_factor_all(const float *red, float eps, int nct) {
+    constexpr int G = kC / 64;
+    constexpr int V = G <= 32 ? 1 : (G <= 64 ? 2 : (G <= 128 ? 4 : 8));
+    static_assert(G <= 32 * V, "group sums fit the lanes");
+    named_bar(1, nct);
+    const int lane = threadIdx.x & 31;
+    float t[V];
+#pragma unroll
+    for (int j = 0; j < V; ++j) t[j] = lane * V + j < G ? red[lane * V + j] : kNegZero;
+#pragma unroll
+    for (int h = V / 2; h >= 1; h >>= 1)
+#pragma unroll
+        for (int j = 0; j < h; ++j) t[j] = kTree ? __fadd_rn(t[2 * j], t[2 * j + 1]) : t[2 * j] + t[2 * j + 1];
+    float ss = t[0];
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const float o = __shfl_xor_sync(0xffffffffu, ss, d);
+        ss = kTree ? __fadd_rn(ss, o) : ss + o;
+    }
+    if constexpr (kTree) {
+        constexpr bool kPow2 = (kC & (kC - 1)) == 0;
+        const float mean = kPow2 ? __fmul_rn(ss, 1.0f / static_cast<float>(kC)) : __fdiv_rn(ss, static_cast<float>(kC));
+        return __frcp_rn(__fsqrt_rn(__fadd_rn(mean, eps)));
+    } else {
+        return rsqrtf(ss / static_cast<float>(kC) + eps);
+    }
+}
+
+// Group sums of NU units at once: the thread's pairwise sum of a unit's 4
+// values, then butterfly steps at distances 1, 2, 4 and 8 over the 16 threads
+// of the unit's group (the pairwise tree over its 64 values); the steps of
+// the NU units are interleaved so that their shuffles overlap.
+template <bool kTree, int NU>
+__device__ __forceinline__ void sum4_groups(const float4 (&v)[NU], float (&s)[NU]) {
+#pragma unroll
+    for (int k = 0; k < NU; ++k)
+        s[k] = kTree ? __fadd_rn(__fadd_rn(v[k].x, v[k].y), __fadd_rn(v[k].z, v[k].w))
+                     : (v[k].x + v[k].y) + (v[k].z + v[k].w);
 #pragma unroll
     for (int d = 1; d < 16; d <<= 1) {
-        const float o = __shfl_xor_sync(0xffffffffu, s, d);
-        s = kTree ? __fadd_rn(s, o) : s + o;
+        float o[NU];
+#pragma unroll
+        for (int k = 0; k < NU; ++k) o[k] = __shfl_xor_sync(0xffffffffu, s[k], d);
+#pragma unroll
+        for (int k = 0; k < NU; ++k) s[k] = kTree ? __fadd_rn(s[k], o[k]) : s[k] + o[k];
     }
-    return s;
 }
 
 template <bool kTree, int kC, int kNct>
 __device__ __forceinline__ void coop_prologue(const Q4Args &a, const CoopIn<(kC / 4 + kNct - 1) / kNct> &in,
                                               float *act, float *gs, unsigned *gneg, unsigned *spec, int cw,
-                                              float *red, float *rbox) {
+                                              float *red) {
     constexpr int NU = (kC / 4 + kNct - 1) / kNct;
     static_assert((kC / 4) % kNct == 0, "every thread has NU whole units");
     const int t = threadIdx.x - 32, lane = threadIdx.x & 31;
@@ -447,15 +497,19 @@ __device__ __forceinline__ void coop_prologue(const Q4Args &a, const CoopIn<(kC 
         for (int k = 0; k < NU; ++k) v[k] = x4[t + k * kNct];
     }
     if (a.prologue == kProRmsq) {
+        float4 sq[NU];
+        float ss[NU];
+#pragma unroll
+        for (int k = 0; k < NU; ++k)
+            sq[k] = make_float4(__fmul_rn(v[k].x, v[k].x), __fmul_rn(v[k].y, v[k].y), __fmul_rn(v[k].z, v[k].z),
+                                __fmul_rn(v[k].w, v[k].w));
+        sum4_groups<kTree, NU>(sq, ss);
 #pragma unroll
         for (int k = 0; k < NU; ++k) {
-            const float4 q = v[k];
-            const float s = sum4_group<kTree>(make_float4(__fmul_rn(q.x, q.x), __fmul_rn(q.y, q.y),
-                                                          __fmul_rn(q.z, q.z), __fmul_rn(q.w, q.w)));
             const int u = t + k * kNct;
-            if ((u & 15) == 0) red[u >> 4] = s;
+            if ((u & 15) == 0) red[u >> 4] = ss[k];
         }
-        const float r = rms_from_blocks<kTree>(red, kC, a.eps, cw, kNct, rbox);
+        const float r = rms_factor_all<kTree, kC>(red, a.eps, kNct);
 #pragma unroll
         for (int k = 0; k < NU; ++k) {
             const float4 q = v[k], w = in.w[k];
@@ -463,27 +517,52 @@ __device__ __forceinline__ void coop_prologue(const Q4Args &a, const CoopIn<(kC 
                                __fmul_rn(__fmul_rn(q.z, r), w.z), __fmul_rn(__fmul_rn(q.w, r), w.w));
         }
     }
+    if (a.prologue != kProNone) {
+        float gsum[NU];
+        sum4_groups<kTree, NU>(v, gsum);
+#pragma unroll
+        for (int k = 0; k < NU; ++k) {
+            const int u = t + k * kNct;
+            if ((u & 15) == 0) gs[u >> 4] = gsum[k];
+        }
+    }
+    unsigned bspk[NU], bnegk[NU];
+#pragma unroll
+    for (int k = 0; k < NU; ++k) {
+        const float4 q = v[k];
+        const bool sp = !x_ordinary(q.x) || !x_ordinary(q.y) || !x_ordinary(q.z) || !x_ordinary(q.w);
+        const bool neg = q.x < 0.f && q.y < 0.f && q.z < 0.f && q.w < 0.f;
+        bspk[k] = __ballot_sync(0xffffffffu, sp);
+        bnegk[k] = __ballot_sync(0xffffffffu, neg);
+    }
 #pragma unroll
     for (int k = 0; k < NU; ++k) {
         const int u = t + k * kNct, c = 4 * u;
         const float4 q = v[k];
-        if (a.prologue != kProNone) {
-            const float s = sum4_group<kTree>(q);
-            if ((u & 15) == 0) gs[u >> 4] = s;
-        }
-        const bool sp = !x_ordinary(q.x) || !x_ordinary(q.y) || !x_ordinary(q.z) || !x_ordinary(q.w);
-        const bool neg = q.x < 0.f && q.y < 0.f && q.z < 0.f && q.w < 0.f;
-        const unsigned bsp = __ballot_sync(0xffffffffu, sp), bneg = __ballot_sync(0xffffffffu, neg);
+        const unsigned bsp = bspk[k], bneg = bnegk[k];
         if (lane == 0) spec[u >> 5] = bsp != 0u;
         if ((u & 15) == 0) gneg[u >> 4] = ((bneg >> (lane & 16)) & 0xffffu) == 0xffffu;
         const int ch = c >> 10, l = (c & 1023) >> 5, i = (c & 31) >> 2;
-        reinterpret_cast<float4 *>(act)[(ch * 8 + i) * 32 + l] = q;
+        // a 128-column block of ordinary values (this warp's 32 units) is
+        // staged times -2^(23-4k) of its columns' nibbles, the exact path's
+        // operands; a block with a special value is staged as it is
+        float4 st = q;
+        if (bsp == 0u) {
+            const int j0 = c & 4;
+            st = make_float4(__fmul_rn(q.x, -nib_scale(j0)), __fmul_rn(q.y, -nib_scale(j0 + 1)),
+                             __fmul_rn(q.z, -nib_scale(j0 + 2)), __fmul_rn(q.w, -nib_scale(j0 + 3)));
+        }
+        reinterpret_cast<float4 *>(act)[(ch * 8 + i) * 32 + l] = st;
     }
     named_bar(1, kNct);
 }
 
 // A warp's slice of the staged activation (chunk ch; fixed shapes: every
-// lane's columns lie inside the row).
+// lane's columns lie inside the row).  Blocks of ordinary values were staged
+// as the exact path's operands; on the plain path (a special value somewhere
+// in the chunk) a lane whose own 128-column block was scaled takes the
+// scaling back, which is exact (ordinary values were scaled up by at least
+// 2^7 without overflow).
 template <bool kTree, int kLg>
 __device__ __forceinline__ void slice_from_stage(const Q4Args &a, int ch, int lane, const float *act,
                                                  const float *gs, const unsigned *gneg, const unsigned *spec,
@@ -495,9 +574,9 @@ __device__ __forceinline__ void slice_from_stage(const Q4Args &a, int ch, int la
         const float4 q = s4[(ch * 8 + i) * 32 + lane];
         v[4 * i] = q.x, v[4 * i + 1] = q.y, v[4 * i + 2] = q.z, v[4 * i + 3] = q.w;
     }
-    bool sp = false;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) sp |= spec[ch * 8 + i] != 0u;
+    const uint4 f0 = reinterpret_cast<const uint4 *>(spec + ch * 8)[0];
+    const uint4 f1 = reinterpret_cast<const uint4 *>(spec + ch * 8)[1];
+    const bool sp = (f0.x | f0.y | f0.z | f0.w | f1.x | f1.y | f1.z | f1.w) != 0u;
     const int g = ch * (32 >> kLg) + (lane >> kLg);
     sl.exact = !sp;
     sl.xs = a.prologue == kProNone ? a.xsum[g] : gs[g];
@@ -505,15 +584,12 @@ __device__ __forceinline__ void slice_from_stage(const Q4Args &a, int ch, int la
     sl.neg = kTree && gneg[g] != 0u;
     sl.anyneg = __any_sync(0xffffffffu, sl.neg);
     sl.act = sl.actp = sl.full = true;
+    if (sp && spec[ch * 8 + (lane >> 2)] == 0u) {
 #pragma unroll
-    for (int m = 0; m < 16; ++m) {
-        if (sl.exact) {
-            const float s = -nib_scale(m & 7);
-            sl.X[m] = f2(__fmul_rn(v[m], s), __fmul_rn(v[m + 16], s));
-        } else {
-            sl.X[m] = f2(v[m], v[m + 16]);
-        }
+        for (int m = 0; m < 32; ++m) v[m] = __fmul_rn(v[m], -nib_unscale(m & 7));
     }
+#pragma unroll
+    for (int m = 0; m < 16; ++m) sl.X[m] = f2(v[m], v[m + 16]);
 }
 
 // Locates tiles of a grouped launch.  A block visits its tiles in increasing
@@ -829,8 +905,9 @@ __global__ void __launch_bounds__(layout_threads(kLayout), layout_blocks(kLayout
             const int pidx = a.paired ? 0 : cur.find(a, t, tile);
             const Q4Prob &P = a.prob[pidx];
             // a SwiGLU pair's tile: TR/2 rows of the gate product into the
-            // stage's first half, the same rows of the up product after them
-            const int trp = a.paired ? TR / 2 : TR;
+            // stage's first half, the same rows of the up product after them;
+            // otherwise the problem's tile rows (at most TR)
+            const int trp = a.paired ? TR / 2 : static_cast<int>(P.tr);
             const int64_t r0 = static_cast<int64_t>(tile) * trp;
             const int rows = static_cast<int>(min(static_cast<int64_t>(trp), P.n - r0));
             unsigned char *st = smem + a.off_stage + static_cast<size_t>(s) * stage_bytes;
@@ -896,53 +973,37 @@ __global__ void __launch_bounds__(layout_threads(kLayout), layout_blocks(kLayout
 #pragma unroll
         for (int k = 0; k < kNU; ++k) cin.w[k] = __ldg(w4 + ct + k * kNct);
     }
-    if (wait_first) {
-        grid_dep_wait();
-        grid_dep_launch();
-    }
     Slice sl;
     int cur_ch = -1;
     float rms_r = 0.f;
-    if constexpr (kFix) {
-        // the activation once per block, staged in shared memory
-        float *act = reinterpret_cast<float *>(smem + a.off_act);
-        float *gs = act + kC;
-        unsigned *gneg = reinterpret_cast<unsigned *>(gs + kC / 64);
-        unsigned *spec = gneg + kC / 64;
-        coop_prologue<kTree, kC, kNct>(a, cin, act, gs, gneg, spec, cw, s_red, &s_rbox);
-        slice_from_stage<kTree, kLg>(a, ch0, lane, act, gs, gneg, spec, sl);
-        cur_ch = ch0;
-    } else if (a.prologue == kProRmsq) {
-        // one pass over x, after which the warp's slice is ready for every
-        // tile; only in the main instantiations (tree mode, 8 rows per item,
-        // block layout 0, staged scale/bias): in the others the product
-        // loop would lose registers to it, so they keep the two passes
-        constexpr bool kOnePass = kTree && R == 8 && kLayout == 0 && kSbSmem;
-        if (kOnePass && fixed_ch) {
-            rms_slice<kTree, kLg>(a, ch0, !idle, rb0 == 0, cw, nw, lane, s_red, &s_rbox, sl);
-            if (!idle) cur_ch = ch0;
-        } else {
-            rms_r = block_rms_factor<kTree>(a.x, a.cols, a.eps, cw, nw, lane, s_red, &s_rbox);
+    if constexpr (!kFix) {
+        if (wait_first) {
+            grid_dep_wait();
+            grid_dep_launch();
+        }
+        if (a.prologue == kProRmsq) {
+            // one pass over x, after which the warp's slice is ready for every
+            // tile; only in the main instantiations (tree mode, 8 rows per item,
+            // block layout 0, staged scale/bias): in the others the product
+            // loop would lose registers to it, so they keep the two passes
+            constexpr bool kOnePass = kTree && R == 8 && kLayout == 0 && kSbSmem;
+            if (kOnePass && fixed_ch) {
+                rms_slice<kTree, kLg>(a, ch0, !idle, rb0 == 0, cw, nw, lane, s_red, &s_rbox, sl);
+                if (!idle) cur_ch = ch0;
+            } else {
+                rms_r = block_rms_factor<kTree>(a.x, a.cols, a.eps, cw, nw, lane, s_red, &s_rbox);
+            }
         }
     }
-    const bool f16 = a.sb_f16 != 0;
-    // stored scale or bias i (elements) from the stage or from global memory
-    auto sb_at = [&](const void *base, int64_t i) -> float {
-        if constexpr (kHalf) {
-            const unsigned short h = kSbSmem ? static_cast<const unsigned short *>(base)[i]
-                                             : __ldg(static_cast<const unsigned short *>(base) + i);
-            return widen16(h, f16);
-        } else {
-            return kSbSmem ? static_cast<const float *>(base)[i] : __ldg(static_cast<const float *>(base) + i);
-        }
-    };
-
     // Lane constants of the current chunk position (set with its slice):
     // byte offsets in a row block of the item rows' 16-byte column quads,
     // v[i] <- row (i ^ pi), and the lane's and its partner's group.
     // Rows are loaded in batches of B = min(R, 4): batch b's row i is row
     // (4b + i) ^ pi = (i ^ pi) + 4b or - 4b, so one set of B offsets and the
     // batch step serve all batches.
+    // (Fixed shapes set them before the dependency wait and stage the
+    // activation after it; the other instantiations wait and compute their
+    // prologue before this point.)
     constexpr int B = R < 4 ? R : 4;
     const int pi = rev_lane_bits<kLogR>(lane);
     const uint32_t rowW = static_cast<uint32_t>(W) * 4u;
@@ -975,7 +1036,35 @@ __global__ void __launch_bounds__(layout_threads(kLayout), layout_blocks(kLayout
         for (int i = 0; i < NB; ++i) sbo[i] = (srow(i ^ pi) * G + gown) * kElem;
         sbd = (gpar - gown) * static_cast<int>(kElem);
     };
-    if (cur_ch >= 0) set_chunk(cur_ch);  // slice computed by the prologue
+    if constexpr (kFix) {
+        // a fixed shape's lane constants need no activation: set before the wait
+        sl.act = sl.actp = sl.full = true;
+        set_chunk(ch0);
+        if (wait_first) {
+            grid_dep_wait();
+            grid_dep_launch();
+        }
+        // the activation once per block, staged in shared memory
+        float *act = reinterpret_cast<float *>(smem + a.off_act);
+        float *gs = act + kC;
+        unsigned *gneg = reinterpret_cast<unsigned *>(gs + kC / 64);
+        unsigned *spec = gneg + kC / 64;
+        coop_prologue<kTree, kC, kNct>(a, cin, act, gs, gneg, spec, cw, s_red);
+        slice_from_stage<kTree, kLg>(a, ch0, lane, act, gs, gneg, spec, sl);
+        cur_ch = ch0;
+    }
+    if (!kFix && cur_ch >= 0) set_chunk(cur_ch);  // slice computed by the prologue
+    const bool f16 = a.sb_f16 != 0;
+    // stored scale or bias i (elements) from the stage or from global memory
+    auto sb_at = [&](const void *base, int64_t i) -> float {
+        if constexpr (kHalf) {
+            const unsigned short h = kSbSmem ? static_cast<const unsigned short *>(base)[i]
+                                             : __ldg(static_cast<const unsigned short *>(base) + i);
+            return widen16(h, f16);
+        } else {
+            return kSbSmem ? static_cast<const float *>(base)[i] : __ldg(static_cast<const float *>(base) + i);
+        }
+    };
 
     // One item: rows rb*R .. rb*R + R-1 of the tile in the stage at stg, for
     // the lane's 32 columns of chunk ch.  Rows past a ragged tile's end are
@@ -1090,8 +1179,9 @@ __global__ void __launch_bounds__(layout_threads(kLayout), layout_blocks(kLayout
     uint32_t fph = 0, dph = 0, pdph = 0;  // full and done phase parities (current and previous tile)
     if constexpr (kFix) {
         // One item per warp and tile: rows rb0*R .. rb0*R + R-1 of chunk ch0
-        // (the tile has R rows per warp of a chunk).  A ragged last tile's
-        // rows past its end are computed from stale words into values that
+        // (the tile has R rows per warp of a chunk).  In a tile of fewer rows
+        // the items wholly past its end are skipped; a partly filled item's
+        // rows past the end are computed from stale words into values that
         // are never written to y.  Warps of chunk 0 keep their chunk totals
         // in a register and, one tile later (once every warp's partials of
         // that tile are in), add the other chunks' partials by the tree and
@@ -1142,7 +1232,13 @@ __global__ void __launch_bounds__(layout_threads(kLayout), layout_blocks(kLayout
                 if (!wait_or_abort(&full[s], fph, &s_abort, kSiteFull)) break;
                 const unsigned char *stg = stage0 + static_cast<uint32_t>(s) * stage_bytes;
                 float *prt = part + p * TR * nch;
-                const float v = item(exact_c, std::false_type{}, stg, s_hdr[p], prt, ch0, rb0, lead);
+                // where the planner may cut quarter tiles (a quarter of the
+                // tile is a whole number of items), a tile of fewer rows skips
+                // the items wholly past its rows
+                constexpr bool kQuarter = kTRf / 4 >= R && (kTRf / 4) % R == 0;
+                const float v = (!kQuarter || rb0 * rbm < s_hdr[p].rows)
+                                    ? item(exact_c, std::false_type{}, stg, s_hdr[p], prt, ch0, rb0, lead)
+                                    : 0.f;
                 __syncwarp();
                 if (lane == 0) {
                     mbar_arrive(&empty[s]);

@@ -207,3 +207,30 @@ def test_swiglu_pair(cols, adjacent):
     assert_bits_equal(host(yd), oracle.q4mv(*md.arrays(), o, osum, n), "reader of the SwiGLU")
     assert abg.device_status(clear=True) == 0
     g.close()
+
+
+@pytest.mark.parametrize("cols,rows", [(2048, (4096, 512, 500)), (4096, (2048, 401, 299)), (3072, (1500, 300, 37))])
+def test_grouped_products_with_quarter_tiles(cols, rows):
+    """Three products of one stage sharing the RMS-norm prologue (one grouped
+    launch), sized so that the whole tiles exceed the SMs by a little: the last
+    products run as quarter tiles (ragged ends included).  Every output is the
+    oracle's, bit for bit."""
+    rng = np.random.default_rng([cols, *rows])
+    ms = [synth.q4_matrix(rng, n, cols) for n in rows]
+    h = synth.activations(rng, cols)
+    wt = synth.rms_weights(rng, cols)
+    hd, wtd = dev(h), dev(wt)
+    mats = [(dev_words(m.w), dev(m.scale), dev(m.bias)) for m in ms]
+    ys = [empty(n) for n in rows]
+    nodes = [abg.Node.q4mv(0, *mat, y, cols, x=hd, wt=wtd, eps=1e-6, prologue=abg.PRO_RMSQ)
+             for mat, y in zip(mats, ys)]
+    g = abg.StageGraph(nodes, keep=[hd, wtd, *ys, *[t for mat in mats for t in mat]])
+    assert g.launches == 1
+    for _ in range(2):
+        g.launch()
+    torch.cuda.synchronize()
+    xn, xs = oracle.rmsq(h, wt, 1e-6)
+    for m, y, n in zip(ms, ys, rows):
+        assert_bits_equal(host(y), oracle.q4mv(*m.arrays(), xn, xs, cols), f"{n}x{cols}")
+    assert abg.device_status(clear=True) == 0
+    g.close()
