@@ -418,8 +418,10 @@ abg_status abg_q4mm(const uint32_t *w, const float *scale, const float *bias, co
     // (programmatic launch) without waiting for it.
     const bool pdl = pdl_enabled();
     for (int64_t t0 = 0; t0 < T;) {
-        // token pairs share a launch; an odd last token runs alone
-        const int width = (T - t0 >= 2) ? 2 : 1;
+        // four tokens share a launch on rows of 2048 columns with staged
+        // scale and bias, otherwise pairs; an odd last token runs alone
+        int width = (T - t0 >= 2) ? 2 : 1;
+        if (T - t0 >= 4 && cols == 2048 && sb_bulk(c)) width = 4;
         const bool sibling = pdl && t0 > 0;
         const int ntok = width;
         Q4Call ct = c;

@@ -22,9 +22,15 @@ void *mmf_ptr() {
     return reinterpret_cast<void *>(&q4mm_fixed_kernel<kTree, kC>);
 }
 
-// Rows per item: T * R = 8 values per lane.  shape != 0: the fixed-shape pair
-// kernel for rows of `shape` columns.
+template <bool kTree>
+void *mm4_ptr() {
+    return reinterpret_cast<void *>(&q4mm4_fixed_kernel<kTree>);
+}
+
+// Rows per item: T * R = 8 values per lane.  shape != 0: the fixed-shape
+// kernel for rows of `shape` columns (T = 4: only the fixed shape exists).
 void *select_mm(int T, bool tree, bool sb, int shape = 0) {
+    if (T == 4) return (sb && shape == kMm4Cols) ? (tree ? mm4_ptr<true>() : mm4_ptr<false>()) : nullptr;
     if (T == 2 && sb && shape == 2048) return tree ? mmf_ptr<true, 2048>() : mmf_ptr<false, 2048>();
     if (T == 2 && sb && shape == 4096) return tree ? mmf_ptr<true, 4096>() : mmf_ptr<false, 4096>();
     if (T == 2) {
@@ -43,7 +49,8 @@ inline uint32_t align_up(uint32_t v, uint32_t a) { return (v + a - 1) / a * a; }
 bool plan_q4mm(Q4Plan *plan, const Q4Prob *probs, int nprob, int cols, int T, int ntok, const float *const *xt,
                const float *const *xst, int prologue, bool tree, int rows_per_warp, bool sb_smem) {
     (void)rows_per_warp;  // rows per item follow from T (T * R = 8 values per lane)
-    if (!select_mm(T, tree, sb_smem) || ntok < 1 || ntok > T) return false;
+    if ((T == 2 ? !select_mm(T, tree, sb_smem) : !(T == 4 && cols == kMm4Cols && sb_smem)) || ntok < 1 || ntok > T)
+        return false;
     Q4Args &a = plan->args;
     a = Q4Args{};
     const int R = mm_rows(T);
@@ -112,10 +119,12 @@ bool plan_q4mm(Q4Plan *plan, const Q4Prob *probs, int nprob, int cols, int T, in
     a.smem_bytes = a.off_bar + 8u * (2 * S + a.parts);
     // the fixed-shape kernel when the plan has its shape (its stage layout and
     // tile rows are compile-time constants equal to these)
-    const bool fixed_shape = T == 2 && sb_smem && (C == 2048 || C == 4096) && nw == 8 && TR == mmf_tr(C) &&
-                             a.parts <= kMaxHdr;
+    const bool fixed_shape =
+        a.parts <= kMaxHdr && sb_smem && nw == 8 &&
+        ((T == 2 && (C == 2048 || C == 4096) && TR == mmf_tr(C)) || (T == 4 && C == kMm4Cols && TR == kMm4Rows));
     plan->shape = fixed_shape ? C : 0;
     void *fn = select_mm(T, tree, sb_smem, plan->shape);
+    if (!fn) return false;
     int fit = 1;
     if (raise_smem_limit(fn) == cudaSuccess) {
         int nb = 0;

@@ -381,7 +381,7 @@ def bench_batched(abg, stream, args):
     s = torch.from_numpy(m.scale).cuda()
     b = torch.from_numpy(m.bias).cuda()
     pb = product_bytes(m.rows, m.cols)
-    out = {"workload": "q4mm 248320x2048 head, T tokens per call (pairs share a launch)"}
+    out = {"workload": "q4mm 248320x2048 head, T tokens per call (four or two tokens share a launch)"}
     for T in (1, 2, 4, 8):
         rng = np.random.default_rng([6, T])
         X_np = np.stack([synth.activations(rng, m.cols) for _ in range(T)])

@@ -141,8 +141,10 @@ abg_status abg_q4mv_ex(const uint32_t *w, const void *scale, const void *bias, i
  *   x     f32 [T][cols], 16-byte aligned (rows follow each other)
  *   xsum  f32 [T][cols/64]   xsum[t][g] = tree sum of token t's group g
  *   y     f32 [T][n]
- *   T     1..8.  Each pair of tokens is one launch that reads the weights
- *         once for both; an odd last token runs as a single-token product.
+ *   T     1..8.  Each group of four tokens (rows of 2048 columns with
+ *         bulk-copied scale and bias) or pair of tokens is one launch that
+ *         reads the weights once for all of them; an odd last token runs as
+ *         a single-token product.
  *         The first launch waits for the stream's earlier work; the later
  *         ones may start while it runs (programmatic dependent launch, off
  *         with ABG_PDL=0), since they read the same inputs and write other

@@ -2,8 +2,9 @@
 
 A batch of T tokens shares one pass over the weights; every token's output must
 be bit-for-bit its own single-token product (tree mode), or within the
-fast-mode bound.  Covers T = 1..8 (token pairs share a launch, an odd last
-token runs alone), shapes with ragged row tiles and
+fast-mode bound.  Covers T = 1..8 (four tokens share a launch on rows of 2048
+columns, otherwise pairs; an odd last token runs alone), shapes with ragged
+row tiles and
 column counts that are not a multiple of a warp's chunk, up to 16384 columns;
 tokens whose slices take different product paths; row ranges; unaligned
 scale/bias; the 4096x2048 product and the 248320x2048 head in full.
