@@ -16,9 +16,9 @@ struct Q4Prob {
     const void *scale;  // f32, or bf16 / f16 bit patterns
     const void *bias;
     float *y;
-    int64_t n;      // rows to compute
-    int64_t tiles;  // ceil(n / tr)
-    int64_t tr;     // rows per tile of this problem: tile_rows, or a quarter of it (see plan_q4mv)
+    int64_t n;  // rows to compute
+    int tiles;  // ceil(n / tr) (a launch's tiles fit in 32 bits)
+    int tr;     // rows per tile of this problem: tile_rows, or a quarter of it (see plan_q4mv)
 };
 
 // Everything the product kernel needs, passed by value (__grid_constant__).

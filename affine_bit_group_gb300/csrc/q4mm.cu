@@ -90,9 +90,11 @@ bool plan_q4mm(Q4Plan *plan, const Q4Prob *probs, int nprob, int cols, int T, in
     a.total_tiles = 0;
     for (int i = 0; i < nprob; ++i) {
         a.prob[i] = probs[i];
+        const int64_t tiles = (probs[i].n + TR - 1) / TR;
+        if (tiles > 0x7fffffff) return false;
         a.prob[i].tr = TR;
-        a.prob[i].tiles = (probs[i].n + TR - 1) / TR;
-        a.total_tiles += a.prob[i].tiles;
+        a.prob[i].tiles = static_cast<int>(tiles);
+        a.total_tiles += tiles;
     }
     if (a.total_tiles > 0x7fffffff) return false;
     for (int t = 0; t < T; ++t) {

@@ -105,7 +105,7 @@ void quarter_tail(Q4Args &a, int TR, int R, int64_t sms) {
     if (whole > sms || whole + quarter > 2 * sms) return;
     for (int i = first; i < a.nprob; ++i) {
         a.prob[i].tr = tq;
-        a.prob[i].tiles = (a.prob[i].n + tq - 1) / tq;
+        a.prob[i].tiles = static_cast<int>((a.prob[i].n + tq - 1) / tq);
     }
     a.total_tiles = whole + quarter;
 }
@@ -187,9 +187,11 @@ bool plan_once(Q4Plan *plan, const Q4Prob *probs, int nprob, int cols, int group
     a.total_tiles = 0;
     for (int i = 0; i < nprob; ++i) {
         a.prob[i] = probs[i];
+        const int64_t tiles = (probs[i].n + TR - 1) / TR;
+        if (tiles > 0x7fffffff) return false;
         a.prob[i].tr = TR;
-        a.prob[i].tiles = (probs[i].n + TR - 1) / TR;
-        a.total_tiles += a.prob[i].tiles;
+        a.prob[i].tiles = static_cast<int>(tiles);
+        a.total_tiles += tiles;
     }
     if (a.total_tiles > 0x7fffffff) return false;  // the kernel counts tiles in 32 bits
     // the budget loop may have halved the tile rows after the few-tiles
@@ -247,7 +249,9 @@ bool plan_once(Q4Plan *plan, const Q4Prob *probs, int nprob, int cols, int group
     cudaGetLastError();
     int bps = std::min(fit, wide ? 1 : (tune.blocks_per_sm > 0 ? tune.blocks_per_sm : (few ? 1 : 2)));
     bps = std::max(bps, 1);
-    if (bps == 1) quarter_tail(a, TR, R, sm_count());
+    // (fixed shapes skip a quarter tile's empty items only in the few-tiles
+    // layout; elsewhere the generic kernel does)
+    if (bps == 1 && (shape == 0 || layout == 1)) quarter_tail(a, TR, R, sm_count());
     const int64_t cap = static_cast<int64_t>(sm_count()) * bps;
     plan->grid = dim3(static_cast<unsigned>(std::max<int64_t>(1, std::min(a.total_tiles, cap))));
     plan->block = dim3(32u * (1 + nw));

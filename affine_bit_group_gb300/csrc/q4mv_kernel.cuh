@@ -475,10 +475,45 @@ __device__ __forceinline__ void sum4_groups(const float4 (&v)[NU], float (&s)[NU
     }
 }
 
-template <bool kTree, int kC, int kNct>
+template <bool kTree>
+__device__ __forceinline__ float sum4_group(float4 v) {
+    float s = kTree ? __fadd_rn(__fadd_rn(v.x, v.y), __fadd_rn(v.z, v.w)) : (v.x + v.y) + (v.z + v.w);
+#pragma unroll
+    for (int d = 1; d < 16; d <<= 1) {
+        const float o = __shfl_xor_sync(0xffffffffu, s, d);
+        s = kTree ? __fadd_rn(s, o) : s + o;
+    }
+    return s;
+}
+
+// Stages unit k of a thread (4 columns from c): the block flags, and the
+// values in the per-lane layout.  A 128-column block of ordinary values (a
+// warp's 32 units) is staged times -2^(23-4k) of its columns' nibbles, the
+// exact path's operands; a block with a special value is staged as it is.
+__device__ __forceinline__ void stage_unit(float4 q, int u, int lane, unsigned bsp, unsigned bneg, float *act,
+                                           unsigned *gneg, unsigned *spec) {
+    const int c = 4 * u;
+    if (lane == 0) spec[u >> 5] = bsp != 0u;
+    if ((u & 15) == 0) gneg[u >> 4] = ((bneg >> (lane & 16)) & 0xffffu) == 0xffffu;
+    const int ch = c >> 10, l = (c & 1023) >> 5, i = (c & 31) >> 2;
+    float4 st = q;
+    if (bsp == 0u) {
+        const int j0 = c & 4;
+        st = make_float4(__fmul_rn(q.x, -nib_scale(j0)), __fmul_rn(q.y, -nib_scale(j0 + 1)),
+                         __fmul_rn(q.z, -nib_scale(j0 + 2)), __fmul_rn(q.w, -nib_scale(j0 + 3)));
+    }
+    reinterpret_cast<float4 *>(act)[(ch * 8 + i) * 32 + l] = st;
+}
+
+// kLatency (the few-tiles layout, whose launches are latency-bound): every
+// warp computes the RMS-norm factor after one barrier, and the butterflies of
+// a thread's units are interleaved.  Otherwise one warp computes the factor
+// between two barriers and the units go one after the other (the throughput
+// layout's product loop measured faster with this prologue).
+template <bool kTree, int kC, int kNct, bool kLatency>
 __device__ __forceinline__ void coop_prologue(const Q4Args &a, const CoopIn<(kC / 4 + kNct - 1) / kNct> &in,
                                               float *act, float *gs, unsigned *gneg, unsigned *spec, int cw,
-                                              float *red) {
+                                              float *red, float *rbox) {
     constexpr int NU = (kC / 4 + kNct - 1) / kNct;
     static_assert((kC / 4) % kNct == 0, "every thread has NU whole units");
     const int t = threadIdx.x - 32, lane = threadIdx.x & 31;
@@ -498,18 +533,29 @@ __device__ __forceinline__ void coop_prologue(const Q4Args &a, const CoopIn<(kC 
     }
     if (a.prologue == kProRmsq) {
         float4 sq[NU];
-        float ss[NU];
 #pragma unroll
         for (int k = 0; k < NU; ++k)
             sq[k] = make_float4(__fmul_rn(v[k].x, v[k].x), __fmul_rn(v[k].y, v[k].y), __fmul_rn(v[k].z, v[k].z),
                                 __fmul_rn(v[k].w, v[k].w));
-        sum4_groups<kTree, NU>(sq, ss);
+        float r;
+        if constexpr (kLatency) {
+            float ss[NU];
+            sum4_groups<kTree, NU>(sq, ss);
 #pragma unroll
-        for (int k = 0; k < NU; ++k) {
-            const int u = t + k * kNct;
-            if ((u & 15) == 0) red[u >> 4] = ss[k];
+            for (int k = 0; k < NU; ++k) {
+                const int u = t + k * kNct;
+                if ((u & 15) == 0) red[u >> 4] = ss[k];
+            }
+            r = rms_factor_all<kTree, kC>(red, a.eps, kNct);
+        } else {
+#pragma unroll
+            for (int k = 0; k < NU; ++k) {
+                const float s = sum4_group<kTree>(sq[k]);
+                const int u = t + k * kNct;
+                if ((u & 15) == 0) red[u >> 4] = s;
+            }
+            r = rms_from_blocks<kTree>(red, kC, a.eps, cw, kNct, rbox);
         }
-        const float r = rms_factor_all<kTree, kC>(red, a.eps, kNct);
 #pragma unroll
         for (int k = 0; k < NU; ++k) {
             const float4 q = v[k], w = in.w[k];
@@ -517,42 +563,41 @@ __device__ __forceinline__ void coop_prologue(const Q4Args &a, const CoopIn<(kC 
                                __fmul_rn(__fmul_rn(q.z, r), w.z), __fmul_rn(__fmul_rn(q.w, r), w.w));
         }
     }
-    if (a.prologue != kProNone) {
-        float gsum[NU];
-        sum4_groups<kTree, NU>(v, gsum);
+    if constexpr (kLatency) {
+        if (a.prologue != kProNone) {
+            float gsum[NU];
+            sum4_groups<kTree, NU>(v, gsum);
+#pragma unroll
+            for (int k = 0; k < NU; ++k) {
+                const int u = t + k * kNct;
+                if ((u & 15) == 0) gs[u >> 4] = gsum[k];
+            }
+        }
+        unsigned bspk[NU], bnegk[NU];
+#pragma unroll
+        for (int k = 0; k < NU; ++k) {
+            const float4 q = v[k];
+            const bool sp = !x_ordinary(q.x) || !x_ordinary(q.y) || !x_ordinary(q.z) || !x_ordinary(q.w);
+            const bool neg = q.x < 0.f && q.y < 0.f && q.z < 0.f && q.w < 0.f;
+            bspk[k] = __ballot_sync(0xffffffffu, sp);
+            bnegk[k] = __ballot_sync(0xffffffffu, neg);
+        }
+#pragma unroll
+        for (int k = 0; k < NU; ++k) stage_unit(v[k], t + k * kNct, lane, bspk[k], bnegk[k], act, gneg, spec);
+    } else {
 #pragma unroll
         for (int k = 0; k < NU; ++k) {
             const int u = t + k * kNct;
-            if ((u & 15) == 0) gs[u >> 4] = gsum[k];
+            const float4 q = v[k];
+            if (a.prologue != kProNone) {
+                const float s = sum4_group<kTree>(q);
+                if ((u & 15) == 0) gs[u >> 4] = s;
+            }
+            const bool sp = !x_ordinary(q.x) || !x_ordinary(q.y) || !x_ordinary(q.z) || !x_ordinary(q.w);
+            const bool neg = q.x < 0.f && q.y < 0.f && q.z < 0.f && q.w < 0.f;
+            const unsigned bsp = __ballot_sync(0xffffffffu, sp), bneg = __ballot_sync(0xffffffffu, neg);
+            stage_unit(q, u, lane, bsp, bneg, act, gneg, spec);
         }
-    }
-    unsigned bspk[NU], bnegk[NU];
-#pragma unroll
-    for (int k = 0; k < NU; ++k) {
-        const float4 q = v[k];
-        const bool sp = !x_ordinary(q.x) || !x_ordinary(q.y) || !x_ordinary(q.z) || !x_ordinary(q.w);
-        const bool neg = q.x < 0.f && q.y < 0.f && q.z < 0.f && q.w < 0.f;
-        bspk[k] = __ballot_sync(0xffffffffu, sp);
-        bnegk[k] = __ballot_sync(0xffffffffu, neg);
-    }
-#pragma unroll
-    for (int k = 0; k < NU; ++k) {
-        const int u = t + k * kNct, c = 4 * u;
-        const float4 q = v[k];
-        const unsigned bsp = bspk[k], bneg = bnegk[k];
-        if (lane == 0) spec[u >> 5] = bsp != 0u;
-        if ((u & 15) == 0) gneg[u >> 4] = ((bneg >> (lane & 16)) & 0xffffu) == 0xffffu;
-        const int ch = c >> 10, l = (c & 1023) >> 5, i = (c & 31) >> 2;
-        // a 128-column block of ordinary values (this warp's 32 units) is
-        // staged times -2^(23-4k) of its columns' nibbles, the exact path's
-        // operands; a block with a special value is staged as it is
-        float4 st = q;
-        if (bsp == 0u) {
-            const int j0 = c & 4;
-            st = make_float4(__fmul_rn(q.x, -nib_scale(j0)), __fmul_rn(q.y, -nib_scale(j0 + 1)),
-                             __fmul_rn(q.z, -nib_scale(j0 + 2)), __fmul_rn(q.w, -nib_scale(j0 + 3)));
-        }
-        reinterpret_cast<float4 *>(act)[(ch * 8 + i) * 32 + l] = st;
     }
     named_bar(1, kNct);
 }
@@ -907,7 +952,7 @@ __global__ void __launch_bounds__(layout_threads(kLayout), layout_blocks(kLayout
             // a SwiGLU pair's tile: TR/2 rows of the gate product into the
             // stage's first half, the same rows of the up product after them;
             // otherwise the problem's tile rows (at most TR)
-            const int trp = a.paired ? TR / 2 : static_cast<int>(P.tr);
+            const int trp = a.paired ? TR / 2 : (kFix && kLayout != 1 ? TR : static_cast<int>(P.tr));
             const int64_t r0 = static_cast<int64_t>(tile) * trp;
             const int rows = static_cast<int>(min(static_cast<int64_t>(trp), P.n - r0));
             unsigned char *st = smem + a.off_stage + static_cast<size_t>(s) * stage_bytes;
@@ -1001,9 +1046,9 @@ __global__ void __launch_bounds__(layout_threads(kLayout), layout_blocks(kLayout
     // Rows are loaded in batches of B = min(R, 4): batch b's row i is row
     // (4b + i) ^ pi = (i ^ pi) + 4b or - 4b, so one set of B offsets and the
     // batch step serve all batches.
-    // (Fixed shapes set them before the dependency wait and stage the
-    // activation after it; the other instantiations wait and compute their
-    // prologue before this point.)
+    // (The fixed shapes' few-tiles layout sets them before the dependency
+    // wait; the other instantiations wait and compute their prologue before
+    // setting them.)
     constexpr int B = R < 4 ? R : 4;
     const int pi = rev_lane_bits<kLogR>(lane);
     const uint32_t rowW = static_cast<uint32_t>(W) * 4u;
@@ -1037,9 +1082,10 @@ __global__ void __launch_bounds__(layout_threads(kLayout), layout_blocks(kLayout
         sbd = (gpar - gown) * static_cast<int>(kElem);
     };
     if constexpr (kFix) {
-        // a fixed shape's lane constants need no activation: set before the wait
+        // a fixed shape's lane constants need no activation: the few-tiles
+        // layout, bound by latency, sets them before the wait
         sl.act = sl.actp = sl.full = true;
-        set_chunk(ch0);
+        if constexpr (kLayout == 1) set_chunk(ch0);
         if (wait_first) {
             grid_dep_wait();
             grid_dep_launch();
@@ -1049,8 +1095,9 @@ __global__ void __launch_bounds__(layout_threads(kLayout), layout_blocks(kLayout
         float *gs = act + kC;
         unsigned *gneg = reinterpret_cast<unsigned *>(gs + kC / 64);
         unsigned *spec = gneg + kC / 64;
-        coop_prologue<kTree, kC, kNct>(a, cin, act, gs, gneg, spec, cw, s_red);
+        coop_prologue<kTree, kC, kNct, kLayout == 1>(a, cin, act, gs, gneg, spec, cw, s_red, &s_rbox);
         slice_from_stage<kTree, kLg>(a, ch0, lane, act, gs, gneg, spec, sl);
+        if constexpr (kLayout != 1) set_chunk(ch0);
         cur_ch = ch0;
     }
     if (!kFix && cur_ch >= 0) set_chunk(cur_ch);  // slice computed by the prologue
@@ -1232,10 +1279,10 @@ __global__ void __launch_bounds__(layout_threads(kLayout), layout_blocks(kLayout
                 if (!wait_or_abort(&full[s], fph, &s_abort, kSiteFull)) break;
                 const unsigned char *stg = stage0 + static_cast<uint32_t>(s) * stage_bytes;
                 float *prt = part + p * TR * nch;
-                // where the planner may cut quarter tiles (a quarter of the
-                // tile is a whole number of items), a tile of fewer rows skips
-                // the items wholly past its rows
-                constexpr bool kQuarter = kTRf / 4 >= R && (kTRf / 4) % R == 0;
+                // in the few-tiles layout, where the planner cuts quarter
+                // tiles (a quarter of the tile is a whole number of items), a
+                // tile of fewer rows skips the items wholly past its rows
+                constexpr bool kQuarter = kLayout == 1 && kTRf / 4 >= R && (kTRf / 4) % R == 0;
                 const float v = (!kQuarter || rb0 * rbm < s_hdr[p].rows)
                                     ? item(exact_c, std::false_type{}, stg, s_hdr[p], prt, ch0, rb0, lead)
                                     : 0.f;
