@@ -130,8 +130,8 @@ bool plan_once(Q4Plan *plan, const Q4Prob *probs, int nprob, int cols, int group
                        : (!fmt_default || R != 8 || tune.consumer_warps == 0)
                            ? 0
                            : (tune.consumer_warps > 8 ? 1 : (tune.consumer_warps <= 6 ? 2 : 0));
-    const bool wide = layout == 1;
-    const int nw_max = wide ? 16 : (layout == 2 ? 6 : 8);
+    const bool wide = layout == 1 || layout == 4;  // one block per SM, the large shared-memory budget
+    const int nw_max = layout_max_warps(layout);
     int nw = force_layout >= 0 ? 0 : tune.consumer_warps;
     if (nw <= 0) nw = nch <= nw_max ? nch * (nw_max / nch) : nw_max;
     if (nch <= nw_max) nw = nch * (std::min(nw, nw_max) / nch);
@@ -228,7 +228,8 @@ bool plan_once(Q4Plan *plan, const Q4Prob *probs, int nprob, int cols, int group
     // a plan with the compile-time shape of its row length runs the
     // fixed-shape instantiation (same results, constant sizes)
     int shape = 0;
-    if (fmt_default && sb_smem && ((layout == 0 && R == 8) || (layout == 1 && R == 4)) &&
+    if (fmt_default && sb_smem &&
+        ((layout == 0 && R == 8) || (layout == 1 && R == 4) || (layout == 4 && R == 8 && C == 6144)) &&
         (C == 2048 || C == 4096 || C == 6144) && TR == fixed_tr(C, R, layout) && nw == fixed_nw(C, layout) &&
         nch == fixed_nch(C) && a.stage_w_bytes == static_cast<uint32_t>(TR * C / 2) &&
         a.stage_sb_bytes == static_cast<uint32_t>(TR * G * 4))
@@ -313,6 +314,19 @@ bool plan_q4mv(Q4Plan *plan, const Q4Prob *probs, int nprob, int cols, int group
                 return true;
         }
         rows_per_warp = 8;
+    }
+    // rows of 6144 columns in a launch of many tiles: 18 computing warps in one
+    // block per SM (three per chunk), where the two-block layout has six
+    if (rows_per_warp == 8 && cols == 6144 && group == 64 && sb_type == ABG_SB_F32 && sb_smem &&
+        tune.smem_kb == 0 && tune.consumer_warps == 0 && tune.blocks_per_sm == 0 && tune.stage_kb == 0) {
+        const int tr = fixed_tr(cols, 8, 4);
+        int64_t tiles = 0;
+        for (int i = 0; i < nprob; ++i) tiles += (probs[i].n + tr - 1) / tr;
+        if (tiles > static_cast<int64_t>(kFewTilesPerSm) * sm_count() &&
+            plan_once(plan, probs, nprob, cols, group, sb_type, prologue, x, xsum, wt, eps, tree, 8, sb_smem, tune,
+                      false, 4) &&
+            plan->shape == cols)
+            return true;
     }
     for (int R = rows_per_warp; R >= 1; R /= 2)
         if (plan_once(plan, probs, nprob, cols, group, sb_type, prologue, x, xsum, wt, eps, tree, R, sb_smem, tune,

@@ -10,7 +10,9 @@
 namespace abg {
 
 // rows per item R and block layout: (8, 0) for launches of many tiles, (4, 1)
-// for launches of few tiles (16 computing warps, one block per SM)
+// for launches of few tiles (16 computing warps, one block per SM), and for
+// rows of 6144 columns in launches of many tiles (8, 4) (18 computing warps,
+// one block per SM)
 template <int R, int L>
 void *select_fixed(int cols, bool tree) {
     switch (cols) {
@@ -24,6 +26,8 @@ void *select_fixed(int cols, bool tree) {
 void *q4mv_select_fixed(int cols, bool tree, int R, int layout) {
     if (R == 8 && layout == 0) return select_fixed<8, 0>(cols, tree);
     if (R == 4 && layout == 1) return select_fixed<4, 1>(cols, tree);
+    if (R == 8 && layout == 4 && cols == 6144)
+        return tree ? kernel_ptr<8, true, true, 4, 1, false, 6144>() : kernel_ptr<8, false, true, 4, 1, false, 6144>();
     return nullptr;
 }
 

@@ -515,21 +515,28 @@ __device__ __forceinline__ void coop_prologue(const Q4Args &a, const CoopIn<(kC 
                                               float *act, float *gs, unsigned *gneg, unsigned *spec, int cw,
                                               float *red, float *rbox) {
     constexpr int NU = (kC / 4 + kNct - 1) / kNct;
-    static_assert((kC / 4) % kNct == 0, "every thread has NU whole units");
+    // units per thread: NU, or in a block whose threads do not divide the
+    // units, NU - 1 for the threads of the last round's idle warps (whole
+    // warps: the units and the threads are multiples of 32)
+    constexpr bool kWhole = (kC / 4) % kNct == 0;
+    static_assert((kC / 4) % 32 == 0 && kNct % 32 == 0 && (kWhole || !kLatency), "whole warps of units");
     const int t = threadIdx.x - 32, lane = threadIdx.x & 31;
+    auto has = [&](int k) { return kWhole || t + k * kNct < kC / 4; };
     const float4 *x4 = reinterpret_cast<const float4 *>(a.x);
     float4 v[NU];
     if (a.prologue == kProSwq) {
         const float4 *u4 = reinterpret_cast<const float4 *>(a.x + kC);
 #pragma unroll
         for (int k = 0; k < NU; ++k) {
+            v[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (!has(k)) continue;
             const float4 g = x4[t + k * kNct], u = u4[t + k * kNct];
             v[k] = make_float4(swiglu<kTree>(g.x, u.x), swiglu<kTree>(g.y, u.y), swiglu<kTree>(g.z, u.z),
                                swiglu<kTree>(g.w, u.w));
         }
     } else {
 #pragma unroll
-        for (int k = 0; k < NU; ++k) v[k] = x4[t + k * kNct];
+        for (int k = 0; k < NU; ++k) v[k] = has(k) ? x4[t + k * kNct] : make_float4(0.f, 0.f, 0.f, 0.f);
     }
     if (a.prologue == kProRmsq) {
         float4 sq[NU];
@@ -550,6 +557,7 @@ __device__ __forceinline__ void coop_prologue(const Q4Args &a, const CoopIn<(kC 
         } else {
 #pragma unroll
             for (int k = 0; k < NU; ++k) {
+                if (!has(k)) continue;
                 const float s = sum4_group<kTree>(sq[k]);
                 const int u = t + k * kNct;
                 if ((u & 15) == 0) red[u >> 4] = s;
@@ -558,6 +566,7 @@ __device__ __forceinline__ void coop_prologue(const Q4Args &a, const CoopIn<(kC 
         }
 #pragma unroll
         for (int k = 0; k < NU; ++k) {
+            if (!has(k)) continue;
             const float4 q = v[k], w = in.w[k];
             v[k] = make_float4(__fmul_rn(__fmul_rn(q.x, r), w.x), __fmul_rn(__fmul_rn(q.y, r), w.y),
                                __fmul_rn(__fmul_rn(q.z, r), w.z), __fmul_rn(__fmul_rn(q.w, r), w.w));
@@ -587,6 +596,7 @@ __device__ __forceinline__ void coop_prologue(const Q4Args &a, const CoopIn<(kC 
     } else {
 #pragma unroll
         for (int k = 0; k < NU; ++k) {
+            if (!has(k)) continue;
             const int u = t + k * kNct;
             const float4 q = v[k];
             if (a.prologue != kProNone) {
@@ -743,10 +753,18 @@ __device__ __forceinline__ void levels(float (&v)[N], float (&out)[lv_count<N, D
 // so the warps per SM set the registers per thread):
 //   kLayout 0: up to 8 computing warps, two blocks per SM (96 registers);
 //   kLayout 1: up to 16 computing warps, one block per SM;
-//   kLayout 2: up to 6 computing warps, two blocks per SM (128 registers).
+//   kLayout 2: up to 6 computing warps, two blocks per SM (128 registers);
+//   kLayout 4: up to 18 computing warps, one block per SM (rows of 6144
+//              columns: three warps per 1024-column chunk).
 // With two blocks per SM the next launch of a chain can start beside this one.
-constexpr int layout_threads(int l) { return l == 1 ? 544 : (l == 2 ? 224 : 288); }
-constexpr int layout_blocks(int l) { return l == 1 ? 1 : 2; }
+constexpr int layout_threads(int l) { return l == 1 ? 544 : (l == 2 ? 224 : (l == 4 ? 608 : 288)); }
+constexpr int layout_blocks(int l) { return (l == 1 || l == 4) ? 1 : 2; }
+// The launch-bounds thread count: layout 4 declares 21 warps (it launches
+// 19) so that the register cap is 96, which keeps the 5 warps of its fullest
+// SM sub-partition within the sub-partition's 16K registers.
+constexpr int layout_bound_threads(int l) { return l == 4 ? 672 : layout_threads(l); }
+// computing warps at most per block
+__host__ __device__ constexpr int layout_max_warps(int l) { return l == 1 ? 16 : (l == 4 ? 18 : (l == 2 ? 6 : 8)); }
 
 // Where a tile's results go.  The producer writes the header of a block's
 // k-th tile into slot k mod (S + 2) -- the slot of the tile's partial-sum
@@ -848,8 +866,8 @@ __device__ __forceinline__ float tree_chunks(const float *p, int m) {
 // offsets are constants.
 __host__ __device__ constexpr int fixed_nch(int C) { return (C + 1023) / 1024; }
 __host__ __device__ constexpr int fixed_nw(int C, int layout = 0) {
-    return fixed_nch(C) <= (layout == 1 ? 16 : 8) ? fixed_nch(C) * ((layout == 1 ? 16 : 8) / fixed_nch(C))
-                                                 : (layout == 1 ? 16 : 8);
+    return fixed_nch(C) <= layout_max_warps(layout) ? fixed_nch(C) * (layout_max_warps(layout) / fixed_nch(C))
+                                                    : layout_max_warps(layout);
 }
 __host__ __device__ constexpr int fixed_tr(int C, int R, int layout = 0) {
     const int nch = fixed_nch(C), nw = fixed_nw(C, layout), kk = nch <= nw ? nw / nch : 1;
@@ -875,9 +893,9 @@ __device__ __forceinline__ float tree_fixed(const float (&v)[N]) {
 }
 
 template <int R, bool kTree, bool kSbSmem, int kLayout, int kLg, bool kHalf, int kC = 0>
-__global__ void __launch_bounds__(layout_threads(kLayout), layout_blocks(kLayout))
+__global__ void __launch_bounds__(layout_bound_threads(kLayout), layout_blocks(kLayout))
     q4mv_kernel(const __grid_constant__ Q4Args a) {
-    static_assert(kC == 0 || (kLayout <= 1 && kLg == 1 && !kHalf && kSbSmem), "fixed shapes: default format only");
+    static_assert(kC == 0 || (kLayout != 2 && kLg == 1 && !kHalf && kSbSmem), "fixed shapes: default format only");
     constexpr bool kFix = kC != 0;
     constexpr int kL = 1 << kLg;                  // lanes per group
     constexpr uint32_t kElem = kHalf ? 2u : 4u;   // bytes per stored scale or bias
@@ -1016,7 +1034,8 @@ __global__ void __launch_bounds__(layout_threads(kLayout), layout_blocks(kLayout
     if (kFix && a.prologue == kProRmsq) {
         const float4 *w4 = reinterpret_cast<const float4 *>(a.wt);
 #pragma unroll
-        for (int k = 0; k < kNU; ++k) cin.w[k] = __ldg(w4 + ct + k * kNct);
+        for (int k = 0; k < kNU; ++k)
+            if ((kC / 4) % kNct == 0 || ct + k * kNct < kC / 4) cin.w[k] = __ldg(w4 + ct + k * kNct);
     }
     Slice sl;
     int cur_ch = -1;

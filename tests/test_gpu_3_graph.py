@@ -234,3 +234,48 @@ def test_grouped_products_with_quarter_tiles(cols, rows):
         assert_bits_equal(host(y), oracle.q4mv(*m.arrays(), xn, xs, cols), f"{n}x{cols}")
     assert abg.device_status(clear=True) == 0
     g.close()
+
+
+@pytest.mark.parametrize("prologue", ["rmsq", "swq", "gsum", "special"])
+def test_prologues_many_tiles_6144(prologue):
+    """Rows of 6144 columns in a launch of many tiles run 18 computing warps per
+    block, whose cooperative prologue has a partial last round of units (1536
+    units over 576 threads): each prologue, and an activation with special
+    values and all-negative groups (the plain path in some warps), bit-exact
+    in tree mode and within the bound in fast mode."""
+    rows, cols = 20000, 6144
+    rng = np.random.default_rng([rows, cols, len(prologue)])
+    m = synth.q4_matrix(rng, rows, cols)
+    w, sc, bi = dev_words(m.w), dev(m.scale), dev(m.bias)
+    if prologue == "swq":
+        a = np.concatenate([synth.activations(rng, cols), synth.activations(rng, cols)])
+        x, xs = oracle.swq(a)
+        xin, kw = dev(a), dict(prologue=abg.PRO_SWQ)
+    elif prologue == "rmsq":
+        h = synth.activations(rng, cols)
+        wt = synth.rms_weights(rng, cols)
+        x, xs = oracle.rmsq(h, wt, 1e-6)
+        wtd = dev(wt)
+        xin, kw = dev(h), dict(prologue=abg.PRO_RMSQ, wt=wtd, eps=1e-6)
+    else:
+        x = synth.activations(rng, cols)
+        if prologue == "special":
+            x[64:128] = -np.abs(x[64:128])
+            x[5000] = np.inf
+            x[5001] = -0.0
+        xs = oracle.gsum(x)
+        xin, kw = dev(x), dict(prologue=abg.PRO_GSUM)
+    tree = oracle.q4mv(*m.arrays(), x, xs, cols)
+    keep = [xin, w, sc, bi] + [v for v in kw.values() if hasattr(v, "data_ptr")]
+    for mode in (abg.TREE, abg.FAST):
+        y = empty(rows)
+        g = abg.StageGraph([abg.Node.q4mv(0, w, sc, bi, y, cols, x=xin, **kw)], keep=keep + [y], mode=mode)
+        g.launch()
+        torch.cuda.synchronize()
+        if mode == abg.TREE:
+            assert_bits_equal(host(y), tree, f"{prologue} {rows}x{cols}")
+        elif prologue != "special":
+            assert_fast_close(host(y), tree, oracle.q4mv_absmag(*m.arrays(), x, xs, cols),
+                              what=f"fast {prologue} {rows}x{cols}")
+        g.close()
+    assert abg.device_status(clear=True) == 0
