@@ -72,6 +72,12 @@ def _load():
             lib.or_f16_to_f32.restype = ctypes.c_float
             lib.or_gsum_ex.argtypes = [f32p, f32p, i64, ctypes.c_int]
             lib.or_q4mv_ex.argtypes = [u32p, vp, vp, ctypes.c_int, ctypes.c_int, f32p, f32p, f32p, i64, i64, i64, i64]
+            lib.or_log.argtypes = [ctypes.c_float]
+            lib.or_log.restype = ctypes.c_float
+            lib.or_log_array.argtypes = [f32p, f32p, i64]
+            fl = ctypes.c_float
+            lib.or_gdn.argtypes = [f32p, f32p, f32p, f32p, f32p, f32p, f32p, f32p, f32p, f32p, f32p, f32p,
+                                   i64, i64, i64, fl, fl]
             _lib = lib
     return _lib
 
@@ -279,3 +285,45 @@ def q4mm(w, scale, bias, X, XS, cols, row0=0, n=None) -> np.ndarray:
     if X.shape[0] != XS.shape[0]:
         raise ValueError("X and XS hold different token counts")
     return np.stack([q4mv(w, scale, bias, X[t], XS[t], cols, row0=row0, n=n) for t in range(X.shape[0])])
+
+
+def log(v) -> np.ndarray:
+    """The specified binary32 natural logarithm, elementwise (oracle.c LOG)."""
+    v, pv = _f32(v)
+    out = np.empty(v.shape, np.float32)
+    _load().or_log_array(pv, _f32(out)[1], v.size)
+    return out
+
+
+def gdn(x, conv, state, a, b, z, A_log, dt_bias, nw, S, eps=1e-6, eps_n=1e-6):
+    """One token of the gated DeltaNet mixer (oracle.c or_gdn): returns
+    (y, ysum, S_new, state_new) without touching the inputs.
+
+    Shapes: x [3*H*D] (q | k | v), conv [3*H*D][K], state [3*H*D][K-1],
+    a, b, A_log, dt_bias [H], z [H*D], nw [D], S [H][D][D] (keys by values).
+    """
+    S = np.array(S, dtype=np.float32, copy=True)
+    H, D = S.shape[0], S.shape[1]
+    if S.shape != (H, D, D) or D % 64 or D > 1024:
+        raise ValueError("S must be [H][D][D] with D a multiple of 64, at most 1024")
+    conv = np.ascontiguousarray(conv, dtype=np.float32)
+    K = conv.shape[-1]
+    if conv.shape != (3 * H * D, K) or not 2 <= K <= 8:
+        raise ValueError("conv must be [3*H*D][K] with 2 <= K <= 8")
+    state = np.array(state, dtype=np.float32, copy=True).reshape(3 * H * D, K - 1)
+    x, px = _f32(x)
+    if x.size != 3 * H * D:
+        raise ValueError("x must hold 3*H*D values")
+    a, pa = _f32(a)
+    b, pb = _f32(b)
+    A_log, pA = _f32(A_log)
+    dt_bias, pdt = _f32(dt_bias)
+    z, pz = _f32(z)
+    nw, pn = _f32(nw)
+    if a.size != H or b.size != H or A_log.size != H or dt_bias.size != H or z.size != H * D or nw.size != D:
+        raise ValueError("a, b, A_log, dt_bias must hold H values, z H*D, nw D")
+    y = np.empty(H * D, np.float32)
+    ys = np.empty(H * D // 64, np.float32)
+    _load().or_gdn(px, _f32(conv)[1], _f32(state)[1], pa, pb, pz, pA, pdt, pn, _f32(S)[1], _f32(y)[1],
+                   _f32(ys)[1], H, D, K, ctypes.c_float(np.float32(eps)), ctypes.c_float(np.float32(eps_n)))
+    return y, ys, S, state

@@ -369,3 +369,184 @@ void or_q4mv_ex(const uint32_t *w, const void *scale, const void *bias, int sb_d
     }
     free(t);
 }
+
+/* ------------------------------------------------------------------------ */
+/* LOG: a natural logarithm both sides compute from this written definition */
+/* (the gdn mixer's softplus needs one; as with EXP, a vendor log would move */
+/* the last bits).  Reduction to m in [sqrt(1/2), sqrt(2)) times 2^e, then   */
+/* log(m) = 2 atanh(s) with s = (m - 1)/(m + 1), the atanh series summed to  */
+/* the s^9 term (|s| <= 0.1716, so the first omitted term is below 1e-9 of    */
+/* the result), and e*ln2 added in two parts:                                */
+/*   special: NaN -> NaN; v < 0 -> NaN; v == 0 -> -inf; +inf -> +inf         */
+/*   subnormal v: v*2^23 (exact), e -= 23                                     */
+/*   m = v's significand in [1, 2), e = its exponent                          */
+/*   if m > RN(sqrt 2) (0x3FB504F3): m = m*0.5, e = e + 1   (exact)           */
+/*   f = m - 1 (exact);  s = f / (2 + f);  t = s*s                            */
+/*   p = D9;  p = p*t + D7;  p = p*t + D5;  p = p*t + D3;  p = p*t + 2        */
+/*   (D_k = RN(2/k); each step a multiply then an add)                        */
+/*   result = e*LN2HI + (s*p + e*LN2LO)     (LN2HI, LN2LO as in EXP; e*LN2HI */
+/*   and e*LN2LO are exact for |e| < 2^12)                                    */
+/* ------------------------------------------------------------------------ */
+float or_log(float v)
+{
+    if (v != v) return v;
+    if (v < 0.0f) return NAN;
+    if (v == 0.0f) return -INFINITY;
+    if (v == INFINITY) return v;
+    int e = 0;
+    uint32_t b;
+    memcpy(&b, &v, sizeof b);
+    if ((b >> 23) == 0) { /* subnormal */
+        const float vs = v * pow2i(23);
+        memcpy(&b, &vs, sizeof b);
+        e = -23;
+    }
+    e += (int)(b >> 23) - 127;
+    float m = f32_from_bits((b & 0x007FFFFFu) | 0x3F800000u);
+    if (m > f32_from_bits(0x3FB504F3u)) {
+        m = m * 0.5f;
+        e = e + 1;
+    }
+    const float LN2HI = f32_from_bits(0x3F317000u);
+    const float LN2LO = f32_from_bits(0x3805FDF4u);
+    const float D9 = 2.0f / 9.0f, D7 = 2.0f / 7.0f, D5 = 2.0f / 5.0f, D3 = 2.0f / 3.0f;
+    const float f = m - 1.0f;
+    const float den = 2.0f + f;
+    const float s = f / den;
+    const float t = s * s;
+    float p = D9;
+    p = p * t;
+    p = p + D7;
+    p = p * t;
+    p = p + D5;
+    p = p * t;
+    p = p + D3;
+    p = p * t;
+    p = p + 2.0f;
+    const float ef = (float)e;
+    const float hi = ef * LN2HI;
+    const float lo = ef * LN2LO;
+    const float sp = s * p;
+    const float r = sp + lo;
+    return hi + r;
+}
+
+void or_log_array(const float *v, float *out, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = or_log(v[i]);
+}
+
+/* ------------------------------------------------------------------------ */
+/* gdn: one token of a gated DeltaNet mixer.  [fused-token] Change, the      */
+/* Array.gdn bullet, lists the phases -- conv window and activation, q/k L2  */
+/* norms, decay and beta, the delta-rule rows, the gated norm and group      */
+/* sums -- with one threadgroup per value head, every phase local to its     */
+/* head.  The pages give no formulas; the reading (the published gated       */
+/* DeltaNet recurrence, one key head per value head, head dimension D for q, */
+/* k and v, K conv taps, every sum a TREE, every step one RN binary32 op):   */
+/*   SIGMOID(u) = 1 / (1 + EXP(-u));  SILU(u) = u / (1 + EXP(-u)) (as swq)   */
+/*   SOFTPLUS(u) = u if u > 20, else LOG(1 + EXP(u))                         */
+/* Channels c of x = [q | k | v] (3*H*D values, head h's block at h*D):       */
+/*   window w = [state[c][0..K-2], x[c]];  a_c = SILU(TREE_j(conv[c][j]*w[j])) */
+/*   state[c] <- w[1..K-1]                                                   */
+/* Head h (q, k, v its D activations; i indexes keys, j values):             */
+/*   rq = 1 / sqrt(TREE_i(q_i*q_i) + eps);  qh_i = (q_i*rq) * RN(1/sqrt(D))   */
+/*   rk = 1 / sqrt(TREE_i(k_i*k_i) + eps);  kh_i = k_i*rk                    */
+/*   alpha = EXP(-(EXP(A_log[h]) * SOFTPLUS(a[h] + dt_bias[h])))              */
+/*   beta  = SIGMOID(b[h])                                                   */
+/*   S[i][j] <- S[i][j]*alpha                                                */
+/*   kv_j = TREE_i(S[i][j]*kh_i);  d_j = beta*(v_j - kv_j)                    */
+/*   S[i][j] <- S[i][j] + kh_i*d_j                                           */
+/*   o_j = TREE_i(S[i][j]*qh_i)                                              */
+/*   r = 1 / sqrt(TREE_j(o_j*o_j) / D + eps_n)                               */
+/*   y_j = ((o_j*r) * nw_j) * SILU(z_j)                                      */
+/* ysum = the 64-value group sums of y.  S [H][D][D] and state [3HD][K-1]    */
+/* are updated in place.  D a multiple of 64 (<= 1024), K <= 8.               */
+/* ------------------------------------------------------------------------ */
+static float or_sigmoid(float u)
+{
+    const float e = or_exp(-u);
+    const float den = 1.0f + e;
+    return 1.0f / den;
+}
+
+static float or_silu(float u)
+{
+    const float e = or_exp(-u);
+    const float den = 1.0f + e;
+    return u / den;
+}
+
+static float or_softplus(float u)
+{
+    if (u > 20.0f) return u;
+    const float e = or_exp(u);
+    const float one_e = 1.0f + e;
+    return or_log(one_e);
+}
+
+void or_gdn(const float *x, const float *conv, float *state, const float *a, const float *b, const float *z,
+            const float *A_log, const float *dt_bias, const float *nw, float *S, float *y, float *ysum,
+            int64_t H, int64_t D, int64_t K, float eps, float eps_n)
+{
+    const int64_t C = 3 * H * D;
+    float *act = (float *)malloc((size_t)C * sizeof(float));
+    float *tmp = (float *)malloc((size_t)(D > K ? D : K) * sizeof(float));
+    float *qh = (float *)malloc((size_t)D * sizeof(float));
+    float *kh = (float *)malloc((size_t)D * sizeof(float));
+    float *o = (float *)malloc((size_t)D * sizeof(float));
+    float wv[8];
+    for (int64_t c = 0; c < C; ++c) {
+        for (int64_t j = 0; j < K - 1; ++j) wv[j] = state[c * (K - 1) + j];
+        wv[K - 1] = x[c];
+        for (int64_t j = 0; j < K; ++j) tmp[j] = conv[c * K + j] * wv[j];
+        act[c] = or_silu(or_tree(tmp, K));
+        for (int64_t j = 0; j < K - 1; ++j) state[c * (K - 1) + j] = wv[j + 1];
+    }
+    const float qscale = 1.0f / sqrtf((float)D);
+    for (int64_t h = 0; h < H; ++h) {
+        const float *q = act + h * D, *k = act + H * D + h * D, *v = act + 2 * H * D + h * D;
+        for (int64_t i = 0; i < D; ++i) tmp[i] = q[i] * q[i];
+        const float rq = 1.0f / sqrtf(or_tree(tmp, D) + eps);
+        for (int64_t i = 0; i < D; ++i) {
+            const float t = q[i] * rq;
+            qh[i] = t * qscale;
+        }
+        for (int64_t i = 0; i < D; ++i) tmp[i] = k[i] * k[i];
+        const float rk = 1.0f / sqrtf(or_tree(tmp, D) + eps);
+        for (int64_t i = 0; i < D; ++i) kh[i] = k[i] * rk;
+        const float dec = or_exp(A_log[h]) * or_softplus(a[h] + dt_bias[h]);
+        const float alpha = or_exp(-dec);
+        const float beta = or_sigmoid(b[h]);
+        float *Sh = S + h * D * D;
+        for (int64_t i = 0; i < D * D; ++i) Sh[i] = Sh[i] * alpha;
+        for (int64_t j = 0; j < D; ++j) {
+            for (int64_t i = 0; i < D; ++i) tmp[i] = Sh[i * D + j] * kh[i];
+            const float kv = or_tree(tmp, D);
+            const float dv = v[j] - kv;
+            const float d = beta * dv;
+            for (int64_t i = 0; i < D; ++i) {
+                const float u = kh[i] * d;
+                Sh[i * D + j] = Sh[i * D + j] + u;
+            }
+        }
+        for (int64_t j = 0; j < D; ++j) {
+            for (int64_t i = 0; i < D; ++i) tmp[i] = Sh[i * D + j] * qh[i];
+            o[j] = or_tree(tmp, D);
+        }
+        for (int64_t j = 0; j < D; ++j) tmp[j] = o[j] * o[j];
+        const float mean = or_tree(tmp, D) / (float)D;
+        const float r = 1.0f / sqrtf(mean + eps_n);
+        for (int64_t j = 0; j < D; ++j) {
+            const float on = o[j] * r;
+            const float ow = on * nw[j];
+            y[h * D + j] = ow * or_silu(z[h * D + j]);
+        }
+    }
+    or_gsum(y, ysum, H * D);
+    free(act);
+    free(tmp);
+    free(qh);
+    free(kh);
+    free(o);
+}
