@@ -89,6 +89,8 @@ def library(build_if_missing: bool = True) -> ctypes.CDLL:
             lib.abg_stage_graph_swiglu_pairs.argtypes = [P, ctypes.POINTER(I64)]
             lib.abg_swiglu_mlp_static.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P, I64, I64, I64, I, P]
             lib.abg_stage_graph_destroy.argtypes = [P]
+            F = ctypes.c_float
+            lib.abg_gdn.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P, I64, I64, I64, F, F, I, P]
             lib.abg_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32), I]
             lib.abg_selftest_wait_timeout.argtypes = [P]
             lib.abg_set_q4mv_tuning.argtypes = [I, I, I, I]
@@ -99,7 +101,7 @@ def library(build_if_missing: bool = True) -> ctypes.CDLL:
             for f in ("abg_q4mv", "abg_q4mm", "abg_gsum", "abg_rmsq", "abg_swq", "abg_q4mv_ex", "abg_gsum_ex", "abg_rmsq_ex",
                       "abg_swq_ex", "abg_stage_graph_create",
                       "abg_stage_graph_launch", "abg_stage_graph_launches", "abg_stage_graph_swiglu_pairs",
-                      "abg_stage_graph_destroy", "abg_swiglu_mlp_static",
+                      "abg_stage_graph_destroy", "abg_swiglu_mlp_static", "abg_gdn",
                       "abg_device_status", "abg_set_q4mv_tuning", "abg_selftest_wait_timeout"):
                 getattr(lib, f).restype = ctypes.c_int
             _lib = lib
@@ -193,6 +195,24 @@ def q4mm(w, scale, bias, X, XS, Y, cols: int, row0: int = 0, n: int | None = Non
         rows, cols, row0, n, T, mode, rows_per_warp, _stream(stream))
     _check(st, "abg_q4mm")
     return Y
+
+
+def gdn(x, conv, state, a, b, z, A_log, dt_bias, nw, S, y, ysum, eps: float = 1e-6, eps_n: float = 1e-6,
+        mode: int = TREE, stream=None):
+    """One token of the gated DeltaNet mixer (see abg_gdn): S [H][D][D] and
+    state [3*H*D][K-1] are updated in place; y [H*D] and ysum [H*D/64] written."""
+    _, f32 = _dtypes()
+    H, D = S.shape[0], S.shape[1]
+    K = conv.shape[-1]
+    C = 3 * H * D
+    st = library().abg_gdn(
+        _ptr(x, f32, C, "x"), _ptr(conv, f32, C * K, "conv"), _ptr(state, f32, C * (K - 1), "state"),
+        _ptr(a, f32, H, "a"), _ptr(b, f32, H, "b"), _ptr(z, f32, H * D, "z"), _ptr(A_log, f32, H, "A_log"),
+        _ptr(dt_bias, f32, H, "dt_bias"), _ptr(nw, f32, D, "nw"), _ptr(S, f32, H * D * D, "S"),
+        _ptr(y, f32, H * D, "y"), _ptr(ysum, f32, H * D // 64, "ysum"), H, D, K, ctypes.c_float(eps),
+        ctypes.c_float(eps_n), mode, _stream(stream))
+    _check(st, "abg_gdn")
+    return y
 
 
 def swiglu_mlp_static(gate, up, down, x, xsum, y, cols: int, mode: int = TREE, stream=None):

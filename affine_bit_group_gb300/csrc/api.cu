@@ -488,6 +488,32 @@ abg_status abg_swq_ex(const float *a, float *o, float *osum, int64_t n, int grou
     return cuda_fail(launch_swq(a, o, osum, n, group, mode == ABG_TREE, static_cast<cudaStream_t>(stream), false));
 }
 
+abg_status abg_gdn(const float *x, const float *conv, float *state, const float *a, const float *b, const float *z,
+                   const float *A_log, const float *dt_bias, const float *nw, float *S, float *y, float *ysum,
+                   int64_t H, int64_t D, int64_t K, float eps, float eps_n, int mode, void *stream) {
+    if (mode != ABG_TREE && mode != ABG_FAST) return ABG_EINVAL;
+    if (!x || !conv || !state || !a || !b || !z || !A_log || !dt_bias || !nw || !S || !y || !ysum) return ABG_EINVAL;
+    if (H < 1 || (D != 64 && D != 128 && D != 256) || K < 2 || K > 8 || H * D > (int64_t(1) << 20))
+        return ABG_ESHAPE;
+    const void *all[] = {x, conv, state, a, b, z, A_log, dt_bias, nw, S, y, ysum};
+    for (const void *p : all)
+        if (!aligned(p, 4)) return ABG_EALIGN;
+    const int64_t C = 3 * H * D;
+    const Range in[] = {rng(x, C, 4), rng(conv, C * K, 4), rng(a, H, 4), rng(b, H, 4), rng(z, H * D, 4),
+                        rng(A_log, H, 4), rng(dt_bias, H, 4), rng(nw, D, 4)};
+    const Range out[] = {rng(state, C * (K - 1), 4), rng(S, H * D * D, 4), rng(y, H * D, 4), rng(ysum, H * D / 64, 4)};
+    for (int i = 0; i < 4; ++i) {
+        for (const Range &r : in)
+            if (overlap(out[i], r)) return ABG_EALIAS;
+        for (int k = i + 1; k < 4; ++k)
+            if (overlap(out[i], out[k])) return ABG_EALIAS;
+    }
+    return cuda_fail(launch_gdn(x, conv, state, a, b, z, A_log, dt_bias, nw, S, y, ysum, static_cast<int>(H),
+                                static_cast<int>(D), static_cast<int>(K), eps, eps_n,
+                                static_cast<cudaStream_t>(stream)),
+                     "gdn launch");
+}
+
 abg_status abg_stage_graph_create(const abg_node *nodes, int64_t count, int mode, int rows_per_warp,
                                   void **graph_out) {
     if (!graph_out) return ABG_EINVAL;

@@ -199,3 +199,28 @@ def decode_model(seed: int = 3, n_layers: int = N_LAYERS, hidden: int = HIDDEN, 
     model.head = q4_matrix(rng, head_rows, hidden)
     h = activations(rng, hidden)
     return model, h
+
+
+# The gated DeltaNet mixer's synthetic token: 16 value heads of 128 columns
+# and 4 conv taps (a 2B-class decoder's linear-attention layer; the pages
+# give no dimensions).
+GDN_HEADS = 16
+GDN_DIM = 128
+GDN_TAPS = 4
+
+
+def gdn_case(rng: np.random.Generator, H: int = GDN_HEADS, D: int = GDN_DIM, K: int = GDN_TAPS) -> dict:
+    """Inputs of one gdn token (names as abg_gdn): x, conv, state ~ N(0,1)
+    scaled 1, 0.5, 1; a, b, z ~ N(0,1); A_log, dt_bias ~ N(0, 0.5);
+    nw ~ 1 + N(0, 0.1); S ~ N(0, 0.1), all float32."""
+    C = 3 * H * D
+    return dict(x=rng.standard_normal(C).astype(np.float32),
+                conv=(0.5 * rng.standard_normal((C, K))).astype(np.float32),
+                state=rng.standard_normal((C, K - 1)).astype(np.float32),
+                a=rng.standard_normal(H).astype(np.float32),
+                b=rng.standard_normal(H).astype(np.float32),
+                z=rng.standard_normal(H * D).astype(np.float32),
+                A_log=(0.5 * rng.standard_normal(H)).astype(np.float32),
+                dt_bias=(0.5 * rng.standard_normal(H)).astype(np.float32),
+                nw=(1.0 + 0.1 * rng.standard_normal(D)).astype(np.float32),
+                S=(0.1 * rng.standard_normal((H, D, D))).astype(np.float32))

@@ -203,6 +203,43 @@ abg_status abg_swq(const float *a, float *o, float *osum, int64_t n, int mode, v
  * osum f32 [n/group]; n also a multiple of group). */
 abg_status abg_swq_ex(const float *a, float *o, float *osum, int64_t n, int group, int mode, void *stream);
 
+/*
+ * gdn: one token of a gated DeltaNet mixer ([fused-token] Change, Array.gdn
+ * bullet: conv window and activation, q/k L2 norms, decay and beta, the
+ * delta-rule rows, the gated norm and group sums; one threadgroup per value
+ * head, every phase local to its head).  The page gives no formulas; this is
+ * the published gated DeltaNet recurrence with one key head per value head,
+ * every step one binary32 operation rounded to nearest, every sum the
+ * library's pairwise tree, EXP as in swq and LOG the library's own logarithm
+ * (reduction to [sqrt(1/2), sqrt(2)) times 2^e, 2 atanh(s) by its series to
+ * s^9, e*ln2 in two parts):
+ *   SIGMOID(u) = 1/(1 + EXP(-u)), SILU(u) = u/(1 + EXP(-u)),
+ *   SOFTPLUS(u) = u if u > 20, else LOG(1 + EXP(u))
+ *   channel c of x = [q | k | v]: window w = [state[c][0..K-2], x[c]],
+ *     a_c = SILU(tree_t conv[c][t]*w[t]), state[c] <- w[1..K-1]
+ *   head h: qh = q * (1/sqrt(tree q*q + eps)) * RN(1/sqrt(D)),
+ *     kh = k * (1/sqrt(tree k*k + eps)),
+ *     alpha = EXP(-(EXP(A_log[h]) * SOFTPLUS(a[h] + dt_bias[h]))),
+ *     beta = SIGMOID(b[h]),
+ *     S <- alpha*S;  d_j = beta*(v_j - tree_i S[i][j]*kh_i);
+ *     S[i][j] <- S[i][j] + kh_i*d_j;  o_j = tree_i S[i][j]*qh_i,
+ *     y_j = ((o_j * 1/sqrt(tree(o*o)/D + eps_n)) * nw_j) * SILU(z[h*D+j])
+ *   ysum = 64-value group sums of y.
+ *   x        f32 [3*H*D] (q, then k, then v; head h's block at h*D)
+ *   conv     f32 [3*H*D][K]         state  f32 [3*H*D][K-1], updated in place
+ *   a, b, A_log, dt_bias f32 [H]    z      f32 [H*D]      nw  f32 [D]
+ *   S        f32 [H][D][D] (key i, value j), updated in place
+ *   y        f32 [H*D]              ysum   f32 [H*D/64]
+ *   D = 64, 128 or 256; 2 <= K <= 8; H >= 1, H*D <= 2^20.
+ * Both modes compute the same bits.  Errors: null pointer or mode
+ * ABG_EINVAL; shape ABG_ESHAPE; a pointer not 4-byte aligned ABG_EALIGN; an
+ * output (state, S, y, ysum) overlapping an input or another output
+ * ABG_EALIAS.  Asynchronous on `stream`.
+ */
+abg_status abg_gdn(const float *x, const float *conv, float *state, const float *a, const float *b, const float *z,
+                   const float *A_log, const float *dt_bias, const float *nw, float *S, float *y, float *ysum,
+                   int64_t H, int64_t D, int64_t K, float eps, float eps_n, int mode, void *stream);
+
 /* ---------------------------------------------------------------------------
  * Stage graph: one decode token's dependent stages recorded into one CUDA
  * graph, replayed with one launch and synchronized once by the caller

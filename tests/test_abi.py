@@ -219,3 +219,30 @@ def test_static_mlp_rejects_before_device_work(lib):
     q[0] += 4                                              # gate words not 16-byte aligned
     assert f(*q, 1024, 2048, 10, 0, None) == EALIGN
     assert f(*([None] + p[1:]), 1024, 2048, 10, 0, None) == EINVAL
+
+
+def test_gdn_rejects_before_device_work(lib):
+    """abg_gdn checks its shape, mode, alignment and output overlaps before any
+    device work (fake, well-separated addresses; none is dereferenced)."""
+    f = lib.abg_gdn
+    p = [0x7F0000100000 + (1 << 24) * i for i in range(12)]
+    F = ctypes.c_float
+    ok = dict(H=4, D=128, K=4)
+
+    def call(ptrs, H=4, D=128, K=4, mode=0):
+        return f(*ptrs, H, D, K, F(1e-6), F(1e-6), mode, None)
+
+    assert call(p, D=96) == ESHAPE                # head dimension not 64, 128 or 256
+    assert call(p, K=1) == ESHAPE and call(p, K=9) == ESHAPE
+    assert call(p, H=0) == ESHAPE
+    assert call(p, mode=3) == EINVAL
+    assert call([None] + p[1:]) == EINVAL
+    q = list(p)
+    q[9] = p[0]                                   # S over x
+    assert call(q, **ok) == EALIAS
+    q = list(p)
+    q[10] = p[11]                                 # y over ysum
+    assert call(q, **ok) == EALIAS
+    q = list(p)
+    q[2] += 2                                     # state not 4-byte aligned
+    assert call(q, **ok) == EALIGN
