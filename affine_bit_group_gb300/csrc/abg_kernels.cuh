@@ -126,6 +126,7 @@ cudaError_t q4mm_status(unsigned *bits, bool clear);
 cudaError_t launch_gdn(const float *x, const float *conv, float *state, const float *a, const float *b,
                        const float *z, const float *A_log, const float *dt_bias, const float *nw, float *S, float *y,
                        float *ysum, int H, int D, int K, float eps, float eps_n, cudaStream_t stream);
+cudaError_t mixer_status(unsigned *bits, bool clear);
 
 // Each translation unit's device status word (OR-ed into *bits).
 cudaError_t q4mv_status(unsigned *bits, bool clear);

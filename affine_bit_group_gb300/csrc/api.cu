@@ -498,6 +498,7 @@ abg_status abg_gdn(const float *x, const float *conv, float *state, const float 
     const void *all[] = {x, conv, state, a, b, z, A_log, dt_bias, nw, S, y, ysum};
     for (const void *p : all)
         if (!aligned(p, 4)) return ABG_EALIGN;
+    if (!aligned(S, 16)) return ABG_EALIGN;  // a head's state is one bulk copy
     const int64_t C = 3 * H * D;
     const Range in[] = {rng(x, C, 4), rng(conv, C * K, 4), rng(a, H, 4), rng(b, H, 4), rng(z, H * D, 4),
                         rng(A_log, H, 4), rng(dt_bias, H, 4), rng(nw, D, 4)};
@@ -738,6 +739,7 @@ abg_status abg_device_status(uint32_t *bits, int clear) {
     if (e == cudaSuccess) e = q4mv_status(&v, clear != 0);
     if (e == cudaSuccess) e = vec_status(&v, clear != 0);
     if (e == cudaSuccess) e = q4mm_status(&v, clear != 0);
+    if (e == cudaSuccess) e = mixer_status(&v, clear != 0);
     if (e != cudaSuccess) return cuda_fail(e);
     *bits = v;
     return (v & 1u) ? ABG_ETIMEOUT : ABG_OK;  // bit 0: a bounded wait timed out

@@ -12,9 +12,12 @@
 //   - the conv window of the thread's three channels (q, k, v) and SiLU;
 //   - block sums for the L2 norms and the gated norm: a 5-step butterfly in
 //     each warp, then the tree over the warps' sums;
-//   - the state column S[.][j]: read twice from global memory (coalesced over
-//     j), the decay recomputed on the second read, and each column's sums
-//     over the keys i taken in blocks of 32 keys.
+//   - the state column S[.][j]: for D <= 128 the head's state is brought into
+//     shared memory by one bulk copy at the start (overlapping the conv window,
+//     the norms and the decay), otherwise read from global memory; read twice,
+//     the decay recomputed on the second read, each column's sums over the
+//     keys i taken in blocks of 32 keys, and the new column written to global
+//     memory (coalesced over j).
 #include "abg_dev.cuh"
 #include "abg_kernels.cuh"
 
@@ -131,10 +134,29 @@ __global__ void __launch_bounds__(D) gdn_kernel(const float *__restrict__ x, con
                                                 const float *__restrict__ A_log, const float *__restrict__ dt_bias,
                                                 const float *__restrict__ nw, float *S, float *y, float *ysum,
                                                 int H, int K, float eps, float eps_n) {
+    // D <= 128: the head's state (D*D floats, at most 64 KB) is brought into
+    // shared memory by one bulk copy issued at the start, which overlaps the
+    // conv window, the norms and the decay; both passes over the state then
+    // read shared memory.  D = 256 reads its 256 KB state from global memory.
+    constexpr bool kStage = D <= 128;
+    extern __shared__ __align__(128) float Ss[];
     __shared__ float qh_s[D], kh_s[D];
     __shared__ float red[D / 32];
+    __shared__ uint64_t bar;
     const int h = blockIdx.x, j = threadIdx.x;
     const int64_t HD = static_cast<int64_t>(H) * D;
+    float *const Sh = S + static_cast<int64_t>(h) * D * D;
+    if constexpr (kStage) {
+        if (j == 0) {
+            mbar_init(&bar, 1);
+            fence_mbar_init();
+        }
+        __syncthreads();
+        if (j == 0) {
+            mbar_arrive_expect_tx(&bar, D * D * 4);
+            bulk_g2s(Ss, Sh, D * D * 4, &bar, l2_evict_first());
+        }
+    }
     // conv window and SiLU of the thread's q, k and v channels
     float act[3];
 #pragma unroll
@@ -158,11 +180,16 @@ __global__ void __launch_bounds__(D) gdn_kernel(const float *__restrict__ x, con
     const float alpha = exp_tree(-__fmul_rn(exp_tree(A_log[h]), softplus_tree(__fadd_rn(a[h], dt_bias[h]))));
     const float beta = sigmoid_tree(b[h]);
     __syncthreads();
+    // the state, staged: a bounded wait (on a timeout the status word records
+    // it and the block leaves its state and outputs untouched)
+    if constexpr (kStage) {
+        if (!mbar_wait(&bar, 0)) return;
+    }
+    const float *Src = kStage ? Ss : Sh;
     // the delta rule on column j of the head's state (S[i][j]: key i, value
     // j), its sums over the keys taken in blocks of 32 (the pairwise tree
     // over D is the tree over the blocks' trees)
     constexpr int NB = D / 32;
-    float *Sj = S + static_cast<int64_t>(h) * D * D + j;
     float bs[8];
 #pragma unroll 1
     for (int ib = 0; ib < NB; ++ib) {
@@ -170,7 +197,7 @@ __global__ void __launch_bounds__(D) gdn_kernel(const float *__restrict__ x, con
 #pragma unroll
         for (int t = 0; t < 32; ++t) {
             const int i = ib * 32 + t;
-            p[t] = __fmul_rn(__fmul_rn(Sj[static_cast<int64_t>(i) * D], alpha), kh_s[i]);
+            p[t] = __fmul_rn(__fmul_rn(Src[i * D + j], alpha), kh_s[i]);
         }
         bs[ib] = tree32v(p);
     }
@@ -181,9 +208,8 @@ __global__ void __launch_bounds__(D) gdn_kernel(const float *__restrict__ x, con
 #pragma unroll
         for (int t = 0; t < 32; ++t) {
             const int i = ib * 32 + t;
-            float *sp = Sj + static_cast<int64_t>(i) * D;
-            const float sv = __fadd_rn(__fmul_rn(*sp, alpha), __fmul_rn(kh_s[i], d));
-            *sp = sv;
+            const float sv = __fadd_rn(__fmul_rn(Src[i * D + j], alpha), __fmul_rn(kh_s[i], d));
+            Sh[static_cast<int64_t>(i) * D + j] = sv;
             p[t] = __fmul_rn(sv, qh_s[i]);
         }
         bs[ib] = tree32v(p);
@@ -203,26 +229,44 @@ __global__ void __launch_bounds__(D) gdn_kernel(const float *__restrict__ x, con
     if ((j & 63) == 0) ysum[yi >> 6] = __fadd_rn(red[j >> 5], red[(j >> 5) + 1]);
 }
 
+template <int D>
+cudaError_t launch_gdn_d(const float *x, const float *conv, float *state, const float *a, const float *b,
+                         const float *z, const float *A_log, const float *dt_bias, const float *nw, float *S,
+                         float *y, float *ysum, int H, int K, float eps, float eps_n, cudaStream_t stream) {
+    constexpr int kSmem = D <= 128 ? D * D * 4 : 0;
+    static const cudaError_t attr =
+        cudaFuncSetAttribute(gdn_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    if (attr != cudaSuccess) return attr;
+    gdn_kernel<D><<<H, D, kSmem, stream>>>(x, conv, state, a, b, z, A_log, dt_bias, nw, S, y, ysum, H, K, eps,
+                                           eps_n);
+    return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_gdn(const float *x, const float *conv, float *state, const float *a, const float *b,
                        const float *z, const float *A_log, const float *dt_bias, const float *nw, float *S, float *y,
                        float *ysum, int H, int D, int K, float eps, float eps_n, cudaStream_t stream) {
     switch (D) {
-    case 64:
-        gdn_kernel<64><<<H, 64, 0, stream>>>(x, conv, state, a, b, z, A_log, dt_bias, nw, S, y, ysum, H, K, eps, eps_n);
-        break;
+    case 64: return launch_gdn_d<64>(x, conv, state, a, b, z, A_log, dt_bias, nw, S, y, ysum, H, K, eps, eps_n, stream);
     case 128:
-        gdn_kernel<128><<<H, 128, 0, stream>>>(x, conv, state, a, b, z, A_log, dt_bias, nw, S, y, ysum, H, K, eps,
-                                               eps_n);
-        break;
+        return launch_gdn_d<128>(x, conv, state, a, b, z, A_log, dt_bias, nw, S, y, ysum, H, K, eps, eps_n, stream);
     case 256:
-        gdn_kernel<256><<<H, 256, 0, stream>>>(x, conv, state, a, b, z, A_log, dt_bias, nw, S, y, ysum, H, K, eps,
-                                               eps_n);
-        break;
+        return launch_gdn_d<256>(x, conv, state, a, b, z, A_log, dt_bias, nw, S, y, ysum, H, K, eps, eps_n, stream);
     default: return cudaErrorInvalidValue;
     }
-    return cudaGetLastError();
+}
+
+// This unit's device status word (OR-ed into *bits).
+cudaError_t mixer_status(unsigned *bits, bool clear) {
+    unsigned v = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&v, g_status, sizeof v);
+    if (e == cudaSuccess && clear && v) {
+        const unsigned zero = 0;
+        e = cudaMemcpyToSymbol(g_status, &zero, sizeof zero);
+    }
+    *bits |= v;
+    return e;
 }
 
 }  // namespace abg

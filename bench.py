@@ -299,6 +299,7 @@ def run_ours(args, rank, world):
         extra["formats"] = bench_formats(abg, stream, args, peak, l2)
         extra["batched"] = bench_batched(abg, stream, args)
         extra["pages_way"] = bench_pages_way(abg, stream, args)
+        extra["gdn"] = bench_gdn(abg, stream, args)
         extra["sweep"] = bench_sweep(abg, stream, args, peak, l2)
 
     res = dict(value=value, ms_step=ms_step, us_per_product=us_per_product, achieved=achieved,
@@ -515,6 +516,56 @@ def bench_pages_way(abg, stream, args):
             "us_per_call": round(us, 3), "gbs": round(product_bytes(MID_ROWS, MID_COLS) / (us * 1e-6) / 1e9, 1)}
 
 
+def bench_gdn(abg, stream, args):
+    """One token of the gated DeltaNet mixer (abg_gdn), 16 heads of 128 columns,
+    4 conv taps: calls back to back, each on its own copy of the state (S and
+    the conv state rotate over copies totalling more than L2), us per token;
+    the first call's outputs checked bit for bit against the oracle."""
+    import torch
+
+    import oracle
+    c = synth.gdn_case(np.random.default_rng(21))
+    H, D, K = c["S"].shape[0], c["S"].shape[1], c["conv"].shape[1]
+    d = {k: torch.from_numpy(np.ascontiguousarray(v)).cuda() for k, v in c.items()}
+    l2 = getattr(torch.cuda.get_device_properties(0), "L2_cache_size", 126 * 2 ** 20)
+    copies = max(2, math.ceil(1.5 * l2 / (c["S"].nbytes + c["state"].nbytes)))
+    Ss = [d["S"].clone() for _ in range(copies)]
+    sts = [d["state"].clone() for _ in range(copies)]
+    y = torch.empty(H * D, dtype=torch.float32, device="cuda")
+    ys = torch.empty(H * D // 64, dtype=torch.float32, device="cuda")
+    args_of = lambda i: (d["x"], d["conv"], sts[i], d["a"], d["b"], d["z"], d["A_log"], d["dt_bias"], d["nw"], Ss[i])
+    abg.gdn(*args_of(0), y, ys, stream=stream)
+    torch.cuda.synchronize()
+    ey, eys, eS, est = oracle.gdn(**c)
+    same = (np.array_equal(y.cpu().numpy().view(np.uint32), ey.view(np.uint32))
+            and np.array_equal(ys.cpu().numpy().view(np.uint32), eys.view(np.uint32))
+            and np.array_equal(Ss[0].cpu().numpy().view(np.uint32), eS.view(np.uint32))
+            and np.array_equal(sts[0].cpu().numpy().view(np.uint32), est.view(np.uint32)))
+    if not same:
+        raise SystemExit("gdn differs from the oracle")
+    reps = 200
+    for i in range(args.warmup * 10):
+        abg.gdn(*args_of(i % copies), y, ys, stream=stream)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(reps):
+        abg.gdn(*args_of(i % copies), y, ys, stream=stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / reps
+    # algorithmic bytes: S and the conv state read and written once, x, conv,
+    # z, the per-head scalars and the norm weights read, y and ysum written
+    nbytes = 2 * c["S"].nbytes + 2 * c["state"].nbytes + c["x"].nbytes + c["conv"].nbytes + c["z"].nbytes + \
+        4 * 4 * H + c["nw"].nbytes + 4 * H * D + 4 * H * D // 64
+    del Ss, sts
+    torch.cuda.empty_cache()
+    return {"workload": f"gdn mixer, one token: {H} heads x {D} columns, {K} conv taps; state rotating over "
+                        f"{copies} copies (> L2); calls back to back",
+            "us_per_token": round(us, 3), "bytes_per_token": int(nbytes),
+            "gbs": round(nbytes / (us * 1e-6) / 1e9, 1), "bit_exact": True}
+
+
 def bench_decode(abg, decode, stream, args):
     import torch
     model, h = synth.decode_model()
@@ -641,7 +692,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-extra", action="store_true", help="skip the head and decode-token measurements")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
-    ap.add_argument("--only", choices=["head", "decode", "formats", "batched", "sweep", "pages_way"], default=None,
+    ap.add_argument("--only", choices=["head", "decode", "formats", "batched", "sweep", "pages_way", "gdn"],
+                    default=None,
                     help="run one secondary workload alone and print its numbers (for profiling)")
     args = ap.parse_args()
     if args.only:
@@ -657,6 +709,8 @@ def main():
             out = bench_decode(abg, decode, stream, args)
         elif args.only == "batched":
             out = bench_batched(abg, stream, args)
+        elif args.only == "gdn":
+            out = bench_gdn(abg, stream, args)
         elif args.only == "pages_way":
             out = bench_pages_way(abg, stream, args)
         elif args.only == "sweep":

@@ -228,11 +228,12 @@ abg_status abg_swq_ex(const float *a, float *o, float *osum, int64_t n, int grou
  *   x        f32 [3*H*D] (q, then k, then v; head h's block at h*D)
  *   conv     f32 [3*H*D][K]         state  f32 [3*H*D][K-1], updated in place
  *   a, b, A_log, dt_bias f32 [H]    z      f32 [H*D]      nw  f32 [D]
- *   S        f32 [H][D][D] (key i, value j), updated in place
+ *   S        f32 [H][D][D] (key i, value j), updated in place; 16-byte aligned
  *   y        f32 [H*D]              ysum   f32 [H*D/64]
  *   D = 64, 128 or 256; 2 <= K <= 8; H >= 1, H*D <= 2^20.
  * Both modes compute the same bits.  Errors: null pointer or mode
- * ABG_EINVAL; shape ABG_ESHAPE; a pointer not 4-byte aligned ABG_EALIGN; an
+ * ABG_EINVAL; shape ABG_ESHAPE; a pointer not 4-byte aligned, or S not
+ * 16-byte aligned, ABG_EALIGN; an
  * output (state, S, y, ysum) overlapping an input or another output
  * ABG_EALIAS.  Asynchronous on `stream`.
  */

@@ -246,3 +246,6 @@ def test_gdn_rejects_before_device_work(lib):
     q = list(p)
     q[2] += 2                                     # state not 4-byte aligned
     assert call(q, **ok) == EALIGN
+    q = list(p)
+    q[9] += 4                                     # S not 16-byte aligned (one bulk copy per head)
+    assert call(q, **ok) == EALIGN
