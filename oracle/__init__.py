@@ -78,6 +78,8 @@ def _load():
             fl = ctypes.c_float
             lib.or_gdn.argtypes = [f32p, f32p, f32p, f32p, f32p, f32p, f32p, f32p, f32p, f32p, f32p, f32p,
                                    i64, i64, i64, fl, fl]
+            lib.or_atq.argtypes = [f32p, f32p, f32p, f32p, f32p, f32p, f32p, f32p, f32p, f32p, f32p, f32p,
+                                   i64, i64, i64, i64, i64, fl]
             _lib = lib
     return _lib
 
@@ -327,3 +329,34 @@ def gdn(x, conv, state, a, b, z, A_log, dt_bias, nw, S, eps=1e-6, eps_n=1e-6):
     _load().or_gdn(px, _f32(conv)[1], _f32(state)[1], pa, pb, pz, pA, pdt, pn, _f32(S)[1], _f32(y)[1],
                    _f32(ys)[1], H, D, K, ctypes.c_float(np.float32(eps)), ctypes.c_float(np.float32(eps_n)))
     return y, ys, S, state
+
+
+def atq(q, gate, k, v, qn_w, kn_w, cos, sin, Kc, Vc, pos: int, eps=1e-6):
+    """One token of gated attention at position pos (oracle.c or_atq): returns
+    (y, ysum, Kc_new, Vc_new) without touching the inputs.
+
+    Shapes: q, gate [Hq*D]; k, v [Hkv*D]; qn_w, kn_w [D]; cos, sin [D/2];
+    Kc, Vc [Hkv][P][D] with rows < pos filled.
+    """
+    Kc = np.array(Kc, dtype=np.float32, copy=True)
+    Vc = np.array(Vc, dtype=np.float32, copy=True)
+    Hkv, P, D = Kc.shape
+    q, pq = _f32(q)
+    Hq = q.size // D
+    if Vc.shape != Kc.shape or D % 64 or D > 1024 or q.size != Hq * D or Hq % Hkv or not 0 <= pos < P:
+        raise ValueError("bad atq shapes")
+    gate, pg = _f32(gate)
+    k, pk = _f32(k)
+    v, pv = _f32(v)
+    qn_w, pqn = _f32(qn_w)
+    kn_w, pkn = _f32(kn_w)
+    cos, pc = _f32(cos)
+    sin, ps = _f32(sin)
+    if gate.size != Hq * D or k.size != Hkv * D or v.size != Hkv * D or qn_w.size != D or kn_w.size != D or \
+            cos.size != D // 2 or sin.size != D // 2:
+        raise ValueError("bad atq shapes")
+    y = np.empty(Hq * D, np.float32)
+    ys = np.empty(Hq * D // 64, np.float32)
+    _load().or_atq(pq, pg, pk, pv, pqn, pkn, pc, ps, _f32(Kc)[1], _f32(Vc)[1], _f32(y)[1], _f32(ys)[1],
+                   Hq, Hkv, D, P, pos, ctypes.c_float(np.float32(eps)))
+    return y, ys, Kc, Vc

@@ -550,3 +550,82 @@ void or_gdn(const float *x, const float *conv, float *state, const float *a, con
     free(kh);
     free(o);
 }
+
+/* ------------------------------------------------------------------------ */
+/* atq: one token of gated attention over key and value caches.              */
+/* [fused-token] Change, the Array.atq bullet, lists the phases -- q/k RMS   */
+/* norm and rotation, the new k/v into the caches, scores, softmax, weighted */
+/* values, sigmoid gate and group sums -- with one threadgroup per query     */
+/* head; the first head of each KV group writes the cache row and the others */
+/* use the new k/v, so no head reads a row another head writes.  The page    */
+/* gives no formulas; the reading (grouped-query attention at position pos,  */
+/* Hq query heads sharing Hkv key/value heads, head dimension D, the         */
+/* rotation given as this position's cos/sin of each column pair):           */
+/*   RMS(u) = 1 / sqrt(TREE(u*u) / D + eps)                                  */
+/*   qn = (q_h * RMS(q_h)) * qn_w;  kn = (k_g * RMS(k_g)) * kn_w  (g = h/(Hq/Hkv)) */
+/*   rotation of pairs (i, i + D/2), i < D/2:                                */
+/*     r_i = u_i*cos_i - u_{i+D/2}*sin_i;  r_{i+D/2} = u_{i+D/2}*cos_i + u_i*sin_i */
+/*   Kc[g][pos] = rot(kn), Vc[g][pos] = v_g                                  */
+/*   s_t = TREE_j(rot(qn)_j * Kc[g][t][j]) * RN(1/RN(sqrt D)),  t = 0..pos    */
+/*   m = max_t s_t;  e_t = EXP(s_t - m);  p_t = e_t / TREE_t(e_t)             */
+/*   y_j = TREE_t(p_t * Vc[g][t][j]) * SIGMOID(gate_hj);  ysum = group sums  */
+/* Caches [Hkv][P][D], pos < P; D a multiple of 64, at most 1024.            */
+/* ------------------------------------------------------------------------ */
+static void or_rms_rot(const float *u, const float *w, const float *cs, const float *sn, float eps, int64_t D,
+                       float *tmp, float *out)
+{
+    for (int64_t i = 0; i < D; ++i) tmp[i] = u[i] * u[i];
+    const float mean = or_tree(tmp, D) / (float)D;
+    const float r = 1.0f / sqrtf(mean + eps);
+    for (int64_t i = 0; i < D; ++i) {
+        const float t = u[i] * r;
+        tmp[i] = t * w[i];
+    }
+    const int64_t h = D / 2;
+    for (int64_t i = 0; i < h; ++i) {
+        const float a = tmp[i] * cs[i], b = tmp[i + h] * sn[i];
+        const float c = tmp[i + h] * cs[i], d = tmp[i] * sn[i];
+        out[i] = a - b;
+        out[i + h] = c + d;
+    }
+}
+
+void or_atq(const float *q, const float *gate, const float *k, const float *v, const float *qn_w,
+            const float *kn_w, const float *cs, const float *sn, float *Kc, float *Vc, float *y, float *ysum,
+            int64_t Hq, int64_t Hkv, int64_t D, int64_t P, int64_t pos, float eps)
+{
+    const int64_t n = pos + 1, per = Hq / Hkv;
+    float *tmp = (float *)malloc((size_t)D * sizeof(float));
+    float *qr = (float *)malloc((size_t)D * sizeof(float));
+    float *s = (float *)malloc((size_t)n * sizeof(float));
+    float *pv = (float *)malloc((size_t)n * sizeof(float));
+    for (int64_t g = 0; g < Hkv; ++g) {
+        or_rms_rot(k + g * D, kn_w, cs, sn, eps, D, tmp, Kc + (g * P + pos) * D);
+        memcpy(Vc + (g * P + pos) * D, v + g * D, (size_t)D * sizeof(float));
+    }
+    const float scale = 1.0f / sqrtf((float)D);
+    for (int64_t h = 0; h < Hq; ++h) {
+        const int64_t g = h / per;
+        or_rms_rot(q + h * D, qn_w, cs, sn, eps, D, tmp, qr);
+        float m = -INFINITY;
+        for (int64_t t = 0; t < n; ++t) {
+            const float *kr = Kc + (g * P + t) * D;
+            for (int64_t j = 0; j < D; ++j) tmp[j] = qr[j] * kr[j];
+            s[t] = or_tree(tmp, D) * scale;
+            if (s[t] > m) m = s[t];
+        }
+        for (int64_t t = 0; t < n; ++t) s[t] = or_exp(s[t] - m);
+        const float Z = or_tree(s, n);
+        for (int64_t t = 0; t < n; ++t) s[t] = s[t] / Z;
+        for (int64_t j = 0; j < D; ++j) {
+            for (int64_t t = 0; t < n; ++t) pv[t] = s[t] * Vc[(g * P + t) * D + j];
+            const float o = or_tree(pv, n);
+            y[h * D + j] = o * or_sigmoid(gate[h * D + j]);
+        }
+    }
+    or_gsum(y, ysum, Hq * D);
+    free(tmp);
+    free(qr);
+    free(s);
+    free(pv);
+}
