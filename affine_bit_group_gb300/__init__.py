@@ -91,6 +91,7 @@ def library(build_if_missing: bool = True) -> ctypes.CDLL:
             lib.abg_stage_graph_destroy.argtypes = [P]
             F = ctypes.c_float
             lib.abg_gdn.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P, I64, I64, I64, F, F, I, P]
+            lib.abg_atq.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P, I64, I64, I64, I64, I64, F, I, P]
             lib.abg_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32), I]
             lib.abg_selftest_wait_timeout.argtypes = [P]
             lib.abg_set_q4mv_tuning.argtypes = [I, I, I, I]
@@ -101,7 +102,7 @@ def library(build_if_missing: bool = True) -> ctypes.CDLL:
             for f in ("abg_q4mv", "abg_q4mm", "abg_gsum", "abg_rmsq", "abg_swq", "abg_q4mv_ex", "abg_gsum_ex", "abg_rmsq_ex",
                       "abg_swq_ex", "abg_stage_graph_create",
                       "abg_stage_graph_launch", "abg_stage_graph_launches", "abg_stage_graph_swiglu_pairs",
-                      "abg_stage_graph_destroy", "abg_swiglu_mlp_static", "abg_gdn",
+                      "abg_stage_graph_destroy", "abg_swiglu_mlp_static", "abg_gdn", "abg_atq",
                       "abg_device_status", "abg_set_q4mv_tuning", "abg_selftest_wait_timeout"):
                 getattr(lib, f).restype = ctypes.c_int
             _lib = lib
@@ -212,6 +213,23 @@ def gdn(x, conv, state, a, b, z, A_log, dt_bias, nw, S, y, ysum, eps: float = 1e
         _ptr(y, f32, H * D, "y"), _ptr(ysum, f32, H * D // 64, "ysum"), H, D, K, ctypes.c_float(eps),
         ctypes.c_float(eps_n), mode, _stream(stream))
     _check(st, "abg_gdn")
+    return y
+
+
+def atq(q, gate, k, v, qn_w, kn_w, cos, sin, Kc, Vc, y, ysum, pos: int, eps: float = 1e-6, mode: int = TREE,
+        stream=None):
+    """One token of gated attention at position pos (see abg_atq): row pos of
+    Kc and Vc [Hkv][P][D] is written; y [Hq*D] and ysum [Hq*D/64] written."""
+    _, f32 = _dtypes()
+    Hkv, P, D = Kc.shape
+    Hq = q.numel() // D
+    st = library().abg_atq(
+        _ptr(q, f32, Hq * D, "q"), _ptr(gate, f32, Hq * D, "gate"), _ptr(k, f32, Hkv * D, "k"),
+        _ptr(v, f32, Hkv * D, "v"), _ptr(qn_w, f32, D, "qn_w"), _ptr(kn_w, f32, D, "kn_w"),
+        _ptr(cos, f32, D // 2, "cos"), _ptr(sin, f32, D // 2, "sin"), _ptr(Kc, f32, Hkv * P * D, "Kc"),
+        _ptr(Vc, f32, Hkv * P * D, "Vc"), _ptr(y, f32, Hq * D, "y"), _ptr(ysum, f32, Hq * D // 64, "ysum"),
+        Hq, Hkv, D, P, pos, ctypes.c_float(eps), mode, _stream(stream))
+    _check(st, "abg_atq")
     return y
 
 

@@ -515,6 +515,32 @@ abg_status abg_gdn(const float *x, const float *conv, float *state, const float 
                      "gdn launch");
 }
 
+abg_status abg_atq(const float *q, const float *gate, const float *k, const float *v, const float *qn_w,
+                   const float *kn_w, const float *cos, const float *sin, float *Kc, float *Vc, float *y, float *ysum,
+                   int64_t Hq, int64_t Hkv, int64_t D, int64_t P, int64_t pos, float eps, int mode, void *stream) {
+    if (mode != ABG_TREE && mode != ABG_FAST) return ABG_EINVAL;
+    if (!q || !gate || !k || !v || !qn_w || !kn_w || !cos || !sin || !Kc || !Vc || !y || !ysum) return ABG_EINVAL;
+    if (Hq < 1 || Hkv < 1 || Hq % Hkv || (D != 64 && D != 128 && D != 256) || pos < 0 || pos >= P ||
+        pos + 1 > 8192 || Hq * D > (int64_t(1) << 20))
+        return ABG_ESHAPE;
+    const void *all[] = {q, gate, k, v, qn_w, kn_w, cos, sin, Kc, Vc, y, ysum};
+    for (const void *p : all)
+        if (!aligned(p, 4)) return ABG_EALIGN;
+    const Range in[] = {rng(q, Hq * D, 4),  rng(gate, Hq * D, 4), rng(k, Hkv * D, 4), rng(v, Hkv * D, 4),
+                        rng(qn_w, D, 4),    rng(kn_w, D, 4),      rng(cos, D / 2, 4), rng(sin, D / 2, 4)};
+    const Range out[] = {rng(Kc, Hkv * P * D, 4), rng(Vc, Hkv * P * D, 4), rng(y, Hq * D, 4), rng(ysum, Hq * D / 64, 4)};
+    for (int i = 0; i < 4; ++i) {
+        for (const Range &r : in)
+            if (overlap(out[i], r)) return ABG_EALIAS;
+        for (int k2 = i + 1; k2 < 4; ++k2)
+            if (overlap(out[i], out[k2])) return ABG_EALIAS;
+    }
+    return cuda_fail(launch_atq(q, gate, k, v, qn_w, kn_w, cos, sin, Kc, Vc, y, ysum, static_cast<int>(Hq),
+                                static_cast<int>(Hkv), static_cast<int>(D), static_cast<int>(P), static_cast<int>(pos),
+                                eps, static_cast<cudaStream_t>(stream)),
+                     "atq launch");
+}
+
 abg_status abg_stage_graph_create(const abg_node *nodes, int64_t count, int mode, int rows_per_warp,
                                   void **graph_out) {
     if (!graph_out) return ABG_EINVAL;

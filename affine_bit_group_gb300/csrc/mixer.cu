@@ -242,6 +242,172 @@ cudaError_t launch_gdn_d(const float *x, const float *conv, float *state, const 
     return cudaGetLastError();
 }
 
+// ------------------------------------------------------------------ atq ----
+// One token of gated attention ("Metal: queued rmsq, swq, gdn and atq
+// kernels ...", Change, the Array.atq bullet: q/k RMS norm and rotation, the
+// new k/v into the caches, scores, softmax, weighted values, sigmoid gate and
+// group sums; one threadgroup per query head, the first head of each KV group
+// writing the cache row while the others use the new k/v).
+//
+// One block per query head, one thread per column j (D threads).  Sums over
+// the positions t = 0..pos (pos + 1 of them, the pairwise tree with an odd
+// element carried) are taken over blocks of 32 positions padded with -0,
+// then over the blocks' sums padded with -0 to a power of two: carrying an
+// element is adding -0, so this is the same tree.
+constexpr int kAtqMaxPositions = 8192;
+
+// The block's maximum of one value per thread (exact in any order).
+template <int D>
+__device__ __forceinline__ float block_max(float v, float *red) {
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, d));
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+    __syncthreads();
+    float m = red[0];
+#pragma unroll
+    for (int i = 1; i < D / 32; ++i) m = fmaxf(m, red[i]);
+    __syncthreads();
+    return m;
+}
+
+// RMS norm with weights, then the rotation of column pairs (i, i + D/2):
+// thread j's rotated value.  `un` (D floats of shared memory) carries the
+// normed values between the threads.
+template <int D>
+__device__ __forceinline__ float rms_rotate(float u, float w, const float *cs, const float *sn, float eps,
+                                            float *un, float *red) {
+    const int j = threadIdx.x;
+    const float mean = __fdiv_rn(block_tree<D>(__fmul_rn(u, u), red), static_cast<float>(D));
+    const float r = __frcp_rn(__fsqrt_rn(__fadd_rn(mean, eps)));
+    un[j] = __fmul_rn(__fmul_rn(u, r), w);
+    __syncthreads();
+    float out;
+    if (j < D / 2) {
+        out = __fsub_rn(__fmul_rn(un[j], cs[j]), __fmul_rn(un[j + D / 2], sn[j]));
+    } else {
+        const int i = j - D / 2;
+        out = __fadd_rn(__fmul_rn(un[j], cs[i]), __fmul_rn(un[i], sn[i]));
+    }
+    __syncthreads();  // un is reused
+    return out;
+}
+
+template <int D>
+__global__ void __launch_bounds__(D) atq_kernel(const float *__restrict__ q, const float *__restrict__ gate,
+                                                const float *__restrict__ k, const float *__restrict__ v,
+                                                const float *__restrict__ qn_w, const float *__restrict__ kn_w,
+                                                const float *__restrict__ cs, const float *__restrict__ sn,
+                                                float *Kc, float *Vc, float *y, float *ysum, int Hq, int Hkv, int P,
+                                                int pos, float eps) {
+    constexpr int NW = D / 32, CPL = D / 32;  // warps; columns per lane in a score
+    extern __shared__ float sc[];            // scores, then probabilities (pos + 1)
+    __shared__ float un[D], qr_s[D], kr_s[D], vn_s[D];
+    __shared__ float red[NW];
+    __shared__ float bs[2][kAtqMaxPositions / 32];
+    const int h = blockIdx.x, j = threadIdx.x, warp = j >> 5, lane = j & 31;
+    const int g = h / (Hq / Hkv);
+    const int n = pos + 1;
+    const float *Kg = Kc + static_cast<int64_t>(g) * P * D;
+    const float *Vg = Vc + static_cast<int64_t>(g) * P * D;
+    // normed, rotated query and key; the new value
+    const float qr = rms_rotate<D>(q[static_cast<int64_t>(h) * D + j], qn_w[j], cs, sn, eps, un, red);
+    const float kr = rms_rotate<D>(k[static_cast<int64_t>(g) * D + j], kn_w[j], cs, sn, eps, un, red);
+    const float vn = v[static_cast<int64_t>(g) * D + j];
+    qr_s[j] = qr;
+    kr_s[j] = kr;
+    vn_s[j] = vn;
+    if (h % (Hq / Hkv) == 0) {  // the first head of the group appends the row
+        Kc[(static_cast<int64_t>(g) * P + pos) * D + j] = kr;
+        Vc[(static_cast<int64_t>(g) * P + pos) * D + j] = vn;
+    }
+    __syncthreads();
+    // scores: warp w takes positions w, w + NW, ...; lane l the columns
+    // l*CPL .. l*CPL + CPL-1 (their tree, then the butterfly: the tree over D)
+    const float scale = __frcp_rn(__fsqrt_rn(static_cast<float>(D)));
+    for (int t = warp; t < n; t += NW) {
+        const float *kt = t == pos ? kr_s : Kg + static_cast<int64_t>(t) * D;
+        float pr[CPL];
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) pr[c] = __fmul_rn(qr_s[lane * CPL + c], kt[lane * CPL + c]);
+#pragma unroll
+        for (int hh = CPL / 2; hh >= 1; hh >>= 1)
+#pragma unroll
+            for (int c = 0; c < hh; ++c) pr[c] = __fadd_rn(pr[2 * c], pr[2 * c + 1]);
+        float dot = pr[0];
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) dot = __fadd_rn(dot, __shfl_xor_sync(0xffffffffu, dot, d));
+        if (lane == 0) sc[t] = __fmul_rn(dot, scale);
+    }
+    __syncthreads();
+    // softmax
+    float mx = -__int_as_float(0x7f800000);
+    for (int t = j; t < n; t += D) mx = fmaxf(mx, sc[t]);
+    const float m = block_max<D>(mx, red);
+    for (int t = j; t < n; t += D) sc[t] = exp_tree(__fsub_rn(sc[t], m));
+    __syncthreads();
+    const int nb = (n + 31) / 32;
+    int p2 = 1;
+    while (p2 < nb) p2 <<= 1;
+    for (int b = j; b < p2; b += D) {
+        float e[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) e[i] = (b < nb && 32 * b + i < n) ? sc[32 * b + i] : -0.0f;
+        bs[0][b] = tree32v(e);
+    }
+    __syncthreads();
+    int cur = 0;
+    for (int half = p2 / 2; half >= 1; half >>= 1) {
+        for (int b = j; b < half; b += D) bs[cur ^ 1][b] = __fadd_rn(bs[cur][2 * b], bs[cur][2 * b + 1]);
+        cur ^= 1;
+        __syncthreads();
+    }
+    const float Z = bs[cur][0];
+    for (int t = j; t < n; t += D) sc[t] = __fdiv_rn(sc[t], Z);
+    __syncthreads();
+    // weighted values of column j: blocks of 32 positions, their sums combined
+    // by a running pairwise tree over p2 blocks (-0 past the last)
+    float lv[10];
+    for (int b = 0; b < p2; ++b) {
+        float blk = -0.0f;
+        if (b < nb) {
+            float e[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const int t = 32 * b + i;
+                e[i] = t < n ? __fmul_rn(sc[t], t == pos ? vn_s[j] : Vg[static_cast<int64_t>(t) * D + j]) : -0.0f;
+            }
+            blk = tree32v(e);
+        }
+        int l = 0;
+        while ((b >> l) & 1) {
+            blk = __fadd_rn(lv[l], blk);
+            ++l;
+        }
+        lv[l] = blk;
+    }
+    int top = 0;
+    while ((1 << top) < p2) ++top;
+    const float o = lv[top];
+    const int64_t yi = static_cast<int64_t>(h) * D + j;
+    const float yv = __fmul_rn(o, sigmoid_tree(gate[yi]));
+    y[yi] = yv;
+    float gsm = yv;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) gsm = __fadd_rn(gsm, __shfl_xor_sync(0xffffffffu, gsm, d));
+    if (lane == 0) red[warp] = gsm;
+    __syncthreads();
+    if ((j & 63) == 0) ysum[yi >> 6] = __fadd_rn(red[warp], red[warp + 1]);
+}
+
+template <int D>
+cudaError_t launch_atq_d(const float *q, const float *gate, const float *k, const float *v, const float *qn_w,
+                         const float *kn_w, const float *cs, const float *sn, float *Kc, float *Vc, float *y,
+                         float *ysum, int Hq, int Hkv, int P, int pos, float eps, cudaStream_t stream) {
+    atq_kernel<D><<<Hq, D, static_cast<size_t>(pos + 1) * 4, stream>>>(q, gate, k, v, qn_w, kn_w, cs, sn, Kc, Vc,
+                                                                       y, ysum, Hq, Hkv, P, pos, eps);
+    return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_gdn(const float *x, const float *conv, float *state, const float *a, const float *b,
@@ -253,6 +419,20 @@ cudaError_t launch_gdn(const float *x, const float *conv, float *state, const fl
         return launch_gdn_d<128>(x, conv, state, a, b, z, A_log, dt_bias, nw, S, y, ysum, H, K, eps, eps_n, stream);
     case 256:
         return launch_gdn_d<256>(x, conv, state, a, b, z, A_log, dt_bias, nw, S, y, ysum, H, K, eps, eps_n, stream);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t launch_atq(const float *q, const float *gate, const float *k, const float *v, const float *qn_w,
+                       const float *kn_w, const float *cs, const float *sn, float *Kc, float *Vc, float *y,
+                       float *ysum, int Hq, int Hkv, int D, int P, int pos, float eps, cudaStream_t stream) {
+    if (pos + 1 > kAtqMaxPositions) return cudaErrorInvalidValue;
+    switch (D) {
+    case 64: return launch_atq_d<64>(q, gate, k, v, qn_w, kn_w, cs, sn, Kc, Vc, y, ysum, Hq, Hkv, P, pos, eps, stream);
+    case 128:
+        return launch_atq_d<128>(q, gate, k, v, qn_w, kn_w, cs, sn, Kc, Vc, y, ysum, Hq, Hkv, P, pos, eps, stream);
+    case 256:
+        return launch_atq_d<256>(q, gate, k, v, qn_w, kn_w, cs, sn, Kc, Vc, y, ysum, Hq, Hkv, P, pos, eps, stream);
     default: return cudaErrorInvalidValue;
     }
 }

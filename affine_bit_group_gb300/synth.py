@@ -224,3 +224,33 @@ def gdn_case(rng: np.random.Generator, H: int = GDN_HEADS, D: int = GDN_DIM, K: 
                 dt_bias=(0.5 * rng.standard_normal(H)).astype(np.float32),
                 nw=(1.0 + 0.1 * rng.standard_normal(D)).astype(np.float32),
                 S=(0.1 * rng.standard_normal((H, D, D))).astype(np.float32))
+
+
+# The gated attention token: 8 query heads over 2 key/value heads of 256
+# columns, caches of 4096 positions, a mid-context position (the pages give
+# no dimensions; Metal's kernel handled positions below 4096).
+ATQ_QHEADS = 8
+ATQ_KVHEADS = 2
+ATQ_DIM = 256
+ATQ_CACHE = 4096
+ATQ_POS = 2047
+
+
+def atq_case(rng: np.random.Generator, Hq: int = ATQ_QHEADS, Hkv: int = ATQ_KVHEADS, D: int = ATQ_DIM,
+             P: int = ATQ_CACHE, pos: int = ATQ_POS) -> dict:
+    """Inputs of one atq token (names as abg_atq): q, gate, k, v ~ N(0,1);
+    qn_w, kn_w ~ 1 + N(0, 0.1); cos, sin of angles uniform on [0, 2 pi) per
+    column pair; cache rows below pos ~ N(0,1) (rows pos.. zero), float32."""
+    ang = rng.uniform(0.0, 2.0 * np.pi, D // 2)
+    Kc = np.zeros((Hkv, P, D), np.float32)
+    Vc = np.zeros((Hkv, P, D), np.float32)
+    Kc[:, :pos] = rng.standard_normal((Hkv, pos, D))
+    Vc[:, :pos] = rng.standard_normal((Hkv, pos, D))
+    return dict(q=rng.standard_normal(Hq * D).astype(np.float32),
+                gate=rng.standard_normal(Hq * D).astype(np.float32),
+                k=rng.standard_normal(Hkv * D).astype(np.float32),
+                v=rng.standard_normal(Hkv * D).astype(np.float32),
+                qn_w=(1.0 + 0.1 * rng.standard_normal(D)).astype(np.float32),
+                kn_w=(1.0 + 0.1 * rng.standard_normal(D)).astype(np.float32),
+                cos=np.cos(ang).astype(np.float32), sin=np.sin(ang).astype(np.float32),
+                Kc=Kc, Vc=Vc, pos=pos)

@@ -241,6 +241,39 @@ abg_status abg_gdn(const float *x, const float *conv, float *state, const float 
                    const float *A_log, const float *dt_bias, const float *nw, float *S, float *y, float *ysum,
                    int64_t H, int64_t D, int64_t K, float eps, float eps_n, int mode, void *stream);
 
+/*
+ * atq: one token of gated attention over key and value caches ([fused-token]
+ * Change, Array.atq bullet: q/k RMS norm and rotation, the new k/v into the
+ * caches, scores, softmax, weighted values, sigmoid gate and group sums; one
+ * threadgroup per query head, the first head of each KV group writing the
+ * cache row while the others use the new k/v).  The page gives no formulas;
+ * this is grouped-query attention at position pos (query head h reads
+ * key/value head h / (Hq/Hkv)) with the library's steps (one RN binary32 op
+ * each, pairwise trees, EXP and SIGMOID as in gdn):
+ *   RMS(u) = 1/sqrt(tree(u*u)/D + eps);  qn = (q_h*RMS(q_h))*qn_w,
+ *     kn = (k_g*RMS(k_g))*kn_w
+ *   rotation of column pairs (i, i + D/2) by this position's cos_i, sin_i:
+ *     r_i = u_i*cos_i - u_{i+D/2}*sin_i, r_{i+D/2} = u_{i+D/2}*cos_i + u_i*sin_i
+ *   Kc[g][pos] = rot(kn), Vc[g][pos] = v_g
+ *   s_t = tree_j(rot(qn)_j*Kc[g][t][j]) * RN(1/sqrt D), t = 0..pos
+ *   p_t = EXP(s_t - max s) / tree_t EXP(s_t - max s)
+ *   y_j = tree_t(p_t*Vc[g][t][j]) * SIGMOID(gate[h*D+j]);  ysum = 64-value
+ *   group sums of y
+ *   q, gate  f32 [Hq*D]    k, v  f32 [Hkv*D]    qn_w, kn_w  f32 [D]
+ *   cos, sin f32 [D/2]     Kc, Vc f32 [Hkv][P][D], rows < pos filled; row pos
+ *                          written (by the call)
+ *   y        f32 [Hq*D]    ysum  f32 [Hq*D/64]
+ *   D = 64, 128 or 256; Hq a multiple of Hkv; 0 <= pos < P; pos + 1 <= 8192
+ *   (the scores of one head stay in shared memory); Hq*D <= 2^20.
+ * Both modes compute the same bits.  Errors: null pointer or mode ABG_EINVAL;
+ * shape ABG_ESHAPE; a pointer not 4-byte aligned ABG_EALIGN; an output (Kc,
+ * Vc, y, ysum) overlapping an input or another output ABG_EALIAS.
+ * Asynchronous on `stream`.
+ */
+abg_status abg_atq(const float *q, const float *gate, const float *k, const float *v, const float *qn_w,
+                   const float *kn_w, const float *cos, const float *sin, float *Kc, float *Vc, float *y, float *ysum,
+                   int64_t Hq, int64_t Hkv, int64_t D, int64_t P, int64_t pos, float eps, int mode, void *stream);
+
 /* ---------------------------------------------------------------------------
  * Stage graph: one decode token's dependent stages recorded into one CUDA
  * graph, replayed with one launch and synchronized once by the caller

@@ -249,3 +249,31 @@ def test_gdn_rejects_before_device_work(lib):
     q = list(p)
     q[9] += 4                                     # S not 16-byte aligned (one bulk copy per head)
     assert call(q, **ok) == EALIGN
+
+
+def test_atq_rejects_before_device_work(lib):
+    """abg_atq checks its shape (including the 8192-position limit), mode,
+    alignment and output overlaps before any device work."""
+    f = lib.abg_atq
+    p = [0x7F0000100000 + (1 << 28) * i for i in range(12)]
+    F = ctypes.c_float
+
+    def call(ptrs, Hq=8, Hkv=2, D=256, P=4096, pos=100, mode=0):
+        return f(*ptrs, Hq, Hkv, D, P, pos, F(1e-6), mode, None)
+
+    assert call(p, Hq=6, Hkv=4) == ESHAPE        # query heads not a multiple of the kv heads
+    assert call(p, D=96) == ESHAPE
+    assert call(p, pos=4096) == ESHAPE           # pos past the cache
+    assert call(p, P=10000, pos=8192) == ESHAPE  # past the position limit
+    assert call(p, pos=-1) == ESHAPE
+    assert call(p, mode=5) == EINVAL
+    assert call([None] + p[1:]) == EINVAL
+    q = list(p)
+    q[10] = p[0]                                 # y over q
+    assert call(q) == EALIAS
+    q = list(p)
+    q[9] = p[8]                                  # V cache over K cache
+    assert call(q) == EALIAS
+    q = list(p)
+    q[8] += 2
+    assert call(q) == EALIGN

@@ -69,3 +69,35 @@ def test_gdn_gate_and_decay_edges():
     c["conv"][5 * D:6 * D] = 0.0
     c["conv"][5 * D:6 * D, K - 1] = 1.0
     run_gdn(c)
+
+
+def run_atq(c, tokens=1):
+    """Runs tokens at positions pos, pos+1, ... (same q, k, v) on the device and
+    in the oracle, comparing y, ysum and both caches after each."""
+    d = {k: dev(v) for k, v in c.items() if k != "pos"}
+    Hkv, P, D = c["Kc"].shape
+    Hq = c["q"].size // D
+    Kr, Vr = c["Kc"], c["Vc"]
+    for t in range(tokens):
+        pos = c["pos"] + t
+        y, ys = empty(Hq * D), empty(Hq * D // 64)
+        abg.atq(d["q"], d["gate"], d["k"], d["v"], d["qn_w"], d["kn_w"], d["cos"], d["sin"], d["Kc"], d["Vc"], y, ys,
+                pos=pos)
+        torch.cuda.synchronize()
+        ey, eys, Kr, Vr = oracle.atq(**dict(c, Kc=Kr, Vc=Vr, pos=pos))
+        assert_bits_equal(host(y), ey, f"y at {pos}")
+        assert_bits_equal(host(ys), eys, f"ysum at {pos}")
+        assert_bits_equal(host(d["Kc"]).reshape(Kr.shape), Kr, f"K cache at {pos}")
+        assert_bits_equal(host(d["Vc"]).reshape(Vr.shape), Vr, f"V cache at {pos}")
+    assert abg.device_status(clear=True) == 0
+
+
+@pytest.mark.parametrize("Hq,Hkv,D,P,pos", [(8, 2, 256, 4096, 2047), (4, 4, 64, 64, 0), (4, 2, 128, 300, 31),
+                                            (4, 2, 128, 300, 32), (6, 3, 64, 200, 33), (2, 1, 256, 8192, 8191),
+                                            (8, 1, 128, 5000, 1000)])
+def test_atq_bit_exact(Hq, Hkv, D, P, pos):
+    run_atq(synth.atq_case(np.random.default_rng([Hq, Hkv, D, P, pos]), Hq, Hkv, D, P, pos))
+
+
+def test_atq_tokens_append_rows():
+    run_atq(synth.atq_case(np.random.default_rng(5), 4, 2, 128, 256, 60), tokens=5)
