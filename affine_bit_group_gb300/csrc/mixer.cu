@@ -21,6 +21,8 @@
 #include "abg_dev.cuh"
 #include "abg_kernels.cuh"
 
+#include <mutex>
+
 namespace abg {
 
 namespace {
@@ -249,14 +251,20 @@ cudaError_t launch_gdn_d(const float *x, const float *conv, float *state, const 
 // group sums; one threadgroup per query head, the first head of each KV group
 // writing the cache row while the others use the new k/v).
 //
-// One block per query head, one thread per column j (D threads).  Sums over
-// the positions t = 0..pos (pos + 1 of them, the pairwise tree with an odd
-// element carried) are taken over blocks of 32 positions padded with -0,
-// then over the blocks' sums padded with -0 to a power of two: carrying an
-// element is adding -0, so this is the same tree.
+// The positions t = 0..pos are split into chunks of 256 (one block per query
+// head and chunk), in four launches on the stream: scores and the
+// chunk's maximum; the exponentials and the chunk's sum; the probabilities
+// and the chunk's weighted values; the tree over the chunks, the gate and the
+// group sums.  Every sum over positions is the pairwise tree with an odd
+// element carried, which equals the tree over the positions padded with -0
+// to a power of two (carrying is adding -0); the padded tree's subtrees are
+// the aligned 32-position blocks and 256-position chunks, so the chunks'
+// sums, combined by the tree, give the oracle's bits.
 constexpr int kAtqMaxPositions = 8192;
+constexpr int kAtqChunk = 256;
+constexpr int kAtqMaxChunks = kAtqMaxPositions / kAtqChunk;
 
-// The block's maximum of one value per thread (exact in any order).
+// The maximum over the block's D threads (exact in any order).
 template <int D>
 __device__ __forceinline__ float block_max(float v, float *red) {
 #pragma unroll
@@ -292,120 +300,279 @@ __device__ __forceinline__ float rms_rotate(float u, float w, const float *cs, c
     return out;
 }
 
+// The same two steps in a block wider than D: only threads j < D hold a
+// column (the others pass 0 and get 0); every thread of the block calls them.
 template <int D>
-__global__ void __launch_bounds__(D) atq_kernel(const float *__restrict__ q, const float *__restrict__ gate,
-                                                const float *__restrict__ k, const float *__restrict__ v,
-                                                const float *__restrict__ qn_w, const float *__restrict__ kn_w,
-                                                const float *__restrict__ cs, const float *__restrict__ sn,
-                                                float *Kc, float *Vc, float *y, float *ysum, int Hq, int Hkv, int P,
-                                                int pos, float eps) {
-    constexpr int NW = D / 32, CPL = D / 32;  // warps; columns per lane in a score
-    extern __shared__ float sc[];            // scores, then probabilities (pos + 1)
-    __shared__ float un[D], qr_s[D], kr_s[D], vn_s[D];
-    __shared__ float red[NW];
-    __shared__ float bs[2][kAtqMaxPositions / 32];
-    const int h = blockIdx.x, j = threadIdx.x, warp = j >> 5, lane = j & 31;
-    const int g = h / (Hq / Hkv);
-    const int n = pos + 1;
-    const float *Kg = Kc + static_cast<int64_t>(g) * P * D;
-    const float *Vg = Vc + static_cast<int64_t>(g) * P * D;
-    // normed, rotated query and key; the new value
-    const float qr = rms_rotate<D>(q[static_cast<int64_t>(h) * D + j], qn_w[j], cs, sn, eps, un, red);
-    const float kr = rms_rotate<D>(k[static_cast<int64_t>(g) * D + j], kn_w[j], cs, sn, eps, un, red);
-    const float vn = v[static_cast<int64_t>(g) * D + j];
-    qr_s[j] = qr;
-    kr_s[j] = kr;
-    vn_s[j] = vn;
-    if (h % (Hq / Hkv) == 0) {  // the first head of the group appends the row
-        Kc[(static_cast<int64_t>(g) * P + pos) * D + j] = kr;
-        Vc[(static_cast<int64_t>(g) * P + pos) * D + j] = vn;
-    }
+__device__ __forceinline__ float block_tree_first(float v, float *red) {
+    constexpr int NW = D / 32;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, d));
+    if ((threadIdx.x & 31) == 0 && (threadIdx.x >> 5) < NW) red[threadIdx.x >> 5] = v;
     __syncthreads();
-    // scores: warp w takes positions w, w + NW, ...; lane l the columns
-    // l*CPL .. l*CPL + CPL-1 (their tree, then the butterfly: the tree over D)
-    const float scale = __frcp_rn(__fsqrt_rn(static_cast<float>(D)));
-    for (int t = warp; t < n; t += NW) {
-        const float *kt = t == pos ? kr_s : Kg + static_cast<int64_t>(t) * D;
-        float pr[CPL];
+    float w[NW];
 #pragma unroll
-        for (int c = 0; c < CPL; ++c) pr[c] = __fmul_rn(qr_s[lane * CPL + c], kt[lane * CPL + c]);
+    for (int i = 0; i < NW; ++i) w[i] = red[i];
 #pragma unroll
-        for (int hh = CPL / 2; hh >= 1; hh >>= 1)
+    for (int h = NW / 2; h >= 1; h >>= 1)
 #pragma unroll
-            for (int c = 0; c < hh; ++c) pr[c] = __fadd_rn(pr[2 * c], pr[2 * c + 1]);
-        float dot = pr[0];
-#pragma unroll
-        for (int d = 1; d < 32; d <<= 1) dot = __fadd_rn(dot, __shfl_xor_sync(0xffffffffu, dot, d));
-        if (lane == 0) sc[t] = __fmul_rn(dot, scale);
-    }
+        for (int i = 0; i < h; ++i) w[i] = __fadd_rn(w[2 * i], w[2 * i + 1]);
     __syncthreads();
-    // softmax
-    float mx = -__int_as_float(0x7f800000);
-    for (int t = j; t < n; t += D) mx = fmaxf(mx, sc[t]);
-    const float m = block_max<D>(mx, red);
-    for (int t = j; t < n; t += D) sc[t] = exp_tree(__fsub_rn(sc[t], m));
-    __syncthreads();
-    const int nb = (n + 31) / 32;
-    int p2 = 1;
-    while (p2 < nb) p2 <<= 1;
-    for (int b = j; b < p2; b += D) {
-        float e[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) e[i] = (b < nb && 32 * b + i < n) ? sc[32 * b + i] : -0.0f;
-        bs[0][b] = tree32v(e);
-    }
-    __syncthreads();
-    int cur = 0;
-    for (int half = p2 / 2; half >= 1; half >>= 1) {
-        for (int b = j; b < half; b += D) bs[cur ^ 1][b] = __fadd_rn(bs[cur][2 * b], bs[cur][2 * b + 1]);
-        cur ^= 1;
-        __syncthreads();
-    }
-    const float Z = bs[cur][0];
-    for (int t = j; t < n; t += D) sc[t] = __fdiv_rn(sc[t], Z);
-    __syncthreads();
-    // weighted values of column j: blocks of 32 positions, their sums combined
-    // by a running pairwise tree over p2 blocks (-0 past the last)
-    float lv[10];
-    for (int b = 0; b < p2; ++b) {
-        float blk = -0.0f;
-        if (b < nb) {
-            float e[32];
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const int t = 32 * b + i;
-                e[i] = t < n ? __fmul_rn(sc[t], t == pos ? vn_s[j] : Vg[static_cast<int64_t>(t) * D + j]) : -0.0f;
-            }
-            blk = tree32v(e);
-        }
-        int l = 0;
-        while ((b >> l) & 1) {
-            blk = __fadd_rn(lv[l], blk);
-            ++l;
-        }
-        lv[l] = blk;
-    }
-    int top = 0;
-    while ((1 << top) < p2) ++top;
-    const float o = lv[top];
-    const int64_t yi = static_cast<int64_t>(h) * D + j;
-    const float yv = __fmul_rn(o, sigmoid_tree(gate[yi]));
-    y[yi] = yv;
-    float gsm = yv;
-#pragma unroll
-    for (int d = 1; d < 32; d <<= 1) gsm = __fadd_rn(gsm, __shfl_xor_sync(0xffffffffu, gsm, d));
-    if (lane == 0) red[warp] = gsm;
-    __syncthreads();
-    if ((j & 63) == 0) ysum[yi >> 6] = __fadd_rn(red[warp], red[warp + 1]);
+    return w[0];
 }
 
 template <int D>
-cudaError_t launch_atq_d(const float *q, const float *gate, const float *k, const float *v, const float *qn_w,
-                         const float *kn_w, const float *cs, const float *sn, float *Kc, float *Vc, float *y,
-                         float *ysum, int Hq, int Hkv, int P, int pos, float eps, cudaStream_t stream) {
-    atq_kernel<D><<<Hq, D, static_cast<size_t>(pos + 1) * 4, stream>>>(q, gate, k, v, qn_w, kn_w, cs, sn, Kc, Vc,
-                                                                       y, ysum, Hq, Hkv, P, pos, eps);
+__device__ __forceinline__ float rms_rotate_first(float u, float w, const float *cs, const float *sn, float eps,
+                                                  float *un, float *red) {
+    const int j = threadIdx.x;
+    const float mean = __fdiv_rn(block_tree_first<D>(__fmul_rn(u, u), red), static_cast<float>(D));
+    const float r = __frcp_rn(__fsqrt_rn(__fadd_rn(mean, eps)));
+    if (j < D) un[j] = __fmul_rn(__fmul_rn(u, r), w);
+    __syncthreads();
+    float out = 0.0f;
+    if (j < D / 2) {
+        out = __fsub_rn(__fmul_rn(un[j], cs[j]), __fmul_rn(un[j + D / 2], sn[j]));
+    } else if (j < D) {
+        const int i = j - D / 2;
+        out = __fadd_rn(__fmul_rn(un[j], cs[i]), __fmul_rn(un[i], sn[i]));
+    }
+    __syncthreads();
+    return out;
+}
+
+// The pairwise tree over v[0 .. m), padded with -0 to a power of two (m <= 32).
+__device__ __forceinline__ float tree_padded32(const float *v, int m) {
+    float e[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) e[i] = i < m ? v[i] : -0.0f;
+    int p = 1;
+    while (p < m) p <<= 1;
+    for (int h = p / 2; h >= 1; h >>= 1)
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+            if (i < h) e[i] = __fadd_rn(e[2 * i], e[2 * i + 1]);
+    return e[0];
+}
+
+struct AtqArgs {
+    const float *q, *gate, *k, *v, *qn_w, *kn_w, *cs, *sn;
+    float *Kc, *Vc, *y, *ysum;
+    float *sc;    // [Hq][C*256] scores, then exponentials
+    float *cmax;  // [Hq][C] the chunks' maxima
+    float *csum;  // [Hq][C] the chunks' sums of exponentials
+    float *opart; // [Hq][C][D] the chunks' weighted values
+    int Hq, Hkv, P, pos, C;
+    float eps;
+};
+
+// 1: the rotated query (and key), the cache row (written by the group's first
+// head, in the chunk holding pos), the chunk's scores and their maximum.  32
+// warps, 8 rows each: the chunk's 256 rows are loaded in one step.
+constexpr int kAtqScoreThreads = 1024;
+
+template <int D>
+__global__ void __launch_bounds__(kAtqScoreThreads) atq_scores_kernel(const __grid_constant__ AtqArgs a) {
+    constexpr int NW = kAtqScoreThreads / 32, CPL = D / 32, kRows = kAtqChunk / NW;
+    __shared__ float un[D], qr_s[D], kr_s[D];
+    __shared__ float red[NW];
+    const int h = blockIdx.x, c = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int j = tid < D ? tid : 0;
+    const int g = h / (a.Hq / a.Hkv), n = a.pos + 1;
+    const float qr = rms_rotate_first<D>(tid < D ? a.q[static_cast<int64_t>(h) * D + j] : 0.0f, a.qn_w[j], a.cs,
+                                         a.sn, a.eps, un, red);
+    const float kr = rms_rotate_first<D>(tid < D ? a.k[static_cast<int64_t>(g) * D + j] : 0.0f, a.kn_w[j], a.cs,
+                                         a.sn, a.eps, un, red);
+    if (tid < D) {
+        qr_s[j] = qr;
+        kr_s[j] = kr;
+        if (h % (a.Hq / a.Hkv) == 0 && c == a.C - 1) {
+            a.Kc[(static_cast<int64_t>(g) * a.P + a.pos) * D + j] = kr;
+            a.Vc[(static_cast<int64_t>(g) * a.P + a.pos) * D + j] = a.v[static_cast<int64_t>(g) * D + j];
+        }
+    }
+    __syncthreads();
+    // warp w takes rows t_lo + kRows*w ..; lane l the columns l*CPL .. l*CPL +
+    // CPL-1 (their tree, then the butterfly: the tree over D).  Row pos is this
+    // block's own key (the cache row may be written by another block).
+    const float *Kg = a.Kc + static_cast<int64_t>(g) * a.P * D;
+    const float scale = __frcp_rn(__fsqrt_rn(static_cast<float>(D)));
+    const int t_lo = c * kAtqChunk, t_hi = min(t_lo + kAtqChunk, n);
+    float mx = -__int_as_float(0x7f800000);
+    // (at most 32 loaded values a lane at a time: 64 registers a thread)
+    constexpr int kPass = 32 / CPL < kRows ? 32 / CPL : kRows;
+#pragma unroll
+    for (int r0 = 0; r0 < kRows; r0 += kPass) {
+        const int t0 = t_lo + warp * kRows + r0;
+        float kv[kPass][CPL];
+#pragma unroll
+        for (int r = 0; r < kPass; ++r) {
+            const int t = t0 + r;
+            const float *kt = t == a.pos ? kr_s : Kg + static_cast<int64_t>(t < t_hi ? t : t_lo) * D;
+#pragma unroll
+            for (int cc = 0; cc < CPL; ++cc) kv[r][cc] = kt[lane * CPL + cc];
+        }
+#pragma unroll
+        for (int r = 0; r < kPass; ++r) {
+            float pr[CPL];
+#pragma unroll
+            for (int cc = 0; cc < CPL; ++cc) pr[cc] = __fmul_rn(qr_s[lane * CPL + cc], kv[r][cc]);
+#pragma unroll
+            for (int hh = CPL / 2; hh >= 1; hh >>= 1)
+#pragma unroll
+                for (int cc = 0; cc < hh; ++cc) pr[cc] = __fadd_rn(pr[2 * cc], pr[2 * cc + 1]);
+            float dot = pr[0];
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) dot = __fadd_rn(dot, __shfl_xor_sync(0xffffffffu, dot, d));
+            const float sv = __fmul_rn(dot, scale);
+            if (t0 + r < t_hi) {
+                mx = fmaxf(mx, sv);
+                if (lane == 0) a.sc[static_cast<int64_t>(h) * a.C * kAtqChunk + t0 + r] = sv;
+            }
+        }
+    }
+    const float m = block_max<kAtqScoreThreads>(mx, red);
+    if (tid == 0) a.cmax[h * a.C + c] = m;
+}
+
+// 2: the exponentials of the chunk (against the head's maximum) and their sum.
+template <int D>
+__global__ void __launch_bounds__(D) atq_exp_kernel(const __grid_constant__ AtqArgs a) {
+    __shared__ float es[kAtqChunk];
+    __shared__ float red[D / 32];
+    const int h = blockIdx.x, c = blockIdx.y, j = threadIdx.x;
+    const int n = a.pos + 1, t_lo = c * kAtqChunk;
+    float mx = -__int_as_float(0x7f800000);
+    for (int i = j; i < a.C; i += D) mx = fmaxf(mx, a.cmax[h * a.C + i]);
+    const float m = block_max<D>(mx, red);
+    float *sh = a.sc + static_cast<int64_t>(h) * a.C * kAtqChunk;
+    for (int i = j; i < kAtqChunk; i += D) {
+        const int t = t_lo + i;
+        float e = -0.0f;
+        if (t < n) {
+            e = exp_tree(__fsub_rn(sh[t], m));
+            sh[t] = e;
+        }
+        es[i] = e;
+    }
+    __syncthreads();
+    if (j < 32) {
+        // lane l < 8: the tree over block l's 32 positions; then the tree over
+        // the 8 blocks
+        float b = j < kAtqChunk / 32 ? tree_padded32(es + 32 * j, 32) : -0.0f;
+#pragma unroll
+        for (int d = 1; d < kAtqChunk / 32; d <<= 1) b = __fadd_rn(b, __shfl_xor_sync(0xffffffffu, b, d));
+        if (j == 0) a.csum[h * a.C + c] = b;
+    }
+}
+
+// 3: the probabilities of the chunk and its weighted values.  NG thread
+// groups of D threads (threads qg*D + j: column j): group qg sums the chunk's
+// 32-position blocks qg*BPG .. qg*BPG + BPG-1 (an aligned subtree of the
+// chunk's tree), then the NG parts are combined by the tree.
+template <int D>
+__host__ __device__ constexpr int atq_value_groups() { return D == 64 ? 8 : 1024 / D; }
+
+template <int D>
+__global__ void __launch_bounds__(D * atq_value_groups<D>()) atq_values_kernel(const __grid_constant__ AtqArgs a) {
+    constexpr int NG = atq_value_groups<D>(), BPG = kAtqChunk / 32 / NG;
+    __shared__ float ps[kAtqChunk];
+    __shared__ float part[NG][D];
+    const int h = blockIdx.x, c = blockIdx.y, tid = threadIdx.x, qg = tid / D, j = tid % D;
+    const int g = h / (a.Hq / a.Hkv), n = a.pos + 1, t_lo = c * kAtqChunk;
+    const float Z = tree_padded32(a.csum + h * a.C, a.C);
+    const float *sh = a.sc + static_cast<int64_t>(h) * a.C * kAtqChunk;
+    for (int i = tid; i < kAtqChunk; i += D * NG) {
+        const int t = t_lo + i;
+        ps[i] = t < n ? __fdiv_rn(sh[t], Z) : 0.0f;
+    }
+    __syncthreads();
+    const float *Vg = a.Vc + static_cast<int64_t>(g) * a.P * D + j;
+    float bsum[BPG];
+#pragma unroll
+    for (int bb = 0; bb < BPG; ++bb) {
+        const int b = qg * BPG + bb;
+        float e[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            const int t = t_lo + 32 * b + i;
+            e[i] = t < n ? __fmul_rn(ps[32 * b + i], Vg[static_cast<int64_t>(t) * D]) : -0.0f;
+        }
+        bsum[bb] = tree32v(e);
+    }
+#pragma unroll
+    for (int hh = BPG / 2; hh >= 1; hh >>= 1)
+#pragma unroll
+        for (int bb = 0; bb < hh; ++bb) bsum[bb] = __fadd_rn(bsum[2 * bb], bsum[2 * bb + 1]);
+    part[qg][j] = bsum[0];
+    __syncthreads();
+    if (tid < D) {
+        float w[NG];
+#pragma unroll
+        for (int i = 0; i < NG; ++i) w[i] = part[i][tid];
+#pragma unroll
+        for (int hh = NG / 2; hh >= 1; hh >>= 1)
+#pragma unroll
+            for (int i = 0; i < hh; ++i) w[i] = __fadd_rn(w[2 * i], w[2 * i + 1]);
+        a.opart[(static_cast<int64_t>(h) * a.C + c) * D + tid] = w[0];
+    }
+}
+
+// 4: the tree over the chunks, the gate and the group sums.
+template <int D>
+__global__ void __launch_bounds__(D) atq_out_kernel(const __grid_constant__ AtqArgs a) {
+    __shared__ float red[D / 32];
+    const int h = blockIdx.x, j = threadIdx.x;
+    float o[kAtqMaxChunks];
+    for (int c = 0; c < a.C; ++c) o[c] = a.opart[(static_cast<int64_t>(h) * a.C + c) * D + j];
+    const float ov = tree_padded32(o, a.C);
+    const int64_t yi = static_cast<int64_t>(h) * D + j;
+    const float yv = __fmul_rn(ov, sigmoid_tree(a.gate[yi]));
+    a.y[yi] = yv;
+    float gsm = yv;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) gsm = __fadd_rn(gsm, __shfl_xor_sync(0xffffffffu, gsm, d));
+    if ((j & 31) == 0) red[j >> 5] = gsm;
+    __syncthreads();
+    if ((j & 63) == 0) a.ysum[yi >> 6] = __fadd_rn(red[j >> 5], red[(j >> 5) + 1]);
+}
+
+template <int D>
+cudaError_t launch_atq_d(const AtqArgs &a, cudaStream_t stream) {
+    const dim3 grid(a.Hq, a.C);
+    atq_scores_kernel<D><<<grid, kAtqScoreThreads, 0, stream>>>(a);
+    atq_exp_kernel<D><<<grid, D, 0, stream>>>(a);
+    atq_values_kernel<D><<<grid, D * atq_value_groups<D>(), 0, stream>>>(a);
+    atq_out_kernel<D><<<a.Hq, D, 0, stream>>>(a);
     return cudaGetLastError();
+}
+
+// Device scratch for the chunk results, per device, grown when a call needs
+// more (freed only at exit).
+std::mutex g_atq_mu;
+float *g_atq_scratch[64];
+size_t g_atq_bytes[64];
+
+cudaError_t atq_scratch(size_t bytes, float **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_atq_mu);
+    if (g_atq_bytes[dev] < bytes) {
+        if (g_atq_scratch[dev]) {
+            e = cudaDeviceSynchronize();  // a launch may still use the old buffer
+            if (e == cudaSuccess) e = cudaFree(g_atq_scratch[dev]);
+            if (e != cudaSuccess) return e;
+            g_atq_scratch[dev] = nullptr;
+            g_atq_bytes[dev] = 0;
+        }
+        void *p = nullptr;
+        e = cudaMalloc(&p, bytes);
+        if (e != cudaSuccess) return e;
+        g_atq_scratch[dev] = static_cast<float *>(p);
+        g_atq_bytes[dev] = bytes;
+    }
+    *out = g_atq_scratch[dev];
+    return cudaSuccess;
 }
 
 }  // namespace
@@ -426,14 +593,21 @@ cudaError_t launch_gdn(const float *x, const float *conv, float *state, const fl
 cudaError_t launch_atq(const float *q, const float *gate, const float *k, const float *v, const float *qn_w,
                        const float *kn_w, const float *cs, const float *sn, float *Kc, float *Vc, float *y,
                        float *ysum, int Hq, int Hkv, int D, int P, int pos, float eps, cudaStream_t stream) {
-    if (pos + 1 > kAtqMaxPositions) return cudaErrorInvalidValue;
+    if (pos + 1 > kAtqMaxPositions || (D != 64 && D != 128 && D != 256)) return cudaErrorInvalidValue;
+    AtqArgs a{q, gate, k, v, qn_w, kn_w, cs, sn, Kc, Vc, y, ysum, nullptr, nullptr, nullptr, nullptr,
+              Hq, Hkv, P, pos, (pos + kAtqChunk) / kAtqChunk, eps};
+    const size_t nsc = static_cast<size_t>(Hq) * a.C * kAtqChunk, nc = static_cast<size_t>(Hq) * a.C;
+    float *base = nullptr;
+    cudaError_t e = atq_scratch((nsc + 2 * nc + nc * D) * sizeof(float), &base);
+    if (e != cudaSuccess) return e;
+    a.sc = base;
+    a.cmax = base + nsc;
+    a.csum = a.cmax + nc;
+    a.opart = a.csum + nc;
     switch (D) {
-    case 64: return launch_atq_d<64>(q, gate, k, v, qn_w, kn_w, cs, sn, Kc, Vc, y, ysum, Hq, Hkv, P, pos, eps, stream);
-    case 128:
-        return launch_atq_d<128>(q, gate, k, v, qn_w, kn_w, cs, sn, Kc, Vc, y, ysum, Hq, Hkv, P, pos, eps, stream);
-    case 256:
-        return launch_atq_d<256>(q, gate, k, v, qn_w, kn_w, cs, sn, Kc, Vc, y, ysum, Hq, Hkv, P, pos, eps, stream);
-    default: return cudaErrorInvalidValue;
+    case 64: return launch_atq_d<64>(a, stream);
+    case 128: return launch_atq_d<128>(a, stream);
+    default: return launch_atq_d<256>(a, stream);
     }
 }
 

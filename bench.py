@@ -300,6 +300,7 @@ def run_ours(args, rank, world):
         extra["batched"] = bench_batched(abg, stream, args)
         extra["pages_way"] = bench_pages_way(abg, stream, args)
         extra["gdn"] = bench_gdn(abg, stream, args)
+        extra["atq"] = bench_atq(abg, stream, args)
         extra["sweep"] = bench_sweep(abg, stream, args, peak, l2)
 
     res = dict(value=value, ms_step=ms_step, us_per_product=us_per_product, achieved=achieved,
@@ -516,11 +517,41 @@ def bench_pages_way(abg, stream, args):
             "us_per_call": round(us, 3), "gbs": round(product_bytes(MID_ROWS, MID_COLS) / (us * 1e-6) / 1e9, 1)}
 
 
+def time_calls_graph(fn, count: int, replays: int = 5) -> float:
+    """us per call of `count` calls of fn(i, stream) captured in one CUDA graph
+    (so the host's per-call cost is not timed), median over replays."""
+    import torch
+    cs = torch.cuda.Stream()
+    cs.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(cs):
+        fn(0, cs)  # warm-up outside the capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=cs):
+        for i in range(count):
+            fn(i, cs)
+    torch.cuda.synchronize()
+    g.replay()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(replays):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(cs)
+        with torch.cuda.stream(cs):
+            g.replay()
+        e1.record(cs)
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1) * 1e3 / count)
+    del g
+    return statistics.median(times)
+
+
 def bench_gdn(abg, stream, args):
     """One token of the gated DeltaNet mixer (abg_gdn), 16 heads of 128 columns,
-    4 conv taps: calls back to back, each on its own copy of the state (S and
-    the conv state rotate over copies totalling more than L2), us per token;
-    the first call's outputs checked bit for bit against the oracle."""
+    4 conv taps: calls captured in a CUDA graph (the host's per-call cost not
+    timed), each on its own copy of the state (S and the conv state rotate over
+    copies totalling more than L2), us per token; the first call's outputs
+    checked bit for bit against the oracle."""
     import torch
 
     import oracle
@@ -543,17 +574,7 @@ def bench_gdn(abg, stream, args):
             and np.array_equal(sts[0].cpu().numpy().view(np.uint32), est.view(np.uint32)))
     if not same:
         raise SystemExit("gdn differs from the oracle")
-    reps = 200
-    for i in range(args.warmup * 10):
-        abg.gdn(*args_of(i % copies), y, ys, stream=stream)
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for i in range(reps):
-        abg.gdn(*args_of(i % copies), y, ys, stream=stream)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    us = e0.elapsed_time(e1) * 1e3 / reps
+    us = time_calls_graph(lambda i, st: abg.gdn(*args_of(i % copies), y, ys, stream=st), 200)
     # algorithmic bytes: S and the conv state read and written once, x, conv,
     # z, the per-head scalars and the norm weights read, y and ysum written
     nbytes = 2 * c["S"].nbytes + 2 * c["state"].nbytes + c["x"].nbytes + c["conv"].nbytes + c["z"].nbytes + \
@@ -561,7 +582,49 @@ def bench_gdn(abg, stream, args):
     del Ss, sts
     torch.cuda.empty_cache()
     return {"workload": f"gdn mixer, one token: {H} heads x {D} columns, {K} conv taps; state rotating over "
-                        f"{copies} copies (> L2); calls back to back",
+                        f"{copies} copies (> L2); 200 calls captured in one CUDA graph, median of 5 replays",
+            "us_per_token": round(us, 3), "bytes_per_token": int(nbytes),
+            "gbs": round(nbytes / (us * 1e-6) / 1e9, 1), "bit_exact": True}
+
+
+def bench_atq(abg, stream, args):
+    """One token of gated attention (abg_atq): 8 query heads over 2 key/value
+    heads of 256 columns at position 2047 of 4096-row caches; calls captured in
+    a CUDA graph, the caches rotating over copies larger than L2; us per token;
+    the first call's outputs checked bit for bit against the oracle."""
+    import torch
+
+    import oracle
+    c = synth.atq_case(np.random.default_rng(22))
+    Hkv, P, D = c["Kc"].shape
+    Hq, pos = c["q"].size // D, c["pos"]
+    d = {k: torch.from_numpy(np.ascontiguousarray(v)).cuda() for k, v in c.items() if k != "pos"}
+    l2 = getattr(torch.cuda.get_device_properties(0), "L2_cache_size", 126 * 2 ** 20)
+    copies = max(2, math.ceil(1.5 * l2 / (2 * c["Kc"].nbytes)))
+    Ks = [d["Kc"].clone() for _ in range(copies)]
+    Vs = [d["Vc"].clone() for _ in range(copies)]
+    y = torch.empty(Hq * D, dtype=torch.float32, device="cuda")
+    ys = torch.empty(Hq * D // 64, dtype=torch.float32, device="cuda")
+    args_of = lambda i: (d["q"], d["gate"], d["k"], d["v"], d["qn_w"], d["kn_w"], d["cos"], d["sin"], Ks[i], Vs[i])
+    abg.atq(*args_of(0), y, ys, pos=pos, stream=stream)
+    torch.cuda.synchronize()
+    ey, eys, eK, eV = oracle.atq(**c)
+    same = (np.array_equal(y.cpu().numpy().view(np.uint32), ey.view(np.uint32))
+            and np.array_equal(ys.cpu().numpy().view(np.uint32), eys.view(np.uint32))
+            and np.array_equal(Ks[0].cpu().numpy().view(np.uint32), eK.view(np.uint32))
+            and np.array_equal(Vs[0].cpu().numpy().view(np.uint32), eV.view(np.uint32)))
+    if not same:
+        raise SystemExit("atq differs from the oracle")
+    us = time_calls_graph(lambda i, st: abg.atq(*args_of(i % copies), y, ys, pos=pos, stream=st), 100)
+    # algorithmic bytes: the caches' rows 0..pos read once (each group's rows
+    # serve its query heads), one row of each written, the vectors
+    nbytes = 2 * Hkv * (pos + 1) * D * 4 + 2 * Hkv * D * 4 + (2 * Hq + 2 * Hkv) * D * 4 + 2 * D * 4 + \
+        D * 4 + Hq * D * 4 + Hq * D // 16
+    del Ks, Vs
+    torch.cuda.empty_cache()
+    return {"workload": f"atq, one token: {Hq} query heads over {Hkv} kv heads x {D} columns at position {pos} of "
+                        f"{P}-row caches; caches rotating over {copies} copies (> L2); 100 calls captured in one "
+                        "CUDA graph, median of 5 replays",
             "us_per_token": round(us, 3), "bytes_per_token": int(nbytes),
             "gbs": round(nbytes / (us * 1e-6) / 1e9, 1), "bit_exact": True}
 
@@ -692,7 +755,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-extra", action="store_true", help="skip the head and decode-token measurements")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
-    ap.add_argument("--only", choices=["head", "decode", "formats", "batched", "sweep", "pages_way", "gdn"],
+    ap.add_argument("--only", choices=["head", "decode", "formats", "batched", "sweep", "pages_way", "gdn", "atq"],
                     default=None,
                     help="run one secondary workload alone and print its numbers (for profiling)")
     args = ap.parse_args()
@@ -711,6 +774,8 @@ def main():
             out = bench_batched(abg, stream, args)
         elif args.only == "gdn":
             out = bench_gdn(abg, stream, args)
+        elif args.only == "atq":
+            out = bench_atq(abg, stream, args)
         elif args.only == "pages_way":
             out = bench_pages_way(abg, stream, args)
         elif args.only == "sweep":

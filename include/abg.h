@@ -265,10 +265,15 @@ abg_status abg_gdn(const float *x, const float *conv, float *state, const float 
  *   y        f32 [Hq*D]    ysum  f32 [Hq*D/64]
  *   D = 64, 128 or 256; Hq a multiple of Hkv; 0 <= pos < P; pos + 1 <= 8192
  *   (the scores of one head stay in shared memory); Hq*D <= 2^20.
- * Both modes compute the same bits.  Errors: null pointer or mode ABG_EINVAL;
- * shape ABG_ESHAPE; a pointer not 4-byte aligned ABG_EALIGN; an output (Kc,
- * Vc, y, ysum) overlapping an input or another output ABG_EALIAS.
- * Asynchronous on `stream`.
+ * Both modes compute the same bits.  The positions run in chunks of 256 (four
+ * launches); the chunks' partial results live in a device buffer the library
+ * allocates on a device's first call and grows when a call needs more (the
+ * growth synchronizes the device); calls that can overlap on the GPU (on
+ * different streams or host threads) share it and must be ordered by the
+ * caller.  Errors: null pointer or mode ABG_EINVAL; shape ABG_ESHAPE; a
+ * pointer not 4-byte aligned ABG_EALIGN; an output (Kc, Vc, y, ysum)
+ * overlapping an input or another output ABG_EALIAS.  Asynchronous on
+ * `stream`.
  */
 abg_status abg_atq(const float *q, const float *gate, const float *k, const float *v, const float *qn_w,
                    const float *kn_w, const float *cos, const float *sin, float *Kc, float *Vc, float *y, float *ysum,
