@@ -23,7 +23,7 @@ __all__ = [
 
 TREE, FAST = 0, 1
 MAX_COLS = 16384
-NODE_Q4MV, NODE_RMSQ, NODE_SWQ, NODE_GSUM = 0, 1, 2, 3
+NODE_Q4MV, NODE_RMSQ, NODE_SWQ, NODE_GSUM, NODE_GDN, NODE_ATQ = 0, 1, 2, 3, 4, 5
 PRO_NONE, PRO_GSUM, PRO_RMSQ, PRO_SWQ = 0, 1, 2, 3
 SB_F32, SB_BF16, SB_F16 = 0, 1, 2
 SB_TYPES = {"f32": SB_F32, "bf16": SB_BF16, "f16": SB_F16}
@@ -58,7 +58,23 @@ class _Node(ctypes.Structure):
         ("out", ctypes.c_void_p), ("out_sum", ctypes.c_void_p),
         ("len", ctypes.c_int64),
         ("group", ctypes.c_int32), ("sb_type", ctypes.c_int32),
+        ("args", ctypes.c_void_p),
     ]
+
+
+class _GdnArgs(ctypes.Structure):
+    """Mirror of struct abg_gdn_args in include/abg.h."""
+    _fields_ = [(f, ctypes.c_void_p) for f in ("x", "conv", "state", "a", "b", "z", "A_log", "dt_bias", "nw", "S",
+                                               "y", "ysum")] + \
+               [("H", ctypes.c_int64), ("D", ctypes.c_int64), ("K", ctypes.c_int64),
+                ("eps", ctypes.c_float), ("eps_n", ctypes.c_float)]
+
+
+class _AtqArgs(ctypes.Structure):
+    """Mirror of struct abg_atq_args in include/abg.h."""
+    _fields_ = [(f, ctypes.c_void_p) for f in ("q", "gate", "k", "v", "qn_w", "kn_w", "cos", "sin", "Kc", "Vc", "y",
+                                               "ysum")] + \
+               [(f, ctypes.c_int64) for f in ("Hq", "Hkv", "D", "P", "pos")] + [("eps", ctypes.c_float)]
 
 
 def library(build_if_missing: bool = True) -> ctypes.CDLL:
@@ -198,20 +214,37 @@ def q4mm(w, scale, bias, X, XS, Y, cols: int, row0: int = 0, n: int | None = Non
     return Y
 
 
-def gdn(x, conv, state, a, b, z, A_log, dt_bias, nw, S, y, ysum, eps: float = 1e-6, eps_n: float = 1e-6,
-        mode: int = TREE, stream=None):
-    """One token of the gated DeltaNet mixer (see abg_gdn): S [H][D][D] and
-    state [3*H*D][K-1] are updated in place; y [H*D] and ysum [H*D/64] written."""
+def _gdn_args(x, conv, state, a, b, z, A_log, dt_bias, nw, S, y, ysum, eps, eps_n):
     _, f32 = _dtypes()
     H, D = S.shape[0], S.shape[1]
     K = conv.shape[-1]
     C = 3 * H * D
-    st = library().abg_gdn(
+    return _GdnArgs(
         _ptr(x, f32, C, "x"), _ptr(conv, f32, C * K, "conv"), _ptr(state, f32, C * (K - 1), "state"),
         _ptr(a, f32, H, "a"), _ptr(b, f32, H, "b"), _ptr(z, f32, H * D, "z"), _ptr(A_log, f32, H, "A_log"),
         _ptr(dt_bias, f32, H, "dt_bias"), _ptr(nw, f32, D, "nw"), _ptr(S, f32, H * D * D, "S"),
-        _ptr(y, f32, H * D, "y"), _ptr(ysum, f32, H * D // 64, "ysum"), H, D, K, ctypes.c_float(eps),
-        ctypes.c_float(eps_n), mode, _stream(stream))
+        _ptr(y, f32, H * D, "y"), _ptr(ysum, f32, H * D // 64, "ysum"), H, D, K, eps, eps_n)
+
+
+def _atq_args(q, gate, k, v, qn_w, kn_w, cos, sin, Kc, Vc, y, ysum, pos, eps):
+    _, f32 = _dtypes()
+    Hkv, P, D = Kc.shape
+    Hq = q.numel() // D
+    return _AtqArgs(
+        _ptr(q, f32, Hq * D, "q"), _ptr(gate, f32, Hq * D, "gate"), _ptr(k, f32, Hkv * D, "k"),
+        _ptr(v, f32, Hkv * D, "v"), _ptr(qn_w, f32, D, "qn_w"), _ptr(kn_w, f32, D, "kn_w"),
+        _ptr(cos, f32, D // 2, "cos"), _ptr(sin, f32, D // 2, "sin"), _ptr(Kc, f32, Hkv * P * D, "Kc"),
+        _ptr(Vc, f32, Hkv * P * D, "Vc"), _ptr(y, f32, Hq * D, "y"), _ptr(ysum, f32, Hq * D // 64, "ysum"),
+        Hq, Hkv, D, P, pos, eps)
+
+
+def gdn(x, conv, state, a, b, z, A_log, dt_bias, nw, S, y, ysum, eps: float = 1e-6, eps_n: float = 1e-6,
+        mode: int = TREE, stream=None):
+    """One token of the gated DeltaNet mixer (see abg_gdn): S [H][D][D] and
+    state [3*H*D][K-1] are updated in place; y [H*D] and ysum [H*D/64] written."""
+    g = _gdn_args(x, conv, state, a, b, z, A_log, dt_bias, nw, S, y, ysum, eps, eps_n)
+    st = library().abg_gdn(g.x, g.conv, g.state, g.a, g.b, g.z, g.A_log, g.dt_bias, g.nw, g.S, g.y, g.ysum,
+                           g.H, g.D, g.K, ctypes.c_float(eps), ctypes.c_float(eps_n), mode, _stream(stream))
     _check(st, "abg_gdn")
     return y
 
@@ -220,15 +253,9 @@ def atq(q, gate, k, v, qn_w, kn_w, cos, sin, Kc, Vc, y, ysum, pos: int, eps: flo
         stream=None):
     """One token of gated attention at position pos (see abg_atq): row pos of
     Kc and Vc [Hkv][P][D] is written; y [Hq*D] and ysum [Hq*D/64] written."""
-    _, f32 = _dtypes()
-    Hkv, P, D = Kc.shape
-    Hq = q.numel() // D
-    st = library().abg_atq(
-        _ptr(q, f32, Hq * D, "q"), _ptr(gate, f32, Hq * D, "gate"), _ptr(k, f32, Hkv * D, "k"),
-        _ptr(v, f32, Hkv * D, "v"), _ptr(qn_w, f32, D, "qn_w"), _ptr(kn_w, f32, D, "kn_w"),
-        _ptr(cos, f32, D // 2, "cos"), _ptr(sin, f32, D // 2, "sin"), _ptr(Kc, f32, Hkv * P * D, "Kc"),
-        _ptr(Vc, f32, Hkv * P * D, "Vc"), _ptr(y, f32, Hq * D, "y"), _ptr(ysum, f32, Hq * D // 64, "ysum"),
-        Hq, Hkv, D, P, pos, ctypes.c_float(eps), mode, _stream(stream))
+    t = _atq_args(q, gate, k, v, qn_w, kn_w, cos, sin, Kc, Vc, y, ysum, pos, eps)
+    st = library().abg_atq(t.q, t.gate, t.k, t.v, t.qn_w, t.kn_w, t.cos, t.sin, t.Kc, t.Vc, t.y, t.ysum,
+                           t.Hq, t.Hkv, t.D, t.P, t.pos, ctypes.c_float(eps), mode, _stream(stream))
     _check(st, "abg_atq")
     return y
 
@@ -311,6 +338,22 @@ class Node:
     def gsum(stage, v, out_sum, group=64):
         return _Node(kind=NODE_GSUM, stage=stage, x=_ptr(v, name="v"), out_sum=_ptr(out_sum, name="out_sum"),
                      len=v.numel(), group=group)
+
+    @staticmethod
+    def gdn(stage, x, conv, state, a, b, z, A_log, dt_bias, nw, S, y, ysum, eps=1e-6, eps_n=1e-6):
+        """A gdn node: arguments as gdn()."""
+        g = _gdn_args(x, conv, state, a, b, z, A_log, dt_bias, nw, S, y, ysum, eps, eps_n)
+        nd = _Node(kind=NODE_GDN, stage=stage, args=ctypes.addressof(g))
+        nd._args = g  # read when the graph is created
+        return nd
+
+    @staticmethod
+    def atq(stage, q, gate, k, v, qn_w, kn_w, cos, sin, Kc, Vc, y, ysum, pos, eps=1e-6):
+        """An atq node for position pos (fixed in the graph): arguments as atq()."""
+        t = _atq_args(q, gate, k, v, qn_w, kn_w, cos, sin, Kc, Vc, y, ysum, pos, eps)
+        nd = _Node(kind=NODE_ATQ, stage=stage, args=ctypes.addressof(t))
+        nd._args = t
+        return nd
 
 
 class StageGraph:

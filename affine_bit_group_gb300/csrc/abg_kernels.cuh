@@ -121,18 +121,6 @@ bool plan_q4mm(Q4Plan *plan, const Q4Prob *probs, int nprob, int cols, int T, in
 cudaError_t launch_q4mm(const Q4Plan &plan, cudaStream_t stream, bool pdl);
 cudaError_t q4mm_status(unsigned *bits, bool clear);
 
-// gdn mixer (mixer.cu): one token for H heads of D (64, 128 or 256) columns, K
-// conv taps (2..8); arguments as abg_gdn.
-cudaError_t launch_gdn(const float *x, const float *conv, float *state, const float *a, const float *b,
-                       const float *z, const float *A_log, const float *dt_bias, const float *nw, float *S, float *y,
-                       float *ysum, int H, int D, int K, float eps, float eps_n, cudaStream_t stream);
-// atq (mixer.cu): one token for Hq query heads over Hkv key/value heads of D
-// (64, 128 or 256) columns at position pos (pos + 1 <= 8192); as abg_atq.
-cudaError_t launch_atq(const float *q, const float *gate, const float *k, const float *v, const float *qn_w,
-                       const float *kn_w, const float *cs, const float *sn, float *Kc, float *Vc, float *y,
-                       float *ysum, int Hq, int Hkv, int D, int P, int pos, float eps, cudaStream_t stream);
-cudaError_t mixer_status(unsigned *bits, bool clear);
-
 // Each translation unit's device status word (OR-ed into *bits).
 cudaError_t q4mv_status(unsigned *bits, bool clear);
 cudaError_t vec_status(unsigned *bits, bool clear);

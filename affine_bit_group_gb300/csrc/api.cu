@@ -11,6 +11,7 @@
 // the one wait.
 #include "../../include/abg.h"
 #include "abg_kernels.cuh"
+#include "mixer.cuh"
 
 #include <algorithm>
 #include <chrono>
@@ -179,6 +180,78 @@ abg_status check_swq(const float *a, const float *o, const float *osum, int64_t 
     return ABG_OK;
 }
 
+// the ranges a gdn call reads and writes (state and S are read and written)
+void gdn_io(const abg_gdn_args &g, std::vector<Range> &in, std::vector<Range> &out) {
+    const int64_t C = 3 * g.H * g.D;
+    in = {rng(g.x, C, 4),     rng(g.conv, C * g.K, 4),  rng(g.a, g.H, 4),  rng(g.b, g.H, 4),
+          rng(g.z, g.H * g.D, 4), rng(g.A_log, g.H, 4), rng(g.dt_bias, g.H, 4), rng(g.nw, g.D, 4)};
+    out = {rng(g.state, C * (g.K - 1), 4), rng(g.S, g.H * g.D * g.D, 4), rng(g.y, g.H * g.D, 4),
+           rng(g.ysum, g.H * g.D / 64, 4)};
+}
+
+// the ranges an atq call reads and writes (the caches are read and written)
+void atq_io(const abg_atq_args &t, std::vector<Range> &in, std::vector<Range> &out) {
+    in = {rng(t.q, t.Hq * t.D, 4),  rng(t.gate, t.Hq * t.D, 4), rng(t.k, t.Hkv * t.D, 4),
+          rng(t.v, t.Hkv * t.D, 4), rng(t.qn_w, t.D, 4),        rng(t.kn_w, t.D, 4),
+          rng(t.cos, t.D / 2, 4),   rng(t.sin, t.D / 2, 4)};
+    out = {rng(t.Kc, t.Hkv * t.P * t.D, 4), rng(t.Vc, t.Hkv * t.P * t.D, 4), rng(t.y, t.Hq * t.D, 4),
+           rng(t.ysum, t.Hq * t.D / 64, 4)};
+}
+
+// no output overlaps an input or another output
+abg_status disjoint_outputs(const std::vector<Range> &in, const std::vector<Range> &out) {
+    for (size_t i = 0; i < out.size(); ++i) {
+        for (const Range &r : in)
+            if (overlap(out[i], r)) return ABG_EALIAS;
+        for (size_t k = i + 1; k < out.size(); ++k)
+            if (overlap(out[i], out[k])) return ABG_EALIAS;
+    }
+    return ABG_OK;
+}
+
+abg_status check_gdn(const abg_gdn_args &g, int mode) {
+    if (mode != ABG_TREE && mode != ABG_FAST) return ABG_EINVAL;
+    if (!g.x || !g.conv || !g.state || !g.a || !g.b || !g.z || !g.A_log || !g.dt_bias || !g.nw || !g.S || !g.y ||
+        !g.ysum)
+        return ABG_EINVAL;
+    if (g.H < 1 || (g.D != 64 && g.D != 128 && g.D != 256) || g.K < 2 || g.K > 8 || g.H * g.D > (int64_t(1) << 20))
+        return ABG_ESHAPE;
+    const void *all[] = {g.x, g.conv, g.state, g.a, g.b, g.z, g.A_log, g.dt_bias, g.nw, g.S, g.y, g.ysum};
+    for (const void *p : all)
+        if (!aligned(p, 4)) return ABG_EALIGN;
+    if (!aligned(g.S, 16)) return ABG_EALIGN;  // a head's state is one bulk copy
+    std::vector<Range> in, out;
+    gdn_io(g, in, out);
+    return disjoint_outputs(in, out);
+}
+
+abg_status check_atq(const abg_atq_args &t, int mode) {
+    if (mode != ABG_TREE && mode != ABG_FAST) return ABG_EINVAL;
+    if (!t.q || !t.gate || !t.k || !t.v || !t.qn_w || !t.kn_w || !t.cos || !t.sin || !t.Kc || !t.Vc || !t.y ||
+        !t.ysum)
+        return ABG_EINVAL;
+    if (t.Hq < 1 || t.Hkv < 1 || t.Hq % t.Hkv || (t.D != 64 && t.D != 128 && t.D != 256) || t.pos < 0 ||
+        t.pos >= t.P || t.pos + 1 > 8192 || t.Hq * t.D > (int64_t(1) << 20))
+        return ABG_ESHAPE;
+    const void *all[] = {t.q, t.gate, t.k, t.v, t.qn_w, t.kn_w, t.cos, t.sin, t.Kc, t.Vc, t.y, t.ysum};
+    for (const void *p : all)
+        if (!aligned(p, 4)) return ABG_EALIGN;
+    std::vector<Range> in, out;
+    atq_io(t, in, out);
+    return disjoint_outputs(in, out);
+}
+
+cudaError_t run_gdn(const abg_gdn_args &g, cudaStream_t s) {
+    return launch_gdn(g.x, g.conv, g.state, g.a, g.b, g.z, g.A_log, g.dt_bias, g.nw, g.S, g.y, g.ysum,
+                      static_cast<int>(g.H), static_cast<int>(g.D), static_cast<int>(g.K), g.eps, g.eps_n, s);
+}
+
+cudaError_t run_atq(const abg_atq_args &t, float *scratch, cudaStream_t s) {
+    return launch_atq(t.q, t.gate, t.k, t.v, t.qn_w, t.kn_w, t.cos, t.sin, t.Kc, t.Vc, t.y, t.ysum,
+                      static_cast<int>(t.Hq), static_cast<int>(t.Hkv), static_cast<int>(t.D), static_cast<int>(t.P),
+                      static_cast<int>(t.pos), t.eps, scratch, s);
+}
+
 // --------------------------------------------------------------- graphs ----
 struct Launch {
     int kind;  // abg_node_kind
@@ -190,6 +263,9 @@ struct Launch {
     float eps = 0.f;
     int64_t len = 0;
     int group = 64;
+    abg_gdn_args gdn{};
+    abg_atq_args atq{};
+    float *atq_scratch = nullptr;  // owned by the graph
 };
 
 struct StageGraph {
@@ -197,7 +273,7 @@ struct StageGraph {
     cudaGraphExec_t exec = nullptr;
     int64_t launches = 0;
     int64_t swiglu_pairs = 0;
-    std::vector<void *> scratch;  // device buffers of fused SwiGLU vectors
+    std::vector<void *> scratch;  // device buffers: fused SwiGLU vectors, atq chunk results
 };
 
 void free_scratch(StageGraph *g) {
@@ -264,13 +340,19 @@ abg_status fuse_swiglu_pairs(std::vector<Launch> &launches, StageGraph *g, int m
 }
 
 cudaError_t prepare(const Launch &L) {
+    if (L.kind == ABG_NODE_GDN) return prepare_gdn(static_cast<int>(L.gdn.D));
     if (L.kind != ABG_NODE_Q4MV) return cudaSuccess;
     return prepare_q4mv(L.plan);
 }
 
+// The mixers' kernels start only after the previous launch has finished (no
+// programmatic dependent launch); the launch after them may overlap their
+// tail with its prologue, as after any other launch.
 cudaError_t run(const Launch &L, cudaStream_t s, bool pdl, bool tree) {
     switch (L.kind) {
     case ABG_NODE_Q4MV: return launch_q4mv(L.plan, s, pdl);
+    case ABG_NODE_GDN: return run_gdn(L.gdn, s);
+    case ABG_NODE_ATQ: return run_atq(L.atq, L.atq_scratch, s);
     case ABG_NODE_RMSQ: return launch_rmsq(L.a, L.b, L.eps, L.o, L.os, L.len, L.group, tree, s, pdl);
     case ABG_NODE_SWQ: return launch_swq(L.a, L.o, L.os, L.len, L.group, tree, s, pdl);
     default: return launch_gsum(L.a, L.os, L.len, L.group, tree, s, pdl);
@@ -313,6 +395,8 @@ void node_io(const abg_node &nd, std::vector<Range> &in, std::vector<Range> &out
         in = {rng(nd.x, 2 * nd.len, 4)};
         out = {rng(nd.out, nd.len, 4), rng(nd.out_sum, nd.len / node_group(nd.group), 4)};
         break;
+    case ABG_NODE_GDN: gdn_io(*static_cast<const abg_gdn_args *>(nd.args), in, out); break;
+    case ABG_NODE_ATQ: atq_io(*static_cast<const abg_atq_args *>(nd.args), in, out); break;
     default:
         in = {rng(nd.x, nd.len, 4)};
         out = {rng(nd.out_sum, nd.len / node_group(nd.group), 4)};
@@ -491,54 +575,19 @@ abg_status abg_swq_ex(const float *a, float *o, float *osum, int64_t n, int grou
 abg_status abg_gdn(const float *x, const float *conv, float *state, const float *a, const float *b, const float *z,
                    const float *A_log, const float *dt_bias, const float *nw, float *S, float *y, float *ysum,
                    int64_t H, int64_t D, int64_t K, float eps, float eps_n, int mode, void *stream) {
-    if (mode != ABG_TREE && mode != ABG_FAST) return ABG_EINVAL;
-    if (!x || !conv || !state || !a || !b || !z || !A_log || !dt_bias || !nw || !S || !y || !ysum) return ABG_EINVAL;
-    if (H < 1 || (D != 64 && D != 128 && D != 256) || K < 2 || K > 8 || H * D > (int64_t(1) << 20))
-        return ABG_ESHAPE;
-    const void *all[] = {x, conv, state, a, b, z, A_log, dt_bias, nw, S, y, ysum};
-    for (const void *p : all)
-        if (!aligned(p, 4)) return ABG_EALIGN;
-    if (!aligned(S, 16)) return ABG_EALIGN;  // a head's state is one bulk copy
-    const int64_t C = 3 * H * D;
-    const Range in[] = {rng(x, C, 4), rng(conv, C * K, 4), rng(a, H, 4), rng(b, H, 4), rng(z, H * D, 4),
-                        rng(A_log, H, 4), rng(dt_bias, H, 4), rng(nw, D, 4)};
-    const Range out[] = {rng(state, C * (K - 1), 4), rng(S, H * D * D, 4), rng(y, H * D, 4), rng(ysum, H * D / 64, 4)};
-    for (int i = 0; i < 4; ++i) {
-        for (const Range &r : in)
-            if (overlap(out[i], r)) return ABG_EALIAS;
-        for (int k = i + 1; k < 4; ++k)
-            if (overlap(out[i], out[k])) return ABG_EALIAS;
-    }
-    return cuda_fail(launch_gdn(x, conv, state, a, b, z, A_log, dt_bias, nw, S, y, ysum, static_cast<int>(H),
-                                static_cast<int>(D), static_cast<int>(K), eps, eps_n,
-                                static_cast<cudaStream_t>(stream)),
-                     "gdn launch");
+    const abg_gdn_args g{x, conv, state, a, b, z, A_log, dt_bias, nw, S, y, ysum, H, D, K, eps, eps_n};
+    const abg_status st = check_gdn(g, mode);
+    if (st != ABG_OK) return st;
+    return cuda_fail(run_gdn(g, static_cast<cudaStream_t>(stream)), "gdn launch");
 }
 
 abg_status abg_atq(const float *q, const float *gate, const float *k, const float *v, const float *qn_w,
                    const float *kn_w, const float *cos, const float *sin, float *Kc, float *Vc, float *y, float *ysum,
                    int64_t Hq, int64_t Hkv, int64_t D, int64_t P, int64_t pos, float eps, int mode, void *stream) {
-    if (mode != ABG_TREE && mode != ABG_FAST) return ABG_EINVAL;
-    if (!q || !gate || !k || !v || !qn_w || !kn_w || !cos || !sin || !Kc || !Vc || !y || !ysum) return ABG_EINVAL;
-    if (Hq < 1 || Hkv < 1 || Hq % Hkv || (D != 64 && D != 128 && D != 256) || pos < 0 || pos >= P ||
-        pos + 1 > 8192 || Hq * D > (int64_t(1) << 20))
-        return ABG_ESHAPE;
-    const void *all[] = {q, gate, k, v, qn_w, kn_w, cos, sin, Kc, Vc, y, ysum};
-    for (const void *p : all)
-        if (!aligned(p, 4)) return ABG_EALIGN;
-    const Range in[] = {rng(q, Hq * D, 4),  rng(gate, Hq * D, 4), rng(k, Hkv * D, 4), rng(v, Hkv * D, 4),
-                        rng(qn_w, D, 4),    rng(kn_w, D, 4),      rng(cos, D / 2, 4), rng(sin, D / 2, 4)};
-    const Range out[] = {rng(Kc, Hkv * P * D, 4), rng(Vc, Hkv * P * D, 4), rng(y, Hq * D, 4), rng(ysum, Hq * D / 64, 4)};
-    for (int i = 0; i < 4; ++i) {
-        for (const Range &r : in)
-            if (overlap(out[i], r)) return ABG_EALIAS;
-        for (int k2 = i + 1; k2 < 4; ++k2)
-            if (overlap(out[i], out[k2])) return ABG_EALIAS;
-    }
-    return cuda_fail(launch_atq(q, gate, k, v, qn_w, kn_w, cos, sin, Kc, Vc, y, ysum, static_cast<int>(Hq),
-                                static_cast<int>(Hkv), static_cast<int>(D), static_cast<int>(P), static_cast<int>(pos),
-                                eps, static_cast<cudaStream_t>(stream)),
-                     "atq launch");
+    const abg_atq_args t{q, gate, k, v, qn_w, kn_w, cos, sin, Kc, Vc, y, ysum, Hq, Hkv, D, P, pos, eps};
+    const abg_status st = check_atq(t, mode);
+    if (st != ABG_OK) return st;
+    return cuda_fail(run_atq(t, nullptr, static_cast<cudaStream_t>(stream)), "atq launch");
 }
 
 abg_status abg_stage_graph_create(const abg_node *nodes, int64_t count, int mode, int rows_per_warp,
@@ -558,6 +607,12 @@ abg_status abg_stage_graph_create(const abg_node *nodes, int64_t count, int mode
         case ABG_NODE_RMSQ: st = check_rmsq(nd.x, nd.wt, nd.out, nd.out_sum, nd.len, node_group(nd.group), mode); break;
         case ABG_NODE_SWQ: st = check_swq(nd.x, nd.out, nd.out_sum, nd.len, node_group(nd.group), mode); break;
         case ABG_NODE_GSUM: st = check_gsum(nd.x, nd.out_sum, nd.len, node_group(nd.group), mode); break;
+        case ABG_NODE_GDN:
+            st = nd.args ? check_gdn(*static_cast<const abg_gdn_args *>(nd.args), mode) : ABG_EINVAL;
+            break;
+        case ABG_NODE_ATQ:
+            st = nd.args ? check_atq(*static_cast<const abg_atq_args *>(nd.args), mode) : ABG_EINVAL;
+            break;
         default: st = ABG_EINVAL;
         }
         if (st != ABG_OK) return st;
@@ -618,6 +673,10 @@ abg_status abg_stage_graph_create(const abg_node *nodes, int64_t count, int mode
                 abg_status st = plan_calls(&L.plan, group, mode, rows_per_warp);
                 if (st != ABG_OK) return st;
                 L.calls = group;
+            } else if (nd.kind == ABG_NODE_GDN) {
+                L.gdn = *static_cast<const abg_gdn_args *>(nd.args);
+            } else if (nd.kind == ABG_NODE_ATQ) {
+                L.atq = *static_cast<const abg_atq_args *>(nd.args);
             } else {
                 L.a = nd.x;
                 L.b = nd.wt;
@@ -642,6 +701,19 @@ abg_status abg_stage_graph_create(const abg_node *nodes, int64_t count, int mode
     }
     cudaError_t e = cudaSuccess;
     std::string where;
+    // each atq launch gets its own buffer for the chunk results
+    for (Launch &L : launches) {
+        if (L.kind != ABG_NODE_ATQ || e != cudaSuccess) continue;
+        void *p = nullptr;
+        const size_t bytes = atq_scratch_bytes(static_cast<int>(L.atq.Hq), static_cast<int>(L.atq.D),
+                                               static_cast<int>(L.atq.pos));
+        if ((e = cudaMalloc(&p, bytes)) != cudaSuccess) {
+            where = "cudaMalloc (atq chunk results)";
+            break;
+        }
+        g->scratch.push_back(p);
+        L.atq_scratch = static_cast<float *>(p);
+    }
     for (const Launch &L : launches)
         if (e == cudaSuccess && (e = prepare(L)) != cudaSuccess) where = "kernel attributes";
     cudaStream_t cs = nullptr;

@@ -20,6 +20,7 @@
 //     memory (coalesced over j).
 #include "abg_dev.cuh"
 #include "abg_kernels.cuh"
+#include "mixer.cuh"
 
 #include <mutex>
 
@@ -232,12 +233,25 @@ __global__ void __launch_bounds__(D) gdn_kernel(const float *__restrict__ x, con
 }
 
 template <int D>
+constexpr int gdn_smem() {
+    return D <= 128 ? D * D * 4 : 0;
+}
+
+// the shared-memory attribute, set once (before any stream capture when a
+// stage graph holds the launch)
+template <int D>
+cudaError_t gdn_attr() {
+    static const cudaError_t attr =
+        cudaFuncSetAttribute(gdn_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, gdn_smem<D>());
+    return attr;
+}
+
+template <int D>
 cudaError_t launch_gdn_d(const float *x, const float *conv, float *state, const float *a, const float *b,
                          const float *z, const float *A_log, const float *dt_bias, const float *nw, float *S,
                          float *y, float *ysum, int H, int K, float eps, float eps_n, cudaStream_t stream) {
-    constexpr int kSmem = D <= 128 ? D * D * 4 : 0;
-    static const cudaError_t attr =
-        cudaFuncSetAttribute(gdn_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    constexpr int kSmem = gdn_smem<D>();
+    const cudaError_t attr = gdn_attr<D>();
     if (attr != cudaSuccess) return attr;
     gdn_kernel<D><<<H, D, kSmem, stream>>>(x, conv, state, a, b, z, A_log, dt_bias, nw, S, y, ysum, H, K, eps,
                                            eps_n);
@@ -590,15 +604,30 @@ cudaError_t launch_gdn(const float *x, const float *conv, float *state, const fl
     }
 }
 
+cudaError_t prepare_gdn(int D) {
+    switch (D) {
+    case 64: return gdn_attr<64>();
+    case 128: return gdn_attr<128>();
+    case 256: return gdn_attr<256>();
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+size_t atq_scratch_bytes(int Hq, int D, int pos) {
+    const size_t nc = static_cast<size_t>(Hq) * ((pos + kAtqChunk) / kAtqChunk);
+    return (nc * kAtqChunk + 2 * nc + nc * D) * sizeof(float);
+}
+
 cudaError_t launch_atq(const float *q, const float *gate, const float *k, const float *v, const float *qn_w,
                        const float *kn_w, const float *cs, const float *sn, float *Kc, float *Vc, float *y,
-                       float *ysum, int Hq, int Hkv, int D, int P, int pos, float eps, cudaStream_t stream) {
+                       float *ysum, int Hq, int Hkv, int D, int P, int pos, float eps, float *scratch,
+                       cudaStream_t stream) {
     if (pos + 1 > kAtqMaxPositions || (D != 64 && D != 128 && D != 256)) return cudaErrorInvalidValue;
     AtqArgs a{q, gate, k, v, qn_w, kn_w, cs, sn, Kc, Vc, y, ysum, nullptr, nullptr, nullptr, nullptr,
               Hq, Hkv, P, pos, (pos + kAtqChunk) / kAtqChunk, eps};
     const size_t nsc = static_cast<size_t>(Hq) * a.C * kAtqChunk, nc = static_cast<size_t>(Hq) * a.C;
-    float *base = nullptr;
-    cudaError_t e = atq_scratch((nsc + 2 * nc + nc * D) * sizeof(float), &base);
+    float *base = scratch;
+    cudaError_t e = scratch ? cudaSuccess : atq_scratch(atq_scratch_bytes(Hq, D, pos), &base);
     if (e != cudaSuccess) return e;
     a.sc = base;
     a.cmax = base + nsc;

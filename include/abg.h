@@ -310,13 +310,44 @@ abg_status abg_atq(const float *q, const float *gate, const float *k, const floa
  *   ABG_NODE_RMSQ  x, wt, eps, len -> out (xn), out_sum (xsum)
  *   ABG_NODE_SWQ   x (2*len), len -> out (o), out_sum (osum)
  *   ABG_NODE_GSUM  x, len -> out_sum
+ *   ABG_NODE_GDN   args (abg_gdn_args): as abg_gdn; reads and writes state
+ *                  and S in place
+ *   ABG_NODE_ATQ   args (abg_atq_args): as abg_atq; writes row pos of Kc, Vc
+ *                  (the graph owns the buffer of the chunk results of each
+ *                  ATQ node, so replays of different graphs do not share it)
  * Every kind also reads `group` (0 means 64): the group size of the product's
  * scale, bias and xsum (Q4MV, including the group sums its prologue
  * computes) or of out_sum (RMSQ, SWQ, GSUM); Q4MV reads `sb_type` (an
  * abg_sb_type; scale and bias then point at that type).  Sizes given above
  * as cols/64 or len/64 are cols/group and len/group.
  * ------------------------------------------------------------------------- */
-typedef enum { ABG_NODE_Q4MV = 0, ABG_NODE_RMSQ = 1, ABG_NODE_SWQ = 2, ABG_NODE_GSUM = 3 } abg_node_kind;
+typedef enum {
+    ABG_NODE_Q4MV = 0,
+    ABG_NODE_RMSQ = 1,
+    ABG_NODE_SWQ = 2,
+    ABG_NODE_GSUM = 3,
+    ABG_NODE_GDN = 4, /* args -> abg_gdn_args */
+    ABG_NODE_ATQ = 5  /* args -> abg_atq_args */
+} abg_node_kind;
+
+/* The arguments of abg_gdn and abg_atq, for their stage-graph nodes (the
+ * struct is read when the graph is created; the pointers must stay valid for
+ * the graph's lifetime, like every node's). */
+typedef struct abg_gdn_args {
+    const float *x, *conv;
+    float *state;
+    const float *a, *b, *z, *A_log, *dt_bias, *nw;
+    float *S, *y, *ysum;
+    int64_t H, D, K;
+    float eps, eps_n;
+} abg_gdn_args;
+
+typedef struct abg_atq_args {
+    const float *q, *gate, *k, *v, *qn_w, *kn_w, *cos, *sin;
+    float *Kc, *Vc, *y, *ysum;
+    int64_t Hq, Hkv, D, P, pos;
+    float eps;
+} abg_atq_args;
 typedef enum { ABG_PRO_NONE = 0, ABG_PRO_GSUM = 1, ABG_PRO_RMSQ = 2, ABG_PRO_SWQ = 3 } abg_prologue;
 
 typedef struct abg_node {
@@ -337,6 +368,7 @@ typedef struct abg_node {
     int64_t len;       /* RMSQ, SWQ, GSUM vector length n */
     int32_t group;     /* group size 32, 64 or 128; 0 = 64 */
     int32_t sb_type;   /* Q4MV: abg_sb_type of scale and bias */
+    const void *args;  /* GDN: abg_gdn_args; ATQ: abg_atq_args */
 } abg_node;
 
 /* Validates every node (same rules as the single calls), checks that no node

@@ -40,21 +40,25 @@ def test_every_declared_function_is_exported(lib):
     assert set(names) <= exported
 
 
-def test_node_struct_layout_matches_c(tmp_path):
-    """sizeof and field offsets of struct abg_node as gcc sees the header."""
-    fields = [f for f, _ in abg._Node._fields_]
+@pytest.mark.parametrize("ctype,cname", [(abg._Node, "abg_node"), (abg._GdnArgs, "abg_gdn_args"),
+                                         (abg._AtqArgs, "abg_atq_args")])
+def test_struct_layout_matches_c(tmp_path, ctype, cname):
+    """sizeof and field offsets of the node and mixer-argument structs as gcc
+    sees the header."""
+    fields = [f for f, _ in ctype._fields_]
     prog = tmp_path / "layout.c"
     lines = ["#include <stdio.h>", "#include <stddef.h>", '#include "abg.h"', "int main(void){",
-             'printf("%zu\\n", sizeof(abg_node));']
-    lines += [f'printf("%zu\\n", offsetof(abg_node, {f}));' for f in fields]
+             f'printf("%zu\\n", sizeof({cname}));']
+    lines += [f'printf("%zu\\n", offsetof({cname}, {f}));' for f in fields]
     lines += ["return 0;}"]
     prog.write_text("\n".join(lines))
     exe = tmp_path / "layout"
     subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), str(prog), "-o", str(exe)], check=True)
     out = [int(v) for v in subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()]
-    assert out[0] == ctypes.sizeof(abg._Node)
+    assert out[0] == ctypes.sizeof(ctype)
+    assert len(out) == len(fields) + 1
     for f, off in zip(fields, out[1:]):
-        assert getattr(abg._Node, f).offset == off, f
+        assert getattr(ctype, f).offset == off, f
 
 
 def test_status_strings(lib):
@@ -176,6 +180,56 @@ def test_stage_graph_validation(lib):
     assert create(lib, [node(**prod), node(**{**prod, "w": A + 0x600000})]) == EALIAS
     assert lib.abg_stage_graph_launch(None, None) == EINVAL
     assert lib.abg_stage_graph_destroy(None) == EINVAL
+
+
+def _gdn_args(H=4, D=128, K=4, **over):
+    """gdn arguments at fake, well-separated addresses (16 MiB apart)."""
+    names = ["x", "conv", "state", "a", "b", "z", "A_log", "dt_bias", "nw", "S", "y", "ysum"]
+    kw = {n: 0x7F0000100000 + (1 << 24) * i for i, n in enumerate(names)}
+    kw.update(H=H, D=D, K=K, eps=1e-6, eps_n=1e-6)
+    kw.update(over)
+    return abg._GdnArgs(**kw)
+
+
+def _atq_args(Hq=8, Hkv=2, D=128, P=4096, pos=100, **over):
+    names = ["q", "gate", "k", "v", "qn_w", "kn_w", "cos", "sin", "Kc", "Vc", "y", "ysum"]
+    kw = {n: 0x7E0000100000 + (1 << 26) * i for i, n in enumerate(names)}
+    kw.update(Hq=Hq, Hkv=Hkv, D=D, P=P, pos=pos, eps=1e-6)
+    kw.update(over)
+    return abg._AtqArgs(**kw)
+
+
+def test_stage_graph_mixer_node_validation(lib):
+    """gdn and atq nodes: null or invalid argument structs are refused as the
+    direct calls refuse them, and their outputs (including the state and the
+    caches they update in place) take part in the stage hazard checks."""
+    assert create(lib, [node(kind=abg.NODE_GDN, stage=0)]) == EINVAL           # no args
+    assert create(lib, [node(kind=abg.NODE_ATQ, stage=0)]) == EINVAL
+    g = _gdn_args(D=96)
+    assert create(lib, [node(kind=abg.NODE_GDN, stage=0, args=ctypes.addressof(g))]) == ESHAPE
+    g = _gdn_args(S=0x7F0000100000 + 9 * (1 << 24) + 4)                         # S not 16-byte aligned
+    assert create(lib, [node(kind=abg.NODE_GDN, stage=0, args=ctypes.addressof(g))]) == EALIGN
+    g = _gdn_args(y=0x7F0000100000)                                             # y == x
+    assert create(lib, [node(kind=abg.NODE_GDN, stage=0, args=ctypes.addressof(g))]) == EALIAS
+    t = _atq_args(pos=4096)                                                     # pos >= P
+    assert create(lib, [node(kind=abg.NODE_ATQ, stage=0, args=ctypes.addressof(t))]) == ESHAPE
+    t = _atq_args(Hq=6, Hkv=4)
+    assert create(lib, [node(kind=abg.NODE_ATQ, stage=0, args=ctypes.addressof(t))]) == ESHAPE
+    # a product in the gdn node's stage reading its y
+    g = _gdn_args()
+    prod = dict(kind=0, stage=0, w=A, scale=A + 0x100000, bias=A + 0x200000, rows=8, cols=128, row0=0, n=8,
+                y=A + 0x400000, x=g.y, xsum=A + 0x310000)
+    gn = node(kind=abg.NODE_GDN, stage=0, args=ctypes.addressof(g))
+    assert create(lib, [gn, node(**prod)]) == EALIAS
+    # a product of the same stage reading the recurrent state S the node updates
+    assert create(lib, [gn, node(**{**prod, "x": g.S})]) == EALIAS
+    # an atq node writing a product's weights (its value cache over w)
+    t = _atq_args(Vc=A)
+    tn = node(kind=abg.NODE_ATQ, stage=0, args=ctypes.addressof(t))
+    assert create(lib, [tn, node(**{**prod, "stage": 1, "x": A + 0x300000})]) == EALIAS
+    # two mixers of one stage that share an output
+    t2 = _atq_args(y=g.y)
+    assert create(lib, [gn, node(kind=abg.NODE_ATQ, stage=0, args=ctypes.addressof(t2))]) == EALIAS
 
 
 def test_tuning_validation(lib):

@@ -13,7 +13,7 @@ import pytest
 
 import oracle
 from affine_bit_group_gb300 import synth
-from helpers import assert_bits_equal, dev, empty, host
+from helpers import assert_bits_equal, dev, dev_words, empty, host
 
 pytestmark = pytest.mark.gpu
 
@@ -101,3 +101,56 @@ def test_atq_bit_exact(Hq, Hkv, D, P, pos):
 
 def test_atq_tokens_append_rows():
     run_atq(synth.atq_case(np.random.default_rng(5), 4, 2, 128, 256, 60), tokens=5)
+
+
+def test_mixers_as_stage_graph_nodes():
+    """gdn and atq as nodes of one stage of a stage graph, each followed in the
+    next stage by a product reading its y and group sums.  Every replay is the
+    oracle's next token, bit for bit (the gdn state carried, the atq cache row
+    rewritten), also with a direct atq call at a later position (which grows
+    the calls' shared buffer) between replays: the graph's atq has its own."""
+    rng = np.random.default_rng(11)
+    cg = synth.gdn_case(rng)                              # y: 16 x 128
+    ca = synth.atq_case(rng, 4, 2, 128, 600, 300)        # y: 4 x 128
+    Hg, Dg = cg["S"].shape[0], cg["S"].shape[1]
+    Dq = ca["Kc"].shape[2]
+    Hq = ca["q"].size // Dq
+    mg, ma = synth.q4_matrix(rng, 1000, Hg * Dg), synth.q4_matrix(rng, 700, Hq * Dq)
+    g_ = {k: dev(v) for k, v in cg.items()}
+    a_ = {k: dev(v) for k, v in ca.items() if k != "pos"}
+    wg, wa = [dev_words(mg.w), dev(mg.scale), dev(mg.bias)], [dev_words(ma.w), dev(ma.scale), dev(ma.bias)]
+    yg, ysg, ya, ysa = empty(Hg * Dg), empty(Hg * Dg // 64), empty(Hq * Dq), empty(Hq * Dq // 64)
+    og, oa = empty(mg.rows), empty(ma.rows)
+    N = abg.Node
+    nodes = [N.gdn(0, g_["x"], g_["conv"], g_["state"], g_["a"], g_["b"], g_["z"], g_["A_log"], g_["dt_bias"],
+                   g_["nw"], g_["S"], yg, ysg),
+             N.atq(0, a_["q"], a_["gate"], a_["k"], a_["v"], a_["qn_w"], a_["kn_w"], a_["cos"], a_["sin"], a_["Kc"],
+                   a_["Vc"], ya, ysa, pos=ca["pos"]),
+             N.q4mv(1, *wg, og, Hg * Dg, yg, ysg),
+             N.q4mv(1, *wa, oa, Hq * Dq, ya, ysa)]
+    keep = list(g_.values()) + list(a_.values()) + wg + wa + [yg, ysg, ya, ysa, og, oa]
+    graph = abg.StageGraph(nodes, keep=keep)
+    assert graph.launches == 4
+    other = synth.atq_case(np.random.default_rng(12), 8, 2, 256, 4096, 4000)
+    o_ = {k: dev(v) for k, v in other.items() if k != "pos"}
+    S_ref, st_ref, Kr, Vr = cg["S"], cg["state"], ca["Kc"], ca["Vc"]
+    for t in range(3):
+        graph.launch()
+        if t == 1:
+            abg.atq(o_["q"], o_["gate"], o_["k"], o_["v"], o_["qn_w"], o_["kn_w"], o_["cos"], o_["sin"], o_["Kc"],
+                    o_["Vc"], empty(8 * 256), empty(32), pos=other["pos"])
+        torch.cuda.synchronize()
+        ey, eys, S_ref, st_ref = oracle.gdn(**dict(cg, S=S_ref, state=st_ref))
+        ay, ays, Kr, Vr = oracle.atq(**dict(ca, Kc=Kr, Vc=Vr))
+        assert_bits_equal(host(yg), ey, f"gdn y, replay {t}")
+        assert_bits_equal(host(ysg), eys, f"gdn ysum, replay {t}")
+        assert_bits_equal(host(g_["S"]).reshape(S_ref.shape), S_ref, f"gdn S, replay {t}")
+        assert_bits_equal(host(g_["state"]).reshape(st_ref.shape), st_ref, f"gdn conv state, replay {t}")
+        assert_bits_equal(host(ya), ay, f"atq y, replay {t}")
+        assert_bits_equal(host(ysa), ays, f"atq ysum, replay {t}")
+        assert_bits_equal(host(a_["Kc"]).reshape(Kr.shape), Kr, f"K cache, replay {t}")
+        assert_bits_equal(host(a_["Vc"]).reshape(Vr.shape), Vr, f"V cache, replay {t}")
+        assert_bits_equal(host(og), oracle.q4mv(mg.w, mg.scale, mg.bias, ey, eys, Hg * Dg), f"gdn product {t}")
+        assert_bits_equal(host(oa), oracle.q4mv(ma.w, ma.scale, ma.bias, ay, ays, Hq * Dq), f"atq product {t}")
+    graph.close()
+    assert abg.device_status(clear=True) == 0
