@@ -236,6 +236,7 @@ abg_status check_atq(const abg_atq_args &t, int mode) {
     const void *all[] = {t.q, t.gate, t.k, t.v, t.qn_w, t.kn_w, t.cos, t.sin, t.Kc, t.Vc, t.y, t.ysum};
     for (const void *p : all)
         if (!aligned(p, 4)) return ABG_EALIGN;
+    if (!aligned(t.Kc, 16) || !aligned(t.Vc, 16)) return ABG_EALIGN;  // cache rows are read as 16-byte units
     std::vector<Range> in, out;
     atq_io(t, in, out);
     return disjoint_outputs(in, out);
@@ -246,10 +247,12 @@ cudaError_t run_gdn(const abg_gdn_args &g, cudaStream_t s) {
                       static_cast<int>(g.H), static_cast<int>(g.D), static_cast<int>(g.K), g.eps, g.eps_n, s);
 }
 
+bool pdl_enabled();
+
 cudaError_t run_atq(const abg_atq_args &t, float *scratch, cudaStream_t s) {
     return launch_atq(t.q, t.gate, t.k, t.v, t.qn_w, t.kn_w, t.cos, t.sin, t.Kc, t.Vc, t.y, t.ysum,
                       static_cast<int>(t.Hq), static_cast<int>(t.Hkv), static_cast<int>(t.D), static_cast<int>(t.P),
-                      static_cast<int>(t.pos), t.eps, scratch, s);
+                      static_cast<int>(t.pos), t.eps, scratch, pdl_enabled(), s);
 }
 
 // --------------------------------------------------------------- graphs ----
@@ -341,6 +344,8 @@ abg_status fuse_swiglu_pairs(std::vector<Launch> &launches, StageGraph *g, int m
 
 cudaError_t prepare(const Launch &L) {
     if (L.kind == ABG_NODE_GDN) return prepare_gdn(static_cast<int>(L.gdn.D));
+    if (L.kind == ABG_NODE_ATQ)
+        return prepare_atq(static_cast<int>(L.atq.Hq), static_cast<int>(L.atq.Hkv), static_cast<int>(L.atq.D));
     if (L.kind != ABG_NODE_Q4MV) return cudaSuccess;
     return prepare_q4mv(L.plan);
 }

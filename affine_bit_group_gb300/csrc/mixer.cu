@@ -262,284 +262,385 @@ cudaError_t launch_gdn_d(const float *x, const float *conv, float *state, const 
 // One token of gated attention ("Metal: queued rmsq, swq, gdn and atq
 // kernels ...", Change, the Array.atq bullet: q/k RMS norm and rotation, the
 // new k/v into the caches, scores, softmax, weighted values, sigmoid gate and
-// group sums; one threadgroup per query head, the first head of each KV group
-// writing the cache row while the others use the new k/v).
+// group sums; the first head of each KV group writing the cache row while the
+// others use the new k/v).
 //
-// The positions t = 0..pos are split into chunks of 256 (one block per query
-// head and chunk), in four launches on the stream: scores and the
-// chunk's maximum; the exponentials and the chunk's sum; the probabilities
-// and the chunk's weighted values; the tree over the chunks, the gate and the
-// group sums.  Every sum over positions is the pairwise tree with an odd
-// element carried, which equals the tree over the positions padded with -0
-// to a power of two (carrying is adding -0); the padded tree's subtrees are
-// the aligned 32-position blocks and 256-position chunks, so the chunks'
-// sums, combined by the tree, give the oracle's bits.
+// A block takes GB query heads of one KV group (GB = 4, 2 or 1, dividing the
+// group) and one chunk of 64 positions.  Four launches, the last three
+// started early by programmatic dependent launch:
+//   scores: the normed, rotated queries (and, in the chunk holding pos, the
+//     key, written to the cache row with the new value by the group's first
+//     block), the chunk's scores (each row of keys read once for the GB
+//     heads) and each head's maximum over the chunk;
+//   exponentials: each head's maximum over the chunks, the chunk's
+//     exponentials (in place of the scores) and their sum;
+//   values: before its wait it copies the chunk's value rows into shared
+//     memory (rows below pos, which no earlier launch of the call writes; row
+//     pos is the new v); then Z, the tree over the chunks' sums, the
+//     probabilities e/Z and the chunk's weighted values;
+//   out (one block a head): the tree over the chunks' weighted values (one
+//     bulk copy of them), the sigmoid gate and the group sums.
+// Every sum over positions is the pairwise tree with an odd element carried,
+// which equals the tree over the positions padded with -0 to a power of two
+// (carrying is adding -0); its aligned subtrees of 32 and 64 positions are
+// the warps' and chunks' sums, so the pieces, combined by the tree over the
+// chunks (padded with -0 to 128), give the oracle's bits.
 constexpr int kAtqMaxPositions = 8192;
-constexpr int kAtqChunk = 256;
-constexpr int kAtqMaxChunks = kAtqMaxPositions / kAtqChunk;
-
-// The maximum over the block's D threads (exact in any order).
-template <int D>
-__device__ __forceinline__ float block_max(float v, float *red) {
-#pragma unroll
-    for (int d = 1; d < 32; d <<= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, d));
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
-    __syncthreads();
-    float m = red[0];
-#pragma unroll
-    for (int i = 1; i < D / 32; ++i) m = fmaxf(m, red[i]);
-    __syncthreads();
-    return m;
-}
-
-// RMS norm with weights, then the rotation of column pairs (i, i + D/2):
-// thread j's rotated value.  `un` (D floats of shared memory) carries the
-// normed values between the threads.
-template <int D>
-__device__ __forceinline__ float rms_rotate(float u, float w, const float *cs, const float *sn, float eps,
-                                            float *un, float *red) {
-    const int j = threadIdx.x;
-    const float mean = __fdiv_rn(block_tree<D>(__fmul_rn(u, u), red), static_cast<float>(D));
-    const float r = __frcp_rn(__fsqrt_rn(__fadd_rn(mean, eps)));
-    un[j] = __fmul_rn(__fmul_rn(u, r), w);
-    __syncthreads();
-    float out;
-    if (j < D / 2) {
-        out = __fsub_rn(__fmul_rn(un[j], cs[j]), __fmul_rn(un[j + D / 2], sn[j]));
-    } else {
-        const int i = j - D / 2;
-        out = __fadd_rn(__fmul_rn(un[j], cs[i]), __fmul_rn(un[i], sn[i]));
-    }
-    __syncthreads();  // un is reused
-    return out;
-}
-
-// The same two steps in a block wider than D: only threads j < D hold a
-// column (the others pass 0 and get 0); every thread of the block calls them.
-template <int D>
-__device__ __forceinline__ float block_tree_first(float v, float *red) {
-    constexpr int NW = D / 32;
-#pragma unroll
-    for (int d = 1; d < 32; d <<= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, d));
-    if ((threadIdx.x & 31) == 0 && (threadIdx.x >> 5) < NW) red[threadIdx.x >> 5] = v;
-    __syncthreads();
-    float w[NW];
-#pragma unroll
-    for (int i = 0; i < NW; ++i) w[i] = red[i];
-#pragma unroll
-    for (int h = NW / 2; h >= 1; h >>= 1)
-#pragma unroll
-        for (int i = 0; i < h; ++i) w[i] = __fadd_rn(w[2 * i], w[2 * i + 1]);
-    __syncthreads();
-    return w[0];
-}
-
-template <int D>
-__device__ __forceinline__ float rms_rotate_first(float u, float w, const float *cs, const float *sn, float eps,
-                                                  float *un, float *red) {
-    const int j = threadIdx.x;
-    const float mean = __fdiv_rn(block_tree_first<D>(__fmul_rn(u, u), red), static_cast<float>(D));
-    const float r = __frcp_rn(__fsqrt_rn(__fadd_rn(mean, eps)));
-    if (j < D) un[j] = __fmul_rn(__fmul_rn(u, r), w);
-    __syncthreads();
-    float out = 0.0f;
-    if (j < D / 2) {
-        out = __fsub_rn(__fmul_rn(un[j], cs[j]), __fmul_rn(un[j + D / 2], sn[j]));
-    } else if (j < D) {
-        const int i = j - D / 2;
-        out = __fadd_rn(__fmul_rn(un[j], cs[i]), __fmul_rn(un[i], sn[i]));
-    }
-    __syncthreads();
-    return out;
-}
-
-// The pairwise tree over v[0 .. m), padded with -0 to a power of two (m <= 32).
-__device__ __forceinline__ float tree_padded32(const float *v, int m) {
-    float e[32];
-#pragma unroll
-    for (int i = 0; i < 32; ++i) e[i] = i < m ? v[i] : -0.0f;
-    int p = 1;
-    while (p < m) p <<= 1;
-    for (int h = p / 2; h >= 1; h >>= 1)
-#pragma unroll
-        for (int i = 0; i < 16; ++i)
-            if (i < h) e[i] = __fadd_rn(e[2 * i], e[2 * i + 1]);
-    return e[0];
-}
+constexpr int kAtqL = 64;          // positions per chunk
+constexpr int kAtqThreads = 256;   // scores: 8 warps of 8 positions
+constexpr int kAtqValThreads = 1024;
+constexpr int kAtqMaxChunks = kAtqMaxPositions / kAtqL;
 
 struct AtqArgs {
     const float *q, *gate, *k, *v, *qn_w, *kn_w, *cs, *sn;
     float *Kc, *Vc, *y, *ysum;
-    float *sc;    // [Hq][C*256] scores, then exponentials
-    float *cmax;  // [Hq][C] the chunks' maxima
-    float *csum;  // [Hq][C] the chunks' sums of exponentials
-    float *opart; // [Hq][C][D] the chunks' weighted values
+    float *sc;     // [Hq][C*64] scores, then their exponentials
+    float *cmax;   // [Hq][C] the chunks' maxima
+    float *csum;   // [Hq][C] the chunks' sums of exponentials
+    float *opart;  // [Hq][C][D] the chunks' weighted values
     int Hq, Hkv, P, pos, C;
     float eps;
 };
 
-// 1: the rotated query (and key), the cache row (written by the group's first
-// head, in the chunk holding pos), the chunk's scores and their maximum.  32
-// warps, 8 rows each: the chunk's 256 rows are loaded in one step.
-constexpr int kAtqScoreThreads = 1024;
+// Query heads per block: 4, 2 or 1, dividing the heads of a KV group.
+__host__ __device__ constexpr int atq_heads_per_block(int per) { return per % 4 == 0 ? 4 : (per % 2 == 0 ? 2 : 1); }
 
-template <int D>
-__global__ void __launch_bounds__(kAtqScoreThreads) atq_scores_kernel(const __grid_constant__ AtqArgs a) {
-    constexpr int NW = kAtqScoreThreads / 32, CPL = D / 32, kRows = kAtqChunk / NW;
-    __shared__ float un[D], qr_s[D], kr_s[D];
-    __shared__ float red[NW];
-    const int h = blockIdx.x, c = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int j = tid < D ? tid : 0;
-    const int g = h / (a.Hq / a.Hkv), n = a.pos + 1;
-    const float qr = rms_rotate_first<D>(tid < D ? a.q[static_cast<int64_t>(h) * D + j] : 0.0f, a.qn_w[j], a.cs,
-                                         a.sn, a.eps, un, red);
-    const float kr = rms_rotate_first<D>(tid < D ? a.k[static_cast<int64_t>(g) * D + j] : 0.0f, a.kn_w[j], a.cs,
-                                         a.sn, a.eps, un, red);
-    if (tid < D) {
-        qr_s[j] = qr;
-        kr_s[j] = kr;
-        if (h % (a.Hq / a.Hkv) == 0 && c == a.C - 1) {
-            a.Kc[(static_cast<int64_t>(g) * a.P + a.pos) * D + j] = kr;
-            a.Vc[(static_cast<int64_t>(g) * a.P + a.pos) * D + j] = a.v[static_cast<int64_t>(g) * D + j];
+// Sums each of a lane's N values (N a power of two, at most 32) over the
+// warp's 32 lanes by the pairwise tree in lane order.  At distances 1, 2, ...
+// N/2 each lane keeps half of its values and adds the partner's partial sums
+// of them (a transposed butterfly); the rest is a plain butterfly.  Lane l
+// ends with the sum of value rev(l mod N) (its log2 N low bits reversed).
+template <int N>
+__device__ __forceinline__ float warp_sums(float (&v)[N], int lane) {
+#pragma unroll
+    for (int d = 1; d < N; d <<= 1) {
+        const int cnt = N / (2 * d);
+        const bool up = (lane & d) != 0;
+#pragma unroll
+        for (int i = 0; i < cnt; ++i) {
+            const float send = up ? v[i] : v[i + cnt];
+            const float keep = up ? v[i + cnt] : v[i];
+            v[i] = __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, send, d));
+        }
+    }
+    float x = v[0];
+#pragma unroll
+    for (int d = N; d < 32; d <<= 1) x = __fadd_rn(x, __shfl_xor_sync(0xffffffffu, x, d));
+    return x;
+}
+
+template <int N>
+__device__ __forceinline__ int rev_low_bits(int l) {
+    int r = 0;
+#pragma unroll
+    for (int b = 1; b < N; b <<= 1) r = (r << 1) | ((l & b) ? 1 : 0);
+    return r;
+}
+
+// CPL consecutive floats at p (CPL * 4 bytes aligned).
+template <int CPL>
+__device__ __forceinline__ void load_cols(const float *p, float (&o)[CPL]) {
+    if constexpr (CPL % 4 == 0) {
+#pragma unroll
+        for (int i = 0; i < CPL / 4; ++i) {
+            const float4 t = reinterpret_cast<const float4 *>(p)[i];
+            o[4 * i] = t.x, o[4 * i + 1] = t.y, o[4 * i + 2] = t.z, o[4 * i + 3] = t.w;
+        }
+    } else {
+        const float2 t = *reinterpret_cast<const float2 *>(p);
+        o[0] = t.x, o[1] = t.y;
+    }
+}
+
+// The maximum over v[0 .. C) by one warp (exact in any order).
+__device__ __forceinline__ float warp_max_of(const float *v, int C, int lane) {
+    float mx = -__int_as_float(0x7f800000);
+    for (int i = lane; i < C; i += 32) mx = fmaxf(mx, __ldcg(v + i));
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, d));
+    return mx;
+}
+
+template <int D, int GB>
+__global__ void __launch_bounds__(kAtqThreads) atq_scores_kernel(const __grid_constant__ AtqArgs a) {
+    constexpr int CPL = D / 32, NV = 8 * GB, NR = GB + 1, kStep = kAtqThreads / D;
+    constexpr int kRows = (NR + kStep - 1) / kStep;  // norm rows a thread takes
+    __shared__ __align__(16) float un[NR][D];
+    __shared__ __align__(16) float rot[NR][D];
+    __shared__ float red[NR][D / 32];
+    __shared__ float ssc[GB][kAtqL];
+    // the next launch reads nothing of this one before its own wait
+    grid_dep_launch();
+    const int s = blockIdx.x, c = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int per = a.Hq / a.Hkv, h0 = s * GB, g = h0 / per, n = a.pos + 1, t_lo = c * kAtqL;
+    const bool holds_pos = c == a.C - 1;
+    const int nr = GB + (holds_pos ? 1 : 0);  // the query rows, and the key in the chunk holding pos
+    // the rows to norm (row r of the thread's column j: r0 + k*kStep), their
+    // weights and this column's rotation, read ahead of the cache rows
+    const int j = tid % D, r0 = tid / D, ji = j % (D / 2);
+    float u[kRows];
+#pragma unroll
+    for (int k = 0; k < kRows; ++k) {
+        const int r = r0 + k * kStep;
+        u[k] = r < nr ? (r < GB ? a.q[static_cast<int64_t>(h0 + r) * D + j] : a.k[static_cast<int64_t>(g) * D + j])
+                      : 0.0f;
+    }
+    const float wq = a.qn_w[j], wk = a.kn_w[j], cj = a.cs[ji], sj = a.sn[ji];
+    // cache rows t_lo + 8 warp + r (r < 8) below pos; lane l holds columns
+    // l*CPL .. l*CPL+CPL-1 (row pos is this block's own key)
+    const float *Kg = a.Kc + static_cast<int64_t>(g) * a.P * D + lane * CPL;
+    const int tw = t_lo + 8 * warp;
+    float kv[8][CPL];
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+        if (tw + r < a.pos) {
+            load_cols<CPL>(Kg + static_cast<int64_t>(tw + r) * D, kv[r]);
+        } else {
+#pragma unroll
+            for (int cc = 0; cc < CPL; ++cc) kv[r][cc] = 0.0f;
+        }
+    }
+    // RMS norms: the rows' sums of squares (a warp holds 32 consecutive
+    // columns of one row: the butterfly, then the tree over the warps)
+#pragma unroll
+    for (int k = 0; k < kRows; ++k) {
+        const int r = r0 + k * kStep;
+        if (r < nr) {
+            float sq = __fmul_rn(u[k], u[k]);
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) sq = __fadd_rn(sq, __shfl_xor_sync(0xffffffffu, sq, d));
+            if (lane == 0) red[r][j >> 5] = sq;
         }
     }
     __syncthreads();
-    // warp w takes rows t_lo + kRows*w ..; lane l the columns l*CPL .. l*CPL +
-    // CPL-1 (their tree, then the butterfly: the tree over D).  Row pos is this
-    // block's own key (the cache row may be written by another block).
-    const float *Kg = a.Kc + static_cast<int64_t>(g) * a.P * D;
-    const float scale = __frcp_rn(__fsqrt_rn(static_cast<float>(D)));
-    const int t_lo = c * kAtqChunk, t_hi = min(t_lo + kAtqChunk, n);
-    float mx = -__int_as_float(0x7f800000);
-    // (at most 32 loaded values a lane at a time: 64 registers a thread)
-    constexpr int kPass = 32 / CPL < kRows ? 32 / CPL : kRows;
 #pragma unroll
-    for (int r0 = 0; r0 < kRows; r0 += kPass) {
-        const int t0 = t_lo + warp * kRows + r0;
-        float kv[kPass][CPL];
+    for (int k = 0; k < kRows; ++k) {
+        const int r = r0 + k * kStep;
+        if (r < nr) {
+            float w[D / 32];
 #pragma unroll
-        for (int r = 0; r < kPass; ++r) {
-            const int t = t0 + r;
-            const float *kt = t == a.pos ? kr_s : Kg + static_cast<int64_t>(t < t_hi ? t : t_lo) * D;
+            for (int i = 0; i < D / 32; ++i) w[i] = red[r][i];
 #pragma unroll
-            for (int cc = 0; cc < CPL; ++cc) kv[r][cc] = kt[lane * CPL + cc];
+            for (int h = D / 64; h >= 1; h >>= 1)
+#pragma unroll
+                for (int i = 0; i < h; ++i) w[i] = __fadd_rn(w[2 * i], w[2 * i + 1]);
+            const float mean = __fdiv_rn(w[0], static_cast<float>(D));
+            const float f = __frcp_rn(__fsqrt_rn(__fadd_rn(mean, a.eps)));
+            un[r][j] = __fmul_rn(__fmul_rn(u[k], f), r < GB ? wq : wk);
         }
+    }
+    __syncthreads();
+    // the rotation of column pairs (i, i + D/2)
 #pragma unroll
-        for (int r = 0; r < kPass; ++r) {
+    for (int k = 0; k < kRows; ++k) {
+        const int r = r0 + k * kStep;
+        if (r < nr)
+            rot[r][j] = j < D / 2 ? __fsub_rn(__fmul_rn(un[r][j], cj), __fmul_rn(un[r][j + D / 2], sj))
+                                  : __fadd_rn(__fmul_rn(un[r][j], cj), __fmul_rn(un[r][ji], sj));
+    }
+    __syncthreads();
+    if (holds_pos && h0 % per == 0) {
+        const int64_t row = (static_cast<int64_t>(g) * a.P + a.pos) * D;
+        for (int jj = tid; jj < D; jj += kAtqThreads) {
+            a.Kc[row + jj] = rot[GB][jj];
+            a.Vc[row + jj] = a.v[static_cast<int64_t>(g) * D + jj];
+        }
+    }
+    float qv[GB][CPL];
+#pragma unroll
+    for (int hh = 0; hh < GB; ++hh)
+#pragma unroll
+        for (int cc = 0; cc < CPL; ++cc) qv[hh][cc] = rot[hh][lane * CPL + cc];
+#pragma unroll
+    for (int r = 0; r < 8; ++r)
+        if (tw + r == a.pos)
+#pragma unroll
+            for (int cc = 0; cc < CPL; ++cc) kv[r][cc] = rot[GB][lane * CPL + cc];
+    // value hh*8 + r: the lane's tree over its columns of q_hh . k_r
+    float vals[NV];
+#pragma unroll
+    for (int hh = 0; hh < GB; ++hh)
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
             float pr[CPL];
 #pragma unroll
-            for (int cc = 0; cc < CPL; ++cc) pr[cc] = __fmul_rn(qr_s[lane * CPL + cc], kv[r][cc]);
+            for (int cc = 0; cc < CPL; ++cc) pr[cc] = __fmul_rn(qv[hh][cc], kv[r][cc]);
 #pragma unroll
-            for (int hh = CPL / 2; hh >= 1; hh >>= 1)
+            for (int h = CPL / 2; h >= 1; h >>= 1)
 #pragma unroll
-                for (int cc = 0; cc < hh; ++cc) pr[cc] = __fadd_rn(pr[2 * cc], pr[2 * cc + 1]);
-            float dot = pr[0];
+                for (int cc = 0; cc < h; ++cc) pr[cc] = __fadd_rn(pr[2 * cc], pr[2 * cc + 1]);
+            vals[hh * 8 + r] = pr[0];
+        }
+    const float dot = warp_sums<NV>(vals, lane);
+    if (lane < NV) {
+        const int idx = rev_low_bits<NV>(lane), hh = idx >> 3, r = idx & 7;
+        const float scale = __frcp_rn(__fsqrt_rn(static_cast<float>(D)));
+        ssc[hh][8 * warp + r] = __fmul_rn(dot, scale);
+    }
+    __syncthreads();
+    if (warp < GB) {
+        const int h = h0 + warp;
+        float mx = -__int_as_float(0x7f800000);
+        float *sh = a.sc + static_cast<int64_t>(h) * a.C * kAtqL + t_lo;
 #pragma unroll
-            for (int d = 1; d < 32; d <<= 1) dot = __fadd_rn(dot, __shfl_xor_sync(0xffffffffu, dot, d));
-            const float sv = __fmul_rn(dot, scale);
-            if (t0 + r < t_hi) {
+        for (int i = lane; i < kAtqL; i += 32) {
+            if (t_lo + i < n) {
+                const float sv = ssc[warp][i];
+                sh[i] = sv;
                 mx = fmaxf(mx, sv);
-                if (lane == 0) a.sc[static_cast<int64_t>(h) * a.C * kAtqChunk + t0 + r] = sv;
             }
         }
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, d));
+        if (lane == 0) a.cmax[h * a.C + c] = mx;
     }
-    const float m = block_max<kAtqScoreThreads>(mx, red);
-    if (tid == 0) a.cmax[h * a.C + c] = m;
 }
 
-// 2: the exponentials of the chunk (against the head's maximum) and their sum.
-template <int D>
-__global__ void __launch_bounds__(D) atq_exp_kernel(const __grid_constant__ AtqArgs a) {
-    __shared__ float es[kAtqChunk];
-    __shared__ float red[D / 32];
-    const int h = blockIdx.x, c = blockIdx.y, j = threadIdx.x;
-    const int n = a.pos + 1, t_lo = c * kAtqChunk;
-    float mx = -__int_as_float(0x7f800000);
-    for (int i = j; i < a.C; i += D) mx = fmaxf(mx, a.cmax[h * a.C + i]);
-    const float m = block_max<D>(mx, red);
-    float *sh = a.sc + static_cast<int64_t>(h) * a.C * kAtqChunk;
-    for (int i = j; i < kAtqChunk; i += D) {
-        const int t = t_lo + i;
-        float e = -0.0f;
-        if (t < n) {
-            e = exp_tree(__fsub_rn(sh[t], m));
-            sh[t] = e;
+// Thread i < GB*64: head i / 64, position t_lo + i % 64 (a warp holds 32
+// consecutive positions: its butterfly is their tree).
+template <int GB>
+__global__ void __launch_bounds__(kAtqThreads) atq_exp_kernel(const __grid_constant__ AtqArgs a) {
+    __shared__ float s_m[GB];
+    __shared__ float red[kAtqThreads / 32];
+    // the values launch may start and copy its value rows meanwhile
+    grid_dep_launch();
+    const int s = blockIdx.x, c = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int h0 = s * GB, n = a.pos + 1, t_lo = c * kAtqL;
+    const int hh = tid / kAtqL, i = tid % kAtqL, t = t_lo + i;
+    const bool act = hh < GB && t < n;
+    float *const sp = a.sc + static_cast<int64_t>(h0 + hh) * a.C * kAtqL + t;
+    grid_dep_wait();
+    const float sv = act ? __ldcg(sp) : 0.0f;
+    if (warp < GB) {
+        const float mx = warp_max_of(a.cmax + (h0 + warp) * a.C, a.C, lane);
+        if (lane == 0) s_m[warp] = mx;
+    }
+    __syncthreads();
+    float e = -0.0f;
+    if (act) {
+        e = exp_tree(__fsub_rn(sv, s_m[hh]));
+        *sp = e;
+    }
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) e = __fadd_rn(e, __shfl_xor_sync(0xffffffffu, e, d));
+    if (lane == 0) red[warp] = e;
+    __syncthreads();
+    if (hh < GB && i == 0) a.csum[(h0 + hh) * a.C + c] = __fadd_rn(red[warp], red[warp + 1]);
+}
+
+// 1024 threads, thread i < GB*D holding output (head i / D, column i % D);
+// dynamic shared memory: the chunk's value rows [64][D].
+template <int D, int GB>
+__global__ void __launch_bounds__(kAtqValThreads) atq_values_kernel(const __grid_constant__ AtqArgs a) {
+    extern __shared__ __align__(128) float vs[];
+    __shared__ uint64_t bar;
+    __shared__ float s_z[GB];
+    __shared__ __align__(16) float s_p[GB][kAtqL];
+    const int s = blockIdx.x, c = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int per = a.Hq / a.Hkv, h0 = s * GB, g = h0 / per, n = a.pos + 1, t_lo = c * kAtqL;
+    const int rows_old = max(0, min(t_lo + kAtqL, a.pos) - t_lo);  // cache rows below pos
+    if (tid == 0) {
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (tid == 0 && rows_old > 0) {
+        const uint32_t bytes = static_cast<uint32_t>(rows_old) * D * 4u;
+        mbar_arrive_expect_tx(&bar, bytes);
+        bulk_g2s(vs, a.Vc + (static_cast<int64_t>(g) * a.P + t_lo) * D, bytes, &bar, l2_evict_first());
+    }
+    if (a.pos < t_lo + kAtqL && tid < D) vs[(a.pos - t_lo) * D + tid] = a.v[static_cast<int64_t>(g) * D + tid];
+    grid_dep_wait();
+    grid_dep_launch();
+    // the chunk's exponentials; Z, the tree over the chunks' sums (padded
+    // with -0 to 128 chunks: lane l takes chunks 4l .. 4l+3)
+    const int ph = tid / kAtqL, pi = tid % kAtqL, pt = t_lo + pi;
+    const bool pact = ph < GB && pt < n;
+    const float ev = pact ? __ldcg(a.sc + static_cast<int64_t>(h0 + ph) * a.C * kAtqL + pt) : 0.0f;
+    if (warp < GB) {
+        const float *cs = a.csum + (h0 + warp) * a.C;
+        float e4[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) e4[q] = 4 * lane + q < a.C ? __ldcg(cs + 4 * lane + q) : -0.0f;
+        float z = __fadd_rn(__fadd_rn(e4[0], e4[1]), __fadd_rn(e4[2], e4[3]));
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) z = __fadd_rn(z, __shfl_xor_sync(0xffffffffu, z, d));
+        if (lane == 0) s_z[warp] = z;
+    }
+    __syncthreads();
+    if (ph < GB) s_p[ph][pi] = pact ? __fdiv_rn(ev, s_z[ph]) : 0.0f;
+    if (rows_old > 0) mbar_wait(&bar, 0);
+    __syncthreads();
+    // the chunk's weighted values: trees of 8 positions, then of the 8 trees
+    const int hh = tid / D, j = tid % D;
+    if (tid >= GB * D) return;
+    const bool full = t_lo + kAtqL <= n;
+    float b8[8];
+#pragma unroll
+    for (int blk = 0; blk < 8; ++blk) {
+        const float4 p0 = *reinterpret_cast<const float4 *>(&s_p[hh][8 * blk]);
+        const float4 p1 = *reinterpret_cast<const float4 *>(&s_p[hh][8 * blk + 4]);
+        const float p[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+        float e[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int ti = 8 * blk + i;
+            e[i] = full || t_lo + ti < n ? __fmul_rn(p[i], vs[ti * D + j]) : -0.0f;
         }
-        es[i] = e;
-    }
-    __syncthreads();
-    if (j < 32) {
-        // lane l < 8: the tree over block l's 32 positions; then the tree over
-        // the 8 blocks
-        float b = j < kAtqChunk / 32 ? tree_padded32(es + 32 * j, 32) : -0.0f;
 #pragma unroll
-        for (int d = 1; d < kAtqChunk / 32; d <<= 1) b = __fadd_rn(b, __shfl_xor_sync(0xffffffffu, b, d));
-        if (j == 0) a.csum[h * a.C + c] = b;
+        for (int h = 4; h >= 1; h >>= 1)
+#pragma unroll
+            for (int i = 0; i < h; ++i) e[i] = __fadd_rn(e[2 * i], e[2 * i + 1]);
+        b8[blk] = e[0];
     }
+#pragma unroll
+    for (int h = 4; h >= 1; h >>= 1)
+#pragma unroll
+        for (int i = 0; i < h; ++i) b8[i] = __fadd_rn(b8[2 * i], b8[2 * i + 1]);
+    a.opart[(static_cast<int64_t>(h0 + hh) * a.C + c) * D + j] = b8[0];
 }
 
-// 3: the probabilities of the chunk and its weighted values.  NG thread
-// groups of D threads (threads qg*D + j: column j): group qg sums the chunk's
-// 32-position blocks qg*BPG .. qg*BPG + BPG-1 (an aligned subtree of the
-// chunk's tree), then the NG parts are combined by the tree.
-template <int D>
-__host__ __device__ constexpr int atq_value_groups() { return D == 64 ? 8 : 1024 / D; }
-
-template <int D>
-__global__ void __launch_bounds__(D * atq_value_groups<D>()) atq_values_kernel(const __grid_constant__ AtqArgs a) {
-    constexpr int NG = atq_value_groups<D>(), BPG = kAtqChunk / 32 / NG;
-    __shared__ float ps[kAtqChunk];
-    __shared__ float part[NG][D];
-    const int h = blockIdx.x, c = blockIdx.y, tid = threadIdx.x, qg = tid / D, j = tid % D;
-    const int g = h / (a.Hq / a.Hkv), n = a.pos + 1, t_lo = c * kAtqChunk;
-    const float Z = tree_padded32(a.csum + h * a.C, a.C);
-    const float *sh = a.sc + static_cast<int64_t>(h) * a.C * kAtqChunk;
-    for (int i = tid; i < kAtqChunk; i += D * NG) {
-        const int t = t_lo + i;
-        ps[i] = t < n ? __fdiv_rn(sh[t], Z) : 0.0f;
-    }
-    __syncthreads();
-    const float *Vg = a.Vc + static_cast<int64_t>(g) * a.P * D + j;
-    float bsum[BPG];
-#pragma unroll
-    for (int bb = 0; bb < BPG; ++bb) {
-        const int b = qg * BPG + bb;
-        float e[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            const int t = t_lo + 32 * b + i;
-            e[i] = t < n ? __fmul_rn(ps[32 * b + i], Vg[static_cast<int64_t>(t) * D]) : -0.0f;
-        }
-        bsum[bb] = tree32v(e);
-    }
-#pragma unroll
-    for (int hh = BPG / 2; hh >= 1; hh >>= 1)
-#pragma unroll
-        for (int bb = 0; bb < hh; ++bb) bsum[bb] = __fadd_rn(bsum[2 * bb], bsum[2 * bb + 1]);
-    part[qg][j] = bsum[0];
-    __syncthreads();
-    if (tid < D) {
-        float w[NG];
-#pragma unroll
-        for (int i = 0; i < NG; ++i) w[i] = part[i][tid];
-#pragma unroll
-        for (int hh = NG / 2; hh >= 1; hh >>= 1)
-#pragma unroll
-            for (int i = 0; i < hh; ++i) w[i] = __fadd_rn(w[2 * i], w[2 * i + 1]);
-        a.opart[(static_cast<int64_t>(h) * a.C + c) * D + tid] = w[0];
-    }
-}
-
-// 4: the tree over the chunks, the gate and the group sums.
+// One block a head, thread j its column; dynamic shared memory: the head's
+// chunk results [C][D], brought in by one bulk copy.
 template <int D>
 __global__ void __launch_bounds__(D) atq_out_kernel(const __grid_constant__ AtqArgs a) {
+    extern __shared__ __align__(128) float op[];
+    __shared__ uint64_t bar;
     __shared__ float red[D / 32];
     const int h = blockIdx.x, j = threadIdx.x;
-    float o[kAtqMaxChunks];
-    for (int c = 0; c < a.C; ++c) o[c] = a.opart[(static_cast<int64_t>(h) * a.C + c) * D + j];
-    const float ov = tree_padded32(o, a.C);
     const int64_t yi = static_cast<int64_t>(h) * D + j;
-    const float yv = __fmul_rn(ov, sigmoid_tree(a.gate[yi]));
+    if (j == 0) {
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    const float sg = sigmoid_tree(a.gate[yi]);
+    grid_dep_wait();
+    grid_dep_launch();
+    if (j == 0) {
+        const uint32_t bytes = static_cast<uint32_t>(a.C) * D * 4u;
+        mbar_arrive_expect_tx(&bar, bytes);
+        bulk_g2s(op, a.opart + static_cast<int64_t>(h) * a.C * D, bytes, &bar, l2_evict_first());
+    }
+    mbar_wait(&bar, 0);
+    // the tree over 128 chunks padded with -0: trees of 8, then of the 16
+    float b[16];
+#pragma unroll
+    for (int cb = 0; cb < 16; ++cb) {
+        float e[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) e[i] = 8 * cb + i < a.C ? op[(8 * cb + i) * D + j] : -0.0f;
+#pragma unroll
+        for (int hh = 4; hh >= 1; hh >>= 1)
+#pragma unroll
+            for (int i = 0; i < hh; ++i) e[i] = __fadd_rn(e[2 * i], e[2 * i + 1]);
+        b[cb] = e[0];
+    }
+#pragma unroll
+    for (int hh = 8; hh >= 1; hh >>= 1)
+#pragma unroll
+        for (int i = 0; i < hh; ++i) b[i] = __fadd_rn(b[2 * i], b[2 * i + 1]);
+    const float yv = __fmul_rn(b[0], sg);
     a.y[yi] = yv;
     float gsm = yv;
 #pragma unroll
@@ -549,18 +650,90 @@ __global__ void __launch_bounds__(D) atq_out_kernel(const __grid_constant__ AtqA
     if ((j & 63) == 0) a.ysum[yi >> 6] = __fadd_rn(red[j >> 5], red[(j >> 5) + 1]);
 }
 
-template <int D>
-cudaError_t launch_atq_d(const AtqArgs &a, cudaStream_t stream) {
-    const dim3 grid(a.Hq, a.C);
-    atq_scores_kernel<D><<<grid, kAtqScoreThreads, 0, stream>>>(a);
-    atq_exp_kernel<D><<<grid, D, 0, stream>>>(a);
-    atq_values_kernel<D><<<grid, D * atq_value_groups<D>(), 0, stream>>>(a);
-    atq_out_kernel<D><<<a.Hq, D, 0, stream>>>(a);
-    return cudaGetLastError();
+template <int D, int GB>
+cudaError_t atq_attr() {
+    static const cudaError_t e = [] {
+        cudaError_t r = cudaFuncSetAttribute(atq_values_kernel<D, GB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             kAtqL * D * 4);
+        if (r == cudaSuccess)
+            r = cudaFuncSetAttribute(atq_out_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     kAtqMaxChunks * D * 4);
+        return r;
+    }();
+    return e;
 }
 
-// Device scratch for the chunk results, per device, grown when a call needs
-// more (freed only at exit).
+cudaError_t launch_pdl(const void *fn, dim3 grid, dim3 block, size_t smem, const AtqArgs &a, bool pdl,
+                       cudaStream_t stream) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = pdl ? 1 : 0;
+    void *params[] = {const_cast<AtqArgs *>(&a)};
+    return cudaLaunchKernelExC(&cfg, fn, params);
+}
+
+template <int D, int GB>
+cudaError_t launch_atq_dg(const AtqArgs &a, bool pdl, cudaStream_t stream) {
+    cudaError_t e = atq_attr<D, GB>();
+    if (e != cudaSuccess) return e;
+    const dim3 grid(a.Hq / GB, a.C);
+    atq_scores_kernel<D, GB><<<grid, kAtqThreads, 0, stream>>>(a);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if ((e = launch_pdl(reinterpret_cast<const void *>(atq_exp_kernel<GB>), grid, dim3(kAtqThreads), 0, a, pdl,
+                        stream)) != cudaSuccess)
+        return e;
+    if ((e = launch_pdl(reinterpret_cast<const void *>(atq_values_kernel<D, GB>), grid, dim3(kAtqValThreads),
+                        kAtqL * D * 4, a, pdl, stream)) != cudaSuccess)
+        return e;
+    return launch_pdl(reinterpret_cast<const void *>(atq_out_kernel<D>), dim3(a.Hq), dim3(D),
+                      static_cast<size_t>(a.C) * D * 4, a, pdl, stream);
+}
+
+template <int D>
+cudaError_t launch_atq_d(const AtqArgs &a, bool pdl, cudaStream_t stream) {
+    switch (atq_heads_per_block(a.Hq / a.Hkv)) {
+    case 4: return launch_atq_dg<D, 4>(a, pdl, stream);
+    case 2: return launch_atq_dg<D, 2>(a, pdl, stream);
+    default: return launch_atq_dg<D, 1>(a, pdl, stream);
+    }
+}
+
+template <int D>
+cudaError_t prepare_atq_d(int per) {
+    switch (atq_heads_per_block(per)) {
+    case 4: return atq_attr<D, 4>();
+    case 2: return atq_attr<D, 2>();
+    default: return atq_attr<D, 1>();
+    }
+}
+
+// The scratch layout (offsets in floats, each a multiple of 4): the scores,
+// the chunk maxima and sums, the chunks' weighted values.
+struct AtqLayout {
+    size_t sc, cmax, csum, opart, total;
+};
+
+AtqLayout atq_layout(int Hq, int D, int pos) {
+    const size_t C = static_cast<size_t>(pos + kAtqL) / kAtqL, nc = static_cast<size_t>(Hq) * C;
+    const size_t nc4 = (nc + 3) / 4 * 4;
+    AtqLayout l;
+    l.sc = 0;
+    l.cmax = nc * kAtqL;
+    l.csum = l.cmax + nc4;
+    l.opart = l.csum + nc4;
+    l.total = l.opart + nc * D;
+    return l;
+}
+
+// Device scratch for direct calls, per device, grown when a call needs more
+// (freed only at exit).
 std::mutex g_atq_mu;
 float *g_atq_scratch[64];
 size_t g_atq_bytes[64];
@@ -613,30 +786,34 @@ cudaError_t prepare_gdn(int D) {
     }
 }
 
-size_t atq_scratch_bytes(int Hq, int D, int pos) {
-    const size_t nc = static_cast<size_t>(Hq) * ((pos + kAtqChunk) / kAtqChunk);
-    return (nc * kAtqChunk + 2 * nc + nc * D) * sizeof(float);
+size_t atq_scratch_bytes(int Hq, int D, int pos) { return atq_layout(Hq, D, pos).total * sizeof(float); }
+
+cudaError_t prepare_atq(int Hq, int Hkv, int D) {
+    if (Hkv < 1 || Hq % Hkv) return cudaErrorInvalidValue;
+    switch (D) {
+    case 64: return prepare_atq_d<64>(Hq / Hkv);
+    case 128: return prepare_atq_d<128>(Hq / Hkv);
+    case 256: return prepare_atq_d<256>(Hq / Hkv);
+    default: return cudaErrorInvalidValue;
+    }
 }
 
 cudaError_t launch_atq(const float *q, const float *gate, const float *k, const float *v, const float *qn_w,
                        const float *kn_w, const float *cs, const float *sn, float *Kc, float *Vc, float *y,
-                       float *ysum, int Hq, int Hkv, int D, int P, int pos, float eps, float *scratch,
+                       float *ysum, int Hq, int Hkv, int D, int P, int pos, float eps, float *scratch, bool pdl,
                        cudaStream_t stream) {
-    if (pos + 1 > kAtqMaxPositions || (D != 64 && D != 128 && D != 256)) return cudaErrorInvalidValue;
-    AtqArgs a{q, gate, k, v, qn_w, kn_w, cs, sn, Kc, Vc, y, ysum, nullptr, nullptr, nullptr, nullptr,
-              Hq, Hkv, P, pos, (pos + kAtqChunk) / kAtqChunk, eps};
-    const size_t nsc = static_cast<size_t>(Hq) * a.C * kAtqChunk, nc = static_cast<size_t>(Hq) * a.C;
+    if (pos < 0 || pos + 1 > kAtqMaxPositions || (D != 64 && D != 128 && D != 256) || Hkv < 1 || Hq % Hkv)
+        return cudaErrorInvalidValue;
+    const AtqLayout l = atq_layout(Hq, D, pos);
     float *base = scratch;
-    cudaError_t e = scratch ? cudaSuccess : atq_scratch(atq_scratch_bytes(Hq, D, pos), &base);
+    const cudaError_t e = scratch ? cudaSuccess : atq_scratch(l.total * sizeof(float), &base);
     if (e != cudaSuccess) return e;
-    a.sc = base;
-    a.cmax = base + nsc;
-    a.csum = a.cmax + nc;
-    a.opart = a.csum + nc;
+    const AtqArgs a{q, gate, k, v, qn_w, kn_w, cs, sn, Kc, Vc, y, ysum, base + l.sc, base + l.cmax, base + l.csum,
+                    base + l.opart, Hq, Hkv, P, pos, (pos + kAtqL) / kAtqL, eps};
     switch (D) {
-    case 64: return launch_atq_d<64>(a, stream);
-    case 128: return launch_atq_d<128>(a, stream);
-    default: return launch_atq_d<256>(a, stream);
+    case 64: return launch_atq_d<64>(a, pdl, stream);
+    case 128: return launch_atq_d<128>(a, pdl, stream);
+    default: return launch_atq_d<256>(a, pdl, stream);
     }
 }
 

@@ -263,15 +263,17 @@ abg_status abg_gdn(const float *x, const float *conv, float *state, const float 
  *   cos, sin f32 [D/2]     Kc, Vc f32 [Hkv][P][D], rows < pos filled; row pos
  *                          written (by the call)
  *   y        f32 [Hq*D]    ysum  f32 [Hq*D/64]
- *   D = 64, 128 or 256; Hq a multiple of Hkv; 0 <= pos < P; pos + 1 <= 8192
- *   (the scores of one head stay in shared memory); Hq*D <= 2^20.
- * Both modes compute the same bits.  The positions run in chunks of 256 (four
- * launches); the chunks' partial results live in a device buffer the library
- * allocates on a device's first call and grows when a call needs more (the
- * growth synchronizes the device); calls that can overlap on the GPU (on
- * different streams or host threads) share it and must be ordered by the
- * caller.  Errors: null pointer or mode ABG_EINVAL; shape ABG_ESHAPE; a
- * pointer not 4-byte aligned ABG_EALIGN; an output (Kc, Vc, y, ysum)
+ *   D = 64, 128 or 256; Hq a multiple of Hkv; 0 <= pos < P; pos + 1 <= 8192;
+ *   Hq*D <= 2^20.
+ * Both modes compute the same bits.  The positions run in chunks of 64 (two
+ * launches, the second started early by programmatic dependent launch unless
+ * ABG_PDL=0); the chunks' partial results and a completion counter per head
+ * set live in a device buffer the library allocates, zeroed, on a device's
+ * first call and grows when a call needs more (the growth synchronizes the
+ * device); calls that can overlap on the GPU (on different streams or host
+ * threads) share it and must be ordered by the caller.  Errors: null pointer
+ * or mode ABG_EINVAL; shape ABG_ESHAPE; a pointer not 4-byte aligned, or Kc
+ * or Vc not 16-byte aligned, ABG_EALIGN; an output (Kc, Vc, y, ysum)
  * overlapping an input or another output ABG_EALIAS.  Asynchronous on
  * `stream`.
  */

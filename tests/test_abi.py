@@ -331,3 +331,7 @@ def test_atq_rejects_before_device_work(lib):
     q = list(p)
     q[8] += 2
     assert call(q) == EALIGN
+    for i in (8, 9):                             # a cache 4- but not 16-byte aligned
+        q = list(p)
+        q[i] += 4
+        assert call(q) == EALIGN
