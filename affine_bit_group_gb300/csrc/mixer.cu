@@ -268,10 +268,10 @@ cudaError_t launch_gdn_d(const float *x, const float *conv, float *state, const 
 // A block takes GB query heads of one KV group (GB = 4, 2 or 1, dividing the
 // group) and one chunk of 64 positions.  Four launches, the last three
 // started early by programmatic dependent launch:
-//   scores: the normed, rotated queries (and, in the chunk holding pos, the
-//     key, written to the cache row with the new value by the group's first
-//     block), the chunk's scores (each row of keys read once for the GB
-//     heads) and each head's maximum over the chunk;
+//   scores (one block a half chunk): the normed, rotated queries (and, in
+//     the block holding pos, the key, written to the cache row with the new
+//     value by the group's first block), the block's scores (each row of
+//     keys read once for the GB heads) and each head's maximum over them;
 //   exponentials: each head's maximum over the chunks, the chunk's
 //     exponentials (in place of the scores) and their sum;
 //   values: before its wait it copies the chunk's value rows into shared
@@ -287,7 +287,9 @@ cudaError_t launch_gdn_d(const float *x, const float *conv, float *state, const 
 // chunks (padded with -0 to 128), give the oracle's bits.
 constexpr int kAtqMaxPositions = 8192;
 constexpr int kAtqL = 64;          // positions per chunk
-constexpr int kAtqThreads = 256;   // scores: 8 warps of 8 positions
+constexpr int kAtqSL = 32;         // positions per scores block (half a chunk)
+constexpr int kAtqRW = 4;          // positions per warp of a scores block
+constexpr int kAtqThreads = 256;   // scores: 8 warps of 4 positions
 constexpr int kAtqValThreads = 1024;
 constexpr int kAtqMaxChunks = kAtqMaxPositions / kAtqL;
 
@@ -295,7 +297,7 @@ struct AtqArgs {
     const float *q, *gate, *k, *v, *qn_w, *kn_w, *cs, *sn;
     float *Kc, *Vc, *y, *ysum;
     float *sc;     // [Hq][C*64] scores, then their exponentials
-    float *cmax;   // [Hq][C] the chunks' maxima
+    float *cmax;   // [Hq][2C] the half chunks' maxima
     float *csum;   // [Hq][C] the chunks' sums of exponentials
     float *opart;  // [Hq][C][D] the chunks' weighted values
     int Hq, Hkv, P, pos, C;
@@ -363,18 +365,18 @@ __device__ __forceinline__ float warp_max_of(const float *v, int C, int lane) {
 
 template <int D, int GB>
 __global__ void __launch_bounds__(kAtqThreads) atq_scores_kernel(const __grid_constant__ AtqArgs a) {
-    constexpr int CPL = D / 32, NV = 8 * GB, NR = GB + 1, kStep = kAtqThreads / D;
+    constexpr int CPL = D / 32, NV = kAtqRW * GB, NR = GB + 1, kStep = kAtqThreads / D;
     constexpr int kRows = (NR + kStep - 1) / kStep;  // norm rows a thread takes
     __shared__ __align__(16) float un[NR][D];
     __shared__ __align__(16) float rot[NR][D];
     __shared__ float red[NR][D / 32];
-    __shared__ float ssc[GB][kAtqL];
+    __shared__ float ssc[GB][kAtqSL];
     // the next launch reads nothing of this one before its own wait
     grid_dep_launch();
     const int s = blockIdx.x, c = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int per = a.Hq / a.Hkv, h0 = s * GB, g = h0 / per, n = a.pos + 1, t_lo = c * kAtqL;
-    const bool holds_pos = c == a.C - 1;
-    const int nr = GB + (holds_pos ? 1 : 0);  // the query rows, and the key in the chunk holding pos
+    const int per = a.Hq / a.Hkv, h0 = s * GB, g = h0 / per, n = a.pos + 1, t_lo = c * kAtqSL;
+    const bool holds_pos = c == a.pos / kAtqSL;
+    const int nr = GB + (holds_pos ? 1 : 0);  // the query rows, and the key in the block holding pos
     // the rows to norm (row r of the thread's column j: r0 + k*kStep), their
     // weights and this column's rotation, read ahead of the cache rows
     const int j = tid % D, r0 = tid / D, ji = j % (D / 2);
@@ -386,13 +388,13 @@ __global__ void __launch_bounds__(kAtqThreads) atq_scores_kernel(const __grid_co
                       : 0.0f;
     }
     const float wq = a.qn_w[j], wk = a.kn_w[j], cj = a.cs[ji], sj = a.sn[ji];
-    // cache rows t_lo + 8 warp + r (r < 8) below pos; lane l holds columns
+    // cache rows t_lo + 4 warp + r (r < 4) below pos; lane l holds columns
     // l*CPL .. l*CPL+CPL-1 (row pos is this block's own key)
     const float *Kg = a.Kc + static_cast<int64_t>(g) * a.P * D + lane * CPL;
-    const int tw = t_lo + 8 * warp;
-    float kv[8][CPL];
+    const int tw = t_lo + kAtqRW * warp;
+    float kv[kAtqRW][CPL];
 #pragma unroll
-    for (int r = 0; r < 8; ++r) {
+    for (int r = 0; r < kAtqRW; ++r) {
         if (tw + r < a.pos) {
             load_cols<CPL>(Kg + static_cast<int64_t>(tw + r) * D, kv[r]);
         } else {
@@ -452,16 +454,16 @@ __global__ void __launch_bounds__(kAtqThreads) atq_scores_kernel(const __grid_co
 #pragma unroll
         for (int cc = 0; cc < CPL; ++cc) qv[hh][cc] = rot[hh][lane * CPL + cc];
 #pragma unroll
-    for (int r = 0; r < 8; ++r)
+    for (int r = 0; r < kAtqRW; ++r)
         if (tw + r == a.pos)
 #pragma unroll
             for (int cc = 0; cc < CPL; ++cc) kv[r][cc] = rot[GB][lane * CPL + cc];
-    // value hh*8 + r: the lane's tree over its columns of q_hh . k_r
+    // value hh*4 + r: the lane's tree over its columns of q_hh . k_r
     float vals[NV];
 #pragma unroll
     for (int hh = 0; hh < GB; ++hh)
 #pragma unroll
-        for (int r = 0; r < 8; ++r) {
+        for (int r = 0; r < kAtqRW; ++r) {
             float pr[CPL];
 #pragma unroll
             for (int cc = 0; cc < CPL; ++cc) pr[cc] = __fmul_rn(qv[hh][cc], kv[r][cc]);
@@ -469,30 +471,27 @@ __global__ void __launch_bounds__(kAtqThreads) atq_scores_kernel(const __grid_co
             for (int h = CPL / 2; h >= 1; h >>= 1)
 #pragma unroll
                 for (int cc = 0; cc < h; ++cc) pr[cc] = __fadd_rn(pr[2 * cc], pr[2 * cc + 1]);
-            vals[hh * 8 + r] = pr[0];
+            vals[hh * kAtqRW + r] = pr[0];
         }
     const float dot = warp_sums<NV>(vals, lane);
     if (lane < NV) {
-        const int idx = rev_low_bits<NV>(lane), hh = idx >> 3, r = idx & 7;
+        const int idx = rev_low_bits<NV>(lane), hh = idx / kAtqRW, r = idx % kAtqRW;
         const float scale = __frcp_rn(__fsqrt_rn(static_cast<float>(D)));
-        ssc[hh][8 * warp + r] = __fmul_rn(dot, scale);
+        ssc[hh][kAtqRW * warp + r] = __fmul_rn(dot, scale);
     }
     __syncthreads();
     if (warp < GB) {
         const int h = h0 + warp;
         float mx = -__int_as_float(0x7f800000);
         float *sh = a.sc + static_cast<int64_t>(h) * a.C * kAtqL + t_lo;
-#pragma unroll
-        for (int i = lane; i < kAtqL; i += 32) {
-            if (t_lo + i < n) {
-                const float sv = ssc[warp][i];
-                sh[i] = sv;
-                mx = fmaxf(mx, sv);
-            }
+        if (t_lo + lane < n) {
+            const float sv = ssc[warp][lane];
+            sh[lane] = sv;
+            mx = sv;
         }
 #pragma unroll
         for (int d = 1; d < 32; d <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, d));
-        if (lane == 0) a.cmax[h * a.C + c] = mx;
+        if (lane == 0) a.cmax[h * 2 * a.C + c] = mx;
     }
 }
 
@@ -512,7 +511,7 @@ __global__ void __launch_bounds__(kAtqThreads) atq_exp_kernel(const __grid_const
     grid_dep_wait();
     const float sv = act ? __ldcg(sp) : 0.0f;
     if (warp < GB) {
-        const float mx = warp_max_of(a.cmax + (h0 + warp) * a.C, a.C, lane);
+        const float mx = warp_max_of(a.cmax + (h0 + warp) * 2 * a.C, a.pos / kAtqSL + 1, lane);
         if (lane == 0) s_m[warp] = mx;
     }
     __syncthreads();
@@ -536,6 +535,7 @@ __global__ void __launch_bounds__(kAtqValThreads) atq_values_kernel(const __grid
     __shared__ uint64_t bar;
     __shared__ float s_z[GB];
     __shared__ __align__(16) float s_p[GB][kAtqL];
+    __shared__ float s_part[4][GB][D];
     const int s = blockIdx.x, c = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int per = a.Hq / a.Hkv, h0 = s * GB, g = h0 / per, n = a.pos + 1, t_lo = c * kAtqL;
     const int rows_old = max(0, min(t_lo + kAtqL, a.pos) - t_lo);  // cache rows below pos
@@ -571,33 +571,44 @@ __global__ void __launch_bounds__(kAtqValThreads) atq_values_kernel(const __grid
     if (ph < GB) s_p[ph][pi] = pact ? __fdiv_rn(ev, s_z[ph]) : 0.0f;
     if (rows_old > 0) mbar_wait(&bar, 0);
     __syncthreads();
-    // the chunk's weighted values: trees of 8 positions, then of the 8 trees
-    const int hh = tid / D, j = tid % D;
-    if (tid >= GB * D) return;
+    // the chunk's weighted values: quarter q = tid / 256 of the chunk (16
+    // positions), thread tid % 256 column j and heads hs, hs + 256/D, ...
+    // (each value row read once for them); then the tree over the quarters
+    constexpr int kHS = kAtqThreads / D, kHPT = GB / kHS > 0 ? GB / kHS : 1;
+    const int q = tid >> 8, hs = (tid & 255) / D, j = tid % D;
     const bool full = t_lo + kAtqL <= n;
-    float b8[8];
+    if (hs < GB) {
+        float vv[16];
 #pragma unroll
-    for (int blk = 0; blk < 8; ++blk) {
-        const float4 p0 = *reinterpret_cast<const float4 *>(&s_p[hh][8 * blk]);
-        const float4 p1 = *reinterpret_cast<const float4 *>(&s_p[hh][8 * blk + 4]);
-        const float p[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
-        float e[8];
+        for (int i = 0; i < 16; ++i) vv[i] = vs[(16 * q + i) * D + j];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int ti = 8 * blk + i;
-            e[i] = full || t_lo + ti < n ? __fmul_rn(p[i], vs[ti * D + j]) : -0.0f;
+        for (int k = 0; k < kHPT; ++k) {
+            const int hh = hs + k * kHS;
+            if (hh >= GB) break;
+            float e[16];
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                const float4 p4 = *reinterpret_cast<const float4 *>(&s_p[hh][16 * q + 4 * m]);
+                const float p[4] = {p4.x, p4.y, p4.z, p4.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int ti = 16 * q + 4 * m + i;
+                    e[4 * m + i] = full || t_lo + ti < n ? __fmul_rn(p[i], vv[4 * m + i]) : -0.0f;
+                }
+            }
+#pragma unroll
+            for (int h = 8; h >= 1; h >>= 1)
+#pragma unroll
+                for (int i = 0; i < h; ++i) e[i] = __fadd_rn(e[2 * i], e[2 * i + 1]);
+            s_part[q][hh][j] = e[0];
         }
-#pragma unroll
-        for (int h = 4; h >= 1; h >>= 1)
-#pragma unroll
-            for (int i = 0; i < h; ++i) e[i] = __fadd_rn(e[2 * i], e[2 * i + 1]);
-        b8[blk] = e[0];
     }
-#pragma unroll
-    for (int h = 4; h >= 1; h >>= 1)
-#pragma unroll
-        for (int i = 0; i < h; ++i) b8[i] = __fadd_rn(b8[2 * i], b8[2 * i + 1]);
-    a.opart[(static_cast<int64_t>(h0 + hh) * a.C + c) * D + j] = b8[0];
+    __syncthreads();
+    if (tid < GB * D) {
+        const int hh = tid / D, jj = tid % D;
+        a.opart[(static_cast<int64_t>(h0 + hh) * a.C + c) * D + jj] =
+            __fadd_rn(__fadd_rn(s_part[0][hh][jj], s_part[1][hh][jj]), __fadd_rn(s_part[2][hh][jj], s_part[3][hh][jj]));
+    }
 }
 
 // One block a head, thread j its column; dynamic shared memory: the head's
@@ -627,14 +638,17 @@ __global__ void __launch_bounds__(D) atq_out_kernel(const __grid_constant__ AtqA
     float b[16];
 #pragma unroll
     for (int cb = 0; cb < 16; ++cb) {
-        float e[8];
+        b[cb] = -0.0f;
+        if (8 * cb < a.C) {
+            float e[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) e[i] = 8 * cb + i < a.C ? op[(8 * cb + i) * D + j] : -0.0f;
+            for (int i = 0; i < 8; ++i) e[i] = 8 * cb + i < a.C ? op[(8 * cb + i) * D + j] : -0.0f;
 #pragma unroll
-        for (int hh = 4; hh >= 1; hh >>= 1)
+            for (int hh = 4; hh >= 1; hh >>= 1)
 #pragma unroll
-            for (int i = 0; i < hh; ++i) e[i] = __fadd_rn(e[2 * i], e[2 * i + 1]);
-        b[cb] = e[0];
+                for (int i = 0; i < hh; ++i) e[i] = __fadd_rn(e[2 * i], e[2 * i + 1]);
+            b[cb] = e[0];
+        }
     }
 #pragma unroll
     for (int hh = 8; hh >= 1; hh >>= 1)
@@ -684,7 +698,7 @@ cudaError_t launch_atq_dg(const AtqArgs &a, bool pdl, cudaStream_t stream) {
     cudaError_t e = atq_attr<D, GB>();
     if (e != cudaSuccess) return e;
     const dim3 grid(a.Hq / GB, a.C);
-    atq_scores_kernel<D, GB><<<grid, kAtqThreads, 0, stream>>>(a);
+    atq_scores_kernel<D, GB><<<dim3(a.Hq / GB, a.pos / kAtqSL + 1), kAtqThreads, 0, stream>>>(a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if ((e = launch_pdl(reinterpret_cast<const void *>(atq_exp_kernel<GB>), grid, dim3(kAtqThreads), 0, a, pdl,
                         stream)) != cudaSuccess)
@@ -715,7 +729,7 @@ cudaError_t prepare_atq_d(int per) {
 }
 
 // The scratch layout (offsets in floats, each a multiple of 4): the scores,
-// the chunk maxima and sums, the chunks' weighted values.
+// the half chunks' maxima, the chunks' sums and weighted values.
 struct AtqLayout {
     size_t sc, cmax, csum, opart, total;
 };
@@ -726,7 +740,7 @@ AtqLayout atq_layout(int Hq, int D, int pos) {
     AtqLayout l;
     l.sc = 0;
     l.cmax = nc * kAtqL;
-    l.csum = l.cmax + nc4;
+    l.csum = l.cmax + 2 * nc4;
     l.opart = l.csum + nc4;
     l.total = l.opart + nc * D;
     return l;
