@@ -4,20 +4,22 @@
 // the delta-rule rows, the gated norm and group sums; one threadgroup per
 // value head, every phase local to its head).
 //
-// One thread block per head, one thread per value column j (D threads).  The
-// steps are the library's reading of the published gated DeltaNet recurrence
-// (see abg_gdn in abg.h), every one a single binary32 operation rounded to
-// nearest and every sum the pairwise tree in index order, so each output is
-// bit-identical to the oracle's:
-//   - the conv window of the thread's three channels (q, k, v) and SiLU;
+// One thread block per head, four threads per value column j (4*D threads,
+// one per quarter of the keys).  The steps are the library's reading of the
+// published gated DeltaNet recurrence (see abg_gdn in abg.h), every one a
+// single binary32 operation rounded to nearest and every sum the pairwise
+// tree in index order, so each output is bit-identical to the oracle's:
+//   - the conv window of column j's three channels (q, k, v; one quarter
+//     each) and SiLU;
 //   - block sums for the L2 norms and the gated norm: a 5-step butterfly in
 //     each warp, then the tree over the warps' sums;
 //   - the state column S[.][j]: for D <= 128 the head's state is brought into
 //     shared memory by one bulk copy at the start (overlapping the conv window,
 //     the norms and the decay), otherwise read from global memory; read twice,
-//     the decay recomputed on the second read, each column's sums over the
-//     keys i taken in blocks of 32 keys, and the new column written to global
-//     memory (coalesced over j).
+//     the decay recomputed on the second read, each quarter of the keys summed
+//     by its own thread (a subtree of the tree over the keys, in blocks of at
+//     most 32 keys) and the quarters combined by the tree, and the new column
+//     written to global memory (coalesced over j).
 #include "abg_dev.cuh"
 #include "abg_kernels.cuh"
 #include "mixer.cuh"
@@ -89,16 +91,16 @@ __device__ __forceinline__ float tree_upto8(float (&v)[8], int K) {
     return v[0];
 }
 
-// Sum over the block's D threads (one value each, in thread order) by the
-// pairwise tree: butterfly steps within each warp, then the tree over the
-// D/32 warp sums (every thread computes it from shared memory).  Every
-// thread of the block calls it; `red` holds D/32 floats.
+// A warp-sum over the first D threads of the block (one value each, thread
+// order) by the pairwise tree: the butterfly in each warp, then the tree over
+// the D/32 warp sums, returned to every thread of the block.  `red` holds
+// D/32 floats; every thread of the block calls it.
 template <int D>
-__device__ __forceinline__ float block_tree(float v, float *red) {
+__device__ __forceinline__ float first_d_tree(float v, float *red) {
     constexpr int NW = D / 32;
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, d));
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+    if ((threadIdx.x & 31) == 0 && threadIdx.x < D) red[threadIdx.x >> 5] = v;
     __syncthreads();
     float w[NW];
 #pragma unroll
@@ -111,77 +113,88 @@ __device__ __forceinline__ float block_tree(float v, float *red) {
     return w[0];
 }
 
-// Pairwise tree over 32 values in index order.
-__device__ __forceinline__ float tree32v(float (&v)[32]) {
+// The pairwise tree over KQ (16, 32 or 64) values f(t), t < KQ: trees of 32
+// (or of 16), then their sum.
+template <int KQ, typename F>
+__device__ __forceinline__ float quarter_tree(F f) {
+    constexpr int B = KQ < 32 ? KQ : 32;
+    float bsum[KQ / B];
+#pragma unroll 1
+    for (int ib = 0; ib < KQ / B; ++ib) {
+        float p[B];
 #pragma unroll
-    for (int h = 16; h >= 1; h >>= 1)
+        for (int t = 0; t < B; ++t) p[t] = f(ib * B + t);
 #pragma unroll
-        for (int i = 0; i < h; ++i) v[i] = __fadd_rn(v[2 * i], v[2 * i + 1]);
-    return v[0];
+        for (int h = B / 2; h >= 1; h >>= 1)
+#pragma unroll
+            for (int i = 0; i < h; ++i) p[i] = __fadd_rn(p[2 * i], p[2 * i + 1]);
+        bsum[ib] = p[0];
+    }
+    return KQ / B == 2 ? __fadd_rn(bsum[0], bsum[1]) : bsum[0];
 }
 
-// Pairwise tree over NB <= 8 values (NB a power of two).
-template <int NB>
-__device__ __forceinline__ float tree_blocks(float (&v)[8]) {
-#pragma unroll
-    for (int h = NB / 2; h >= 1; h >>= 1)
-#pragma unroll
-        for (int i = 0; i < h; ++i) v[i] = __fadd_rn(v[2 * i], v[2 * i + 1]);
-    return v[0];
-}
-
+// 4*D threads: thread (quarter r, column j) with j = tid % D, r = tid / D
+// walks keys r*D/4 .. (r+1)*D/4 - 1 of state column j (a subtree of the
+// pairwise tree over the D keys; the four quarters' sums are combined by the
+// tree).  The conv windows of the q, k and v channels of column j run in
+// quarters 0, 1 and 2; the norms use the first D threads.
 template <int D>
-__global__ void __launch_bounds__(D) gdn_kernel(const float *__restrict__ x, const float *__restrict__ conv,
-                                                float *state, const float *__restrict__ a,
-                                                const float *__restrict__ b, const float *__restrict__ z,
-                                                const float *__restrict__ A_log, const float *__restrict__ dt_bias,
-                                                const float *__restrict__ nw, float *S, float *y, float *ysum,
-                                                int H, int K, float eps, float eps_n) {
+__global__ void __launch_bounds__(4 * D) gdn_kernel(const float *__restrict__ x, const float *__restrict__ conv,
+                                                    float *state, const float *__restrict__ a,
+                                                    const float *__restrict__ b, const float *__restrict__ z,
+                                                    const float *__restrict__ A_log,
+                                                    const float *__restrict__ dt_bias,
+                                                    const float *__restrict__ nw, float *S, float *y, float *ysum,
+                                                    int H, int K, float eps, float eps_n) {
     // D <= 128: the head's state (D*D floats, at most 64 KB) is brought into
     // shared memory by one bulk copy issued at the start, which overlaps the
     // conv window, the norms and the decay; both passes over the state then
     // read shared memory.  D = 256 reads its 256 KB state from global memory.
     constexpr bool kStage = D <= 128;
+    constexpr int KQ = D / 4;
     extern __shared__ __align__(128) float Ss[];
-    __shared__ float qh_s[D], kh_s[D];
+    __shared__ float act_s[3][D], qh_s[D], kh_s[D];
+    __shared__ float part[4][D];
     __shared__ float red[D / 32];
     __shared__ uint64_t bar;
-    const int h = blockIdx.x, j = threadIdx.x;
+    const int h = blockIdx.x, tid = threadIdx.x, j = tid % D, r = tid / D;
     const int64_t HD = static_cast<int64_t>(H) * D;
     float *const Sh = S + static_cast<int64_t>(h) * D * D;
     if constexpr (kStage) {
-        if (j == 0) {
+        if (tid == 0) {
             mbar_init(&bar, 1);
             fence_mbar_init();
         }
         __syncthreads();
-        if (j == 0) {
+        if (tid == 0) {
             mbar_arrive_expect_tx(&bar, D * D * 4);
             bulk_g2s(Ss, Sh, D * D * 4, &bar, l2_evict_first());
         }
     }
-    // conv window and SiLU of the thread's q, k and v channels
-    float act[3];
-#pragma unroll
-    for (int part = 0; part < 3; ++part) {
-        const int64_t c = part * HD + static_cast<int64_t>(h) * D + j;
+    // conv window and SiLU of channel r (q, k, v) of column j
+    if (r < 3) {
+        const int64_t c = r * HD + static_cast<int64_t>(h) * D + j;
         float w[8], p[8];
         for (int t = 0; t < K - 1; ++t) w[t] = state[c * (K - 1) + t];
         w[K - 1] = x[c];
         for (int t = 0; t < K; ++t) p[t] = __fmul_rn(conv[c * K + t], w[t]);
-        act[part] = silu_tree(tree_upto8(p, K));
+        act_s[r][j] = silu_tree(tree_upto8(p, K));
         for (int t = 0; t < K - 1; ++t) state[c * (K - 1) + t] = w[t + 1];
     }
-    const float q = act[0], k = act[1], v = act[2];
-    // L2 norms; the query also scaled by RN(1 / RN(sqrt D))
-    const float rq = __frcp_rn(__fsqrt_rn(__fadd_rn(block_tree<D>(__fmul_rn(q, q), red), eps)));
-    const float rk = __frcp_rn(__fsqrt_rn(__fadd_rn(block_tree<D>(__fmul_rn(k, k), red), eps)));
-    const float qscale = __frcp_rn(__fsqrt_rn(static_cast<float>(D)));
-    qh_s[j] = __fmul_rn(__fmul_rn(q, rq), qscale);
-    kh_s[j] = __fmul_rn(k, rk);
-    // decay and beta
+    // decay and beta (every thread)
     const float alpha = exp_tree(-__fmul_rn(exp_tree(A_log[h]), softplus_tree(__fadd_rn(a[h], dt_bias[h]))));
     const float beta = sigmoid_tree(b[h]);
+    __syncthreads();
+    // L2 norms; the query also scaled by RN(1 / RN(sqrt D))
+    const float q = act_s[0][j], k = act_s[1][j], v = act_s[2][j];
+    const float qq = tid < D ? __fmul_rn(q, q) : 0.0f, kk = tid < D ? __fmul_rn(k, k) : 0.0f;
+    const float rq = __frcp_rn(__fsqrt_rn(__fadd_rn(first_d_tree<D>(qq, red), eps)));
+    const float rk = __frcp_rn(__fsqrt_rn(__fadd_rn(first_d_tree<D>(kk, red), eps)));
+    if (tid < D) {
+        const float qscale = __frcp_rn(__fsqrt_rn(static_cast<float>(D)));
+        qh_s[j] = __fmul_rn(__fmul_rn(q, rq), qscale);
+        kh_s[j] = __fmul_rn(k, rk);
+    }
     __syncthreads();
     // the state, staged: a bounded wait (on a timeout the status word records
     // it and the block leaves its state and outputs untouched)
@@ -189,46 +202,35 @@ __global__ void __launch_bounds__(D) gdn_kernel(const float *__restrict__ x, con
         if (!mbar_wait(&bar, 0)) return;
     }
     const float *Src = kStage ? Ss : Sh;
-    // the delta rule on column j of the head's state (S[i][j]: key i, value
-    // j), its sums over the keys taken in blocks of 32 (the pairwise tree
-    // over D is the tree over the blocks' trees)
-    constexpr int NB = D / 32;
-    float bs[8];
-#pragma unroll 1
-    for (int ib = 0; ib < NB; ++ib) {
-        float p[32];
-#pragma unroll
-        for (int t = 0; t < 32; ++t) {
-            const int i = ib * 32 + t;
-            p[t] = __fmul_rn(__fmul_rn(Src[i * D + j], alpha), kh_s[i]);
-        }
-        bs[ib] = tree32v(p);
-    }
-    const float d = __fmul_rn(beta, __fadd_rn(v, -tree_blocks<NB>(bs)));
-#pragma unroll 1
-    for (int ib = 0; ib < NB; ++ib) {
-        float p[32];
-#pragma unroll
-        for (int t = 0; t < 32; ++t) {
-            const int i = ib * 32 + t;
-            const float sv = __fadd_rn(__fmul_rn(Src[i * D + j], alpha), __fmul_rn(kh_s[i], d));
-            Sh[static_cast<int64_t>(i) * D + j] = sv;
-            p[t] = __fmul_rn(sv, qh_s[i]);
-        }
-        bs[ib] = tree32v(p);
-    }
-    const float o = tree_blocks<NB>(bs);
-    // gated RMS norm and the output's group sums
-    const float mean = __fdiv_rn(block_tree<D>(__fmul_rn(o, o), red), static_cast<float>(D));
-    const float r = __frcp_rn(__fsqrt_rn(__fadd_rn(mean, eps_n)));
+    const int i0 = r * KQ;
+    // the delta rule on column j (S[i][j]: key i, value j)
+    part[r][j] = quarter_tree<KQ>(
+        [&](int t) { return __fmul_rn(__fmul_rn(Src[(i0 + t) * D + j], alpha), kh_s[i0 + t]); });
+    __syncthreads();
+    const float d = __fmul_rn(
+        beta, __fadd_rn(v, -__fadd_rn(__fadd_rn(part[0][j], part[1][j]), __fadd_rn(part[2][j], part[3][j]))));
+    __syncthreads();  // part is rewritten
+    part[r][j] = quarter_tree<KQ>([&](int t) {
+        const int i = i0 + t;
+        const float sv = __fadd_rn(__fmul_rn(Src[i * D + j], alpha), __fmul_rn(kh_s[i], d));
+        Sh[static_cast<int64_t>(i) * D + j] = sv;
+        return __fmul_rn(sv, qh_s[i]);
+    });
+    __syncthreads();
+    const float o = __fadd_rn(__fadd_rn(part[0][j], part[1][j]), __fadd_rn(part[2][j], part[3][j]));
+    // gated RMS norm and the output's group sums (the first D threads)
+    const float mean =
+        __fdiv_rn(first_d_tree<D>(tid < D ? __fmul_rn(o, o) : 0.0f, red), static_cast<float>(D));
+    if (tid >= D) return;
+    const float rn = __frcp_rn(__fsqrt_rn(__fadd_rn(mean, eps_n)));
     const int64_t yi = static_cast<int64_t>(h) * D + j;
-    const float yv = __fmul_rn(__fmul_rn(__fmul_rn(o, r), nw[j]), silu_tree(z[yi]));
+    const float yv = __fmul_rn(__fmul_rn(__fmul_rn(o, rn), nw[j]), silu_tree(z[yi]));
     y[yi] = yv;
     float g = yv;
 #pragma unroll
     for (int dd = 1; dd < 32; dd <<= 1) g = __fadd_rn(g, __shfl_xor_sync(0xffffffffu, g, dd));
     if ((j & 31) == 0) red[j >> 5] = g;
-    __syncthreads();
+    named_bar(2, D);
     if ((j & 63) == 0) ysum[yi >> 6] = __fadd_rn(red[j >> 5], red[(j >> 5) + 1]);
 }
 
@@ -253,8 +255,8 @@ cudaError_t launch_gdn_d(const float *x, const float *conv, float *state, const 
     constexpr int kSmem = gdn_smem<D>();
     const cudaError_t attr = gdn_attr<D>();
     if (attr != cudaSuccess) return attr;
-    gdn_kernel<D><<<H, D, kSmem, stream>>>(x, conv, state, a, b, z, A_log, dt_bias, nw, S, y, ysum, H, K, eps,
-                                           eps_n);
+    gdn_kernel<D><<<H, 4 * D, kSmem, stream>>>(x, conv, state, a, b, z, A_log, dt_bias, nw, S, y, ysum, H, K, eps,
+                                               eps_n);
     return cudaGetLastError();
 }
 
