@@ -77,18 +77,29 @@ __device__ __forceinline__ float softplus_tree(float u) {
     return u > 20.0f ? u : log_tree(__fadd_rn(1.0f, exp_tree(u)));
 }
 
-// The pairwise tree over v[0 .. K), an odd last element carried (K <= 8).
-__device__ __forceinline__ float tree_upto8(float (&v)[8], int K) {
-    int m = K;
-    while (m > 1) {
-        const int half = m >> 1;
+// Channel c's conv window (the K-1 stored inputs, then x[c]) into w, and
+// SiLU of its K products' pairwise tree (padded with -0 to 8: the odd element
+// carried); indices fixed at compile time so w stays in registers.
+__device__ __forceinline__ float conv_window(const float *x, const float *conv, const float *state, int64_t c,
+                                             int K, float (&w)[8]) {
+    float p[8];
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-            if (i < half) v[i] = __fadd_rn(v[2 * i], v[2 * i + 1]);
-        if (m & 1) v[half] = v[m - 1];
-        m = half + (m & 1);
+    for (int t = 0; t < 8; ++t) {
+        w[t] = t < K - 1 ? state[c * (K - 1) + t] : (t == K - 1 ? x[c] : 0.0f);
+        p[t] = t < K ? __fmul_rn(conv[c * K + t], w[t]) : -0.0f;
     }
-    return v[0];
+#pragma unroll
+    for (int hh = 4; hh >= 1; hh >>= 1)
+#pragma unroll
+        for (int t = 0; t < hh; ++t) p[t] = __fadd_rn(p[2 * t], p[2 * t + 1]);
+    return silu_tree(p[0]);
+}
+
+// The window moves on: inputs 1 .. K-1 become the stored ones.
+__device__ __forceinline__ void conv_shift(float *state, int64_t c, int K, const float (&w)[8]) {
+#pragma unroll
+    for (int t = 0; t < 7; ++t)
+        if (t < K - 1) state[c * (K - 1) + t] = w[t + 1];
 }
 
 // A warp-sum over the first D threads of the block (one value each, thread
@@ -113,8 +124,8 @@ __device__ __forceinline__ float first_d_tree(float v, float *red) {
     return w[0];
 }
 
-// The pairwise tree over KQ (16, 32 or 64) values f(t), t < KQ: trees of 32
-// (or of 16), then their sum.
+// The pairwise tree over KQ (8, 16, 32 or 64) values f(t), t < KQ: trees of
+// at most 32, then their sum.
 template <int KQ, typename F>
 __device__ __forceinline__ float quarter_tree(F f) {
     constexpr int B = KQ < 32 ? KQ : 32;
@@ -133,32 +144,39 @@ __device__ __forceinline__ float quarter_tree(F f) {
     return KQ / B == 2 ? __fadd_rn(bsum[0], bsum[1]) : bsum[0];
 }
 
-// 4*D threads: thread (quarter r, column j) with j = tid % D, r = tid / D
-// walks keys r*D/4 .. (r+1)*D/4 - 1 of state column j (a subtree of the
-// pairwise tree over the D keys; the four quarters' sums are combined by the
-// tree).  The conv windows of the q, k and v channels of column j run in
-// quarters 0, 1 and 2; the norms use the first D threads.
+// Key groups per state column (8 for D = 128 measured slower).
 template <int D>
-__global__ void __launch_bounds__(4 * D) gdn_kernel(const float *__restrict__ x, const float *__restrict__ conv,
-                                                    float *state, const float *__restrict__ a,
-                                                    const float *__restrict__ b, const float *__restrict__ z,
-                                                    const float *__restrict__ A_log,
-                                                    const float *__restrict__ dt_bias,
-                                                    const float *__restrict__ nw, float *S, float *y, float *ysum,
-                                                    int H, int K, float eps, float eps_n) {
+__host__ __device__ constexpr int gdn_groups() {
+    return 4;
+}
+
+// G*D threads (G = gdn_groups<D>()): thread (group r, column j) with j = tid %
+// D, r = tid / D walks keys r*D/G .. (r+1)*D/G - 1 of state column j (a
+// subtree of the pairwise tree over the D keys; the groups' sums are combined
+// by the tree).  The conv windows of the q, k and v channels of column j run
+// in groups 0, 1 and 2, the decay, beta and the output gate's SiLU in group
+// 3; the norms use the first D threads.
+template <int D>
+__global__ void __launch_bounds__(gdn_groups<D>() * D, 1) gdn_kernel(
+    const float *__restrict__ x, const float *__restrict__ conv, float *state, const float *__restrict__ a,
+    const float *__restrict__ b, const float *__restrict__ z, const float *__restrict__ A_log,
+    const float *__restrict__ dt_bias, const float *__restrict__ nw, float *S, float *y, float *ysum, int H, int K,
+    float eps, float eps_n) {
     // D <= 128: the head's state (D*D floats, at most 64 KB) is brought into
     // shared memory by one bulk copy issued at the start, which overlaps the
     // conv window, the norms and the decay; both passes over the state then
     // read shared memory.  D = 256 reads its 256 KB state from global memory.
     constexpr bool kStage = D <= 128;
-    constexpr int KQ = D / 4;
+    constexpr int G = gdn_groups<D>(), KQ = D / G;
     extern __shared__ __align__(128) float Ss[];
-    __shared__ float act_s[3][D], qh_s[D], kh_s[D];
-    __shared__ float part[4][D];
-    __shared__ float red[D / 32];
+    __shared__ float act_s[3][D], qh_s[D], kh_s[D], gate_s[D];
+    __shared__ float part[G][D];
+    __shared__ float red[D / 32], red2[2][D / 32];
+    __shared__ float s_ab[2];
     __shared__ uint64_t bar;
     const int h = blockIdx.x, tid = threadIdx.x, j = tid % D, r = tid / D;
     const int64_t HD = static_cast<int64_t>(H) * D;
+    const int64_t yi = static_cast<int64_t>(h) * D + j;
     float *const Sh = S + static_cast<int64_t>(h) * D * D;
     if constexpr (kStage) {
         if (tid == 0) {
@@ -171,30 +189,55 @@ __global__ void __launch_bounds__(4 * D) gdn_kernel(const float *__restrict__ x,
             bulk_g2s(Ss, Sh, D * D * 4, &bar, l2_evict_first());
         }
     }
-    // conv window and SiLU of channel r (q, k, v) of column j
     if (r < 3) {
+        // conv window and SiLU of channel r (q, k, v) of column j
         const int64_t c = r * HD + static_cast<int64_t>(h) * D + j;
-        float w[8], p[8];
-        for (int t = 0; t < K - 1; ++t) w[t] = state[c * (K - 1) + t];
-        w[K - 1] = x[c];
-        for (int t = 0; t < K; ++t) p[t] = __fmul_rn(conv[c * K + t], w[t]);
-        act_s[r][j] = silu_tree(tree_upto8(p, K));
-        for (int t = 0; t < K - 1; ++t) state[c * (K - 1) + t] = w[t + 1];
+        float w[8];
+        act_s[r][j] = conv_window(x, conv, state, c, K, w);
+        conv_shift(state, c, K, w);
+    } else if (r == 3) {
+        // decay and beta
+        const float alpha = exp_tree(-__fmul_rn(exp_tree(A_log[h]), softplus_tree(__fadd_rn(a[h], dt_bias[h]))));
+        const float beta = sigmoid_tree(b[h]);
+        if (j == 0) {
+            s_ab[0] = alpha;
+            s_ab[1] = beta;
+        }
+        gate_s[j] = silu_tree(z[yi]);
     }
-    // decay and beta (every thread)
-    const float alpha = exp_tree(-__fmul_rn(exp_tree(A_log[h]), softplus_tree(__fadd_rn(a[h], dt_bias[h]))));
-    const float beta = sigmoid_tree(b[h]);
     __syncthreads();
-    // L2 norms; the query also scaled by RN(1 / RN(sqrt D))
+    // L2 norms (both sums in one pass: the butterflies in each warp, then the
+    // tree over the warps' sums); the query also scaled by RN(1 / RN(sqrt D))
     const float q = act_s[0][j], k = act_s[1][j], v = act_s[2][j];
-    const float qq = tid < D ? __fmul_rn(q, q) : 0.0f, kk = tid < D ? __fmul_rn(k, k) : 0.0f;
-    const float rq = __frcp_rn(__fsqrt_rn(__fadd_rn(first_d_tree<D>(qq, red), eps)));
-    const float rk = __frcp_rn(__fsqrt_rn(__fadd_rn(first_d_tree<D>(kk, red), eps)));
+    float qq = __fmul_rn(q, q), kk = __fmul_rn(k, k);
+#pragma unroll
+    for (int dd = 1; dd < 32; dd <<= 1) {
+        qq = __fadd_rn(qq, __shfl_xor_sync(0xffffffffu, qq, dd));
+        kk = __fadd_rn(kk, __shfl_xor_sync(0xffffffffu, kk, dd));
+    }
+    if ((tid & 31) == 0 && tid < D) {
+        red2[0][tid >> 5] = qq;
+        red2[1][tid >> 5] = kk;
+    }
+    __syncthreads();
+    float wsq[D / 32], wsk[D / 32];
+#pragma unroll
+    for (int i = 0; i < D / 32; ++i) wsq[i] = red2[0][i], wsk[i] = red2[1][i];
+#pragma unroll
+    for (int hh = D / 64; hh >= 1; hh >>= 1)
+#pragma unroll
+        for (int i = 0; i < hh; ++i) {
+            wsq[i] = __fadd_rn(wsq[2 * i], wsq[2 * i + 1]);
+            wsk[i] = __fadd_rn(wsk[2 * i], wsk[2 * i + 1]);
+        }
+    const float rq = __frcp_rn(__fsqrt_rn(__fadd_rn(wsq[0], eps)));
+    const float rk = __frcp_rn(__fsqrt_rn(__fadd_rn(wsk[0], eps)));
     if (tid < D) {
         const float qscale = __frcp_rn(__fsqrt_rn(static_cast<float>(D)));
         qh_s[j] = __fmul_rn(__fmul_rn(q, rq), qscale);
         kh_s[j] = __fmul_rn(k, rk);
     }
+    const float alpha = s_ab[0], beta = s_ab[1];
     __syncthreads();
     // the state, staged: a bounded wait (on a timeout the status word records
     // it and the block leaves its state and outputs untouched)
@@ -203,28 +246,48 @@ __global__ void __launch_bounds__(4 * D) gdn_kernel(const float *__restrict__ x,
     }
     const float *Src = kStage ? Ss : Sh;
     const int i0 = r * KQ;
-    // the delta rule on column j (S[i][j]: key i, value j)
-    part[r][j] = quarter_tree<KQ>(
-        [&](int t) { return __fmul_rn(__fmul_rn(Src[(i0 + t) * D + j], alpha), kh_s[i0 + t]); });
+    auto groups_tree = [&](int jj) {
+        float t[G];
+#pragma unroll
+        for (int g = 0; g < G; ++g) t[g] = part[g][jj];
+#pragma unroll
+        for (int hh = G / 2; hh >= 1; hh >>= 1)
+#pragma unroll
+            for (int g = 0; g < hh; ++g) t[g] = __fadd_rn(t[2 * g], t[2 * g + 1]);
+        return t[0];
+    };
+    // the delta rule on column j (S[i][j]: key i, value j); with at most 32
+    // keys a group, RN(S*alpha) stays in registers between the two passes
+    constexpr bool kKeep = KQ <= 32;
+    float sa[kKeep ? KQ : 1];
+    part[r][j] = quarter_tree<KQ>([&](int t) {
+        const float v1 = __fmul_rn(Src[(i0 + t) * D + j], alpha);
+        if constexpr (kKeep) sa[t] = v1;
+        return __fmul_rn(v1, kh_s[i0 + t]);
+    });
     __syncthreads();
-    const float d = __fmul_rn(
-        beta, __fadd_rn(v, -__fadd_rn(__fadd_rn(part[0][j], part[1][j]), __fadd_rn(part[2][j], part[3][j]))));
+    const float d = __fmul_rn(beta, __fadd_rn(v, -groups_tree(j)));
     __syncthreads();  // part is rewritten
     part[r][j] = quarter_tree<KQ>([&](int t) {
         const int i = i0 + t;
-        const float sv = __fadd_rn(__fmul_rn(Src[i * D + j], alpha), __fmul_rn(kh_s[i], d));
+        float v1;
+        if constexpr (kKeep) {
+            v1 = sa[t];
+        } else {
+            v1 = __fmul_rn(Src[i * D + j], alpha);
+        }
+        const float sv = __fadd_rn(v1, __fmul_rn(kh_s[i], d));
         Sh[static_cast<int64_t>(i) * D + j] = sv;
         return __fmul_rn(sv, qh_s[i]);
     });
     __syncthreads();
-    const float o = __fadd_rn(__fadd_rn(part[0][j], part[1][j]), __fadd_rn(part[2][j], part[3][j]));
+    const float o = groups_tree(j);
     // gated RMS norm and the output's group sums (the first D threads)
     const float mean =
         __fdiv_rn(first_d_tree<D>(tid < D ? __fmul_rn(o, o) : 0.0f, red), static_cast<float>(D));
     if (tid >= D) return;
     const float rn = __frcp_rn(__fsqrt_rn(__fadd_rn(mean, eps_n)));
-    const int64_t yi = static_cast<int64_t>(h) * D + j;
-    const float yv = __fmul_rn(__fmul_rn(__fmul_rn(o, rn), nw[j]), silu_tree(z[yi]));
+    const float yv = __fmul_rn(__fmul_rn(__fmul_rn(o, rn), nw[j]), gate_s[j]);
     y[yi] = yv;
     float g = yv;
 #pragma unroll
@@ -255,8 +318,8 @@ cudaError_t launch_gdn_d(const float *x, const float *conv, float *state, const 
     constexpr int kSmem = gdn_smem<D>();
     const cudaError_t attr = gdn_attr<D>();
     if (attr != cudaSuccess) return attr;
-    gdn_kernel<D><<<H, 4 * D, kSmem, stream>>>(x, conv, state, a, b, z, A_log, dt_bias, nw, S, y, ysum, H, K, eps,
-                                               eps_n);
+    gdn_kernel<D><<<H, gdn_groups<D>() * D, kSmem, stream>>>(x, conv, state, a, b, z, A_log, dt_bias, nw, S, y,
+                                                             ysum, H, K, eps, eps_n);
     return cudaGetLastError();
 }
 
