@@ -132,3 +132,37 @@ def test_batched_pdl_switch_gives_the_same_bits(pdl):
                        timeout=600)
     assert r.returncode == 0, r.stderr[-2000:]
     assert "EQUAL 1" in r.stdout
+
+
+CHILD_ATQ = """
+import sys
+sys.path.insert(0, {root!r})
+import numpy as np, torch
+import affine_bit_group_gb300 as abg
+import oracle
+from affine_bit_group_gb300 import synth
+c = synth.atq_case(np.random.default_rng(31), 8, 2, 128, 700, 300)
+d = {{k: torch.from_numpy(np.ascontiguousarray(v)).cuda() for k, v in c.items() if k != "pos"}}
+y = torch.empty(c["q"].size, device="cuda")
+ys = torch.empty(c["q"].size // 64, device="cuda")
+for _ in range(2):
+    abg.atq(d["q"], d["gate"], d["k"], d["v"], d["qn_w"], d["kn_w"], d["cos"], d["sin"], d["Kc"], d["Vc"], y, ys,
+            pos=c["pos"])
+torch.cuda.synchronize()
+ey, eys, eK, eV = oracle.atq(**c)
+same = all(np.array_equal(a.view(np.uint32), b.view(np.uint32)) for a, b in
+           ((y.cpu().numpy(), ey), (ys.cpu().numpy(), eys), (d["Kc"].cpu().numpy(), eK), (d["Vc"].cpu().numpy(), eV)))
+print("EQUAL", int(same))
+"""
+
+
+@pytest.mark.parametrize("pdl", ["0", "1"])
+def test_atq_pdl_switch_gives_the_same_bits(pdl):
+    """The atq call's four launches (the last three started early unless
+    ABG_PDL=0): every output bit-exact to the oracle either way."""
+    env = dict(os.environ)
+    env["ABG_PDL"] = pdl
+    r = subprocess.run([sys.executable, "-c", CHILD_ATQ.format(root=ROOT)], env=env, capture_output=True,
+                       text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    assert "EQUAL 1" in r.stdout

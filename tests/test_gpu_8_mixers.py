@@ -94,7 +94,8 @@ def run_atq(c, tokens=1):
 
 @pytest.mark.parametrize("Hq,Hkv,D,P,pos", [(8, 2, 256, 4096, 2047), (4, 4, 64, 64, 0), (4, 2, 128, 300, 31),
                                             (4, 2, 128, 300, 32), (6, 3, 64, 200, 33), (2, 1, 256, 8192, 8191),
-                                            (8, 1, 128, 5000, 1000)])
+                                            (8, 1, 128, 5000, 1000), (6, 2, 64, 130, 127), (8, 2, 64, 700, 64),
+                                            (16, 4, 128, 1000, 511), (3, 1, 256, 100, 95)])
 def test_atq_bit_exact(Hq, Hkv, D, P, pos):
     run_atq(synth.atq_case(np.random.default_rng([Hq, Hkv, D, P, pos]), Hq, Hkv, D, P, pos))
 
