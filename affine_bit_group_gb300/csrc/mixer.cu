@@ -337,8 +337,8 @@ cudaError_t launch_gdn_d(const float *x, const float *conv, float *state, const 
 //     the block holding pos, the key, written to the cache row with the new
 //     value by the group's first block), the block's scores (each row of
 //     keys read once for the GB heads) and each head's maximum over them;
-//   exponentials: each head's maximum over the chunks, the chunk's
-//     exponentials (in place of the scores) and their sum;
+//   exponentials: each head's maximum over the half chunks' maxima, the
+//     chunk's exponentials (in place of the scores) and their sum;
 //   values: before its wait it copies the chunk's value rows into shared
 //     memory (rows below pos, which no earlier launch of the call writes; row
 //     pos is the new v); then Z, the tree over the chunks' sums, the
