@@ -652,6 +652,18 @@ abg_status abg_stage_graph_create(const abg_node *nodes, int64_t count, int mode
                 for (const Range &r : wr)
                     if (overlap(o, r)) return ABG_EALIAS;
     }
+    // an atq node reads its key cache rows before waiting for the launch
+    // before it: no other node writes its caches
+    for (int64_t i = 0; i < count; ++i) {
+        if (nodes[i].kind != ABG_NODE_ATQ) continue;
+        const Range caches[2] = {outs[i][0], outs[i][1]};  // Kc, Vc (atq_io's first two outputs)
+        for (int64_t j = 0; j < count; ++j) {
+            if (j == i) continue;
+            for (const Range &o : outs[j])
+                for (const Range &r : caches)
+                    if (overlap(o, r)) return ABG_EALIAS;
+        }
+    }
     // 3. launches: stage by stage; products of a stage that share their
     //    activation become one grouped launch
     std::vector<Launch> launches;

@@ -332,7 +332,8 @@ cudaError_t launch_gdn_d(const float *x, const float *conv, float *state, const 
 //
 // A block takes GB query heads of one KV group (GB = 4, 2 or 1, dividing the
 // group) and one chunk of 64 positions.  Four launches, the last three
-// started early by programmatic dependent launch:
+// started early by programmatic dependent launch (the first too: it reads
+// its cache rows below pos before waiting for the launch before it):
 //   scores (one block a half chunk): the normed, rotated queries (and, in
 //     the block holding pos, the key, written to the cache row with the new
 //     value by the group's first block), the block's scores (each row of
@@ -436,24 +437,12 @@ __global__ void __launch_bounds__(kAtqThreads) atq_scores_kernel(const __grid_co
     __shared__ __align__(16) float rot[NR][D];
     __shared__ float red[NR][D / 32];
     __shared__ float ssc[GB][kAtqSL];
-    // the next launch reads nothing of this one before its own wait
-    grid_dep_launch();
     const int s = blockIdx.x, c = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int per = a.Hq / a.Hkv, h0 = s * GB, g = h0 / per, n = a.pos + 1, t_lo = c * kAtqSL;
     const bool holds_pos = c == a.pos / kAtqSL;
     const int nr = GB + (holds_pos ? 1 : 0);  // the query rows, and the key in the block holding pos
-    // the rows to norm (row r of the thread's column j: r0 + k*kStep), their
-    // weights and this column's rotation, read ahead of the cache rows
-    const int j = tid % D, r0 = tid / D, ji = j % (D / 2);
-    float u[kRows];
-#pragma unroll
-    for (int k = 0; k < kRows; ++k) {
-        const int r = r0 + k * kStep;
-        u[k] = r < nr ? (r < GB ? a.q[static_cast<int64_t>(h0 + r) * D + j] : a.k[static_cast<int64_t>(g) * D + j])
-                      : 0.0f;
-    }
-    const float wq = a.qn_w[j], wk = a.kn_w[j], cj = a.cs[ji], sj = a.sn[ji];
-    // cache rows t_lo + 4 warp + r (r < 4) below pos; lane l holds columns
+    // cache rows t_lo + 4 warp + r (r < 4) below pos, read before waiting for
+    // the previous launch (which must not write them); lane l holds columns
     // l*CPL .. l*CPL+CPL-1 (row pos is this block's own key)
     const float *Kg = a.Kc + static_cast<int64_t>(g) * a.P * D + lane * CPL;
     const int tw = t_lo + kAtqRW * warp;
@@ -467,6 +456,19 @@ __global__ void __launch_bounds__(kAtqThreads) atq_scores_kernel(const __grid_co
             for (int cc = 0; cc < CPL; ++cc) kv[r][cc] = 0.0f;
         }
     }
+    grid_dep_wait();
+    grid_dep_launch();
+    // the rows to norm (row r of the thread's column j: r0 + k*kStep), their
+    // weights and this column's rotation
+    const int j = tid % D, r0 = tid / D, ji = j % (D / 2);
+    float u[kRows];
+#pragma unroll
+    for (int k = 0; k < kRows; ++k) {
+        const int r = r0 + k * kStep;
+        u[k] = r < nr ? (r < GB ? a.q[static_cast<int64_t>(h0 + r) * D + j] : a.k[static_cast<int64_t>(g) * D + j])
+                      : 0.0f;
+    }
+    const float wq = a.qn_w[j], wk = a.kn_w[j], cj = a.cs[ji], sj = a.sn[ji];
     // RMS norms: the rows' sums of squares (a warp holds 32 consecutive
     // columns of one row: the butterfly, then the tree over the warps)
 #pragma unroll
@@ -763,8 +765,9 @@ cudaError_t launch_atq_dg(const AtqArgs &a, bool pdl, cudaStream_t stream) {
     cudaError_t e = atq_attr<D, GB>();
     if (e != cudaSuccess) return e;
     const dim3 grid(a.Hq / GB, a.C);
-    atq_scores_kernel<D, GB><<<dim3(a.Hq / GB, a.pos / kAtqSL + 1), kAtqThreads, 0, stream>>>(a);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if ((e = launch_pdl(reinterpret_cast<const void *>(atq_scores_kernel<D, GB>), dim3(a.Hq / GB, a.pos / kAtqSL + 1),
+                        dim3(kAtqThreads), 0, a, pdl, stream)) != cudaSuccess)
+        return e;
     if ((e = launch_pdl(reinterpret_cast<const void *>(atq_exp_kernel<GB>), grid, dim3(kAtqThreads), 0, a, pdl,
                         stream)) != cudaSuccess)
         return e;

@@ -265,13 +265,15 @@ abg_status abg_gdn(const float *x, const float *conv, float *state, const float 
  *   y        f32 [Hq*D]    ysum  f32 [Hq*D/64]
  *   D = 64, 128 or 256; Hq a multiple of Hkv; 0 <= pos < P; pos + 1 <= 8192;
  *   Hq*D <= 2^20.
- * Both modes compute the same bits.  The positions run in chunks of 64 (two
- * launches, the second started early by programmatic dependent launch unless
- * ABG_PDL=0); the chunks' partial results and a completion counter per head
- * set live in a device buffer the library allocates, zeroed, on a device's
- * first call and grows when a call needs more (the growth synchronizes the
- * device); calls that can overlap on the GPU (on different streams or host
- * threads) share it and must be ordered by the caller.  Errors: null pointer
+ * Both modes compute the same bits.  The positions run in chunks of 64 (four
+ * launches, started early by programmatic dependent launch unless
+ * ABG_PDL=0): the first reads the key cache rows below pos before it waits
+ * for the launch before it on the stream, which therefore must not write
+ * them.  The chunks' partial results live in a device buffer the library
+ * allocates on a device's first call and grows when a call needs more (the
+ * growth synchronizes the device); calls that can overlap on the GPU (on
+ * different streams or host threads) share it and must be ordered by the
+ * caller.  Errors: null pointer
  * or mode ABG_EINVAL; shape ABG_ESHAPE; a pointer not 4-byte aligned, or Kc
  * or Vc not 16-byte aligned, ABG_EALIGN; an output (Kc, Vc, y, ysum)
  * overlapping an input or another output ABG_EALIAS.  Asynchronous on
@@ -316,7 +318,8 @@ abg_status abg_atq(const float *q, const float *gate, const float *k, const floa
  *                  and S in place
  *   ABG_NODE_ATQ   args (abg_atq_args): as abg_atq; writes row pos of Kc, Vc
  *                  (the graph owns the buffer of the chunk results of each
- *                  ATQ node, so replays of different graphs do not share it)
+ *                  ATQ node, so replays of different graphs do not share it);
+ *                  no other node may write its Kc or Vc (ABG_EALIAS)
  * Every kind also reads `group` (0 means 64): the group size of the product's
  * scale, bias and xsum (Q4MV, including the group sums its prologue
  * computes) or of out_sum (RMSQ, SWQ, GSUM); Q4MV reads `sb_type` (an

@@ -230,6 +230,10 @@ def test_stage_graph_mixer_node_validation(lib):
     # two mixers of one stage that share an output
     t2 = _atq_args(y=g.y)
     assert create(lib, [gn, node(kind=abg.NODE_ATQ, stage=0, args=ctypes.addressof(t2))]) == EALIAS
+    # a node of an earlier stage writing an atq node's key cache
+    t3 = _atq_args()
+    gs = dict(kind=3, stage=0, x=A + 0x500000, out_sum=t3.Kc + 4096, len=128)
+    assert create(lib, [node(**gs), node(kind=abg.NODE_ATQ, stage=1, args=ctypes.addressof(t3))]) == EALIAS
 
 
 def test_tuning_validation(lib):
