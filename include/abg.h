@@ -271,9 +271,11 @@ abg_status abg_gdn(const float *x, const float *conv, float *state, const float 
  * for the launch before it on the stream, which therefore must not write
  * them.  The chunks' partial results live in a device buffer the library
  * allocates on a device's first call and grows when a call needs more (the
- * growth synchronizes the device); calls that can overlap on the GPU (on
- * different streams or host threads) share it and must be ordered by the
- * caller.  Errors: null pointer
+ * growth synchronizes the device, so a call recorded into a stream capture
+ * must not need more than an earlier call outside it: ABG_ECUDA otherwise);
+ * calls that can overlap on the GPU (on different streams or host threads)
+ * share it and must be ordered by the caller.  A stage graph's atq nodes
+ * have buffers of their own.  Errors: null pointer
  * or mode ABG_EINVAL; shape ABG_ESHAPE; a pointer not 4-byte aligned, or Kc
  * or Vc not 16-byte aligned, ABG_EALIGN; an output (Kc, Vc, y, ysum)
  * overlapping an input or another output ABG_EALIAS.  Asynchronous on
