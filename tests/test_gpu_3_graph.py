@@ -279,3 +279,27 @@ def test_prologues_many_tiles_6144(prologue):
                               what=f"fast {prologue} {rows}x{cols}")
         g.close()
     assert abg.device_status(clear=True) == 0
+
+
+def test_many_products_of_one_stage():
+    """300 products of one stage reading one x, of seven row counts: grouped
+    launches of at most 64 products (five), each launch walking its problems
+    tile by tile.  Every output bit-exact to the oracle."""
+    rng = np.random.default_rng(77)
+    cols = 512
+    mats = [synth.q4_matrix(rng, 40 + 8 * (i % 7), cols) for i in range(300)]
+    x = synth.activations(rng, cols)
+    xs = oracle.gsum(x)
+    dx, dxs = dev(x), dev(xs)
+    dm = [(dev_words(m.w), dev(m.scale), dev(m.bias)) for m in mats]
+    ys = [empty(m.rows) for m in mats]
+    nodes = [abg.Node.q4mv(0, *dm[i], ys[i], cols, x=dx, xsum=dxs) for i in range(len(mats))]
+    g = abg.StageGraph(nodes, keep=[dx, dxs] + ys + [t for d in dm for t in d])
+    assert g.launches == 5
+    for _ in range(2):
+        g.launch()
+    torch.cuda.synchronize()
+    for i, m in enumerate(mats):
+        assert_bits_equal(host(ys[i]), oracle.q4mv(m.w, m.scale, m.bias, x, xs, cols), f"product {i}")
+    g.close()
+    assert abg.device_status(clear=True) == 0
