@@ -242,12 +242,13 @@ abg_status check_atq(const abg_atq_args &t, int mode) {
     return disjoint_outputs(in, out);
 }
 
+bool pdl_enabled();
+
 cudaError_t run_gdn(const abg_gdn_args &g, cudaStream_t s) {
     return launch_gdn(g.x, g.conv, g.state, g.a, g.b, g.z, g.A_log, g.dt_bias, g.nw, g.S, g.y, g.ysum,
-                      static_cast<int>(g.H), static_cast<int>(g.D), static_cast<int>(g.K), g.eps, g.eps_n, s);
+                      static_cast<int>(g.H), static_cast<int>(g.D), static_cast<int>(g.K), g.eps, g.eps_n,
+                      pdl_enabled(), s);
 }
-
-bool pdl_enabled();
 
 cudaError_t run_atq(const abg_atq_args &t, float *scratch, cudaStream_t s) {
     return launch_atq(t.q, t.gate, t.k, t.v, t.qn_w, t.kn_w, t.cos, t.sin, t.Kc, t.Vc, t.y, t.ysum,
@@ -350,9 +351,10 @@ cudaError_t prepare(const Launch &L) {
     return prepare_q4mv(L.plan);
 }
 
-// The mixers' kernels start only after the previous launch has finished (no
-// programmatic dependent launch); the launch after them may overlap their
-// tail with its prologue, as after any other launch.
+// The mixers' launches start early like the products' (programmatic
+// dependent launch): gdn reads every input after its wait; atq's first
+// launch reads only its own key cache rows before it (no other node writes
+// them).
 cudaError_t run(const Launch &L, cudaStream_t s, bool pdl, bool tree) {
     switch (L.kind) {
     case ABG_NODE_Q4MV: return launch_q4mv(L.plan, s, pdl);

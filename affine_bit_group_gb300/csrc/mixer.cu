@@ -184,6 +184,12 @@ __global__ void __launch_bounds__(gdn_groups<D>() * D, 1) gdn_kernel(
             fence_mbar_init();
         }
         __syncthreads();
+    }
+    // every input may come from the launch before (programmatic dependent
+    // launch: this block was scheduled while it ran)
+    grid_dep_wait();
+    grid_dep_launch();
+    if constexpr (kStage) {
         if (tid == 0) {
             mbar_arrive_expect_tx(&bar, D * D * 4);
             bulk_g2s(Ss, Sh, D * D * 4, &bar, l2_evict_first());
@@ -314,13 +320,21 @@ cudaError_t gdn_attr() {
 template <int D>
 cudaError_t launch_gdn_d(const float *x, const float *conv, float *state, const float *a, const float *b,
                          const float *z, const float *A_log, const float *dt_bias, const float *nw, float *S,
-                         float *y, float *ysum, int H, int K, float eps, float eps_n, cudaStream_t stream) {
-    constexpr int kSmem = gdn_smem<D>();
+                         float *y, float *ysum, int H, int K, float eps, float eps_n, bool pdl, cudaStream_t stream) {
     const cudaError_t attr = gdn_attr<D>();
     if (attr != cudaSuccess) return attr;
-    gdn_kernel<D><<<H, gdn_groups<D>() * D, kSmem, stream>>>(x, conv, state, a, b, z, A_log, dt_bias, nw, S, y,
-                                                             ysum, H, K, eps, eps_n);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(H));
+    cfg.blockDim = dim3(gdn_groups<D>() * D);
+    cfg.dynamicSmemBytes = gdn_smem<D>();
+    cfg.stream = stream;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, gdn_kernel<D>, x, conv, state, a, b, z, A_log, dt_bias, nw, S, y, ysum, H, K,
+                              eps, eps_n);
 }
 
 // ------------------------------------------------------------------ atq ----
@@ -848,13 +862,16 @@ cudaError_t atq_scratch(size_t bytes, float **out) {
 
 cudaError_t launch_gdn(const float *x, const float *conv, float *state, const float *a, const float *b,
                        const float *z, const float *A_log, const float *dt_bias, const float *nw, float *S, float *y,
-                       float *ysum, int H, int D, int K, float eps, float eps_n, cudaStream_t stream) {
+                       float *ysum, int H, int D, int K, float eps, float eps_n, bool pdl, cudaStream_t stream) {
     switch (D) {
-    case 64: return launch_gdn_d<64>(x, conv, state, a, b, z, A_log, dt_bias, nw, S, y, ysum, H, K, eps, eps_n, stream);
+    case 64:
+        return launch_gdn_d<64>(x, conv, state, a, b, z, A_log, dt_bias, nw, S, y, ysum, H, K, eps, eps_n, pdl, stream);
     case 128:
-        return launch_gdn_d<128>(x, conv, state, a, b, z, A_log, dt_bias, nw, S, y, ysum, H, K, eps, eps_n, stream);
+        return launch_gdn_d<128>(x, conv, state, a, b, z, A_log, dt_bias, nw, S, y, ysum, H, K, eps, eps_n, pdl,
+                                 stream);
     case 256:
-        return launch_gdn_d<256>(x, conv, state, a, b, z, A_log, dt_bias, nw, S, y, ysum, H, K, eps, eps_n, stream);
+        return launch_gdn_d<256>(x, conv, state, a, b, z, A_log, dt_bias, nw, S, y, ysum, H, K, eps, eps_n, pdl,
+                                 stream);
     default: return cudaErrorInvalidValue;
     }
 }

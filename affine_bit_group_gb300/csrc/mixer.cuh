@@ -8,10 +8,12 @@
 namespace abg {
 
 // gdn: one token for H heads of D (64, 128 or 256) columns, K conv taps
-// (2..8); arguments as abg_gdn.
+// (2..8); arguments as abg_gdn.  With `pdl` the kernel's blocks may be
+// scheduled while the launch before runs; they read every input after it
+// has finished.
 cudaError_t launch_gdn(const float *x, const float *conv, float *state, const float *a, const float *b,
                        const float *z, const float *A_log, const float *dt_bias, const float *nw, float *S, float *y,
-                       float *ysum, int H, int D, int K, float eps, float eps_n, cudaStream_t stream);
+                       float *ysum, int H, int D, int K, float eps, float eps_n, bool pdl, cudaStream_t stream);
 // sets the gdn kernel's shared-memory attribute for D (done by launch_gdn too)
 cudaError_t prepare_gdn(int D);
 // atq: one token for Hq query heads over Hkv key/value heads of D (64, 128 or

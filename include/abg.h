@@ -231,7 +231,9 @@ abg_status abg_swq_ex(const float *a, float *o, float *osum, int64_t n, int grou
  *   S        f32 [H][D][D] (key i, value j), updated in place; 16-byte aligned
  *   y        f32 [H*D]              ysum   f32 [H*D/64]
  *   D = 64, 128 or 256; 2 <= K <= 8; H >= 1, H*D <= 2^20.
- * Both modes compute the same bits.  Errors: null pointer or mode
+ * Both modes compute the same bits.  One launch, started early by
+ * programmatic dependent launch unless ABG_PDL=0 (it reads every input after
+ * the launch before it has finished).  Errors: null pointer or mode
  * ABG_EINVAL; shape ABG_ESHAPE; a pointer not 4-byte aligned, or S not
  * 16-byte aligned, ABG_EALIGN; an
  * output (state, S, y, ysum) overlapping an input or another output
