@@ -25,6 +25,7 @@
 #include "mixer.cuh"
 
 #include <mutex>
+#include <type_traits>
 
 namespace abg {
 
@@ -657,8 +658,10 @@ __global__ void __launch_bounds__(kAtqValThreads) atq_values_kernel(const __grid
     // (each value row read once for them); then the tree over the quarters
     constexpr int kHS = kAtqThreads / D, kHPT = GB / kHS > 0 ? GB / kHS : 1;
     const int q = tid >> 8, hs = (tid & 255) / D, j = tid % D;
-    const bool full = t_lo + kAtqL <= n;
-    if (hs < GB) {
+    // (positions past pos only in the chunk holding it: a separate copy of
+    // the loop, so full chunks run without the per-position test)
+    auto weighted = [&](auto ragged_c) {
+        constexpr bool kRagged = decltype(ragged_c)::value;
         float vv[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) vv[i] = vs[(16 * q + i) * D + j];
@@ -674,7 +677,7 @@ __global__ void __launch_bounds__(kAtqValThreads) atq_values_kernel(const __grid
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const int ti = 16 * q + 4 * m + i;
-                    e[4 * m + i] = full || t_lo + ti < n ? __fmul_rn(p[i], vv[4 * m + i]) : -0.0f;
+                    e[4 * m + i] = !kRagged || t_lo + ti < n ? __fmul_rn(p[i], vv[4 * m + i]) : -0.0f;
                 }
             }
 #pragma unroll
@@ -682,6 +685,13 @@ __global__ void __launch_bounds__(kAtqValThreads) atq_values_kernel(const __grid
 #pragma unroll
                 for (int i = 0; i < h; ++i) e[i] = __fadd_rn(e[2 * i], e[2 * i + 1]);
             s_part[q][hh][j] = e[0];
+        }
+    };
+    if (hs < GB) {
+        if (t_lo + kAtqL <= n) {
+            weighted(std::false_type{});
+        } else {
+            weighted(std::true_type{});
         }
     }
     __syncthreads();
