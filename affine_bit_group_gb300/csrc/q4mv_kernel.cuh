@@ -895,7 +895,7 @@ __device__ __forceinline__ float tree_fixed(const float (&v)[N]) {
 template <int R, bool kTree, bool kSbSmem, int kLayout, int kLg, bool kHalf, int kC = 0>
 __global__ void __launch_bounds__(layout_bound_threads(kLayout), layout_blocks(kLayout))
     q4mv_kernel(const __grid_constant__ Q4Args a) {
-    static_assert(kC == 0 || (kLayout != 2 && kLg == 1 && !kHalf && kSbSmem), "fixed shapes: default format only");
+    static_assert(kC == 0 || (kLayout != 2 && kLg == 1 && kSbSmem), "fixed shapes: groups of 64, staged scale/bias");
     constexpr bool kFix = kC != 0;
     constexpr int kL = 1 << kLg;                  // lanes per group
     constexpr uint32_t kElem = kHalf ? 2u : 4u;   // bytes per stored scale or bias
@@ -921,7 +921,7 @@ __global__ void __launch_bounds__(layout_bound_threads(kLayout), layout_blocks(k
     const int TR = kFix ? kTRf : a.tile_rows, W = kFix ? kC / 8 : a.W, G = kFix ? kC / 64 : a.G;
     const int nch = kFix ? fixed_nch(kC) : a.nch, nw = kFix ? fixed_nw(kC, kLayout) : a.nw;
     const uint32_t stage_w_bytes = kFix ? static_cast<uint32_t>(kTRf * kC / 2) : a.stage_w_bytes;
-    const uint32_t stage_sb_bytes = kFix ? static_cast<uint32_t>(kTRf * (kC / 64) * 4) : a.stage_sb_bytes;
+    const uint32_t stage_sb_bytes = kFix ? static_cast<uint32_t>(kTRf * (kC / 64)) * kElem : a.stage_sb_bytes;
     const uint32_t stage_bytes = kFix ? stage_w_bytes + 2 * stage_sb_bytes : a.stage_bytes;
 
     if (threadIdx.x == 0) {
