@@ -24,8 +24,12 @@ cudaError_t q4mv_status_g128(unsigned *bits, bool clear);
 cudaError_t q4mv_status_g128h(unsigned *bits, bool clear);
 void *q4mv_select_fixed(int cols, bool tree, int R, int layout);
 void *q4mv_select_fixed_half(int cols, bool tree, int R, int layout);
+void *q4mv_select_fixed_g32(int cols, bool tree, int R, int layout, bool half);
+void *q4mv_select_fixed_g128(int cols, bool tree, int R, int layout, bool half);
 cudaError_t q4mv_status_fixed(unsigned *bits, bool clear);
 cudaError_t q4mv_status_fixed_half(unsigned *bits, bool clear);
+cudaError_t q4mv_status_fixed_g32(unsigned *bits, bool clear);
+cudaError_t q4mv_status_fixed_g128(unsigned *bits, bool clear);
 
 namespace {
 
@@ -35,7 +39,11 @@ namespace {
 // with 8 rows per item only).  shape != 0 selects the fixed-shape
 // instantiation for that row length (q4mv_fixed.cu).
 void *select_kernel(int lg, bool half, int R, bool tree, bool sb, int layout, int shape = 0) {
-    if (shape != 0) return half ? q4mv_select_fixed_half(shape, tree, R, layout) : q4mv_select_fixed(shape, tree, R, layout);
+    if (shape != 0) {
+        if (lg == 0) return q4mv_select_fixed_g32(shape, tree, R, layout, half);
+        if (lg == 2) return q4mv_select_fixed_g128(shape, tree, R, layout, half);
+        return half ? q4mv_select_fixed_half(shape, tree, R, layout) : q4mv_select_fixed(shape, tree, R, layout);
+    }
     if (lg == 1 && !half) {
         if (layout == 0) return select_layout0<1, false>(R, tree, sb);
         if (R != 8) return nullptr;
@@ -65,7 +73,8 @@ inline uint32_t align_up(uint32_t v, uint32_t a) { return (v + a - 1) / a * a; }
 cudaError_t q4mv_status(unsigned *bits, bool clear) {
     cudaError_t (*const units[])(unsigned *, bool) = {read_status_word,   q4mv_status_g32,  q4mv_status_g32h,
                                                       q4mv_status_g64h,   q4mv_status_g128, q4mv_status_g128h,
-                                                      q4mv_status_fixed,  q4mv_status_fixed_half};
+                                                      q4mv_status_fixed,  q4mv_status_fixed_half,
+                                                      q4mv_status_fixed_g32, q4mv_status_fixed_g128};
     for (auto f : units) {
         const cudaError_t e = f(bits, clear);
         if (e != cudaSuccess) return e;
@@ -142,7 +151,7 @@ bool plan_once(Q4Plan *plan, const Q4Prob *probs, int nprob, int cols, int group
     const uint32_t row_bytes = static_cast<uint32_t>(C / 2) + (sb_smem ? 2u * G * elem : 0u);
     // the fixed-shape prologue stages the activation: cols floats, G group
     // sums, G group flags and a flag per 128 columns
-    const bool fmt_fixed = lg == 1;  // the formats with fixed-shape instantiations: groups of 64, any scale/bias type
+    const bool fmt_fixed = lg >= 0 && lg <= 2;  // every format has fixed-shape instantiations
     const bool act_stage = fmt_fixed && sb_smem && (C == 2048 || C == 4096 || C == 6144);
     const uint32_t act_bytes = act_stage ? align_up(static_cast<uint32_t>(C * 4 + G * 8 + C / 32), 128) : 0u;
     const uint32_t fixed = 1024 + act_bytes;  // barriers, alignment slack and the staged activation
@@ -305,7 +314,7 @@ bool plan_q4mv(Q4Plan *plan, const Q4Prob *probs, int nprob, int cols, int group
     if (rows_per_warp == 0) {
         const bool plain_tuning = tune.smem_kb == 0 && tune.consumer_warps == 0 && tune.blocks_per_sm == 0 &&
                                   tune.stage_kb == 0;
-        if (plain_tuning && group == 64 && sb_smem && (cols == 2048 || cols == 4096 || cols == 6144)) {
+        if (plain_tuning && sb_smem && (cols == 2048 || cols == 4096 || cols == 6144)) {
             const int tr = fixed_tr(cols, 4, 1);
             int64_t tiles = 0;
             for (int i = 0; i < nprob; ++i) tiles += (probs[i].n + tr - 1) / tr;
@@ -319,7 +328,7 @@ bool plan_q4mv(Q4Plan *plan, const Q4Prob *probs, int nprob, int cols, int group
     }
     // rows of 6144 columns in a launch of many tiles: 18 computing warps in one
     // block per SM (three per chunk), where the two-block layout has six
-    if (rows_per_warp == 8 && cols == 6144 && group == 64 && sb_smem &&
+    if (rows_per_warp == 8 && cols == 6144 && group != 32 && sb_smem &&
         tune.smem_kb == 0 && tune.consumer_warps == 0 && tune.blocks_per_sm == 0 && tune.stage_kb == 0) {
         const int tr = fixed_tr(cols, 8, 4);
         int64_t tiles = 0;

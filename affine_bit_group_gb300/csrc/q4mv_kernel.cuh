@@ -456,17 +456,18 @@ __device__ __forceinline__ float rms_factor_all(const float *red, float eps, int
 }
 
 // Group sums of NU units at once: the thread's pairwise sum of a unit's 4
-// values, then butterfly steps at distances 1, 2, 4 and 8 over the 16 threads
-// of the unit's group (the pairwise tree over its 64 values); the steps of
-// the NU units are interleaved so that their shuffles overlap.
-template <bool kTree, int NU>
+// values, then butterfly steps at distances 1, 2, .. UG/2 over the UG threads
+// of the unit's group (the pairwise tree over its 4 UG values: UG = 16 for 64
+// values); the steps of the NU units are interleaved so that their shuffles
+// overlap.
+template <bool kTree, int NU, int UG = 16>
 __device__ __forceinline__ void sum4_groups(const float4 (&v)[NU], float (&s)[NU]) {
 #pragma unroll
     for (int k = 0; k < NU; ++k)
         s[k] = kTree ? __fadd_rn(__fadd_rn(v[k].x, v[k].y), __fadd_rn(v[k].z, v[k].w))
                      : (v[k].x + v[k].y) + (v[k].z + v[k].w);
 #pragma unroll
-    for (int d = 1; d < 16; d <<= 1) {
+    for (int d = 1; d < UG; d <<= 1) {
         float o[NU];
 #pragma unroll
         for (int k = 0; k < NU; ++k) o[k] = __shfl_xor_sync(0xffffffffu, s[k], d);
@@ -475,11 +476,11 @@ __device__ __forceinline__ void sum4_groups(const float4 (&v)[NU], float (&s)[NU
     }
 }
 
-template <bool kTree>
+template <bool kTree, int UG = 16>
 __device__ __forceinline__ float sum4_group(float4 v) {
     float s = kTree ? __fadd_rn(__fadd_rn(v.x, v.y), __fadd_rn(v.z, v.w)) : (v.x + v.y) + (v.z + v.w);
 #pragma unroll
-    for (int d = 1; d < 16; d <<= 1) {
+    for (int d = 1; d < UG; d <<= 1) {
         const float o = __shfl_xor_sync(0xffffffffu, s, d);
         s = kTree ? __fadd_rn(s, o) : s + o;
     }
@@ -490,11 +491,14 @@ __device__ __forceinline__ float sum4_group(float4 v) {
 // values in the per-lane layout.  A 128-column block of ordinary values (a
 // warp's 32 units) is staged times -2^(23-4k) of its columns' nibbles, the
 // exact path's operands; a block with a special value is staged as it is.
+// gneg is per group of UG units (the format's group: 32, 64 or 128 columns).
+template <int UG>
 __device__ __forceinline__ void stage_unit(float4 q, int u, int lane, unsigned bsp, unsigned bneg, float *act,
                                            unsigned *gneg, unsigned *spec) {
+    constexpr unsigned kMask = UG == 32 ? 0xffffffffu : (1u << UG) - 1u;
     const int c = 4 * u;
     if (lane == 0) spec[u >> 5] = bsp != 0u;
-    if ((u & 15) == 0) gneg[u >> 4] = ((bneg >> (lane & 16)) & 0xffffu) == 0xffffu;
+    if ((u & (UG - 1)) == 0) gneg[u / UG] = ((bneg >> (lane & (32 - UG))) & kMask) == kMask;
     const int ch = c >> 10, l = (c & 1023) >> 5, i = (c & 31) >> 2;
     float4 st = q;
     if (bsp == 0u) {
@@ -510,11 +514,12 @@ __device__ __forceinline__ void stage_unit(float4 q, int u, int lane, unsigned b
 // a thread's units are interleaved.  Otherwise one warp computes the factor
 // between two barriers and the units go one after the other (the throughput
 // layout's product loop measured faster with this prologue).
-template <bool kTree, int kC, int kNct, bool kLatency>
+template <bool kTree, int kC, int kNct, bool kLatency, int kLg>
 __device__ __forceinline__ void coop_prologue(const Q4Args &a, const CoopIn<(kC / 4 + kNct - 1) / kNct> &in,
                                               float *act, float *gs, unsigned *gneg, unsigned *spec, int cw,
                                               float *red, float *rbox) {
     constexpr int NU = (kC / 4 + kNct - 1) / kNct;
+    constexpr int UG = 8 << kLg;  // units of the format's group (the sums of squares use groups of 64)
     // units per thread: NU, or in a block whose threads do not divide the
     // units, NU - 1 for the threads of the last round's idle warps (whole
     // warps: the units and the threads are multiples of 32)
@@ -575,11 +580,11 @@ __device__ __forceinline__ void coop_prologue(const Q4Args &a, const CoopIn<(kC 
     if constexpr (kLatency) {
         if (a.prologue != kProNone) {
             float gsum[NU];
-            sum4_groups<kTree, NU>(v, gsum);
+            sum4_groups<kTree, NU, UG>(v, gsum);
 #pragma unroll
             for (int k = 0; k < NU; ++k) {
                 const int u = t + k * kNct;
-                if ((u & 15) == 0) gs[u >> 4] = gsum[k];
+                if ((u & (UG - 1)) == 0) gs[u / UG] = gsum[k];
             }
         }
         unsigned bspk[NU], bnegk[NU];
@@ -592,7 +597,7 @@ __device__ __forceinline__ void coop_prologue(const Q4Args &a, const CoopIn<(kC 
             bnegk[k] = __ballot_sync(0xffffffffu, neg);
         }
 #pragma unroll
-        for (int k = 0; k < NU; ++k) stage_unit(v[k], t + k * kNct, lane, bspk[k], bnegk[k], act, gneg, spec);
+        for (int k = 0; k < NU; ++k) stage_unit<UG>(v[k], t + k * kNct, lane, bspk[k], bnegk[k], act, gneg, spec);
     } else {
 #pragma unroll
         for (int k = 0; k < NU; ++k) {
@@ -600,13 +605,13 @@ __device__ __forceinline__ void coop_prologue(const Q4Args &a, const CoopIn<(kC 
             const int u = t + k * kNct;
             const float4 q = v[k];
             if (a.prologue != kProNone) {
-                const float s = sum4_group<kTree>(q);
-                if ((u & 15) == 0) gs[u >> 4] = s;
+                const float s = sum4_group<kTree, UG>(q);
+                if ((u & (UG - 1)) == 0) gs[u / UG] = s;
             }
             const bool sp = !x_ordinary(q.x) || !x_ordinary(q.y) || !x_ordinary(q.z) || !x_ordinary(q.w);
             const bool neg = q.x < 0.f && q.y < 0.f && q.z < 0.f && q.w < 0.f;
             const unsigned bsp = __ballot_sync(0xffffffffu, sp), bneg = __ballot_sync(0xffffffffu, neg);
-            stage_unit(q, u, lane, bsp, bneg, act, gneg, spec);
+            stage_unit<UG>(q, u, lane, bsp, bneg, act, gneg, spec);
         }
     }
     named_bar(1, kNct);
@@ -895,7 +900,7 @@ __device__ __forceinline__ float tree_fixed(const float (&v)[N]) {
 template <int R, bool kTree, bool kSbSmem, int kLayout, int kLg, bool kHalf, int kC = 0>
 __global__ void __launch_bounds__(layout_bound_threads(kLayout), layout_blocks(kLayout))
     q4mv_kernel(const __grid_constant__ Q4Args a) {
-    static_assert(kC == 0 || (kLayout != 2 && kLg == 1 && kSbSmem), "fixed shapes: groups of 64, staged scale/bias");
+    static_assert(kC == 0 || (kLayout != 2 && kSbSmem), "fixed shapes: staged scale/bias");
     constexpr bool kFix = kC != 0;
     constexpr int kL = 1 << kLg;                  // lanes per group
     constexpr uint32_t kElem = kHalf ? 2u : 4u;   // bytes per stored scale or bias
@@ -918,10 +923,10 @@ __global__ void __launch_bounds__(layout_bound_threads(kLayout), layout_blocks(k
     const int S = a.stages;
     constexpr int kTRf = kFix ? fixed_tr(kC, R, kLayout) : 0;
     static_assert(!kFix || kTRf == R * (fixed_nw(kC, kLayout) / fixed_nch(kC)), "one item per warp and tile");
-    const int TR = kFix ? kTRf : a.tile_rows, W = kFix ? kC / 8 : a.W, G = kFix ? kC / 64 : a.G;
+    const int TR = kFix ? kTRf : a.tile_rows, W = kFix ? kC / 8 : a.W, G = kFix ? kC / (32 << kLg) : a.G;
     const int nch = kFix ? fixed_nch(kC) : a.nch, nw = kFix ? fixed_nw(kC, kLayout) : a.nw;
     const uint32_t stage_w_bytes = kFix ? static_cast<uint32_t>(kTRf * kC / 2) : a.stage_w_bytes;
-    const uint32_t stage_sb_bytes = kFix ? static_cast<uint32_t>(kTRf * (kC / 64)) * kElem : a.stage_sb_bytes;
+    const uint32_t stage_sb_bytes = kFix ? static_cast<uint32_t>(kTRf * (kC / (32 << kLg))) * kElem : a.stage_sb_bytes;
     const uint32_t stage_bytes = kFix ? stage_w_bytes + 2 * stage_sb_bytes : a.stage_bytes;
 
     if (threadIdx.x == 0) {
@@ -1112,9 +1117,9 @@ __global__ void __launch_bounds__(layout_bound_threads(kLayout), layout_blocks(k
         // the activation once per block, staged in shared memory
         float *act = reinterpret_cast<float *>(smem + a.off_act);
         float *gs = act + kC;
-        unsigned *gneg = reinterpret_cast<unsigned *>(gs + kC / 64);
-        unsigned *spec = gneg + kC / 64;
-        coop_prologue<kTree, kC, kNct, kLayout == 1>(a, cin, act, gs, gneg, spec, cw, s_red, &s_rbox);
+        unsigned *gneg = reinterpret_cast<unsigned *>(gs + kC / (32 << kLg));
+        unsigned *spec = gneg + kC / (32 << kLg);
+        coop_prologue<kTree, kC, kNct, kLayout == 1, kLg>(a, cin, act, gs, gneg, spec, cw, s_red, &s_rbox);
         slice_from_stage<kTree, kLg>(a, ch0, lane, act, gs, gneg, spec, sl);
         if constexpr (kLayout != 1) set_chunk(ch0);
         cur_ch = ch0;

@@ -204,17 +204,19 @@ def test_producers_group_sums(group):
     assert_bits_equal(host(os_), oracle.gsum_ex(o_o, group), "swq sums")
 
 
-@pytest.mark.parametrize("sb", ["bf16", "f16"])
+@pytest.mark.parametrize("group,sb", [(64, "bf16"), (64, "f16"), (32, "f32"), (32, "bf16"), (128, "f32"),
+                                      (128, "f16")])
 @pytest.mark.parametrize("rows,cols", [(20480, 2048), (9000, 4096), (15360, 6144), (2048, 2048), (700, 6144)])
-def test_fixed_shapes_with_16bit_scale_bias(sb, rows, cols):
-    """Groups of 64 with bf16 or f16 scale and bias run the fixed-shape
-    instantiations (many tiles: 8 rows per item, two blocks per SM or, for 6144
+def test_fixed_shapes_every_format(group, sb, rows, cols):
+    """Every format runs the fixed-shape instantiations at 2048, 4096 and 6144
+    columns (many tiles: 8 rows per item, two blocks per SM or, for 6144
     columns, 18 warps in one; few tiles: 4 rows per item, 16 warps): every row
-    bit-exact in tree mode, fast mode within its bound."""
-    m, x = synth.fmt_case(64, sb, rows, cols)
+    bit-exact in tree mode; fast mode within its bound (the smaller shapes)."""
+    m, x = synth.fmt_case(group, sb, rows, cols)
     exp = expect(m, x)
-    assert_bits_equal(run(m, x), exp, f"g64 {sb} {rows}x{cols}")
-    assert_fast_close(run(m, x, mode=abg.FAST), exp, magnitude(m, x), what=f"fast g64 {sb} {rows}x{cols}")
+    assert_bits_equal(run(m, x), exp, f"g{group} {sb} {rows}x{cols}")
+    if rows * cols <= 8 << 20:
+        assert_fast_close(run(m, x, mode=abg.FAST), exp, magnitude(m, x), what=f"fast g{group} {sb} {rows}x{cols}")
     assert abg.device_status(clear=True) == 0
 
 
