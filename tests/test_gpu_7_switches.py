@@ -166,3 +166,45 @@ def test_atq_pdl_switch_gives_the_same_bits(pdl):
                        text=True, timeout=600)
     assert r.returncode == 0, r.stderr[-2000:]
     assert "EQUAL 1" in r.stdout
+
+
+CHILD_GDN = """
+import sys
+sys.path.insert(0, {root!r})
+import numpy as np, torch
+import affine_bit_group_gb300 as abg
+import oracle
+from affine_bit_group_gb300 import synth
+rng = np.random.default_rng(41)
+c = synth.gdn_case(rng)
+xs = [rng.standard_normal(c["x"].size).astype(np.float32) for _ in range(3)]
+d = {{k: torch.from_numpy(np.ascontiguousarray(v)).cuda() for k, v in c.items()}}
+H, D = c["S"].shape[0], c["S"].shape[1]
+ys = [torch.empty(H * D, device="cuda") for _ in xs]
+yss = [torch.empty(H * D // 64, device="cuda") for _ in xs]
+dx = [torch.from_numpy(x).cuda() for x in xs]
+for t in range(3):   # three tokens back to back, the state carried, no sync between
+    abg.gdn(dx[t], d["conv"], d["state"], d["a"], d["b"], d["z"], d["A_log"], d["dt_bias"], d["nw"], d["S"], ys[t],
+            yss[t])
+torch.cuda.synchronize()
+S, st, same = c["S"], c["state"], True
+for t in range(3):
+    ey, eys, S, st = oracle.gdn(**dict(c, x=xs[t], S=S, state=st))
+    same &= np.array_equal(ys[t].cpu().numpy().view(np.uint32), ey.view(np.uint32))
+    same &= np.array_equal(yss[t].cpu().numpy().view(np.uint32), eys.view(np.uint32))
+same &= np.array_equal(d["S"].cpu().numpy().view(np.uint32), S.view(np.uint32))
+print("EQUAL", int(same))
+"""
+
+
+@pytest.mark.parametrize("pdl", ["0", "1"])
+def test_gdn_pdl_switch_gives_the_same_bits(pdl):
+    """Three gdn tokens on one state back to back (each launch scheduled early
+    unless ABG_PDL=0, reading its inputs after the previous one finished):
+    every output and the final state bit-exact to the oracle either way."""
+    env = dict(os.environ)
+    env["ABG_PDL"] = pdl
+    r = subprocess.run([sys.executable, "-c", CHILD_GDN.format(root=ROOT)], env=env, capture_output=True,
+                       text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    assert "EQUAL 1" in r.stdout
