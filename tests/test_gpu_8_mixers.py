@@ -155,3 +155,31 @@ def test_mixers_as_stage_graph_nodes():
         assert_bits_equal(host(oa), oracle.q4mv(ma.w, ma.scale, ma.bias, ay, ays, Hq * Dq), f"atq product {t}")
     graph.close()
     assert abg.device_status(clear=True) == 0
+
+
+def test_atq_tokens_back_to_back():
+    """Four tokens at positions 127..130 (across a chunk boundary) queued back
+    to back on one stream, with no sync between them: each token's first launch
+    reads the cache rows below its position before waiting for the launch
+    before it, so the row the previous token wrote must already be there.
+    Every output and both caches bit-exact to the oracle."""
+    c = synth.atq_case(np.random.default_rng(9), 8, 2, 128, 300, 127)
+    d = {k: dev(v) for k, v in c.items() if k != "pos"}
+    Hkv, P, D = c["Kc"].shape
+    Hq = c["q"].size // D
+    rng = np.random.default_rng(10)
+    ins = [{k: rng.standard_normal(c[k].size).astype(np.float32) for k in ("q", "gate", "k", "v")} for _ in range(4)]
+    dins = [{k: dev(v) for k, v in t.items()} for t in ins]
+    ys = [(empty(Hq * D), empty(Hq * D // 64)) for _ in ins]
+    for t in range(4):
+        abg.atq(dins[t]["q"], dins[t]["gate"], dins[t]["k"], dins[t]["v"], d["qn_w"], d["kn_w"], d["cos"], d["sin"],
+                d["Kc"], d["Vc"], ys[t][0], ys[t][1], pos=127 + t)
+    torch.cuda.synchronize()
+    Kr, Vr = c["Kc"], c["Vc"]
+    for t in range(4):
+        ey, eys, Kr, Vr = oracle.atq(**dict(c, **ins[t], Kc=Kr, Vc=Vr, pos=127 + t))
+        assert_bits_equal(host(ys[t][0]), ey, f"y at {127 + t}")
+        assert_bits_equal(host(ys[t][1]), eys, f"ysum at {127 + t}")
+    assert_bits_equal(host(d["Kc"]).reshape(Kr.shape), Kr, "K cache")
+    assert_bits_equal(host(d["Vc"]).reshape(Vr.shape), Vr, "V cache")
+    assert abg.device_status(clear=True) == 0
