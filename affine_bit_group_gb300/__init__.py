@@ -80,6 +80,8 @@ class _AtqArgs(ctypes.Structure):
 def library(build_if_missing: bool = True) -> ctypes.CDLL:
     """Loads libabg.so (building it with nvcc first if it is missing or stale)."""
     global _lib
+    if _lib is not None:  # loaded: no lock on the per-call path
+        return _lib
     with _lock:
         if _lib is None:
             if build_if_missing:
@@ -158,9 +160,15 @@ def _stream(stream):
     return stream.cuda_stream
 
 
+_DTYPES = None
+
+
 def _dtypes():
-    import torch
-    return torch.int32, torch.float32
+    global _DTYPES
+    if _DTYPES is None:
+        import torch
+        _DTYPES = (torch.int32, torch.float32)
+    return _DTYPES
 
 
 def q4mv(w, scale, bias, x, xsum, y, cols: int, row0: int = 0, n: int | None = None, mode: int = TREE,
