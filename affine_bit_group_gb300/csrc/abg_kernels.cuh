@@ -1,12 +1,22 @@
 // Launch descriptors and host-side launchers of the library's kernels.
 #pragma once
 
+#include <cstddef>
 #include <cstdint>
+#include <cstring>
 #include <cuda_runtime.h>
 
 namespace abg {
 
-constexpr int kMaxProbs = 64;  // products that share one activation in a grouped launch
+// Products that share one activation in a grouped launch: the table of the
+// planner and of the throughput kernels.  A kernel's argument block costs
+// launch time in proportion to its size (about 0.02 us per KB on every
+// launch), so each kernel family takes the smallest table its launches need:
+// the few-tiles instantiations (a decode token's products) kFewProbs, the
+// batched product's kernels (one product a launch) kMmProbs.
+constexpr int kMaxProbs = 256;
+constexpr int kFewProbs = 16;
+constexpr int kMmProbs = 1;
 
 enum Prologue { kProNone = 0, kProGsum = 1, kProRmsq = 2, kProSwq = 3 };
 
@@ -21,9 +31,11 @@ struct Q4Prob {
     int tr;     // rows per tile of this problem: tile_rows, or a quarter of it (see plan_q4mv)
 };
 
-// Everything the product kernel needs, passed by value (__grid_constant__).
-struct Q4Args {
-    Q4Prob prob[kMaxProbs];
+// Everything the product kernel needs, passed by value (__grid_constant__),
+// with a table of kP products after the other fields (so every table size
+// lays those fields out alike).
+template <int kP>
+struct Q4ArgsT {
     int nprob;
     int64_t total_tiles;
     // activation: x/xsum for kProNone; producer inputs otherwise (see abg.h)
@@ -63,7 +75,18 @@ struct Q4Args {
     const float *xt[4];
     const float *xst[4];
     int ntok;
+    Q4Prob prob[kP];
 };
+using Q4Args = Q4ArgsT<kMaxProbs>;
+
+// A plan's arguments with a smaller table (nprob <= kP, which the planners
+// ensure for the kernels that take one).
+template <int kP>
+void narrow_args(Q4ArgsT<kP> &dst, const Q4Args &src) {
+    static_assert(offsetof(Q4ArgsT<kP>, prob) == offsetof(Q4Args, prob), "fields laid out alike");
+    std::memcpy(&dst, &src, offsetof(Q4Args, prob));
+    std::memcpy(dst.prob, src.prob, static_cast<size_t>(src.nprob < kP ? src.nprob : kP) * sizeof(Q4Prob));
+}
 
 struct Q4Tuning {
     int smem_kb = 0;

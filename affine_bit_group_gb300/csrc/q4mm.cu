@@ -49,7 +49,8 @@ inline uint32_t align_up(uint32_t v, uint32_t a) { return (v + a - 1) / a * a; }
 bool plan_q4mm(Q4Plan *plan, const Q4Prob *probs, int nprob, int cols, int T, int ntok, const float *const *xt,
                const float *const *xst, int prologue, bool tree, int rows_per_warp, bool sb_smem) {
     (void)rows_per_warp;  // rows per item follow from T (T * R = 8 values per lane)
-    if ((T == 2 ? !select_mm(T, tree, sb_smem) : !(T == 4 && cols == kMm4Cols && sb_smem)) || ntok < 1 || ntok > T)
+    if ((T == 2 ? !select_mm(T, tree, sb_smem) : !(T == 4 && cols == kMm4Cols && sb_smem)) || ntok < 1 || ntok > T ||
+        nprob < 1 || nprob > kMmProbs)
         return false;
     Q4Args &a = plan->args;
     a = Q4Args{};
@@ -164,7 +165,9 @@ cudaError_t launch_q4mm(const Q4Plan &plan, cudaStream_t stream, bool pdl) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    void *params[] = {const_cast<Q4Args *>(&plan.args)};
+    Q4ArgsT<kMmProbs> mm;
+    narrow_args(mm, plan.args);
+    void *params[] = {&mm};
     return cudaLaunchKernelExC(&cfg, fn, params);
 }
 

@@ -46,7 +46,7 @@ __host__ __device__ constexpr int mmf_tr(int C) { return C == 2048 ? 32 : 16; } 
 constexpr int kMmfItems = 4;  // items per warp and tile
 
 template <bool kTree, int kC>
-__global__ void __launch_bounds__(288, 2) q4mm_fixed_kernel(const __grid_constant__ Q4Args a) {
+__global__ void __launch_bounds__(288, 2) q4mm_fixed_kernel(const __grid_constant__ Q4ArgsT<kMmProbs> a) {
     constexpr int T = 2, R = 4, LC = 16, kL = 4, GPC = 8;
     constexpr int W = kC / 8, G = kC / 64, NCH = mmf_nch(kC), NW = 8, KK = mmf_kk(kC), TR = mmf_tr(kC);
     static_assert(TR == R * KK * kMmfItems, "4 items per warp and tile");
@@ -274,7 +274,7 @@ constexpr int kMm4Cols = 2048;
 constexpr int kMm4Rows = 32;  // tile rows (8 items of 4 rows per warp)
 
 template <bool kTree>
-__global__ void __launch_bounds__(288, 2) q4mm4_fixed_kernel(const __grid_constant__ Q4Args a) {
+__global__ void __launch_bounds__(288, 2) q4mm4_fixed_kernel(const __grid_constant__ Q4ArgsT<kMmProbs> a) {
     constexpr int T = 4, R = 4, LC = 8, kL = 8, GPC = 4, kC = kMm4Cols;
     constexpr int W = kC / 8, G = kC / 64, NCH = kC / 256, NW = 8, TR = kMm4Rows, NI = TR / R;
     static_assert(NCH == NW, "one chunk per computing warp");

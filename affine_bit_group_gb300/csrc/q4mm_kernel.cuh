@@ -87,7 +87,7 @@ struct MSlice {
 // Activation slices for chunk ch: x of token t at a.xt[t]; group sums given
 // (kProNone, a.xst[t]) or computed (kProGsum).
 template <int T, int LC, bool kTree>
-__device__ __forceinline__ void load_mslice(const Q4Args &a, int ch, int lane, MSlice<T, LC> &sl) {
+__device__ __forceinline__ void load_mslice(const Q4ArgsT<kMmProbs> &a, int ch, int lane, MSlice<T, LC> &sl) {
     constexpr int kL = 64 / LC, GPC = 32 / kL;
     const int C = a.cols, base = ch * 32 * LC + lane * LC;
     const bool active = base < C;
@@ -201,7 +201,7 @@ __device__ __forceinline__ float pick(const float (&xs)[T], int t) {
 }
 
 template <int T, int R, bool kTree, bool kSbSmem>
-__global__ void __launch_bounds__(288, 2) q4mm_kernel(const __grid_constant__ Q4Args a) {
+__global__ void __launch_bounds__(288, 2) q4mm_kernel(const __grid_constant__ Q4ArgsT<kMmProbs> a) {
     constexpr int LC = mm_lane_cols<T>();
     constexpr int CW = 32 * LC;      // columns of a warp's chunk
     constexpr int kL = 64 / LC;      // lanes per 64-column group

@@ -124,6 +124,7 @@ void quarter_tail(Q4Args &a, int TR, int R, int64_t sms) {
 bool plan_once(Q4Plan *plan, const Q4Prob *probs, int nprob, int cols, int group, int sb_type, int prologue,
                const float *x, const float *xsum, const float *wt, float eps, bool tree, int rows_per_warp,
                bool sb_smem, const Q4Tuning &tune, bool allow_few, int force_layout = -1) {
+    if (nprob < 1 || nprob > kMaxProbs) return false;
     Q4Args &a = plan->args;
     a = Q4Args{};
     const int R = rows_per_warp;
@@ -238,9 +239,10 @@ bool plan_once(Q4Plan *plan, const Q4Prob *probs, int nprob, int cols, int group
     a.smem_bytes = a.off_act + act_bytes;
 
     // a plan with the compile-time shape of its row length runs the
-    // fixed-shape instantiation (same results, constant sizes)
+    // fixed-shape instantiation (same results, constant sizes) if its product
+    // table holds the launch's products
     int shape = 0;
-    if (fmt_fixed && sb_smem &&
+    if (fmt_fixed && sb_smem && nprob <= kernel_probs(layout, C) &&
         ((layout == 0 && R == 8) || (layout == 1 && R == 4) || (layout == 4 && R == 8 && C == 6144)) &&
         (C == 2048 || C == 4096 || C == 6144) && TR == fixed_tr(C, R, layout) && nw == fixed_nw(C, layout) &&
         nch == fixed_nch(C) && a.stage_w_bytes == static_cast<uint32_t>(TR * C / 2) &&
@@ -366,6 +368,12 @@ cudaError_t launch_q4mv(const Q4Plan &plan, cudaStream_t stream, bool pdl) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
+    if (kernel_probs(plan.layout, plan.shape) == kFewProbs) {
+        Q4ArgsT<kFewProbs> few;
+        narrow_args(few, plan.args);
+        void *params[] = {&few};
+        return cudaLaunchKernelExC(&cfg, fn, params);
+    }
     void *params[] = {const_cast<Q4Args *>(&plan.args)};
     return cudaLaunchKernelExC(&cfg, fn, params);
 }

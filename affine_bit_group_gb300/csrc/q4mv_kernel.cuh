@@ -261,8 +261,8 @@ struct Slice {
 
 // The rest of a slice from its activation values v (zero where inactive):
 // the product path, the group sums, and the pairs X of lane_sum32.
-template <bool kTree, int kLg>
-__device__ __forceinline__ void finish_slice(const Q4Args &a, int ch, int lane, bool active, float (&v)[32],
+template <bool kTree, int kLg, class A>
+__device__ __forceinline__ void finish_slice(const A &a, int ch, int lane, bool active, float (&v)[32],
                                              Slice &sl) {
     // special values take the plain path; groups whose values are all
     // negative are marked for the sign of a zero group sum (see the product
@@ -318,8 +318,8 @@ __device__ __forceinline__ void finish_slice(const Q4Args &a, int ch, int lane, 
     }
 }
 
-template <bool kTree, int kLg>
-__device__ __forceinline__ void load_slice(const Q4Args &a, int ch, int lane, float rms_r, Slice &sl) {
+template <bool kTree, int kLg, class A>
+__device__ __forceinline__ void load_slice(const A &a, int ch, int lane, float rms_r, Slice &sl) {
     const int C = a.cols, base = ch * 1024 + lane * 32;
     const bool active = base < C;
     float v[32];
@@ -365,8 +365,8 @@ __device__ __forceinline__ void load_slice(const Q4Args &a, int ch, int lane, fl
 // block_rms_factor's), one warp per chunk posts them (post), and the factor
 // scales the values in place.  Every computing warp calls this, idle ones with
 // has = false, since it holds the block barriers.
-template <bool kTree, int kLg>
-__device__ __forceinline__ void rms_slice(const Q4Args &a, int ch, bool has, bool post, int cw, int nw, int lane,
+template <bool kTree, int kLg, class A>
+__device__ __forceinline__ void rms_slice(const A &a, int ch, bool has, bool post, int cw, int nw, int lane,
                                           float *red, float *rbox, Slice &sl) {
     const int C = a.cols, base = ch * 1024 + lane * 32;
     const bool active = has && base < C;
@@ -514,8 +514,8 @@ __device__ __forceinline__ void stage_unit(float4 q, int u, int lane, unsigned b
 // a thread's units are interleaved.  Otherwise one warp computes the factor
 // between two barriers and the units go one after the other (the throughput
 // layout's product loop measured faster with this prologue).
-template <bool kTree, int kC, int kNct, bool kLatency, int kLg>
-__device__ __forceinline__ void coop_prologue(const Q4Args &a, const CoopIn<(kC / 4 + kNct - 1) / kNct> &in,
+template <bool kTree, int kC, int kNct, bool kLatency, int kLg, class A>
+__device__ __forceinline__ void coop_prologue(const A &a, const CoopIn<(kC / 4 + kNct - 1) / kNct> &in,
                                               float *act, float *gs, unsigned *gneg, unsigned *spec, int cw,
                                               float *red, float *rbox) {
     constexpr int NU = (kC / 4 + kNct - 1) / kNct;
@@ -623,8 +623,8 @@ __device__ __forceinline__ void coop_prologue(const Q4Args &a, const CoopIn<(kC 
 // in the chunk) a lane whose own 128-column block was scaled takes the
 // scaling back, which is exact (ordinary values were scaled up by at least
 // 2^7 without overflow).
-template <bool kTree, int kLg>
-__device__ __forceinline__ void slice_from_stage(const Q4Args &a, int ch, int lane, const float *act,
+template <bool kTree, int kLg, class A>
+__device__ __forceinline__ void slice_from_stage(const A &a, int ch, int lane, const float *act,
                                                  const float *gs, const unsigned *gneg, const unsigned *spec,
                                                  Slice &sl) {
     float v[32];
@@ -658,7 +658,8 @@ __device__ __forceinline__ void slice_from_stage(const Q4Args &a, int ch, int la
 struct ProbCursor {
     int p = 0;
     int base = 0;  // first tile of problem p
-    __device__ __forceinline__ int find(const Q4Args &a, int t, int &tile) {
+    template <class A>
+    __device__ __forceinline__ int find(const A &a, int t, int &tile) {
         while (p + 1 < a.nprob && t >= base + static_cast<int>(a.prob[p].tiles)) {
             base += static_cast<int>(a.prob[p].tiles);
             ++p;
@@ -789,7 +790,8 @@ struct TileHdr {
 };
 
 // The i-th tile of this block: tiles blockIdx.x, blockIdx.x + gridDim.x, ...
-__device__ __forceinline__ int tile_of(const Q4Args &, int i) {
+template <class A>
+__device__ __forceinline__ int tile_of(const A &, int i) {
     return static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x);
 }
 constexpr int kMaxStages = 8;
@@ -897,9 +899,16 @@ __device__ __forceinline__ float tree_fixed(const float (&v)[N]) {
     }
 }
 
+// The product table of an instantiation: the few-tiles fixed shapes (block
+// layout 1 with a compile-time row length, a decode token's launches) take
+// kFewProbs products, every other instantiation kMaxProbs.
+__host__ __device__ constexpr int kernel_probs(int layout, int c) {
+    return layout == 1 && c != 0 ? kFewProbs : kMaxProbs;
+}
+
 template <int R, bool kTree, bool kSbSmem, int kLayout, int kLg, bool kHalf, int kC = 0>
 __global__ void __launch_bounds__(layout_bound_threads(kLayout), layout_blocks(kLayout))
-    q4mv_kernel(const __grid_constant__ Q4Args a) {
+    q4mv_kernel(const __grid_constant__ Q4ArgsT<kernel_probs(kLayout, kC)> a) {
     static_assert(kC == 0 || (kLayout != 2 && kSbSmem), "fixed shapes: staged scale/bias");
     constexpr bool kFix = kC != 0;
     constexpr int kL = 1 << kLg;                  // lanes per group

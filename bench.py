@@ -6,16 +6,16 @@ Verification: a 4096x2048 product run 400 times, printing a hash of y).  One
 step = the activation's group sums, then the 400 products queued as one stage
 ("Array.q4go/Array.q4wait ..." #1437, Change: queued products run
 concurrently and none reads another's y), recorded as one stage graph and
-launched once.  Each product reads its own copy of the weights from a ring
-whose total size is several times the L2 cache, so every call streams its
-weights from HBM.
+launched once.  Each of the 400 products reads its own copy of the weights
+(2.1 GB in all, many times the L2 cache), so every call streams its weights
+from HBM and nothing read in one step is still cached in the next.
 
 Also measured in the same run (as "extra"): the same 400 products as 400
 dependent stages (each waits for the previous one: decode-like latency), the
 248320x2048 output head, one synthetic 24-layer decode token (fused and
 unfused stage graphs), the 4096x2048 product in every weight format
 (groups of 32, 64 or 128 columns; f32, bf16 or f16 scale and bias), each as a
-grouped launch of 64 products streaming from HBM, the batched product
+grouped launch of 256 products streaming from HBM, the batched product
 (1, 2, 4 and 8 tokens sharing the 248320x2048 head's weights), and the pages'
 own timing of the 4096x2048 product ((400-call - 1-call)/400, median of 6).
 and the rows x cols x rows-per-item x mode sweep (GB/s and fraction of peak
@@ -46,7 +46,7 @@ sys.path.insert(0, ROOT)
 from affine_bit_group_gb300 import synth  # noqa: E402
 
 CALLS = 400
-GROUP = 64  # products per grouped launch (the library's limit)
+GROUP = 256  # products per grouped launch (the library's limit)
 MID_ROWS, MID_COLS = 4096, 2048
 PEAK_FALLBACK_GBS = 6800.0
 
@@ -230,7 +230,9 @@ def run_ours(args, rank, world):
     # ---------------------------------------------------------------- mid ---
     m, x_np = synth.mid()
     pbytes = product_bytes(MID_ROWS, MID_COLS)
-    copies = max(2, math.ceil(3 * l2 / (m.nbytes)))
+    # one copy per product of the step: no product of a grouped launch or of
+    # the next step finds its weights in L2
+    copies = max(CALLS, math.ceil(3 * l2 / (m.nbytes)))
     mats = rotating_copies(m, copies)
     x = torch.from_numpy(x_np).cuda()
     xsum = torch.empty(MID_COLS // 64, dtype=torch.float32, device="cuda")
@@ -250,7 +252,7 @@ def run_ours(args, rank, world):
     us_per_product = ms_step * 1e3 / CALLS
     launches_per_step = g.launches
 
-    # the dominant kernel alone: one grouped launch of 64 products (the
+    # the dominant kernel alone: one grouped launch of 256 products (the
     # step's product launches are of this kind), timed with CUDA events on
     # the stream it runs on
     g1 = abg.StageGraph([abg.Node.q4mv(0, *mats[i % len(mats)], ys[i], MID_COLS, x=x, xsum=xsum)
@@ -335,18 +337,18 @@ def bench_head(abg, stream, args, peak):
 
 
 def bench_formats(abg, stream, args, peak, l2):
-    """The 4096x2048 product in each format: one grouped launch of 64 products,
-    each on its own copy of the weights (the copies total several times L2)."""
+    """The 4096x2048 product in each format: one grouped launch of 256 products,
+    each on its own copy of the weights (the copies total many times L2)."""
     import torch
 
     import oracle
-    out = {"workload": "q4mv 4096x2048, one grouped launch of 64 products per replay, weights from HBM"}
+    out = {"workload": "q4mv 4096x2048, one grouped launch of 256 products per replay, weights from HBM"}
     for group in synth.GROUPS:
         for sb in synth.SB_TYPES:
             m, x_np = synth.fmt_case(group, sb, MID_ROWS, MID_COLS)
             sbb = 4 if sb == "f32" else 2
             pb = product_bytes(MID_ROWS, MID_COLS, group, sbb)
-            copies = max(2, math.ceil(3 * l2 / m.nbytes))
+            copies = max(GROUP, math.ceil(3 * l2 / m.nbytes))
             w = torch.from_numpy(m.w.view(np.int32)).cuda()
             sc = torch.from_numpy(m.scale.view(np.int16) if sbb == 2 else m.scale).cuda()
             bi = torch.from_numpy(m.bias.view(np.int16) if sbb == 2 else m.bias).cuda()
@@ -482,12 +484,12 @@ def bench_sweep(abg, stream, args, peak, l2):
 
 def bench_pages_way(abg, stream, args):
     """The pages' timing of the 4096x2048 product: (400-call - 1-call) / 400, rounds
-    alternating, median of 6, calls back to back on one stream over rotating
-    weight copies (> 3x L2)."""
+    alternating, median of 6, calls back to back on one stream, each call of a
+    round on its own copy of the weights."""
     import torch
     m, x_np = synth.mid()
     l2 = getattr(torch.cuda.get_device_properties(0), "L2_cache_size", 126 * 2 ** 20)
-    copies = max(2, math.ceil(3 * l2 / m.nbytes))
+    copies = max(CALLS, math.ceil(3 * l2 / m.nbytes))
     mats = rotating_copies(m, copies)
     x = torch.from_numpy(x_np).cuda()
     xs = torch.empty(MID_COLS // 64, dtype=torch.float32, device="cuda")
@@ -812,7 +814,7 @@ def main():
         "hash32": res["hash"],
         "roofline": {"bound": "hbm", "achieved": res["achieved"], "peak": res["peak"], "unit": "GB/s",
                      "frac": res["achieved"] / res["peak"], "traffic": traffic, "peak_kind": res["peak_kind"],
-                     "kernel": "q4mv_kernel<8,tree,bulk scale/bias>: one launch of 64 products of 4096x2048",
+                     "kernel": "q4mv_kernel<8,tree,bulk scale/bias>: one launch of 256 products of 4096x2048",
                      "bytes_per_launch": GROUP * product_bytes(MID_ROWS, MID_COLS),
                      "launch_us": res["launch_us"]},
         "clocks": res["clocks"], "e2e": res["e2e"], "gpu_launches": res["launches"], "extra": res["extra"],

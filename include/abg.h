@@ -297,7 +297,8 @@ abg_status abg_atq(const float *q, const float *gate, const float *k, const floa
  * Nodes carry a stage index.  Nodes with the same index form one stage and
  * may run concurrently; every node of stage s+1 runs after every node of
  * stage s has finished.  Products of one stage that read the same x (for
- * example q/k/v, or gate/up) are run as one grouped launch.  Consecutive
+ * example q/k/v, or gate/up) are run as grouped launches of up to 256
+ * products each (abg_stage_graph_launches counts them).  Consecutive
  * launches overlap through programmatic dependent launch: a product fetches
  * its weights before the previous stage has finished and waits only before
  * it reads its activation.  Weights, and the norm weights of an RMS-norm

@@ -283,7 +283,7 @@ def test_prologues_many_tiles_6144(prologue):
 
 def test_many_products_of_one_stage():
     """300 products of one stage reading one x, of seven row counts: grouped
-    launches of at most 64 products (five), each launch walking its problems
+    launches of at most 256 products (two), each launch walking its problems
     tile by tile.  Every output bit-exact to the oracle."""
     rng = np.random.default_rng(77)
     cols = 512
@@ -295,11 +295,40 @@ def test_many_products_of_one_stage():
     ys = [empty(m.rows) for m in mats]
     nodes = [abg.Node.q4mv(0, *dm[i], ys[i], cols, x=dx, xsum=dxs) for i in range(len(mats))]
     g = abg.StageGraph(nodes, keep=[dx, dxs] + ys + [t for d in dm for t in d])
-    assert g.launches == 5
+    assert g.launches == 2
     for _ in range(2):
         g.launch()
     torch.cuda.synchronize()
     for i, m in enumerate(mats):
         assert_bits_equal(host(ys[i]), oracle.q4mv(m.w, m.scale, m.bias, x, xs, cols), f"product {i}")
+    g.close()
+    assert abg.device_status(clear=True) == 0
+
+
+@pytest.mark.parametrize("count", [16, 17, 40])
+def test_few_tiles_table_capacity(count):
+    """A stage of small products of 2048 columns reading one x (with the
+    RMS-norm prologue): one grouped launch of few tiles.  Up to 16 products
+    it runs the few-tiles instantiation, whose product table holds 16; more
+    products run the 8-row instantiation with the full table.  Every output
+    bit-exact to the oracle, in both cases."""
+    rng = np.random.default_rng(500 + count)
+    cols = 2048
+    mats = [synth.q4_matrix(rng, 32 + 16 * (i % 3), cols) for i in range(count)]
+    h = synth.activations(rng, cols)
+    wt = synth.rms_weights(rng, cols)
+    xn, xs = oracle.rmsq(h, wt, 1e-6)
+    dh, dwt = dev(h), dev(wt)
+    dm = [(dev_words(m.w), dev(m.scale), dev(m.bias)) for m in mats]
+    ys = [empty(m.rows) for m in mats]
+    nodes = [abg.Node.q4mv(0, *dm[i], ys[i], cols, x=dh, wt=dwt, eps=1e-6, prologue=abg.PRO_RMSQ)
+             for i in range(count)]
+    g = abg.StageGraph(nodes, keep=[dh, dwt] + ys + [t for d in dm for t in d])
+    assert g.launches == 1
+    for _ in range(2):
+        g.launch()
+    torch.cuda.synchronize()
+    for i, m in enumerate(mats):
+        assert_bits_equal(host(ys[i]), oracle.q4mv(m.w, m.scale, m.bias, xn, xs, cols), f"product {i}")
     g.close()
     assert abg.device_status(clear=True) == 0
