@@ -51,7 +51,9 @@ print("HASH", oracle.hash32(got))
 
 
 def child(env_extra, fused, reps):
-    env = dict(os.environ)
+    # the switches a test does not set are off in the child, whatever the
+    # parent's environment holds
+    env = {k: v for k, v in os.environ.items() if k not in ("ABG_PDL", "ABG_TRACE")}
     env.update(env_extra)
     code = CHILD.format(root=ROOT, small=SMALL, fused=fused, reps=reps)
     r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=600)
@@ -126,7 +128,7 @@ print("EQUAL", int(np.array_equal(got.view(np.uint32), exp.view(np.uint32))))
 def test_batched_pdl_switch_gives_the_same_bits(pdl):
     """Five tokens (two pair launches and a single-token launch, the later ones
     started early unless ABG_PDL=0): every token bit-exact either way."""
-    env = dict(os.environ)
+    env = {k: v for k, v in os.environ.items() if k != "ABG_TRACE"}
     env["ABG_PDL"] = pdl
     r = subprocess.run([sys.executable, "-c", CHILD_MM.format(root=ROOT)], env=env, capture_output=True, text=True,
                        timeout=600)
@@ -160,7 +162,7 @@ print("EQUAL", int(same))
 def test_atq_pdl_switch_gives_the_same_bits(pdl):
     """The atq call's four launches (the last three started early unless
     ABG_PDL=0): every output bit-exact to the oracle either way."""
-    env = dict(os.environ)
+    env = {k: v for k, v in os.environ.items() if k != "ABG_TRACE"}
     env["ABG_PDL"] = pdl
     r = subprocess.run([sys.executable, "-c", CHILD_ATQ.format(root=ROOT)], env=env, capture_output=True,
                        text=True, timeout=600)
@@ -202,7 +204,7 @@ def test_gdn_pdl_switch_gives_the_same_bits(pdl):
     """Three gdn tokens on one state back to back (each launch scheduled early
     unless ABG_PDL=0, reading its inputs after the previous one finished):
     every output and the final state bit-exact to the oracle either way."""
-    env = dict(os.environ)
+    env = {k: v for k, v in os.environ.items() if k != "ABG_TRACE"}
     env["ABG_PDL"] = pdl
     r = subprocess.run([sys.executable, "-c", CHILD_GDN.format(root=ROOT)], env=env, capture_output=True,
                        text=True, timeout=600)
