@@ -23,7 +23,7 @@ __all__ = [
 
 TREE, FAST = 0, 1
 MAX_COLS = 16384
-NODE_Q4MV, NODE_RMSQ, NODE_SWQ, NODE_GSUM, NODE_GDN, NODE_ATQ = 0, 1, 2, 3, 4, 5
+NODE_Q4MV, NODE_RMSQ, NODE_SWQ, NODE_GSUM, NODE_GDN, NODE_ATQ, NODE_COPY = 0, 1, 2, 3, 4, 5, 6
 PRO_NONE, PRO_GSUM, PRO_RMSQ, PRO_SWQ = 0, 1, 2, 3
 SB_F32, SB_BF16, SB_F16 = 0, 1, 2
 SB_TYPES = {"f32": SB_F32, "bf16": SB_BF16, "f16": SB_F16}
@@ -362,6 +362,21 @@ class Node:
         nd = _Node(kind=NODE_ATQ, stage=stage, args=ctypes.addressof(t))
         nd._args = t
         return nd
+
+    @staticmethod
+    def copy(stage, src, dst):
+        """A copy node: src's float32 values into dst.  Each is a CUDA tensor or
+        a pinned CPU tensor, so that a replay can take its inputs from host
+        memory and hand its results back there."""
+        import torch
+        for t, name in ((src, "src"), (dst, "dst")):
+            if t.dtype != torch.float32 or not t.is_contiguous():
+                raise ValueError(f"{name} must be a contiguous float32 tensor")
+            if not t.is_cuda and not t.is_pinned():
+                raise ValueError(f"{name} must be a CUDA tensor or pinned host memory")
+        if dst.numel() < src.numel():
+            raise ValueError(f"dst holds {dst.numel()} elements, needs {src.numel()}")
+        return _Node(kind=NODE_COPY, stage=stage, x=src.data_ptr(), out=dst.data_ptr(), len=src.numel())
 
 
 class StageGraph:

@@ -180,6 +180,28 @@ abg_status check_swq(const float *a, const float *o, const float *osum, int64_t 
     return ABG_OK;
 }
 
+// A copy node: len floats from x to out, each device memory or page-locked
+// host memory (a captured copy from pageable memory would not be an
+// asynchronous graph node).
+bool copyable(const void *p) {
+    cudaPointerAttributes at{};
+    const cudaError_t e = cudaPointerGetAttributes(&at, p);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeHost || at.type == cudaMemoryTypeManaged;
+}
+
+abg_status check_copy(const float *x, const float *out, int64_t len) {
+    if (!x || !out) return ABG_EINVAL;
+    if (len <= 0) return ABG_ESHAPE;
+    if (!aligned(x, 4) || !aligned(out, 4)) return ABG_EALIGN;
+    if (overlap(rng(x, len, 4), rng(out, len, 4))) return ABG_EALIAS;
+    if (!copyable(x) || !copyable(out)) return ABG_EINVAL;
+    return ABG_OK;
+}
+
 // the ranges a gdn call reads and writes (state and S are read and written)
 void gdn_io(const abg_gdn_args &g, std::vector<Range> &in, std::vector<Range> &out) {
     const int64_t C = 3 * g.H * g.D;
@@ -244,16 +266,15 @@ abg_status check_atq(const abg_atq_args &t, int mode) {
 
 bool pdl_enabled();
 
-cudaError_t run_gdn(const abg_gdn_args &g, cudaStream_t s) {
+cudaError_t run_gdn(const abg_gdn_args &g, cudaStream_t s, bool pdl) {
     return launch_gdn(g.x, g.conv, g.state, g.a, g.b, g.z, g.A_log, g.dt_bias, g.nw, g.S, g.y, g.ysum,
-                      static_cast<int>(g.H), static_cast<int>(g.D), static_cast<int>(g.K), g.eps, g.eps_n,
-                      pdl_enabled(), s);
+                      static_cast<int>(g.H), static_cast<int>(g.D), static_cast<int>(g.K), g.eps, g.eps_n, pdl, s);
 }
 
-cudaError_t run_atq(const abg_atq_args &t, float *scratch, cudaStream_t s) {
+cudaError_t run_atq(const abg_atq_args &t, float *scratch, cudaStream_t s, bool pdl) {
     return launch_atq(t.q, t.gate, t.k, t.v, t.qn_w, t.kn_w, t.cos, t.sin, t.Kc, t.Vc, t.y, t.ysum,
                       static_cast<int>(t.Hq), static_cast<int>(t.Hkv), static_cast<int>(t.D), static_cast<int>(t.P),
-                      static_cast<int>(t.pos), t.eps, scratch, pdl_enabled(), s);
+                      static_cast<int>(t.pos), t.eps, scratch, pdl, s);
 }
 
 // --------------------------------------------------------------- graphs ----
@@ -354,12 +375,15 @@ cudaError_t prepare(const Launch &L) {
 // The mixers' launches start early like the products' (programmatic
 // dependent launch): gdn reads every input after its wait; atq's first
 // launch reads only its own key cache rows before it (no other node writes
-// them).
-cudaError_t run(const Launch &L, cudaStream_t s, bool pdl, bool tree) {
+// them).  No launch starts early after a copy (`after_copy`): early start
+// overlaps a kernel with the kernel before it only.
+cudaError_t run(const Launch &L, cudaStream_t s, bool pdl, bool tree, bool after_copy) {
     switch (L.kind) {
     case ABG_NODE_Q4MV: return launch_q4mv(L.plan, s, pdl);
-    case ABG_NODE_GDN: return run_gdn(L.gdn, s);
-    case ABG_NODE_ATQ: return run_atq(L.atq, L.atq_scratch, s);
+    case ABG_NODE_GDN: return run_gdn(L.gdn, s, pdl_enabled() && !after_copy);
+    case ABG_NODE_ATQ: return run_atq(L.atq, L.atq_scratch, s, pdl_enabled() && !after_copy);
+    case ABG_NODE_COPY:
+        return cudaMemcpyAsync(L.o, L.a, static_cast<size_t>(L.len) * sizeof(float), cudaMemcpyDefault, s);
     case ABG_NODE_RMSQ: return launch_rmsq(L.a, L.b, L.eps, L.o, L.os, L.len, L.group, tree, s, pdl);
     case ABG_NODE_SWQ: return launch_swq(L.a, L.o, L.os, L.len, L.group, tree, s, pdl);
     default: return launch_gsum(L.a, L.os, L.len, L.group, tree, s, pdl);
@@ -404,6 +428,10 @@ void node_io(const abg_node &nd, std::vector<Range> &in, std::vector<Range> &out
         break;
     case ABG_NODE_GDN: gdn_io(*static_cast<const abg_gdn_args *>(nd.args), in, out); break;
     case ABG_NODE_ATQ: atq_io(*static_cast<const abg_atq_args *>(nd.args), in, out); break;
+    case ABG_NODE_COPY:
+        in = {rng(nd.x, nd.len, 4)};
+        out = {rng(nd.out, nd.len, 4)};
+        break;
     default:
         in = {rng(nd.x, nd.len, 4)};
         out = {rng(nd.out_sum, nd.len / node_group(nd.group), 4)};
@@ -585,7 +613,7 @@ abg_status abg_gdn(const float *x, const float *conv, float *state, const float 
     const abg_gdn_args g{x, conv, state, a, b, z, A_log, dt_bias, nw, S, y, ysum, H, D, K, eps, eps_n};
     const abg_status st = check_gdn(g, mode);
     if (st != ABG_OK) return st;
-    return cuda_fail(run_gdn(g, static_cast<cudaStream_t>(stream)), "gdn launch");
+    return cuda_fail(run_gdn(g, static_cast<cudaStream_t>(stream), pdl_enabled()), "gdn launch");
 }
 
 abg_status abg_atq(const float *q, const float *gate, const float *k, const float *v, const float *qn_w,
@@ -594,7 +622,7 @@ abg_status abg_atq(const float *q, const float *gate, const float *k, const floa
     const abg_atq_args t{q, gate, k, v, qn_w, kn_w, cos, sin, Kc, Vc, y, ysum, Hq, Hkv, D, P, pos, eps};
     const abg_status st = check_atq(t, mode);
     if (st != ABG_OK) return st;
-    return cuda_fail(run_atq(t, nullptr, static_cast<cudaStream_t>(stream)), "atq launch");
+    return cuda_fail(run_atq(t, nullptr, static_cast<cudaStream_t>(stream), pdl_enabled()), "atq launch");
 }
 
 abg_status abg_stage_graph_create(const abg_node *nodes, int64_t count, int mode, int rows_per_warp,
@@ -620,6 +648,7 @@ abg_status abg_stage_graph_create(const abg_node *nodes, int64_t count, int mode
         case ABG_NODE_ATQ:
             st = nd.args ? check_atq(*static_cast<const abg_atq_args *>(nd.args), mode) : ABG_EINVAL;
             break;
+        case ABG_NODE_COPY: st = check_copy(nd.x, nd.out, nd.len); break;
         default: st = ABG_EINVAL;
         }
         if (st != ABG_OK) return st;
@@ -709,7 +738,7 @@ abg_status abg_stage_graph_create(const abg_node *nodes, int64_t count, int mode
         }
     }
     auto *g = new StageGraph();
-    g->launches = static_cast<int64_t>(launches.size());
+    for (const Launch &L : launches) g->launches += L.kind == ABG_NODE_COPY ? 0 : (L.kind == ABG_NODE_ATQ ? 4 : 1);
     {
         const abg_status st = fuse_swiglu_pairs(launches, g, mode, rows_per_warp);
         if (st != ABG_OK) {
@@ -747,9 +776,12 @@ abg_status abg_stage_graph_create(const abg_node *nodes, int64_t count, int mode
         if (launches[i].kind == ABG_NODE_Q4MV && launches[i].stage == launches[i - 1].stage)
             launches[i].plan.args.wait_first = 0;
     if (e == cudaSuccess) {
-        for (size_t i = 0; i < launches.size() && e == cudaSuccess; ++i)
-            if ((e = run(launches[i], cs, pdl_on && i > 0, mode == ABG_TREE)) != cudaSuccess)
+        for (size_t i = 0; i < launches.size() && e == cudaSuccess; ++i) {
+            const bool after_copy = i > 0 && launches[i - 1].kind == ABG_NODE_COPY;
+            if ((e = run(launches[i], cs, pdl_on && i > 0 && !after_copy, mode == ABG_TREE, after_copy)) !=
+                cudaSuccess)
                 where = "launch " + std::to_string(i) + " (kind " + std::to_string(launches[i].kind) + ")";
+        }
         cudaGraph_t graph = nullptr;
         const cudaError_t e2 = cudaStreamEndCapture(cs, &graph);
         if (e == cudaSuccess && (e = e2) != cudaSuccess) where = "cudaStreamEndCapture";

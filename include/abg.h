@@ -325,6 +325,14 @@ abg_status abg_atq(const float *q, const float *gate, const float *k, const floa
  *                  (the graph owns the buffer of the chunk results of each
  *                  ATQ node, so replays of different graphs do not share it);
  *                  no other node may write its Kc or Vc (ABG_EALIAS)
+ *   ABG_NODE_COPY  x, len -> out: copies len floats (a memory copy, no
+ *                  arithmetic), so that a replay can take its inputs from
+ *                  host memory and return its results there: each of x and
+ *                  out is device memory or page-locked host memory (pinned or
+ *                  registered); pageable host memory, len <= 0, a pointer not
+ *                  4-byte aligned or overlapping ranges give ABG_EINVAL,
+ *                  ABG_ESHAPE, ABG_EALIGN and ABG_EALIAS.  The kernel launch
+ *                  that follows a copy does not start early.
  * Every kind also reads `group` (0 means 64): the group size of the product's
  * scale, bias and xsum (Q4MV, including the group sums its prologue
  * computes) or of out_sum (RMSQ, SWQ, GSUM); Q4MV reads `sb_type` (an
@@ -337,7 +345,8 @@ typedef enum {
     ABG_NODE_SWQ = 2,
     ABG_NODE_GSUM = 3,
     ABG_NODE_GDN = 4, /* args -> abg_gdn_args */
-    ABG_NODE_ATQ = 5  /* args -> abg_atq_args */
+    ABG_NODE_ATQ = 5, /* args -> abg_atq_args */
+    ABG_NODE_COPY = 6 /* x -> out, len floats */
 } abg_node_kind;
 
 /* The arguments of abg_gdn and abg_atq, for their stage-graph nodes (the
@@ -373,9 +382,9 @@ typedef struct abg_node {
     const float *x;    /* activation / producer input (see above) */
     const float *xsum; /* Q4MV with ABG_PRO_NONE */
     const float *wt;   /* RMSQ node and ABG_PRO_RMSQ */
-    float *out;        /* RMSQ, SWQ */
+    float *out;        /* RMSQ, SWQ, COPY */
     float *out_sum;    /* RMSQ, SWQ, GSUM */
-    int64_t len;       /* RMSQ, SWQ, GSUM vector length n */
+    int64_t len;       /* RMSQ, SWQ, GSUM vector length n; COPY floats */
     int32_t group;     /* group size 32, 64 or 128; 0 = 64 */
     int32_t sb_type;   /* Q4MV: abg_sb_type of scale and bias */
     const void *args;  /* GDN: abg_gdn_args; ATQ: abg_atq_args */
@@ -395,7 +404,8 @@ abg_status abg_stage_graph_create(const abg_node *nodes, int64_t count, int mode
  * With the environment variable ABG_TRACE=1 each launch also synchronizes and
  * prints the launch count, GPU milliseconds and wall milliseconds to stderr. */
 abg_status abg_stage_graph_launch(void *graph, void *stream);
-/* Number of kernel launches one replay performs (after sibling grouping). */
+/* Number of kernel launches one replay performs (after sibling grouping; an
+ * ATQ node performs four, a COPY node none). */
 abg_status abg_stage_graph_launches(void *graph, int64_t *launches);
 /* SwiGLU pairs: when a Q4MV node with the ABG_PRO_SWQ prologue reads a =
  * [gate | up] (2n values) written by the only two products of the launch

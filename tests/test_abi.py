@@ -236,6 +236,28 @@ def test_stage_graph_mixer_node_validation(lib):
     assert create(lib, [node(**gs), node(kind=abg.NODE_ATQ, stage=1, args=ctypes.addressof(t3))]) == EALIAS
 
 
+def test_stage_graph_copy_node_validation(lib):
+    """Copy nodes: null pointers, an empty or misaligned copy and overlapping
+    ranges are refused before any device call."""
+    cp = dict(kind=abg.NODE_COPY, stage=0, x=A, out=A + 0x100000, len=64)
+    assert create(lib, [node(**{**cp, "x": 0})]) == EINVAL
+    assert create(lib, [node(**{**cp, "out": 0})]) == EINVAL
+    assert create(lib, [node(**{**cp, "len": 0})]) == ESHAPE
+    assert create(lib, [node(**{**cp, "x": A + 2})]) == EALIGN
+    assert create(lib, [node(**{**cp, "out": A + 128})]) == EALIAS
+
+
+def test_stage_graph_copy_node_validation(lib):
+    """Copy nodes: null pointers, an empty or misaligned copy and overlapping
+    ranges are refused before any device call."""
+    cp = dict(kind=abg.NODE_COPY, stage=0, x=A, out=A + 0x100000, len=64)
+    assert create(lib, [node(**{**cp, "x": 0})]) == EINVAL
+    assert create(lib, [node(**{**cp, "out": 0})]) == EINVAL
+    assert create(lib, [node(**{**cp, "len": 0})]) == ESHAPE
+    assert create(lib, [node(**{**cp, "x": A + 2})]) == EALIGN
+    assert create(lib, [node(**{**cp, "out": A + 128})]) == EALIAS
+
+
 def test_tuning_validation(lib):
     assert lib.abg_set_q4mv_tuning(300, 0, 0, 0) == EINVAL
     assert lib.abg_set_q4mv_tuning(0, 17, 0, 0) == EINVAL

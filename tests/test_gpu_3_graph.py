@@ -332,3 +332,92 @@ def test_few_tiles_table_capacity(count):
         assert_bits_equal(host(ys[i]), oracle.q4mv(m.w, m.scale, m.bias, xn, xs, cols), f"product {i}")
     g.close()
     assert abg.device_status(clear=True) == 0
+
+
+def test_copy_nodes_host_in_host_out():
+    """A replay that starts and ends in pinned host memory: copy x in, its
+    group sums, three products of one stage (one grouped launch), copy the
+    outputs out.  The launch count counts kernels only; every replay reads the
+    host x as it is then (a new x gives the new results, bit-exact to the
+    oracle)."""
+    rng = np.random.default_rng(91)
+    cols = 2048
+    mats = [synth.q4_matrix(rng, r, cols) for r in (4096, 512, 512)]
+    dm = [(dev_words(m.w), dev(m.scale), dev(m.bias)) for m in mats]
+    xh = torch.empty(cols, dtype=torch.float32).pin_memory()
+    yh = [torch.empty(m.rows, dtype=torch.float32).pin_memory() for m in mats]
+    xd, xsd = empty(cols), empty(cols // 64)
+    yd = [empty(m.rows) for m in mats]
+    N = abg.Node
+    nodes = ([N.copy(0, xh, xd), N.gsum(1, xd, xsd)] +
+             [N.q4mv(2, *dm[i], yd[i], cols, x=xd, xsum=xsd) for i in range(3)] +
+             [N.copy(3, yd[i], yh[i]) for i in range(3)])
+    g = abg.StageGraph(nodes, keep=[xh, xd, xsd] + yh + yd + [t for d in dm for t in d])
+    assert g.launches == 2
+    for rep in range(3):
+        x = synth.activations(rng, cols)
+        xh.copy_(torch.from_numpy(x))
+        g.launch()
+        torch.cuda.synchronize()
+        xs = oracle.gsum(x)
+        for i, m in enumerate(mats):
+            assert_bits_equal(yh[i].numpy(), oracle.q4mv(m.w, m.scale, m.bias, x, xs, cols), f"product {i}, {rep}")
+    g.close()
+    assert abg.device_status(clear=True) == 0
+
+
+def test_copy_node_between_kernels():
+    """A device-to-device copy between two dependent kernels (the RMS norm's
+    output copied, then read by a product): the product starts only after
+    the copy; bit-exact."""
+    rng = np.random.default_rng(92)
+    cols = 2048
+    m = synth.q4_matrix(rng, 1000, cols)
+    h = synth.activations(rng, cols)
+    wt = synth.rms_weights(rng, cols)
+    xn_ref, xs_ref = oracle.rmsq(h, wt, 1e-6)
+    hd, wtd = dev(h), dev(wt)
+    xn, xs, xn2, xs2 = empty(cols), empty(cols // 64), empty(cols), empty(cols // 64)
+    y = empty(m.rows)
+    w, sc, bi = dev_words(m.w), dev(m.scale), dev(m.bias)
+    N = abg.Node
+    nodes = [N.rmsq(0, hd, wtd, xn, xs), N.copy(1, xn, xn2), N.copy(1, xs, xs2),
+             N.q4mv(2, w, sc, bi, y, cols, x=xn2, xsum=xs2)]
+    g = abg.StageGraph(nodes, keep=[hd, wtd, xn, xs, xn2, xs2, y, w, sc, bi])
+    assert g.launches == 2
+    for _ in range(2):
+        y.fill_(float("nan"))
+        g.launch()
+        torch.cuda.synchronize()
+        assert_bits_equal(host(y), oracle.q4mv(m.w, m.scale, m.bias, xn_ref, xs_ref, cols), "product after copies")
+    g.close()
+    assert abg.device_status(clear=True) == 0
+
+
+def test_copy_node_refusals():
+    """Copy nodes in the stage hazard checks, and pageable host memory."""
+    rng = np.random.default_rng(93)
+    cols = 2048
+    m = synth.q4_matrix(rng, 256, cols)
+    w, sc, bi = dev_words(m.w), dev(m.scale), dev(m.bias)
+    xh = torch.empty(cols, dtype=torch.float32).pin_memory()
+    xd, xsd, y = empty(cols), empty(cols // 64), empty(m.rows)
+    N = abg.Node
+    # a product of the copy's own stage reading what it writes
+    with pytest.raises(abg.AbgError) as e:
+        abg.StageGraph([N.copy(0, xh, xd), N.q4mv(0, w, sc, bi, y, cols, x=xd, xsum=xsd)])
+    assert e.value.status == 4
+    # a copy over a product's weights
+    sview = sc.view(-1)[: cols]
+    with pytest.raises(abg.AbgError) as e:
+        abg.StageGraph([N.copy(0, xh, sview), N.q4mv(1, w, sc, bi, y, cols, x=xd, xsum=xsd)])
+    assert e.value.status == 4
+    # pageable host memory: refused by the binding, and by the library
+    pageable = torch.empty(cols, dtype=torch.float32)
+    with pytest.raises(ValueError):
+        N.copy(0, pageable, xd)
+    raw = abg._Node(kind=abg.NODE_COPY, stage=0, x=pageable.data_ptr(), out=xd.data_ptr(), len=cols)
+    with pytest.raises(abg.AbgError) as e:
+        abg.StageGraph([raw])
+    assert e.value.status == 1
+    assert abg.device_status(clear=True) == 0

@@ -131,7 +131,7 @@ def test_mixers_as_stage_graph_nodes():
              N.q4mv(1, *wa, oa, Hq * Dq, ya, ysa)]
     keep = list(g_.values()) + list(a_.values()) + wg + wa + [yg, ysg, ya, ysa, og, oa]
     graph = abg.StageGraph(nodes, keep=keep)
-    assert graph.launches == 4
+    assert graph.launches == 7  # gdn, the four atq launches, two products
     other = synth.atq_case(np.random.default_rng(12), 8, 2, 256, 4096, 4000)
     o_ = {k: dev(v) for k, v in other.items() if k != "pos"}
     S_ref, st_ref, Kr, Vr = cg["S"], cg["state"], ca["Kc"], ca["Vc"]
@@ -182,4 +182,47 @@ def test_atq_tokens_back_to_back():
         assert_bits_equal(host(ys[t][1]), eys, f"ysum at {127 + t}")
     assert_bits_equal(host(d["Kc"]).reshape(Kr.shape), Kr, "K cache")
     assert_bits_equal(host(d["Vc"]).reshape(Vr.shape), Vr, "V cache")
+    assert abg.device_status(clear=True) == 0
+
+
+def test_mixers_after_copy_nodes():
+    """gdn and atq nodes right after copy nodes (their first launches start
+    only after the copies), taking x and q from pinned host memory and handing
+    y back there: bit-exact to the oracle over two replays."""
+    rng = np.random.default_rng(94)
+    cg = synth.gdn_case(rng, 4, 128, 4)
+    ca = synth.atq_case(rng, 4, 2, 128, 400, 200)
+    g_ = {k: dev(v) for k, v in cg.items()}
+    a_ = {k: dev(v) for k, v in ca.items() if k != "pos"}
+    Hg, Dg = cg["S"].shape[0], cg["S"].shape[1]
+    Dq = ca["Kc"].shape[2]
+    Hq = ca["q"].size // Dq
+    xh = torch.from_numpy(cg["x"]).pin_memory()
+    qh = torch.from_numpy(ca["q"].ravel()).pin_memory()
+    yg, ysg, ya, ysa = empty(Hg * Dg), empty(Hg * Dg // 64), empty(Hq * Dq), empty(Hq * Dq // 64)
+    ygh = torch.empty(Hg * Dg, dtype=torch.float32).pin_memory()
+    yah = torch.empty(Hq * Dq, dtype=torch.float32).pin_memory()
+    N = abg.Node
+    nodes = [N.copy(0, xh, g_["x"]), N.copy(0, qh, a_["q"]),
+             N.gdn(1, g_["x"], g_["conv"], g_["state"], g_["a"], g_["b"], g_["z"], g_["A_log"], g_["dt_bias"],
+                   g_["nw"], g_["S"], yg, ysg),
+             N.copy(2, yg, ygh),
+             N.atq(3, a_["q"], a_["gate"], a_["k"], a_["v"], a_["qn_w"], a_["kn_w"], a_["cos"], a_["sin"], a_["Kc"],
+                   a_["Vc"], ya, ysa, pos=ca["pos"]),
+             N.copy(4, ya, yah)]
+    keep = list(g_.values()) + list(a_.values()) + [xh, qh, yg, ysg, ya, ysa, ygh, yah]
+    graph = abg.StageGraph(nodes, keep=keep)
+    assert graph.launches == 5
+    S_ref, st_ref, Kr, Vr = cg["S"], cg["state"], ca["Kc"], ca["Vc"]
+    for t in range(2):
+        graph.launch()
+        torch.cuda.synchronize()
+        ey, eys, S_ref, st_ref = oracle.gdn(**dict(cg, S=S_ref, state=st_ref))
+        ay, ays, Kr, Vr = oracle.atq(**dict(ca, Kc=Kr, Vc=Vr))
+        assert_bits_equal(ygh.numpy(), ey, f"gdn y, replay {t}")
+        assert_bits_equal(host(ysg), eys, f"gdn ysum, replay {t}")
+        assert_bits_equal(yah.numpy(), ay, f"atq y, replay {t}")
+        assert_bits_equal(host(ysa), ays, f"atq ysum, replay {t}")
+        assert_bits_equal(host(a_["Kc"]).reshape(Kr.shape), Kr, f"K cache, replay {t}")
+    graph.close()
     assert abg.device_status(clear=True) == 0
