@@ -89,11 +89,13 @@ class DeviceModel:
 
 
 def decode_token_graph(dm: DeviceModel, h0, fused: bool = True, mode: int = TREE, rows_per_warp: int = 0,
-                       eps: float = 1e-6):
+                       eps: float = 1e-6, host_io=None):
     """(graph, outputs): the token's stage graph reading h0 and the buffers it writes.
 
     outputs["logits"] is the head's output; the per-layer buffers are kept in
-    outputs["layers"] for inspection.
+    outputs["layers"] for inspection.  With host_io = (h_host, logits_host),
+    pinned host tensors, every replay first copies h_host into h0 and last
+    copies the logits into logits_host (copy nodes of the same graph).
     """
     import torch
 
@@ -103,6 +105,10 @@ def decode_token_graph(dm: DeviceModel, h0, fused: bool = True, mode: int = TREE
     nodes, keep = [], [h0]
     layers_out = []
     stage = 0
+    if host_io is not None:
+        nodes.append(Node.copy(0, host_io[0], h0))
+        keep += list(host_io)
+        stage = 1
     h = h0
     H, M = dm.hidden, dm.mlp
     for L in dm.layers:
@@ -168,4 +174,6 @@ def decode_token_graph(dm: DeviceModel, h0, fused: bool = True, mode: int = TREE
         nodes.append(Node.q4mv(stage, m.w, m.scale, m.bias, logits, m.cols, x=out["xf"], xsum=out["xfs"]))
         keep += [out["xf"], out["xfs"]]
     keep += [logits, dm.rms_final, dm.head]
+    if host_io is not None:
+        nodes.append(Node.copy(stage + 1, logits, host_io[1]))
     return StageGraph(nodes, mode=mode, rows_per_warp=rows_per_warp, keep=keep), out

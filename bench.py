@@ -659,6 +659,30 @@ def bench_decode(abg, decode, stream, args):
         out[key] = {"gpu_ms_per_token": ms, "wall_ms_per_token": statistics.median(walls), "launches": g.launches,
                     "gbs": dm.product_bytes / (ms * 1e-3) / 1e9}
         g.close()
+    # end to end: the fused token as one graph that copies the hidden vector in
+    # from pinned host memory and the logits back out; wall time of launch +
+    # one sync, median of 50 replays; the host logits checked against a replay
+    # of the graph without copies
+    h_host = torch.from_numpy(h).pin_memory()
+    logits_host = torch.empty(dm.head.rows, dtype=torch.float32).pin_memory()
+    h_dev = torch.empty_like(h0)
+    g, o = decode.decode_token_graph(dm, h_dev, fused=True, host_io=(h_host, logits_host))
+    walls = []
+    for i in range(55):
+        t0 = time.perf_counter()
+        g.launch(stream)
+        stream.synchronize()
+        if i >= 5:
+            walls.append((time.perf_counter() - t0) * 1e3)
+    g.close()
+    g2, o2 = decode.decode_token_graph(dm, h0, fused=True)
+    g2.launch(stream)
+    stream.synchronize()
+    if not torch.equal(o2["logits"].cpu(), logits_host):
+        raise SystemExit("the decode token's host logits differ from its device logits")
+    g2.close()
+    out["e2e"] = {"wall_ms_per_token": statistics.median(walls), "h2d_bytes": 4 * h.size,
+                  "d2h_bytes": 4 * dm.head.rows}
     return out
 
 

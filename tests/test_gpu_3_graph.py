@@ -421,3 +421,24 @@ def test_copy_node_refusals():
         abg.StageGraph([raw])
     assert e.value.status == 1
     assert abg.device_status(clear=True) == 0
+
+
+def test_decode_token_host_io(small):
+    """The fused token reading its hidden vector from pinned host memory and
+    writing its logits there (copy nodes of the same graph): the host logits
+    bit-exact to the oracle, then again after a new hidden vector."""
+    model, h, logits, _, dm = small
+    h_host = torch.from_numpy(h).pin_memory()
+    lh = torch.empty(logits.size, dtype=torch.float32).pin_memory()
+    h_dev = empty(h.size)
+    g, _ = decode.decode_token_graph(dm, h_dev, fused=True, host_io=(h_host, lh))
+    g.launch()
+    torch.cuda.synchronize()
+    assert_bits_equal(lh.numpy(), logits, "logits")
+    h2 = synth.activations(np.random.default_rng(5), h.size)
+    h_host.copy_(torch.from_numpy(h2))
+    g.launch()
+    torch.cuda.synchronize()
+    assert_bits_equal(lh.numpy(), oracle.decode_token(model, h2), "logits, new hidden vector")
+    g.close()
+    assert abg.device_status(clear=True) == 0
