@@ -165,7 +165,7 @@ cudaError_t launch_q4mm(const Q4Plan &plan, cudaStream_t stream, bool pdl) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    Q4ArgsT<kMmProbs> mm;
+    Q4ArgsT<kMmProbs> mm{};
     narrow_args(mm, plan.args);
     void *params[] = {&mm};
     return cudaLaunchKernelExC(&cfg, fn, params);

@@ -369,7 +369,7 @@ cudaError_t launch_q4mv(const Q4Plan &plan, cudaStream_t stream, bool pdl) {
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
     if (kernel_probs(plan.layout, plan.shape) == kFewProbs) {
-        Q4ArgsT<kFewProbs> few;
+        Q4ArgsT<kFewProbs> few{};
         narrow_args(few, plan.args);
         void *params[] = {&few};
         return cudaLaunchKernelExC(&cfg, fn, params);
