@@ -61,6 +61,22 @@ def test_struct_layout_matches_c(tmp_path, ctype, cname):
         assert getattr(ctype, f).offset == off, f
 
 
+def test_constants_match_c(tmp_path):
+    """The binding's mode, node-kind, prologue and scale/bias-type constants
+    equal the header's enumerators, as gcc sees them."""
+    names = ["TREE", "FAST", "NODE_Q4MV", "NODE_RMSQ", "NODE_SWQ", "NODE_GSUM", "NODE_GDN", "NODE_ATQ", "NODE_COPY",
+             "PRO_NONE", "PRO_GSUM", "PRO_RMSQ", "PRO_SWQ", "SB_F32", "SB_BF16", "SB_F16"]
+    prog = tmp_path / "consts.c"
+    lines = ["#include <stdio.h>", '#include "abg.h"', "int main(void){"]
+    lines += [f'printf("%d\\n", (int)ABG_{n});' for n in names]
+    lines += ["return 0;}"]
+    prog.write_text("\n".join(lines))
+    exe = tmp_path / "consts"
+    subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), str(prog), "-o", str(exe)], check=True)
+    out = [int(v) for v in subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()]
+    assert out == [getattr(abg, n) for n in names]
+
+
 def test_status_strings(lib):
     assert lib.abg_status_str(0) == b"ok"
     assert lib.abg_status_str(4) == b"output overlaps an input"
