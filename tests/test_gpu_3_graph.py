@@ -281,13 +281,14 @@ def test_prologues_many_tiles_6144(prologue):
     assert abg.device_status(clear=True) == 0
 
 
-def test_many_products_of_one_stage():
-    """300 products of one stage reading one x, of seven row counts: grouped
-    launches of at most 256 products (two), each launch walking its problems
-    tile by tile.  Every output bit-exact to the oracle."""
+@pytest.mark.parametrize("count,launches", [(256, 1), (257, 2), (300, 2)])
+def test_many_products_of_one_stage(count, launches):
+    """Products of one stage reading one x, of seven row counts: grouped
+    launches of at most 256 products, each launch walking its problems tile
+    by tile.  Every output bit-exact to the oracle."""
     rng = np.random.default_rng(77)
     cols = 512
-    mats = [synth.q4_matrix(rng, 40 + 8 * (i % 7), cols) for i in range(300)]
+    mats = [synth.q4_matrix(rng, 40 + 8 * (i % 7), cols) for i in range(count)]
     x = synth.activations(rng, cols)
     xs = oracle.gsum(x)
     dx, dxs = dev(x), dev(xs)
@@ -295,7 +296,7 @@ def test_many_products_of_one_stage():
     ys = [empty(m.rows) for m in mats]
     nodes = [abg.Node.q4mv(0, *dm[i], ys[i], cols, x=dx, xsum=dxs) for i in range(len(mats))]
     g = abg.StageGraph(nodes, keep=[dx, dxs] + ys + [t for d in dm for t in d])
-    assert g.launches == 2
+    assert g.launches == launches
     for _ in range(2):
         g.launch()
     torch.cuda.synchronize()
@@ -305,7 +306,7 @@ def test_many_products_of_one_stage():
     assert abg.device_status(clear=True) == 0
 
 
-@pytest.mark.parametrize("count", [16, 17, 40])
+@pytest.mark.parametrize("count", [16, 17, 40, 256])
 def test_few_tiles_table_capacity(count):
     """A stage of small products of 2048 columns reading one x (with the
     RMS-norm prologue): one grouped launch of few tiles.  Up to 16 products
